@@ -1,0 +1,263 @@
+"""Seeded synthetic inputs for the verify step (shared by the tests, the CUDA
+path's callers and the benchmark).
+
+This module only *draws* inputs: bf16 weights / activations / KV history, NVFP4
+encoded expert weights, draft trees and router hot sets.  It holds none of the
+verify step's arithmetic.  Every tensor is a pure function of (seed, tensor
+stream id, element index) through the Philox4x32-10 counter-based generator, so
+it can be drawn on the host (``synth.c``) or, for the 62-layer stack, straight
+into device memory (``synth_gpu.cu``) with bit-identical results.
+
+Workload shapes follow the configurations the verify step is measured on; the
+pages (an LMSYS/SGLang megakernel report on "Muse Spark Open") give the layer
+structure (orcarouter.ai page, § "where the kernel boundary sits": 62 layers,
+46 sliding-window over 2,048 tokens and 16 global, router top-8 of 256, pooler
+and unpooler around NVFP4 experts) but no widths; the widths, value
+distributions and routing pattern below are synthetic stand-ins for the pages'
+single GSM8K request (no dataset or trained weights are used).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass, field, replace
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = None
+_LOCK = threading.Lock()
+
+T = 16  # tokens in the verification tree
+
+# tensor stream kinds
+K_QKV, K_O, K_POOL, K_ROUTER, K_BIAS, K_UNPOOL, K_NORM_ATTN, K_NORM_MOE = 1, 2, 3, 4, 5, 6, 7, 8
+K_W1, K_W2, K_NORM_FINAL, K_LM, K_HIDDEN, K_PARENT, K_KCACHE, K_VCACHE = 9, 10, 11, 12, 13, 14, 15, 16
+K_ROUTE_KEEP, K_ROUTE_PICK = 17, 18
+
+
+def build(force: bool = False) -> str:
+    """Compile synth.c into _build/libsynth.so (gcc, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    out = os.path.join(_BUILD, "libsynth.so")
+    src = os.path.join(_HERE, "synth.c")
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        tmp = out + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+                               "-std=c11", src, "-o", tmp, "-lm"])
+        os.replace(tmp, out)
+    return out
+
+
+def lib():
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            L = ctypes.CDLL(build())
+            u64, dbl, vp, i64 = ctypes.c_uint64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int64
+            L.synth_stream.argtypes = [ctypes.c_int] * 4
+            L.synth_stream.restype = u64
+            L.synth_philox.argtypes = [u64, u64, u64, vp]
+            for fn in (L.synth_normal_f64, L.synth_normal_f32, L.synth_normal_bf16):
+                fn.argtypes = [u64, u64, u64, dbl, dbl, vp]
+            L.synth_nvfp4_encode.argtypes = [vp, i64, i64, vp, vp]
+            L.synth_nvfp4_encode.restype = ctypes.c_float
+            L.synth_nvfp4_matrix.argtypes = [u64, u64, i64, i64, dbl, vp, vp, vp]
+            L.synth_nvfp4_matrix.restype = ctypes.c_float
+            L.synth_parent.argtypes = [u64, u64, ctypes.c_int, vp]
+            L.synth_subset.argtypes = [u64, u64, ctypes.c_int, ctypes.c_int, vp]
+            L.synth_bernoulli.argtypes = [u64, u64, u64, dbl, vp]
+            L.synth_bf16_from_double.argtypes = [dbl]
+            L.synth_bf16_from_double.restype = ctypes.c_uint16
+            _LIB = L
+    return _LIB
+
+
+def stream(kind: int, layer: int = 0, expert: int = 0, part: int = 0) -> int:
+    return lib().synth_stream(kind, layer, expert, part)
+
+
+# --------------------------------------------------------------------------
+# configurations
+# --------------------------------------------------------------------------
+@dataclass(frozen=True)
+class Config:
+    name: str
+    d: int            # d_model
+    hq: int           # query heads
+    hkv: int          # key/value heads
+    hd: int           # head dim
+    p: int            # pooled width (pooler output, expert input/output)
+    f: int            # expert FFN width (SwiGLU hidden)
+    e: int            # experts
+    k: int            # top-k
+    n_layers: int
+    vocab: int        # 0: no LM head (single-layer workloads output the hidden state)
+    window: int       # sliding window W of SWA layers
+    history: int      # cached KV rows before the tree; pos0 = history
+    layer_global: tuple = field(default=())
+    n_hot: int = 0        # router hot-set size (0: no bias)
+    hot_bias: float = 0.0 # +bias on the hot set, -bias elsewhere
+    rms_eps: float = 1e-6
+    rope_theta: float = 10000.0
+    router_std: float = 0.0  # 0: 1/sqrt(d)
+
+    @property
+    def max_ctx(self) -> int:
+        return self.history + 64
+
+    @property
+    def pos0(self) -> int:
+        return self.history
+
+    @property
+    def nqkv(self) -> int:
+        return (self.hq + 2 * self.hkv) * self.hd
+
+    def is_global(self, layer: int) -> bool:
+        return bool(self.layer_global[layer])
+
+
+def _cfg4_globals(n=62):
+    g = [0] * n
+    for l in range(3, 60, 4):
+        g[l] = 1
+    g[61] = 1
+    return tuple(g)
+
+
+CFG1 = Config("single MoE layer, tiny (d512, SWA128 over 256 rows)", d=512, hq=8, hkv=2, hd=64,
+              p=256, f=512, e=32, k=4, n_layers=1, vocab=0, window=128, history=256,
+              layer_global=(0,))
+CFG2 = Config("one SWA-2048 layer (d4096, 8192 rows, 256 experts top-8)", d=4096, hq=32, hkv=8,
+              hd=128, p=2048, f=1024, e=256, k=8, n_layers=1, vocab=0, window=2048,
+              history=8192, layer_global=(0,), n_hot=49, hot_bias=4.0)
+CFG3 = replace(CFG2, name="one global layer (d4096, 32768 rows)", history=32768, layer_global=(1,))
+CFG4 = replace(CFG2, name="62-layer verify step (46 SWA-2048 + 16 global, ctx 8192, vocab 131072)",
+               n_layers=62, vocab=131072, layer_global=_cfg4_globals())
+# small multi-layer stack at config-1 widths: exercises the launch chain and the LM head
+CFG1_STACK = replace(CFG1, name="4-layer stack at tiny widths", n_layers=4, vocab=1024,
+                     layer_global=(0, 1, 0, 1))
+
+CONFIGS = {"cfg1": CFG1, "cfg2": CFG2, "cfg3": CFG3, "cfg4": CFG4, "cfg1_stack": CFG1_STACK}
+
+
+# --------------------------------------------------------------------------
+# host-side draws
+# --------------------------------------------------------------------------
+def normal_bf16(seed, strm, n, mean=0.0, std=1.0) -> np.ndarray:
+    out = np.empty(n, np.uint16)
+    lib().synth_normal_bf16(seed, strm, n, mean, std, out.ctypes.data)
+    return out
+
+
+def normal_f32(seed, strm, n, mean=0.0, std=1.0) -> np.ndarray:
+    out = np.empty(n, np.float32)
+    lib().synth_normal_f32(seed, strm, n, mean, std, out.ctypes.data)
+    return out
+
+
+def nvfp4_matrix(seed, strm, rows, cols, std):
+    codes = np.empty(rows * cols // 2, np.uint8)
+    sf = np.empty(rows * cols // 16, np.uint8)
+    scratch = np.empty(rows * cols, np.float32)
+    gs = lib().synth_nvfp4_matrix(seed, strm, rows, cols, std, codes.ctypes.data, sf.ctypes.data,
+                                  scratch.ctypes.data)
+    return codes.reshape(rows, cols // 2), sf.reshape(rows, cols // 16), np.float32(gs)
+
+
+def parent_array(seed, strm=None) -> np.ndarray:
+    out = np.empty(T, np.int32)
+    lib().synth_parent(seed, stream(K_PARENT) if strm is None else strm, T, out.ctypes.data)
+    return out
+
+
+def subset(seed, strm, n, m) -> np.ndarray:
+    out = np.empty(m, np.int32)
+    lib().synth_subset(seed, strm, n, m, out.ctypes.data)
+    return out
+
+
+def router_bias(cfg: Config, bias_seed: int, layer: int) -> np.ndarray:
+    """+hot_bias on a seeded hot set of n_hot experts, -hot_bias elsewhere (0 if no hot set)."""
+    b = np.zeros(cfg.e, np.float32)
+    if cfg.n_hot > 0:
+        hot = subset(bias_seed, stream(K_BIAS, layer), cfg.e, cfg.n_hot)
+        b[:] = -cfg.hot_bias
+        b[hot] = cfg.hot_bias
+    return b
+
+
+def bf16_to_f32(a: np.ndarray) -> np.ndarray:
+    return (a.astype(np.uint32) << 16).view(np.float32)
+
+
+def layer_weights(cfg: Config, seed: int, layer: int, bias_seed: int | None = None,
+                  experts: bool = True) -> dict:
+    """All weights of one decoder layer, host numpy (bf16 as uint16)."""
+    d, p, f, e = cfg.d, cfg.p, cfg.f, cfg.e
+    rstd = cfg.router_std if cfg.router_std > 0 else 1.0 / np.sqrt(d)
+    w = {
+        "w_qkv": normal_bf16(seed, stream(K_QKV, layer), cfg.nqkv * d, 0, 0.02).reshape(cfg.nqkv, d),
+        "w_o": normal_bf16(seed, stream(K_O, layer), d * cfg.hq * cfg.hd, 0, 0.02).reshape(d, cfg.hq * cfg.hd),
+        "w_pool": normal_bf16(seed, stream(K_POOL, layer), p * d, 0, 0.02).reshape(p, d),
+        "w_router": normal_bf16(seed, stream(K_ROUTER, layer), e * p, 0, rstd).reshape(e, p),
+        "b_router": router_bias(cfg, seed if bias_seed is None else bias_seed, layer),
+        "w_unpool": normal_bf16(seed, stream(K_UNPOOL, layer), d * p, 0, 0.02).reshape(d, p),
+        "norm_attn": normal_bf16(seed, stream(K_NORM_ATTN, layer), d, 1.0, 0.02),
+        "norm_moe": normal_bf16(seed, stream(K_NORM_MOE, layer), d, 1.0, 0.02),
+    }
+    if experts:
+        w1c = np.empty((e, 2 * f, p // 2), np.uint8)
+        w1s = np.empty((e, 2 * f, p // 16), np.uint8)
+        w1g = np.empty(e, np.float32)
+        w2c = np.empty((e, p, f // 2), np.uint8)
+        w2s = np.empty((e, p, f // 16), np.uint8)
+        w2g = np.empty(e, np.float32)
+        for x in range(e):
+            w1c[x], w1s[x], w1g[x] = nvfp4_matrix(seed, stream(K_W1, layer, x), 2 * f, p, 0.02)
+            w2c[x], w2s[x], w2g[x] = nvfp4_matrix(seed, stream(K_W2, layer, x), p, f, 0.02)
+        w.update(w1_codes=w1c, w1_sf=w1s, w1_gs=w1g, w2_codes=w2c, w2_sf=w2s, w2_gs=w2g)
+    return w
+
+
+def final_weights(cfg: Config, seed: int) -> dict:
+    if cfg.vocab <= 0:
+        return {}
+    return {
+        "norm_final": normal_bf16(seed, stream(K_NORM_FINAL), cfg.d, 1.0, 0.02),
+        "w_lm": normal_bf16(seed, stream(K_LM), cfg.vocab * cfg.d, 0, 0.02).reshape(cfg.vocab, cfg.d),
+    }
+
+
+def hidden_in(cfg: Config, seed: int, step: int = 0) -> np.ndarray:
+    return normal_bf16(seed, stream(K_HIDDEN, 0, 0, step), T * cfg.d, 0, 1.0).reshape(T, cfg.d)
+
+
+def kv_history(cfg: Config, seed: int, layer: int):
+    """K and V caches of one layer, [Hkv][max_ctx][D] bf16: rows [0, history) drawn
+    N(0,1) (K taken as already rotated), the rest zero."""
+    out = []
+    for kind in (K_KCACHE, K_VCACHE):
+        c = np.zeros((cfg.hkv, cfg.max_ctx, cfg.hd), np.uint16)
+        for h in range(cfg.hkv):
+            c[h, :cfg.history] = normal_bf16(seed, stream(kind, layer, h), cfg.history * cfg.hd,
+                                             0, 1.0).reshape(cfg.history, cfg.hd)
+        out.append(c)
+    return out[0], out[1]
+
+
+def parity_seeds(name: str) -> dict:
+    """Seeds selected for a workload by tests/golden/select_seeds.py (margin / expert-count
+    rules), or the defaults."""
+    import json
+    path = os.path.join(os.path.dirname(_HERE), "tests", "golden", "seeds.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            s = json.load(fh)
+        if name in s:
+            return s[name]
+    return {"seed": 1, "bias_seeds": None}
