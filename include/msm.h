@@ -1,0 +1,236 @@
+/*
+ * msm.h — C ABI of libmsm: one speculative-decoding verify step of a batch-1
+ * mixture-of-experts decoder on one GB300 GPU, one persistent kernel launch per
+ * decoder layer.
+ *
+ * The method (LMSYS/SGLang megakernel for "Muse Spark Open", as reported by the
+ * alphasignal.ai article "LMSYS Doubles Muse Spark Open Speed to 1,109 Tokens per
+ * Second" and the orcarouter.ai article "Muse Spark Open: 1,109 tokens/s is a
+ * kernel-level change"):
+ *   - the target model verifies a 16-token tree proposed by a draft model in one
+ *     pass (alphasignal.ai, § "Draft and verify share one graph"; orcarouter.ai,
+ *     § on the draft model: the candidates form a tree, not a linear chain);
+ *   - each launch covers one decoder layer's attention through the next layer's
+ *     QKV projection and KV-cache write (alphasignal.ai, § "Launch boundaries
+ *     leave hardware idle"; orcarouter.ai, § "where the kernel boundary sits");
+ *   - the layer: tree-masked attention over the KV history (46 sliding-window
+ *     layers over the last 2,048 tokens, 16 global), output projection, pooler,
+ *     router top-8 of 256, two NVFP4 expert GEMMs, unpooler and combine
+ *     (orcarouter.ai, § "where the kernel boundary sits").
+ *
+ * Conventions
+ *   - Every call is host-synchronous in its validation and asynchronous on the
+ *     stream it is given for GPU work.  Host-detectable errors (null pointers,
+ *     invalid parent array, positions out of range, unsupported widths) return
+ *     at once without enqueuing anything.
+ *   - Device pointers are passed as plain pointers; `stream` is a cudaStream_t
+ *     passed as void* (NULL = legacy default stream).
+ *   - The caller owns every buffer it passes: weights (only read during
+ *     msm_model_create, which copies them into a packed, model-owned layout —
+ *     they may be freed once it returns), KV caches, hidden states, logits.
+ *   - The model owns its packed weights, exchange buffers, routing records,
+ *     timing buffer and device status word.
+ *   - Bounded device waits: every in-kernel wait gives up after
+ *     msm_config.timeout_us, records MSM_ERR_DEVICE_TIMEOUT in the model's status
+ *     word and lets the launch finish; msm_sync() reports it and re-arms the
+ *     model.  Nothing traps.
+ *   - A model is not thread-safe; one model may be used by one host thread at a
+ *     time.  Two steps of one model must not overlap on the GPU.
+ *
+ * Layouts (row-major; "bf16" is the 16-bit brain-float bit pattern)
+ *   hidden state      bf16 [16][d_model]        (tree token i in row i)
+ *   parent            int32 [16] host array: parent[0] == -1, 0 <= parent[i] < i
+ *   KV cache (layer)  bf16 [n_kv_heads][max_ctx][head_dim]; rows [0, pos0) hold
+ *                     the history (K already rotated); the step writes the K/V of
+ *                     tree token i to row pos0 + i
+ *   logits            fp32 [16][vocab]
+ *   w_qkv             bf16 [(n_q_heads + 2 n_kv_heads) head_dim][d_model]
+ *                     (rows: q heads, then k heads, then v heads)
+ *   w_o               bf16 [d_model][n_q_heads head_dim]
+ *   w_pool            bf16 [pool_dim][d_model]
+ *   w_router          bf16 [n_experts][pool_dim];  b_router fp32 [n_experts]
+ *   w_unpool          bf16 [d_model][pool_dim]
+ *   norm_attn/norm_moe/norm_final  bf16 [d_model] RMSNorm gains
+ *   w1 (NVFP4)        codes uint8 [n_experts][2 ffn_dim][pool_dim/2] (two E2M1
+ *                     codes per byte, low nibble = even column), scales E4M3
+ *                     [n_experts][2 ffn_dim][pool_dim/16], tensor scale fp32
+ *                     [n_experts]; rows [0, ffn_dim) = SwiGLU gate, the rest = up
+ *   w2 (NVFP4)        codes [n_experts][pool_dim][ffn_dim/2], scales
+ *                     [n_experts][pool_dim][ffn_dim/16], tensor scale [n_experts]
+ *   w_lm              bf16 [vocab][d_model]
+ */
+#ifndef MSM_H
+#define MSM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MSM_TREE_TOKENS 16
+
+typedef enum {
+  MSM_OK = 0,
+  MSM_ERR_INVALID_ARG = 1,    /* bad pointer, parent array, position or config */
+  MSM_ERR_CUDA = 2,           /* a CUDA runtime call failed (see msm_last_error) */
+  MSM_ERR_OOM = 3,            /* device allocation failed */
+  MSM_ERR_DEVICE_TIMEOUT = 4, /* a bounded in-kernel wait expired */
+  MSM_ERR_UNSUPPORTED = 5     /* widths / features this build does not implement */
+} msm_status;
+
+/* msm_config.flags */
+#define MSM_FLAG_SELF_TIMING 0x1u      /* %globaltimer stamps per block and phase (the
+                                          orcarouter.ai article, § "where the 5.9 ms
+                                          still goes": the kernel times itself) */
+#define MSM_FLAG_EXPERT_PREFETCH 0x2u  /* L2 prefetch of the previous step's most-used
+                                          experts (alphasignal.ai, § "Four mechanisms
+                                          keep work moving") */
+#define MSM_FLAG_KV_PREFETCH 0x4u      /* L2 prefetch of the next layer's KV history at
+                                          combine time (orcarouter.ai, § "where the
+                                          5.9 ms still goes") */
+#define MSM_FLAG_PDL 0x8u              /* chain layer launches with programmatic
+                                          dependent launch */
+#define MSM_FLAG_TEST_DROP_HANDOFF 0x10000u /* test hook: one producer never fills one
+                                          exchange slot, so its consumers time out */
+
+typedef struct {
+  int d_model, n_q_heads, n_kv_heads, head_dim;
+  int pool_dim, ffn_dim, n_experts, top_k;
+  int n_layers;
+  int vocab;        /* 0: no LM head; the step then returns the final hidden state */
+  int window;       /* sliding window (keys r with tpos - r < window) of non-global layers */
+  int max_ctx;      /* KV rows per layer and head */
+  const uint8_t* layer_is_global; /* host [n_layers]: 1 = global attention */
+  float rms_eps, rope_theta;
+  uint32_t flags;   /* MSM_FLAG_* */
+  int grid_blocks;  /* persistent blocks per launch; 0 = one per SM */
+  int attn_splits;  /* KV splits per kv head; 0 = automatic */
+  int prefetch_experts; /* experts prefetched by MSM_FLAG_EXPERT_PREFETCH; 0 = 14 */
+  uint32_t timeout_us;  /* bounded-wait limit; 0 = 200000 */
+} msm_config;
+
+/* Device pointers, one per layer (host arrays of n_layers entries). */
+typedef struct {
+  const void* const* w_qkv;
+  const void* const* w_o;
+  const void* const* w_pool;
+  const void* const* w_router;
+  const float* const* b_router;
+  const void* const* w_unpool;
+  const void* const* norm_attn;
+  const void* const* norm_moe;
+  const uint8_t* const* w1_codes;
+  const uint8_t* const* w1_scales;
+  const float* const* w1_tensor_scale;
+  const uint8_t* const* w2_codes;
+  const uint8_t* const* w2_scales;
+  const float* const* w2_tensor_scale;
+  const void* norm_final; /* required when vocab > 0 */
+  const void* w_lm;       /* required when vocab > 0 */
+} msm_weights;
+
+typedef struct msm_model msm_model;
+
+/* Statistics of the model and of its last step (host struct). */
+typedef struct {
+  int grid_blocks, threads_per_block, smem_bytes, attn_splits;
+  int launches_per_step;         /* kernel launches one msm_verify_step enqueues */
+  int cooperative;               /* 1 if launches are cooperative (co-residency guaranteed) */
+  uint64_t packed_weight_bytes;  /* model-owned packed weights */
+  uint64_t exchange_bytes;       /* model-owned exchange buffers */
+} msm_stats;
+
+/*
+ * Create a model on `device`: validate the config, pack the caller's weights
+ * into the model's layout (GPU kernels on an internal stream, completed before
+ * return) and allocate the exchange buffers.
+ * Errors: MSM_ERR_INVALID_ARG (null pointer, bad config), MSM_ERR_UNSUPPORTED
+ * (widths outside what the kernels implement: d_model, pool_dim, ffn_dim and
+ * n_q_heads*head_dim multiples of 64, head_dim 64 or 128, n_q_heads/n_kv_heads
+ * in {1,2,4,8}, top_k <= 8, n_experts <= 256 and a multiple of 16, vocab a
+ * multiple of 16), MSM_ERR_OOM, MSM_ERR_CUDA.  On error *out is NULL.
+ */
+msm_status msm_model_create(const msm_config* config, const msm_weights* weights, int device,
+                            msm_model** out);
+
+/* Free every model-owned buffer.  Waits for the model's work to finish.  NULL is ignored. */
+void msm_model_destroy(msm_model* model);
+
+/*
+ * One verify step: for every layer in order, tree attention over the cache rows
+ * [0, pos0) and the tree's own rows, then the MoE block; writes the K/V rows of
+ * the 16 tree tokens to rows pos0..pos0+15 of every layer's cache, and the
+ * logits of all 16 tree tokens (vocab > 0) and/or the final hidden state.
+ *   hidden_in   device bf16 [16][d_model] (read)
+ *   parent      host int32 [16]; parent[0] == -1, 0 <= parent[i] < i
+ *   pos0        first tree row; 0 <= pos0 and pos0 + 16 <= max_ctx
+ *   k_cache, v_cache  host arrays of n_layers device pointers (see layout)
+ *   logits_out  device fp32 [16][vocab] or NULL (must be non-NULL if vocab > 0)
+ *   hidden_out  device bf16 [16][d_model] or NULL (must be non-NULL if vocab == 0)
+ * Enqueues n_layers launches on `stream`.  Device-side failures are reported
+ * by the next msm_sync().
+ */
+msm_status msm_verify_step(msm_model* model, const void* hidden_in, const int32_t* parent,
+                           int32_t pos0, void* const* k_cache, void* const* v_cache,
+                           float* logits_out, void* hidden_out, void* stream);
+
+/*
+ * The same step with hidden_in / logits_out / hidden_out in HOST memory: copies
+ * the input to the device, runs the step, copies the results back and waits
+ * for the stream.  Returns the step's device status as msm_sync() would.
+ * Host buffers may be pageable; pinned buffers make the copies asynchronous.
+ */
+msm_status msm_verify_step_host(msm_model* model, const void* hidden_in_host,
+                                const int32_t* parent, int32_t pos0, void* const* k_cache,
+                                void* const* v_cache, float* logits_host, void* hidden_out_host,
+                                void* stream);
+
+/* Wait for `stream`, then return (and clear) the device status latched by the
+ * model's launches.  After MSM_ERR_DEVICE_TIMEOUT the model re-arms its exchange
+ * buffers, so the next step starts clean. */
+msm_status msm_sync(msm_model* model, void* stream);
+
+/* Routing of the last completed step: idx int32 [n_layers][16][top_k] (expert
+ * indices, larger logit first, ties to the lower index) and w fp32
+ * [n_layers][16][top_k] (softmax over the selected logits).  Host buffers; either
+ * may be NULL.  Synchronises the device. */
+msm_status msm_get_routing(msm_model* model, int32_t* idx, float* w);
+
+/* Tree as computed on the device in the last step: anc uint32 [16]
+ * (ancestor-or-self bitmask), tpos int32 [16] (pos0 + depth).  Host buffers. */
+msm_status msm_get_tree(msm_model* model, uint32_t* anc, int32_t* tpos);
+
+/* Self-timing stamps of the last step (MSM_FLAG_SELF_TIMING):
+ * uint64 [n_layers][grid_blocks][MSM_TIMING_EVENTS] %globaltimer values (ns).
+ * `n` is the capacity of `buf` in elements. */
+#define MSM_TIMING_EVENTS 16
+msm_status msm_get_timing(msm_model* model, uint64_t* buf, size_t n);
+
+msm_status msm_get_stats(const msm_model* model, msm_stats* out);
+
+/* Diagnostic: copy an exchange buffer of the last launch of the last step to host
+ * memory.  `name` is one of "o" (attention output, bf16 [16][n_q_heads head_dim]),
+ * "h1" (residual after attention, bf16 [16][d_model]), "u" (pooled, bf16
+ * [16][pool_dim]), "logits" (router logits, fp32 [16][n_experts]), "a" (SwiGLU
+ * activations, fp32 [16 top_k][ffn_dim]), "z" (combined expert output, bf16
+ * [16][pool_dim]), "h2" (layer output, bf16 [16][d_model]).  Slots a launch never
+ * filled keep their sentinels (0xFFFF / -0.0).  `bytes` is the capacity of `host`.
+ * Synchronises the device. */
+msm_status msm_get_exchange(msm_model* model, const char* name, void* host, size_t bytes);
+
+/*
+ * Draft step (DFlash-style draft proposing the 15 tree candidates).  Not built
+ * in this version: always returns MSM_ERR_UNSUPPORTED.
+ */
+msm_status msm_draft_step(msm_model* model, const void* draft_hidden_in, int32_t* tokens_out,
+                          int32_t* parent_out, void* stream);
+
+/* Message of the last error on the calling thread ("" if none). */
+const char* msm_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MSM_H */

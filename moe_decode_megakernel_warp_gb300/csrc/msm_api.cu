@@ -1,0 +1,608 @@
+// Host runtime and C ABI of libmsm (declared in include/msm.h).
+//
+// A model packs the caller's weights once, owns the exchange buffers the layer
+// launches hand data through, and enqueues one persistent kernel launch per
+// decoder layer for every verify step (alphasignal.ai, "LMSYS Doubles Muse
+// Spark Open Speed to 1,109 Tokens per Second": each layer runs as one kernel,
+// § "Launch boundaries leave hardware idle").
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "msm.h"
+#include "msm_internal.h"
+
+namespace msm {
+cudaError_t launch_pack_dense(const void* W, void* out, int N, int K, int kind, int hd, int hq, int hkv,
+                              cudaStream_t s);
+cudaError_t launch_pack_nvfp4(const void* codes, const void* sf, void* out, int E, int rows, int K, int swiglu,
+                              int F, cudaStream_t s);
+cudaError_t launch_fill_u32(void* p, uint64_t n, uint32_t v, cudaStream_t s);
+}  // namespace msm
+
+using namespace msm;
+
+namespace {
+thread_local std::string g_err;
+
+msm_status fail(msm_status st, const std::string& msg) {
+  g_err = msg;
+  return st;
+}
+msm_status cuda_fail(cudaError_t e, const char* what) {
+  g_err = std::string(what) + ": " + cudaGetErrorString(e);
+  return e == cudaErrorMemoryAllocation ? MSM_ERR_OOM : MSM_ERR_CUDA;
+}
+#define CK(call)                                   \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+  } while (0)
+
+uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+
+struct LayerPack {
+  uint8_t *qkv = nullptr, *o = nullptr, *pool = nullptr, *router = nullptr, *unpool = nullptr, *w1 = nullptr,
+          *w2 = nullptr;
+  float *b = nullptr, *w1gs = nullptr, *w2gs = nullptr;
+  uint16_t *g_attn = nullptr, *g_moe = nullptr;
+};
+}  // namespace
+
+struct msm_model {
+  int device = 0;
+  msm_config cfg{};
+  Dims dm{};
+  std::vector<uint8_t> global;
+  int G = 0, ring_bytes = 0, act_bytes = 0, smem_bytes = 0;
+  std::vector<LayerPack> L;
+  uint8_t* lm = nullptr;
+  uint16_t* g_final = nullptr;
+  std::vector<void*> allocs;
+  uint8_t* x[2] = {nullptr, nullptr};
+  uint8_t* sbuf = nullptr;
+  XOffsets xo{};
+  SOffsets so{};
+  uint16_t* in_q[2] = {nullptr, nullptr};
+  uint16_t* in_h[2] = {nullptr, nullptr};
+  float* rope = nullptr;
+  double* inv_freq = nullptr;
+  int32_t* routing_idx = nullptr;
+  float* routing_w = nullptr;
+  uint32_t* hist = nullptr;
+  uint32_t* tree_dbg = nullptr;
+  uint64_t* timing = nullptr;
+  DevStatus* status = nullptr;
+  uint64_t packed_bytes = 0;
+  uint64_t launch_count = 0, step_count = 0;
+  std::vector<CUtensorMap> tmk, tmv;
+  std::vector<const void*> tmk_ptr, tmv_ptr;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  cudaStream_t aux = nullptr;
+  uint16_t* io_in = nullptr;      // device staging of msm_verify_step_host
+  uint16_t* io_hidden = nullptr;
+  float* io_logits = nullptr;
+
+  template <class Tp>
+  cudaError_t alloc(Tp** p, uint64_t bytes) {
+    void* v = nullptr;
+    cudaError_t e = cudaMalloc(&v, bytes ? bytes : 256);
+    if (e == cudaSuccess) allocs.push_back(v);
+    *p = static_cast<Tp*>(v);
+    return e;
+  }
+};
+
+namespace {
+
+msm_status validate_config(const msm_config* c) {
+  if (!c) return fail(MSM_ERR_INVALID_ARG, "config is NULL");
+  if (c->d_model <= 0 || c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 || c->pool_dim <= 0 ||
+      c->ffn_dim <= 0 || c->n_experts <= 0 || c->top_k <= 0 || c->n_layers <= 0 || c->max_ctx < T ||
+      c->vocab < 0 || c->window <= 0 || !c->layer_is_global)
+    return fail(MSM_ERR_INVALID_ARG, "config: non-positive size or missing layer_is_global");
+  if (c->top_k > c->n_experts) return fail(MSM_ERR_INVALID_ARG, "config: top_k > n_experts");
+  if (c->n_q_heads % c->n_kv_heads) return fail(MSM_ERR_INVALID_ARG, "config: n_q_heads % n_kv_heads != 0");
+  const int group = c->n_q_heads / c->n_kv_heads;
+  if (c->head_dim != 64 && c->head_dim != 128) return fail(MSM_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (group != 1 && group != 2 && group != 4 && group != 8)
+    return fail(MSM_ERR_UNSUPPORTED, "n_q_heads / n_kv_heads must be 1, 2, 4 or 8");
+  if (c->d_model % 64 || c->pool_dim % 64 || c->ffn_dim % 64 || (c->n_q_heads * c->head_dim) % 64)
+    return fail(MSM_ERR_UNSUPPORTED, "d_model, pool_dim, ffn_dim, n_q_heads*head_dim must be multiples of 64");
+  if (c->top_k > kMaxTopK) return fail(MSM_ERR_UNSUPPORTED, "top_k > 8");
+  if (c->n_experts > kMaxExperts || c->n_experts % 16) return fail(MSM_ERR_UNSUPPORTED, "n_experts must be <= 256 and a multiple of 16");
+  if (c->vocab % 16) return fail(MSM_ERR_UNSUPPORTED, "vocab must be a multiple of 16");
+  if (c->grid_blocks < 0 || c->attn_splits < 0 || c->prefetch_experts < 0)
+    return fail(MSM_ERR_INVALID_ARG, "config: negative grid_blocks / attn_splits / prefetch_experts");
+  return MSM_OK;
+}
+
+bool parent_valid(const int32_t* parent) {
+  if (!parent || parent[0] != -1) return false;
+  for (int i = 1; i < T; ++i)
+    if (parent[i] < 0 || parent[i] >= i) return false;
+  return true;
+}
+
+msm_status encode_kv_map(msm_model* m, CUtensorMap* map, const void* ptr) {
+  const Dims& dm = m->dm;
+  cuuint64_t dims[3] = {(cuuint64_t)dm.hd, (cuuint64_t)dm.max_ctx, (cuuint64_t)dm.hkv};
+  cuuint64_t strides[2] = {(cuuint64_t)dm.hd * 2, (cuuint64_t)dm.max_ctx * dm.hd * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)dm.attn_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = m->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MSM_ERR_CUDA, "cuTensorMapEncodeTiled failed for a KV cache");
+  return MSM_OK;
+}
+
+msm_status rearm_all(msm_model* m, cudaStream_t s) {
+  for (int c = 0; c < 2; ++c) {
+    uint8_t* x = m->x[c];
+    const XOffsets& o = m->xo;
+    CK(launch_fill_u32(x, o.logits / 4, 0xFFFFFFFFu, s));                       // o, h1, u
+    CK(launch_fill_u32(x + o.logits, (o.z - o.logits) / 4, 0x80000000u, s));    // logits, a
+    CK(launch_fill_u32(x + o.z, (o.total - o.z) / 4, 0xFFFFFFFFu, s));          // z, h2, q0, tkv0
+  }
+  CK(launch_fill_u32(m->sbuf, m->so.y / 4, 0x80000000u, s));                    // part, ml
+  CK(launch_fill_u32(m->sbuf + m->so.y, (m->so.total - m->so.y) / 4, 0xFFFFFFFFu, s));  // y
+  return MSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* msm_last_error(void) { return g_err.c_str(); }
+
+msm_status msm_model_create(const msm_config* config, const msm_weights* w, int device, msm_model** out) {
+  if (!out) return fail(MSM_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  msm_status st = validate_config(config);
+  if (st != MSM_OK) return st;
+  if (!w) return fail(MSM_ERR_INVALID_ARG, "weights is NULL");
+  const msm_config& c = *config;
+  if (!w->w_qkv || !w->w_o || !w->w_pool || !w->w_router || !w->b_router || !w->w_unpool || !w->norm_attn ||
+      !w->norm_moe || !w->w1_codes || !w->w1_scales || !w->w1_tensor_scale || !w->w2_codes || !w->w2_scales ||
+      !w->w2_tensor_scale)
+    return fail(MSM_ERR_INVALID_ARG, "weights: a per-layer pointer array is NULL");
+  for (int l = 0; l < c.n_layers; ++l)
+    if (!w->w_qkv[l] || !w->w_o[l] || !w->w_pool[l] || !w->w_router[l] || !w->b_router[l] || !w->w_unpool[l] ||
+        !w->norm_attn[l] || !w->norm_moe[l] || !w->w1_codes[l] || !w->w1_scales[l] || !w->w1_tensor_scale[l] ||
+        !w->w2_codes[l] || !w->w2_scales[l] || !w->w2_tensor_scale[l])
+      return fail(MSM_ERR_INVALID_ARG, "weights: NULL pointer for layer " + std::to_string(l));
+  if (c.vocab > 0 && (!w->norm_final || !w->w_lm)) return fail(MSM_ERR_INVALID_ARG, "vocab > 0 needs norm_final and w_lm");
+
+  int ndev = 0;
+  CK(cudaGetDeviceCount(&ndev));
+  if (device < 0 || device >= ndev) return fail(MSM_ERR_INVALID_ARG, "no such device");
+  CK(cudaSetDevice(device));
+  int sms = 0, smem_optin = 0, cc_major = 0, cc_minor = 0;
+  CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device));
+  CK(cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device));
+  CK(cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, device));
+  CK(cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, device));
+  if (cc_major != 10 || cc_minor != 3) return fail(MSM_ERR_UNSUPPORTED, "libmsm is built for sm_103a (GB300) only");
+
+  msm_model* m = new msm_model();
+  m->device = device;
+  m->cfg = c;
+  m->global.assign(c.layer_is_global, c.layer_is_global + c.n_layers);
+  m->cfg.layer_is_global = nullptr;
+  Dims& dm = m->dm;
+  dm.d = c.d_model; dm.hq = c.n_q_heads; dm.hkv = c.n_kv_heads; dm.hd = c.head_dim; dm.p = c.pool_dim;
+  dm.f = c.ffn_dim; dm.e = c.n_experts; dm.k = c.top_k; dm.vocab = c.vocab; dm.max_ctx = c.max_ctx;
+  dm.window = c.window; dm.n_layers = c.n_layers;
+  dm.nqkv = (dm.hq + 2 * dm.hkv) * dm.hd;
+  dm.group = dm.hq / dm.hkv;
+  dm.attn_rows = dm.hd == 128 ? 32 : 64;
+  dm.attn_nk = std::max(16, dm.attn_rows * dm.group / 8);
+  dm.attn_wph = dm.attn_rows / dm.attn_nk;
+  dm.rms_eps = c.rms_eps;
+  m->G = c.grid_blocks > 0 ? std::min(c.grid_blocks, sms) : sms;
+  dm.splits = c.attn_splits > 0 ? c.attn_splits : std::max(1, m->G / dm.hkv);
+  if (dm.hkv * dm.splits > m->G) {
+    delete m;
+    return fail(MSM_ERR_INVALID_ARG, "attn_splits * n_kv_heads exceeds the grid");
+  }
+  // shared memory: ring | act | small
+  const int D = dm.hd;
+  const uint64_t attn_need = (uint64_t)dm.group * (D / 16) * kKStepBytes + 2ull * 16 * D * 2 +
+                             (uint64_t)dm.group * dm.attn_wph * 32 * (4 + D / 2) * 4;
+  const uint64_t kmax = (uint64_t)std::max(std::max(dm.d, dm.hq * dm.hd), dm.p);
+  uint64_t act = std::max(std::max(kmax * 32, (uint64_t)dm.p * 32), std::max((uint64_t)dm.f * 32, attn_need));
+  act = (act + 1023) & ~uint64_t(1023);
+  const int smem_cap = std::min(kMaxSmem, smem_optin);
+  long long ring = (long long)smem_cap - (long long)act - kSmallBytes;
+  ring &= ~1023ll;
+  const uint64_t max_tile =
+      std::max(std::max((uint64_t)kDenseTileSteps * kKStepBytes, exp_unit_bytes(dm.p)),
+               std::max(exp_unit_bytes(dm.f), (uint64_t)dm.attn_rows * D * 4));
+  if (ring < (long long)(2 * max_tile)) {
+    delete m;
+    return fail(MSM_ERR_UNSUPPORTED, "widths too large for the shared-memory budget");
+  }
+  m->act_bytes = (int)act;
+  m->ring_bytes = (int)ring;
+  m->smem_bytes = (int)(ring + act + kSmallBytes);
+
+  auto bail = [&](msm_status s2) {
+    msm_model_destroy(m);
+    return s2;
+  };
+#define CKM(call)                                          \
+  do {                                                     \
+    cudaError_t e_ = (call);                               \
+    if (e_ != cudaSuccess) return bail(cuda_fail(e_, #call)); \
+  } while (0)
+
+  CKM(cudaStreamCreateWithFlags(&m->aux, cudaStreamNonBlocking));
+  for (int t = 0; t < 2; ++t)
+    CKM(cudaFuncSetAttribute(layer_kernel(t != 0), cudaFuncAttributeMaxDynamicSharedMemorySize, m->smem_bytes));
+  int occ = 0;
+  CKM(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, layer_kernel(false), kThreads, m->smem_bytes));
+  if (occ < 1) return bail(fail(MSM_ERR_UNSUPPORTED, "the layer kernel does not fit on an SM"));
+
+  cudaDriverEntryPointQueryResult qr;
+  void* fn = nullptr;
+  CKM(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr));
+  if (!fn || qr != cudaDriverEntryPointSuccess) return bail(fail(MSM_ERR_CUDA, "cuTensorMapEncodeTiled unavailable"));
+  m->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+
+  // ---- pack weights ----
+  cudaStream_t s = m->aux;
+  m->L.resize(c.n_layers);
+  const int u1pe = dm.f / 8, u2pe = dm.p / 16;
+  for (int l = 0; l < c.n_layers; ++l) {
+    LayerPack& lp = m->L[l];
+    const uint64_t b_qkv = (dm.nqkv / 16) * dense_unit_bytes(dm.d), b_o = (dm.d / 16) * dense_unit_bytes(dm.hq * dm.hd),
+                   b_pool = (dm.p / 16) * dense_unit_bytes(dm.d), b_r = (dm.e / 16) * dense_unit_bytes(dm.p),
+                   b_unp = (dm.d / 16) * dense_unit_bytes(dm.p),
+                   b_w1 = (uint64_t)dm.e * u1pe * exp_unit_bytes(dm.p),
+                   b_w2 = (uint64_t)dm.e * u2pe * exp_unit_bytes(dm.f);
+    CKM(m->alloc(&lp.qkv, b_qkv));
+    CKM(m->alloc(&lp.o, b_o));
+    CKM(m->alloc(&lp.pool, b_pool));
+    CKM(m->alloc(&lp.router, b_r));
+    CKM(m->alloc(&lp.unpool, b_unp));
+    CKM(m->alloc(&lp.w1, b_w1));
+    CKM(m->alloc(&lp.w2, b_w2));
+    CKM(m->alloc(&lp.b, dm.e * 4));
+    CKM(m->alloc(&lp.w1gs, dm.e * 4));
+    CKM(m->alloc(&lp.w2gs, dm.e * 4));
+    CKM(m->alloc(&lp.g_attn, dm.d * 2));
+    CKM(m->alloc(&lp.g_moe, dm.d * 2));
+    m->packed_bytes += b_qkv + b_o + b_pool + b_r + b_unp + b_w1 + b_w2;
+    CKM(launch_pack_dense(w->w_qkv[l], lp.qkv, dm.nqkv, dm.d, 1, dm.hd, dm.hq, dm.hkv, s));
+    CKM(launch_pack_dense(w->w_o[l], lp.o, dm.d, dm.hq * dm.hd, 0, dm.hd, dm.hq, dm.hkv, s));
+    CKM(launch_pack_dense(w->w_pool[l], lp.pool, dm.p, dm.d, 0, dm.hd, dm.hq, dm.hkv, s));
+    CKM(launch_pack_dense(w->w_router[l], lp.router, dm.e, dm.p, 0, dm.hd, dm.hq, dm.hkv, s));
+    CKM(launch_pack_dense(w->w_unpool[l], lp.unpool, dm.d, dm.p, 0, dm.hd, dm.hq, dm.hkv, s));
+    CKM(launch_pack_nvfp4(w->w1_codes[l], w->w1_scales[l], lp.w1, dm.e, 2 * dm.f, dm.p, 1, dm.f, s));
+    CKM(launch_pack_nvfp4(w->w2_codes[l], w->w2_scales[l], lp.w2, dm.e, dm.p, dm.f, 0, dm.f, s));
+    CKM(cudaMemcpyAsync(lp.b, w->b_router[l], dm.e * 4, cudaMemcpyDeviceToDevice, s));
+    CKM(cudaMemcpyAsync(lp.w1gs, w->w1_tensor_scale[l], dm.e * 4, cudaMemcpyDeviceToDevice, s));
+    CKM(cudaMemcpyAsync(lp.w2gs, w->w2_tensor_scale[l], dm.e * 4, cudaMemcpyDeviceToDevice, s));
+    CKM(cudaMemcpyAsync(lp.g_attn, w->norm_attn[l], dm.d * 2, cudaMemcpyDeviceToDevice, s));
+    CKM(cudaMemcpyAsync(lp.g_moe, w->norm_moe[l], dm.d * 2, cudaMemcpyDeviceToDevice, s));
+  }
+  if (dm.vocab > 0) {
+    const uint64_t b_lm = (dm.vocab / 16) * dense_unit_bytes(dm.d);
+    CKM(m->alloc(&m->lm, b_lm));
+    CKM(m->alloc(&m->g_final, dm.d * 2));
+    m->packed_bytes += b_lm;
+    CKM(launch_pack_dense(w->w_lm, m->lm, dm.vocab, dm.d, 0, dm.hd, dm.hq, dm.hkv, s));
+    CKM(cudaMemcpyAsync(m->g_final, w->norm_final, dm.d * 2, cudaMemcpyDeviceToDevice, s));
+  }
+
+  // ---- exchange buffers ----
+  XOffsets& xo = m->xo;
+  uint64_t o = 0;
+  xo.o = o; o += align256((uint64_t)T * dm.hq * dm.hd * 2);
+  xo.h1 = o; o += align256((uint64_t)T * dm.d * 2);
+  xo.u = o; o += align256((uint64_t)T * dm.p * 2);
+  xo.logits = o; o += align256((uint64_t)T * dm.e * 4);
+  xo.a = o; o += align256((uint64_t)T * dm.k * dm.f * 4);
+  xo.z = o; o += align256((uint64_t)T * dm.p * 2);
+  xo.h2 = o; o += align256((uint64_t)T * dm.d * 2);
+  xo.q0 = o; o += align256((uint64_t)T * dm.hq * dm.hd * 2);
+  xo.tkv0 = o; o += align256(2ull * dm.hkv * T * dm.hd * 2);
+  xo.total = o;
+  SOffsets& so = m->so;
+  o = 0;
+  so.part = o; o += align256((uint64_t)dm.hkv * dm.splits * T * dm.group * dm.hd * 4);
+  so.ml = o; o += align256((uint64_t)dm.hkv * dm.splits * T * dm.group * 2 * 4);
+  so.y = o; o += align256((uint64_t)T * dm.k * dm.p * 2);
+  so.total = o;
+  CKM(m->alloc(&m->x[0], xo.total));
+  CKM(m->alloc(&m->x[1], xo.total));
+  CKM(m->alloc(&m->sbuf, so.total));
+  for (int i = 0; i < 2; ++i) {
+    CKM(m->alloc(&m->in_q[i], (uint64_t)T * dm.hq * dm.hd * 2));
+    CKM(m->alloc(&m->in_h[i], (uint64_t)T * dm.d * 2));
+  }
+  CKM(m->alloc(&m->rope, (uint64_t)T * (dm.hd / 2) * 2 * 4));
+  CKM(m->alloc(&m->inv_freq, (uint64_t)(dm.hd / 2) * 8));
+  {
+    std::vector<double> inv(dm.hd / 2);
+    for (int i = 0; i < dm.hd / 2; ++i) inv[i] = std::pow((double)c.rope_theta, -2.0 * i / dm.hd);
+    CKM(cudaMemcpyAsync(m->inv_freq, inv.data(), inv.size() * 8, cudaMemcpyHostToDevice, s));
+    CKM(cudaStreamSynchronize(s));
+  }
+  CKM(m->alloc(&m->routing_idx, (uint64_t)c.n_layers * T * dm.k * 4));
+  CKM(m->alloc(&m->routing_w, (uint64_t)c.n_layers * T * dm.k * 4));
+  CKM(m->alloc(&m->hist, 2ull * c.n_layers * dm.e * 4));
+  CKM(m->alloc(&m->tree_dbg, 32 * 4));
+  CKM(m->alloc(&m->timing, (uint64_t)c.n_layers * m->G * kTimingEvents * 8));
+  CKM(m->alloc(&m->status, sizeof(DevStatus)));
+  CKM(m->alloc(&m->io_in, (uint64_t)T * dm.d * 2));
+  CKM(m->alloc(&m->io_hidden, (uint64_t)T * dm.d * 2));
+  if (dm.vocab > 0) CKM(m->alloc(&m->io_logits, (uint64_t)T * dm.vocab * 4));
+  CKM(cudaMemsetAsync(m->hist, 0, 2ull * c.n_layers * dm.e * 4, s));
+  CKM(cudaMemsetAsync(m->status, 0, sizeof(DevStatus), s));
+  CKM(cudaMemsetAsync(m->timing, 0, (uint64_t)c.n_layers * m->G * kTimingEvents * 8, s));
+  st = rearm_all(m, s);
+  if (st != MSM_OK) return bail(st);
+  CKM(cudaStreamSynchronize(s));
+  m->tmk.resize(c.n_layers);
+  m->tmv.resize(c.n_layers);
+  m->tmk_ptr.assign(c.n_layers, nullptr);
+  m->tmv_ptr.assign(c.n_layers, nullptr);
+#undef CKM
+  *out = m;
+  return MSM_OK;
+}
+
+void msm_model_destroy(msm_model* m) {
+  if (!m) return;
+  cudaSetDevice(m->device);
+  cudaDeviceSynchronize();
+  for (void* p : m->allocs) cudaFree(p);
+  if (m->aux) cudaStreamDestroy(m->aux);
+  delete m;
+}
+
+msm_status msm_verify_step(msm_model* m, const void* hidden_in, const int32_t* parent, int32_t pos0,
+                           void* const* k_cache, void* const* v_cache, float* logits_out, void* hidden_out,
+                           void* stream) {
+  if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
+  const Dims& dm = m->dm;
+  if (!hidden_in || !k_cache || !v_cache) return fail(MSM_ERR_INVALID_ARG, "NULL hidden_in or cache array");
+  if (!parent_valid(parent)) return fail(MSM_ERR_INVALID_ARG, "parent must satisfy parent[0] == -1, 0 <= parent[i] < i");
+  if (pos0 < 0 || (int64_t)pos0 + T > dm.max_ctx) return fail(MSM_ERR_INVALID_ARG, "pos0 out of range");
+  if (dm.vocab > 0 && !logits_out) return fail(MSM_ERR_INVALID_ARG, "logits_out is NULL but vocab > 0");
+  if (dm.vocab == 0 && !hidden_out) return fail(MSM_ERR_INVALID_ARG, "hidden_out is NULL but vocab == 0");
+  if ((reinterpret_cast<uintptr_t>(hidden_in) & 15) || (reinterpret_cast<uintptr_t>(hidden_out) & 15) ||
+      (reinterpret_cast<uintptr_t>(logits_out) & 15))
+    return fail(MSM_ERR_INVALID_ARG, "hidden / logits buffers must be 16-byte aligned");
+  for (int l = 0; l < dm.n_layers; ++l) {
+    if (!k_cache[l] || !v_cache[l]) return fail(MSM_ERR_INVALID_ARG, "NULL KV cache pointer");
+    if ((reinterpret_cast<uintptr_t>(k_cache[l]) & 15) || (reinterpret_cast<uintptr_t>(v_cache[l]) & 15))
+      return fail(MSM_ERR_INVALID_ARG, "KV caches must be 16-byte aligned");
+  }
+  CK(cudaSetDevice(m->device));
+  for (int l = 0; l < dm.n_layers; ++l) {
+    if (m->tmk_ptr[l] != k_cache[l]) {
+      msm_status st = encode_kv_map(m, &m->tmk[l], k_cache[l]);
+      if (st != MSM_OK) return st;
+      m->tmk_ptr[l] = k_cache[l];
+    }
+    if (m->tmv_ptr[l] != v_cache[l]) {
+      msm_status st = encode_kv_map(m, &m->tmv[l], v_cache[l]);
+      if (st != MSM_OK) return st;
+      m->tmv_ptr[l] = v_cache[l];
+    }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint64_t tmo = (uint64_t)(m->cfg.timeout_us ? m->cfg.timeout_us : 200000u) * 1000ull;
+  const int sp = (int)(m->step_count & 1);
+  LaunchParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.dm = dm;
+  P.xo = m->xo;
+  P.so = m->so;
+  P.s_buf = m->sbuf;
+  P.rope = m->rope;
+  P.inv_freq = m->inv_freq;
+  P.tree_dbg = m->tree_dbg;
+  P.status = m->status;
+  P.pos0 = pos0;
+  P.ring_bytes = m->ring_bytes;
+  P.act_bytes = m->act_bytes;
+  P.flags = m->cfg.flags;
+  P.timeout_ns_lo = (uint32_t)tmo;
+  P.timeout_ns_hi = (uint32_t)(tmo >> 32);
+  P.prefetch_experts = m->cfg.prefetch_experts > 0 ? m->cfg.prefetch_experts : 14;
+  P.phase_rot = 13;
+  std::memcpy(P.parent, parent, sizeof(int32_t) * T);
+  P.hidden_in = static_cast<const uint16_t*>(hidden_in);
+  P.logits = logits_out;
+  const bool timing = (m->cfg.flags & MSM_FLAG_SELF_TIMING) != 0;
+  const bool pdl = (m->cfg.flags & MSM_FLAG_PDL) != 0;
+  for (int l = 0; l < dm.n_layers; ++l) {
+    const LayerPack& lp = m->L[l];
+    const bool first = l == 0, last = l == dm.n_layers - 1;
+    const int c = (int)(m->launch_count & 1);
+    P.layer = l;
+    P.first = first;
+    P.last = last;
+    P.is_global = m->global[l] != 0;
+    P.next_global = last ? 0 : (m->global[l + 1] != 0);
+    P.w_qkv_pro = first ? lp.qkv : nullptr;
+    P.g_attn_pro = first ? lp.g_attn : nullptr;
+    P.w_o = lp.o;
+    P.w_pool = lp.pool;
+    P.w_router = lp.router;
+    P.b_router = lp.b;
+    P.w_unpool = lp.unpool;
+    P.g_moe = lp.g_moe;
+    P.w1 = lp.w1;
+    P.w2 = lp.w2;
+    P.w1_gs = lp.w1gs;
+    P.w2_gs = lp.w2gs;
+    P.w_tail = last ? m->lm : m->L[l + 1].qkv;
+    P.g_tail = last ? m->g_final : m->L[l + 1].g_attn;
+    P.hidden_out = last ? static_cast<uint16_t*>(hidden_out) : nullptr;
+    P.kc = static_cast<uint16_t*>(k_cache[l]);
+    P.vc = static_cast<uint16_t*>(v_cache[l]);
+    P.kc_next = last ? nullptr : static_cast<uint16_t*>(k_cache[l + 1]);
+    P.vc_next = last ? nullptr : static_cast<uint16_t*>(v_cache[l + 1]);
+    P.kc_pf = P.kc_next;
+    P.vc_pf = P.vc_next;
+    P.x_cur = m->x[c];
+    P.x_next = m->x[c ^ 1];
+    P.in_q = m->in_q[c];
+    P.in_h = m->in_h[c];
+    P.out_q = m->in_q[c ^ 1];
+    P.out_h = m->in_h[c ^ 1];
+    P.routing_idx = m->routing_idx + (size_t)l * T * dm.k;
+    P.routing_w = m->routing_w + (size_t)l * T * dm.k;
+    P.hist_cur = m->hist + ((size_t)sp * dm.n_layers + l) * dm.e;
+    P.hist_prev = m->step_count > 0 ? m->hist + ((size_t)(sp ^ 1) * dm.n_layers + l) * dm.e : nullptr;
+    P.timing = m->timing + (size_t)l * m->G * kTimingEvents;
+    P.tmap_k = m->tmk[l];
+    P.tmap_v = m->tmv[l];
+
+    cudaLaunchConfig_t lc;
+    std::memset(&lc, 0, sizeof(lc));
+    lc.gridDim = dim3(m->G);
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = m->smem_bytes;
+    lc.stream = s;
+    cudaLaunchAttribute attr[1];
+    int na = 0;
+    if (pdl && !first) {
+      attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[na].val.programmaticStreamSerializationAllowed = 1;
+      ++na;
+    }
+    lc.attrs = na ? attr : nullptr;
+    lc.numAttrs = na;
+    void* args[] = {&P};
+    cudaError_t e = cudaLaunchKernelExC(&lc, layer_kernel(timing), args);
+    if (e != cudaSuccess) return cuda_fail(e, "layer kernel launch");
+    ++m->launch_count;
+  }
+  ++m->step_count;
+  return MSM_OK;
+}
+
+msm_status msm_sync(msm_model* m, void* stream) {
+  if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
+  CK(cudaSetDevice(m->device));
+  CK(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  DevStatus ds;
+  CK(cudaMemcpy(&ds, m->status, sizeof(ds), cudaMemcpyDeviceToHost));
+  if (ds.code == 0) return MSM_OK;
+  char buf[160];
+  std::snprintf(buf, sizeof(buf), "device wait timed out (layer %d, phase %d, block %d)", ds.layer, ds.phase, ds.block);
+  msm_status st = (ds.code == MSM_ERR_DEVICE_TIMEOUT) ? MSM_ERR_DEVICE_TIMEOUT : MSM_ERR_CUDA;
+  if (ds.code != MSM_ERR_DEVICE_TIMEOUT) std::snprintf(buf, sizeof(buf), "device error %d (phase %d)", ds.code, ds.phase);
+  // re-arm every exchange buffer and clear the status for the next step
+  msm_status r = rearm_all(m, m->aux);
+  if (r != MSM_OK) return r;
+  CK(cudaMemsetAsync(m->status, 0, sizeof(DevStatus), m->aux));
+  CK(cudaStreamSynchronize(m->aux));
+  return fail(st, buf);
+}
+
+msm_status msm_verify_step_host(msm_model* m, const void* hidden_in_host, const int32_t* parent, int32_t pos0,
+                                void* const* k_cache, void* const* v_cache, float* logits_host,
+                                void* hidden_out_host, void* stream) {
+  if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
+  const Dims& dm = m->dm;
+  if (!hidden_in_host) return fail(MSM_ERR_INVALID_ARG, "hidden_in_host is NULL");
+  if (dm.vocab > 0 && !logits_host) return fail(MSM_ERR_INVALID_ARG, "logits_host is NULL but vocab > 0");
+  if (dm.vocab == 0 && !hidden_out_host) return fail(MSM_ERR_INVALID_ARG, "hidden_out_host is NULL but vocab == 0");
+  CK(cudaSetDevice(m->device));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t h_bytes = (size_t)T * dm.d * 2, l_bytes = (size_t)T * dm.vocab * 4;
+  CK(cudaMemcpyAsync(m->io_in, hidden_in_host, h_bytes, cudaMemcpyHostToDevice, s));
+  msm_status st = msm_verify_step(m, m->io_in, parent, pos0, k_cache, v_cache, dm.vocab > 0 ? m->io_logits : nullptr,
+                                  hidden_out_host ? m->io_hidden : nullptr, stream);
+  if (st != MSM_OK) return st;
+  if (dm.vocab > 0) CK(cudaMemcpyAsync(logits_host, m->io_logits, l_bytes, cudaMemcpyDeviceToHost, s));
+  if (hidden_out_host) CK(cudaMemcpyAsync(hidden_out_host, m->io_hidden, h_bytes, cudaMemcpyDeviceToHost, s));
+  return msm_sync(m, stream);
+}
+
+msm_status msm_get_routing(msm_model* m, int32_t* idx, float* w) {
+  if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
+  CK(cudaSetDevice(m->device));
+  CK(cudaDeviceSynchronize());
+  const size_t n = (size_t)m->dm.n_layers * T * m->dm.k;
+  if (idx) CK(cudaMemcpy(idx, m->routing_idx, n * 4, cudaMemcpyDeviceToHost));
+  if (w) CK(cudaMemcpy(w, m->routing_w, n * 4, cudaMemcpyDeviceToHost));
+  return MSM_OK;
+}
+
+msm_status msm_get_tree(msm_model* m, uint32_t* anc, int32_t* tpos) {
+  if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
+  CK(cudaSetDevice(m->device));
+  CK(cudaDeviceSynchronize());
+  uint32_t buf[32];
+  CK(cudaMemcpy(buf, m->tree_dbg, sizeof(buf), cudaMemcpyDeviceToHost));
+  if (anc) std::memcpy(anc, buf, 16 * 4);
+  if (tpos) std::memcpy(tpos, buf + 16, 16 * 4);
+  return MSM_OK;
+}
+
+msm_status msm_get_timing(msm_model* m, uint64_t* buf, size_t n) {
+  if (!m || !buf) return fail(MSM_ERR_INVALID_ARG, "model or buffer is NULL");
+  const size_t need = (size_t)m->dm.n_layers * m->G * kTimingEvents;
+  if (n < need) return fail(MSM_ERR_INVALID_ARG, "timing buffer too small");
+  CK(cudaSetDevice(m->device));
+  CK(cudaDeviceSynchronize());
+  CK(cudaMemcpy(buf, m->timing, need * 8, cudaMemcpyDeviceToHost));
+  return MSM_OK;
+}
+
+msm_status msm_get_stats(const msm_model* m, msm_stats* out) {
+  if (!m || !out) return fail(MSM_ERR_INVALID_ARG, "model or out is NULL");
+  out->grid_blocks = m->G;
+  out->threads_per_block = kThreads;
+  out->smem_bytes = m->smem_bytes;
+  out->attn_splits = m->dm.splits;
+  out->launches_per_step = m->dm.n_layers;
+  out->cooperative = 0;
+  out->packed_weight_bytes = m->packed_bytes;
+  out->exchange_bytes = 2 * m->xo.total + m->so.total;
+  return MSM_OK;
+}
+
+msm_status msm_get_exchange(msm_model* m, const char* name, void* host, size_t bytes) {
+  if (!m || !name || !host) return fail(MSM_ERR_INVALID_ARG, "model, name or buffer is NULL");
+  if (m->launch_count == 0) return fail(MSM_ERR_INVALID_ARG, "no step has run");
+  const XOffsets& o = m->xo;
+  struct { const char* n; uint64_t off, len; } tab[] = {
+      {"o", o.o, (uint64_t)T * m->dm.hq * m->dm.hd * 2}, {"h1", o.h1, (uint64_t)T * m->dm.d * 2},
+      {"u", o.u, (uint64_t)T * m->dm.p * 2},            {"logits", o.logits, (uint64_t)T * m->dm.e * 4},
+      {"a", o.a, (uint64_t)T * m->dm.k * m->dm.f * 4},  {"z", o.z, (uint64_t)T * m->dm.p * 2},
+      {"h2", o.h2, (uint64_t)T * m->dm.d * 2}};
+  for (auto& e : tab) {
+    if (std::strcmp(e.n, name) != 0) continue;
+    if (bytes < e.len) return fail(MSM_ERR_INVALID_ARG, "buffer too small");
+    CK(cudaSetDevice(m->device));
+    CK(cudaDeviceSynchronize());
+    const int c = (int)((m->launch_count - 1) & 1);
+    CK(cudaMemcpy(host, m->x[c] + e.off, e.len, cudaMemcpyDeviceToHost));
+    return MSM_OK;
+  }
+  return fail(MSM_ERR_INVALID_ARG, std::string("unknown exchange buffer ") + name);
+}
+
+msm_status msm_draft_step(msm_model* m, const void* draft_hidden_in, int32_t* tokens_out, int32_t* parent_out,
+                          void* stream) {
+  (void)m; (void)draft_hidden_in; (void)tokens_out; (void)parent_out; (void)stream;
+  return fail(MSM_ERR_UNSUPPORTED, "msm_draft_step is not built in this version");
+}
+
+}  // extern "C"

@@ -1,0 +1,131 @@
+// Internal definitions shared by the host runtime (msm_api.cu) and the kernels
+// (msm_kernel.cu, msm_pack.cu) of libmsm.  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <stdint.h>
+
+namespace msm {
+
+constexpr int T = 16;                 // tree tokens per verify step
+constexpr int kThreads = 384;         // 12 warps per persistent block
+constexpr int kLoaderWarp = 0;        // TMA producer of the shared-memory weight ring
+constexpr int kPrefetchWarp = 3;      // L2 prefetch of the previous step's hot experts
+constexpr int kFirstCompute = 4;      // warps 4..11: attention / GEMM / expert workers
+constexpr int kComputeWarps = 8;
+constexpr int kComputeThreads = kComputeWarps * 32;
+constexpr int kSlots = 12;            // descriptors of the variable-size ring
+constexpr int kDenseTileSteps = 32;   // 16-row x 512-column bf16 tiles: 32 k-steps x 512 B
+constexpr int kKStepBytes = 512;      // one 16x16 bf16 (or f16) block in ldmatrix order
+constexpr int kExpGroupBytes = 576;   // 16 rows x 64 columns NVFP4: 512 B codes + 64 B scales
+constexpr int kSmallBytes = 8 * 1024; // barriers, routing tables, scratch
+constexpr int kMaxSmem = 232448;      // 227 KB opt-in dynamic shared memory per block
+constexpr int kTimingEvents = 16;
+constexpr int kMaxTopK = 8;
+constexpr int kMaxExperts = 256;
+
+// phases of one layer launch (also the self-timing event ids)
+enum Phase : int {
+  PH_START = 0, PH_PROLOGUE = 1, PH_ATTN = 2, PH_ATTN_MERGE = 3, PH_OPROJ = 4, PH_POOL = 5,
+  PH_ROUTER = 6, PH_ROUTE = 7, PH_GEMM1 = 8, PH_GEMM2 = 9, PH_COMBINE = 10, PH_UNPOOL = 11,
+  PH_TAIL = 12, PH_END = 13
+};
+
+// device status word
+struct DevStatus {
+  int code;    // 0 or msm_status
+  int phase;   // Phase where the first failure was seen
+  int block;
+  int layer;
+  int abort;   // set by the first failing block; every wait gives up once it is set
+  int pad[3];
+};
+
+// Exchange buffers of one launch parity (byte offsets into the parity's region).
+struct XOffsets {
+  uint64_t o, h1, u, logits, a, z, h2, q0, tkv0;  // re-armed by the next launch
+  uint64_t total;
+};
+// Buffers drained by their single consumer (never double-buffered).
+struct SOffsets {
+  uint64_t part, ml, y;
+  uint64_t total;
+};
+
+struct Dims {
+  int d, hq, hkv, hd, p, f, e, k, vocab, max_ctx, window, n_layers;
+  int nqkv;        // (hq + 2 hkv) hd
+  int group;       // hq / hkv
+  int attn_rows;   // R: KV rows per attention tile
+  int attn_nk;     // keys per warp per tile
+  int attn_wph;    // warps per q head
+  int splits;      // attention splits per kv head
+  float rms_eps;
+};
+
+struct LaunchParams {
+  Dims dm;
+  // packed weights
+  const uint8_t* w_qkv_pro;   // layer 0 QKV (prologue of launch 0) or null
+  const uint16_t* g_attn_pro; // layer 0 attention norm gain
+  const uint8_t* w_o;
+  const uint8_t* w_pool;
+  const uint8_t* w_router;
+  const float* b_router;
+  const uint8_t* w_unpool;
+  const uint16_t* g_moe;
+  const uint8_t* w1;
+  const uint8_t* w2;
+  const float* w1_gs;
+  const float* w2_gs;
+  const uint8_t* w_tail;      // next layer's QKV, or the LM head on the last layer
+  const uint16_t* g_tail;     // next layer's attention gain, or the final gain
+  // caller buffers
+  const uint16_t* hidden_in;  // launch 0
+  uint16_t* hidden_out;       // last launch (optional)
+  float* logits;              // last launch with vocab > 0
+  uint16_t* kc;               // this layer's caches
+  uint16_t* vc;
+  uint16_t* kc_next;          // next layer's caches (tail writes the tree rows)
+  uint16_t* vc_next;
+  const uint16_t* kc_pf;      // next layer's caches for the KV L2 prefetch
+  const uint16_t* vc_pf;
+  // model buffers
+  uint8_t* x_cur;             // exchange region of this launch's parity
+  uint8_t* x_next;            // the other parity: re-armed here
+  uint8_t* s_buf;             // single-consumer buffers
+  XOffsets xo;
+  SOffsets so;
+  const uint16_t* in_q;       // Q / residual handed over by the previous launch
+  const uint16_t* in_h;
+  uint16_t* out_q;            // ... and to the next launch
+  uint16_t* out_h;
+  float* rope;                // [16 depth][hd/2][2] cos, sin (filled by launch 0)
+  const double* inv_freq;     // [hd/2]
+  int32_t* routing_idx;       // [16][k] of this layer
+  float* routing_w;
+  uint32_t* hist_cur;         // [e] expert usage of this layer in this step
+  const uint32_t* hist_prev;  // [e] ... in the previous step
+  uint32_t* tree_dbg;         // [32]: anc[16], tpos[16]
+  uint64_t* timing;           // [grid][kTimingEvents] of this layer
+  DevStatus* status;
+  // scalars
+  int layer, first, last, is_global, next_global, pos0;
+  int ring_bytes, act_bytes;
+  uint32_t flags;
+  uint32_t timeout_ns_lo, timeout_ns_hi;
+  int prefetch_experts;
+  int phase_rot;
+  int32_t parent[16];
+  // KV cache tensor maps of this layer: 3-D {hd, max_ctx, hkv}, 128-byte swizzle
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
+};
+
+// packed sizes
+__host__ __device__ inline uint64_t dense_unit_bytes(int K) { return (uint64_t)K * 32; }  // 16 rows x K bf16
+__host__ __device__ inline uint64_t exp_unit_bytes(int K) { return (uint64_t)(K / 64) * kExpGroupBytes; }
+
+// kernel entry points (defined in msm_kernel.cu / msm_pack.cu)
+const void* layer_kernel(bool timing);
+
+}  // namespace msm

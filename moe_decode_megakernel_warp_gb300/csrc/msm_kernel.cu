@@ -1,0 +1,1477 @@
+// The per-layer persistent kernel of the verify step (sm_103a).
+//
+// One launch runs, on every SM, one 384-thread block with fixed warp roles
+// (alphasignal.ai, "LMSYS Doubles Muse Spark Open Speed to 1,109 Tokens per
+// Second", § "A 12-warp pipeline takes over scheduling"; orcarouter.ai,
+// "Muse Spark Open: 1,109 tokens/s is a kernel-level change", § "where the
+// kernel boundary sits"):
+//   warp 0      TMA producer: streams the block's weight tiles (and KV tiles)
+//               into a shared-memory ring, running ahead into the next op's
+//               weights while the current op waits for its inputs
+//   warps 1-2   re-arm the exchange buffers the next launch will use
+//   warp 3      L2 prefetch of the previous step's most-used experts
+//   warps 4-11  attention, dense GEMMs, expert GEMMs, combines
+// The launch covers layer l's attention through layer l+1's QKV projection and
+// KV-cache write (alphasignal.ai, § "Launch boundaries leave hardware idle").
+// Blocks hand data to each other through global-memory slots that carry their
+// own readiness: a slot is empty while it holds a sentinel (0xFFFF for bf16, an
+// all-ones NaN no rounding produces; -0.0 for fp32, since writers store x+0.0)
+// and consumers poll the payload itself, with no write-fence-flag sequence
+// (alphasignal.ai, § "Four mechanisms keep work moving"; orcarouter.ai, §
+// "three bills").  Every wait is bounded by %globaltimer.
+#include "msm_device.cuh"
+#include "msm_internal.h"
+
+namespace msm {
+
+// ---------------------------------------------------------------------------
+// shared memory carve-up
+// ---------------------------------------------------------------------------
+struct Smem {
+  uint8_t* ring;
+  uint8_t* act;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* route_bar;
+  uint32_t* slot_off;
+  volatile int* abort;
+  int* n_active;
+  uint32_t* anc;
+  int32_t* tpos;
+  int32_t* depth;
+  int32_t* topk_idx;  // [16][8]
+  float* topk_w;      // [16][8]
+  int16_t* act_e;     // [128]
+  uint8_t* act_n;     // [128]
+  uint8_t* act_tok;   // [128][16]
+  uint8_t* act_slot;  // [128][16]
+  float* x_ts;        // [16]
+  float* a_ts;        // [16]
+  float* red;         // [8][16]
+};
+
+__device__ __forceinline__ Smem carve(uint8_t* base, const LaunchParams& P) {
+  Smem s;
+  s.ring = base;
+  s.act = base + P.ring_bytes;
+  uint8_t* sm = s.act + P.act_bytes;
+  s.full = reinterpret_cast<uint64_t*>(sm + 0);
+  s.empty = reinterpret_cast<uint64_t*>(sm + 96);
+  s.route_bar = reinterpret_cast<uint64_t*>(sm + 192);
+  s.slot_off = reinterpret_cast<uint32_t*>(sm + 200);
+  s.abort = reinterpret_cast<volatile int*>(sm + 248);
+  s.n_active = reinterpret_cast<int*>(sm + 252);
+  s.anc = reinterpret_cast<uint32_t*>(sm + 256);
+  s.tpos = reinterpret_cast<int32_t*>(sm + 320);
+  s.depth = reinterpret_cast<int32_t*>(sm + 384);
+  s.topk_idx = reinterpret_cast<int32_t*>(sm + 448);
+  s.topk_w = reinterpret_cast<float*>(sm + 960);
+  s.act_e = reinterpret_cast<int16_t*>(sm + 1472);
+  s.act_n = sm + 1728;
+  s.act_tok = sm + 1856;
+  s.act_slot = sm + 3904;
+  s.x_ts = reinterpret_cast<float*>(sm + 5952);
+  s.a_ts = reinterpret_cast<float*>(sm + 6016);
+  s.red = reinterpret_cast<float*>(sm + 6080);
+  return s;
+}
+
+// ---------------------------------------------------------------------------
+// bounded waits
+// ---------------------------------------------------------------------------
+struct Ctx {
+  const LaunchParams* P;
+  Smem S;
+  uint64_t deadline;
+  int block;
+
+  __device__ void fail(int phase) {
+    *S.abort = 1;
+    if (atomicCAS(&P->status->code, 0, 4 /* MSM_ERR_DEVICE_TIMEOUT */) == 0) {
+      P->status->phase = phase;
+      P->status->block = block;
+      P->status->layer = P->layer;
+    }
+    atomicExch(&P->status->abort, 1);
+  }
+  // true when the caller must give up
+  __device__ bool expired(int phase) {
+    if (*S.abort) return true;
+    if (ld_relaxed_u32(&P->status->abort) != 0) {
+      *S.abort = 1;
+      return true;
+    }
+    if (globaltimer() > deadline) {
+      fail(phase);
+      return true;
+    }
+    return false;
+  }
+};
+
+__device__ __forceinline__ bool wait_bar(Ctx& cx, uint64_t* bar, uint32_t parity, int phase) {
+  uint32_t n = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++n & 15) == 0 && cx.expired(phase)) return false;
+  }
+  return true;
+}
+
+// poll a 16-byte bf16 chunk until none of its 8 elements is the sentinel
+__device__ __forceinline__ bool poll_bf16x8(Ctx& cx, const void* p, uint4& v, int phase) {
+  uint32_t n = 0;
+  v = ld_relaxed_v4(p);
+  while (!bf16x8_ready(v)) {
+    if ((++n & 31) == 0 && cx.expired(phase)) return false;
+    v = ld_relaxed_v4(p);
+  }
+  return true;
+}
+__device__ __forceinline__ bool poll_f32x4(Ctx& cx, const void* p, uint4& v, int phase) {
+  uint32_t n = 0;
+  v = ld_relaxed_v4(p);
+  while (!f32x4_ready(v)) {
+    if ((++n & 31) == 0 && cx.expired(phase)) return false;
+    v = ld_relaxed_v4(p);
+  }
+  return true;
+}
+__device__ __forceinline__ bool poll_f32x2(Ctx& cx, const void* p, uint2& v, int phase) {
+  uint32_t n = 0;
+  v = ld_relaxed_v2(p);
+  while (v.x == kF32Empty || v.y == kF32Empty) {
+    if ((++n & 31) == 0 && cx.expired(phase)) return false;
+    v = ld_relaxed_v2(p);
+  }
+  return true;
+}
+
+template <bool kTiming>
+__device__ __forceinline__ void stamp(const LaunchParams& P, int block, int ev) {
+  if (kTiming) P.timing[(size_t)block * kTimingEvents + ev] = globaltimer();
+}
+
+// ---------------------------------------------------------------------------
+// work split (identical in the loader and the consumers)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void unit_range(int n_units, int bb, int G, int& lo, int& hi) {
+  lo = (int)(((long long)n_units * bb) / G);
+  hi = (int)(((long long)n_units * (bb + 1)) / G);
+}
+__device__ __forceinline__ int rot_block(int b, int rot, int G) { return (b + rot) % G; }
+
+// attention unit of block bb: kv head, split, row range
+struct AttnUnit {
+  int valid, hk, s, r0, r1, n_sub, tree;
+};
+__device__ __forceinline__ AttnUnit attn_unit(const LaunchParams& P, int bb, int is_global) {
+  const Dims& dm = P.dm;
+  AttnUnit u;
+  u.valid = bb < dm.hkv * dm.splits;
+  u.hk = u.valid ? bb / dm.splits : 0;
+  u.s = u.valid ? bb % dm.splits : 0;
+  int lo = is_global ? 0 : max(0, P.pos0 - dm.window + 1);
+  int n = P.pos0 - lo;
+  int chunk = (n + dm.splits - 1) / dm.splits;
+  chunk = ((chunk + dm.attn_rows - 1) / dm.attn_rows) * dm.attn_rows;
+  if (chunk < dm.attn_rows) chunk = dm.attn_rows;
+  u.r0 = min(P.pos0, lo + u.s * chunk);
+  u.r1 = min(P.pos0, u.r0 + chunk);
+  u.n_sub = u.valid ? (u.r1 - u.r0 + dm.attn_rows - 1) / dm.attn_rows : 0;
+  u.tree = u.valid && (u.s == dm.splits - 1);
+  return u;
+}
+
+// ---------------------------------------------------------------------------
+// the variable-size shared-memory ring (producer side)
+// ---------------------------------------------------------------------------
+struct Ring {
+  uint32_t issued;  // tiles issued
+  uint32_t tail;    // oldest tile not known to be released
+  uint32_t head;    // next free byte
+  uint32_t off[kSlots], end[kSlots];
+};
+
+__device__ bool ring_place(Ctx& cx, Ring& r, uint32_t bytes, uint32_t& off_out) {
+  const uint32_t cap = (uint32_t)cx.P->ring_bytes;
+  uint32_t off = r.head;
+  if (off + bytes > cap) off = 0;
+  for (;;) {
+    bool conflict = (r.issued - r.tail) >= (uint32_t)kSlots;
+    for (uint32_t j = r.tail; j < r.issued && !conflict; ++j) {
+      uint32_t s = j % kSlots;
+      if (r.off[s] < off + bytes && off < r.end[s]) conflict = true;
+    }
+    if (!conflict) break;
+    uint32_t s = r.tail % kSlots;
+    if (!wait_bar(cx, &cx.S.empty[s], (r.tail / kSlots) & 1, 99)) return false;
+    ++r.tail;
+  }
+  off_out = off;
+  r.head = off + ((bytes + 1023u) & ~1023u);
+  return true;
+}
+
+struct Seg {
+  const void* src;
+  uint32_t bytes;
+};
+
+// issue one tile made of up to 4 contiguous segments
+__device__ bool ring_issue(Ctx& cx, Ring& r, const Seg* seg, int nseg, uint64_t pol) {
+  uint32_t total = 0;
+  for (int i = 0; i < nseg; ++i) total += seg[i].bytes;
+  uint32_t off;
+  if (!ring_place(cx, r, total, off)) return false;
+  const uint32_t s = r.issued % kSlots;
+  r.off[s] = off;
+  r.end[s] = off + total;
+  cx.S.slot_off[s] = off;
+  mbar_expect_tx(&cx.S.full[s], total);
+  uint32_t o = off;
+  for (int i = 0; i < nseg; ++i) {
+    bulk_g2s(cx.S.ring + o, seg[i].src, seg[i].bytes, &cx.S.full[s], pol);
+    o += seg[i].bytes;
+  }
+  ++r.issued;
+  return true;
+}
+
+__device__ bool ring_issue_kv(Ctx& cx, Ring& r, int hk, int row, uint32_t tile_bytes) {
+  const LaunchParams& P = *cx.P;
+  uint32_t off;
+  if (!ring_place(cx, r, tile_bytes, off)) return false;
+  const uint32_t s = r.issued % kSlots;
+  r.off[s] = off;
+  r.end[s] = off + tile_bytes;
+  cx.S.slot_off[s] = off;
+  mbar_expect_tx(&cx.S.full[s], tile_bytes);
+  const int R = P.dm.attn_rows;
+  const int halves = P.dm.hd / 64;
+  uint8_t* dst = cx.S.ring + off;
+  for (int h = 0; h < halves; ++h) {
+    tma_load_3d(dst + h * R * 128, &P.tmap_k, h * 64, row, hk, &cx.S.full[s]);
+    tma_load_3d(dst + (halves + h) * R * 128, &P.tmap_v, h * 64, row, hk, &cx.S.full[s]);
+  }
+  ++r.issued;
+  return true;
+}
+
+__device__ bool load_dense(Ctx& cx, Ring& r, const uint8_t* W, int K, int N, int rot, uint64_t pol) {
+  const LaunchParams& P = *cx.P;
+  const int G = gridDim.x;
+  int lo, hi;
+  unit_range(N / 16, rot_block(cx.block, rot, G), G, lo, hi);
+  const int steps = K / 16;
+  const uint64_t ub = dense_unit_bytes(K);
+  for (int u = lo; u < hi; ++u) {
+    for (int k0 = 0; k0 < steps; k0 += kDenseTileSteps) {
+      int ns = min(kDenseTileSteps, steps - k0);
+      Seg sg = {W + (uint64_t)u * ub + (uint64_t)k0 * kKStepBytes, (uint32_t)ns * kKStepBytes};
+      if (!ring_issue(cx, r, &sg, 1, pol)) return false;
+    }
+  }
+  (void)P;
+  return true;
+}
+
+template <bool kTiming>
+__device__ void loader(Ctx& cx) {
+  const LaunchParams& P = *cx.P;
+  const Dims& dm = P.dm;
+  const int G = gridDim.x;
+  const uint64_t pol = policy_evict_first();
+  prefetch_tensormap(&P.tmap_k);
+  prefetch_tensormap(&P.tmap_v);
+  Ring r;
+  r.issued = r.tail = r.head = 0;
+  bool ok = true;
+  // weights do not depend on the previous launch: stream before the dependency wait
+  if (P.first) ok = ok && load_dense(cx, r, P.w_qkv_pro, dm.d, dm.nqkv, P.phase_rot * 1, pol);
+  {
+    AttnUnit au = attn_unit(P, rot_block(cx.block, P.phase_rot * 2, G), P.is_global);
+    const uint32_t tb = (uint32_t)dm.attn_rows * dm.hd * 2 * 2;
+    for (int i = 0; ok && i < au.n_sub; ++i) ok = ring_issue_kv(cx, r, au.hk, au.r0 + i * dm.attn_rows, tb);
+  }
+  // the deadline of the bounded waits starts once the previous launch is done
+  pdl_wait();
+  cx.deadline = globaltimer() + (((uint64_t)P.timeout_ns_hi << 32) | P.timeout_ns_lo);
+  ok = ok && load_dense(cx, r, P.w_o, dm.hq * dm.hd, dm.d, P.phase_rot * 3, pol);
+  ok = ok && load_dense(cx, r, P.w_pool, dm.d, dm.p, P.phase_rot * 4, pol);
+  ok = ok && load_dense(cx, r, P.w_router, dm.p, dm.e, P.phase_rot * 5, pol);
+  // expert tiles wait for this block's routing decision
+  ok = ok && wait_bar(cx, cx.S.route_bar, 0, PH_ROUTE);
+  if (ok) {
+    const int na = *cx.S.n_active;
+    const int u1pe = dm.f / 8, u2pe = dm.p / 16;
+    const uint64_t ub1 = exp_unit_bytes(dm.p), ub2 = exp_unit_bytes(dm.f);
+    int lo, hi;
+    unit_range(na * u1pe, rot_block(cx.block, P.phase_rot * 6, G), G, lo, hi);
+    for (int gu = lo; ok && gu < hi; ++gu) {
+      int e = cx.S.act_e[gu / u1pe];
+      Seg sg = {P.w1 + ((uint64_t)e * u1pe + gu % u1pe) * ub1, (uint32_t)ub1};
+      ok = ring_issue(cx, r, &sg, 1, pol);
+    }
+    unit_range(na * u2pe, rot_block(cx.block, P.phase_rot * 7, G), G, lo, hi);
+    for (int gu = lo; ok && gu < hi; ++gu) {
+      int e = cx.S.act_e[gu / u2pe];
+      Seg sg = {P.w2 + ((uint64_t)e * u2pe + gu % u2pe) * ub2, (uint32_t)ub2};
+      ok = ring_issue(cx, r, &sg, 1, pol);
+    }
+  }
+  ok = ok && load_dense(cx, r, P.w_unpool, dm.p, dm.d, P.phase_rot * 8, pol);
+  if (!P.last) ok = ok && load_dense(cx, r, P.w_tail, dm.d, dm.nqkv, P.phase_rot * 9, pol);
+  else if (dm.vocab > 0) ok = ok && load_dense(cx, r, P.w_tail, dm.d, dm.vocab, P.phase_rot * 9, pol);
+  if (!ok) {
+    // give every copy still in flight a chance to land before the block exits
+    cx.deadline = globaltimer() + 20000000ull;
+    *cx.S.abort = 1;
+    for (uint32_t j = r.tail; j < r.issued; ++j) {
+      uint32_t s = j % kSlots, n = 0;
+      while (!mbar_try_wait(&cx.S.full[s], (j / kSlots) & 1)) {
+        if ((++n & 15) == 0 && globaltimer() > cx.deadline) break;
+      }
+    }
+  }
+  pdl_launch_dependents();
+}
+
+// ---------------------------------------------------------------------------
+// consumers
+// ---------------------------------------------------------------------------
+struct Worker {
+  Ctx* cx;
+  int cw, lane, g, q;
+  uint32_t ti;  // next tile index of the block's sequence
+  bool ok;
+};
+
+__device__ __forceinline__ void cbar() { named_bar(1, kComputeThreads); }
+
+// B-operand layout of a [16 tokens][K] activation: per 16-column k-step four 8x8
+// matrices (tokens 0-7 | k 0-7, tokens 0-7 | k 8-15, tokens 8-15 | k 0-7,
+// tokens 8-15 | k 8-15), 16 bytes per matrix row.
+__device__ __forceinline__ uint32_t act_off(int t, int k) {
+  return (uint32_t)(k >> 4) * kKStepBytes + (uint32_t)(((t >> 3) << 1) + ((k >> 3) & 1)) * 128u +
+         (uint32_t)(t & 7) * 16u;
+}
+
+// Stage a [16][K] bf16 activation from global memory into the B layout,
+// optionally polling its sentinels and applying RMSNorm with `gain`.
+__device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, const uint16_t* gain,
+                          float eps, int phase) {
+  Ctx& cx = *w.cx;
+  cbar();  // every compute warp is done with the act buffer
+  const int tid = w.cw * 32 + w.lane;
+  const int t = tid >> 4, sub = tid & 15;
+  const int nch = K / 8;
+  float ss = 0.f;
+  bool ok = w.ok;
+  for (int c = sub; c < nch && ok; c += 16) {
+    const uint16_t* p = src + (size_t)t * K + c * 8;
+    uint4 v;
+    if (poll) ok = poll_bf16x8(cx, p, v, phase);
+    else v = *reinterpret_cast<const uint4*>(p);
+    if (!ok) break;
+    uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float a = bf16_to_f32((uint16_t)(wd[i] & 0xFFFF)), b = bf16_to_f32((uint16_t)(wd[i] >> 16));
+      ss = fmaf(a, a, ss);
+      ss = fmaf(b, b, ss);
+    }
+    *reinterpret_cast<uint4*>(cx.S.act + act_off(t, c * 8)) = v;
+  }
+  ok = __all_sync(0xffffffffu, ok);
+  if (ok && gain != nullptr) {
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = rsqrtf(ss / (float)K + eps);
+    for (int c = sub; c < nch; c += 16) {
+      uint4* sp = reinterpret_cast<uint4*>(cx.S.act + act_off(t, c * 8));
+      uint4 v = *sp;
+      uint4 gv = *reinterpret_cast<const uint4*>(gain + c * 8);
+      uint32_t wd[4] = {v.x, v.y, v.z, v.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float a = bf16_to_f32((uint16_t)(wd[i] & 0xFFFF)) * inv * bf16_to_f32((uint16_t)(gw[i] & 0xFFFF));
+        float b = bf16_to_f32((uint16_t)(wd[i] >> 16)) * inv * bf16_to_f32((uint16_t)(gw[i] >> 16));
+        wd[i] = pack_bf16x2(a, b);
+      }
+      *sp = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    }
+  }
+  w.ok = ok;
+  cbar();
+  // all compute warps must agree (a failure anywhere aborts the block)
+  if (*cx.S.abort) w.ok = false;
+  return w.ok;
+}
+
+__device__ __forceinline__ uint32_t lane_mat_off(int lane) {
+  return (uint32_t)(lane >> 3) * 128u + (uint32_t)(lane & 7) * 16u;
+}
+
+// One 16-row dense unit: acc[nt][.] for tokens nt*8.. over the full K.
+template <class Epi>
+__device__ void dense_phase(Worker& w, const int K, const int N, const int rot, Epi&& epi) {
+  Ctx& cx = *w.cx;
+  const int G = gridDim.x;
+  int lo, hi;
+  unit_range(N / 16, rot_block(cx.block, rot, G), G, lo, hi);
+  const int steps = K / 16;
+  const int ktiles = (steps + kDenseTileSteps - 1) / kDenseTileSteps;
+  const uint32_t act_base = smem_u32(cx.S.act) + lane_mat_off(w.lane);
+  for (int loc = w.cw; loc < hi - lo; loc += kComputeWarps) {
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    for (int kt = 0; kt < ktiles; ++kt) {
+      const uint32_t t = w.ti + (uint32_t)(loc * ktiles + kt);
+      const uint32_t s = t % kSlots;
+      if (w.ok) w.ok = wait_bar(cx, &cx.S.full[s], (t / kSlots) & 1, 50);
+      if (!w.ok) break;
+      const uint32_t wbase = smem_u32(cx.S.ring + cx.S.slot_off[s]) + lane_mat_off(w.lane);
+      const int k0 = kt * kDenseTileSteps;
+      const int ns = min(kDenseTileSteps, steps - k0);
+#pragma unroll 4
+      for (int i = 0; i < ns; ++i) {
+        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+        ldsm_x4(wbase + i * kKStepBytes, a0, a1, a2, a3);
+        ldsm_x4(act_base + (k0 + i) * kKStepBytes, b0, b1, b2, b3);
+        mma_bf16(acc[0], a0, a1, a2, a3, b0, b1);
+        mma_bf16(acc[1], a0, a1, a2, a3, b2, b3);
+      }
+      __syncwarp();
+      if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps);
+    }
+    if (w.ok) epi(lo + loc, acc);
+  }
+  w.ti += (uint32_t)((hi - lo) * ktiles);
+}
+
+// ---------------------------------------------------------------------------
+// attention
+// ---------------------------------------------------------------------------
+// physical byte offset of (row, d) inside a tile loaded with the 128-byte swizzle
+// (two 64-column halves of `rows` rows each)
+__device__ __forceinline__ uint32_t swz(int row, int d, int rows) {
+  return (uint32_t)(d >> 6) * rows * 128u + (uint32_t)row * 128u + ((((d & 63) >> 3) ^ (row & 7)) << 4);
+}
+
+template <int D>
+struct AttnState {
+  float m[2], l[2];
+  float o[D / 8][4];
+};
+
+// process 16 keys [kb, kb+16) of a K/V tile for head fragments qa
+template <int D, class Vis>
+__device__ __forceinline__ void attn_keys16(AttnState<D>& st, const uint32_t (&qa)[D / 16][4],
+                                            uint32_t kbase, uint32_t vbase, int rows, int kb, int lane,
+                                            float scale_log2, Vis vis) {
+  float s[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[nt][i] = 0.f;
+  }
+  const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const int key = kb + nt * 8 + r8;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ks += 2) {
+      const int d0 = (ks + (mi >> 1)) * 16 + (mi & 1) * 8;
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kbase + swz(key, d0, rows), b0, b1, b2, b3);
+      mma_bf16(s[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+      mma_bf16(s[nt], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
+    }
+  }
+  const int g = lane >> 2, q = lane & 3;
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = g + ((i >> 1) << 3);     // token
+      const int key = kb + nt * 8 + 2 * q + (i & 1);
+      float v = vis(row, key) ? s[nt][i] * scale_log2 : -INFINITY;
+      s[nt][i] = v;
+      mx[i >> 1] = fmaxf(mx[i >> 1], v);
+    }
+  }
+  float alpha[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+    const float mnew = fmaxf(st.m[r], mx[r]);
+    const float muse = (mnew == -INFINITY) ? 0.f : mnew;
+    alpha[r] = exp2f(st.m[r] - muse);
+    st.m[r] = mnew;
+    mx[r] = muse;
+  }
+  float rs[2] = {0.f, 0.f};
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float p = exp2f(s[nt][i] - mx[i >> 1]);
+      s[nt][i] = p;
+      rs[i >> 1] += p;
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) st.l[r] = st.l[r] * alpha[r] + rs[r];
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) {
+    st.o[n][0] *= alpha[0];
+    st.o[n][1] *= alpha[0];
+    st.o[n][2] *= alpha[1];
+    st.o[n][3] *= alpha[1];
+  }
+  const uint32_t pa0 = pack_bf16x2(s[0][0], s[0][1]), pa1 = pack_bf16x2(s[0][2], s[0][3]);
+  const uint32_t pa2 = pack_bf16x2(s[1][0], s[1][1]), pa3 = pack_bf16x2(s[1][2], s[1][3]);
+#pragma unroll
+  for (int n = 0; n < D / 8; n += 2) {
+    const int key = kb + (mi & 1) * 8 + r8;
+    const int d0 = (n + (mi >> 1)) * 8;
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4_t(vbase + swz(key, d0, rows), b0, b1, b2, b3);
+    mma_bf16(st.o[n], pa0, pa1, pa2, pa3, b0, b1);
+    mma_bf16(st.o[n + 1], pa0, pa1, pa2, pa3, b2, b3);
+  }
+}
+
+template <int D>
+__device__ void attention_phase(Worker& w) {
+  Ctx& cx = *w.cx;
+  const LaunchParams& P = *cx.P;
+  const Dims& dm = P.dm;
+  const int G = gridDim.x;
+  const AttnUnit au = attn_unit(P, rot_block(cx.block, P.phase_rot * 2, G), P.is_global);
+  if (!au.valid) return;
+  const int group = dm.group, R = dm.attn_rows, NK = dm.attn_nk, WPH = dm.attn_wph;
+  // act buffer regions: Q fragments source, tree K/V, merge scratch
+  uint8_t* qsm = cx.S.act;
+  uint8_t* tk = qsm + group * (D / 16) * kKStepBytes;
+  uint8_t* tv = tk + 16 * D * 2;
+  float* scratch = reinterpret_cast<float*>(tv + 16 * D * 2);
+  const int tid = w.cw * 32 + w.lane;
+  // stage Q of this kv head's query heads (A operand layout)
+  {
+    const uint16_t* qsrc = P.first ? reinterpret_cast<const uint16_t*>(P.x_cur + P.xo.q0) : P.in_q;
+    const int nch = T * group * D / 8;
+    for (int c = tid; c < nch && w.ok; c += kComputeThreads) {
+      const int t = c / (group * D / 8), rem = c % (group * D / 8), j = rem / (D / 8), d = (rem % (D / 8)) * 8;
+      const uint16_t* p = qsrc + (size_t)t * dm.hq * D + (size_t)(au.hk * group + j) * D + d;
+      uint4 v;
+      if (P.first) w.ok = poll_bf16x8(cx, p, v, PH_ATTN);
+      else v = *reinterpret_cast<const uint4*>(p);
+      const int m = ((d >> 3) & 1) * 2 + (t >> 3);
+      *reinterpret_cast<uint4*>(qsm + j * (D / 16) * kKStepBytes + (d >> 4) * kKStepBytes + m * 128 + (t & 7) * 16) = v;
+    }
+    if (au.tree) {
+      for (int c = tid; c < 2 * 16 * D / 8 && w.ok; c += kComputeThreads) {
+        const int kv = c / (16 * D / 8), rem = c % (16 * D / 8), row = rem / (D / 8), d = (rem % (D / 8)) * 8;
+        uint4 v;
+        if (P.first) {
+          const uint16_t* p = reinterpret_cast<const uint16_t*>(P.x_cur + P.xo.tkv0) +
+                              (((size_t)kv * dm.hkv + au.hk) * 16 + row) * D + d;
+          w.ok = poll_bf16x8(cx, p, v, PH_ATTN);
+        } else {
+          const uint16_t* cache = kv ? P.vc : P.kc;
+          v = *reinterpret_cast<const uint4*>(cache + ((size_t)au.hk * dm.max_ctx + P.pos0 + row) * D + d);
+        }
+        *reinterpret_cast<uint4*>((kv ? tv : tk) + swz(row, d, 16)) = v;
+      }
+    }
+  }
+  w.ok = __all_sync(0xffffffffu, w.ok);
+  cbar();
+  if (*cx.S.abort) w.ok = false;
+  const int j = w.cw / WPH, part = w.cw % WPH;
+  const bool active = j < group;
+  uint32_t qa[D / 16][4];
+  AttnState<D> st;
+  st.m[0] = st.m[1] = -INFINITY;
+  st.l[0] = st.l[1] = 0.f;
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
+  if (active) {
+    const uint32_t qb = smem_u32(qsm) + j * (D / 16) * kKStepBytes + lane_mat_off(w.lane);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) ldsm_x4(qb + ks * kKStepBytes, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+  }
+  const float scale_log2 = 1.4426950408889634f * rsqrtf((float)D);
+  const int pos0 = P.pos0, window = dm.window, glob = P.is_global;
+  const int32_t* tpos = cx.S.tpos;
+  for (int i = 0; i < au.n_sub; ++i) {
+    const uint32_t t = w.ti + (uint32_t)i;
+    const uint32_t s = t % kSlots;
+    if (w.ok) w.ok = wait_bar(cx, &cx.S.full[s], (t / kSlots) & 1, PH_ATTN);
+    if (!w.ok) break;
+    if (active) {
+      const uint32_t kb_ = smem_u32(cx.S.ring + cx.S.slot_off[s]);
+      const uint32_t vb_ = kb_ + (uint32_t)R * D * 2;
+      const int row0 = au.r0 + i * R, r1 = au.r1;
+      auto vis = [&](int tok, int key) {
+        const int r = row0 + key;
+        return r < r1 && (glob || tpos[tok] - r < window);
+      };
+      for (int kb = part * NK; kb < (part + 1) * NK; kb += 16)
+        attn_keys16<D>(st, qa, kb_, vb_, R, kb, w.lane, scale_log2, vis);
+    }
+    __syncwarp();
+    if (w.lane == 0) mbar_arrive(&cx.S.empty[s], 1);
+  }
+  w.ti += (uint32_t)au.n_sub;
+  if (w.ok && active && au.tree && part == 0) {
+    const uint32_t* anc = cx.S.anc;
+    auto vis = [&](int tok, int key) { return ((anc[tok] >> key) & 1u) != 0u; };
+    attn_keys16<D>(st, qa, smem_u32(tk), smem_u32(tv), 16, 0, w.lane, scale_log2, vis);
+  }
+  (void)pos0;
+  // finish the row sums across the quad
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    st.l[r] += __shfl_xor_sync(0xffffffffu, st.l[r], 1);
+    st.l[r] += __shfl_xor_sync(0xffffffffu, st.l[r], 2);
+  }
+  // merge the WPH warps of each head through shared memory
+  const int g = w.g, q = w.q;
+  const int per_warp = 2 + 2 + D / 8 * 4;  // m[2], l[2], o
+  if (WPH > 1) {
+    if (active && part > 0) {
+      float* sc = scratch + ((size_t)(j * WPH + part) * 32 + w.lane) * per_warp;
+      sc[0] = st.m[0]; sc[1] = st.m[1]; sc[2] = st.l[0]; sc[3] = st.l[1];
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n)
+        for (int i = 0; i < 4; ++i) sc[4 + n * 4 + i] = st.o[n][i];
+    }
+    cbar();
+    if (active && part == 0) {
+      for (int pp = 1; pp < WPH; ++pp) {
+        const float* sc = scratch + ((size_t)(j * WPH + pp) * 32 + w.lane) * per_warp;
+        float al[2], be[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float mn = fmaxf(st.m[r], sc[r]);
+          const float mu = (mn == -INFINITY) ? 0.f : mn;
+          al[r] = exp2f(st.m[r] - mu);
+          be[r] = exp2f(sc[r] - mu);
+          st.m[r] = mn;
+          st.l[r] = st.l[r] * al[r] + sc[2 + r] * be[r];
+        }
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+          st.o[n][0] = st.o[n][0] * al[0] + sc[4 + n * 4 + 0] * be[0];
+          st.o[n][1] = st.o[n][1] * al[0] + sc[4 + n * 4 + 1] * be[0];
+          st.o[n][2] = st.o[n][2] * al[1] + sc[4 + n * 4 + 2] * be[1];
+          st.o[n][3] = st.o[n][3] * al[1] + sc[4 + n * 4 + 3] * be[1];
+        }
+      }
+    }
+  }
+  if (w.ok && active && part == 0) {
+    // partial of (kv head, split): acc [16][group][D], (m, l) [16][group] in log2 units
+    float* part_acc = reinterpret_cast<float*>(P.s_buf + P.so.part) +
+                      ((size_t)(au.hk * dm.splits + au.s) * T) * group * D;
+    float* part_ml = reinterpret_cast<float*>(P.s_buf + P.so.ml) + ((size_t)(au.hk * dm.splits + au.s) * T) * group * 2;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int tok = g + r * 8;
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        float* dst = part_acc + ((size_t)tok * group + j) * D + n * 8 + 2 * q;
+        uint2 v = make_uint2(__float_as_uint(f32_canon(st.o[n][2 * r])), __float_as_uint(f32_canon(st.o[n][2 * r + 1])));
+        asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%2};" ::"l"(dst), "r"(v.x), "r"(v.y) : "memory");
+      }
+      if (q == 0) {
+        float* dst = part_ml + ((size_t)tok * group + j) * 2;
+        asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%2};" ::"l"(dst), "r"(__float_as_uint(f32_canon(st.m[r]))),
+                     "r"(__float_as_uint(f32_canon(st.l[r])))
+                     : "memory");
+      }
+    }
+  }
+}
+
+// merge the split partials of every (token, q head): O = bf16(sum_s 2^(m_s-M) acc_s / L)
+template <int D>
+__device__ void attn_merge_phase(Worker& w) {
+  Ctx& cx = *w.cx;
+  const LaunchParams& P = *cx.P;
+  const Dims& dm = P.dm;
+  const int G = gridDim.x;
+  const int group = dm.group, S = dm.splits;
+  const int gw = rot_block(cx.block, P.phase_rot * 2, G) * kComputeWarps + w.cw;
+  constexpr int PER = D / 32;  // floats per lane
+  float* part_acc = reinterpret_cast<float*>(P.s_buf + P.so.part);
+  float* part_ml = reinterpret_cast<float*>(P.s_buf + P.so.ml);
+  uint16_t* o_out = reinterpret_cast<uint16_t*>(P.x_cur + P.xo.o);
+  for (int it = gw; it < T * dm.hq && w.ok; it += G * kComputeWarps) {
+    const int t = it / dm.hq, h = it % dm.hq, hk = h / group, j = h % group;
+    float M = -INFINITY;
+    for (int s = 0; s < S && w.ok; ++s) {
+      uint2 v;
+      w.ok = poll_f32x2(cx, part_ml + (((size_t)(hk * S + s) * T + t) * group + j) * 2, v, PH_ATTN_MERGE);
+      M = fmaxf(M, __uint_as_float(v.x));
+    }
+    w.ok = __all_sync(0xffffffffu, w.ok);
+    if (!w.ok) break;
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float acc[PER], L = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+    for (int s = 0; s < S && w.ok; ++s) {
+      float* mlp = part_ml + (((size_t)(hk * S + s) * T + t) * group + j) * 2;
+      uint2 mlv = ld_relaxed_v2(mlp);
+      const float ws = exp2f(__uint_as_float(mlv.x) - Mu);
+      L += ws * __uint_as_float(mlv.y);
+      float* ap = part_acc + (((size_t)(hk * S + s) * T + t) * group + j) * D + w.lane * PER;
+      if constexpr (PER == 4) {
+        uint4 v;
+        w.ok = poll_f32x4(cx, ap, v, PH_ATTN_MERGE);
+        acc[0] += ws * __uint_as_float(v.x);
+        acc[1] += ws * __uint_as_float(v.y);
+        acc[2 % PER] += ws * __uint_as_float(v.z);
+        acc[3 % PER] += ws * __uint_as_float(v.w);
+        st_relaxed_v4(ap, make_uint4(kF32Empty, kF32Empty, kF32Empty, kF32Empty));
+      } else {
+        uint2 v;
+        w.ok = poll_f32x2(cx, ap, v, PH_ATTN_MERGE);
+        acc[0] += ws * __uint_as_float(v.x);
+        acc[1 % PER] += ws * __uint_as_float(v.y);
+        asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%2};" ::"l"(ap), "r"(kF32Empty), "r"(kF32Empty) : "memory");
+      }
+    }
+    w.ok = __all_sync(0xffffffffu, w.ok);
+    if (!w.ok) break;
+    __syncwarp();
+    if (w.lane == 0)
+      for (int s = 0; s < S; ++s)
+        asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%2};" ::"l"(part_ml + (((size_t)(hk * S + s) * T + t) * group + j) * 2),
+                     "r"(kF32Empty), "r"(kF32Empty)
+                     : "memory");
+    const float inv = 1.f / L;
+    uint16_t* dst = o_out + (size_t)t * dm.hq * D + (size_t)h * D + w.lane * PER;
+    if constexpr (PER == 4) {
+      uint2 v = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2 % PER] * inv, acc[3 % PER] * inv));
+      asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%2};" ::"l"(dst), "r"(v.x), "r"(v.y) : "memory");
+    } else {
+      st_relaxed_u32(dst, pack_bf16x2(acc[0] * inv, acc[1 % PER] * inv));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// routing: top-k per token, expert dispatch, NVFP4 quantisation of the pooled
+// activations (orcarouter.ai, § "where the kernel boundary sits": top-8 of 256,
+// experts in NVFP4)
+// ---------------------------------------------------------------------------
+// quantise one row of n fp32 values (lane-parallel over 16-element blocks) into
+// f16 values e2m1 * e4m3-scale written by `put(block, j, f16x2 pair)`; returns the row scale
+template <class Get, class Put>
+__device__ __forceinline__ float nvfp4_row(int n, int lane, Get get, Put put) {
+  const int nb = n / 16;
+  float amax = 0.f;
+  for (int b = lane; b < nb; b += 32)
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(get(b * 16 + j)));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float ts = __fdiv_rn(amax, 2688.0f);
+  for (int b = lane; b < nb; b += 32) {
+    float bmax = 0.f;
+    for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(get(b * 16 + j)));
+    uint32_t sc = 0;
+    if (ts > 0.f) sc = f32_to_e4m3(__fdiv_rn(bmax, __fmul_rn(6.0f, ts)));
+    const float sv = e4m3_to_f32(sc);
+    const float denom = __fmul_rn(sv, ts);
+    const uint32_t s2 = e4m3x2_to_f16x2(sc | (sc << 8));
+    for (int j = 0; j < 16; j += 2) {
+      uint32_t code = 0;
+      if (sc != 0) code = f32x2_to_e2m1x2(__fdiv_rn(get(b * 16 + j), denom), __fdiv_rn(get(b * 16 + j + 1), denom));
+      put(b, j, hmul2(e2m1x2_to_f16x2(code), s2));
+    }
+  }
+  return ts;
+}
+
+__device__ void route_phase(Worker& w) {
+  Ctx& cx = *w.cx;
+  const LaunchParams& P = *cx.P;
+  const Dims& dm = P.dm;
+  const int E = dm.e, K = dm.k;
+  const float* logits = reinterpret_cast<const float*>(P.x_cur + P.xo.logits);
+  // top-k: warp cw takes tokens 2cw, 2cw+1
+  for (int tt = 0; tt < 2; ++tt) {
+    const int t = w.cw * 2 + tt;
+    float v[kMaxExperts / 32];
+    bool used[kMaxExperts / 32];
+    const int per = E / 32 + ((E % 32) ? 1 : 0);
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      v[i] = -INFINITY;
+      used[i] = true;
+      const int e = w.lane + 32 * i;
+      if (i < per && e < E && w.ok) {
+        uint32_t n = 0;
+        uint32_t bits = ld_relaxed_u32(logits + t * E + e);
+        while (bits == kF32Empty) {
+          if ((++n & 31) == 0 && cx.expired(PH_ROUTE)) { w.ok = false; break; }
+          bits = ld_relaxed_u32(logits + t * E + e);
+        }
+        v[i] = __uint_as_float(bits);
+        used[i] = false;
+      }
+    }
+    w.ok = __all_sync(0xffffffffu, w.ok);
+    if (!w.ok) break;
+    float sel_v[kMaxTopK];
+    for (int c = 0; c < K; ++c) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = w.lane + 32 * i;
+        if (!used[i] && (v[i] > bv || (v[i] == bv && e < bi))) { bv = v[i]; bi = e; }
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      if ((bi & 31) == w.lane) used[bi >> 5] = true;
+      sel_v[c] = bv;
+      if (w.lane == 0) cx.S.topk_idx[t * kMaxTopK + c] = bi;
+    }
+    if (w.lane == 0) {
+      float sum = 0.f, ex[kMaxTopK];
+      for (int c = 0; c < K; ++c) { ex[c] = expf(sel_v[c] - sel_v[0]); sum += ex[c]; }
+      for (int c = 0; c < K; ++c) cx.S.topk_w[t * kMaxTopK + c] = ex[c] / sum;
+    }
+  }
+  cbar();
+  if (*cx.S.abort) w.ok = false;
+  // dispatch: thread e counts its tokens, then a block-wide scan compacts the active experts
+  const int tid = w.cw * 32 + w.lane;
+  int cnt = 0;
+  if (tid < E)
+    for (int t = 0; t < T; ++t)
+      for (int c = 0; c < K; ++c) cnt += (cx.S.topk_idx[t * kMaxTopK + c] == tid);
+  const int act = cnt > 0;
+  int incl = act;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (w.lane >= o) incl += y;
+  }
+  float* red = cx.S.red;
+  if (w.lane == 31) reinterpret_cast<int*>(red)[w.cw] = incl;
+  cbar();
+  int base = 0;
+  for (int i = 0; i < w.cw; ++i) base += reinterpret_cast<int*>(red)[i];
+  const int rank = base + incl - act;
+  if (act) {
+    cx.S.act_e[rank] = (int16_t)tid;
+    cx.S.act_n[rank] = (uint8_t)cnt;
+    int n = 0;
+    for (int t = 0; t < T; ++t)
+      for (int c = 0; c < K; ++c)
+        if (cx.S.topk_idx[t * kMaxTopK + c] == tid) {
+          cx.S.act_tok[rank * 16 + n] = (uint8_t)t;
+          cx.S.act_slot[rank * 16 + n] = (uint8_t)(t * K + c);
+          ++n;
+        }
+  }
+  if (tid == kComputeThreads - 1) {
+    int tot = 0;
+    for (int i = 0; i < kComputeWarps; ++i) tot += reinterpret_cast<int*>(red)[i];
+    *cx.S.n_active = tot;
+  }
+  // routing record and expert usage (block 0)
+  if (cx.block == 0) {
+    if (tid < T * K) {
+      const int t = tid / K, c = tid % K;
+      P.routing_idx[tid] = cx.S.topk_idx[t * kMaxTopK + c];
+      P.routing_w[tid] = cx.S.topk_w[t * kMaxTopK + c];
+    }
+    if (tid < E) P.hist_cur[tid] = (uint32_t)cnt;
+    if (tid < T) {
+      P.tree_dbg[tid] = cx.S.anc[tid];
+      P.tree_dbg[16 + tid] = (uint32_t)cx.S.tpos[tid];
+    }
+  }
+  // NVFP4 activations of the pooled vectors (GEMM1 B operand, f16, one row per token)
+  const uint16_t* u = reinterpret_cast<const uint16_t*>(P.x_cur + P.xo.u);
+  for (int tt = 0; tt < 2 && w.ok; ++tt) {
+    const int t = w.cw * 2 + tt;
+    const uint16_t* row = u + (size_t)t * dm.p;
+    uint8_t* act = cx.S.act;
+    float ts = nvfp4_row(
+        dm.p, w.lane, [&](int i) { return bf16_to_f32(ld_relaxed_u16(row + i)); },
+        [&](int b, int j, uint32_t h2) {
+          const int k = b * 16 + j;
+          *reinterpret_cast<uint32_t*>(act + act_off(t, k) + (k & 7) * 2) = h2;
+        });
+    if (w.lane == 0) cx.S.x_ts[t] = ts;
+  }
+  cbar();
+  if (*cx.S.abort) w.ok = false;
+  if (tid == 0) mbar_arrive(cx.S.route_bar, 1);
+}
+
+// NVFP4 expert tile: A fragments of rows g and g+8 for one 16-column k-step,
+// weights dequantised e2m1 * e4m3 into f16 (exact)
+__device__ __forceinline__ void exp_frags(uint64_t cg, uint64_t cg8, uint32_t sg, uint32_t sg8, int ks,
+                                          uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+  const uint32_t lo_g = (uint32_t)(cg >> (ks * 16)) & 0xFFu, hi_g = (uint32_t)(cg >> (ks * 16 + 8)) & 0xFFu;
+  const uint32_t lo_8 = (uint32_t)(cg8 >> (ks * 16)) & 0xFFu, hi_8 = (uint32_t)(cg8 >> (ks * 16 + 8)) & 0xFFu;
+  const uint32_t s_g = (sg >> (ks * 8)) & 0xFFu, s_8 = (sg8 >> (ks * 8)) & 0xFFu;
+  const uint32_t f_g = e4m3x2_to_f16x2(s_g | (s_g << 8)), f_8 = e4m3x2_to_f16x2(s_8 | (s_8 << 8));
+  a0 = hmul2(e2m1x2_to_f16x2(lo_g), f_g);
+  a2 = hmul2(e2m1x2_to_f16x2(hi_g), f_g);
+  a1 = hmul2(e2m1x2_to_f16x2(lo_8), f_8);
+  a3 = hmul2(e2m1x2_to_f16x2(hi_8), f_8);
+}
+
+// acc[nt] += W_unit (16 rows x K, NVFP4 tile at tbase) * act rows (token list via rowof)
+template <class RowOf>
+__device__ __forceinline__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* tbase, int K, int ntiles,
+                                             uint32_t act_s, int lane, RowOf rowof) {
+  const int g = lane >> 2, q = lane & 3;
+  const int mi = lane >> 3, r8 = lane & 7;
+  const int ng = K / 64;
+  uint32_t bro[2];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const int t = rowof(nt * 8 + r8);
+    bro[nt] = act_s + (uint32_t)(((t >> 3) << 1) + (mi & 1)) * 128u + (uint32_t)(t & 7) * 16u;
+  }
+  for (int gi = 0; gi < ng; ++gi) {
+    const uint8_t* gb = tbase + gi * kExpGroupBytes;
+    const uint64_t cg = *reinterpret_cast<const uint64_t*>(gb + g * 32 + q * 8);
+    const uint64_t cg8 = *reinterpret_cast<const uint64_t*>(gb + (g + 8) * 32 + q * 8);
+    const uint32_t sg = *reinterpret_cast<const uint32_t*>(gb + 512 + g * 4);
+    const uint32_t sg8 = *reinterpret_cast<const uint32_t*>(gb + 512 + (g + 8) * 4);
+#pragma unroll
+    for (int kp = 0; kp < 4; kp += 2) {
+      uint32_t a[2][4];
+      exp_frags(cg, cg8, sg, sg8, kp, a[0][0], a[0][1], a[0][2], a[0][3]);
+      exp_frags(cg, cg8, sg, sg8, kp + 1, a[1][0], a[1][1], a[1][2], a[1][3]);
+      const uint32_t kstep = (uint32_t)(gi * 4 + kp + (mi >> 1)) * kKStepBytes;
+      for (int nt = 0; nt < ntiles; ++nt) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(bro[nt] + kstep, b0, b1, b2, b3);
+        mma_f16(acc[nt], a[0][0], a[0][1], a[0][2], a[0][3], b0, b1);
+        mma_f16(acc[nt], a[1][0], a[1][1], a[1][2], a[1][3], b2, b3);
+      }
+    }
+  }
+}
+
+__device__ void gemm1_phase(Worker& w) {
+  Ctx& cx = *w.cx;
+  const LaunchParams& P = *cx.P;
+  const Dims& dm = P.dm;
+  const int G = gridDim.x;
+  const int na = *cx.S.n_active, u1pe = dm.f / 8;
+  int lo, hi;
+  unit_range(na * u1pe, rot_block(cx.block, P.phase_rot * 6, G), G, lo, hi);
+  float* aout = reinterpret_cast<float*>(P.x_cur + P.xo.a);
+  const uint32_t act_s = smem_u32(cx.S.act);
+  for (int loc = w.cw; loc < hi - lo; loc += kComputeWarps) {
+    const int gu = lo + loc, a = gu / u1pe, jg = gu % u1pe;
+    const int e = cx.S.act_e[a], n = cx.S.act_n[a];
+    const uint8_t* toks = cx.S.act_tok + a * 16;
+    const uint32_t t = w.ti + (uint32_t)loc;
+    const uint32_t s = t % kSlots;
+    if (w.ok) w.ok = wait_bar(cx, &cx.S.full[s], (t / kSlots) & 1, PH_GEMM1);
+    if (!w.ok) break;
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    exp_unit_mma(acc, cx.S.ring + cx.S.slot_off[s], dm.p, n > 8 ? 2 : 1, act_s, w.lane,
+                 [&](int p) { return (int)toks[p < n ? p : 0]; });
+    __syncwarp();
+    if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps);
+    const float gs = P.w1_gs[e];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int ii = 0; ii < 2; ++ii) {
+        const int p = nt * 8 + 2 * w.q + ii;
+        if (p < n) {
+          const int tok = toks[p], slot = cx.S.act_slot[a * 16 + p];
+          const float sc = cx.S.x_ts[tok] * gs;
+          const float gate = acc[nt][ii] * sc, up = acc[nt][2 + ii] * sc;
+          const float av = gate / (1.0f + expf(-gate)) * up;
+          st_relaxed_u32(aout + (size_t)slot * dm.f + jg * 8 + w.g, __float_as_uint(f32_canon(av)));
+        }
+      }
+  }
+  w.ti += (uint32_t)(hi - lo);
+}
+
+__device__ void gemm2_phase(Worker& w) {
+  Ctx& cx = *w.cx;
+  const LaunchParams& P = *cx.P;
+  const Dims& dm = P.dm;
+  const int G = gridDim.x;
+  const int na = *cx.S.n_active, u2pe = dm.p / 16;
+  int lo, hi;
+  unit_range(na * u2pe, rot_block(cx.block, P.phase_rot * 7, G), G, lo, hi);
+  const float* ain = reinterpret_cast<const float*>(P.x_cur + P.xo.a);
+  uint16_t* yout = reinterpret_cast<uint16_t*>(P.s_buf + P.so.y);
+  const uint32_t act_s = smem_u32(cx.S.act);
+  if (hi > lo) {
+    const int a_first = lo / u2pe, a_last = (hi - 1) / u2pe;
+    for (int a = a_first; a <= a_last; ++a) {
+      const int e = cx.S.act_e[a], n = cx.S.act_n[a];
+      cbar();  // previous expert's units are done with the act buffer
+      if (*cx.S.abort) w.ok = false;
+      // stage this expert's NVFP4 activations: row p = p-th token of the expert
+      for (int p = w.cw; p < n && w.ok; p += kComputeWarps) {
+        const float* row = ain + (size_t)cx.S.act_slot[a * 16 + p] * dm.f;
+        // poll the whole row (each lane its own 16-byte chunks) before quantising
+        for (int c = w.lane; c < dm.f / 4 && w.ok; c += 32) {
+          uint4 v;
+          w.ok = poll_f32x4(cx, row + c * 4, v, PH_GEMM2);
+        }
+        w.ok = __all_sync(0xffffffffu, w.ok);
+        if (!w.ok) break;
+        uint8_t* act = cx.S.act;
+        float ts = nvfp4_row(
+            dm.f, w.lane, [&](int i) { return __uint_as_float(ld_relaxed_u32(row + i)); },
+            [&](int b, int j, uint32_t h2) {
+              const int k = b * 16 + j;
+              *reinterpret_cast<uint32_t*>(act + act_off(p, k) + (k & 7) * 2) = h2;
+            });
+        if (w.lane == 0) cx.S.a_ts[p] = ts;
+      }
+      w.ok = __all_sync(0xffffffffu, w.ok);
+      cbar();
+      if (*cx.S.abort) w.ok = false;
+      const int u_lo = max(lo, a * u2pe), u_hi = min(hi, (a + 1) * u2pe);
+      for (int gu = u_lo; gu < u_hi; ++gu) {
+        const int loc = gu - lo;
+        if (loc % kComputeWarps != w.cw) continue;
+        const int pr = gu % u2pe;
+        const uint32_t t = w.ti + (uint32_t)loc;
+        const uint32_t s = t % kSlots;
+        if (w.ok) w.ok = wait_bar(cx, &cx.S.full[s], (t / kSlots) & 1, PH_GEMM2);
+        if (!w.ok) break;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        exp_unit_mma(acc, cx.S.ring + cx.S.slot_off[s], dm.f, n > 8 ? 2 : 1, act_s, w.lane,
+                     [&](int p) { return p < n ? p : 0; });
+        __syncwarp();
+        if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps);
+        const float gs = P.w2_gs[e];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int ii = 0; ii < 2; ++ii) {
+            const int p = nt * 8 + 2 * w.q + ii;
+            if (p < n) {
+              const int slot = cx.S.act_slot[a * 16 + p];
+              const float sc = cx.S.a_ts[p] * gs;
+              st_relaxed_u16(yout + (size_t)slot * dm.p + pr * 16 + w.g, bf16_bits_rn(acc[nt][ii] * sc));
+              st_relaxed_u16(yout + (size_t)slot * dm.p + pr * 16 + w.g + 8, bf16_bits_rn(acc[nt][2 + ii] * sc));
+            }
+          }
+      }
+    }
+  }
+  w.ti += (uint32_t)(hi - lo);
+}
+
+// z[t] = bf16(sum_c w[t][c] * y[t*k + c]); each y element has this one consumer,
+// which re-arms it after reading
+__device__ void combine_phase(Worker& w) {
+  Ctx& cx = *w.cx;
+  const LaunchParams& P = *cx.P;
+  const Dims& dm = P.dm;
+  const int G = gridDim.x;
+  uint16_t* y = reinterpret_cast<uint16_t*>(P.s_buf + P.so.y);
+  uint16_t* z = reinterpret_cast<uint16_t*>(P.x_cur + P.xo.z);
+  const int nch = dm.p / 8;
+  const int gt = rot_block(cx.block, P.phase_rot * 10, G) * kComputeThreads + w.cw * 32 + w.lane;
+  for (int it = gt; it < T * nch && w.ok; it += G * kComputeThreads) {
+    const int t = it / nch, pc = it % nch;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int c = 0; c < dm.k; ++c) {
+      uint16_t* src = y + (size_t)(t * dm.k + c) * dm.p + pc * 8;
+      uint4 v;
+      if (!poll_bf16x8(cx, src, v, PH_COMBINE)) { w.ok = false; break; }
+      const float wt = cx.S.topk_w[t * kMaxTopK + c];
+      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] += wt * bf16_to_f32((uint16_t)(wd[i] & 0xFFFF));
+        acc[2 * i + 1] += wt * bf16_to_f32((uint16_t)(wd[i] >> 16));
+      }
+      st_relaxed_v4(src, make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu));
+    }
+    if (!w.ok) break;
+    st_relaxed_v4(z + (size_t)t * dm.p + pc * 8,
+                  make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                             pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+  }
+  w.ok = __all_sync(0xffffffffu, w.ok);
+}
+
+// rotary table [depth 0..15][hd/2] (cos, sin); angle in fp64, reduced to [-pi, pi]
+__device__ void rope_table(Worker& w) {
+  const LaunchParams& P = *w.cx->P;
+  const int half = P.dm.hd / 2;
+  const int tid = w.cw * 32 + w.lane;
+  for (int i = tid; i < 16 * half; i += kComputeThreads) {
+    const int dep = i / half, k = i % half;
+    double ang = (double)(P.pos0 + dep) * P.inv_freq[k];
+    const double two_pi = 6.283185307179586476925286766559;
+    ang = ang - two_pi * rint(ang / two_pi);
+    float s, c;
+    sincosf((float)ang, &s, &c);
+    P.rope[2 * i] = c;
+    P.rope[2 * i + 1] = s;
+  }
+}
+
+// QKV epilogue: RoPE pairs (d, d + hd/2) share a unit (rows g and g+8)
+struct QkvDst {
+  uint16_t* q;         // [16][hq*hd]
+  bool q_relaxed;
+  uint16_t* kc;        // caches of the layer whose rows are written
+  uint16_t* vc;
+  uint16_t* tkv;       // optional sentinel copy [2][hkv][16][hd]
+};
+
+__device__ __forceinline__ void qkv_epilogue(const LaunchParams& P, const Smem& S, const QkvDst& dst, int u,
+                                             const float (&acc)[2][4], int g, int q) {
+  const Dims& dm = P.dm;
+  const int D = dm.hd, upd = D / 16;
+  const int nQ = dm.hq * upd, nK = dm.hkv * upd;
+  const float* rope = P.rope;
+  if (u < nQ + nK) {
+    const bool isq = u < nQ;
+    const int hu = isq ? u : u - nQ, h = hu / upd, j = hu % upd;
+    const int dim = j * 8 + g;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int ii = 0; ii < 2; ++ii) {
+        const int t = nt * 8 + 2 * q + ii;
+        const float x = acc[nt][ii], y = acc[nt][2 + ii];
+        const float* cs = rope + ((size_t)S.depth[t] * (D / 2) + dim) * 2;
+        const float c = cs[0], s = cs[1];
+        const uint16_t xr = bf16_bits_rn(x * c - y * s), yr = bf16_bits_rn(y * c + x * s);
+        if (isq) {
+          uint16_t* p = dst.q + (size_t)t * dm.hq * D + (size_t)h * D + dim;
+          if (dst.q_relaxed) { st_relaxed_u16(p, xr); st_relaxed_u16(p + D / 2, yr); }
+          else { p[0] = xr; p[D / 2] = yr; }
+        } else {
+          uint16_t* p = dst.kc + ((size_t)h * dm.max_ctx + P.pos0 + t) * D + dim;
+          p[0] = xr;
+          p[D / 2] = yr;
+          if (dst.tkv) {
+            uint16_t* tp = dst.tkv + (((size_t)0 * dm.hkv + h) * 16 + t) * D + dim;
+            st_relaxed_u16(tp, xr);
+            st_relaxed_u16(tp + D / 2, yr);
+          }
+        }
+      }
+  } else {
+    const int hu = u - nQ - nK, h = hu / upd, j = hu % upd;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int ii = 0; ii < 2; ++ii) {
+        const int t = nt * 8 + 2 * q + ii;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int dim = j * 16 + g + half * 8;
+          const uint16_t v = bf16_bits_rn(acc[nt][half * 2 + ii]);
+          dst.vc[((size_t)h * dm.max_ctx + P.pos0 + t) * D + dim] = v;
+          if (dst.tkv) st_relaxed_u16(dst.tkv + (((size_t)1 * dm.hkv + h) * 16 + t) * D + dim, v);
+        }
+      }
+  }
+}
+
+// re-arm the exchange buffers of the other parity (warps 1-2)
+__device__ void rearm(const LaunchParams& P, int block, int tid, int nthreads) {
+  struct R { uint64_t off, bytes; uint32_t pat; };
+  const R regs[] = {
+      {P.xo.o, P.xo.h1 - P.xo.o, 0xFFFFFFFFu},   {P.xo.h1, P.xo.u - P.xo.h1, 0xFFFFFFFFu},
+      {P.xo.u, P.xo.logits - P.xo.u, 0xFFFFFFFFu}, {P.xo.logits, P.xo.a - P.xo.logits, kF32Empty},
+      {P.xo.a, P.xo.z - P.xo.a, kF32Empty},       {P.xo.z, P.xo.h2 - P.xo.z, 0xFFFFFFFFu},
+      {P.xo.h2, P.xo.q0 - P.xo.h2, 0xFFFFFFFFu},   {P.xo.q0, P.xo.tkv0 - P.xo.q0, 0xFFFFFFFFu},
+      {P.xo.tkv0, P.xo.total - P.xo.tkv0, 0xFFFFFFFFu}};
+  const int G = gridDim.x;
+  for (const R& r : regs) {
+    const uint64_t n16 = r.bytes / 16;
+    const uint64_t lo = n16 * block / G, hi = n16 * (block + 1) / G;
+    const uint4 v = make_uint4(r.pat, r.pat, r.pat, r.pat);
+    for (uint64_t i = lo + tid; i < hi; i += nthreads)
+      *reinterpret_cast<uint4*>(P.x_next + r.off + i * 16) = v;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the compute warps' sequence of one launch
+// ---------------------------------------------------------------------------
+template <bool kTiming>
+__device__ void compute_main(Worker& w) {
+  Ctx& cx = *w.cx;
+  const LaunchParams& P = *cx.P;
+  const Dims& dm = P.dm;
+  const int g = w.g, q = w.q;
+  const int b = blockIdx.x;
+  uint8_t* X = P.x_cur;
+  if (P.first) {
+    // the rotary table of this step's tree positions, then the prologue:
+    // RMSNorm(hidden_in) -> layer 0 QKV -> RoPE -> layer 0 KV rows and Q
+    rope_table(w);
+    stage_act(w, P.hidden_in, dm.d, false, P.g_attn_pro, dm.rms_eps, PH_PROLOGUE);
+    QkvDst dq{reinterpret_cast<uint16_t*>(X + P.xo.q0), true, P.kc, P.vc, reinterpret_cast<uint16_t*>(X + P.xo.tkv0)};
+    dense_phase(w, dm.d, dm.nqkv, P.phase_rot * 1,
+                [&](int u, const float(&acc)[2][4]) { qkv_epilogue(P, cx.S, dq, u, acc, g, q); });
+    stamp<kTiming>(P, b, PH_PROLOGUE);
+    cbar();
+  }
+  // a2: tree attention (split over blocks), a3: merge of the split partials
+  if (dm.hd == 128) attention_phase<128>(w);
+  else attention_phase<64>(w);
+  stamp<kTiming>(P, b, PH_ATTN);
+  if (dm.hd == 128) attn_merge_phase<128>(w);
+  else attn_merge_phase<64>(w);
+  stamp<kTiming>(P, b, PH_ATTN_MERGE);
+  // a4: h1 = bf16(h + bf16(O W_o^T))
+  {
+    const uint16_t* hprev = P.first ? P.hidden_in : P.in_h;
+    uint16_t* h1 = reinterpret_cast<uint16_t*>(X + P.xo.h1);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.o), dm.hq * dm.hd, true, nullptr, 0.f, PH_OPROJ);
+    dense_phase(w, dm.hq * dm.hd, dm.d, P.phase_rot * 3, [&](int u, const float(&acc)[2][4]) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int ii = 0; ii < 2; ++ii)
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int t = nt * 8 + 2 * q + ii, n = u * 16 + g + hf * 8;
+            const float o = bf16_to_f32(bf16_bits_rn(acc[nt][hf * 2 + ii]));
+            // test hook: the first element of the whole h1 exchange is never written
+            if ((P.flags & 0x10000u) && u == 0 && t == 0 && g == 0 && hf == 0) continue;
+            st_relaxed_u16(h1 + (size_t)t * dm.d + n, bf16_bits_rn(bf16_to_f32(hprev[(size_t)t * dm.d + n]) + o));
+          }
+    });
+    stamp<kTiming>(P, b, PH_OPROJ);
+  }
+  // a5: u = bf16(bf16(RMSNorm(h1)) W_pool^T)
+  {
+    uint16_t* uo = reinterpret_cast<uint16_t*>(X + P.xo.u);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h1), dm.d, true, P.g_moe, dm.rms_eps, PH_POOL);
+    dense_phase(w, dm.d, dm.p, P.phase_rot * 4, [&](int u, const float(&acc)[2][4]) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int ii = 0; ii < 2; ++ii)
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int t = nt * 8 + 2 * q + ii, n = u * 16 + g + hf * 8;
+            st_relaxed_u16(uo + (size_t)t * dm.p + n, bf16_bits_rn(acc[nt][hf * 2 + ii]));
+          }
+    });
+    stamp<kTiming>(P, b, PH_POOL);
+  }
+  // a6: router logits = u W_r^T + b (fp32)
+  {
+    float* lg = reinterpret_cast<float*>(X + P.xo.logits);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.u), dm.p, true, nullptr, 0.f, PH_ROUTER);
+    dense_phase(w, dm.p, dm.e, P.phase_rot * 5, [&](int u, const float(&acc)[2][4]) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int ii = 0; ii < 2; ++ii)
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int t = nt * 8 + 2 * q + ii, n = u * 16 + g + hf * 8;
+            st_relaxed_u32(lg + (size_t)t * dm.e + n, __float_as_uint(f32_canon(acc[nt][hf * 2 + ii] + P.b_router[n])));
+          }
+    });
+    stamp<kTiming>(P, b, PH_ROUTER);
+  }
+  // a6/a7/a8: top-k, dispatch, NVFP4 activations
+  cbar();
+  route_phase(w);
+  stamp<kTiming>(P, b, PH_ROUTE);
+  // a9, a10: the expert GEMMs
+  gemm1_phase(w);
+  stamp<kTiming>(P, b, PH_GEMM1);
+  gemm2_phase(w);
+  stamp<kTiming>(P, b, PH_GEMM2);
+  // move the next layer's KV history toward L2 while the combine waits
+  if ((P.flags & 0x4u) && !P.last && w.cw == 0 && w.lane == 0 && P.kc_pf != nullptr) {
+    const AttnUnit au = attn_unit(P, rot_block(b, P.phase_rot * 2, gridDim.x), P.next_global);
+    if (au.valid && au.r1 > au.r0) {
+      const size_t off = ((size_t)au.hk * dm.max_ctx + au.r0) * dm.hd;
+      const uint32_t bytes = (uint32_t)((au.r1 - au.r0) * dm.hd * 2);
+      prefetch_l2(P.kc_pf + off, bytes);
+      prefetch_l2(P.vc_pf + off, bytes);
+    }
+  }
+  // a11: combine, then h2 = bf16(h1 + bf16(z W_unp^T))
+  combine_phase(w);
+  stamp<kTiming>(P, b, PH_COMBINE);
+  {
+    const uint16_t* h1 = reinterpret_cast<const uint16_t*>(X + P.xo.h1);
+    uint16_t* h2 = reinterpret_cast<uint16_t*>(X + P.xo.h2);
+    uint16_t* hnext = P.last ? P.hidden_out : P.out_h;
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.z), dm.p, true, nullptr, 0.f, PH_UNPOOL);
+    dense_phase(w, dm.p, dm.d, P.phase_rot * 8, [&](int u, const float(&acc)[2][4]) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int ii = 0; ii < 2; ++ii)
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int t = nt * 8 + 2 * q + ii, n = u * 16 + g + hf * 8;
+            const float o = bf16_to_f32(bf16_bits_rn(acc[nt][hf * 2 + ii]));
+            const uint16_t v = bf16_bits_rn(bf16_to_f32(ld_relaxed_u16(h1 + (size_t)t * dm.d + n)) + o);
+            st_relaxed_u16(h2 + (size_t)t * dm.d + n, v);
+            if (hnext) hnext[(size_t)t * dm.d + n] = v;
+          }
+    });
+    stamp<kTiming>(P, b, PH_UNPOOL);
+  }
+  pdl_launch_dependents();
+  // a12: next layer's RMSNorm + QKV + RoPE + KV write; a12': final norm + LM head
+  if (!P.last) {
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h2), dm.d, true, P.g_tail, dm.rms_eps, PH_TAIL);
+    QkvDst dq{P.out_q, false, P.kc_next, P.vc_next, nullptr};
+    dense_phase(w, dm.d, dm.nqkv, P.phase_rot * 9,
+                [&](int u, const float(&acc)[2][4]) { qkv_epilogue(P, cx.S, dq, u, acc, g, q); });
+  } else if (dm.vocab > 0) {
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h2), dm.d, true, P.g_tail, dm.rms_eps, PH_TAIL);
+    dense_phase(w, dm.d, dm.vocab, P.phase_rot * 9, [&](int u, const float(&acc)[2][4]) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int ii = 0; ii < 2; ++ii)
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int t = nt * 8 + 2 * q + ii, n = u * 16 + g + hf * 8;
+            P.logits[(size_t)t * dm.vocab + n] = acc[nt][hf * 2 + ii];
+          }
+    });
+  }
+  stamp<kTiming>(P, b, PH_TAIL);
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <bool kTiming>
+__global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_constant__ LaunchParams P) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Ctx cx;
+  cx.P = &P;
+  cx.S = carve(smem, P);
+  cx.block = blockIdx.x;
+  cx.deadline = globaltimer() + (((uint64_t)P.timeout_ns_hi << 32) | P.timeout_ns_lo) + 1000000000ull;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&cx.S.full[i], 1);
+      mbar_init(&cx.S.empty[i], kComputeWarps);
+    }
+    mbar_init(cx.S.route_bar, 1);
+    *cx.S.abort = (smem_u32(smem) & 1023u) != 0u;  // the swizzled tiles need 1 KB alignment
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // a1: the tree (ancestor-or-self masks, depths, positions) from the parent array
+  if (warp == 1 && lane < T) {
+    uint32_t m = 0;
+    int dep = 0;
+    for (int j = lane; j >= 0; j = P.parent[j]) {
+      m |= 1u << j;
+      if (j != lane) ++dep;
+    }
+    cx.S.anc[lane] = m;
+    cx.S.depth[lane] = dep;
+    cx.S.tpos[lane] = P.pos0 + dep;
+  }
+  __syncthreads();
+  if (*cx.S.abort) {
+    if (threadIdx.x == 0 && atomicCAS(&P.status->code, 0, 2) == 0) P.status->phase = PH_START;
+    pdl_launch_dependents();
+    return;
+  }
+  if (warp == kLoaderWarp) {
+    if (lane == 0) loader<kTiming>(cx);
+    pdl_launch_dependents();
+    return;
+  }
+  if (warp == 1 || warp == 2) {
+    pdl_wait();
+    rearm(P, blockIdx.x, threadIdx.x - 32, 64);
+    pdl_launch_dependents();
+    return;
+  }
+  if (warp == kPrefetchWarp) {
+    pdl_wait();
+    if ((P.flags & 0x2u) && P.hist_prev != nullptr && P.prefetch_experts > 0) {
+      // the previous step's most-used experts of this layer -> L2 (block-strided slices)
+      const Dims& dm = P.dm;
+      const uint64_t ub1 = exp_unit_bytes(dm.p) * (dm.f / 8), ub2 = exp_unit_bytes(dm.f) * (dm.p / 16);
+      uint32_t taken[kMaxExperts / 32] = {0};
+      for (int c = 0; c < P.prefetch_experts && c < dm.e; ++c) {
+        uint32_t best = 0;
+        int bi = -1;
+        for (int e = lane; e < dm.e; e += 32) {
+          const uint32_t h = P.hist_prev[e];
+          if (!((taken[e >> 5] >> (e & 31)) & 1u) && h > 0 && (bi < 0 || h > best)) { best = h; bi = e; }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+          const uint32_t ob = __shfl_xor_sync(0xffffffffu, best, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (oi >= 0 && (bi < 0 || ob > best || (ob == best && oi < bi))) { best = ob; bi = oi; }
+        }
+        if (bi < 0) break;
+        taken[bi >> 5] |= 1u << (bi & 31);
+        const uint8_t* srcs[2] = {P.w1 + (uint64_t)bi * ub1, P.w2 + (uint64_t)bi * ub2};
+        const uint64_t sizes[2] = {ub1, ub2};
+        for (int m = 0; m < 2; ++m) {
+          const uint64_t chunk = 16384;
+          const uint64_t nck = (sizes[m] + chunk - 1) / chunk;
+          for (uint64_t ck = (uint64_t)blockIdx.x * 32 + lane; ck < nck; ck += (uint64_t)gridDim.x * 32) {
+            const uint64_t o = ck * chunk;
+            prefetch_l2(srcs[m] + o, (uint32_t)min(chunk, sizes[m] - o));
+          }
+        }
+      }
+    }
+    pdl_launch_dependents();
+    return;
+  }
+  // ---- compute warps ----
+  Worker w;
+  w.cx = &cx;
+  w.cw = warp - kFirstCompute;
+  w.lane = lane;
+  w.g = lane >> 2;
+  w.q = lane & 3;
+  w.ti = 0;
+  w.ok = true;
+  pdl_wait();
+  cx.deadline = globaltimer() + (((uint64_t)P.timeout_ns_hi << 32) | P.timeout_ns_lo);
+  stamp<kTiming>(P, blockIdx.x, PH_START);
+  compute_main<kTiming>(w);
+  stamp<kTiming>(P, blockIdx.x, PH_END);
+}
+
+const void* layer_kernel(bool timing) {
+  return timing ? reinterpret_cast<const void*>(&msm_layer_kernel<true>)
+                : reinterpret_cast<const void*>(&msm_layer_kernel<false>);
+}
+
+}  // namespace msm

@@ -261,3 +261,17 @@ def parity_seeds(name: str) -> dict:
         if name in s:
             return s[name]
     return {"seed": 1, "bias_seeds": None}
+
+
+# --------------------------------------------------------------------------
+# device upload (torch is used for device memory only)
+# --------------------------------------------------------------------------
+def to_torch(arrs: dict, device="cuda"):
+    """numpy dict -> torch tensors on `device` (bf16 bit patterns travel as int16)."""
+    import torch
+    out = {}
+    for k, a in arrs.items():
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        out[k] = torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return out
