@@ -48,6 +48,7 @@ struct Smem {
   float* x_ts;        // [16]
   float* a_ts;        // [16]
   float* red;         // [8][16]
+  volatile uint32_t* slot_tile;  // [kSlots] index of the tile the loader last put in each slot
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* base, const LaunchParams& P) {
@@ -73,6 +74,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const LaunchParams& P) {
   s.x_ts = reinterpret_cast<float*>(sm + 5952);
   s.a_ts = reinterpret_cast<float*>(sm + 6016);
   s.red = reinterpret_cast<float*>(sm + 6080);
+  s.slot_tile = reinterpret_cast<volatile uint32_t*>(sm + 6592);
   return s;
 }
 
@@ -115,6 +117,19 @@ __device__ __forceinline__ bool wait_bar(Ctx& cx, uint64_t* bar, uint32_t parity
     if ((++n & 15) == 0 && cx.expired(phase)) return false;
   }
   return true;
+}
+
+// Wait until tile t of the block's sequence has landed.  A slot's mbarrier only
+// tells phases apart by parity, so a consumer first waits until the loader has
+// put tile t in its slot (the slot then cannot move on before t is released) and
+// only then tests the parity of t's phase.
+__device__ __forceinline__ bool wait_tile(Ctx& cx, uint32_t t, int phase) {
+  const uint32_t s = t % kSlots;
+  uint32_t n = 0;
+  while (cx.S.slot_tile[s] != t) {
+    if ((++n & 15) == 0 && cx.expired(phase)) return false;
+  }
+  return wait_bar(cx, &cx.S.full[s], (t / kSlots) & 1, phase);
 }
 
 // poll a 16-byte bf16 chunk until none of its 8 elements is the sentinel
@@ -227,6 +242,7 @@ __device__ bool ring_issue(Ctx& cx, Ring& r, const Seg* seg, int nseg, uint64_t 
   r.off[s] = off;
   r.end[s] = off + total;
   cx.S.slot_off[s] = off;
+  cx.S.slot_tile[s] = r.issued;
   mbar_expect_tx(&cx.S.full[s], total);
   uint32_t o = off;
   for (int i = 0; i < nseg; ++i) {
@@ -245,6 +261,7 @@ __device__ bool ring_issue_kv(Ctx& cx, Ring& r, int hk, int row, uint32_t tile_b
   r.off[s] = off;
   r.end[s] = off + tile_bytes;
   cx.S.slot_off[s] = off;
+  cx.S.slot_tile[s] = r.issued;
   mbar_expect_tx(&cx.S.full[s], tile_bytes);
   const int R = P.dm.attn_rows;
   const int halves = P.dm.hd / 64;
@@ -427,7 +444,7 @@ __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, 
     for (int kt = 0; kt < ktiles; ++kt) {
       const uint32_t t = w.ti + (uint32_t)(loc * ktiles + kt);
       const uint32_t s = t % kSlots;
-      if (w.ok) w.ok = wait_bar(cx, &cx.S.full[s], (t / kSlots) & 1, 50);
+      if (w.ok) w.ok = wait_tile(cx, t, 50);
       if (!w.ok) break;
       const uint32_t wbase = smem_u32(cx.S.ring + cx.S.slot_off[s]) + lane_mat_off(w.lane);
       const int k0 = kt * kDenseTileSteps;
@@ -609,7 +626,7 @@ __device__ void attention_phase(Worker& w) {
   for (int i = 0; i < au.n_sub; ++i) {
     const uint32_t t = w.ti + (uint32_t)i;
     const uint32_t s = t % kSlots;
-    if (w.ok) w.ok = wait_bar(cx, &cx.S.full[s], (t / kSlots) & 1, PH_ATTN);
+    if (w.ok) w.ok = wait_tile(cx, t, PH_ATTN);
     if (!w.ok) break;
     if (active) {
       const uint32_t kb_ = smem_u32(cx.S.ring + cx.S.slot_off[s]);
@@ -986,7 +1003,7 @@ __device__ void gemm1_phase(Worker& w) {
     const uint8_t* toks = cx.S.act_tok + a * 16;
     const uint32_t t = w.ti + (uint32_t)loc;
     const uint32_t s = t % kSlots;
-    if (w.ok) w.ok = wait_bar(cx, &cx.S.full[s], (t / kSlots) & 1, PH_GEMM1);
+    if (w.ok) w.ok = wait_tile(cx, t, PH_GEMM1);
     if (!w.ok) break;
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     exp_unit_mma(acc, cx.S.ring + cx.S.slot_off[s], dm.p, n > 8 ? 2 : 1, act_s, w.lane,
@@ -1057,7 +1074,7 @@ __device__ void gemm2_phase(Worker& w) {
         const int pr = gu % u2pe;
         const uint32_t t = w.ti + (uint32_t)loc;
         const uint32_t s = t % kSlots;
-        if (w.ok) w.ok = wait_bar(cx, &cx.S.full[s], (t / kSlots) & 1, PH_GEMM2);
+        if (w.ok) w.ok = wait_tile(cx, t, PH_GEMM2);
         if (!w.ok) break;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         exp_unit_mma(acc, cx.S.ring + cx.S.slot_off[s], dm.f, n > 8 ? 2 : 1, act_s, w.lane,
@@ -1384,6 +1401,7 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
       mbar_init(&cx.S.empty[i], kComputeWarps);
     }
     mbar_init(cx.S.route_bar, 1);
+    for (int i = 0; i < kSlots; ++i) cx.S.slot_tile[i] = 0xFFFFFFFFu;
     *cx.S.abort = (smem_u32(smem) & 1023u) != 0u;  // the swizzled tiles need 1 KB alignment
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }

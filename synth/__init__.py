@@ -44,7 +44,8 @@ def build(force: bool = False) -> str:
     os.makedirs(_BUILD, exist_ok=True)
     out = os.path.join(_BUILD, "libsynth.so")
     src = os.path.join(_HERE, "synth.c")
-    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+    hdr = os.path.join(_HERE, "synth_defs.h")
+    if force or not os.path.exists(out) or os.path.getmtime(out) < max(os.path.getmtime(src), os.path.getmtime(hdr)):
         tmp = out + ".tmp%d" % os.getpid()
         subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
                                "-std=c11", src, "-o", tmp, "-lm"])
@@ -275,3 +276,107 @@ def to_torch(arrs: dict, device="cuda"):
             a = a.view(np.int16)
         out[k] = torch.from_numpy(np.ascontiguousarray(a)).to(device)
     return out
+
+
+# --------------------------------------------------------------------------
+# device-side draws (same definitions, bit-identical; for the full-size stack)
+# --------------------------------------------------------------------------
+_GLIB = None
+
+
+def build_gpu(force: bool = False) -> str:
+    """Compile synth_gpu.cu into _build/libsynth_gpu.so (nvcc, sm_103a, no FMA contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    out = os.path.join(_BUILD, "libsynth_gpu.so")
+    srcs = [os.path.join(_HERE, "synth_gpu.cu"), os.path.join(_HERE, "synth_defs.h")]
+    if force or not os.path.exists(out) or os.path.getmtime(out) < max(os.path.getmtime(s) for s in srcs):
+        tmp = out + ".tmp%d" % os.getpid()
+        nvcc = "/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else "nvcc"
+        subprocess.check_call([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-fmad=false",
+                               "-Xcompiler", "-fPIC", "-shared", "-cudart", "static", srcs[0], "-o", tmp])
+        os.replace(tmp, out)
+    return out
+
+
+def glib():
+    global _GLIB
+    with _LOCK:
+        if _GLIB is None:
+            L = ctypes.CDLL(build_gpu())
+            u64, dbl, vp, i64 = ctypes.c_uint64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int64
+            for fn in (L.synth_gpu_normal_bf16, L.synth_gpu_normal_f32):
+                fn.argtypes = [u64, u64, u64, dbl, dbl, vp, vp]
+                fn.restype = ctypes.c_int
+            L.synth_gpu_nvfp4_experts.argtypes = [u64, u64, ctypes.c_int, i64, i64, dbl, vp, vp, vp, vp, vp]
+            L.synth_gpu_nvfp4_experts.restype = ctypes.c_int
+            _GLIB = L
+    return _GLIB
+
+
+def _gchk(rc):
+    if rc != 0:
+        raise RuntimeError("device generator failed: cuda error %d" % rc)
+
+
+def _cur_stream(t):
+    import torch
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def gpu_normal_bf16(seed, strm, shape, mean=0.0, std=1.0, device="cuda"):
+    import torch
+    t = torch.empty(shape, dtype=torch.int16, device=device)
+    _gchk(glib().synth_gpu_normal_bf16(seed, strm, t.numel(), mean, std, t.data_ptr(), _cur_stream(t)))
+    return t
+
+
+def gpu_nvfp4_experts(seed, kind, layer, E, rows, cols, std, device="cuda"):
+    import torch
+    codes = torch.empty((E, rows, cols // 2), dtype=torch.uint8, device=device)
+    sf = torch.empty((E, rows, cols // 16), dtype=torch.uint8, device=device)
+    gs = torch.empty(E, dtype=torch.float32, device=device)
+    scratch = torch.empty(E, dtype=torch.int32, device=device)
+    _gchk(glib().synth_gpu_nvfp4_experts(seed, stream(kind, layer, 0), E, rows, cols, std, codes.data_ptr(),
+                                         sf.data_ptr(), gs.data_ptr(), scratch.data_ptr(), _cur_stream(codes)))
+    return codes, sf, gs
+
+
+def gpu_layer_weights(cfg: Config, seed: int, layer: int, bias_seed: int | None = None, device="cuda") -> dict:
+    """layer_weights() drawn directly into device memory (torch tensors)."""
+    import torch
+    d, p, f, e = cfg.d, cfg.p, cfg.f, cfg.e
+    rstd = cfg.router_std if cfg.router_std > 0 else 1.0 / np.sqrt(d)
+    w = {
+        "w_qkv": gpu_normal_bf16(seed, stream(K_QKV, layer), (cfg.nqkv, d), 0, 0.02, device),
+        "w_o": gpu_normal_bf16(seed, stream(K_O, layer), (d, cfg.hq * cfg.hd), 0, 0.02, device),
+        "w_pool": gpu_normal_bf16(seed, stream(K_POOL, layer), (p, d), 0, 0.02, device),
+        "w_router": gpu_normal_bf16(seed, stream(K_ROUTER, layer), (e, p), 0, rstd, device),
+        "b_router": torch.from_numpy(router_bias(cfg, seed if bias_seed is None else bias_seed, layer)).to(device),
+        "w_unpool": gpu_normal_bf16(seed, stream(K_UNPOOL, layer), (d, p), 0, 0.02, device),
+        "norm_attn": gpu_normal_bf16(seed, stream(K_NORM_ATTN, layer), (d,), 1.0, 0.02, device),
+        "norm_moe": gpu_normal_bf16(seed, stream(K_NORM_MOE, layer), (d,), 1.0, 0.02, device),
+    }
+    w["w1_codes"], w["w1_sf"], w["w1_gs"] = gpu_nvfp4_experts(seed, K_W1, layer, e, 2 * f, p, 0.02, device)
+    w["w2_codes"], w["w2_sf"], w["w2_gs"] = gpu_nvfp4_experts(seed, K_W2, layer, e, p, f, 0.02, device)
+    return w
+
+
+def gpu_final_weights(cfg: Config, seed: int, device="cuda") -> dict:
+    if cfg.vocab <= 0:
+        return {}
+    return {"norm_final": gpu_normal_bf16(seed, stream(K_NORM_FINAL), (cfg.d,), 1.0, 0.02, device),
+            "w_lm": gpu_normal_bf16(seed, stream(K_LM), (cfg.vocab, cfg.d), 0, 0.02, device)}
+
+
+def gpu_kv_history(cfg: Config, seed: int, layer: int, device="cuda"):
+    import torch
+    out = []
+    for kind in (K_KCACHE, K_VCACHE):
+        c = torch.zeros((cfg.hkv, cfg.max_ctx, cfg.hd), dtype=torch.int16, device=device)
+        for h in range(cfg.hkv):
+            if cfg.history:
+                view = c[h, :cfg.history]
+                _gchk(glib().synth_gpu_normal_bf16(seed, stream(kind, layer, h), view.numel(), 0.0, 1.0,
+                                                   view.data_ptr(), _cur_stream(c)))
+        out.append(c)
+    return out[0], out[1]

@@ -25,31 +25,10 @@
 #include <stdlib.h>
 #include <string.h>
 
-#define PHILOX_M0 0xD2511F53u
-#define PHILOX_M1 0xCD9E8D57u
-#define PHILOX_W0 0x9E3779B9u
-#define PHILOX_W1 0xBB67AE85u
+#include "synth_defs.h"
 
-static void philox4x32_10(uint32_t ctr[4], uint32_t k0, uint32_t k1, uint32_t out[4]) {
-  uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
-  for (int r = 0; r < 10; ++r) {
-    uint64_t p0 = (uint64_t)PHILOX_M0 * c0;
-    uint64_t p1 = (uint64_t)PHILOX_M1 * c2;
-    uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
-    uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
-    uint32_t n0 = hi1 ^ c1 ^ k0;
-    uint32_t n2 = hi0 ^ c3 ^ k1;
-    c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
-    k0 += PHILOX_W0; k1 += PHILOX_W1;
-  }
-  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
-}
-
-/* Four 32-bit words for (seed, stream, block). */
 static void draw_block(uint64_t seed, uint64_t stream, uint64_t block, uint32_t out[4]) {
-  uint32_t ctr[4] = {(uint32_t)block, (uint32_t)(block >> 32), (uint32_t)stream,
-                     (uint32_t)(stream >> 32)};
-  philox4x32_10(ctr, (uint32_t)seed, (uint32_t)(seed >> 32), out);
+  synth_draw(seed, stream, block, out);
 }
 
 /* Public: raw words, for tests of the generator itself. */
@@ -63,60 +42,26 @@ uint64_t synth_stream(int kind, int layer, int expert, int part) {
          ((uint64_t)(uint16_t)expert << 16) | (uint64_t)(uint16_t)part;
 }
 
-/* Unit-variance Irwin-Hall(8) deviate for element i of the stream. */
-static double unit_normal(uint64_t seed, uint64_t stream, uint64_t i) {
-  uint32_t w[4];
-  draw_block(seed, stream, i, w);
-  int64_t s = 0;
-  for (int j = 0; j < 4; ++j) s += (int64_t)(w[j] & 0xFFFFu) + (int64_t)(w[j] >> 16);
-  /* uniforms u = (j + 1/2) / 65536; sum of eight has mean 4 and variance 8/12 */
-  int64_t centred2 = 2 * s + 8 - 8 * 65536; /* = 2 * 65536 * (sum - 4) */
-  const double k = 1.2247448713915890 / 131072.0; /* sqrt(12/8) / (2 * 65536) */
-  return (double)centred2 * k;
-}
-
-/* Round-to-nearest-even of a double to bf16 bits (no double rounding via fp32). */
-static uint16_t bf16_bits_rne(double x) {
-  uint16_t sign = signbit(x) ? 0x8000u : 0u;
-  double a = fabs(x);
-  if (isnan(x)) return 0x7FC0u;
-  if (a == 0.0) return sign;
-  int e;
-  double m = frexp(a, &e); /* a = m * 2^e, m in [0.5, 1) */
-  double q;
-  if (e - 1 < -126) {
-    /* subnormal bf16: quantum 2^-133 */
-    q = nearbyint(ldexp(a, 133));
-    q = ldexp(q, -133);
-  } else {
-    double r = nearbyint(ldexp(m, 8)); /* 8 significant bits */
-    q = ldexp(r, e - 8);
-  }
-  if (q > 3.3895313892515355e38) return sign | 0x7F80u; /* overflow to inf */
-  float f = (float)q; /* exact */
-  uint32_t bits;
-  memcpy(&bits, &f, 4);
-  return sign | (uint16_t)((bits >> 16) & 0x7FFFu);
-}
+static uint16_t bf16_bits_rne(double x) { return synth_bf16_rne(x); }
 
 void synth_normal_f64(uint64_t seed, uint64_t stream, uint64_t n, double mean, double std,
                       double* out) {
 #pragma omp parallel for schedule(static)
-  for (int64_t i = 0; i < (int64_t)n; ++i) out[i] = mean + std * unit_normal(seed, stream, (uint64_t)i);
+  for (int64_t i = 0; i < (int64_t)n; ++i) out[i] = synth_value(seed, stream, (uint64_t)i, mean, std);
 }
 
 void synth_normal_f32(uint64_t seed, uint64_t stream, uint64_t n, double mean, double std,
                       float* out) {
 #pragma omp parallel for schedule(static)
   for (int64_t i = 0; i < (int64_t)n; ++i)
-    out[i] = (float)(mean + std * unit_normal(seed, stream, (uint64_t)i));
+    out[i] = (float)synth_value(seed, stream, (uint64_t)i, mean, std);
 }
 
 void synth_normal_bf16(uint64_t seed, uint64_t stream, uint64_t n, double mean, double std,
                        uint16_t* out) {
 #pragma omp parallel for schedule(static)
   for (int64_t i = 0; i < (int64_t)n; ++i)
-    out[i] = bf16_bits_rne(mean + std * unit_normal(seed, stream, (uint64_t)i));
+    out[i] = bf16_bits_rne(synth_value(seed, stream, (uint64_t)i, mean, std));
 }
 
 /* ---- NVFP4 encoding of synthetic weights (input preparation) ----------------
@@ -127,49 +72,9 @@ void synth_normal_bf16(uint64_t seed, uint64_t stream, uint64_t n, double mean, 
  *   block scale  s  = E4M3_rne(amax_block / (6 * ts))           (fp32 in)
  *   code         c  = E2M1_rne(x / (decode(s) * ts)), 0 if s == 0
  */
-static const float kE2M1[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
-
-static uint8_t e2m1_rne(float v) {
-  uint8_t sign = signbit(v) ? 8u : 0u;
-  float a = fabsf(v);
-  if (!(a < 6.0f)) return sign | 7u; /* saturate (and NaN -> max, never occurs) */
-  /* find the bracketing grid points and round to nearest, ties to even code */
-  int lo = 0;
-  for (int c = 7; c >= 0; --c)
-    if (kE2M1[c] <= a) { lo = c; break; }
-  if (lo == 7) return sign | 7u;
-  float dl = a - kE2M1[lo], dh = kE2M1[lo + 1] - a;
-  int c;
-  if (dl < dh) c = lo;
-  else if (dh < dl) c = lo + 1;
-  else c = (lo % 2 == 0) ? lo : lo + 1;
-  return sign | (uint8_t)c;
-}
-
-static float e4m3_value(uint8_t code) {
-  int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
-  float v;
-  if (e == 0) v = ldexpf((float)m, -9);
-  else v = ldexpf(1.0f + (float)m / 8.0f, e - 7);
-  return s ? -v : v;
-}
-
-static uint8_t e4m3_rne_nonneg(float v) {
-  if (!(v > 0.0f)) return 0;
-  if (v >= 448.0f) return 0x7E; /* satfinite */
-  if (v < 0.015625f) {        /* below 2^-6: subnormal, step 2^-9 */
-    float m = nearbyintf(ldexpf(v, 9));
-    return (uint8_t)m;           /* m == 8 is exactly the smallest normal's code */
-  }
-  int e;
-  float f = frexpf(v, &e);        /* v = f * 2^e, f in [0.5, 1) */
-  int E = e - 1;                  /* v = 1.xxx * 2^E */
-  float r = nearbyintf(ldexpf(f, 4)); /* 16 * f in [8, 16] */
-  if (r == 16.0f) { r = 8.0f; E += 1; }
-  int code = ((E + 7) << 3) | ((int)r - 8);
-  if (code > 0x7E) code = 0x7E;
-  return (uint8_t)code;
-}
+#define e2m1_rne synth_e2m1_rne
+#define e4m3_value synth_e4m3_value
+#define e4m3_rne_nonneg synth_e4m3_rne
 
 /* Encode rows x cols fp32 values (cols % 16 == 0). codes: rows*cols/2 bytes, low
  * nibble = even column.  sf: rows*cols/16 E4M3 bytes.  Returns the tensor scale. */
