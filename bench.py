@@ -1,0 +1,430 @@
+"""Benchmark of the verify step (one step = the whole 62-layer verification of a
+16-token tree, one persistent launch per layer, LM head in the last launch).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg4|cfg2|cfg3]
+    python bench.py --impl reference ...     # the CPU oracle arm, on the host cores
+
+Prints one JSON line.  Inputs are seeded synthetic tensors of the workload's
+shapes (weights drawn on the device by synth's device generator); every step
+streams ~20 GB of weights, far more than the 126 MB L2, so no explicit L2 flush
+is needed between timed steps.  With N > 1 (torchrun) every rank runs an
+independent replica on its own GPU: the verify step does not shard (replicas
+only, weak scaling) and there is no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+T = 16
+METRIC = "verify-step ms (16-token tree); us/layer and HBM GB/s reported alongside"
+
+
+# ----------------------------------------------------------------- byte accounting
+def layer_bytes(cfg, layer, n_distinct, pos0):
+    """Algorithmic bytes one layer launch must move: weights touched + KV read + KV write."""
+    d, p, f, e = cfg.d, cfg.p, cfg.f, cfg.e
+    dense = 2 * (cfg.nqkv * d + d * cfg.hq * cfg.hd + p * d + e * p + d * p) + 4 * e
+    w1 = 2 * f * p // 2 + 2 * f * p // 16 + 4
+    w2 = p * f // 2 + p * f // 16 + 4
+    experts = n_distinct * (w1 + w2)
+    lo = 0 if cfg.is_global(layer) else max(0, pos0 - cfg.window + 1)
+    kv_read = (pos0 - lo + T) * cfg.hkv * cfg.hd * 2 * 2
+    kv_write = T * cfg.hkv * cfg.hd * 2 * 2
+    return dense + experts + kv_read + kv_write
+
+
+def step_bytes(cfg, distinct_per_layer, pos0):
+    tot = sum(layer_bytes(cfg, l, distinct_per_layer[l], pos0) for l in range(cfg.n_layers))
+    if cfg.vocab:
+        tot += cfg.vocab * cfg.d * 2 + T * cfg.vocab * 4
+    return tot
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            pk = json.load(fh)
+        return float(pk["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------- ranks
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank number over all ranks (the slowest replica sets the step time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- CPU oracle
+def bias_seed_of(bias, seed, l):
+    return bias[l] if bias and l < len(bias) else seed
+
+
+def host_layer_weights(cfg, seed, bias, l):
+    """One layer's weights as host numpy arrays: drawn on the device and copied back when
+    a GPU is present (bit-identical to the host generator, and seconds instead of a minute)."""
+    bs = bias_seed_of(bias, seed, l)
+    try:
+        import torch
+        if torch.cuda.is_available():
+            w = synth.gpu_layer_weights(cfg, seed, l, bias_seed=bs, device=torch.device("cuda", 0))
+            out = {}
+            for k, t in w.items():
+                a = t.cpu().numpy()
+                out[k] = a.view(np.uint16) if a.dtype == np.int16 else a
+            return out
+    except ImportError:
+        pass
+    return synth.layer_weights(cfg, seed, l, bias_seed=bs)
+
+
+def sample_layers(cfg):
+    """One sliding-window and one global layer of the workload (whichever exist)."""
+    swa = next((l for l in range(cfg.n_layers) if not cfg.is_global(l)), None)
+    glb = next((l for l in range(cfg.n_layers) if cfg.is_global(l)), None)
+    return [l for l in (swa, glb) if l is not None]
+
+
+def oracle_step_ms(cfg, seed, bias, min_seconds=10.0, max_seconds=30.0):
+    """Time the oracle on a bounded sample of one step -- the sample layers, evaluated
+    repeatedly for about min_seconds, and one eighth of the LM head -- and extrapolate
+    to the whole step (46 sliding-window + 16 global layers + LM head)."""
+    import oracle
+    parent = synth.parent_array(seed)
+    h = synth.hidden_in(cfg, seed)
+    layers = sample_layers(cfg)
+    wts = {l: host_layer_weights(cfg, seed, bias, l) for l in layers}
+    kv = {l: synth.kv_history(cfg, seed, l) for l in layers}
+    times = {l: [] for l in layers}
+    t_start = time.perf_counter()
+    i = 0
+    while True:
+        l = layers[i % len(layers)]
+        k, v = kv[l][0].copy(), kv[l][1].copy()
+        t0 = time.perf_counter()
+        oracle.layer(cfg, wts[l], cfg.is_global(l), h, parent, cfg.pos0, k, v)
+        times[l].append(time.perf_counter() - t0)
+        i += 1
+        el = time.perf_counter() - t_start
+        if (el >= min_seconds and i >= len(layers)) or el >= max_seconds:
+            break
+    lm_s = 0.0
+    if cfg.vocab:
+        import dataclasses
+        c8 = dataclasses.replace(cfg, vocab=cfg.vocab // 8)
+        fw = synth.final_weights(c8, seed)
+        t0 = time.perf_counter()
+        oracle.lm_head(c8, fw["norm_final"], fw["w_lm"], h)
+        lm_s = (time.perf_counter() - t0) * 8
+    n_glob = sum(1 for l in range(cfg.n_layers) if cfg.is_global(l))
+    mean = {l: statistics.mean(v) for l, v in times.items()}
+    t_swa = next((mean[l] for l in layers if not cfg.is_global(l)), None)
+    t_glb = next((mean[l] for l in layers if cfg.is_global(l)), None)
+    t_swa = t_glb if t_swa is None else t_swa
+    t_glb = t_swa if t_glb is None else t_glb
+    step_ms = ((cfg.n_layers - n_glob) * t_swa + n_glob * t_glb + lm_s) * 1e3
+    sample = ("CPU oracle (fp64) on %d host threads: %d evaluations of layers %s of this workload (%.1f s) "
+              "plus 1/8 of the LM head, extrapolated to %d layers + LM head"
+              % (oracle.num_threads(), i, layers, sum(sum(v) for v in times.values()), cfg.n_layers))
+    return step_ms, sample, oracle.num_threads()
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, on the host cores, on a bounded sample of
+    the same workload per step (rank 0 only)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    cfg = synth.CONFIGS[args.workload]
+    seeds = synth.parity_seeds(args.workload)
+    seed, bias = seeds["seed"], seeds["bias_seeds"]
+    parent = synth.parent_array(seed)
+    h = synth.hidden_in(cfg, seed)
+    layers = sample_layers(cfg)
+    wts = {l: host_layer_weights(cfg, seed, bias, l) for l in layers}
+    kv = {l: synth.kv_history(cfg, seed, l) for l in layers}
+    per = {l: [] for l in layers}
+    for i in range(args.warmup + args.steps):
+        l = layers[i % len(layers)]
+        k, v = kv[l][0].copy(), kv[l][1].copy()
+        t0 = time.perf_counter()
+        oracle.layer(cfg, wts[l], cfg.is_global(l), h, parent, cfg.pos0, k, v)
+        if i >= args.warmup:
+            per[l].append(time.perf_counter() - t0)
+    n_glob = sum(1 for l in range(cfg.n_layers) if cfg.is_global(l))
+    mean = {l: statistics.mean(v) for l, v in per.items() if v}
+    t_any = statistics.mean(mean.values())
+    t_swa = next((mean[l] for l in mean if not cfg.is_global(l)), t_any)
+    t_glb = next((mean[l] for l in mean if cfg.is_global(l)), t_any)
+    step_ms = ((cfg.n_layers - n_glob) * t_swa + n_glob * t_glb) * 1e3
+    sample = ("each step: one decoder layer of this workload on the CPU oracle (alternating sliding-window and "
+              "global layers), extrapolated to %d layers; LM head not included" % cfg.n_layers)
+    line = {"impl": "reference", "metric": METRIC, "value": step_ms, "unit": "ms", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "parallelism": "replicas"},
+            "cpu_baseline": {"kind": "oracle", "cores": oracle.num_threads(), "sample": sample,
+                             "value": step_ms, "unit": "ms"},
+            "e2e": {"value": step_ms, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------- our arm
+def build_model(cfg, seed, bias, dev, local, flags):
+    import torch
+    import moe_decode_megakernel_warp_gb300 as msm
+    layers = [synth.gpu_layer_weights(cfg, seed, l, bias_seed=bias_seed_of(bias, seed, l), device=dev)
+              for l in range(cfg.n_layers)]
+    final = synth.gpu_final_weights(cfg, seed, device=dev)
+    torch.cuda.synchronize()
+    model = msm.Model(cfg, layers, final, device=local, flags=flags)
+    del layers, final
+    torch.cuda.empty_cache()
+    return model
+
+
+def run_ours(args):
+    import torch
+    import moe_decode_megakernel_warp_gb300 as msm
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = synth.CONFIGS[args.workload]
+    seeds = synth.parity_seeds(args.workload)
+    seed, bias = seeds["seed"], seeds["bias_seeds"]
+    flags = msm.MSM_FLAG_PDL | (msm.MSM_FLAG_EXPERT_PREFETCH if args.expert_prefetch else 0) | (
+        msm.MSM_FLAG_KV_PREFETCH if args.kv_prefetch else 0)
+
+    t_setup = time.time()
+    model = build_model(cfg, seed, bias, dev, local, flags)
+    kv = [synth.gpu_kv_history(cfg, seed, l, device=dev) for l in range(cfg.n_layers)]
+    kc, vc = [k for k, _ in kv], [v for _, v in kv]
+    hidden = torch.from_numpy(synth.hidden_in(cfg, seed).view(np.int16)).to(dev)
+    parent = synth.parent_array(seed)
+    logits = torch.empty((T, cfg.vocab), dtype=torch.float32, device=dev) if cfg.vocab else None
+    hout = torch.empty((T, cfg.d), dtype=torch.int16, device=dev)
+    setup_s = time.time() - t_setup
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    def step(m):
+        m.verify_step(hidden, parent, cfg.pos0, kc, vc, logits_out=logits, hidden_out=hout, stream=sptr)
+
+    for _ in range(args.warmup):
+        step(model)
+    if model.sync(sptr) != 0:
+        raise SystemExit("warm-up step failed: %s" % msm.msm_last_error())
+
+    # ---- timed region: device time from CUDA events on the launching stream
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.4)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    barrier(world)
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step(model)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    if model.sync(sptr) != 0:
+        raise SystemExit("timed steps failed: %s" % msm.msm_last_error())
+    per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    ms_step = max_over_ranks(ev[0].elapsed_time(ev[args.steps]) / args.steps, world, dev)
+
+    # ---- algorithmic bytes from the step's routing
+    idx, _ = model.routing()
+    distinct = [len(np.unique(idx[l])) for l in range(cfg.n_layers)]
+    bytes_step = step_bytes(cfg, distinct, cfg.pos0)
+    peak, peak_kind = measured_peaks()
+    achieved = bytes_step / (ms_step * 1e-3) / 1e9
+    n_launch = model.stats().launches_per_step
+
+    # ---- end to end through the host-buffer entry point (copies inside the timed region)
+    h_host = torch.from_numpy(synth.hidden_in(cfg, seed).view(np.int16)).pin_memory().numpy()
+    lg_host = torch.empty((T, max(cfg.vocab, 1)), dtype=torch.float32).pin_memory().numpy()
+    ho_host = torch.empty((T, cfg.d), dtype=torch.int16).pin_memory().numpy()
+
+    def step_host():
+        return model.verify_step_host(h_host, parent, cfg.pos0, kc, vc,
+                                      logits_host=lg_host if cfg.vocab else None,
+                                      hidden_out_host=None if cfg.vocab else ho_host, stream=sptr)
+    for _ in range(2):
+        step_host()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        if step_host() != 0:
+            raise SystemExit("host-buffer step failed: %s" % msm.msm_last_error())
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.steps, world, dev)
+    model.close()
+
+    # ---- per-layer times from the kernel's own %globaltimer stamps (separate, untimed model)
+    us_layer = lm_us = None
+    if not args.no_self_timing:
+        tm_model = build_model(cfg, seed, bias, dev, local, flags | msm.MSM_FLAG_SELF_TIMING)
+        for _ in range(3):
+            step(tm_model)
+        tm_model.sync(sptr)
+        tm = tm_model.timing().astype(np.int64)  # [L][G][events]
+        tm_model.close()
+        spans = (tm[:, :, 13].max(axis=1) - tm[:, :, 0].min(axis=1)) / 1e3
+        if cfg.vocab:
+            lm_us = float((tm[-1, :, 12].max() - tm[-1, :, 11].max()) / 1e3)
+            spans[-1] -= lm_us
+        us_layer = float(np.mean(spans))
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_ms, sample, cores = oracle_step_ms(cfg, seed, bias)
+        cpu = {"value": cpu_ms, "unit": "ms", "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": ms_step, "unit": "ms", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "ms_per_step_median": statistics.median(per_step),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4+bf16",
+            "data": "synthetic (seeded; weights drawn on the device)",
+            "config": {"workload": cfg.name, "layers": cfg.n_layers, "tree_tokens": T, "pos0": cfg.pos0,
+                       "window": cfg.window, "experts": cfg.e, "top_k": cfg.k, "vocab": cfg.vocab,
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": "not flushed: every step streams %.2f GB (> 126 MB L2)" % (bytes_step / 1e9),
+                       "flags": flags},
+            "us_per_layer": us_layer, "lm_head_us": lm_us, "launches_per_step": n_launch,
+            "gpu_launches": n_launch * args.steps, "hbm_gbs": achieved, "hbm_frac_of_8tbs": achieved / 8000.0,
+            "distinct_experts_per_layer": {"mean": float(np.mean(distinct)), "min": int(min(distinct)),
+                                           "max": int(max(distinct))},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": args.traffic,
+                         "peak_kind": peak_kind,
+                         "note": "algorithmic bytes per step / device time of the step's %d launches of the "
+                                 "layer kernel (the only kernel in the step)" % n_launch},
+            "algorithmic_bytes_per_step": bytes_step,
+            "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": T * cfg.d * 2,
+                    "d2h_bytes_per_step": T * cfg.vocab * 4 if cfg.vocab else T * cfg.d * 2},
+            "clocks": clk, "setup_seconds": setup_s,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="cfg4", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--expert-prefetch", action="store_true")
+    ap.add_argument("--kv-prefetch", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-self-timing", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch from an ncu capture of the current kernel (reported as is)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
