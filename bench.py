@@ -360,9 +360,10 @@ def run_ours(args):
         tm_model.sync(sptr)
         tm = tm_model.timing().astype(np.int64)  # [L][G][events]
         tm_model.close()
-        spans = (tm[:, :, 13].max(axis=1) - tm[:, :, 0].min(axis=1)) / 1e3
+        ev = msm.EV
+        spans = (tm[:, :, ev["end"]].max(axis=1) - tm[:, :, ev["start"]].min(axis=1)) / 1e3
         if cfg.vocab:
-            lm_us = float((tm[-1, :, 12].max() - tm[-1, :, 11].max()) / 1e3)
+            lm_us = float((tm[-1, :, ev["tail_done"]].max() - tm[-1, :, ev["unpool_done"]].max()) / 1e3)
             spans[-1] -= lm_us
         us_layer = float(np.mean(spans))
 

@@ -203,9 +203,16 @@ msm_status msm_get_routing(msm_model* model, int32_t* idx, float* w);
 msm_status msm_get_tree(msm_model* model, uint32_t* anc, int32_t* tpos);
 
 /* Self-timing stamps of the last step (MSM_FLAG_SELF_TIMING):
- * uint64 [n_layers][grid_blocks][MSM_TIMING_EVENTS] %globaltimer values (ns).
+ * uint64 [n_layers][grid_blocks][MSM_TIMING_EVENTS] %globaltimer values (ns), 0
+ * where an event did not occur.  Event ids (per block of a launch; "_IN" = the
+ * phase's input has been received and staged):
+ *   0 start, 1 prologue in, 2 prologue done, 3 attention in, 4 attention done,
+ *   5 split merge done, 6 o_proj in, 7 o_proj done, 8 pooler in, 9 pooler done,
+ *   10 router in, 11 router done, 12 top-k done, 13 routing done, 14 GEMM1 done,
+ *   15 GEMM2 in, 16 GEMM2 done, 17 combine done, 18 unpooler in, 19 unpooler done,
+ *   20 tail in, 21 tail done, 22 end, 23 loader saw the routing, 24 loader done.
  * `n` is the capacity of `buf` in elements. */
-#define MSM_TIMING_EVENTS 16
+#define MSM_TIMING_EVENTS 32
 msm_status msm_get_timing(msm_model* model, uint64_t* buf, size_t n);
 
 msm_status msm_get_stats(const msm_model* model, msm_stats* out);

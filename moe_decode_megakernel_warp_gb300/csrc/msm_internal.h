@@ -17,13 +17,22 @@ constexpr int kSlots = 12;            // descriptors of the variable-size ring
 constexpr int kDenseTileSteps = 32;   // 16-row x 512-column bf16 tiles: 32 k-steps x 512 B
 constexpr int kKStepBytes = 512;      // one 16x16 bf16 (or f16) block in ldmatrix order
 constexpr int kExpGroupBytes = 576;   // 16 rows x 64 columns NVFP4: 512 B codes + 64 B scales
-constexpr int kSmallBytes = 8 * 1024; // barriers, routing tables, scratch
+constexpr int kSmallBytes = 16 * 1024; // barriers, routing tables, scratch, dense partials
 constexpr int kMaxSmem = 232448;      // 227 KB opt-in dynamic shared memory per block
-constexpr int kTimingEvents = 16;
+constexpr int kTimingEvents = 32;
 constexpr int kMaxTopK = 8;
 constexpr int kMaxExperts = 256;
 
-// phases of one layer launch (also the self-timing event ids)
+// self-timing events of one launch (per block): *_IN = the phase's input is staged
+enum TimingEvent : int {
+  EV_START = 0, EV_PRO_IN = 1, EV_PRO_DONE = 2, EV_ATTN_IN = 3, EV_ATTN_DONE = 4, EV_MERGE_DONE = 5,
+  EV_OPROJ_IN = 6, EV_OPROJ_DONE = 7, EV_POOL_IN = 8, EV_POOL_DONE = 9, EV_ROUTER_IN = 10, EV_ROUTER_DONE = 11,
+  EV_ROUTE_TOPK = 12, EV_ROUTE_DONE = 13, EV_GEMM1_DONE = 14, EV_GEMM2_IN = 15, EV_GEMM2_DONE = 16,
+  EV_COMBINE_DONE = 17, EV_UNPOOL_IN = 18, EV_UNPOOL_DONE = 19, EV_TAIL_IN = 20, EV_TAIL_DONE = 21, EV_END = 22,
+  EV_LOADER_ROUTED = 23, EV_LOADER_END = 24
+};
+
+// phases of one layer launch (recorded in the status word on a timeout)
 enum Phase : int {
   PH_START = 0, PH_PROLOGUE = 1, PH_ATTN = 2, PH_ATTN_MERGE = 3, PH_OPROJ = 4, PH_POOL = 5,
   PH_ROUTER = 6, PH_ROUTE = 7, PH_GEMM1 = 8, PH_GEMM2 = 9, PH_COMBINE = 10, PH_UNPOOL = 11,

@@ -49,6 +49,7 @@ struct Smem {
   float* a_ts;        // [16]
   float* red;         // [8][16]
   volatile uint32_t* slot_tile;  // [kSlots] index of the tile the loader last put in each slot
+  float* dred;        // [8][16][16] dense-phase cross-warp partial sums
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* base, const LaunchParams& P) {
@@ -75,6 +76,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const LaunchParams& P) {
   s.a_ts = reinterpret_cast<float*>(sm + 6016);
   s.red = reinterpret_cast<float*>(sm + 6080);
   s.slot_tile = reinterpret_cast<volatile uint32_t*>(sm + 6592);
+  s.dred = reinterpret_cast<float*>(sm + 8192);
   return s;
 }
 
@@ -161,9 +163,17 @@ __device__ __forceinline__ bool poll_f32x2(Ctx& cx, const void* p, uint2& v, int
   return true;
 }
 
+// one thread per block records: the first compute thread, or the loader lane
 template <bool kTiming>
 __device__ __forceinline__ void stamp(const LaunchParams& P, int block, int ev) {
-  if (kTiming) P.timing[(size_t)block * kTimingEvents + ev] = globaltimer();
+  if (kTiming && (threadIdx.x == kFirstCompute * 32 || threadIdx.x == 0))
+    P.timing[(size_t)block * kTimingEvents + ev] = globaltimer();
+}
+
+// sub-phase stamps inside helpers shared by both kernel variants (runtime flag)
+__device__ __forceinline__ void stamp_rt(const LaunchParams& P, int ev) {
+  if ((P.flags & 0x1u) && threadIdx.x == kFirstCompute * 32)
+    P.timing[(size_t)blockIdx.x * kTimingEvents + ev] = globaltimer();
 }
 
 // ---------------------------------------------------------------------------
@@ -318,6 +328,7 @@ __device__ void loader(Ctx& cx) {
   ok = ok && load_dense(cx, r, P.w_router, dm.p, dm.e, P.phase_rot * 5, pol);
   // expert tiles wait for this block's routing decision
   ok = ok && wait_bar(cx, cx.S.route_bar, 0, PH_ROUTE);
+  stamp<kTiming>(P, cx.block, EV_LOADER_ROUTED);
   if (ok) {
     const int na = *cx.S.n_active;
     const int u1pe = dm.f / 8, u2pe = dm.p / 16;
@@ -339,6 +350,7 @@ __device__ void loader(Ctx& cx) {
   ok = ok && load_dense(cx, r, P.w_unpool, dm.p, dm.d, P.phase_rot * 8, pol);
   if (!P.last) ok = ok && load_dense(cx, r, P.w_tail, dm.d, dm.nqkv, P.phase_rot * 9, pol);
   else if (dm.vocab > 0) ok = ok && load_dense(cx, r, P.w_tail, dm.d, dm.vocab, P.phase_rot * 9, pol);
+  stamp<kTiming>(P, cx.block, EV_LOADER_END);
   if (!ok) {
     // give every copy still in flight a chance to land before the block exits
     cx.deadline = globaltimer() + 20000000ull;
@@ -384,20 +396,33 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, cons
   const int nch = K / 8;
   float ss = 0.f;
   bool ok = w.ok;
-  for (int c = sub; c < nch && ok; c += 16) {
-    const uint16_t* p = src + (size_t)t * K + c * 8;
-    uint4 v;
-    if (poll) ok = poll_bf16x8(cx, p, v, phase);
-    else v = *reinterpret_cast<const uint4*>(p);
-    if (!ok) break;
-    uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+  // loads are issued in batches of 8 before any is inspected, so their latencies overlap
+  constexpr int kB = 8;
+  for (int c0 = sub; c0 < nch && ok; c0 += 16 * kB) {
+    uint4 v[kB];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float a = bf16_to_f32((uint16_t)(wd[i] & 0xFFFF)), b = bf16_to_f32((uint16_t)(wd[i] >> 16));
-      ss = fmaf(a, a, ss);
-      ss = fmaf(b, b, ss);
+    for (int j = 0; j < kB; ++j) {
+      const int c = c0 + 16 * j;
+      if (c < nch) {
+        const uint16_t* p = src + (size_t)t * K + c * 8;
+        v[j] = poll ? ld_relaxed_v4(p) : *reinterpret_cast<const uint4*>(p);
+      }
     }
-    *reinterpret_cast<uint4*>(cx.S.act + act_off(t, c * 8)) = v;
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int c = c0 + 16 * j;
+      if (c >= nch || !ok) continue;
+      if (poll && !bf16x8_ready(v[j])) ok = poll_bf16x8(cx, src + (size_t)t * K + c * 8, v[j], phase);
+      if (!ok) continue;
+      const uint32_t wd[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = bf16_to_f32((uint16_t)(wd[i] & 0xFFFF)), b = bf16_to_f32((uint16_t)(wd[i] >> 16));
+        ss = fmaf(a, a, ss);
+        ss = fmaf(b, b, ss);
+      }
+      *reinterpret_cast<uint4*>(cx.S.act + act_off(t, c * 8)) = v[j];
+    }
   }
   ok = __all_sync(0xffffffffu, ok);
   if (ok && gain != nullptr) {
@@ -429,7 +454,12 @@ __device__ __forceinline__ uint32_t lane_mat_off(int lane) {
   return (uint32_t)(lane >> 3) * 128u + (uint32_t)(lane & 7) * 16u;
 }
 
-// One 16-row dense unit: acc[nt][.] for tokens nt*8.. over the full K.
+// Dense phase: out[16 tokens][N] = act[16][K] . W[N][K]^T over this block's
+// 16-row units.  Every tile (32 k-steps of one unit) is shared by the 8 compute
+// warps, warp w taking k-steps 4w..4w+3, so no warp carries a long dependent
+// MMA chain; each unit ends with a cross-warp sum in fixed warp order (the result
+// does not depend on the grid size) and an epilogue over (row pair, token):
+// epi(unit, p, t, row p value, row p+8 value), run by 128 threads.
 template <class Epi>
 __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, Epi&& epi) {
   Ctx& cx = *w.cx;
@@ -439,28 +469,53 @@ __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, 
   const int steps = K / 16;
   const int ktiles = (steps + kDenseTileSteps - 1) / kDenseTileSteps;
   const uint32_t act_base = smem_u32(cx.S.act) + lane_mat_off(w.lane);
-  for (int loc = w.cw; loc < hi - lo; loc += kComputeWarps) {
+  float* red = cx.S.dred;  // [8 warps][16 rows][16 tokens]
+  const int tid = w.cw * 32 + w.lane;
+  const int ks_lo = w.cw * (kDenseTileSteps / kComputeWarps);
+  for (int u = lo; u < hi; ++u) {
+    const int loc = u - lo;
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     for (int kt = 0; kt < ktiles; ++kt) {
       const uint32_t t = w.ti + (uint32_t)(loc * ktiles + kt);
       const uint32_t s = t % kSlots;
       if (w.ok) w.ok = wait_tile(cx, t, 50);
-      if (!w.ok) break;
-      const uint32_t wbase = smem_u32(cx.S.ring + cx.S.slot_off[s]) + lane_mat_off(w.lane);
-      const int k0 = kt * kDenseTileSteps;
-      const int ns = min(kDenseTileSteps, steps - k0);
-#pragma unroll 4
-      for (int i = 0; i < ns; ++i) {
-        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-        ldsm_x4(wbase + i * kKStepBytes, a0, a1, a2, a3);
-        ldsm_x4(act_base + (k0 + i) * kKStepBytes, b0, b1, b2, b3);
-        mma_bf16(acc[0], a0, a1, a2, a3, b0, b1);
-        mma_bf16(acc[1], a0, a1, a2, a3, b2, b3);
+      if (w.ok) {
+        const uint32_t wbase = smem_u32(cx.S.ring + cx.S.slot_off[s]) + lane_mat_off(w.lane);
+        const int k0 = kt * kDenseTileSteps;
+        const int ns = min(kDenseTileSteps, steps - k0);
+        const int ke = min(ns, ks_lo + kDenseTileSteps / kComputeWarps);
+        for (int i = ks_lo; i < ke; ++i) {
+          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+          ldsm_x4(wbase + i * kKStepBytes, a0, a1, a2, a3);
+          ldsm_x4(act_base + (k0 + i) * kKStepBytes, b0, b1, b2, b3);
+          mma_bf16(acc[0], a0, a1, a2, a3, b0, b1);
+          mma_bf16(acc[1], a0, a1, a2, a3, b2, b3);
+        }
+        __syncwarp();
+        if (w.lane == 0) mbar_arrive(&cx.S.empty[s], 1);
       }
-      __syncwarp();
-      if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps);
     }
-    if (w.ok) epi(lo + loc, acc);
+    // partials -> shared memory: rows g / g+8, tokens nt*8 + 2q (+1)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = w.g + ((i >> 1) << 3), tok = nt * 8 + 2 * w.q + (i & 1);
+        red[(w.cw * 16 + row) * 16 + tok] = acc[nt][i];
+      }
+    cbar();
+    if (tid < 128 && w.ok) {
+      const int p = tid >> 4, tok = tid & 15;
+      float vlo = 0.f, vhi = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < kComputeWarps; ++ww) {
+        vlo += red[(ww * 16 + p) * 16 + tok];
+        vhi += red[(ww * 16 + p + 8) * 16 + tok];
+      }
+      epi(u, p, tok, vlo, vhi);
+    }
+    cbar();
+    if (*cx.S.abort) w.ok = false;
   }
   w.ti += (uint32_t)((hi - lo) * ktiles);
 }
@@ -547,16 +602,25 @@ __device__ __forceinline__ void attn_keys16(AttnState<D>& st, const uint32_t (&q
     st.o[n][2] *= alpha[1];
     st.o[n][3] *= alpha[1];
   }
-  const uint32_t pa0 = pack_bf16x2(s[0][0], s[0][1]), pa1 = pack_bf16x2(s[0][2], s[0][3]);
-  const uint32_t pa2 = pack_bf16x2(s[1][0], s[1][1]), pa3 = pack_bf16x2(s[1][2], s[1][3]);
+  // P as the sum of two bf16 parts (hi + lo): P.V carries ~16 significant bits of P
+  uint32_t ph[4], pl[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float x0 = s[i >> 1][(i & 1) * 2], x1 = s[i >> 1][(i & 1) * 2 + 1];
+    const uint32_t h = pack_bf16x2(x0, x1);
+    ph[i] = h;
+    pl[i] = pack_bf16x2(x0 - bf16_to_f32((uint16_t)(h & 0xFFFFu)), x1 - bf16_to_f32((uint16_t)(h >> 16)));
+  }
 #pragma unroll
   for (int n = 0; n < D / 8; n += 2) {
     const int key = kb + (mi & 1) * 8 + r8;
     const int d0 = (n + (mi >> 1)) * 8;
     uint32_t b0, b1, b2, b3;
     ldsm_x4_t(vbase + swz(key, d0, rows), b0, b1, b2, b3);
-    mma_bf16(st.o[n], pa0, pa1, pa2, pa3, b0, b1);
-    mma_bf16(st.o[n + 1], pa0, pa1, pa2, pa3, b2, b3);
+    mma_bf16(st.o[n], ph[0], ph[1], ph[2], ph[3], b0, b1);
+    mma_bf16(st.o[n + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+    mma_bf16(st.o[n], pl[0], pl[1], pl[2], pl[3], b0, b1);
+    mma_bf16(st.o[n + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
   }
 }
 
@@ -579,14 +643,27 @@ __device__ void attention_phase(Worker& w) {
   {
     const uint16_t* qsrc = P.first ? reinterpret_cast<const uint16_t*>(P.x_cur + P.xo.q0) : P.in_q;
     const int nch = T * group * D / 8;
-    for (int c = tid; c < nch && w.ok; c += kComputeThreads) {
-      const int t = c / (group * D / 8), rem = c % (group * D / 8), j = rem / (D / 8), d = (rem % (D / 8)) * 8;
-      const uint16_t* p = qsrc + (size_t)t * dm.hq * D + (size_t)(au.hk * group + j) * D + d;
-      uint4 v;
-      if (P.first) w.ok = poll_bf16x8(cx, p, v, PH_ATTN);
-      else v = *reinterpret_cast<const uint4*>(p);
-      const int m = ((d >> 3) & 1) * 2 + (t >> 3);
-      *reinterpret_cast<uint4*>(qsm + j * (D / 16) * kKStepBytes + (d >> 4) * kKStepBytes + m * 128 + (t & 7) * 16) = v;
+    constexpr int kB = 4;
+    for (int c0 = tid; c0 < nch && w.ok; c0 += kComputeThreads * kB) {
+      uint4 v[kB];
+      const uint16_t* src[kB];
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        const int c = c0 + i * kComputeThreads;
+        if (c >= nch) continue;
+        const int t = c / (group * D / 8), rem = c % (group * D / 8), j = rem / (D / 8), d = (rem % (D / 8)) * 8;
+        src[i] = qsrc + (size_t)t * dm.hq * D + (size_t)(au.hk * group + j) * D + d;
+        v[i] = P.first ? ld_relaxed_v4(src[i]) : *reinterpret_cast<const uint4*>(src[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        const int c = c0 + i * kComputeThreads;
+        if (c >= nch || !w.ok) continue;
+        if (P.first && !bf16x8_ready(v[i])) w.ok = poll_bf16x8(cx, src[i], v[i], PH_ATTN);
+        const int t = c / (group * D / 8), rem = c % (group * D / 8), j = rem / (D / 8), d = (rem % (D / 8)) * 8;
+        const int m = ((d >> 3) & 1) * 2 + (t >> 3);
+        *reinterpret_cast<uint4*>(qsm + j * (D / 16) * kKStepBytes + (d >> 4) * kKStepBytes + m * 128 + (t & 7) * 16) = v[i];
+      }
     }
     if (au.tree) {
       for (int c = tid; c < 2 * 16 * D / 8 && w.ok; c += kComputeThreads) {
@@ -606,6 +683,7 @@ __device__ void attention_phase(Worker& w) {
   }
   w.ok = __all_sync(0xffffffffu, w.ok);
   cbar();
+  stamp_rt(P, EV_ATTN_IN);
   if (*cx.S.abort) w.ok = false;
   const int j = w.cw / WPH, part = w.cw % WPH;
   const bool active = j < group;
@@ -729,11 +807,22 @@ __device__ void attn_merge_phase(Worker& w) {
   uint16_t* o_out = reinterpret_cast<uint16_t*>(P.x_cur + P.xo.o);
   for (int it = gw; it < T * dm.hq && w.ok; it += G * kComputeWarps) {
     const int t = it / dm.hq, h = it % dm.hq, hk = h / group, j = h % group;
+    auto mlp = [&](int s) { return part_ml + (((size_t)(hk * S + s) * T + t) * group + j) * 2; };
+    auto accp = [&](int s) { return part_acc + (((size_t)(hk * S + s) * T + t) * group + j) * D + w.lane * PER; };
+    constexpr int kB = 8;
+    // pass 1: the running maximum over the splits (loads issued 8 at a time)
     float M = -INFINITY;
-    for (int s = 0; s < S && w.ok; ++s) {
-      uint2 v;
-      w.ok = poll_f32x2(cx, part_ml + (((size_t)(hk * S + s) * T + t) * group + j) * 2, v, PH_ATTN_MERGE);
-      M = fmaxf(M, __uint_as_float(v.x));
+    for (int s0 = 0; s0 < S && w.ok; s0 += kB) {
+      uint2 v[kB];
+#pragma unroll
+      for (int i = 0; i < kB; ++i)
+        if (s0 + i < S) v[i] = ld_relaxed_v2(mlp(s0 + i));
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        if (s0 + i >= S || !w.ok) continue;
+        if (v[i].x == kF32Empty || v[i].y == kF32Empty) w.ok = poll_f32x2(cx, mlp(s0 + i), v[i], PH_ATTN_MERGE);
+        M = fmaxf(M, __uint_as_float(v[i].x));
+      }
     }
     w.ok = __all_sync(0xffffffffu, w.ok);
     if (!w.ok) break;
@@ -741,26 +830,47 @@ __device__ void attn_merge_phase(Worker& w) {
     float acc[PER], L = 0.f;
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-    for (int s = 0; s < S && w.ok; ++s) {
-      float* mlp = part_ml + (((size_t)(hk * S + s) * T + t) * group + j) * 2;
-      uint2 mlv = ld_relaxed_v2(mlp);
-      const float ws = exp2f(__uint_as_float(mlv.x) - Mu);
-      L += ws * __uint_as_float(mlv.y);
-      float* ap = part_acc + (((size_t)(hk * S + s) * T + t) * group + j) * D + w.lane * PER;
-      if constexpr (PER == 4) {
-        uint4 v;
-        w.ok = poll_f32x4(cx, ap, v, PH_ATTN_MERGE);
-        acc[0] += ws * __uint_as_float(v.x);
-        acc[1] += ws * __uint_as_float(v.y);
-        acc[2 % PER] += ws * __uint_as_float(v.z);
-        acc[3 % PER] += ws * __uint_as_float(v.w);
-        st_relaxed_v4(ap, make_uint4(kF32Empty, kF32Empty, kF32Empty, kF32Empty));
-      } else {
-        uint2 v;
-        w.ok = poll_f32x2(cx, ap, v, PH_ATTN_MERGE);
-        acc[0] += ws * __uint_as_float(v.x);
-        acc[1 % PER] += ws * __uint_as_float(v.y);
-        asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%2};" ::"l"(ap), "r"(kF32Empty), "r"(kF32Empty) : "memory");
+    // pass 2: weighted sum of the partials, in split order
+    for (int s0 = 0; s0 < S && w.ok; s0 += kB) {
+      uint2 mv[kB];
+      float av[kB][PER];
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        if (s0 + i >= S) continue;
+        mv[i] = ld_relaxed_v2(mlp(s0 + i));
+        if constexpr (PER == 4) {
+          const uint4 q4 = ld_relaxed_v4(accp(s0 + i));
+          av[i][0] = __uint_as_float(q4.x); av[i][1 % PER] = __uint_as_float(q4.y);
+          av[i][2 % PER] = __uint_as_float(q4.z); av[i][3 % PER] = __uint_as_float(q4.w);
+        } else {
+          const uint2 q2 = ld_relaxed_v2(accp(s0 + i));
+          av[i][0] = __uint_as_float(q2.x); av[i][1 % PER] = __uint_as_float(q2.y);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        if (s0 + i >= S || !w.ok) continue;
+        bool ready = true;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) ready &= __float_as_uint(av[i][e]) != kF32Empty;
+        if (!ready) {
+          if constexpr (PER == 4) {
+            uint4 q4;
+            w.ok = poll_f32x4(cx, accp(s0 + i), q4, PH_ATTN_MERGE);
+            av[i][0] = __uint_as_float(q4.x); av[i][1 % PER] = __uint_as_float(q4.y);
+            av[i][2 % PER] = __uint_as_float(q4.z); av[i][3 % PER] = __uint_as_float(q4.w);
+          } else {
+            uint2 q2;
+            w.ok = poll_f32x2(cx, accp(s0 + i), q2, PH_ATTN_MERGE);
+            av[i][0] = __uint_as_float(q2.x); av[i][1 % PER] = __uint_as_float(q2.y);
+          }
+        }
+        const float ws = exp2f(__uint_as_float(mv[i].x) - Mu);
+        L += ws * __uint_as_float(mv[i].y);
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] += ws * av[i][e];
+        if constexpr (PER == 4) st_relaxed_v4(accp(s0 + i), make_uint4(kF32Empty, kF32Empty, kF32Empty, kF32Empty));
+        else asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%2};" ::"l"(accp(s0 + i)), "r"(kF32Empty), "r"(kF32Empty) : "memory");
       }
     }
     w.ok = __all_sync(0xffffffffu, w.ok);
@@ -831,9 +941,13 @@ __device__ void route_phase(Worker& w) {
       v[i] = -INFINITY;
       used[i] = true;
       const int e = w.lane + 32 * i;
+      if (i < per && e < E) v[i] = __uint_as_float(ld_relaxed_u32(logits + t * E + e));
+    }
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int e = w.lane + 32 * i;
       if (i < per && e < E && w.ok) {
         uint32_t n = 0;
-        uint32_t bits = ld_relaxed_u32(logits + t * E + e);
+        uint32_t bits = __float_as_uint(v[i]);
         while (bits == kF32Empty) {
           if ((++n & 31) == 0 && cx.expired(PH_ROUTE)) { w.ok = false; break; }
           bits = ld_relaxed_u32(logits + t * E + e);
@@ -869,6 +983,7 @@ __device__ void route_phase(Worker& w) {
     }
   }
   cbar();
+  stamp_rt(P, EV_ROUTE_TOPK);
   if (*cx.S.abort) w.ok = false;
   // dispatch: thread e counts its tokens, then a block-wide scan compacts the active experts
   const int tid = w.cw * 32 + w.lane;
@@ -920,18 +1035,31 @@ __device__ void route_phase(Worker& w) {
     }
   }
   // NVFP4 activations of the pooled vectors (GEMM1 B operand, f16, one row per token)
+  // (the router stage already saw every element of u, so plain relaxed loads suffice here)
   const uint16_t* u = reinterpret_cast<const uint16_t*>(P.x_cur + P.xo.u);
+  uint16_t* rowbuf = reinterpret_cast<uint16_t*>(cx.S.act + (size_t)dm.p * 32) + (size_t)w.cw * dm.p;
   for (int tt = 0; tt < 2 && w.ok; ++tt) {
     const int t = w.cw * 2 + tt;
     const uint16_t* row = u + (size_t)t * dm.p;
+    for (int c0 = w.lane; c0 < dm.p / 8; c0 += 32 * 4) {
+      uint4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (c0 + 32 * i < dm.p / 8) v[i] = ld_relaxed_v4(row + (c0 + 32 * i) * 8);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (c0 + 32 * i < dm.p / 8) *reinterpret_cast<uint4*>(rowbuf + (c0 + 32 * i) * 8) = v[i];
+    }
+    __syncwarp();
     uint8_t* act = cx.S.act;
     float ts = nvfp4_row(
-        dm.p, w.lane, [&](int i) { return bf16_to_f32(ld_relaxed_u16(row + i)); },
+        dm.p, w.lane, [&](int i) { return bf16_to_f32(rowbuf[i]); },
         [&](int b, int j, uint32_t h2) {
           const int k = b * 16 + j;
           *reinterpret_cast<uint32_t*>(act + act_off(t, k) + (k & 7) * 2) = h2;
         });
     if (w.lane == 0) cx.S.x_ts[t] = ts;
+    __syncwarp();
   }
   cbar();
   if (*cx.S.abort) w.ok = false;
@@ -959,6 +1087,7 @@ __device__ __forceinline__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* 
   const int g = lane >> 2, q = lane & 3;
   const int mi = lane >> 3, r8 = lane & 7;
   const int ng = K / 64;
+  float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   uint32_t bro[2];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
@@ -981,10 +1110,15 @@ __device__ __forceinline__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* 
         uint32_t b0, b1, b2, b3;
         ldsm_x4(bro[nt] + kstep, b0, b1, b2, b3);
         mma_f16(acc[nt], a[0][0], a[0][1], a[0][2], a[0][3], b0, b1);
-        mma_f16(acc[nt], a[1][0], a[1][1], a[1][2], a[1][3], b2, b3);
+        mma_f16(acc2[nt], a[1][0], a[1][1], a[1][2], a[1][3], b2, b3);
       }
     }
   }
+  // two independent chains (even / odd k-steps), summed in a fixed order
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[nt][i] += acc2[nt][i];
 }
 
 __device__ void gemm1_phase(Worker& w) {
@@ -1048,24 +1182,36 @@ __device__ void gemm2_phase(Worker& w) {
       // stage this expert's NVFP4 activations: row p = p-th token of the expert
       for (int p = w.cw; p < n && w.ok; p += kComputeWarps) {
         const float* row = ain + (size_t)cx.S.act_slot[a * 16 + p] * dm.f;
-        // poll the whole row (each lane its own 16-byte chunks) before quantising
-        for (int c = w.lane; c < dm.f / 4 && w.ok; c += 32) {
-          uint4 v;
-          w.ok = poll_f32x4(cx, row + c * 4, v, PH_GEMM2);
+        float* rowbuf = reinterpret_cast<float*>(cx.S.act + (size_t)dm.f * 32) + (size_t)w.cw * dm.f;
+        // poll the whole row into shared memory, 8 loads in flight per lane
+        for (int c0 = w.lane; c0 < dm.f / 4 && w.ok; c0 += 32 * 8) {
+          uint4 v[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (c0 + 32 * i < dm.f / 4) v[i] = ld_relaxed_v4(row + (c0 + 32 * i) * 4);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (c0 + 32 * i >= dm.f / 4 || !w.ok) continue;
+            if (!f32x4_ready(v[i])) w.ok = poll_f32x4(cx, row + (c0 + 32 * i) * 4, v[i], PH_GEMM2);
+            *reinterpret_cast<uint4*>(rowbuf + (c0 + 32 * i) * 4) = v[i];
+          }
         }
         w.ok = __all_sync(0xffffffffu, w.ok);
         if (!w.ok) break;
+        __syncwarp();
         uint8_t* act = cx.S.act;
         float ts = nvfp4_row(
-            dm.f, w.lane, [&](int i) { return __uint_as_float(ld_relaxed_u32(row + i)); },
+            dm.f, w.lane, [&](int i) { return rowbuf[i]; },
             [&](int b, int j, uint32_t h2) {
               const int k = b * 16 + j;
               *reinterpret_cast<uint32_t*>(act + act_off(p, k) + (k & 7) * 2) = h2;
             });
+        __syncwarp();
         if (w.lane == 0) cx.S.a_ts[p] = ts;
       }
       w.ok = __all_sync(0xffffffffu, w.ok);
       cbar();
+      if (a == a_first) stamp_rt(P, EV_GEMM2_IN);
       if (*cx.S.abort) w.ok = false;
       const int u_lo = max(lo, a * u2pe), u_hi = min(hi, (a + 1) * u2pe);
       for (int gu = u_lo; gu < u_hi; ++gu) {
@@ -1114,12 +1260,17 @@ __device__ void combine_phase(Worker& w) {
   for (int it = gt; it < T * nch && w.ok; it += G * kComputeThreads) {
     const int t = it / nch, pc = it % nch;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int c = 0; c < dm.k; ++c) {
+    uint4 v[kMaxTopK];
+#pragma unroll
+    for (int c = 0; c < kMaxTopK; ++c)
+      if (c < dm.k) v[c] = ld_relaxed_v4(y + (size_t)(t * dm.k + c) * dm.p + pc * 8);
+#pragma unroll
+    for (int c = 0; c < kMaxTopK; ++c) {
+      if (c >= dm.k || !w.ok) continue;
       uint16_t* src = y + (size_t)(t * dm.k + c) * dm.p + pc * 8;
-      uint4 v;
-      if (!poll_bf16x8(cx, src, v, PH_COMBINE)) { w.ok = false; break; }
+      if (!bf16x8_ready(v[c]) && !poll_bf16x8(cx, src, v[c], PH_COMBINE)) { w.ok = false; continue; }
       const float wt = cx.S.topk_w[t * kMaxTopK + c];
-      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+      const uint32_t wd[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         acc[2 * i] += wt * bf16_to_f32((uint16_t)(wd[i] & 0xFFFF));
@@ -1161,55 +1312,44 @@ struct QkvDst {
   uint16_t* tkv;       // optional sentinel copy [2][hkv][16][hd]
 };
 
-__device__ __forceinline__ void qkv_epilogue(const LaunchParams& P, const Smem& S, const QkvDst& dst, int u,
-                                             const float (&acc)[2][4], int g, int q) {
+__device__ __forceinline__ void qkv_epilogue(const LaunchParams& P, const Smem& S, const QkvDst& dst, int u, int p,
+                                             int t, float vlo, float vhi) {
   const Dims& dm = P.dm;
   const int D = dm.hd, upd = D / 16;
   const int nQ = dm.hq * upd, nK = dm.hkv * upd;
-  const float* rope = P.rope;
   if (u < nQ + nK) {
+    // rows p and p+8 of the unit are dims (j*8+p) and (j*8+p + D/2) of one head
     const bool isq = u < nQ;
     const int hu = isq ? u : u - nQ, h = hu / upd, j = hu % upd;
-    const int dim = j * 8 + g;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int ii = 0; ii < 2; ++ii) {
-        const int t = nt * 8 + 2 * q + ii;
-        const float x = acc[nt][ii], y = acc[nt][2 + ii];
-        const float* cs = rope + ((size_t)S.depth[t] * (D / 2) + dim) * 2;
-        const float c = cs[0], s = cs[1];
-        const uint16_t xr = bf16_bits_rn(x * c - y * s), yr = bf16_bits_rn(y * c + x * s);
-        if (isq) {
-          uint16_t* p = dst.q + (size_t)t * dm.hq * D + (size_t)h * D + dim;
-          if (dst.q_relaxed) { st_relaxed_u16(p, xr); st_relaxed_u16(p + D / 2, yr); }
-          else { p[0] = xr; p[D / 2] = yr; }
-        } else {
-          uint16_t* p = dst.kc + ((size_t)h * dm.max_ctx + P.pos0 + t) * D + dim;
-          p[0] = xr;
-          p[D / 2] = yr;
-          if (dst.tkv) {
-            uint16_t* tp = dst.tkv + (((size_t)0 * dm.hkv + h) * 16 + t) * D + dim;
-            st_relaxed_u16(tp, xr);
-            st_relaxed_u16(tp + D / 2, yr);
-          }
-        }
+    const int dim = j * 8 + p;
+    const float* cs = P.rope + ((size_t)S.depth[t] * (D / 2) + dim) * 2;
+    const float c = cs[0], s = cs[1];
+    const uint16_t xr = bf16_bits_rn(vlo * c - vhi * s), yr = bf16_bits_rn(vhi * c + vlo * s);
+    if (isq) {
+      uint16_t* q = dst.q + (size_t)t * dm.hq * D + (size_t)h * D + dim;
+      if (dst.q_relaxed) { st_relaxed_u16(q, xr); st_relaxed_u16(q + D / 2, yr); }
+      else { q[0] = xr; q[D / 2] = yr; }
+    } else {
+      uint16_t* k = dst.kc + ((size_t)h * dm.max_ctx + P.pos0 + t) * D + dim;
+      k[0] = xr;
+      k[D / 2] = yr;
+      if (dst.tkv) {
+        uint16_t* tp = dst.tkv + ((size_t)h * 16 + t) * D + dim;
+        st_relaxed_u16(tp, xr);
+        st_relaxed_u16(tp + D / 2, yr);
       }
+    }
   } else {
     const int hu = u - nQ - nK, h = hu / upd, j = hu % upd;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int ii = 0; ii < 2; ++ii) {
-        const int t = nt * 8 + 2 * q + ii;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int dim = j * 16 + g + half * 8;
-          const uint16_t v = bf16_bits_rn(acc[nt][half * 2 + ii]);
-          dst.vc[((size_t)h * dm.max_ctx + P.pos0 + t) * D + dim] = v;
-          if (dst.tkv) st_relaxed_u16(dst.tkv + (((size_t)1 * dm.hkv + h) * 16 + t) * D + dim, v);
-        }
-      }
+    const uint16_t a = bf16_bits_rn(vlo), b = bf16_bits_rn(vhi);
+    uint16_t* v = dst.vc + ((size_t)h * dm.max_ctx + P.pos0 + t) * D + j * 16 + p;
+    v[0] = a;
+    v[8] = b;
+    if (dst.tkv) {
+      uint16_t* tp = dst.tkv + (((size_t)dm.hkv + h) * 16 + t) * D + j * 16 + p;
+      st_relaxed_u16(tp, a);
+      st_relaxed_u16(tp + 8, b);
+    }
   }
 }
 
@@ -1240,7 +1380,6 @@ __device__ void compute_main(Worker& w) {
   Ctx& cx = *w.cx;
   const LaunchParams& P = *cx.P;
   const Dims& dm = P.dm;
-  const int g = w.g, q = w.q;
   const int b = blockIdx.x;
   uint8_t* X = P.x_cur;
   if (P.first) {
@@ -1248,83 +1387,71 @@ __device__ void compute_main(Worker& w) {
     // RMSNorm(hidden_in) -> layer 0 QKV -> RoPE -> layer 0 KV rows and Q
     rope_table(w);
     stage_act(w, P.hidden_in, dm.d, false, P.g_attn_pro, dm.rms_eps, PH_PROLOGUE);
+    stamp<kTiming>(P, b, EV_PRO_IN);
     QkvDst dq{reinterpret_cast<uint16_t*>(X + P.xo.q0), true, P.kc, P.vc, reinterpret_cast<uint16_t*>(X + P.xo.tkv0)};
     dense_phase(w, dm.d, dm.nqkv, P.phase_rot * 1,
-                [&](int u, const float(&acc)[2][4]) { qkv_epilogue(P, cx.S, dq, u, acc, g, q); });
-    stamp<kTiming>(P, b, PH_PROLOGUE);
+                [&](int u, int p, int t, float lo, float hi) { qkv_epilogue(P, cx.S, dq, u, p, t, lo, hi); });
+    stamp<kTiming>(P, b, EV_PRO_DONE);
     cbar();
   }
   // a2: tree attention (split over blocks), a3: merge of the split partials
   if (dm.hd == 128) attention_phase<128>(w);
   else attention_phase<64>(w);
-  stamp<kTiming>(P, b, PH_ATTN);
+  stamp<kTiming>(P, b, EV_ATTN_DONE);
   if (dm.hd == 128) attn_merge_phase<128>(w);
   else attn_merge_phase<64>(w);
-  stamp<kTiming>(P, b, PH_ATTN_MERGE);
+  stamp<kTiming>(P, b, EV_MERGE_DONE);
   // a4: h1 = bf16(h + bf16(O W_o^T))
   {
     const uint16_t* hprev = P.first ? P.hidden_in : P.in_h;
     uint16_t* h1 = reinterpret_cast<uint16_t*>(X + P.xo.h1);
     stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.o), dm.hq * dm.hd, true, nullptr, 0.f, PH_OPROJ);
-    dense_phase(w, dm.hq * dm.hd, dm.d, P.phase_rot * 3, [&](int u, const float(&acc)[2][4]) {
+    stamp<kTiming>(P, b, EV_OPROJ_IN);
+    dense_phase(w, dm.hq * dm.hd, dm.d, P.phase_rot * 3, [&](int u, int p, int t, float lo, float hi) {
+      const float v2[2] = {lo, hi};
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int ii = 0; ii < 2; ++ii)
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const int t = nt * 8 + 2 * q + ii, n = u * 16 + g + hf * 8;
-            const float o = bf16_to_f32(bf16_bits_rn(acc[nt][hf * 2 + ii]));
-            // test hook: the first element of the whole h1 exchange is never written
-            if ((P.flags & 0x10000u) && u == 0 && t == 0 && g == 0 && hf == 0) continue;
-            st_relaxed_u16(h1 + (size_t)t * dm.d + n, bf16_bits_rn(bf16_to_f32(hprev[(size_t)t * dm.d + n]) + o));
-          }
+      for (int hf = 0; hf < 2; ++hf) {
+        const int n = u * 16 + p + hf * 8;
+        // test hook: the first element of the whole h1 exchange is never written
+        if ((P.flags & 0x10000u) && u == 0 && t == 0 && p == 0 && hf == 0) continue;
+        const float o = bf16_to_f32(bf16_bits_rn(v2[hf]));
+        st_relaxed_u16(h1 + (size_t)t * dm.d + n, bf16_bits_rn(bf16_to_f32(hprev[(size_t)t * dm.d + n]) + o));
+      }
     });
-    stamp<kTiming>(P, b, PH_OPROJ);
+    stamp<kTiming>(P, b, EV_OPROJ_DONE);
   }
   // a5: u = bf16(bf16(RMSNorm(h1)) W_pool^T)
   {
     uint16_t* uo = reinterpret_cast<uint16_t*>(X + P.xo.u);
     stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h1), dm.d, true, P.g_moe, dm.rms_eps, PH_POOL);
-    dense_phase(w, dm.d, dm.p, P.phase_rot * 4, [&](int u, const float(&acc)[2][4]) {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int ii = 0; ii < 2; ++ii)
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const int t = nt * 8 + 2 * q + ii, n = u * 16 + g + hf * 8;
-            st_relaxed_u16(uo + (size_t)t * dm.p + n, bf16_bits_rn(acc[nt][hf * 2 + ii]));
-          }
+    stamp<kTiming>(P, b, EV_POOL_IN);
+    dense_phase(w, dm.d, dm.p, P.phase_rot * 4, [&](int u, int p, int t, float lo, float hi) {
+      st_relaxed_u16(uo + (size_t)t * dm.p + u * 16 + p, bf16_bits_rn(lo));
+      st_relaxed_u16(uo + (size_t)t * dm.p + u * 16 + p + 8, bf16_bits_rn(hi));
     });
-    stamp<kTiming>(P, b, PH_POOL);
+    stamp<kTiming>(P, b, EV_POOL_DONE);
   }
   // a6: router logits = u W_r^T + b (fp32)
   {
     float* lg = reinterpret_cast<float*>(X + P.xo.logits);
     stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.u), dm.p, true, nullptr, 0.f, PH_ROUTER);
-    dense_phase(w, dm.p, dm.e, P.phase_rot * 5, [&](int u, const float(&acc)[2][4]) {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int ii = 0; ii < 2; ++ii)
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const int t = nt * 8 + 2 * q + ii, n = u * 16 + g + hf * 8;
-            st_relaxed_u32(lg + (size_t)t * dm.e + n, __float_as_uint(f32_canon(acc[nt][hf * 2 + ii] + P.b_router[n])));
-          }
+    stamp<kTiming>(P, b, EV_ROUTER_IN);
+    dense_phase(w, dm.p, dm.e, P.phase_rot * 5, [&](int u, int p, int t, float lo, float hi) {
+      const int n = u * 16 + p;
+      st_relaxed_u32(lg + (size_t)t * dm.e + n, __float_as_uint(f32_canon(lo + P.b_router[n])));
+      st_relaxed_u32(lg + (size_t)t * dm.e + n + 8, __float_as_uint(f32_canon(hi + P.b_router[n + 8])));
     });
-    stamp<kTiming>(P, b, PH_ROUTER);
+    stamp<kTiming>(P, b, EV_ROUTER_DONE);
   }
   // a6/a7/a8: top-k, dispatch, NVFP4 activations
   cbar();
   route_phase(w);
-  stamp<kTiming>(P, b, PH_ROUTE);
+  stamp<kTiming>(P, b, EV_ROUTE_DONE);
   // a9, a10: the expert GEMMs
   gemm1_phase(w);
-  stamp<kTiming>(P, b, PH_GEMM1);
+  stamp<kTiming>(P, b, EV_GEMM1_DONE);
   gemm2_phase(w);
-  stamp<kTiming>(P, b, PH_GEMM2);
+  stamp<kTiming>(P, b, EV_GEMM2_DONE);
   // move the next layer's KV history toward L2 while the combine waits
   if ((P.flags & 0x4u) && !P.last && w.cw == 0 && w.lane == 0 && P.kc_pf != nullptr) {
     const AttnUnit au = attn_unit(P, rot_block(b, P.phase_rot * 2, gridDim.x), P.next_global);
@@ -1337,50 +1464,43 @@ __device__ void compute_main(Worker& w) {
   }
   // a11: combine, then h2 = bf16(h1 + bf16(z W_unp^T))
   combine_phase(w);
-  stamp<kTiming>(P, b, PH_COMBINE);
+  stamp<kTiming>(P, b, EV_COMBINE_DONE);
   {
     const uint16_t* h1 = reinterpret_cast<const uint16_t*>(X + P.xo.h1);
     uint16_t* h2 = reinterpret_cast<uint16_t*>(X + P.xo.h2);
     uint16_t* hnext = P.last ? P.hidden_out : P.out_h;
     stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.z), dm.p, true, nullptr, 0.f, PH_UNPOOL);
-    dense_phase(w, dm.p, dm.d, P.phase_rot * 8, [&](int u, const float(&acc)[2][4]) {
+    stamp<kTiming>(P, b, EV_UNPOOL_IN);
+    dense_phase(w, dm.p, dm.d, P.phase_rot * 8, [&](int u, int p, int t, float lo, float hi) {
+      const float v2[2] = {lo, hi};
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int ii = 0; ii < 2; ++ii)
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const int t = nt * 8 + 2 * q + ii, n = u * 16 + g + hf * 8;
-            const float o = bf16_to_f32(bf16_bits_rn(acc[nt][hf * 2 + ii]));
-            const uint16_t v = bf16_bits_rn(bf16_to_f32(ld_relaxed_u16(h1 + (size_t)t * dm.d + n)) + o);
-            st_relaxed_u16(h2 + (size_t)t * dm.d + n, v);
-            if (hnext) hnext[(size_t)t * dm.d + n] = v;
-          }
+      for (int hf = 0; hf < 2; ++hf) {
+        const int n = u * 16 + p + hf * 8;
+        const float o = bf16_to_f32(bf16_bits_rn(v2[hf]));
+        const uint16_t v = bf16_bits_rn(bf16_to_f32(ld_relaxed_u16(h1 + (size_t)t * dm.d + n)) + o);
+        st_relaxed_u16(h2 + (size_t)t * dm.d + n, v);
+        if (hnext) hnext[(size_t)t * dm.d + n] = v;
+      }
     });
-    stamp<kTiming>(P, b, PH_UNPOOL);
+    stamp<kTiming>(P, b, EV_UNPOOL_DONE);
   }
   pdl_launch_dependents();
   // a12: next layer's RMSNorm + QKV + RoPE + KV write; a12': final norm + LM head
   if (!P.last) {
     stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h2), dm.d, true, P.g_tail, dm.rms_eps, PH_TAIL);
+    stamp<kTiming>(P, b, EV_TAIL_IN);
     QkvDst dq{P.out_q, false, P.kc_next, P.vc_next, nullptr};
     dense_phase(w, dm.d, dm.nqkv, P.phase_rot * 9,
-                [&](int u, const float(&acc)[2][4]) { qkv_epilogue(P, cx.S, dq, u, acc, g, q); });
+                [&](int u, int p, int t, float lo, float hi) { qkv_epilogue(P, cx.S, dq, u, p, t, lo, hi); });
   } else if (dm.vocab > 0) {
     stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h2), dm.d, true, P.g_tail, dm.rms_eps, PH_TAIL);
-    dense_phase(w, dm.d, dm.vocab, P.phase_rot * 9, [&](int u, const float(&acc)[2][4]) {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int ii = 0; ii < 2; ++ii)
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const int t = nt * 8 + 2 * q + ii, n = u * 16 + g + hf * 8;
-            P.logits[(size_t)t * dm.vocab + n] = acc[nt][hf * 2 + ii];
-          }
+    stamp<kTiming>(P, b, EV_TAIL_IN);
+    dense_phase(w, dm.d, dm.vocab, P.phase_rot * 9, [&](int u, int p, int t, float lo, float hi) {
+      P.logits[(size_t)t * dm.vocab + u * 16 + p] = lo;
+      P.logits[(size_t)t * dm.vocab + u * 16 + p + 8] = hi;
     });
   }
-  stamp<kTiming>(P, b, PH_TAIL);
+  stamp<kTiming>(P, b, EV_TAIL_DONE);
 }
 
 // ---------------------------------------------------------------------------
@@ -1482,9 +1602,9 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
   w.ok = true;
   pdl_wait();
   cx.deadline = globaltimer() + (((uint64_t)P.timeout_ns_hi << 32) | P.timeout_ns_lo);
-  stamp<kTiming>(P, blockIdx.x, PH_START);
+  stamp<kTiming>(P, blockIdx.x, EV_START);
   compute_main<kTiming>(w);
-  stamp<kTiming>(P, blockIdx.x, PH_END);
+  stamp<kTiming>(P, blockIdx.x, EV_END);
 }
 
 const void* layer_kernel(bool timing) {

@@ -169,7 +169,7 @@ def test_self_timing_stamps_are_ordered():
     tm = got["model"].timing()
     got["model"].close()
     assert got["status"] == [0]
-    start, end = tm[:, :, 0].astype(np.int64), tm[:, :, 13].astype(np.int64)
+    start, end = tm[:, :, msm.EV["start"]].astype(np.int64), tm[:, :, msm.EV["end"]].astype(np.int64)
     assert np.all(start > 0) and np.all(end >= start)
     # launches follow each other
     assert np.all(start[1:].min(axis=1) >= start[:-1].min(axis=1))
