@@ -898,7 +898,8 @@ __device__ void attn_merge_phase(Worker& w) {
 // experts in NVFP4)
 // ---------------------------------------------------------------------------
 // quantise one row of n fp32 values (lane-parallel over 16-element blocks) into
-// f16 values e2m1 * e4m3-scale written by `put(block, j, f16x2 pair)`; returns the row scale
+// f16 values e2m1 * e4m3-scale written by `put(block, j, f16x2 pair)`; returns the
+// row scale (amax / (6 * 448) rounded up to a power of two)
 template <class Get, class Put>
 __device__ __forceinline__ float nvfp4_row(int n, int lane, Get get, Put put) {
   const int nb = n / 16;
@@ -907,7 +908,13 @@ __device__ __forceinline__ float nvfp4_row(int n, int lane, Get get, Put put) {
     for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(get(b * 16 + j)));
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const float ts = __fdiv_rn(amax, 2688.0f);
+  // row scale: amax / (6 * 448) rounded up to a power of two
+  float ts = __fdiv_rn(amax, 2688.0f);
+  if (ts > 0.f) {
+    int e;
+    const float m = frexpf(ts, &e);
+    if (m != 0.5f) ts = ldexpf(1.0f, e);
+  }
   for (int b = lane; b < nb; b += 32) {
     float bmax = 0.f;
     for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(get(b * 16 + j)));

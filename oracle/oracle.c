@@ -104,15 +104,25 @@ uint8_t or_e4m3_encode(float v) {
   return (uint8_t)best;
 }
 
+/* Smallest power of two >= x (0 for x <= 0). */
+static float pow2_ceil(float x) {
+  if (!(x > 0.0f)) return 0.0f;
+  int e;
+  float m = frexpf(x, &e); /* x = m 2^e, m in [0.5, 1) */
+  return (m == 0.5f) ? x : ldexpf(1.0f, e);
+}
+
 /* Quantise one row of n fp32 values (n % 16 == 0) to NVFP4.  The per-row fp32
- * scale is amax / (6 * 448); every decision below is taken in fp32. */
+ * scale is amax / (6 * 448) rounded up to a power of two, so that every block
+ * scale fits E4M3 and a tiny change of the row's largest element cannot move
+ * the scale of every block; every decision below is taken in fp32. */
 float or_nvfp4_quantize(const float* x, int n, uint8_t* codes, uint8_t* sf) {
   float amax = 0.0f;
   for (int i = 0; i < n; ++i) {
     float a = fabsf(x[i]);
     if (a > amax) amax = a;
   }
-  volatile float ts = amax / 2688.0f; /* 6 * 448 */
+  volatile float ts = pow2_ceil(amax / 2688.0f); /* 6 * 448 */
   for (int b = 0; b < n / 16; ++b) {
     float bmax = 0.0f;
     for (int j = 0; j < 16; ++j) {

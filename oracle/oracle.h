@@ -16,7 +16,8 @@
  *
  * Arithmetic: fp64 throughout, rounded to bf16 exactly at the materialisation
  * points listed in or_layer(); the NVFP4 activation quantiser takes its
- * decisions in fp32 (the precision the GPU path uses), and router logits are
+ * decisions in fp32 (the precision the GPU path uses) with a per-row scale
+ * of amax / (6 * 448) rounded up to a power of two, and router logits are
  * rounded to fp32 before the top-k decision.
  *
  * Layouts (all row-major, bf16 stored as uint16 bit patterns):

@@ -97,7 +97,11 @@ def test_nvfp4_quantize_error_bound():
     for _ in range(20):
         x = (rng.standard_normal(256) * rng.uniform(0.01, 10)).astype(np.float32)
         codes, sf, ts = oracle.nvfp4_quantize(x)
-        assert ts == np.float32(np.max(np.abs(x))) / np.float32(2688.0)
+        # row scale: the smallest power of two >= amax / (6 * 448)
+        r = np.float32(np.max(np.abs(x))) / np.float32(2688.0)
+        m, e = np.frexp(r)
+        assert ts == (r if m == 0.5 else np.float32(2.0 ** e))
+        assert ts >= r and ts < 2 * r and np.frexp(ts)[0] == 0.5
         back = oracle.nvfp4_dequant(codes, sf, ts, x.size)
         for b in range(16):
             blk = slice(16 * b, 16 * b + 16)
