@@ -333,7 +333,7 @@ static double silu(double x) { return x / (1.0 + exp(-x)); }
 /*   h1  = bf16(h + bf16(O W_o^T))                                           */
 /*   u   = bf16(bf16(RMSNorm(h1; g_moe)) W_pool^T)                           */
 /*   logits = fp32(u W_r^T + b); top-k; w = softmax over the selected k      */
-/*   per slot: x_q = NVFP4(u); [g | v] = x_q W1_e^T; a = silu(g) v;          */
+/*   per slot: [g | v] = u W1_e^T (bf16 u, NVFP4 weights); a = silu(g) v;   */
 /*             a_q = NVFP4(fp32(a)); y = bf16(a_q W2_e^T)                    */
 /*   z   = bf16(sum_slots w y)                                               */
 /*   h2  = bf16(h1 + bf16(z W_unp^T))                                        */
@@ -341,6 +341,11 @@ static double silu(double x) { return x / (1.0 + exp(-x)); }
 /* top-8 of 256, pooler before the experts, unpooler after, NVFP4 experts);  */
 /* the alphasignal.ai page, § "Launch boundaries leave hardware idle" (the    */
 /* chain attention -> ... -> next layer's QKV projection and KV write).       */
+/* Precision of the expert GEMMs (same orcarouter.ai section): what leaves   */
+/* the first expert GEMM is exchanged as fp4 and what leaves the second as   */
+/* bf16.  Read plainly: GEMM1 takes the pooler's bf16 output as it is, its   */
+/* SwiGLU result is quantised to NVFP4 before GEMM2, and GEMM2's output is   */
+/* bf16.  Nothing on the pages quantises the pooled vector itself.           */
 /* ------------------------------------------------------------------------ */
 int or_layer(const or_dims* dm, const or_layer_weights* w, int is_global, const uint16_t* h_in,
              uint16_t* h_out, const int32_t* parent, int32_t pos0, uint16_t* k_cache,
@@ -401,22 +406,6 @@ int or_layer(const or_dims* dm, const or_layer_weights* w, int is_global, const 
   double* wt = (double*)malloc(sizeof(double) * OR_T * K);
   for (int t = 0; t < OR_T; ++t) or_topk(lgf + t * E, E, K, idx + t * K, wt + t * K);
 
-  /* activation quantisation of u, per token row */
-  uint8_t* xq_codes = (uint8_t*)malloc((size_t)OR_T * P / 2);
-  uint8_t* xq_sf = (uint8_t*)malloc((size_t)OR_T * P / 16);
-  float* xq_ts = (float*)malloc(sizeof(float) * OR_T);
-  double* xdq = (double*)malloc(sizeof(double) * OR_T * P);
-  {
-    float* row = (float*)malloc(sizeof(float) * P);
-    for (int t = 0; t < OR_T; ++t) {
-      for (int c = 0; c < P; ++c) row[c] = (float)u[(size_t)t * P + c];
-      xq_ts[t] = or_nvfp4_quantize(row, P, xq_codes + (size_t)t * P / 2, xq_sf + (size_t)t * P / 16);
-      or_nvfp4_dequant(xq_codes + (size_t)t * P / 2, xq_sf + (size_t)t * P / 16, xq_ts[t], P,
-                       xdq + (size_t)t * P);
-    }
-    free(row);
-  }
-
   /* experts: every (token, slot) pair independently */
   fill_tables();
   double* y = (double*)malloc(sizeof(double) * OR_T * K * P);
@@ -436,7 +425,7 @@ int or_layer(const or_dims* dm, const or_layer_weights* w, int is_global, const 
     for (int r = 0; r < 2 * F; ++r) {
       or_nvfp4_dequant(c1 + (size_t)r * P / 2, s1 + (size_t)r * P / 16, w->w1_gs[e], P, wrow);
       double acc = 0.0;
-      for (int c = 0; c < P; ++c) acc += xdq[(size_t)t * P + c] * wrow[c];
+      for (int c = 0; c < P; ++c) acc += u[(size_t)t * P + c] * wrow[c];
       gv[r] = acc;
     }
     for (int j = 0; j < F; ++j) a[j] = (float)(silu(gv[j]) * gv[F + j]);
@@ -476,7 +465,7 @@ int or_layer(const or_dims* dm, const or_layer_weights* w, int is_global, const 
       for (int i = 0; i < OR_T * P; ++i) tr->moe_z[i] = or_bf16_bits(z[i]);
   }
   free(h); free(xn); free(qkv); free(q); free(att); free(tmp); free(h1); free(u); free(z);
-  free(lg); free(lgf); free(idx); free(wt); free(xq_codes); free(xq_sf); free(xq_ts); free(xdq);
+  free(lg); free(lgf); free(idx); free(wt);
   free(y);
   return 0;
 }

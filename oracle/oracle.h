@@ -15,10 +15,11 @@
  * SwiGLU, combine, unpooler; then the final norm and LM head.
  *
  * Arithmetic: fp64 throughout, rounded to bf16 exactly at the materialisation
- * points listed in or_layer(); the NVFP4 activation quantiser takes its
- * decisions in fp32 (the precision the GPU path uses) with a per-row scale
- * of amax / (6 * 448) rounded up to a power of two, and router logits are
- * rounded to fp32 before the top-k decision.
+ * points listed in or_layer(); the first expert GEMM reads the bf16 pooled
+ * vector as it is; the NVFP4 quantiser of the SwiGLU output (the second expert
+ * GEMM's input) takes its decisions in fp32 (the precision the GPU path uses)
+ * with a per-row scale of amax / (6 * 448) rounded up to a power of two; router
+ * logits are rounded to fp32 before the top-k decision.
  *
  * Layouts (all row-major, bf16 stored as uint16 bit patterns):
  *   w_qkv   [(Hq + 2 Hkv) * D][d]   rows: q heads, then k heads, then v heads

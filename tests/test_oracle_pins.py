@@ -383,12 +383,11 @@ def test_layer_brute_force_tiny():
         e2 = np.array([oracle.e2m1_value(c) for c in range(16)])[nib]
         sc = np.array([oracle.e4m3_value(c) for c in range(256)])[sf]
         return e2 * np.repeat(sc, 16, axis=1) * float(gs)
-    xq = np.stack([oracle.nvfp4_dequant(*oracle.nvfp4_quantize(u[t].astype(np.float32)), P) for t in range(16)])
     Y = np.zeros((E, 16, P))
     for e in range(E):
         W1 = deq(w["w1_codes"][e], w["w1_sf"][e], w["w1_gs"][e], 2 * Fw, P)
         W2 = deq(w["w2_codes"][e], w["w2_sf"][e], w["w2_gs"][e], P, Fw)
-        gv = xq @ W1.T
+        gv = u @ W1.T
         a = (F.silu(torch.from_numpy(gv[:, :Fw])).numpy() * gv[:, Fw:]).astype(np.float32)
         aq = np.stack([oracle.nvfp4_dequant(*oracle.nvfp4_quantize(a[t]), Fw) for t in range(16)])
         Y[e] = _bf(aq @ W2.T)
