@@ -38,7 +38,8 @@ MSM_TIMING_EVENTS = 32
 EV = dict(start=0, pro_in=1, pro_done=2, attn_in=3, attn_done=4, merge_done=5, oproj_in=6, oproj_done=7,
           pool_in=8, pool_done=9, router_in=10, router_done=11, route_topk=12, route_done=13, gemm1_done=14,
           gemm2_in=15, gemm2_done=16, combine_done=17, unpool_in=18, unpool_done=19, tail_in=20, tail_done=21,
-          end=22, loader_routed=23, loader_end=24)
+          end=22, loader_routed=23, loader_end=24, route_dispatch=25,
+          pool_staged=26, xq_row_in=27, xq_row0_done=28, xq_row1_done=29)
 T = 16
 
 EXPORTED = ["msm_model_create", "msm_model_destroy", "msm_verify_step", "msm_verify_step_host", "msm_sync",

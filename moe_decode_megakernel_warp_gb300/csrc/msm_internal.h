@@ -29,7 +29,8 @@ enum TimingEvent : int {
   EV_OPROJ_IN = 6, EV_OPROJ_DONE = 7, EV_POOL_IN = 8, EV_POOL_DONE = 9, EV_ROUTER_IN = 10, EV_ROUTER_DONE = 11,
   EV_ROUTE_TOPK = 12, EV_ROUTE_DONE = 13, EV_GEMM1_DONE = 14, EV_GEMM2_IN = 15, EV_GEMM2_DONE = 16,
   EV_COMBINE_DONE = 17, EV_UNPOOL_IN = 18, EV_UNPOOL_DONE = 19, EV_TAIL_IN = 20, EV_TAIL_DONE = 21, EV_END = 22,
-  EV_LOADER_ROUTED = 23, EV_LOADER_END = 24
+  EV_LOADER_ROUTED = 23, EV_LOADER_END = 24, EV_ROUTE_DISPATCH = 25,
+  EV_POOL_STAGED = 26, EV_XQ_ROW_IN = 27, EV_XQ_ROW0_DONE = 28, EV_XQ_ROW1_DONE = 29
 };
 
 // phases of one layer launch (recorded in the status word on a timeout)

@@ -163,6 +163,29 @@ __device__ __forceinline__ bool poll_f32x2(Ctx& cx, const void* p, uint2& v, int
   return true;
 }
 
+// Poll up to N 16-byte chunks together: every pending chunk is re-read in the same
+// round, so a consumer that arrives before its producers keeps N loads in flight
+// instead of waiting out one round trip per chunk.  `ready` tells whether a chunk
+// holds no sentinel; returns false if the block gave up.
+template <int N, class Ready>
+__device__ __forceinline__ bool poll_batch(Ctx& cx, const uint4* base, int stride, uint4 (&v)[N], uint32_t pending,
+                                           Ready ready, int phase) {
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    if ((pending >> i) & 1u) v[i] = ld_relaxed_v4(base + i * stride);
+  uint32_t n = 0;
+  for (;;) {
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if (((pending >> i) & 1u) && ready(v[i])) pending &= ~(1u << i);
+    if (!pending) return true;
+    if ((++n & 7) == 0 && cx.expired(phase)) return false;
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if ((pending >> i) & 1u) v[i] = ld_relaxed_v4(base + i * stride);
+  }
+}
+
 // one thread per block records: the first compute thread, or the loader lane
 template <bool kTiming>
 __device__ __forceinline__ void stamp(const LaunchParams& P, int block, int ev) {
@@ -396,24 +419,27 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, cons
   const int nch = K / 8;
   float ss = 0.f;
   bool ok = w.ok;
-  // loads are issued in batches of 8 before any is inspected, so their latencies overlap
-  constexpr int kB = 8;
+  // loads are issued in batches of 16 before any is inspected, so their latencies overlap
+  constexpr int kB = 16;
   for (int c0 = sub; c0 < nch && ok; c0 += 16 * kB) {
     uint4 v[kB];
+    const uint4* base = reinterpret_cast<const uint4*>(src + (size_t)t * K + c0 * 8);  // chunk j at base + 16 j
+    uint32_t pending = 0;
 #pragma unroll
-    for (int j = 0; j < kB; ++j) {
-      const int c = c0 + 16 * j;
-      if (c < nch) {
-        const uint16_t* p = src + (size_t)t * K + c * 8;
-        v[j] = poll ? ld_relaxed_v4(p) : *reinterpret_cast<const uint4*>(p);
-      }
+    for (int j = 0; j < kB; ++j)
+      if (c0 + 16 * j < nch) pending |= 1u << j;
+    if (poll) {
+      ok = poll_batch<kB>(cx, base, 16, v, pending, [](const uint4& x) { return bf16x8_ready(x); }, phase);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kB; ++j)
+        if ((pending >> j) & 1u) v[j] = base[16 * j];
     }
+    if (!ok) break;
 #pragma unroll
     for (int j = 0; j < kB; ++j) {
       const int c = c0 + 16 * j;
-      if (c >= nch || !ok) continue;
-      if (poll && !bf16x8_ready(v[j])) ok = poll_bf16x8(cx, src + (size_t)t * K + c * 8, v[j], phase);
-      if (!ok) continue;
+      if (c >= nch) continue;
       const uint32_t wd[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -424,23 +450,33 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, cons
       *reinterpret_cast<uint4*>(cx.S.act + act_off(t, c * 8)) = v[j];
     }
   }
+  if (gain != nullptr && phase == PH_POOL) stamp_rt(*cx.P, EV_POOL_STAGED);
   ok = __all_sync(0xffffffffu, ok);
   if (ok && gain != nullptr) {
 #pragma unroll
     for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float inv = rsqrtf(ss / (float)K + eps);
-    for (int c = sub; c < nch; c += 16) {
-      uint4* sp = reinterpret_cast<uint4*>(cx.S.act + act_off(t, c * 8));
-      uint4 v = *sp;
-      uint4 gv = *reinterpret_cast<const uint4*>(gain + c * 8);
-      uint32_t wd[4] = {v.x, v.y, v.z, v.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
+    for (int c0 = sub; c0 < nch; c0 += 16 * kB) {
+      uint4 gv[kB];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float a = bf16_to_f32((uint16_t)(wd[i] & 0xFFFF)) * inv * bf16_to_f32((uint16_t)(gw[i] & 0xFFFF));
-        float b = bf16_to_f32((uint16_t)(wd[i] >> 16)) * inv * bf16_to_f32((uint16_t)(gw[i] >> 16));
-        wd[i] = pack_bf16x2(a, b);
+      for (int j = 0; j < kB; ++j)
+        if (c0 + 16 * j < nch) gv[j] = __ldg(reinterpret_cast<const uint4*>(gain + (c0 + 16 * j) * 8));
+#pragma unroll
+      for (int j = 0; j < kB; ++j) {
+        const int c = c0 + 16 * j;
+        if (c >= nch) continue;
+        uint4* sp = reinterpret_cast<uint4*>(cx.S.act + act_off(t, c * 8));
+        const uint4 v = *sp;
+        uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t gw[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float a = bf16_to_f32((uint16_t)(wd[i] & 0xFFFF)) * inv * bf16_to_f32((uint16_t)(gw[i] & 0xFFFF));
+          const float b = bf16_to_f32((uint16_t)(wd[i] >> 16)) * inv * bf16_to_f32((uint16_t)(gw[i] >> 16));
+          wd[i] = pack_bf16x2(a, b);
+        }
+        *sp = make_uint4(wd[0], wd[1], wd[2], wd[3]);
       }
-      *sp = make_uint4(wd[0], wd[1], wd[2], wd[3]);
     }
   }
   w.ok = ok;
@@ -602,14 +638,18 @@ __device__ __forceinline__ void attn_keys16(AttnState<D>& st, const uint32_t (&q
     st.o[n][2] *= alpha[1];
     st.o[n][3] *= alpha[1];
   }
-  // P as the sum of two bf16 parts (hi + lo): P.V carries ~16 significant bits of P
-  uint32_t ph[4], pl[4];
+  // P as the sum of three bf16 parts: P.V carries ~24 significant bits of P, as
+  // much as the fp32 softmax itself
+  uint32_t ph[4], pm[4], pl[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float x0 = s[i >> 1][(i & 1) * 2], x1 = s[i >> 1][(i & 1) * 2 + 1];
     const uint32_t h = pack_bf16x2(x0, x1);
+    const float r0 = x0 - bf16_to_f32((uint16_t)(h & 0xFFFFu)), r1 = x1 - bf16_to_f32((uint16_t)(h >> 16));
+    const uint32_t mm = pack_bf16x2(r0, r1);
     ph[i] = h;
-    pl[i] = pack_bf16x2(x0 - bf16_to_f32((uint16_t)(h & 0xFFFFu)), x1 - bf16_to_f32((uint16_t)(h >> 16)));
+    pm[i] = mm;
+    pl[i] = pack_bf16x2(r0 - bf16_to_f32((uint16_t)(mm & 0xFFFFu)), r1 - bf16_to_f32((uint16_t)(mm >> 16)));
   }
 #pragma unroll
   for (int n = 0; n < D / 8; n += 2) {
@@ -619,6 +659,8 @@ __device__ __forceinline__ void attn_keys16(AttnState<D>& st, const uint32_t (&q
     ldsm_x4_t(vbase + swz(key, d0, rows), b0, b1, b2, b3);
     mma_bf16(st.o[n], ph[0], ph[1], ph[2], ph[3], b0, b1);
     mma_bf16(st.o[n + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+    mma_bf16(st.o[n], pm[0], pm[1], pm[2], pm[3], b0, b1);
+    mma_bf16(st.o[n + 1], pm[0], pm[1], pm[2], pm[3], b2, b3);
     mma_bf16(st.o[n], pl[0], pl[1], pl[2], pl[3], b0, b1);
     mma_bf16(st.o[n + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
   }
@@ -1041,13 +1083,19 @@ __device__ void route_phase(Worker& w) {
       P.tree_dbg[16 + tid] = (uint32_t)cx.S.tpos[tid];
     }
   }
-  // NVFP4 activations of the pooled vectors (GEMM1 B operand, f16, one row per token)
+  stamp_rt(P, EV_ROUTE_DISPATCH);
+  // GEMM1 B operand: the bf16 pooled vectors, one row per token, as f16 scaled by a
+  // power of two per row (largest magnitude lands in [2^14, 2^15)).  Every bf16
+  // value within 2^29 of the row's largest is exact in f16, so GEMM1 sees u as it
+  // is; the scale goes back in through x_ts in the GEMM1 epilogue.
   // (the router stage already saw every element of u, so plain relaxed loads suffice here)
   const uint16_t* u = reinterpret_cast<const uint16_t*>(P.x_cur + P.xo.u);
   uint16_t* rowbuf = reinterpret_cast<uint16_t*>(cx.S.act + (size_t)dm.p * 32) + (size_t)w.cw * dm.p;
+  uint8_t* actb = cx.S.act;
   for (int tt = 0; tt < 2 && w.ok; ++tt) {
     const int t = w.cw * 2 + tt;
     const uint16_t* row = u + (size_t)t * dm.p;
+    float amax = 0.f;
     for (int c0 = w.lane; c0 < dm.p / 8; c0 += 32 * 4) {
       uint4 v[4];
 #pragma unroll
@@ -1055,18 +1103,30 @@ __device__ void route_phase(Worker& w) {
         if (c0 + 32 * i < dm.p / 8) v[i] = ld_relaxed_v4(row + (c0 + 32 * i) * 8);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        if (c0 + 32 * i < dm.p / 8) *reinterpret_cast<uint4*>(rowbuf + (c0 + 32 * i) * 8) = v[i];
+        if (c0 + 32 * i < dm.p / 8) {
+          *reinterpret_cast<uint4*>(rowbuf + (c0 + 32 * i) * 8) = v[i];
+          const uint32_t wd[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_to_f32((uint16_t)(wd[j] & 0xFFFF))),
+                                     fabsf(bf16_to_f32((uint16_t)(wd[j] >> 16)))));
+        }
     }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     __syncwarp();
-    uint8_t* act = cx.S.act;
-    float ts = nvfp4_row(
-        dm.p, w.lane, [&](int i) { return bf16_to_f32(rowbuf[i]); },
-        [&](int b, int j, uint32_t h2) {
-          const int k = b * 16 + j;
-          *reinterpret_cast<uint32_t*>(act + act_off(t, k) + (k & 7) * 2) = h2;
-        });
-    if (w.lane == 0) cx.S.x_ts[t] = ts;
+    if (tt == 0) stamp_rt(P, EV_XQ_ROW_IN);
+    int ex = 0;
+    if (amax > 0.f) frexpf(amax, &ex);  // amax = m 2^ex, m in [0.5, 1)
+    const float up = ldexpf(1.0f, 15 - ex);
+    for (int k = w.lane * 2; k < dm.p; k += 64) {
+      const uint32_t pr = *reinterpret_cast<const uint32_t*>(rowbuf + k);
+      const float lo = bf16_to_f32((uint16_t)(pr & 0xFFFF)) * up, hi = bf16_to_f32((uint16_t)(pr >> 16)) * up;
+      *reinterpret_cast<uint32_t*>(actb + act_off(t, k) + (k & 7) * 2) = pack_f16x2(lo, hi);
+    }
+    if (w.lane == 0) cx.S.x_ts[t] = ldexpf(1.0f, ex - 15);
     __syncwarp();
+    stamp_rt(P, tt == 0 ? EV_XQ_ROW0_DONE : EV_XQ_ROW1_DONE);
   }
   cbar();
   if (*cx.S.abort) w.ok = false;
