@@ -212,8 +212,8 @@ msm_status msm_get_tree(msm_model* model, uint32_t* anc, int32_t* tpos);
  *   15 GEMM2 in, 16 GEMM2 done, 17 combine done, 18 unpooler in, 19 unpooler done,
  *   20 tail in, 21 tail done, 22 end, 23 loader saw the routing, 24 loader done,
  *   25 expert dispatch built, 26 pooler input staged (before its norm), 27 first
- *   activation row read for NVFP4 quantisation, 28 / 29 first / second row of
- *   the first compute warp quantised.
+ *   pooled row read for GEMM1, 28 / 29 first / second GEMM1 input row of the
+ *   first compute warp staged.
  * `n` is the capacity of `buf` in elements. */
 #define MSM_TIMING_EVENTS 32
 msm_status msm_get_timing(msm_model* model, uint64_t* buf, size_t n);
