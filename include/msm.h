@@ -187,6 +187,48 @@ msm_status msm_verify_step_host(msm_model* model, const void* hidden_in_host,
                                 void* const* v_cache, float* logits_host, void* hidden_out_host,
                                 void* stream);
 
+/*
+ * msm_verify_step_noalloc: the verify step of msm_verify_step (same arguments,
+ * same results, bit for bit) with its per-step scratch taken from a fixed
+ * static device array instead of the model's own buffers.  The pages describe
+ * no such entry point; it has no counterpart there.
+ *
+ * Who needs it: callers that must not allocate device memory at the time they
+ * run a step -- for instance code under a strict device-memory budget, or code
+ * that pre-plans all of its memory and forbids allocation on the decode path.
+ * On success this call allocates nothing: no cudaMalloc / cudaFree, no
+ * allocating library call.  (msm_verify_step allocates nothing per step either,
+ * but it uses exchange buffers that msm_model_create allocated for the model;
+ * this entry point uses the static array instead.)
+ *
+ * Scratch: MSM_NOALLOC_SCRATCH_BYTES (10 MiB) of __device__ memory per device,
+ * shared by every model on that device.  A step needs
+ *   2 * exchange + attention/expert partials + 2 * (16 n_q_heads head_dim * 2)
+ *   + 2 * (16 d_model * 2) bytes (each part rounded up to 256 bytes), about
+ * 8.2 MiB at d_model 4096, 32/8 heads of 128, pool_dim 2048, ffn_dim 1024,
+ * top-8 on 152 SMs.  A model whose step needs more is rejected with
+ * MSM_ERR_UNSUPPORTED and a message giving both sizes; nothing is launched.
+ * The exchange part must hold its empty sentinels when a step starts; every
+ * call arms it on `stream` before its first layer launch, so no state carries
+ * over from an earlier call, a failed step or another model.
+ *
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current).  Make that first call
+ * before any stream capture is begun on the calling thread.
+ *
+ * Concurrency: the scratch is one array per device.  Calls that overlap on the
+ * device (from other threads, or on other streams of the same device before the
+ * previous call's work has finished) race on it and give wrong results.
+ * Serialise them, e.g. by issuing them on one stream.
+ *
+ * Device-side failures are reported by the next msm_sync(), as for
+ * msm_verify_step.
+ */
+#define MSM_NOALLOC_SCRATCH_BYTES (10u << 20)
+msm_status msm_verify_step_noalloc(msm_model* model, const void* hidden_in, const int32_t* parent,
+                                   int32_t pos0, void* const* k_cache, void* const* v_cache,
+                                   float* logits_out, void* hidden_out, void* stream);
+
 /* Wait for `stream`, then return (and clear) the device status latched by the
  * model's launches.  After MSM_ERR_DEVICE_TIMEOUT the model re-arms its exchange
  * buffers, so the next step starts clean. */

@@ -44,7 +44,9 @@ T = 16
 
 EXPORTED = ["msm_model_create", "msm_model_destroy", "msm_verify_step", "msm_verify_step_host", "msm_sync",
             "msm_get_routing", "msm_get_tree", "msm_get_timing", "msm_get_stats", "msm_get_exchange",
-            "msm_draft_step", "msm_last_error"]
+            "msm_draft_step", "msm_last_error", "msm_verify_step_noalloc"]
+# capacity of the static scratch array behind msm_verify_step_noalloc (MSM_NOALLOC_SCRATCH_BYTES)
+MSM_NOALLOC_SCRATCH_BYTES = 10 << 20
 
 
 def _nvcc():
@@ -134,6 +136,8 @@ def lib():
             L.msm_verify_step.restype = st
             L.msm_verify_step_host.argtypes = [vp, vp, ctypes.POINTER(i32), i32, _PP, _PP, vp, vp, vp]
             L.msm_verify_step_host.restype = st
+            L.msm_verify_step_noalloc.argtypes = [vp, vp, ctypes.POINTER(i32), i32, _PP, _PP, vp, vp, vp]
+            L.msm_verify_step_noalloc.restype = st
             L.msm_sync.argtypes = [vp, vp]
             L.msm_sync.restype = st
             L.msm_get_routing.argtypes = [vp, vp, vp]
@@ -196,6 +200,15 @@ def msm_verify_step(model, hidden_in, parent, pos0, k_ptrs, v_ptrs, logits_out, 
     vpp, _va = _ptr_array(v_ptrs)
     return lib().msm_verify_step(model, ctypes.c_void_p(hidden_in), _i32_array(parent), int(pos0), kp, vpp,
                                  ctypes.c_void_p(logits_out), ctypes.c_void_p(hidden_out), ctypes.c_void_p(stream))
+
+
+def msm_verify_step_noalloc(model, hidden_in, parent, pos0, k_ptrs, v_ptrs, logits_out, hidden_out,
+                            stream=0) -> int:
+    kp, _ka = _ptr_array(k_ptrs)
+    vpp, _va = _ptr_array(v_ptrs)
+    return lib().msm_verify_step_noalloc(model, ctypes.c_void_p(hidden_in), _i32_array(parent), int(pos0), kp,
+                                         vpp, ctypes.c_void_p(logits_out), ctypes.c_void_p(hidden_out),
+                                         ctypes.c_void_p(stream))
 
 
 def msm_verify_step_host(model, hidden_in_host, parent, pos0, k_ptrs, v_ptrs, logits_host, hidden_out_host,
@@ -295,6 +308,14 @@ class Model:
                                       [k.data_ptr() for k in k_caches], [v.data_ptr() for v in v_caches],
                                       logits_out.data_ptr() if logits_out is not None else 0,
                                       hidden_out.data_ptr() if hidden_out is not None else 0, stream))
+
+    def verify_step_noalloc(self, hidden_in, parent, pos0, k_caches, v_caches, logits_out=None, hidden_out=None,
+                            stream=0):
+        """msm_verify_step on the library's static scratch array (no device allocation)."""
+        return _check(msm_verify_step_noalloc(self.handle, hidden_in.data_ptr(), parent, pos0,
+                                              [k.data_ptr() for k in k_caches], [v.data_ptr() for v in v_caches],
+                                              logits_out.data_ptr() if logits_out is not None else 0,
+                                              hidden_out.data_ptr() if hidden_out is not None else 0, stream))
 
     def verify_step_host(self, hidden_in_host, parent, pos0, k_caches, v_caches, logits_host=None,
                          hidden_out_host=None, stream=0):

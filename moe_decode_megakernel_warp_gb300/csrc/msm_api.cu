@@ -13,6 +13,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -609,3 +610,187 @@ msm_status msm_draft_step(msm_model* m, const void* draft_hidden_in, int32_t* to
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// verify step on static scratch (msm_verify_step_noalloc)
+// ---------------------------------------------------------------------------
+// The per-step scratch of the layer kernel (exchange buffers of both parities,
+// attention and expert partials, the layer-to-layer q / hidden hand-off) lives
+// in this array instead of model-owned allocations.  One array per device,
+// shared by every model: overlapping calls race on it (stated in msm.h).
+static __device__ __align__(256) unsigned char msm_noalloc_scratch[MSM_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+unsigned char* g_noalloc_base[kNoAllocMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// device address of the array on `device` (current); looked up once per device
+msm_status noalloc_base(int device, unsigned char** base) {
+  if (device < 0 || device >= kNoAllocMaxDevices) return fail(MSM_ERR_UNSUPPORTED, "device index above 63");
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_base[device]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, msm_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    if (!p) return fail(MSM_ERR_CUDA, "cudaGetSymbolAddress(static scratch) returned NULL");
+    g_noalloc_base[device] = static_cast<unsigned char*>(p);
+  }
+  *base = g_noalloc_base[device];
+  return MSM_OK;
+}
+}  // namespace
+
+extern "C" msm_status msm_verify_step_noalloc(msm_model* m, const void* hidden_in, const int32_t* parent,
+                                              int32_t pos0, void* const* k_cache, void* const* v_cache,
+                                              float* logits_out, void* hidden_out, void* stream) {
+  if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
+  const Dims& dm = m->dm;
+  if (!hidden_in || !k_cache || !v_cache) return fail(MSM_ERR_INVALID_ARG, "NULL hidden_in or cache array");
+  if (!parent_valid(parent)) return fail(MSM_ERR_INVALID_ARG, "parent must satisfy parent[0] == -1, 0 <= parent[i] < i");
+  if (pos0 < 0 || (int64_t)pos0 + T > dm.max_ctx) return fail(MSM_ERR_INVALID_ARG, "pos0 out of range");
+  if (dm.vocab > 0 && !logits_out) return fail(MSM_ERR_INVALID_ARG, "logits_out is NULL but vocab > 0");
+  if (dm.vocab == 0 && !hidden_out) return fail(MSM_ERR_INVALID_ARG, "hidden_out is NULL but vocab == 0");
+  if ((reinterpret_cast<uintptr_t>(hidden_in) & 15) || (reinterpret_cast<uintptr_t>(hidden_out) & 15) ||
+      (reinterpret_cast<uintptr_t>(logits_out) & 15))
+    return fail(MSM_ERR_INVALID_ARG, "hidden / logits buffers must be 16-byte aligned");
+  for (int l = 0; l < dm.n_layers; ++l) {
+    if (!k_cache[l] || !v_cache[l]) return fail(MSM_ERR_INVALID_ARG, "NULL KV cache pointer");
+    if ((reinterpret_cast<uintptr_t>(k_cache[l]) & 15) || (reinterpret_cast<uintptr_t>(v_cache[l]) & 15))
+      return fail(MSM_ERR_INVALID_ARG, "KV caches must be 16-byte aligned");
+  }
+  // carve: x[0] | x[1] | partials | in_q[0] | in_q[1] | in_h[0] | in_h[1]
+  const uint64_t q_bytes = align256((uint64_t)T * dm.hq * dm.hd * 2), h_bytes = align256((uint64_t)T * dm.d * 2);
+  const uint64_t need = 2 * m->xo.total + m->so.total + 2 * q_bytes + 2 * h_bytes;
+  if (need > (uint64_t)MSM_NOALLOC_SCRATCH_BYTES) {
+    char buf[200];
+    std::snprintf(buf, sizeof(buf),
+                  "msm_verify_step_noalloc: this model's step needs %llu bytes of scratch; the static array holds "
+                  "%llu (MSM_NOALLOC_SCRATCH_BYTES)",
+                  (unsigned long long)need, (unsigned long long)MSM_NOALLOC_SCRATCH_BYTES);
+    return fail(MSM_ERR_UNSUPPORTED, buf);
+  }
+  CK(cudaSetDevice(m->device));
+  unsigned char* base = nullptr;
+  msm_status st = noalloc_base(m->device, &base);
+  if (st != MSM_OK) return st;
+  uint8_t* xs[2] = {base, base + m->xo.total};
+  uint8_t* sb = base + 2 * m->xo.total;
+  uint16_t* iq[2] = {reinterpret_cast<uint16_t*>(sb + m->so.total),
+                     reinterpret_cast<uint16_t*>(sb + m->so.total + q_bytes)};
+  uint16_t* ih[2] = {reinterpret_cast<uint16_t*>(sb + m->so.total + 2 * q_bytes),
+                     reinterpret_cast<uint16_t*>(sb + m->so.total + 2 * q_bytes + h_bytes)};
+  for (int l = 0; l < dm.n_layers; ++l) {
+    if (m->tmk_ptr[l] != k_cache[l]) {
+      st = encode_kv_map(m, &m->tmk[l], k_cache[l]);
+      if (st != MSM_OK) return st;
+      m->tmk_ptr[l] = k_cache[l];
+    }
+    if (m->tmv_ptr[l] != v_cache[l]) {
+      st = encode_kv_map(m, &m->tmv[l], v_cache[l]);
+      if (st != MSM_OK) return st;
+      m->tmv_ptr[l] = v_cache[l];
+    }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // arm the exchange part with its sentinels (bf16 0xFFFF, fp32 -0.0) on the caller's stream
+  const XOffsets& o = m->xo;
+  for (int c = 0; c < 2; ++c) {
+    CK(launch_fill_u32(xs[c], o.logits / 4, 0xFFFFFFFFu, s));
+    CK(launch_fill_u32(xs[c] + o.logits, (o.z - o.logits) / 4, 0x80000000u, s));
+    CK(launch_fill_u32(xs[c] + o.z, (o.total - o.z) / 4, 0xFFFFFFFFu, s));
+  }
+  CK(launch_fill_u32(sb, m->so.y / 4, 0x80000000u, s));
+  CK(launch_fill_u32(sb + m->so.y, (m->so.total - m->so.y) / 4, 0xFFFFFFFFu, s));
+
+  const uint64_t tmo = (uint64_t)(m->cfg.timeout_us ? m->cfg.timeout_us : 200000u) * 1000ull;
+  const int sp = (int)(m->step_count & 1);
+  LaunchParams P;
+  std::memset(&P, 0, sizeof(P));
+  P.dm = dm;
+  P.xo = m->xo;
+  P.so = m->so;
+  P.s_buf = sb;
+  P.rope = m->rope;
+  P.inv_freq = m->inv_freq;
+  P.tree_dbg = m->tree_dbg;
+  P.status = m->status;
+  P.pos0 = pos0;
+  P.ring_bytes = m->ring_bytes;
+  P.act_bytes = m->act_bytes;
+  P.flags = m->cfg.flags;
+  P.timeout_ns_lo = (uint32_t)tmo;
+  P.timeout_ns_hi = (uint32_t)(tmo >> 32);
+  P.prefetch_experts = m->cfg.prefetch_experts > 0 ? m->cfg.prefetch_experts : 14;
+  P.phase_rot = 13;
+  std::memcpy(P.parent, parent, sizeof(int32_t) * T);
+  P.hidden_in = static_cast<const uint16_t*>(hidden_in);
+  P.logits = logits_out;
+  const bool timing = (m->cfg.flags & MSM_FLAG_SELF_TIMING) != 0;
+  const bool pdl = (m->cfg.flags & MSM_FLAG_PDL) != 0;
+  for (int l = 0; l < dm.n_layers; ++l) {
+    const LayerPack& lp = m->L[l];
+    const bool first = l == 0, last = l == dm.n_layers - 1;
+    const int c = l & 1;  // both parities were armed above
+    P.layer = l;
+    P.first = first;
+    P.last = last;
+    P.is_global = m->global[l] != 0;
+    P.next_global = last ? 0 : (m->global[l + 1] != 0);
+    P.w_qkv_pro = first ? lp.qkv : nullptr;
+    P.g_attn_pro = first ? lp.g_attn : nullptr;
+    P.w_o = lp.o;
+    P.w_pool = lp.pool;
+    P.w_router = lp.router;
+    P.b_router = lp.b;
+    P.w_unpool = lp.unpool;
+    P.g_moe = lp.g_moe;
+    P.w1 = lp.w1;
+    P.w2 = lp.w2;
+    P.w1_gs = lp.w1gs;
+    P.w2_gs = lp.w2gs;
+    P.w_tail = last ? m->lm : m->L[l + 1].qkv;
+    P.g_tail = last ? m->g_final : m->L[l + 1].g_attn;
+    P.hidden_out = last ? static_cast<uint16_t*>(hidden_out) : nullptr;
+    P.kc = static_cast<uint16_t*>(k_cache[l]);
+    P.vc = static_cast<uint16_t*>(v_cache[l]);
+    P.kc_next = last ? nullptr : static_cast<uint16_t*>(k_cache[l + 1]);
+    P.vc_next = last ? nullptr : static_cast<uint16_t*>(v_cache[l + 1]);
+    P.kc_pf = P.kc_next;
+    P.vc_pf = P.vc_next;
+    P.x_cur = xs[c];
+    P.x_next = xs[c ^ 1];
+    P.in_q = iq[c];
+    P.in_h = ih[c];
+    P.out_q = iq[c ^ 1];
+    P.out_h = ih[c ^ 1];
+    P.routing_idx = m->routing_idx + (size_t)l * T * dm.k;
+    P.routing_w = m->routing_w + (size_t)l * T * dm.k;
+    P.hist_cur = m->hist + ((size_t)sp * dm.n_layers + l) * dm.e;
+    P.hist_prev = m->step_count > 0 ? m->hist + ((size_t)(sp ^ 1) * dm.n_layers + l) * dm.e : nullptr;
+    P.timing = m->timing + (size_t)l * m->G * kTimingEvents;
+    P.tmap_k = m->tmk[l];
+    P.tmap_v = m->tmv[l];
+
+    cudaLaunchConfig_t lc;
+    std::memset(&lc, 0, sizeof(lc));
+    lc.gridDim = dim3(m->G);
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = m->smem_bytes;
+    lc.stream = s;
+    cudaLaunchAttribute attr[1];
+    int na = 0;
+    if (pdl && !first) {
+      attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[na].val.programmaticStreamSerializationAllowed = 1;
+      ++na;
+    }
+    lc.attrs = na ? attr : nullptr;
+    lc.numAttrs = na;
+    void* args[] = {&P};
+    cudaError_t e = cudaLaunchKernelExC(&lc, layer_kernel(timing), args);
+    if (e != cudaSuccess) return cuda_fail(e, "layer kernel launch");
+  }
+  ++m->step_count;
+  return MSM_OK;
+}

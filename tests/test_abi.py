@@ -36,6 +36,13 @@ def test_null_arguments_are_rejected_without_a_device():
     assert msm.msm_sync(None) == msm.MSM_ERR_INVALID_ARG
     assert lib.msm_get_stats(None, None) == msm.MSM_ERR_INVALID_ARG
     assert msm.msm_draft_step(None) == msm.MSM_ERR_UNSUPPORTED
+    assert msm.msm_verify_step_noalloc(None, 0, list(range(-1, 15)), 0, [0], [0], 0, 0) == msm.MSM_ERR_INVALID_ARG
+
+
+def test_noalloc_scratch_capacity_matches_the_header():
+    src = open(os.path.join(ROOT, "include", "msm.h")).read()
+    m = re.search(r"#define MSM_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", src)
+    assert m and int(m.group(1)) << int(m.group(2)) == msm.MSM_NOALLOC_SCRATCH_BYTES
 
 
 def _config(**kw):
