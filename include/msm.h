@@ -109,6 +109,11 @@ typedef struct {
   int attn_splits;  /* KV splits per kv head; 0 = automatic */
   int prefetch_experts; /* experts prefetched by MSM_FLAG_EXPERT_PREFETCH; 0 = 14 */
   uint32_t timeout_us;  /* bounded-wait limit; 0 = 200000 */
+  int l2_runahead_kb;   /* L2 prefetch distance of each block's weight / KV stream, KiB;
+                           0 = off (alphasignal.ai, § "Four mechanisms keep work
+                           moving": weights for the next operation are fetched while
+                           the current one runs, partly staged in L2).  Measured
+                           slower than off on the 62-layer workload, hence off. */
 } msm_config;
 
 /* Device pointers, one per layer (host arrays of n_layers entries). */
@@ -255,9 +260,15 @@ msm_status msm_get_tree(msm_model* model, uint32_t* anc, int32_t* tpos);
  *   20 tail in, 21 tail done, 22 end, 23 loader saw the routing, 24 loader done,
  *   25 expert dispatch built, 26 pooler input staged (before its norm), 27 first
  *   pooled row read for GEMM1, 28 / 29 first / second GEMM1 input row of the
- *   first compute warp staged.
+ *   first compute warp staged, 30 pooler input normalised by the first compute
+ *   warp, 31 pooler norm gain in shared memory; 32-39 o_proj units 0 and 1 of the block (first tile ready, last tile
+ *   ready, partial sums stored, epilogue done), 40-43 GEMM1 of the first compute
+ *   warp (first unit's tile ready / unit done, last unit's tile ready / done),
+ *   44 / 45 loader issued the first / last o_proj tile, 46 / 47 the first / last
+ *   GEMM1 tile; 48 + w / 56 + w compute warp w has staged its part of the pooler /
+ *   o_proj input.
  * `n` is the capacity of `buf` in elements. */
-#define MSM_TIMING_EVENTS 32
+#define MSM_TIMING_EVENTS 64
 msm_status msm_get_timing(msm_model* model, uint64_t* buf, size_t n);
 
 msm_status msm_get_stats(const msm_model* model, msm_stats* out);

@@ -33,13 +33,17 @@ MSM_FLAG_EXPERT_PREFETCH = 0x2
 MSM_FLAG_KV_PREFETCH = 0x4
 MSM_FLAG_PDL = 0x8
 MSM_FLAG_TEST_DROP_HANDOFF = 0x10000
-MSM_TIMING_EVENTS = 32
+MSM_TIMING_EVENTS = 64
 # self-timing event ids (see msm.h)
 EV = dict(start=0, pro_in=1, pro_done=2, attn_in=3, attn_done=4, merge_done=5, oproj_in=6, oproj_done=7,
           pool_in=8, pool_done=9, router_in=10, router_done=11, route_topk=12, route_done=13, gemm1_done=14,
           gemm2_in=15, gemm2_done=16, combine_done=17, unpool_in=18, unpool_done=19, tail_in=20, tail_done=21,
           end=22, loader_routed=23, loader_end=24, route_dispatch=25,
-          pool_staged=26, xq_row_in=27, xq_row0_done=28, xq_row1_done=29)
+          pool_staged=26, xq_row_in=27, xq_row0_done=28, xq_row1_done=29, pool_normed=30, pool_gain=31,
+          op_u0_first=32, op_u0_last=33, op_u0_red=34, op_u0_epi=35, op_u1_first=36, op_u1_last=37,
+          op_u1_red=38, op_u1_epi=39, g1_first_ready=40, g1_first_done=41, g1_last_ready=42, g1_last_done=43,
+          ld_op_first=44, ld_op_last=45, ld_g1_first=46, ld_g1_last=47,
+          **{"pool_w%d" % i: 48 + i for i in range(8)}, **{"op_w%d" % i: 56 + i for i in range(8)})
 T = 16
 
 EXPORTED = ["msm_model_create", "msm_model_destroy", "msm_verify_step", "msm_verify_step_host", "msm_sync",
@@ -96,7 +100,7 @@ class MsmConfig(ctypes.Structure):
         ("layer_is_global", ctypes.POINTER(ctypes.c_uint8)),
         ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("flags", ctypes.c_uint32),
         ("grid_blocks", ctypes.c_int), ("attn_splits", ctypes.c_int), ("prefetch_experts", ctypes.c_int),
-        ("timeout_us", ctypes.c_uint32)]
+        ("timeout_us", ctypes.c_uint32), ("l2_runahead_kb", ctypes.c_int)]
 
 
 _PP = ctypes.POINTER(ctypes.c_void_p)
@@ -262,7 +266,7 @@ class Model:
     model keeps packed copies."""
 
     def __init__(self, dims, layers, final=None, device=0, flags=MSM_FLAG_PDL, grid_blocks=0,
-                 attn_splits=0, prefetch_experts=0, timeout_us=0):
+                 attn_splits=0, prefetch_experts=0, timeout_us=0, l2_runahead_kb=0):
         self.dims = dims
         L = dims.n_layers
         self._glob = (ctypes.c_uint8 * L)(*[1 if dims.is_global(l) else 0 for l in range(L)])
@@ -272,7 +276,7 @@ class Model:
                         layer_is_global=ctypes.cast(self._glob, ctypes.POINTER(ctypes.c_uint8)),
                         rms_eps=dims.rms_eps, rope_theta=dims.rope_theta, flags=flags,
                         grid_blocks=grid_blocks, attn_splits=attn_splits, prefetch_experts=prefetch_experts,
-                        timeout_us=timeout_us)
+                        timeout_us=timeout_us, l2_runahead_kb=l2_runahead_kb)
         keep = []
 
         def arr(key):

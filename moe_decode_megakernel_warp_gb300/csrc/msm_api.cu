@@ -120,6 +120,8 @@ msm_status validate_config(const msm_config* c) {
   if (c->top_k > kMaxTopK) return fail(MSM_ERR_UNSUPPORTED, "top_k > 8");
   if (c->n_experts > kMaxExperts || c->n_experts % 16) return fail(MSM_ERR_UNSUPPORTED, "n_experts must be <= 256 and a multiple of 16");
   if (c->vocab % 16) return fail(MSM_ERR_UNSUPPORTED, "vocab must be a multiple of 16");
+  if (c->l2_runahead_kb < 0 || c->l2_runahead_kb > (1 << 20))
+    return fail(MSM_ERR_INVALID_ARG, "config: l2_runahead_kb outside [0, 1 GiB]");
   if (c->grid_blocks < 0 || c->attn_splits < 0 || c->prefetch_experts < 0)
     return fail(MSM_ERR_INVALID_ARG, "config: negative grid_blocks / attn_splits / prefetch_experts");
   return MSM_OK;
@@ -425,6 +427,7 @@ msm_status msm_verify_step(msm_model* m, const void* hidden_in, const int32_t* p
   P.timeout_ns_lo = (uint32_t)tmo;
   P.timeout_ns_hi = (uint32_t)(tmo >> 32);
   P.prefetch_experts = m->cfg.prefetch_experts > 0 ? m->cfg.prefetch_experts : 14;
+  P.runahead_bytes = m->cfg.l2_runahead_kb > 0 ? (uint32_t)m->cfg.l2_runahead_kb * 1024u : 0u;
   P.phase_rot = 13;
   std::memcpy(P.parent, parent, sizeof(int32_t) * T);
   P.hidden_in = static_cast<const uint16_t*>(hidden_in);
@@ -722,6 +725,7 @@ extern "C" msm_status msm_verify_step_noalloc(msm_model* m, const void* hidden_i
   P.timeout_ns_lo = (uint32_t)tmo;
   P.timeout_ns_hi = (uint32_t)(tmo >> 32);
   P.prefetch_experts = m->cfg.prefetch_experts > 0 ? m->cfg.prefetch_experts : 14;
+  P.runahead_bytes = m->cfg.l2_runahead_kb > 0 ? (uint32_t)m->cfg.l2_runahead_kb * 1024u : 0u;
   P.phase_rot = 13;
   std::memcpy(P.parent, parent, sizeof(int32_t) * T);
   P.hidden_in = static_cast<const uint16_t*>(hidden_in);

@@ -84,6 +84,13 @@ __device__ __forceinline__ void named_bar(int id, int threads) {
 }
 
 // ---- relaxed gpu-scope global accesses (data-as-flag exchange) ------------------------
+// read-only load issued exactly where it stands in the program (volatile asm is not
+// moved past the polling loads that follow it)
+__device__ __forceinline__ uint4 ld_nc_v4_early(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
 __device__ __forceinline__ uint4 ld_relaxed_v4(const void* p) {
   uint4 v;
   asm volatile("ld.relaxed.gpu.global.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -19,7 +19,7 @@ constexpr int kKStepBytes = 512;      // one 16x16 bf16 (or f16) block in ldmatr
 constexpr int kExpGroupBytes = 576;   // 16 rows x 64 columns NVFP4: 512 B codes + 64 B scales
 constexpr int kSmallBytes = 16 * 1024; // barriers, routing tables, scratch, dense partials
 constexpr int kMaxSmem = 232448;      // 227 KB opt-in dynamic shared memory per block
-constexpr int kTimingEvents = 32;
+constexpr int kTimingEvents = 64;
 constexpr int kMaxTopK = 8;
 constexpr int kMaxExperts = 256;
 
@@ -30,7 +30,16 @@ enum TimingEvent : int {
   EV_ROUTE_TOPK = 12, EV_ROUTE_DONE = 13, EV_GEMM1_DONE = 14, EV_GEMM2_IN = 15, EV_GEMM2_DONE = 16,
   EV_COMBINE_DONE = 17, EV_UNPOOL_IN = 18, EV_UNPOOL_DONE = 19, EV_TAIL_IN = 20, EV_TAIL_DONE = 21, EV_END = 22,
   EV_LOADER_ROUTED = 23, EV_LOADER_END = 24, EV_ROUTE_DISPATCH = 25,
-  EV_POOL_STAGED = 26, EV_XQ_ROW_IN = 27, EV_XQ_ROW0_DONE = 28, EV_XQ_ROW1_DONE = 29
+  EV_POOL_STAGED = 26, EV_XQ_ROW_IN = 27, EV_XQ_ROW0_DONE = 28, EV_XQ_ROW1_DONE = 29,
+  EV_POOL_NORMED = 30, EV_POOL_GAIN = 31,
+  // finer stamps: o_proj units 0 / 1 of the block (first tile ready, last tile ready,
+  // partial sums stored, epilogue done), GEMM1 of the first compute warp, and the loader
+  EV_OP_U0_FIRST = 32, EV_OP_U0_LAST = 33, EV_OP_U0_RED = 34, EV_OP_U0_EPI = 35,
+  EV_OP_U1_FIRST = 36, EV_OP_U1_LAST = 37, EV_OP_U1_RED = 38, EV_OP_U1_EPI = 39,
+  EV_G1_FIRST_READY = 40, EV_G1_FIRST_DONE = 41, EV_G1_LAST_READY = 42, EV_G1_LAST_DONE = 43,
+  EV_LD_OP_FIRST = 44, EV_LD_OP_LAST = 45, EV_LD_G1_FIRST = 46, EV_LD_G1_LAST = 47,
+  // staging of the pooler input (48 + warp) and of the o_proj input (56 + warp) done, per compute warp
+  EV_POOL_WARP_STAGED = 48, EV_OP_WARP_STAGED = 56
 };
 
 // phases of one layer launch (recorded in the status word on a timeout)
@@ -124,6 +133,7 @@ struct LaunchParams {
   uint32_t flags;
   uint32_t timeout_ns_lo, timeout_ns_hi;
   int prefetch_experts;
+  uint32_t runahead_bytes;  // L2 run-ahead of the loader's stream; 0 = off
   int phase_rot;
   int32_t parent[16];
   // KV cache tensor maps of this layer: 3-D {hd, max_ctx, hkv}, 128-byte swizzle

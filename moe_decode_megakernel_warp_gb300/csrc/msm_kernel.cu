@@ -89,7 +89,7 @@ struct Ctx {
   uint64_t deadline;
   int block;
 
-  __device__ void fail(int phase) {
+  __device__ __noinline__ void fail(int phase) {
     *S.abort = 1;
     if (atomicCAS(&P->status->code, 0, 4 /* MSM_ERR_DEVICE_TIMEOUT */) == 0) {
       P->status->phase = phase;
@@ -233,11 +233,52 @@ __device__ __forceinline__ AttnUnit attn_unit(const LaunchParams& P, int bb, int
 // ---------------------------------------------------------------------------
 // the variable-size shared-memory ring (producer side)
 // ---------------------------------------------------------------------------
+// L2 run-ahead: the byte ranges the block's loader will stream, in stream order.
+// A cursor keeps cp.async.bulk.prefetch.L2 requests up to `ahead` bytes in front
+// of what the ring has issued, so HBM keeps streaming while the ring waits on
+// its consumers (weights and KV history do not depend on the computation; the
+// expert ranges are appended once the routing is known).  A hint only: ranges
+// that do not fit the table are simply not prefetched.
+constexpr int kMaxRanges = 24;
+struct RunAhead {
+  const uint8_t* p[kMaxRanges];
+  uint32_t n[kMaxRanges];
+  int count, i;
+  uint32_t off;
+  uint64_t pref, used;
+  uint32_t ahead;  // 0 = off
+  __device__ void init(uint32_t a) {
+    count = i = 0;
+    off = 0;
+    pref = used = 0;
+    ahead = a;
+  }
+  __device__ void add(const void* ptr, uint64_t bytes) {
+    if (!ahead || bytes == 0 || count == kMaxRanges) return;
+    p[count] = static_cast<const uint8_t*>(ptr);
+    n[count] = (uint32_t)bytes;
+    ++count;
+  }
+  __device__ void pump() {
+    while (i < count && pref < used + ahead) {
+      const uint32_t c = min(n[i] - off, 65536u);
+      prefetch_l2(p[i] + off, c);
+      off += c;
+      pref += c;
+      if (off == n[i]) {
+        ++i;
+        off = 0;
+      }
+    }
+  }
+};
+
 struct Ring {
   uint32_t issued;  // tiles issued
   uint32_t tail;    // oldest tile not known to be released
   uint32_t head;    // next free byte
   uint32_t off[kSlots], end[kSlots];
+  RunAhead ra;
 };
 
 __device__ bool ring_place(Ctx& cx, Ring& r, uint32_t bytes, uint32_t& off_out) {
@@ -283,6 +324,8 @@ __device__ bool ring_issue(Ctx& cx, Ring& r, const Seg* seg, int nseg, uint64_t 
     o += seg[i].bytes;
   }
   ++r.issued;
+  r.ra.used += total;
+  r.ra.pump();
   return true;
 }
 
@@ -304,10 +347,21 @@ __device__ bool ring_issue_kv(Ctx& cx, Ring& r, int hk, int row, uint32_t tile_b
     tma_load_3d(dst + (halves + h) * R * 128, &P.tmap_v, h * 64, row, hk, &cx.S.full[s]);
   }
   ++r.issued;
+  r.ra.used += tile_bytes;
+  r.ra.pump();
   return true;
 }
 
-__device__ bool load_dense(Ctx& cx, Ring& r, const uint8_t* W, int K, int N, int rot, uint64_t pol) {
+// the contiguous bytes of this block's units of a dense weight (see load_dense)
+__device__ void add_dense_range(RunAhead& ra, const uint8_t* W, int K, int N, int rot) {
+  int lo, hi;
+  unit_range(N / 16, rot_block(blockIdx.x, rot, gridDim.x), gridDim.x, lo, hi);
+  const uint64_t ub = dense_unit_bytes(K);
+  ra.add(W + (uint64_t)lo * ub, (uint64_t)(hi - lo) * ub);
+}
+
+__device__ bool load_dense(Ctx& cx, Ring& r, const uint8_t* W, int K, int N, int rot, uint64_t pol,
+                           int trace = -1) {
   const LaunchParams& P = *cx.P;
   const int G = gridDim.x;
   int lo, hi;
@@ -319,6 +373,8 @@ __device__ bool load_dense(Ctx& cx, Ring& r, const uint8_t* W, int K, int N, int
       int ns = min(kDenseTileSteps, steps - k0);
       Seg sg = {W + (uint64_t)u * ub + (uint64_t)k0 * kKStepBytes, (uint32_t)ns * kKStepBytes};
       if (!ring_issue(cx, r, &sg, 1, pol)) return false;
+      if (trace >= 0 && (P.flags & 0x1u) && ((u == lo && k0 == 0) || (u == hi - 1 && k0 + kDenseTileSteps >= steps)))
+        P.timing[(size_t)cx.block * kTimingEvents + trace + (u == lo && k0 == 0 ? 0 : 1)] = globaltimer();
     }
   }
   (void)P;
@@ -335,18 +391,36 @@ __device__ void loader(Ctx& cx) {
   prefetch_tensormap(&P.tmap_v);
   Ring r;
   r.issued = r.tail = r.head = 0;
+  r.ra.init(P.runahead_bytes);
   bool ok = true;
+  const AttnUnit au = attn_unit(P, rot_block(cx.block, P.phase_rot * 2, G), P.is_global);
+  if (r.ra.ahead) {
+    // everything up to the routing decision, in the order the ring streams it
+    if (P.first) add_dense_range(r.ra, P.w_qkv_pro, dm.d, dm.nqkv, P.phase_rot * 1);
+    if (au.valid && au.r1 > au.r0) {
+      const uint64_t off = ((uint64_t)au.hk * dm.max_ctx + au.r0) * dm.hd, bytes = (uint64_t)(au.r1 - au.r0) * dm.hd * 2;
+      r.ra.add(P.kc + off, bytes);
+      r.ra.add(P.vc + off, bytes);
+    }
+    add_dense_range(r.ra, P.w_o, dm.hq * dm.hd, dm.d, P.phase_rot * 3);
+    add_dense_range(r.ra, P.w_pool, dm.d, dm.p, P.phase_rot * 4);
+    add_dense_range(r.ra, P.w_router, dm.p, dm.e, P.phase_rot * 5);
+    if (cx.block == 0) {
+      prefetch_l2(P.g_moe, (uint32_t)dm.d * 2);
+      if (P.g_tail) prefetch_l2(P.g_tail, (uint32_t)dm.d * 2);
+    }
+    r.ra.pump();
+  }
   // weights do not depend on the previous launch: stream before the dependency wait
   if (P.first) ok = ok && load_dense(cx, r, P.w_qkv_pro, dm.d, dm.nqkv, P.phase_rot * 1, pol);
   {
-    AttnUnit au = attn_unit(P, rot_block(cx.block, P.phase_rot * 2, G), P.is_global);
     const uint32_t tb = (uint32_t)dm.attn_rows * dm.hd * 2 * 2;
     for (int i = 0; ok && i < au.n_sub; ++i) ok = ring_issue_kv(cx, r, au.hk, au.r0 + i * dm.attn_rows, tb);
   }
   // the deadline of the bounded waits starts once the previous launch is done
   pdl_wait();
   cx.deadline = globaltimer() + (((uint64_t)P.timeout_ns_hi << 32) | P.timeout_ns_lo);
-  ok = ok && load_dense(cx, r, P.w_o, dm.hq * dm.hd, dm.d, P.phase_rot * 3, pol);
+  ok = ok && load_dense(cx, r, P.w_o, dm.hq * dm.hd, dm.d, P.phase_rot * 3, pol, EV_LD_OP_FIRST);
   ok = ok && load_dense(cx, r, P.w_pool, dm.d, dm.p, P.phase_rot * 4, pol);
   ok = ok && load_dense(cx, r, P.w_router, dm.p, dm.e, P.phase_rot * 5, pol);
   // expert tiles wait for this block's routing decision
@@ -357,11 +431,33 @@ __device__ void loader(Ctx& cx) {
     const int u1pe = dm.f / 8, u2pe = dm.p / 16;
     const uint64_t ub1 = exp_unit_bytes(dm.p), ub2 = exp_unit_bytes(dm.f);
     int lo, hi;
+    if (r.ra.ahead) {
+      // the rest of the launch's stream: this block's expert units (runs of one expert
+      // are contiguous), the unpooler, then the next layer's QKV or the LM head
+      for (int pass = 0; pass < 2; ++pass) {
+        const int upe = pass ? u2pe : u1pe;
+        const uint64_t ub = pass ? ub2 : ub1;
+        const uint8_t* W = pass ? P.w2 : P.w1;
+        unit_range(na * upe, rot_block(cx.block, P.phase_rot * (pass ? 7 : 6), G), G, lo, hi);
+        for (int gu = lo; gu < hi;) {
+          const int e = cx.S.act_e[gu / upe];
+          const int run = min(hi, (gu / upe + 1) * upe) - gu;
+          r.ra.add(W + ((uint64_t)e * upe + gu % upe) * ub, (uint64_t)run * ub);
+          gu += run;
+        }
+      }
+      add_dense_range(r.ra, P.w_unpool, dm.p, dm.d, P.phase_rot * 8);
+      if (!P.last) add_dense_range(r.ra, P.w_tail, dm.d, dm.nqkv, P.phase_rot * 9);
+      else if (dm.vocab > 0) add_dense_range(r.ra, P.w_tail, dm.d, dm.vocab, P.phase_rot * 9);
+      r.ra.pump();
+    }
     unit_range(na * u1pe, rot_block(cx.block, P.phase_rot * 6, G), G, lo, hi);
     for (int gu = lo; ok && gu < hi; ++gu) {
       int e = cx.S.act_e[gu / u1pe];
       Seg sg = {P.w1 + ((uint64_t)e * u1pe + gu % u1pe) * ub1, (uint32_t)ub1};
       ok = ring_issue(cx, r, &sg, 1, pol);
+      if (gu == lo) stamp<kTiming>(P, cx.block, EV_LD_G1_FIRST);
+      if (gu == hi - 1) stamp<kTiming>(P, cx.block, EV_LD_G1_LAST);
     }
     unit_range(na * u2pe, rot_block(cx.block, P.phase_rot * 7, G), G, lo, hi);
     for (int gu = lo; ok && gu < hi; ++gu) {
@@ -401,17 +497,21 @@ struct Worker {
 __device__ __forceinline__ void cbar() { named_bar(1, kComputeThreads); }
 
 // B-operand layout of a [16 tokens][K] activation: per 16-column k-step four 8x8
-// matrices (tokens 0-7 | k 0-7, tokens 0-7 | k 8-15, tokens 8-15 | k 0-7,
-// tokens 8-15 | k 8-15), 16 bytes per matrix row.
+// matrices m (tokens 0-7 | k 0-7, tokens 0-7 | k 8-15, tokens 8-15 | k 0-7,
+// tokens 8-15 | k 8-15), 16 bytes per matrix row.  Row r of matrix m of k-step ks
+// sits at slot r ^ act_sw(ks, m) of its 128-byte block, so that one token's
+// consecutive 16-byte chunks fall in different banks (ldmatrix still reads each
+// matrix as one 128-byte block).
+__device__ __forceinline__ uint32_t act_sw(int ks, int m) { return (uint32_t)((ks * 2 + m) & 7); }
 __device__ __forceinline__ uint32_t act_off(int t, int k) {
-  return (uint32_t)(k >> 4) * kKStepBytes + (uint32_t)(((t >> 3) << 1) + ((k >> 3) & 1)) * 128u +
-         (uint32_t)(t & 7) * 16u;
+  const int ks = k >> 4, m = ((t >> 3) << 1) + ((k >> 3) & 1);
+  return (uint32_t)ks * kKStepBytes + (uint32_t)m * 128u + ((((uint32_t)t & 7u) ^ act_sw(ks, m)) << 4);
 }
 
 // Stage a [16][K] bf16 activation from global memory into the B layout,
 // optionally polling its sentinels and applying RMSNorm with `gain`.
 __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, const uint16_t* gain,
-                          float eps, int phase) {
+                                       float eps, int phase) {
   Ctx& cx = *w.cx;
   cbar();  // every compute warp is done with the act buffer
   const int tid = w.cw * 32 + w.lane;
@@ -419,6 +519,16 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, cons
   const int nch = K / 8;
   float ss = 0.f;
   bool ok = w.ok;
+  // the norm gain does not depend on the producers: fetch it now (one copy per block,
+  // kept in the reduction scratch, which no one uses between dense phases)
+  const bool gain_smem = gain != nullptr && nch <= 2 * kComputeThreads &&
+                         K * 2 <= (int)(sizeof(float) * kComputeWarps * 16 * 16);
+  uint4 gpre[2];
+  if (gain_smem) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (tid + j * kComputeThreads < nch) gpre[j] = ld_nc_v4_early(reinterpret_cast<const uint4*>(gain) + tid + j * kComputeThreads);
+  }
   // loads are issued in batches of 16 before any is inspected, so their latencies overlap
   constexpr int kB = 16;
   for (int c0 = sub; c0 < nch && ok; c0 += 16 * kB) {
@@ -451,16 +561,29 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, cons
     }
   }
   if (gain != nullptr && phase == PH_POOL) stamp_rt(*cx.P, EV_POOL_STAGED);
+  if ((cx.P->flags & 0x1u) && w.lane == 0 && (phase == PH_POOL || phase == PH_OPROJ))
+    cx.P->timing[(size_t)blockIdx.x * kTimingEvents + (phase == PH_POOL ? EV_POOL_WARP_STAGED : EV_OP_WARP_STAGED) +
+                 w.cw] = globaltimer();
+  if (gain_smem) {
+    uint4* gs = reinterpret_cast<uint4*>(cx.S.dred);
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (tid + j * kComputeThreads < nch) gs[tid + j * kComputeThreads] = gpre[j];
+    cbar();
+    if (phase == PH_POOL) stamp_rt(*cx.P, EV_POOL_GAIN);
+  }
   ok = __all_sync(0xffffffffu, ok);
   if (ok && gain != nullptr) {
 #pragma unroll
     for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
+    const uint4* gs = reinterpret_cast<const uint4*>(cx.S.dred);
     for (int c0 = sub; c0 < nch; c0 += 16 * kB) {
       uint4 gv[kB];
 #pragma unroll
       for (int j = 0; j < kB; ++j)
-        if (c0 + 16 * j < nch) gv[j] = __ldg(reinterpret_cast<const uint4*>(gain + (c0 + 16 * j) * 8));
+        if (c0 + 16 * j < nch)
+          gv[j] = gain_smem ? gs[c0 + 16 * j] : __ldg(reinterpret_cast<const uint4*>(gain + (c0 + 16 * j) * 8));
 #pragma unroll
       for (int j = 0; j < kB; ++j) {
         const int c = c0 + 16 * j;
@@ -479,6 +602,7 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, cons
       }
     }
   }
+  if (gain != nullptr && phase == PH_POOL) stamp_rt(*cx.P, EV_POOL_NORMED);
   w.ok = ok;
   cbar();
   // all compute warps must agree (a failure anywhere aborts the block)
@@ -490,21 +614,128 @@ __device__ __forceinline__ uint32_t lane_mat_off(int lane) {
   return (uint32_t)(lane >> 3) * 128u + (uint32_t)(lane & 7) * 16u;
 }
 
+struct QkvDst {
+  uint16_t* q;         // [16][hq*hd]
+  bool q_relaxed;
+  uint16_t* kc;        // caches of the layer whose rows are written
+  uint16_t* vc;
+  uint16_t* tkv;       // optional sentinel copy [2][hkv][16][hd]
+};
+
+__device__ __forceinline__ void qkv_epilogue(const LaunchParams& P, const Smem& S, const QkvDst& dst, int u, int p,
+                                             int t, float vlo, float vhi) {
+  const Dims& dm = P.dm;
+  const int D = dm.hd, upd = D / 16;
+  const int nQ = dm.hq * upd, nK = dm.hkv * upd;
+  if (u < nQ + nK) {
+    // rows p and p+8 of the unit are dims (j*8+p) and (j*8+p + D/2) of one head
+    const bool isq = u < nQ;
+    const int hu = isq ? u : u - nQ, h = hu / upd, j = hu % upd;
+    const int dim = j * 8 + p;
+    const float* cs = P.rope + ((size_t)S.depth[t] * (D / 2) + dim) * 2;
+    const float c = cs[0], s = cs[1];
+    const uint16_t xr = bf16_bits_rn(vlo * c - vhi * s), yr = bf16_bits_rn(vhi * c + vlo * s);
+    if (isq) {
+      uint16_t* q = dst.q + (size_t)t * dm.hq * D + (size_t)h * D + dim;
+      if (dst.q_relaxed) { st_relaxed_u16(q, xr); st_relaxed_u16(q + D / 2, yr); }
+      else { q[0] = xr; q[D / 2] = yr; }
+    } else {
+      uint16_t* k = dst.kc + ((size_t)h * dm.max_ctx + P.pos0 + t) * D + dim;
+      k[0] = xr;
+      k[D / 2] = yr;
+      if (dst.tkv) {
+        uint16_t* tp = dst.tkv + ((size_t)h * 16 + t) * D + dim;
+        st_relaxed_u16(tp, xr);
+        st_relaxed_u16(tp + D / 2, yr);
+      }
+    }
+  } else {
+    const int hu = u - nQ - nK, h = hu / upd, j = hu % upd;
+    const uint16_t a = bf16_bits_rn(vlo), b = bf16_bits_rn(vhi);
+    uint16_t* v = dst.vc + ((size_t)h * dm.max_ctx + P.pos0 + t) * D + j * 16 + p;
+    v[0] = a;
+    v[8] = b;
+    if (dst.tkv) {
+      uint16_t* tp = dst.tkv + (((size_t)dm.hkv + h) * 16 + t) * D + j * 16 + p;
+      st_relaxed_u16(tp, a);
+      st_relaxed_u16(tp + 8, b);
+    }
+  }
+}
+
+// what a dense phase does with its outputs (one copy of the phase loop serves all)
+enum EpiKind { EPI_QKV = 0, EPI_OPROJ = 1, EPI_POOL = 2, EPI_ROUTER = 3, EPI_UNPOOL = 4, EPI_LMHEAD = 5 };
+struct EpiArgs {
+  int kind;
+  QkvDst dq;               // EPI_QKV
+  const uint16_t* res;     // residual input (EPI_OPROJ: h, EPI_UNPOOL: h1)
+  uint16_t* out;           // bf16 output (h1, u, h2)
+  uint16_t* out2;          // optional second copy of h2 (next launch / caller)
+  float* out32;            // fp32 output (router logits, LM-head logits)
+};
+
+// epilogue of output rows u*16 + p and u*16 + p + 8 for token t (values lo, hi)
+__device__ void dense_epi(const LaunchParams& P, const Smem& S, const EpiArgs& ea, int u, int p, int t,
+                                       float lo, float hi) {
+  const Dims& dm = P.dm;
+  switch (ea.kind) {
+    case EPI_QKV:
+      qkv_epilogue(P, S, ea.dq, u, p, t, lo, hi);
+      break;
+    case EPI_OPROJ:
+    case EPI_UNPOOL: {
+      const float v2[2] = {lo, hi};
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int n = u * 16 + p + hf * 8;
+        // test hook: the first element of the whole h1 exchange is never written
+        if (ea.kind == EPI_OPROJ && (P.flags & 0x10000u) && u == 0 && t == 0 && p == 0 && hf == 0) continue;
+        const float o = bf16_to_f32(bf16_bits_rn(v2[hf]));
+        const uint16_t r = ea.kind == EPI_OPROJ ? ea.res[(size_t)t * dm.d + n] : ld_relaxed_u16(ea.res + (size_t)t * dm.d + n);
+        const uint16_t v = bf16_bits_rn(bf16_to_f32(r) + o);
+        st_relaxed_u16(ea.out + (size_t)t * dm.d + n, v);
+        if (ea.out2) ea.out2[(size_t)t * dm.d + n] = v;
+      }
+      break;
+    }
+    case EPI_POOL:
+      st_relaxed_u16(ea.out + (size_t)t * dm.p + u * 16 + p, bf16_bits_rn(lo));
+      st_relaxed_u16(ea.out + (size_t)t * dm.p + u * 16 + p + 8, bf16_bits_rn(hi));
+      break;
+    case EPI_ROUTER: {
+      const int n = u * 16 + p;
+      st_relaxed_u32(ea.out32 + (size_t)t * dm.e + n, __float_as_uint(f32_canon(lo + P.b_router[n])));
+      st_relaxed_u32(ea.out32 + (size_t)t * dm.e + n + 8, __float_as_uint(f32_canon(hi + P.b_router[n + 8])));
+      break;
+    }
+    default:  // EPI_LMHEAD
+      ea.out32[(size_t)t * dm.vocab + u * 16 + p] = lo;
+      ea.out32[(size_t)t * dm.vocab + u * 16 + p + 8] = hi;
+      break;
+  }
+}
+
 // Dense phase: out[16 tokens][N] = act[16][K] . W[N][K]^T over this block's
 // 16-row units.  Every tile (32 k-steps of one unit) is shared by the 8 compute
 // warps, warp w taking k-steps 4w..4w+3, so no warp carries a long dependent
 // MMA chain; each unit ends with a cross-warp sum in fixed warp order (the result
 // does not depend on the grid size) and an epilogue over (row pair, token):
-// epi(unit, p, t, row p value, row p+8 value), run by 128 threads.
-template <class Epi>
-__device__ void dense_phase(Worker& w, const int K, const int N, const int rot, Epi&& epi) {
+// dense_epi(unit, p, t, row p value, row p+8 value), run by 128 threads.
+__device__ void dense_phase(Worker& w, const int K, const int N, const int rot, const EpiArgs& ea,
+                                         int trace) {
   Ctx& cx = *w.cx;
   const int G = gridDim.x;
   int lo, hi;
   unit_range(N / 16, rot_block(cx.block, rot, G), G, lo, hi);
   const int steps = K / 16;
   const int ktiles = (steps + kDenseTileSteps - 1) / kDenseTileSteps;
-  const uint32_t act_base = smem_u32(cx.S.act) + lane_mat_off(w.lane);
+  // this warp's k-steps of a tile are 4 cw .. 4 cw + 3, so k-step & 3 is the loop index
+  uint32_t act_lane[4];
+#pragma unroll
+  for (int ii = 0; ii < 4; ++ii) {
+    const int m = w.lane >> 3;
+    act_lane[ii] = smem_u32(cx.S.act) + (uint32_t)m * 128u + ((((uint32_t)w.lane & 7u) ^ act_sw(ii, m)) << 4);
+  }
   float* red = cx.S.dred;  // [8 warps][16 rows][16 tokens]
   const int tid = w.cw * 32 + w.lane;
   const int ks_lo = w.cw * (kDenseTileSteps / kComputeWarps);
@@ -515,15 +746,19 @@ __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, 
       const uint32_t t = w.ti + (uint32_t)(loc * ktiles + kt);
       const uint32_t s = t % kSlots;
       if (w.ok) w.ok = wait_tile(cx, t, 50);
+      if (trace >= 0 && loc < 2 && (kt == 0 || kt == ktiles - 1)) stamp_rt(*cx.P, trace + loc * 4 + (kt ? 1 : 0));
       if (w.ok) {
         const uint32_t wbase = smem_u32(cx.S.ring + cx.S.slot_off[s]) + lane_mat_off(w.lane);
         const int k0 = kt * kDenseTileSteps;
         const int ns = min(kDenseTileSteps, steps - k0);
         const int ke = min(ns, ks_lo + kDenseTileSteps / kComputeWarps);
-        for (int i = ks_lo; i < ke; ++i) {
+#pragma unroll
+        for (int ii = 0; ii < kDenseTileSteps / kComputeWarps; ++ii) {
+          const int i = ks_lo + ii;
+          if (i >= ke) break;
           uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
           ldsm_x4(wbase + i * kKStepBytes, a0, a1, a2, a3);
-          ldsm_x4(act_base + (k0 + i) * kKStepBytes, b0, b1, b2, b3);
+          ldsm_x4(act_lane[ii] + (k0 + i) * kKStepBytes, b0, b1, b2, b3);
           mma_bf16(acc[0], a0, a1, a2, a3, b0, b1);
           mma_bf16(acc[1], a0, a1, a2, a3, b2, b3);
         }
@@ -539,6 +774,7 @@ __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, 
         const int row = w.g + ((i >> 1) << 3), tok = nt * 8 + 2 * w.q + (i & 1);
         red[(w.cw * 16 + row) * 16 + tok] = acc[nt][i];
       }
+    if (trace >= 0 && loc < 2) stamp_rt(*cx.P, trace + loc * 4 + 2);
     cbar();
     if (tid < 128 && w.ok) {
       const int p = tid >> 4, tok = tid & 15;
@@ -548,9 +784,10 @@ __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, 
         vlo += red[(ww * 16 + p) * 16 + tok];
         vhi += red[(ww * 16 + p + 8) * 16 + tok];
       }
-      epi(u, p, tok, vlo, vhi);
+      dense_epi(*cx.P, cx.S, ea, u, p, tok, vlo, vhi);
     }
     cbar();
+    if (trace >= 0 && loc < 2) stamp_rt(*cx.P, trace + loc * 4 + 3);
     if (*cx.S.abort) w.ok = false;
   }
   w.ti += (uint32_t)((hi - lo) * ktiles);
@@ -1021,6 +1258,7 @@ __device__ void route_phase(Worker& w) {
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
         if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
       }
+      if (bi >= E) bi = 0;  // only for NaN logits, which are outside the contract
       if ((bi & 31) == w.lane) used[bi >> 5] = true;
       sel_v[c] = bv;
       if (w.lane == 0) cx.S.topk_idx[t * kMaxTopK + c] = bi;
@@ -1034,12 +1272,28 @@ __device__ void route_phase(Worker& w) {
   cbar();
   stamp_rt(P, EV_ROUTE_TOPK);
   if (*cx.S.abort) w.ok = false;
-  // dispatch: thread e counts its tokens, then a block-wide scan compacts the active experts
+  // dispatch: every (token, slot) pair sets its bit in its expert's 128-bit mask, thread
+  // e counts its bits, then a block-wide scan compacts the active experts
   const int tid = w.cw * 32 + w.lane;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(cx.S.dred);  // [E][4], bit s = t K + c
+  for (int i = tid; i < E * 4; i += kComputeThreads) bits[i] = 0u;
+  cbar();
+  if (w.ok && tid < T * K) {
+    // (after a failed wait topk_idx was never written: the index is range-checked)
+    const int e = cx.S.topk_idx[(tid / K) * kMaxTopK + tid % K];
+    if ((unsigned)e < (unsigned)E) atomicOr(&bits[e * 4 + (tid >> 5)], 1u << (tid & 31));
+  }
+  cbar();
   int cnt = 0;
-  if (tid < E)
-    for (int t = 0; t < T; ++t)
-      for (int c = 0; c < K; ++c) cnt += (cx.S.topk_idx[t * kMaxTopK + c] == tid);
+  uint32_t b4[4] = {0u, 0u, 0u, 0u};
+  if (tid < E) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      b4[j] = bits[tid * 4 + j];
+      cnt += __popc(b4[j]);
+    }
+    cnt = min(cnt, 16);  // a token picks an expert at most once (NaN logits aside)
+  }
   const int act = cnt > 0;
   int incl = act;
 #pragma unroll
@@ -1057,13 +1311,14 @@ __device__ void route_phase(Worker& w) {
     cx.S.act_e[rank] = (int16_t)tid;
     cx.S.act_n[rank] = (uint8_t)cnt;
     int n = 0;
-    for (int t = 0; t < T; ++t)
-      for (int c = 0; c < K; ++c)
-        if (cx.S.topk_idx[t * kMaxTopK + c] == tid) {
-          cx.S.act_tok[rank * 16 + n] = (uint8_t)t;
-          cx.S.act_slot[rank * 16 + n] = (uint8_t)(t * K + c);
-          ++n;
-        }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      for (uint32_t m = b4[j]; m && n < 16; m &= m - 1u) {  // slots in increasing (token, slot) order
+        const int sl = j * 32 + __ffs(m) - 1;
+        cx.S.act_tok[rank * 16 + n] = (uint8_t)(sl / K);
+        cx.S.act_slot[rank * 16 + n] = (uint8_t)sl;
+        ++n;
+      }
   }
   if (tid == kComputeThreads - 1) {
     int tot = 0;
@@ -1148,18 +1403,22 @@ __device__ __forceinline__ void exp_frags(uint64_t cg, uint64_t cg8, uint32_t sg
 }
 
 // acc[nt] += W_unit (16 rows x K, NVFP4 tile at tbase) * act rows (token list via rowof)
-template <class RowOf>
-__device__ __forceinline__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* tbase, int K, int ntiles,
-                                             uint32_t act_s, int lane, RowOf rowof) {
+// rows[nt]: the token (activation row) this lane addresses in ldmatrix for n-tile nt
+__device__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* tbase, int K, int ntiles,
+                                          uint32_t act_s, int lane, const int (&rows)[2]) {
   const int g = lane >> 2, q = lane & 3;
-  const int mi = lane >> 3, r8 = lane & 7;
+  const int mi = lane >> 3;
   const int ng = K / 64;
   float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  uint32_t bro[2];
+  // B rows: token rows[nt] of matrix m; k-step & 3 is (kp + (mi >> 1)) & 3 with kp in {0, 2}
+  uint32_t bro[2][2];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
-    const int t = rowof(nt * 8 + r8);
-    bro[nt] = act_s + (uint32_t)(((t >> 3) << 1) + (mi & 1)) * 128u + (uint32_t)(t & 7) * 16u;
+    const int t = rows[nt];
+    const int m = ((t >> 3) << 1) + (mi & 1);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      bro[nt][h] = act_s + (uint32_t)m * 128u + ((((uint32_t)t & 7u) ^ act_sw(2 * h + (mi >> 1), m)) << 4);
   }
   for (int gi = 0; gi < ng; ++gi) {
     const uint8_t* gb = tbase + gi * kExpGroupBytes;
@@ -1175,7 +1434,7 @@ __device__ __forceinline__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* 
       const uint32_t kstep = (uint32_t)(gi * 4 + kp + (mi >> 1)) * kKStepBytes;
       for (int nt = 0; nt < ntiles; ++nt) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(bro[nt] + kstep, b0, b1, b2, b3);
+        ldsm_x4(bro[nt][kp >> 1] + kstep, b0, b1, b2, b3);
         mma_f16(acc[nt], a[0][0], a[0][1], a[0][2], a[0][3], b0, b1);
         mma_f16(acc2[nt], a[1][0], a[1][1], a[1][2], a[1][3], b2, b3);
       }
@@ -1206,9 +1465,13 @@ __device__ void gemm1_phase(Worker& w) {
     const uint32_t s = t % kSlots;
     if (w.ok) w.ok = wait_tile(cx, t, PH_GEMM1);
     if (!w.ok) break;
+    const bool last_u = loc + kComputeWarps >= hi - lo;
+    if (loc == w.cw) stamp_rt(P, EV_G1_FIRST_READY);
+    if (last_u) stamp_rt(P, EV_G1_LAST_READY);
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    exp_unit_mma(acc, cx.S.ring + cx.S.slot_off[s], dm.p, n > 8 ? 2 : 1, act_s, w.lane,
-                 [&](int p) { return (int)toks[p < n ? p : 0]; });
+    const int r8 = w.lane & 7;
+    const int rows[2] = {(int)toks[r8 < n ? r8 : 0], (int)toks[8 + r8 < n ? 8 + r8 : 0]};
+    exp_unit_mma(acc, cx.S.ring + cx.S.slot_off[s], dm.p, n > 8 ? 2 : 1, act_s, w.lane, rows);
     __syncwarp();
     if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps);
     const float gs = P.w1_gs[e];
@@ -1225,6 +1488,8 @@ __device__ void gemm1_phase(Worker& w) {
           st_relaxed_u32(aout + (size_t)slot * dm.f + jg * 8 + w.g, __float_as_uint(f32_canon(av)));
         }
       }
+    if (loc == w.cw) stamp_rt(P, EV_G1_FIRST_DONE);
+    if (last_u) stamp_rt(P, EV_G1_LAST_DONE);
   }
   w.ti += (uint32_t)(hi - lo);
 }
@@ -1290,8 +1555,9 @@ __device__ void gemm2_phase(Worker& w) {
         if (w.ok) w.ok = wait_tile(cx, t, PH_GEMM2);
         if (!w.ok) break;
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        exp_unit_mma(acc, cx.S.ring + cx.S.slot_off[s], dm.f, n > 8 ? 2 : 1, act_s, w.lane,
-                     [&](int p) { return p < n ? p : 0; });
+        const int r8 = w.lane & 7;
+        const int rows[2] = {r8 < n ? r8 : 0, 8 + r8 < n ? 8 + r8 : 0};
+        exp_unit_mma(acc, cx.S.ring + cx.S.slot_off[s], dm.f, n > 8 ? 2 : 1, act_s, w.lane, rows);
         __syncwarp();
         if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps);
         const float gs = P.w2_gs[e];
@@ -1371,55 +1637,6 @@ __device__ void rope_table(Worker& w) {
 }
 
 // QKV epilogue: RoPE pairs (d, d + hd/2) share a unit (rows g and g+8)
-struct QkvDst {
-  uint16_t* q;         // [16][hq*hd]
-  bool q_relaxed;
-  uint16_t* kc;        // caches of the layer whose rows are written
-  uint16_t* vc;
-  uint16_t* tkv;       // optional sentinel copy [2][hkv][16][hd]
-};
-
-__device__ __forceinline__ void qkv_epilogue(const LaunchParams& P, const Smem& S, const QkvDst& dst, int u, int p,
-                                             int t, float vlo, float vhi) {
-  const Dims& dm = P.dm;
-  const int D = dm.hd, upd = D / 16;
-  const int nQ = dm.hq * upd, nK = dm.hkv * upd;
-  if (u < nQ + nK) {
-    // rows p and p+8 of the unit are dims (j*8+p) and (j*8+p + D/2) of one head
-    const bool isq = u < nQ;
-    const int hu = isq ? u : u - nQ, h = hu / upd, j = hu % upd;
-    const int dim = j * 8 + p;
-    const float* cs = P.rope + ((size_t)S.depth[t] * (D / 2) + dim) * 2;
-    const float c = cs[0], s = cs[1];
-    const uint16_t xr = bf16_bits_rn(vlo * c - vhi * s), yr = bf16_bits_rn(vhi * c + vlo * s);
-    if (isq) {
-      uint16_t* q = dst.q + (size_t)t * dm.hq * D + (size_t)h * D + dim;
-      if (dst.q_relaxed) { st_relaxed_u16(q, xr); st_relaxed_u16(q + D / 2, yr); }
-      else { q[0] = xr; q[D / 2] = yr; }
-    } else {
-      uint16_t* k = dst.kc + ((size_t)h * dm.max_ctx + P.pos0 + t) * D + dim;
-      k[0] = xr;
-      k[D / 2] = yr;
-      if (dst.tkv) {
-        uint16_t* tp = dst.tkv + ((size_t)h * 16 + t) * D + dim;
-        st_relaxed_u16(tp, xr);
-        st_relaxed_u16(tp + D / 2, yr);
-      }
-    }
-  } else {
-    const int hu = u - nQ - nK, h = hu / upd, j = hu % upd;
-    const uint16_t a = bf16_bits_rn(vlo), b = bf16_bits_rn(vhi);
-    uint16_t* v = dst.vc + ((size_t)h * dm.max_ctx + P.pos0 + t) * D + j * 16 + p;
-    v[0] = a;
-    v[8] = b;
-    if (dst.tkv) {
-      uint16_t* tp = dst.tkv + (((size_t)dm.hkv + h) * 16 + t) * D + j * 16 + p;
-      st_relaxed_u16(tp, a);
-      st_relaxed_u16(tp + 8, b);
-    }
-  }
-}
-
 // re-arm the exchange buffers of the other parity (warps 1-2)
 __device__ void rearm(const LaunchParams& P, int block, int tid, int nthreads) {
   struct R { uint64_t off, bytes; uint32_t pat; };
@@ -1430,7 +1647,9 @@ __device__ void rearm(const LaunchParams& P, int block, int tid, int nthreads) {
       {P.xo.h2, P.xo.q0 - P.xo.h2, 0xFFFFFFFFu},   {P.xo.q0, P.xo.tkv0 - P.xo.q0, 0xFFFFFFFFu},
       {P.xo.tkv0, P.xo.total - P.xo.tkv0, 0xFFFFFFFFu}};
   const int G = gridDim.x;
-  for (const R& r : regs) {
+#pragma unroll 1
+  for (int ri = 0; ri < 9; ++ri) {
+    const R& r = regs[ri];
     const uint64_t n16 = r.bytes / 16;
     const uint64_t lo = n16 * block / G, hi = n16 * (block + 1) / G;
     const uint4 v = make_uint4(r.pat, r.pat, r.pat, r.pat);
@@ -1455,9 +1674,10 @@ __device__ void compute_main(Worker& w) {
     rope_table(w);
     stage_act(w, P.hidden_in, dm.d, false, P.g_attn_pro, dm.rms_eps, PH_PROLOGUE);
     stamp<kTiming>(P, b, EV_PRO_IN);
-    QkvDst dq{reinterpret_cast<uint16_t*>(X + P.xo.q0), true, P.kc, P.vc, reinterpret_cast<uint16_t*>(X + P.xo.tkv0)};
-    dense_phase(w, dm.d, dm.nqkv, P.phase_rot * 1,
-                [&](int u, int p, int t, float lo, float hi) { qkv_epilogue(P, cx.S, dq, u, p, t, lo, hi); });
+    EpiArgs ea{};
+    ea.kind = EPI_QKV;
+    ea.dq = QkvDst{reinterpret_cast<uint16_t*>(X + P.xo.q0), true, P.kc, P.vc, reinterpret_cast<uint16_t*>(X + P.xo.tkv0)};
+    dense_phase(w, dm.d, dm.nqkv, P.phase_rot * 1, ea, -1);
     stamp<kTiming>(P, b, EV_PRO_DONE);
     cbar();
   }
@@ -1474,17 +1694,11 @@ __device__ void compute_main(Worker& w) {
     uint16_t* h1 = reinterpret_cast<uint16_t*>(X + P.xo.h1);
     stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.o), dm.hq * dm.hd, true, nullptr, 0.f, PH_OPROJ);
     stamp<kTiming>(P, b, EV_OPROJ_IN);
-    dense_phase(w, dm.hq * dm.hd, dm.d, P.phase_rot * 3, [&](int u, int p, int t, float lo, float hi) {
-      const float v2[2] = {lo, hi};
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int n = u * 16 + p + hf * 8;
-        // test hook: the first element of the whole h1 exchange is never written
-        if ((P.flags & 0x10000u) && u == 0 && t == 0 && p == 0 && hf == 0) continue;
-        const float o = bf16_to_f32(bf16_bits_rn(v2[hf]));
-        st_relaxed_u16(h1 + (size_t)t * dm.d + n, bf16_bits_rn(bf16_to_f32(hprev[(size_t)t * dm.d + n]) + o));
-      }
-    });
+    EpiArgs ea{};
+    ea.kind = EPI_OPROJ;
+    ea.res = hprev;
+    ea.out = h1;
+    dense_phase(w, dm.hq * dm.hd, dm.d, P.phase_rot * 3, ea, EV_OP_U0_FIRST);
     stamp<kTiming>(P, b, EV_OPROJ_DONE);
   }
   // a5: u = bf16(bf16(RMSNorm(h1)) W_pool^T)
@@ -1492,10 +1706,10 @@ __device__ void compute_main(Worker& w) {
     uint16_t* uo = reinterpret_cast<uint16_t*>(X + P.xo.u);
     stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h1), dm.d, true, P.g_moe, dm.rms_eps, PH_POOL);
     stamp<kTiming>(P, b, EV_POOL_IN);
-    dense_phase(w, dm.d, dm.p, P.phase_rot * 4, [&](int u, int p, int t, float lo, float hi) {
-      st_relaxed_u16(uo + (size_t)t * dm.p + u * 16 + p, bf16_bits_rn(lo));
-      st_relaxed_u16(uo + (size_t)t * dm.p + u * 16 + p + 8, bf16_bits_rn(hi));
-    });
+    EpiArgs ea{};
+    ea.kind = EPI_POOL;
+    ea.out = uo;
+    dense_phase(w, dm.d, dm.p, P.phase_rot * 4, ea, -1);
     stamp<kTiming>(P, b, EV_POOL_DONE);
   }
   // a6: router logits = u W_r^T + b (fp32)
@@ -1503,11 +1717,10 @@ __device__ void compute_main(Worker& w) {
     float* lg = reinterpret_cast<float*>(X + P.xo.logits);
     stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.u), dm.p, true, nullptr, 0.f, PH_ROUTER);
     stamp<kTiming>(P, b, EV_ROUTER_IN);
-    dense_phase(w, dm.p, dm.e, P.phase_rot * 5, [&](int u, int p, int t, float lo, float hi) {
-      const int n = u * 16 + p;
-      st_relaxed_u32(lg + (size_t)t * dm.e + n, __float_as_uint(f32_canon(lo + P.b_router[n])));
-      st_relaxed_u32(lg + (size_t)t * dm.e + n + 8, __float_as_uint(f32_canon(hi + P.b_router[n + 8])));
-    });
+    EpiArgs ea{};
+    ea.kind = EPI_ROUTER;
+    ea.out32 = lg;
+    dense_phase(w, dm.p, dm.e, P.phase_rot * 5, ea, -1);
     stamp<kTiming>(P, b, EV_ROUTER_DONE);
   }
   // a6/a7/a8: top-k, dispatch, NVFP4 activations
@@ -1538,17 +1751,12 @@ __device__ void compute_main(Worker& w) {
     uint16_t* hnext = P.last ? P.hidden_out : P.out_h;
     stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.z), dm.p, true, nullptr, 0.f, PH_UNPOOL);
     stamp<kTiming>(P, b, EV_UNPOOL_IN);
-    dense_phase(w, dm.p, dm.d, P.phase_rot * 8, [&](int u, int p, int t, float lo, float hi) {
-      const float v2[2] = {lo, hi};
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int n = u * 16 + p + hf * 8;
-        const float o = bf16_to_f32(bf16_bits_rn(v2[hf]));
-        const uint16_t v = bf16_bits_rn(bf16_to_f32(ld_relaxed_u16(h1 + (size_t)t * dm.d + n)) + o);
-        st_relaxed_u16(h2 + (size_t)t * dm.d + n, v);
-        if (hnext) hnext[(size_t)t * dm.d + n] = v;
-      }
-    });
+    EpiArgs ea{};
+    ea.kind = EPI_UNPOOL;
+    ea.res = h1;
+    ea.out = h2;
+    ea.out2 = hnext;
+    dense_phase(w, dm.p, dm.d, P.phase_rot * 8, ea, -1);
     stamp<kTiming>(P, b, EV_UNPOOL_DONE);
   }
   pdl_launch_dependents();
@@ -1556,16 +1764,17 @@ __device__ void compute_main(Worker& w) {
   if (!P.last) {
     stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h2), dm.d, true, P.g_tail, dm.rms_eps, PH_TAIL);
     stamp<kTiming>(P, b, EV_TAIL_IN);
-    QkvDst dq{P.out_q, false, P.kc_next, P.vc_next, nullptr};
-    dense_phase(w, dm.d, dm.nqkv, P.phase_rot * 9,
-                [&](int u, int p, int t, float lo, float hi) { qkv_epilogue(P, cx.S, dq, u, p, t, lo, hi); });
+    EpiArgs ea{};
+    ea.kind = EPI_QKV;
+    ea.dq = QkvDst{P.out_q, false, P.kc_next, P.vc_next, nullptr};
+    dense_phase(w, dm.d, dm.nqkv, P.phase_rot * 9, ea, -1);
   } else if (dm.vocab > 0) {
     stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h2), dm.d, true, P.g_tail, dm.rms_eps, PH_TAIL);
     stamp<kTiming>(P, b, EV_TAIL_IN);
-    dense_phase(w, dm.d, dm.vocab, P.phase_rot * 9, [&](int u, int p, int t, float lo, float hi) {
-      P.logits[(size_t)t * dm.vocab + u * 16 + p] = lo;
-      P.logits[(size_t)t * dm.vocab + u * 16 + p + 8] = hi;
-    });
+    EpiArgs ea{};
+    ea.kind = EPI_LMHEAD;
+    ea.out32 = P.logits;
+    dense_phase(w, dm.d, dm.vocab, P.phase_rot * 9, ea, -1);
   }
   stamp<kTiming>(P, b, EV_TAIL_DONE);
 }
