@@ -578,19 +578,23 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, cons
     for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
     const uint4* gs = reinterpret_cast<const uint4*>(cx.S.dred);
-    for (int c0 = sub; c0 < nch; c0 += 16 * kB) {
-      uint4 gv[kB];
+    // compact loop (this code runs once per phase, cold in the instruction cache):
+    // four chunks per iteration, all loads before any store
+    constexpr int kN = 4;
+#pragma unroll 1
+    for (int c0 = sub; c0 < nch; c0 += 16 * kN) {
+      uint4 v[kN], gv[kN];
+      uint32_t off[kN];
 #pragma unroll
-      for (int j = 0; j < kB; ++j)
-        if (c0 + 16 * j < nch)
-          gv[j] = gain_smem ? gs[c0 + 16 * j] : __ldg(reinterpret_cast<const uint4*>(gain + (c0 + 16 * j) * 8));
+      for (int j = 0; j < kN; ++j) {
+        const int c = min(c0 + 16 * j, nch - 1);
+        off[j] = act_off(t, c * 8);
+        v[j] = *reinterpret_cast<const uint4*>(cx.S.act + off[j]);
+        gv[j] = gain_smem ? gs[c] : __ldg(reinterpret_cast<const uint4*>(gain + c * 8));
+      }
 #pragma unroll
-      for (int j = 0; j < kB; ++j) {
-        const int c = c0 + 16 * j;
-        if (c >= nch) continue;
-        uint4* sp = reinterpret_cast<uint4*>(cx.S.act + act_off(t, c * 8));
-        const uint4 v = *sp;
-        uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+      for (int j = 0; j < kN; ++j) {
+        uint32_t wd[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
         const uint32_t gw[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -598,8 +602,11 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, cons
           const float b = bf16_to_f32((uint16_t)(wd[i] >> 16)) * inv * bf16_to_f32((uint16_t)(gw[i] >> 16));
           wd[i] = pack_bf16x2(a, b);
         }
-        *sp = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        v[j] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
       }
+#pragma unroll
+      for (int j = 0; j < kN; ++j)
+        if (c0 + 16 * j < nch) *reinterpret_cast<uint4*>(cx.S.act + off[j]) = v[j];
     }
   }
   if (gain != nullptr && phase == PH_POOL) stamp_rt(*cx.P, EV_POOL_NORMED);
@@ -1390,25 +1397,36 @@ __device__ void route_phase(Worker& w) {
 
 // NVFP4 expert tile: A fragments of rows g and g+8 for one 16-column k-step,
 // weights dequantised e2m1 * e4m3 into f16 (exact)
+// f16x2 {s, s} * 2^-8 of a UE4M3 scale byte: E4M3 has exponent bias 7 and f16 bias 15,
+// so the byte's 7 magnitude bits shifted into f16 position give the value times 2^-8,
+// exactly (subnormal scales included); bit 7 (a sign UE4M3 does not have) is ignored
+__device__ __forceinline__ uint32_t ue4m3_pair_f16(uint32_t word, int byte) {
+  return (__byte_perm(word, 0u, 0x4040u | (uint32_t)byte | ((uint32_t)byte << 8)) & 0x007F007Fu) << 7;
+}
+
+// NVFP4 expert tile: A fragments of rows g and g+8 for one 16-column k-step, the
+// weights dequantised e2m1 * e4m3 into f16 times 2^-8 (exact: every product has at
+// most 6 significant bits and lies in [2^-18, 10.5]); the caller scales by 2^8
 __device__ __forceinline__ void exp_frags(uint64_t cg, uint64_t cg8, uint32_t sg, uint32_t sg8, int ks,
                                           uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
   const uint32_t lo_g = (uint32_t)(cg >> (ks * 16)) & 0xFFu, hi_g = (uint32_t)(cg >> (ks * 16 + 8)) & 0xFFu;
   const uint32_t lo_8 = (uint32_t)(cg8 >> (ks * 16)) & 0xFFu, hi_8 = (uint32_t)(cg8 >> (ks * 16 + 8)) & 0xFFu;
-  const uint32_t s_g = (sg >> (ks * 8)) & 0xFFu, s_8 = (sg8 >> (ks * 8)) & 0xFFu;
-  const uint32_t f_g = e4m3x2_to_f16x2(s_g | (s_g << 8)), f_8 = e4m3x2_to_f16x2(s_8 | (s_8 << 8));
+  const uint32_t f_g = ue4m3_pair_f16(sg, ks), f_8 = ue4m3_pair_f16(sg8, ks);
   a0 = hmul2(e2m1x2_to_f16x2(lo_g), f_g);
   a2 = hmul2(e2m1x2_to_f16x2(hi_g), f_g);
   a1 = hmul2(e2m1x2_to_f16x2(lo_8), f_8);
   a3 = hmul2(e2m1x2_to_f16x2(hi_8), f_8);
 }
+// the factor exp_frags leaves out
+constexpr float kExpScaleUndo = 256.0f;
 
-// acc[nt] += W_unit (16 rows x K, NVFP4 tile at tbase) * act rows (token list via rowof)
-// rows[nt]: the token (activation row) this lane addresses in ldmatrix for n-tile nt
-__device__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* tbase, int K, int ntiles,
-                                          uint32_t act_s, int lane, const int (&rows)[2]) {
+// acc[nt] += 2^-8 W_unit (16 rows, 64-column groups [g0, g1) of the NVFP4 tile at tbase)
+// * act rows; rows[nt]: the token (activation row) this lane addresses in ldmatrix
+// for n-tile nt
+__device__ __forceinline__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* tbase, int g0, int g1, int ntiles,
+                                             uint32_t act_s, int lane, const int (&rows)[2]) {
   const int g = lane >> 2, q = lane & 3;
   const int mi = lane >> 3;
-  const int ng = K / 64;
   float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   // B rows: token rows[nt] of matrix m; k-step & 3 is (kp + (mi >> 1)) & 3 with kp in {0, 2}
   uint32_t bro[2][2];
@@ -1420,12 +1438,22 @@ __device__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* tbase, int K, in
     for (int h = 0; h < 2; ++h)
       bro[nt][h] = act_s + (uint32_t)m * 128u + ((((uint32_t)t & 7u) ^ act_sw(2 * h + (mi >> 1), m)) << 4);
   }
-  for (int gi = 0; gi < ng; ++gi) {
-    const uint8_t* gb = tbase + gi * kExpGroupBytes;
-    const uint64_t cg = *reinterpret_cast<const uint64_t*>(gb + g * 32 + q * 8);
-    const uint64_t cg8 = *reinterpret_cast<const uint64_t*>(gb + (g + 8) * 32 + q * 8);
-    const uint32_t sg = *reinterpret_cast<const uint32_t*>(gb + 512 + g * 4);
-    const uint32_t sg8 = *reinterpret_cast<const uint32_t*>(gb + 512 + (g + 8) * 4);
+  // the next group's code and scale words are read while this group computes
+  const uint8_t* gb0 = tbase + g0 * kExpGroupBytes;
+  uint64_t ncg = *reinterpret_cast<const uint64_t*>(gb0 + g * 32 + q * 8);
+  uint64_t ncg8 = *reinterpret_cast<const uint64_t*>(gb0 + (g + 8) * 32 + q * 8);
+  uint32_t nsg = *reinterpret_cast<const uint32_t*>(gb0 + 512 + g * 4);
+  uint32_t nsg8 = *reinterpret_cast<const uint32_t*>(gb0 + 512 + (g + 8) * 4);
+  for (int gi = g0; gi < g1; ++gi) {
+    const uint64_t cg = ncg, cg8 = ncg8;
+    const uint32_t sg = nsg, sg8 = nsg8;
+    if (gi + 1 < g1) {
+      const uint8_t* gb = tbase + (gi + 1) * kExpGroupBytes;
+      ncg = *reinterpret_cast<const uint64_t*>(gb + g * 32 + q * 8);
+      ncg8 = *reinterpret_cast<const uint64_t*>(gb + (g + 8) * 32 + q * 8);
+      nsg = *reinterpret_cast<const uint32_t*>(gb + 512 + g * 4);
+      nsg8 = *reinterpret_cast<const uint32_t*>(gb + 512 + (g + 8) * 4);
+    }
 #pragma unroll
     for (int kp = 0; kp < 4; kp += 2) {
       uint32_t a[2][4];
@@ -1447,6 +1475,39 @@ __device__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* tbase, int K, in
     for (int i = 0; i < 4; ++i) acc[nt][i] += acc2[nt][i];
 }
 
+// Expert units are shared by a pair of compute warps (warps 2j and 2j+1), each taking
+// half of the unit's 64-column groups, so twice as many warps work on the tiles the
+// ring holds.  The odd warp hands its partial sums (and whether it got its tile) to
+// the even warp through a double-buffered slot of the reduction scratch; both warps
+// meet at the pair's named barrier once per unit and leave the loop together.
+__device__ __forceinline__ void pair_bar(int pair) { named_bar(2 + pair, 64); }
+
+// returns false (for both warps of the pair) if either warp failed; on success the
+// even warp's acc holds the unit's sum (even half first, then odd half)
+__device__ __forceinline__ bool pair_reduce(Worker& w, float (&acc)[2][4], bool ok, int it) {
+  const int pair = w.cw >> 1, half = w.cw & 1;
+  // partials: [pair][buffer][8][32 lanes] floats = the 8 KB reduction scratch; flags
+  // [pair][buffer][half] in the (then unused) scan scratch
+  float* x = w.cx->S.dred + (pair * 2 + (it & 1)) * 256;
+  int* fl = reinterpret_cast<int*>(w.cx->S.red) + (pair * 2 + (it & 1)) * 2;
+  if (half) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[(nt * 4 + i) * 32 + w.lane] = acc[nt][i];
+  }
+  if (w.lane == 0) fl[half] = ok ? 1 : 0;
+  pair_bar(pair);
+  const bool both = fl[0] != 0 && fl[1] != 0;
+  if (!half && both) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[nt][i] += x[(nt * 4 + i) * 32 + w.lane];
+  }
+  return both;
+}
+
 __device__ void gemm1_phase(Worker& w) {
   Ctx& cx = *w.cx;
   const LaunchParams& P = *cx.P;
@@ -1457,39 +1518,49 @@ __device__ void gemm1_phase(Worker& w) {
   unit_range(na * u1pe, rot_block(cx.block, P.phase_rot * 6, G), G, lo, hi);
   float* aout = reinterpret_cast<float*>(P.x_cur + P.xo.a);
   const uint32_t act_s = smem_u32(cx.S.act);
-  for (int loc = w.cw; loc < hi - lo; loc += kComputeWarps) {
+  const int pair = w.cw >> 1, half = w.cw & 1, ng = dm.p / 64;
+  const int g0 = half ? ng / 2 : 0, g1 = half ? ng : ng / 2;
+  int it = 0;
+  for (int loc = pair; loc < hi - lo; loc += kComputeWarps / 2, ++it) {
     const int gu = lo + loc, a = gu / u1pe, jg = gu % u1pe;
     const int e = cx.S.act_e[a], n = cx.S.act_n[a];
     const uint8_t* toks = cx.S.act_tok + a * 16;
     const uint32_t t = w.ti + (uint32_t)loc;
     const uint32_t s = t % kSlots;
-    if (w.ok) w.ok = wait_tile(cx, t, PH_GEMM1);
-    if (!w.ok) break;
-    const bool last_u = loc + kComputeWarps >= hi - lo;
-    if (loc == w.cw) stamp_rt(P, EV_G1_FIRST_READY);
-    if (last_u) stamp_rt(P, EV_G1_LAST_READY);
+    bool got = w.ok && wait_tile(cx, t, PH_GEMM1);
+    const bool last_u = loc + kComputeWarps / 2 >= hi - lo;
+    if (loc == pair && half == 0) stamp_rt(P, EV_G1_FIRST_READY);
+    if (last_u && half == 0) stamp_rt(P, EV_G1_LAST_READY);
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    const int r8 = w.lane & 7;
-    const int rows[2] = {(int)toks[r8 < n ? r8 : 0], (int)toks[8 + r8 < n ? 8 + r8 : 0]};
-    exp_unit_mma(acc, cx.S.ring + cx.S.slot_off[s], dm.p, n > 8 ? 2 : 1, act_s, w.lane, rows);
-    __syncwarp();
-    if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps);
-    const float gs = P.w1_gs[e];
+    if (got) {
+      const int r8 = w.lane & 7;
+      const int rows[2] = {(int)toks[r8 < n ? r8 : 0], (int)toks[8 + r8 < n ? 8 + r8 : 0]};
+      exp_unit_mma(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, n > 8 ? 2 : 1, act_s, w.lane, rows);
+      __syncwarp();
+      if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps / 2);
+    }
+    if (!pair_reduce(w, acc, got, it)) {
+      w.ok = false;
+      break;
+    }
+    if (half == 0) {
+      const float gs = P.w1_gs[e] * kExpScaleUndo;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int ii = 0; ii < 2; ++ii) {
-        const int p = nt * 8 + 2 * w.q + ii;
-        if (p < n) {
-          const int tok = toks[p], slot = cx.S.act_slot[a * 16 + p];
-          const float sc = cx.S.x_ts[tok] * gs;
-          const float gate = acc[nt][ii] * sc, up = acc[nt][2 + ii] * sc;
-          const float av = gate / (1.0f + expf(-gate)) * up;
-          st_relaxed_u32(aout + (size_t)slot * dm.f + jg * 8 + w.g, __float_as_uint(f32_canon(av)));
+        for (int ii = 0; ii < 2; ++ii) {
+          const int p = nt * 8 + 2 * w.q + ii;
+          if (p < n) {
+            const int tok = toks[p], slot = cx.S.act_slot[a * 16 + p];
+            const float sc = cx.S.x_ts[tok] * gs;
+            const float gate = acc[nt][ii] * sc, up = acc[nt][2 + ii] * sc;
+            const float av = gate / (1.0f + expf(-gate)) * up;
+            st_relaxed_u32(aout + (size_t)slot * dm.f + jg * 8 + w.g, __float_as_uint(f32_canon(av)));
+          }
         }
-      }
-    if (loc == w.cw) stamp_rt(P, EV_G1_FIRST_DONE);
-    if (last_u) stamp_rt(P, EV_G1_LAST_DONE);
+    }
+    if (loc == pair && half == 0) stamp_rt(P, EV_G1_FIRST_DONE);
+    if (last_u && half == 0) stamp_rt(P, EV_G1_LAST_DONE);
   }
   w.ti += (uint32_t)(hi - lo);
 }
@@ -1505,6 +1576,9 @@ __device__ void gemm2_phase(Worker& w) {
   const float* ain = reinterpret_cast<const float*>(P.x_cur + P.xo.a);
   uint16_t* yout = reinterpret_cast<uint16_t*>(P.s_buf + P.so.y);
   const uint32_t act_s = smem_u32(cx.S.act);
+  const int pair = w.cw >> 1, half = w.cw & 1, ng = dm.f / 64;
+  const int g0 = half ? ng / 2 : 0, g1 = half ? ng : ng / 2;
+  int it = 0;
   if (hi > lo) {
     const int a_first = lo / u2pe, a_last = (hi - 1) / u2pe;
     for (int a = a_first; a <= a_last; ++a) {
@@ -1546,33 +1620,41 @@ __device__ void gemm2_phase(Worker& w) {
       if (a == a_first) stamp_rt(P, EV_GEMM2_IN);
       if (*cx.S.abort) w.ok = false;
       const int u_lo = max(lo, a * u2pe), u_hi = min(hi, (a + 1) * u2pe);
-      for (int gu = u_lo; gu < u_hi; ++gu) {
+      // units of this expert: pair j takes every 4th (counted from the block's first unit)
+      int gu = u_lo + ((pair - (u_lo - lo)) % (kComputeWarps / 2) + kComputeWarps / 2) % (kComputeWarps / 2);
+      for (; gu < u_hi; gu += kComputeWarps / 2, ++it) {
         const int loc = gu - lo;
-        if (loc % kComputeWarps != w.cw) continue;
         const int pr = gu % u2pe;
         const uint32_t t = w.ti + (uint32_t)loc;
         const uint32_t s = t % kSlots;
-        if (w.ok) w.ok = wait_tile(cx, t, PH_GEMM2);
-        if (!w.ok) break;
+        bool got = w.ok && wait_tile(cx, t, PH_GEMM2);
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        const int r8 = w.lane & 7;
-        const int rows[2] = {r8 < n ? r8 : 0, 8 + r8 < n ? 8 + r8 : 0};
-        exp_unit_mma(acc, cx.S.ring + cx.S.slot_off[s], dm.f, n > 8 ? 2 : 1, act_s, w.lane, rows);
-        __syncwarp();
-        if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps);
-        const float gs = P.w2_gs[e];
+        if (got) {
+          const int r8 = w.lane & 7;
+          const int rows[2] = {r8 < n ? r8 : 0, 8 + r8 < n ? 8 + r8 : 0};
+          exp_unit_mma(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, n > 8 ? 2 : 1, act_s, w.lane, rows);
+          __syncwarp();
+          if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps / 2);
+        }
+        if (!pair_reduce(w, acc, got, it)) {
+          w.ok = false;
+          break;
+        }
+        if (half == 0) {
+          const float gs = P.w2_gs[e] * kExpScaleUndo;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+          for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int ii = 0; ii < 2; ++ii) {
-            const int p = nt * 8 + 2 * w.q + ii;
-            if (p < n) {
-              const int slot = cx.S.act_slot[a * 16 + p];
-              const float sc = cx.S.a_ts[p] * gs;
-              st_relaxed_u16(yout + (size_t)slot * dm.p + pr * 16 + w.g, bf16_bits_rn(acc[nt][ii] * sc));
-              st_relaxed_u16(yout + (size_t)slot * dm.p + pr * 16 + w.g + 8, bf16_bits_rn(acc[nt][2 + ii] * sc));
+            for (int ii = 0; ii < 2; ++ii) {
+              const int p = nt * 8 + 2 * w.q + ii;
+              if (p < n) {
+                const int slot = cx.S.act_slot[a * 16 + p];
+                const float sc = cx.S.a_ts[p] * gs;
+                st_relaxed_u16(yout + (size_t)slot * dm.p + pr * 16 + w.g, bf16_bits_rn(acc[nt][ii] * sc));
+                st_relaxed_u16(yout + (size_t)slot * dm.p + pr * 16 + w.g + 8, bf16_bits_rn(acc[nt][2 + ii] * sc));
+              }
             }
-          }
+        }
       }
     }
   }
