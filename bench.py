@@ -54,6 +54,33 @@ def step_bytes(cfg, distinct_per_layer, pos0):
     return tot
 
 
+# ----------------------------------------------------------------- DRAM traffic
+# dram__bytes_read.sum + dram__bytes_write.sum of one layer launch, as a multiple of
+# that launch's algorithmic bytes, from an ncu capture of the kernel source whose
+# hash is given (one full-width SWA-2048 layer: 307 MB of traffic for 300.4 MB).
+# Reported only while the kernel source is unchanged; any edit makes it null.
+TRAFFIC_RATIO = {"kernel_sha256": "bbf9e6bd563eb760b5845e19835b7294e7c664e155fa08ae29702c2155b69bcd", "ratio": 1.022,
+                 "capture": "profiles/layer_kernel_cfg2_one_layer_full.md"}
+
+
+def kernel_sha256():
+    import hashlib
+    src = os.path.join(ROOT, "moe_decode_megakernel_warp_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(src)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(src, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def traffic_per_launch(bytes_step, n_launch):
+    """DRAM bytes per launch (read + write) scaled from the capture, or None."""
+    if kernel_sha256() != TRAFFIC_RATIO["kernel_sha256"]:
+        return None
+    return TRAFFIC_RATIO["ratio"] * bytes_step / n_launch
+
+
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi sampled every 200 ms while the timed region runs."""
@@ -390,7 +417,8 @@ def run_ours(args):
             "distinct_experts_per_layer": {"mean": float(np.mean(distinct)), "min": int(min(distinct)),
                                            "max": int(max(distinct))},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": args.traffic,
+                         "frac": achieved / peak,
+                         "traffic": args.traffic if args.traffic is not None else traffic_per_launch(bytes_step, n_launch),
                          "peak_kind": peak_kind,
                          "note": "algorithmic bytes per step / device time of the step's %d launches of the "
                                  "layer kernel (the only kernel in the step)" % n_launch},

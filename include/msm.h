@@ -52,7 +52,8 @@
  *   w_unpool          bf16 [d_model][pool_dim]
  *   norm_attn/norm_moe/norm_final  bf16 [d_model] RMSNorm gains
  *   w1 (NVFP4)        codes uint8 [n_experts][2 ffn_dim][pool_dim/2] (two E2M1
- *                     codes per byte, low nibble = even column), scales E4M3
+ *                     codes per byte, low nibble = even column), block scales
+ *                     unsigned E4M3 (UE4M3: bit 7 must be 0 and is ignored)
  *                     [n_experts][2 ffn_dim][pool_dim/16], tensor scale fp32
  *                     [n_experts]; rows [0, ffn_dim) = SwiGLU gate, the rest = up
  *   w2 (NVFP4)        codes [n_experts][pool_dim][ffn_dim/2], scales
