@@ -517,7 +517,7 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, cons
   const int tid = w.cw * 32 + w.lane;
   const int t = tid >> 4, sub = tid & 15;
   const int nch = K / 8;
-  float ss = 0.f;
+  float2 ss2 = make_float2(0.f, 0.f);  // sums of squares of even / odd elements
   bool ok = w.ok;
   // the norm gain does not depend on the producers: fetch it now (one copy per block,
   // kept in the reduction scratch, which no one uses between dense phases)
@@ -553,9 +553,8 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, cons
       const uint32_t wd[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float a = bf16_to_f32((uint16_t)(wd[i] & 0xFFFF)), b = bf16_to_f32((uint16_t)(wd[i] >> 16));
-        ss = fmaf(a, a, ss);
-        ss = fmaf(b, b, ss);
+        const float2 x2 = make_float2(__uint_as_float(wd[i] << 16), __uint_as_float(wd[i] & 0xFFFF0000u));
+        ss2 = __ffma2_rn(x2, x2, ss2);
       }
       *reinterpret_cast<uint4*>(cx.S.act + act_off(t, c * 8)) = v[j];
     }
@@ -574,9 +573,11 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, cons
   }
   ok = __all_sync(0xffffffffu, ok);
   if (ok && gain != nullptr) {
+    float ss = ss2.x + ss2.y;
 #pragma unroll
     for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
+    const float2 inv2 = make_float2(inv, inv);
     const uint4* gs = reinterpret_cast<const uint4*>(cx.S.dred);
     // compact loop (this code runs once per phase, cold in the instruction cache):
     // four chunks per iteration, all loads before any store
@@ -598,9 +599,12 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, cons
         const uint32_t gw[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float a = bf16_to_f32((uint16_t)(wd[i] & 0xFFFF)) * inv * bf16_to_f32((uint16_t)(gw[i] & 0xFFFF));
-          const float b = bf16_to_f32((uint16_t)(wd[i] >> 16)) * inv * bf16_to_f32((uint16_t)(gw[i] >> 16));
-          wd[i] = pack_bf16x2(a, b);
+          // (x * inv) * g per element in fp32, two elements per instruction; the result
+          // stays in shared memory, so no sentinel mapping is needed
+          const float2 xs = __fmul2_rn(make_float2(__uint_as_float(wd[i] << 16), __uint_as_float(wd[i] & 0xFFFF0000u)), inv2);
+          const float2 y = __fmul2_rn(xs, make_float2(__uint_as_float(gw[i] << 16), __uint_as_float(gw[i] & 0xFFFF0000u)));
+          const __nv_bfloat162 h = __floats2bfloat162_rn(y.x, y.y);
+          wd[i] = *reinterpret_cast<const uint32_t*>(&h);
         }
         v[j] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
       }
@@ -1224,51 +1228,51 @@ __device__ void route_phase(Worker& w) {
   const Dims& dm = P.dm;
   const int E = dm.e, K = dm.k;
   const float* logits = reinterpret_cast<const float*>(P.x_cur + P.xo.logits);
-  // top-k: warp cw takes tokens 2cw, 2cw+1
+  // top-k: warp cw takes tokens 2cw, 2cw+1.  Logits become order-preserving unsigned
+  // keys (router logits are canonical: never -0.0); each round takes the warp-wide
+  // largest key, ties to the lowest expert index, with two warp reductions.
+  const int per = (E + 31) / 32;
   for (int tt = 0; tt < 2; ++tt) {
     const int t = w.cw * 2 + tt;
-    float v[kMaxExperts / 32];
-    bool used[kMaxExperts / 32];
-    const int per = E / 32 + ((E % 32) ? 1 : 0);
+    uint32_t key[kMaxExperts / 32];
+    uint32_t bits[kMaxExperts / 32];
+#pragma unroll
     for (int i = 0; i < kMaxExperts / 32; ++i) {
-      v[i] = -INFINITY;
-      used[i] = true;
       const int e = w.lane + 32 * i;
-      if (i < per && e < E) v[i] = __uint_as_float(ld_relaxed_u32(logits + t * E + e));
+      bits[i] = (i < per && e < E) ? ld_relaxed_u32(logits + t * E + e) : 0u;
     }
+#pragma unroll
     for (int i = 0; i < kMaxExperts / 32; ++i) {
       const int e = w.lane + 32 * i;
+      key[i] = 0u;  // below every real logit's key
       if (i < per && e < E && w.ok) {
         uint32_t n = 0;
-        uint32_t bits = __float_as_uint(v[i]);
-        while (bits == kF32Empty) {
+        while (bits[i] == kF32Empty) {
           if ((++n & 31) == 0 && cx.expired(PH_ROUTE)) { w.ok = false; break; }
-          bits = ld_relaxed_u32(logits + t * E + e);
+          bits[i] = ld_relaxed_u32(logits + t * E + e);
         }
-        v[i] = __uint_as_float(bits);
-        used[i] = false;
+        key[i] = (bits[i] & 0x80000000u) ? ~bits[i] : (bits[i] | 0x80000000u);
       }
     }
     w.ok = __all_sync(0xffffffffu, w.ok);
     if (!w.ok) break;
     float sel_v[kMaxTopK];
+    uint32_t taken = 0u;  // bit i: v[i] of this lane already selected
     for (int c = 0; c < K; ++c) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int i = 0; i < kMaxExperts / 32; ++i) {
-        const int e = w.lane + 32 * i;
-        if (!used[i] && (v[i] > bv || (v[i] == bv && e < bi))) { bv = v[i]; bi = e; }
-      }
+      // this lane's best unselected key (lowest i among equal keys)
+      uint32_t bk = 0u;
+      int bi = 0;
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-      }
-      if (bi >= E) bi = 0;  // only for NaN logits, which are outside the contract
-      if ((bi & 31) == w.lane) used[bi >> 5] = true;
-      sel_v[c] = bv;
-      if (w.lane == 0) cx.S.topk_idx[t * kMaxTopK + c] = bi;
+      for (int i = kMaxExperts / 32 - 1; i >= 0; --i)
+        if (!((taken >> i) & 1u) && key[i] >= bk && i < per) { bk = key[i]; bi = i; }
+      const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+      const uint32_t e_me = (bk == wk) ? (uint32_t)(w.lane + 32 * bi) : 0xFFFFFFFFu;
+      uint32_t e = __reduce_min_sync(0xffffffffu, e_me);
+      if (e >= (uint32_t)E) e = 0;  // only for NaN logits, which are outside the contract
+      if ((int)(e & 31) == w.lane) taken |= 1u << (e >> 5);
+      const uint32_t vb = (wk & 0x80000000u) ? (wk & 0x7FFFFFFFu) : ~wk;
+      sel_v[c] = __uint_as_float(vb);
+      if (w.lane == 0) cx.S.topk_idx[t * kMaxTopK + c] = (int)e;
     }
     if (w.lane == 0) {
       float sum = 0.f, ex[kMaxTopK];
@@ -1349,42 +1353,37 @@ __device__ void route_phase(Worker& w) {
   // GEMM1 B operand: the bf16 pooled vectors, one row per token, as f16 scaled by a
   // power of two per row (largest magnitude lands in [2^14, 2^15)).  Every bf16
   // value within 2^29 of the row's largest is exact in f16, so GEMM1 sees u as it
-  // is; the scale goes back in through x_ts in the GEMM1 epilogue.
-  // (the router stage already saw every element of u, so plain relaxed loads suffice here)
-  const uint16_t* u = reinterpret_cast<const uint16_t*>(P.x_cur + P.xo.u);
-  uint16_t* rowbuf = reinterpret_cast<uint16_t*>(cx.S.act + (size_t)dm.p * 32) + (size_t)w.cw * dm.p;
+  // is; the scale goes back in through x_ts in the GEMM1 epilogue.  The router phase
+  // left u staged in the activation buffer (bf16, same layout), so the rows are
+  // converted in place.
   uint8_t* actb = cx.S.act;
+  const int nch = dm.p / 8;
   for (int tt = 0; tt < 2 && w.ok; ++tt) {
     const int t = w.cw * 2 + tt;
-    const uint16_t* row = u + (size_t)t * dm.p;
-    float amax = 0.f;
-    for (int c0 = w.lane; c0 < dm.p / 8; c0 += 32 * 4) {
-      uint4 v[4];
+    uint32_t amax_bits = 0u;  // |x| of non-negative floats orders like its bits
+    for (int c = w.lane; c < nch; c += 32) {
+      const uint4 v = *reinterpret_cast<const uint4*>(actb + act_off(t, c * 8));
+      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (c0 + 32 * i < dm.p / 8) v[i] = ld_relaxed_v4(row + (c0 + 32 * i) * 8);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (c0 + 32 * i < dm.p / 8) {
-          *reinterpret_cast<uint4*>(rowbuf + (c0 + 32 * i) * 8) = v[i];
-          const uint32_t wd[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            amax = fmaxf(amax, fmaxf(fabsf(bf16_to_f32((uint16_t)(wd[j] & 0xFFFF))),
-                                     fabsf(bf16_to_f32((uint16_t)(wd[j] >> 16)))));
-        }
+      for (int j = 0; j < 4; ++j)
+        amax_bits = max(amax_bits, max((wd[j] & 0x7FFFu) << 16, wd[j] & 0x7FFF0000u));
     }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    __syncwarp();
+    amax_bits = __reduce_max_sync(0xffffffffu, amax_bits);
     if (tt == 0) stamp_rt(P, EV_XQ_ROW_IN);
+    const float amax = __uint_as_float(amax_bits);
     int ex = 0;
     if (amax > 0.f) frexpf(amax, &ex);  // amax = m 2^ex, m in [0.5, 1)
-    const float up = ldexpf(1.0f, 15 - ex);
-    for (int k = w.lane * 2; k < dm.p; k += 64) {
-      const uint32_t pr = *reinterpret_cast<const uint32_t*>(rowbuf + k);
-      const float lo = bf16_to_f32((uint16_t)(pr & 0xFFFF)) * up, hi = bf16_to_f32((uint16_t)(pr >> 16)) * up;
-      *reinterpret_cast<uint32_t*>(actb + act_off(t, k) + (k & 7) * 2) = pack_f16x2(lo, hi);
+    const float2 up = make_float2(ldexpf(1.0f, 15 - ex), ldexpf(1.0f, 15 - ex));
+    for (int c = w.lane; c < nch; c += 32) {
+      uint4* sp = reinterpret_cast<uint4*>(actb + act_off(t, c * 8));
+      const uint4 v = *sp;
+      uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __fmul2_rn(make_float2(__uint_as_float(wd[j] << 16), __uint_as_float(wd[j] & 0xFFFF0000u)), up);
+        wd[j] = pack_f16x2(f.x, f.y);
+      }
+      *sp = make_uint4(wd[0], wd[1], wd[2], wd[3]);
     }
     if (w.lane == 0) cx.S.x_ts[t] = ldexpf(1.0f, ex - 15);
     __syncwarp();
@@ -1460,7 +1459,9 @@ __device__ __forceinline__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* 
       exp_frags(cg, cg8, sg, sg8, kp, a[0][0], a[0][1], a[0][2], a[0][3]);
       exp_frags(cg, cg8, sg, sg8, kp + 1, a[1][0], a[1][1], a[1][2], a[1][3]);
       const uint32_t kstep = (uint32_t)(gi * 4 + kp + (mi >> 1)) * kKStepBytes;
-      for (int nt = 0; nt < ntiles; ++nt) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        if (nt >= ntiles) break;
         uint32_t b0, b1, b2, b3;
         ldsm_x4(bro[nt][kp >> 1] + kstep, b0, b1, b2, b3);
         mma_f16(acc[nt], a[0][0], a[0][1], a[0][2], a[0][3], b0, b1);
