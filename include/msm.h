@@ -266,8 +266,9 @@ msm_status msm_get_tree(msm_model* model, uint32_t* anc, int32_t* tpos);
  *   ready, partial sums stored, epilogue done), 40-43 GEMM1 of the first compute
  *   warp (first unit's tile ready / unit done, last unit's tile ready / done),
  *   44 / 45 loader issued the first / last o_proj tile, 46 / 47 the first / last
- *   GEMM1 tile; 48 + w / 56 + w compute warp w has staged its part of the pooler /
- *   o_proj input.
+ *   GEMM1 tile; 48-51 GEMM2 of the first compute warp pair (first unit's tile ready
+ *   / unit done, last unit's tile ready / done), 52 / 53 staging of the block's
+ *   second expert for GEMM2 begun / done.
  * `n` is the capacity of `buf` in elements. */
 #define MSM_TIMING_EVENTS 64
 msm_status msm_get_timing(msm_model* model, uint64_t* buf, size_t n);

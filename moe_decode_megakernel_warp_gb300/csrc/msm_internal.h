@@ -38,8 +38,10 @@ enum TimingEvent : int {
   EV_OP_U1_FIRST = 36, EV_OP_U1_LAST = 37, EV_OP_U1_RED = 38, EV_OP_U1_EPI = 39,
   EV_G1_FIRST_READY = 40, EV_G1_FIRST_DONE = 41, EV_G1_LAST_READY = 42, EV_G1_LAST_DONE = 43,
   EV_LD_OP_FIRST = 44, EV_LD_OP_LAST = 45, EV_LD_G1_FIRST = 46, EV_LD_G1_LAST = 47,
-  // staging of the pooler input (48 + warp) and of the o_proj input (56 + warp) done, per compute warp
-  EV_POOL_WARP_STAGED = 48, EV_OP_WARP_STAGED = 56
+  // GEMM2 of the first compute warp pair (first / last unit: tile ready, unit done) and
+  // the staging of the block's second expert (start, done)
+  EV_G2_FIRST_READY = 48, EV_G2_FIRST_DONE = 49, EV_G2_LAST_READY = 50, EV_G2_LAST_DONE = 51,
+  EV_G2_STAGE2_IN = 52, EV_G2_STAGE2_DONE = 53
 };
 
 // phases of one layer launch (recorded in the status word on a timeout)

@@ -560,9 +560,6 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, cons
     }
   }
   if (gain != nullptr && phase == PH_POOL) stamp_rt(*cx.P, EV_POOL_STAGED);
-  if ((cx.P->flags & 0x1u) && w.lane == 0 && (phase == PH_POOL || phase == PH_OPROJ))
-    cx.P->timing[(size_t)blockIdx.x * kTimingEvents + (phase == PH_POOL ? EV_POOL_WARP_STAGED : EV_OP_WARP_STAGED) +
-                 w.cw] = globaltimer();
   if (gain_smem) {
     uint4* gs = reinterpret_cast<uint4*>(cx.S.dred);
 #pragma unroll
@@ -1183,45 +1180,9 @@ __device__ void attn_merge_phase(Worker& w) {
 }
 
 // ---------------------------------------------------------------------------
-// routing: top-k per token, expert dispatch, NVFP4 quantisation of the pooled
-// activations (orcarouter.ai, § "where the kernel boundary sits": top-8 of 256,
-// experts in NVFP4)
+// routing: top-k per token, expert dispatch, GEMM1 input (orcarouter.ai, § "where
+// the kernel boundary sits": top-8 of 256, experts in NVFP4)
 // ---------------------------------------------------------------------------
-// quantise one row of n fp32 values (lane-parallel over 16-element blocks) into
-// f16 values e2m1 * e4m3-scale written by `put(block, j, f16x2 pair)`; returns the
-// row scale (amax / (6 * 448) rounded up to a power of two)
-template <class Get, class Put>
-__device__ __forceinline__ float nvfp4_row(int n, int lane, Get get, Put put) {
-  const int nb = n / 16;
-  float amax = 0.f;
-  for (int b = lane; b < nb; b += 32)
-    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(get(b * 16 + j)));
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  // row scale: amax / (6 * 448) rounded up to a power of two
-  float ts = __fdiv_rn(amax, 2688.0f);
-  if (ts > 0.f) {
-    int e;
-    const float m = frexpf(ts, &e);
-    if (m != 0.5f) ts = ldexpf(1.0f, e);
-  }
-  for (int b = lane; b < nb; b += 32) {
-    float bmax = 0.f;
-    for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(get(b * 16 + j)));
-    uint32_t sc = 0;
-    if (ts > 0.f) sc = f32_to_e4m3(__fdiv_rn(bmax, __fmul_rn(6.0f, ts)));
-    const float sv = e4m3_to_f32(sc);
-    const float denom = __fmul_rn(sv, ts);
-    const uint32_t s2 = e4m3x2_to_f16x2(sc | (sc << 8));
-    for (int j = 0; j < 16; j += 2) {
-      uint32_t code = 0;
-      if (sc != 0) code = f32x2_to_e2m1x2(__fdiv_rn(get(b * 16 + j), denom), __fdiv_rn(get(b * 16 + j + 1), denom));
-      put(b, j, hmul2(e2m1x2_to_f16x2(code), s2));
-    }
-  }
-  return ts;
-}
-
 __device__ void route_phase(Worker& w) {
   Ctx& cx = *w.cx;
   const LaunchParams& P = *cx.P;
@@ -1585,40 +1546,77 @@ __device__ void gemm2_phase(Worker& w) {
     for (int a = a_first; a <= a_last; ++a) {
       const int e = cx.S.act_e[a], n = cx.S.act_n[a];
       cbar();  // previous expert's units are done with the act buffer
+      if (a == a_first + 1) stamp_rt(P, EV_G2_STAGE2_IN);
       if (*cx.S.abort) w.ok = false;
       // stage this expert's NVFP4 activations: row p = p-th token of the expert
       for (int p = w.cw; p < n && w.ok; p += kComputeWarps) {
         const float* row = ain + (size_t)cx.S.act_slot[a * 16 + p] * dm.f;
         float* rowbuf = reinterpret_cast<float*>(cx.S.act + (size_t)dm.f * 32) + (size_t)w.cw * dm.f;
-        // poll the whole row into shared memory, 8 loads in flight per lane
-        for (int c0 = w.lane; c0 < dm.f / 4 && w.ok; c0 += 32 * 8) {
-          uint4 v[8];
+        // poll the row into shared memory (every pending chunk of a batch is re-read in
+        // the same round), tracking the row's largest magnitude on the way
+        const int nch4 = dm.f / 4;
+        uint32_t amax_bits = 0u;  // |x| of non-negative floats orders like its bits
+        constexpr int kB = 8;
+        for (int c0 = w.lane; c0 < nch4 && w.ok; c0 += 32 * kB) {
+          uint4 v[kB];
+          uint32_t pending = 0;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (c0 + 32 * i < dm.f / 4) v[i] = ld_relaxed_v4(row + (c0 + 32 * i) * 4);
+          for (int j = 0; j < kB; ++j)
+            if (c0 + 32 * j < nch4) pending |= 1u << j;
+          w.ok = poll_batch<kB>(cx, reinterpret_cast<const uint4*>(row) + c0, 32, v, pending,
+                                [](const uint4& x) { return f32x4_ready(x); }, PH_GEMM2);
+          if (!w.ok) break;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (c0 + 32 * i >= dm.f / 4 || !w.ok) continue;
-            if (!f32x4_ready(v[i])) w.ok = poll_f32x4(cx, row + (c0 + 32 * i) * 4, v[i], PH_GEMM2);
-            *reinterpret_cast<uint4*>(rowbuf + (c0 + 32 * i) * 4) = v[i];
+          for (int j = 0; j < kB; ++j) {
+            if (c0 + 32 * j >= nch4) continue;
+            *reinterpret_cast<uint4*>(rowbuf + (c0 + 32 * j) * 4) = v[j];
+            amax_bits = max(max(amax_bits, max(v[j].x & 0x7FFFFFFFu, v[j].y & 0x7FFFFFFFu)),
+                            max(v[j].z & 0x7FFFFFFFu, v[j].w & 0x7FFFFFFFu));
           }
         }
         w.ok = __all_sync(0xffffffffu, w.ok);
         if (!w.ok) break;
+        amax_bits = __reduce_max_sync(0xffffffffu, amax_bits);
         __syncwarp();
+        // NVFP4 of the row: per-row fp32 scale amax / (6 * 448) rounded up to a power of
+        // two, E4M3 block scale per 16 elements, E2M1 codes, every decision in fp32
+        // (the same steps as the oracle's quantiser); four lanes per 16-element block
+        const float amax = __uint_as_float(amax_bits);
+        float ts = __fdiv_rn(amax, 2688.0f);  // amax / (6 * 448), rounded up to a power of two
+        if (ts > 0.f) {
+          int ex;
+          const float m = frexpf(ts, &ex);
+          if (m != 0.5f) ts = ldexpf(1.0f, ex);
+        }
         uint8_t* act = cx.S.act;
-        float ts = nvfp4_row(
-            dm.f, w.lane, [&](int i) { return rowbuf[i]; },
-            [&](int b, int j, uint32_t h2) {
-              const int k = b * 16 + j;
-              *reinterpret_cast<uint32_t*>(act + act_off(p, k) + (k & 7) * 2) = h2;
-            });
+        for (int base = 0; base < dm.f; base += 128) {
+          const int k = base + w.lane * 4;
+          const bool in = k < dm.f;
+          const float4 x = in ? *reinterpret_cast<const float4*>(rowbuf + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+          float bmax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+          bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
+          bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 2));
+          uint32_t sc = 0;
+          if (ts > 0.f) sc = f32_to_e4m3(__fdiv_rn(bmax, __fmul_rn(6.0f, ts)));
+          const float denom = __fmul_rn(e4m3_to_f32(sc), ts);
+          const uint32_t s2 = e4m3x2_to_f16x2(sc | (sc << 8));
+          uint32_t c01 = 0, c23 = 0;
+          if (sc != 0) {
+            c01 = f32x2_to_e2m1x2(__fdiv_rn(x.x, denom), __fdiv_rn(x.y, denom));
+            c23 = f32x2_to_e2m1x2(__fdiv_rn(x.z, denom), __fdiv_rn(x.w, denom));
+          }
+          if (in) {
+            *reinterpret_cast<uint32_t*>(act + act_off(p, k) + (k & 7) * 2) = hmul2(e2m1x2_to_f16x2(c01), s2);
+            *reinterpret_cast<uint32_t*>(act + act_off(p, k + 2) + ((k + 2) & 7) * 2) = hmul2(e2m1x2_to_f16x2(c23), s2);
+          }
+        }
         __syncwarp();
         if (w.lane == 0) cx.S.a_ts[p] = ts;
       }
       w.ok = __all_sync(0xffffffffu, w.ok);
       cbar();
       if (a == a_first) stamp_rt(P, EV_GEMM2_IN);
+      if (a == a_first + 1) stamp_rt(P, EV_G2_STAGE2_DONE);
       if (*cx.S.abort) w.ok = false;
       const int u_lo = max(lo, a * u2pe), u_hi = min(hi, (a + 1) * u2pe);
       // units of this expert: pair j takes every 4th (counted from the block's first unit)
@@ -1629,6 +1627,10 @@ __device__ void gemm2_phase(Worker& w) {
         const uint32_t t = w.ti + (uint32_t)loc;
         const uint32_t s = t % kSlots;
         bool got = w.ok && wait_tile(cx, t, PH_GEMM2);
+        const bool first_u = gu - pair < lo + kComputeWarps / 2 && a == a_first;
+        const bool last_u = gu + kComputeWarps / 2 >= hi;
+        if (half == 0 && first_u) stamp_rt(P, EV_G2_FIRST_READY);
+        if (half == 0 && last_u) stamp_rt(P, EV_G2_LAST_READY);
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         if (got) {
           const int r8 = w.lane & 7;
@@ -1656,6 +1658,8 @@ __device__ void gemm2_phase(Worker& w) {
               }
             }
         }
+        if (half == 0 && first_u) stamp_rt(P, EV_G2_FIRST_DONE);
+        if (half == 0 && last_u) stamp_rt(P, EV_G2_LAST_DONE);
       }
     }
   }

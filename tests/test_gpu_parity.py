@@ -31,7 +31,11 @@ def check_tree(case, got):
     assert np.array_equal(g_tpos, case.pos0 + depth)
 
 
-def check_routing(case, ref, got, strict_margin=1e-3):
+def check_routing(case, ref, got, strict_margin=1e-3, order_sep=1e-2):
+    """Top-k set equal wherever the oracle's k-th / (k+1)-th margin is >= strict_margin
+    (the seeds guarantee it); order equal where consecutive selected logits differ by
+    more than order_sep (the GPU's fp32 logits differ from the oracle's by up to a few
+    1e-3)."""
     idx_g, w_g = got["routing"]
     for l, tr in enumerate(ref["traces"]):
         idx_o = tr["topk_idx"]
@@ -42,8 +46,8 @@ def check_routing(case, ref, got, strict_margin=1e-3):
             # order: equal wherever consecutive oracle logits are well separated
             lg = tr["router_logits"][t][idx_o[t]]
             for c in range(case.cfg.k):
-                sep_prev = c == 0 or lg[c - 1] - lg[c] > strict_margin
-                sep_next = c == case.cfg.k - 1 or lg[c] - lg[c + 1] > strict_margin
+                sep_prev = c == 0 or lg[c - 1] - lg[c] > order_sep
+                sep_next = c == case.cfg.k - 1 or lg[c] - lg[c + 1] > order_sep
                 if sep_prev and sep_next and mg[t] >= strict_margin:
                     assert idx_g[l, t, c] == idx_o[t, c]
         # weights: softmax over the selected logits (fp32 on the GPU, fp64 in the oracle)
