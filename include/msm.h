@@ -110,11 +110,12 @@ typedef struct {
   int attn_splits;  /* KV splits per kv head; 0 = automatic */
   int prefetch_experts; /* experts prefetched by MSM_FLAG_EXPERT_PREFETCH; 0 = 14 */
   uint32_t timeout_us;  /* bounded-wait limit; 0 = 200000 */
-  int l2_runahead_kb;   /* L2 prefetch distance of each block's weight / KV stream, KiB;
-                           0 = off (alphasignal.ai, § "Four mechanisms keep work
-                           moving": weights for the next operation are fetched while
-                           the current one runs, partly staged in L2).  Measured
-                           slower than off on the 62-layer workload, hence off. */
+  int l2_runahead_kb;   /* L2 prefetch distance of each block's dense-weight / KV
+                           stream (expert tiles are not prefetched), KiB; 0 = off
+                           (alphasignal.ai, § "Four mechanisms keep work moving":
+                           weights for the next operation are fetched while the
+                           current one runs, partly staged in L2).  Measured slower
+                           than off on the 62-layer workload (32 KiB: +7 %), hence off. */
 } msm_config;
 
 /* Device pointers, one per layer (host arrays of n_layers entries). */
@@ -268,7 +269,8 @@ msm_status msm_get_tree(msm_model* model, uint32_t* anc, int32_t* tpos);
  *   44 / 45 loader issued the first / last o_proj tile, 46 / 47 the first / last
  *   GEMM1 tile; 48-51 GEMM2 of the first compute warp pair (first unit's tile ready
  *   / unit done, last unit's tile ready / done), 52 / 53 staging of the block's
- *   second expert for GEMM2 begun / done.
+ *   second expert for GEMM2 begun / done, 54 loader issued the first tile of the
+ *   block's second o_proj unit.
  * `n` is the capacity of `buf` in elements. */
 #define MSM_TIMING_EVENTS 64
 msm_status msm_get_timing(msm_model* model, uint64_t* buf, size_t n);

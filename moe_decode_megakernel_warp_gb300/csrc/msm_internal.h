@@ -41,7 +41,8 @@ enum TimingEvent : int {
   // GEMM2 of the first compute warp pair (first / last unit: tile ready, unit done) and
   // the staging of the block's second expert (start, done)
   EV_G2_FIRST_READY = 48, EV_G2_FIRST_DONE = 49, EV_G2_LAST_READY = 50, EV_G2_LAST_DONE = 51,
-  EV_G2_STAGE2_IN = 52, EV_G2_STAGE2_DONE = 53
+  EV_G2_STAGE2_IN = 52, EV_G2_STAGE2_DONE = 53,
+  EV_LD_OP_U1 = 54  // loader issued the first tile of the block's second o_proj unit
 };
 
 // phases of one layer launch (recorded in the status word on a timeout)

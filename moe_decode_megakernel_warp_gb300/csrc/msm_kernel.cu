@@ -87,6 +87,7 @@ struct Ctx {
   const LaunchParams* P;
   Smem S;
   uint64_t deadline;
+  uint64_t next_abort_check = 0;
   int block;
 
   __device__ __noinline__ void fail(int phase) {
@@ -98,16 +99,22 @@ struct Ctx {
     }
     atomicExch(&P->status->abort, 1);
   }
-  // true when the caller must give up
+  // true when the caller must give up.  The grid-wide abort word lives in global
+  // memory: it is read at most every 4 us per thread, since a global round trip in
+  // a spin loop would delay the caller's notice of the very data it waits for.
   __device__ bool expired(int phase) {
     if (*S.abort) return true;
-    if (ld_relaxed_u32(&P->status->abort) != 0) {
-      *S.abort = 1;
-      return true;
-    }
-    if (globaltimer() > deadline) {
+    const uint64_t now = globaltimer();
+    if (now > deadline) {
       fail(phase);
       return true;
+    }
+    if (now >= next_abort_check) {
+      next_abort_check = now + 4000;
+      if (ld_relaxed_u32(&P->status->abort) != 0) {
+        *S.abort = 1;
+        return true;
+      }
     }
     return false;
   }
@@ -253,6 +260,7 @@ struct RunAhead {
     pref = used = 0;
     ahead = a;
   }
+  // (ptr == nullptr: bytes the ring streams that are not prefetched)
   __device__ void add(const void* ptr, uint64_t bytes) {
     if (!ahead || bytes == 0 || count == kMaxRanges) return;
     p[count] = static_cast<const uint8_t*>(ptr);
@@ -262,7 +270,7 @@ struct RunAhead {
   __device__ void pump() {
     while (i < count && pref < used + ahead) {
       const uint32_t c = min(n[i] - off, 65536u);
-      prefetch_l2(p[i] + off, c);
+      if (p[i]) prefetch_l2(p[i] + off, c);
       off += c;
       pref += c;
       if (off == n[i]) {
@@ -375,6 +383,8 @@ __device__ bool load_dense(Ctx& cx, Ring& r, const uint8_t* W, int K, int N, int
       if (!ring_issue(cx, r, &sg, 1, pol)) return false;
       if (trace >= 0 && (P.flags & 0x1u) && ((u == lo && k0 == 0) || (u == hi - 1 && k0 + kDenseTileSteps >= steps)))
         P.timing[(size_t)cx.block * kTimingEvents + trace + (u == lo && k0 == 0 ? 0 : 1)] = globaltimer();
+      if (trace >= 0 && (P.flags & 0x1u) && u == lo + 1 && k0 == 0)
+        P.timing[(size_t)cx.block * kTimingEvents + EV_LD_OP_U1] = globaltimer();
     }
   }
   (void)P;
@@ -437,12 +447,10 @@ __device__ void loader(Ctx& cx) {
       for (int pass = 0; pass < 2; ++pass) {
         const int upe = pass ? u2pe : u1pe;
         const uint64_t ub = pass ? ub2 : ub1;
-        const uint8_t* W = pass ? P.w2 : P.w1;
         unit_range(na * upe, rot_block(cx.block, P.phase_rot * (pass ? 7 : 6), G), G, lo, hi);
         for (int gu = lo; gu < hi;) {
-          const int e = cx.S.act_e[gu / upe];
           const int run = min(hi, (gu / upe + 1) * upe) - gu;
-          r.ra.add(W + ((uint64_t)e * upe + gu % upe) * ub, (uint64_t)run * ub);
+          r.ra.add(nullptr, (uint64_t)run * ub);  // expert tiles: streamed, not prefetched
           gu += run;
         }
       }
@@ -683,8 +691,9 @@ struct EpiArgs {
 };
 
 // epilogue of output rows u*16 + p and u*16 + p + 8 for token t (values lo, hi)
+// (res2: the residual pair of rows p, p+8 when has_res, else read here)
 __device__ void dense_epi(const LaunchParams& P, const Smem& S, const EpiArgs& ea, int u, int p, int t,
-                                       float lo, float hi) {
+                                       float lo, float hi, bool has_res = false, uint32_t res2 = 0) {
   const Dims& dm = P.dm;
   switch (ea.kind) {
     case EPI_QKV:
@@ -699,7 +708,9 @@ __device__ void dense_epi(const LaunchParams& P, const Smem& S, const EpiArgs& e
         // test hook: the first element of the whole h1 exchange is never written
         if (ea.kind == EPI_OPROJ && (P.flags & 0x10000u) && u == 0 && t == 0 && p == 0 && hf == 0) continue;
         const float o = bf16_to_f32(bf16_bits_rn(v2[hf]));
-        const uint16_t r = ea.kind == EPI_OPROJ ? ea.res[(size_t)t * dm.d + n] : ld_relaxed_u16(ea.res + (size_t)t * dm.d + n);
+        const uint16_t r = has_res ? (uint16_t)(hf ? res2 >> 16 : res2 & 0xFFFFu)
+                           : ea.kind == EPI_OPROJ ? ea.res[(size_t)t * dm.d + n]
+                                                  : ld_relaxed_u16(ea.res + (size_t)t * dm.d + n);
         const uint16_t v = bf16_bits_rn(bf16_to_f32(r) + o);
         st_relaxed_u16(ea.out + (size_t)t * dm.d + n, v);
         if (ea.out2) ea.out2[(size_t)t * dm.d + n] = v;
@@ -737,7 +748,13 @@ __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, 
   unit_range(N / 16, rot_block(cx.block, rot, G), G, lo, hi);
   const int steps = K / 16;
   const int ktiles = (steps + kDenseTileSteps - 1) / kDenseTileSteps;
-  // this warp's k-steps of a tile are 4 cw .. 4 cw + 3, so k-step & 3 is the loop index
+  // The compute warps form two groups of four; group g consumes the unit's tiles
+  // kt = g, g + 2, ... and warp wi of a group takes k-steps 8 wi .. 8 wi + 7 of a tile,
+  // so two tiles are consumed at a time (a tile held by all eight warps at once would
+  // be released only after one warp's whole dependent MMA chain).  k-step & 3 is the
+  // loop index & 3.
+  const int group = w.cw >> 2, wi = w.cw & 3;
+  constexpr int kStepsPerWarp = kDenseTileSteps / 4;
   uint32_t act_lane[4];
 #pragma unroll
   for (int ii = 0; ii < 4; ++ii) {
@@ -746,34 +763,59 @@ __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, 
   }
   float* red = cx.S.dred;  // [8 warps][16 rows][16 tokens]
   const int tid = w.cw * 32 + w.lane;
-  const int ks_lo = w.cw * (kDenseTileSteps / kComputeWarps);
+  const int ks_lo = wi * kStepsPerWarp;
+  // the residual inputs of the o_proj / unpooler epilogues do not depend on this phase:
+  // read them for the block's first units now, while the tiles stream in
+  constexpr int kPreUnits = 4;
+  uint32_t pre[kPreUnits];
+  const bool pre_res = (ea.kind == EPI_OPROJ || ea.kind == EPI_UNPOOL) && tid < 128;
+  if (pre_res) {
+    const int d = cx.P->dm.d, p = tid >> 4, tok = tid & 15;
+#pragma unroll
+    for (int i = 0; i < kPreUnits; ++i) {
+      pre[i] = 0u;
+      if (lo + i < hi) {
+        const uint16_t* r = ea.res + (size_t)tok * d + (lo + i) * 16 + p;
+        const uint32_t a = ea.kind == EPI_OPROJ ? r[0] : ld_relaxed_u16(r);
+        const uint32_t b = ea.kind == EPI_OPROJ ? r[8] : ld_relaxed_u16(r + 8);
+        pre[i] = a | (b << 16);
+      }
+    }
+  }
   for (int u = lo; u < hi; ++u) {
     const int loc = u - lo;
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    for (int kt = 0; kt < ktiles; ++kt) {
+    float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // odd k-steps
+    for (int kt = group; kt < ktiles; kt += 2) {
       const uint32_t t = w.ti + (uint32_t)(loc * ktiles + kt);
       const uint32_t s = t % kSlots;
       if (w.ok) w.ok = wait_tile(cx, t, 50);
-      if (trace >= 0 && loc < 2 && (kt == 0 || kt == ktiles - 1)) stamp_rt(*cx.P, trace + loc * 4 + (kt ? 1 : 0));
+      if (trace >= 0 && loc < 2 && (kt == group || kt + 2 >= ktiles))
+        stamp_rt(*cx.P, trace + loc * 4 + (kt == group ? 0 : 1));
       if (w.ok) {
         const uint32_t wbase = smem_u32(cx.S.ring + cx.S.slot_off[s]) + lane_mat_off(w.lane);
         const int k0 = kt * kDenseTileSteps;
         const int ns = min(kDenseTileSteps, steps - k0);
-        const int ke = min(ns, ks_lo + kDenseTileSteps / kComputeWarps);
+        const int ke = min(ns, ks_lo + kStepsPerWarp);
 #pragma unroll
-        for (int ii = 0; ii < kDenseTileSteps / kComputeWarps; ++ii) {
+        for (int ii = 0; ii < kStepsPerWarp; ++ii) {
           const int i = ks_lo + ii;
           if (i >= ke) break;
           uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
           ldsm_x4(wbase + i * kKStepBytes, a0, a1, a2, a3);
-          ldsm_x4(act_lane[ii] + (k0 + i) * kKStepBytes, b0, b1, b2, b3);
-          mma_bf16(acc[0], a0, a1, a2, a3, b0, b1);
-          mma_bf16(acc[1], a0, a1, a2, a3, b2, b3);
+          ldsm_x4(act_lane[ii & 3] + (k0 + i) * kKStepBytes, b0, b1, b2, b3);
+          float(&c)[2][4] = (ii & 1) ? acc2 : acc;
+          mma_bf16(c[0], a0, a1, a2, a3, b0, b1);
+          mma_bf16(c[1], a0, a1, a2, a3, b2, b3);
         }
         __syncwarp();
-        if (w.lane == 0) mbar_arrive(&cx.S.empty[s], 1);
+        if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps / 4);
       }
     }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[nt][i] += acc2[nt][i];
     // partials -> shared memory: rows g / g+8, tokens nt*8 + 2q (+1)
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -792,7 +834,11 @@ __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, 
         vlo += red[(ww * 16 + p) * 16 + tok];
         vhi += red[(ww * 16 + p + 8) * 16 + tok];
       }
-      dense_epi(*cx.P, cx.S, ea, u, p, tok, vlo, vhi);
+      uint32_t r2 = 0u;
+#pragma unroll
+      for (int i = 0; i < kPreUnits; ++i)
+        if (loc == i) r2 = pre[i];
+      dense_epi(*cx.P, cx.S, ea, u, p, tok, vlo, vhi, pre_res && loc < kPreUnits, r2);
     }
     cbar();
     if (trace >= 0 && loc < 2) stamp_rt(*cx.P, trace + loc * 4 + 3);

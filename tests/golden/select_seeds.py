@@ -11,7 +11,11 @@ experts, the routing pattern of the pages' profiling runs (orcarouter.ai,
 "Muse Spark Open: 1,109 tokens/s is a kernel-level change", § "what the number
 is": 49 experts per layer).  Calls only oracle/ and synth/.
 
-    python tests/golden/select_seeds.py cfg1 cfg1_stack [cfg2 cfg3]
+    python tests/golden/select_seeds.py cfg1 cfg1_stack [cfg2 cfg3 cfg4]
+
+Deep stacks (the 62-layer workload) keep the weight seed and choose each layer's
+bias seed for the margin rule only (margin 1e-2), drawing just the routed experts
+of a layer.
 """
 import json
 import os
@@ -26,11 +30,14 @@ import oracle  # noqa: E402
 import synth  # noqa: E402
 
 MARGIN = 1e-3
+# the 62-layer stack: the GPU's router logits differ from the oracle's by up to a few
+# 1e-3 (bf16 rounding of the pooled vector), so its seeds keep a 1e-2 margin
+DEEP_MARGIN = 1e-2
 
 
-def margin_ok(logits, k):
+def margin_ok(logits, k, margin=MARGIN):
     s = -np.sort(-logits.astype(np.float64), axis=1)
-    return bool(np.all(s[:, k - 1] - s[:, k] >= MARGIN))
+    return bool(np.all(s[:, k - 1] - s[:, k] >= margin))
 
 
 def run_layers(cfg, seed, bias_for_layer):
@@ -60,8 +67,39 @@ def run_layers(cfg, seed, bias_for_layer):
     return chosen
 
 
+def run_stack_routed(cfg, seed, max_tries):
+    """Per-layer bias seeds for a deep full-width stack (margin rule only), drawing
+    only the routed experts of each layer (tests/full_stack.py)."""
+    sys.path.insert(0, os.path.dirname(HERE))
+    import full_stack
+    h = synth.hidden_in(cfg, seed)
+    parent = synth.parent_array(seed)
+    experts = full_stack.ExpertArrays(cfg)
+    chosen = []
+    for l in range(cfg.n_layers):
+        w = synth.layer_weights(cfg, seed, l, bias_seed=1, experts=False)
+        w.update(experts.as_dict())
+        k, v = synth.kv_history(cfg, seed, l)
+        experts.clear()
+        for bs in range(1, max_tries):
+            w["b_router"] = synth.router_bias(cfg, bs, l)
+            logits, idx = full_stack.routing_pass(cfg, w, l, h, parent, cfg.pos0, k, v)
+            if margin_ok(logits, cfg.k, DEEP_MARGIN):
+                break
+        else:
+            raise SystemExit("no bias seed found for layer %d" % l)
+        h, _ = full_stack.full_layer(cfg, seed, l, {a: b for a, b in w.items() if not a.startswith("w1") and
+                                                      not a.startswith("w2")}, experts, h, parent, cfg.pos0,
+                                     k, v, idx)
+        chosen.append(bs)
+        print("layer", l, "bias seed", bs, "distinct experts", len(np.unique(idx)), flush=True)
+    return chosen
+
+
 def select(name, max_tries=400):
     cfg = synth.CONFIGS[name]
+    if cfg.n_layers > 8:
+        return {"seed": 1, "bias_seeds": run_stack_routed(cfg, 1, max_tries)}
     if cfg.n_hot > 0:
         chosen = run_layers(cfg, 1, lambda l: range(1, max_tries))
         if chosen is None:
