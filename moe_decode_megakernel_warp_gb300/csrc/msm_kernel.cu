@@ -49,9 +49,11 @@ struct Smem {
   float* a_ts;        // [16]
   float* red;         // [8][16]
   volatile uint32_t* slot_tile;  // [kSlots] index of the tile the loader last put in each slot
+  struct Ring* ring_state;        // the loader's ring bookkeeping
   float* dred;        // [8][16][16] dense-phase cross-warp partial sums
 };
 
+constexpr int kRingStateOff = 6656;  // in the small area, below the reduction scratch at 8192
 __device__ __forceinline__ Smem carve(uint8_t* base, const LaunchParams& P) {
   Smem s;
   s.ring = base;
@@ -76,6 +78,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const LaunchParams& P) {
   s.a_ts = reinterpret_cast<float*>(sm + 6016);
   s.red = reinterpret_cast<float*>(sm + 6080);
   s.slot_tile = reinterpret_cast<volatile uint32_t*>(sm + 6592);
+  s.ring_state = reinterpret_cast<struct Ring*>(sm + kRingStateOff);
   s.dred = reinterpret_cast<float*>(sm + 8192);
   return s;
 }
@@ -288,6 +291,7 @@ struct Ring {
   uint32_t off[kSlots], end[kSlots];
   RunAhead ra;
 };
+static_assert(kRingStateOff + sizeof(Ring) <= 8192, "ring bookkeeping overlaps the reduction scratch");
 
 __device__ bool ring_place(Ctx& cx, Ring& r, uint32_t bytes, uint32_t& off_out) {
   const uint32_t cap = (uint32_t)cx.P->ring_bytes;
@@ -309,30 +313,19 @@ __device__ bool ring_place(Ctx& cx, Ring& r, uint32_t bytes, uint32_t& off_out) 
   return true;
 }
 
-struct Seg {
-  const void* src;
-  uint32_t bytes;
-};
-
-// issue one tile made of up to 4 contiguous segments
-__device__ bool ring_issue(Ctx& cx, Ring& r, const Seg* seg, int nseg, uint64_t pol) {
-  uint32_t total = 0;
-  for (int i = 0; i < nseg; ++i) total += seg[i].bytes;
+// issue one tile (one contiguous run of bytes)
+__device__ bool ring_issue(Ctx& cx, Ring& r, const uint8_t* src, uint32_t bytes, uint64_t pol) {
   uint32_t off;
-  if (!ring_place(cx, r, total, off)) return false;
+  if (!ring_place(cx, r, bytes, off)) return false;
   const uint32_t s = r.issued % kSlots;
   r.off[s] = off;
-  r.end[s] = off + total;
+  r.end[s] = off + bytes;
   cx.S.slot_off[s] = off;
   cx.S.slot_tile[s] = r.issued;
-  mbar_expect_tx(&cx.S.full[s], total);
-  uint32_t o = off;
-  for (int i = 0; i < nseg; ++i) {
-    bulk_g2s(cx.S.ring + o, seg[i].src, seg[i].bytes, &cx.S.full[s], pol);
-    o += seg[i].bytes;
-  }
+  mbar_expect_tx(&cx.S.full[s], bytes);
+  bulk_g2s(cx.S.ring + off, src, bytes, &cx.S.full[s], pol);
   ++r.issued;
-  r.ra.used += total;
+  r.ra.used += bytes;
   r.ra.pump();
   return true;
 }
@@ -379,8 +372,8 @@ __device__ bool load_dense(Ctx& cx, Ring& r, const uint8_t* W, int K, int N, int
   for (int u = lo; u < hi; ++u) {
     for (int k0 = 0; k0 < steps; k0 += kDenseTileSteps) {
       int ns = min(kDenseTileSteps, steps - k0);
-      Seg sg = {W + (uint64_t)u * ub + (uint64_t)k0 * kKStepBytes, (uint32_t)ns * kKStepBytes};
-      if (!ring_issue(cx, r, &sg, 1, pol)) return false;
+      const uint8_t* src = W + (uint64_t)u * ub + (uint64_t)k0 * kKStepBytes;
+      if (!ring_issue(cx, r, src, (uint32_t)ns * kKStepBytes, pol)) return false;
       if (trace >= 0 && (P.flags & 0x1u) && ((u == lo && k0 == 0) || (u == hi - 1 && k0 + kDenseTileSteps >= steps)))
         P.timing[(size_t)cx.block * kTimingEvents + trace + (u == lo && k0 == 0 ? 0 : 1)] = globaltimer();
       if (trace >= 0 && (P.flags & 0x1u) && u == lo + 1 && k0 == 0)
@@ -399,7 +392,10 @@ __device__ void loader(Ctx& cx) {
   const uint64_t pol = policy_evict_first();
   prefetch_tensormap(&P.tmap_k);
   prefetch_tensormap(&P.tmap_v);
-  Ring r;
+  // the ring's bookkeeping lives in shared memory: as a local array it would sit in
+  // the small L1 left beside a 227 KB carve-out, and its lines, evicted by the compute
+  // warps' traffic, would cost the loader an L2 round trip per access
+  Ring& r = *cx.S.ring_state;
   r.issued = r.tail = r.head = 0;
   r.ra.init(P.runahead_bytes);
   bool ok = true;
@@ -462,16 +458,14 @@ __device__ void loader(Ctx& cx) {
     unit_range(na * u1pe, rot_block(cx.block, P.phase_rot * 6, G), G, lo, hi);
     for (int gu = lo; ok && gu < hi; ++gu) {
       int e = cx.S.act_e[gu / u1pe];
-      Seg sg = {P.w1 + ((uint64_t)e * u1pe + gu % u1pe) * ub1, (uint32_t)ub1};
-      ok = ring_issue(cx, r, &sg, 1, pol);
+      ok = ring_issue(cx, r, P.w1 + ((uint64_t)e * u1pe + gu % u1pe) * ub1, (uint32_t)ub1, pol);
       if (gu == lo) stamp<kTiming>(P, cx.block, EV_LD_G1_FIRST);
       if (gu == hi - 1) stamp<kTiming>(P, cx.block, EV_LD_G1_LAST);
     }
     unit_range(na * u2pe, rot_block(cx.block, P.phase_rot * 7, G), G, lo, hi);
     for (int gu = lo; ok && gu < hi; ++gu) {
       int e = cx.S.act_e[gu / u2pe];
-      Seg sg = {P.w2 + ((uint64_t)e * u2pe + gu % u2pe) * ub2, (uint32_t)ub2};
-      ok = ring_issue(cx, r, &sg, 1, pol);
+      ok = ring_issue(cx, r, P.w2 + ((uint64_t)e * u2pe + gu % u2pe) * ub2, (uint32_t)ub2, pol);
     }
   }
   ok = ok && load_dense(cx, r, P.w_unpool, dm.p, dm.d, P.phase_rot * 8, pol);
