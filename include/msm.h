@@ -93,8 +93,9 @@ typedef enum {
                                           5.9 ms still goes") */
 #define MSM_FLAG_PDL 0x8u              /* chain layer launches with programmatic
                                           dependent launch */
-#define MSM_FLAG_TEST_DROP_HANDOFF 0x10000u /* test hook: one producer never fills one
-                                          exchange slot, so its consumers time out */
+#define MSM_FLAG_TEST_DROP_HANDOFF 0x10000u /* test hook: one block never signals that
+                                          its share of h1 is stored, so the pooler's
+                                          consumers time out */
 
 typedef struct {
   int d_model, n_q_heads, n_kv_heads, head_dim;

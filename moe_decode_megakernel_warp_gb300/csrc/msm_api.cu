@@ -147,13 +147,19 @@ msm_status encode_kv_map(msm_model* m, CUtensorMap* map, const void* ptr) {
   return MSM_OK;
 }
 
+// sentinels (bf16 0xFFFF, fp32 -0.0) in one exchange buffer, its counters zeroed
+msm_status arm_exchange(uint8_t* x, const XOffsets& o, cudaStream_t s) {
+  CK(launch_fill_u32(x, o.logits / 4, 0xFFFFFFFFu, s));                       // o, h1, u
+  CK(launch_fill_u32(x + o.logits, (o.z - o.logits) / 4, 0x80000000u, s));    // logits, a
+  CK(launch_fill_u32(x + o.z, (o.cnt - o.z) / 4, 0xFFFFFFFFu, s));            // z, h2, q0, tkv0
+  CK(launch_fill_u32(x + o.cnt, (o.total - o.cnt) / 4, 0u, s));               // counters
+  return MSM_OK;
+}
+
 msm_status rearm_all(msm_model* m, cudaStream_t s) {
   for (int c = 0; c < 2; ++c) {
-    uint8_t* x = m->x[c];
-    const XOffsets& o = m->xo;
-    CK(launch_fill_u32(x, o.logits / 4, 0xFFFFFFFFu, s));                       // o, h1, u
-    CK(launch_fill_u32(x + o.logits, (o.z - o.logits) / 4, 0x80000000u, s));    // logits, a
-    CK(launch_fill_u32(x + o.z, (o.total - o.z) / 4, 0xFFFFFFFFu, s));          // z, h2, q0, tkv0
+    msm_status st = arm_exchange(m->x[c], m->xo, s);
+    if (st != MSM_OK) return st;
   }
   CK(launch_fill_u32(m->sbuf, m->so.y / 4, 0x80000000u, s));                    // part, ml
   CK(launch_fill_u32(m->sbuf + m->so.y, (m->so.total - m->so.y) / 4, 0xFFFFFFFFu, s));  // y
@@ -321,6 +327,7 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   xo.h2 = o; o += align256((uint64_t)T * dm.d * 2);
   xo.q0 = o; o += align256((uint64_t)T * dm.hq * dm.hd * 2);
   xo.tkv0 = o; o += align256(2ull * dm.hkv * T * dm.hd * 2);
+  xo.cnt = o; o += kCounterBytes;
   xo.total = o;
   SOffsets& so = m->so;
   o = 0;
@@ -696,12 +703,10 @@ extern "C" msm_status msm_verify_step_noalloc(msm_model* m, const void* hidden_i
     }
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // arm the exchange part with its sentinels (bf16 0xFFFF, fp32 -0.0) on the caller's stream
-  const XOffsets& o = m->xo;
+  // arm the exchange part (sentinels, zeroed counters) on the caller's stream
   for (int c = 0; c < 2; ++c) {
-    CK(launch_fill_u32(xs[c], o.logits / 4, 0xFFFFFFFFu, s));
-    CK(launch_fill_u32(xs[c] + o.logits, (o.z - o.logits) / 4, 0x80000000u, s));
-    CK(launch_fill_u32(xs[c] + o.z, (o.total - o.z) / 4, 0xFFFFFFFFu, s));
+    st = arm_exchange(xs[c], m->xo, s);
+    if (st != MSM_OK) return st;
   }
   CK(launch_fill_u32(sb, m->so.y / 4, 0x80000000u, s));
   CK(launch_fill_u32(sb + m->so.y, (m->so.total - m->so.y) / 4, 0xFFFFFFFFu, s));

@@ -65,8 +65,24 @@ struct DevStatus {
 // Exchange buffers of one launch parity (byte offsets into the parity's region).
 struct XOffsets {
   uint64_t o, h1, u, logits, a, z, h2, q0, tkv0;  // re-armed by the next launch
+  uint64_t cnt;                                   // phase-completion counters, zeroed likewise
   uint64_t total;
 };
+// Phase-completion counters of one launch: every block adds 1 to counter i once it
+// has stored its share of phase i; a consumer of the phase's output waits until the
+// counter equals the grid size, then reads the output without sentinel checks.
+enum PhaseCounter : int {
+  CNT_ATTN = 0,    // attention partials (m, l, acc) of every (kv head, split)
+  CNT_MERGE = 1,   // attention output o
+  CNT_OPROJ = 2,   // h1
+  CNT_POOL = 3,    // pooled u
+  CNT_ROUTER = 4,  // router logits
+  CNT_GEMM2 = 5,   // expert outputs y
+  CNT_COMBINE = 6, // combined z
+  CNT_UNPOOL = 7,  // h2
+  kPhaseCounters = 8
+};
+constexpr int kCounterBytes = 256;
 // Buffers drained by their single consumer (never double-buffered).
 struct SOffsets {
   uint64_t part, ml, y;

@@ -498,6 +498,45 @@ struct Worker {
 
 __device__ __forceinline__ void cbar() { named_bar(1, kComputeThreads); }
 
+__device__ __forceinline__ uint32_t* phase_counter(const LaunchParams& P, int i) {
+  return reinterpret_cast<uint32_t*>(P.x_cur + P.xo.cnt) + i;
+}
+
+// The block has stored its share of phase i: the named barrier orders every compute
+// thread's stores before one thread's gpu-scope fence, and the counter add after it.
+// (Test hook: block 0 never signals the o_proj phase, so its consumers time out.)
+__device__ void publish(Worker& w, int i) {
+  cbar();
+  if (w.cw == 0 && w.lane == 0) {
+    const LaunchParams& P = *w.cx->P;
+    if ((P.flags & 0x10000u) && i == CNT_OPROJ && blockIdx.x == 0) return;
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(phase_counter(P, i)) : "memory");
+  }
+}
+
+// Wait until every block has published phase i.  One thread polls the counter with
+// acquire loads; the named barrier then orders the other compute threads' loads of
+// the phase's output after that observation.  The outputs are read with relaxed
+// (L2-coherent) loads and no sentinel checks.  A wait that runs out sets the abort.
+__device__ bool await_phase(Worker& w, int i, int phase) {
+  Ctx& cx = *w.cx;
+  if (w.cw == 0 && w.lane == 0 && !*cx.S.abort) {
+    const uint32_t* c = phase_counter(*cx.P, i);
+    const uint32_t target = gridDim.x;
+    uint32_t n = 0;
+    for (;;) {
+      uint32_t v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+      if (v >= target) break;
+      if ((++n & 15) == 0 && cx.expired(phase)) break;
+    }
+  }
+  cbar();
+  if (*cx.S.abort) w.ok = false;
+  return w.ok;
+}
+
 // B-operand layout of a [16 tokens][K] activation: per 16-column k-step four 8x8
 // matrices m (tokens 0-7 | k 0-7, tokens 0-7 | k 8-15, tokens 8-15 | k 0-7,
 // tokens 8-15 | k 8-15), 16 bytes per matrix row.  Row r of matrix m of k-step ks
@@ -510,12 +549,12 @@ __device__ __forceinline__ uint32_t act_off(int t, int k) {
   return (uint32_t)ks * kKStepBytes + (uint32_t)m * 128u + ((((uint32_t)t & 7u) ^ act_sw(ks, m)) << 4);
 }
 
-// Stage a [16][K] bf16 activation from global memory into the B layout,
-// optionally polling its sentinels and applying RMSNorm with `gain`.
-__device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, const uint16_t* gain,
+// Stage a [16][K] bf16 activation from global memory into the B layout, optionally
+// applying RMSNorm with `gain`.  cnt >= 0: wait for every block to publish that
+// phase counter first; else, with `poll`, poll each chunk's sentinels; else plain loads.
+__device__ bool stage_act(Worker& w, const uint16_t* src, int K, int cnt, bool poll, const uint16_t* gain,
                                        float eps, int phase) {
   Ctx& cx = *w.cx;
-  cbar();  // every compute warp is done with the act buffer
   const int tid = w.cw * 32 + w.lane;
   const int t = tid >> 4, sub = tid & 15;
   const int nch = K / 8;
@@ -531,6 +570,10 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, cons
     for (int j = 0; j < 2; ++j)
       if (tid + j * kComputeThreads < nch) gpre[j] = ld_nc_v4_early(reinterpret_cast<const uint4*>(gain) + tid + j * kComputeThreads);
   }
+  // every compute warp is done with the act buffer (and, with a counter, the producers are done)
+  if (cnt >= 0) await_phase(w, cnt, phase);
+  else cbar();
+  ok = w.ok;
   // loads are issued in batches of 16 before any is inspected, so their latencies overlap
   constexpr int kB = 16;
   for (int c0 = sub; c0 < nch && ok; c0 += 16 * kB) {
@@ -542,6 +585,10 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, bool poll, cons
       if (c0 + 16 * j < nch) pending |= 1u << j;
     if (poll) {
       ok = poll_batch<kB>(cx, base, 16, v, pending, [](const uint4& x) { return bf16x8_ready(x); }, phase);
+    } else if (cnt >= 0) {
+#pragma unroll
+      for (int j = 0; j < kB; ++j)
+        if ((pending >> j) & 1u) v[j] = ld_relaxed_v4(base + 16 * j);
     } else {
 #pragma unroll
       for (int j = 0; j < kB; ++j)
@@ -699,8 +746,6 @@ __device__ void dense_epi(const LaunchParams& P, const Smem& S, const EpiArgs& e
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int n = u * 16 + p + hf * 8;
-        // test hook: the first element of the whole h1 exchange is never written
-        if (ea.kind == EPI_OPROJ && (P.flags & 0x10000u) && u == 0 && t == 0 && p == 0 && hf == 0) continue;
         const float o = bf16_to_f32(bf16_bits_rn(v2[hf]));
         const uint16_t r = has_res ? (uint16_t)(hf ? res2 >> 16 : res2 & 0xFFFFu)
                            : ea.kind == EPI_OPROJ ? ea.res[(size_t)t * dm.d + n]
@@ -1129,36 +1174,33 @@ __device__ void attn_merge_phase(Worker& w) {
   const int group = dm.group, S = dm.splits;
   const int gw = rot_block(cx.block, P.phase_rot * 2, G) * kComputeWarps + w.cw;
   constexpr int PER = D / 32;  // floats per lane
-  float* part_acc = reinterpret_cast<float*>(P.s_buf + P.so.part);
-  float* part_ml = reinterpret_cast<float*>(P.s_buf + P.so.ml);
+  const float* part_acc = reinterpret_cast<const float*>(P.s_buf + P.so.part);
+  const float* part_ml = reinterpret_cast<const float*>(P.s_buf + P.so.ml);
   uint16_t* o_out = reinterpret_cast<uint16_t*>(P.x_cur + P.xo.o);
-  for (int it = gw; it < T * dm.hq && w.ok; it += G * kComputeWarps) {
+  if (!await_phase(w, CNT_ATTN, PH_ATTN_MERGE)) return;
+  for (int it = gw; it < T * dm.hq; it += G * kComputeWarps) {
     const int t = it / dm.hq, h = it % dm.hq, hk = h / group, j = h % group;
     auto mlp = [&](int s) { return part_ml + (((size_t)(hk * S + s) * T + t) * group + j) * 2; };
     auto accp = [&](int s) { return part_acc + (((size_t)(hk * S + s) * T + t) * group + j) * D + w.lane * PER; };
-    constexpr int kB = 8;
-    // pass 1: the running maximum over the splits (loads issued 8 at a time)
+    // pass 1: the running maximum over the splits (loads issued 16 at a time)
+    constexpr int kB1 = 16;
     float M = -INFINITY;
-    for (int s0 = 0; s0 < S && w.ok; s0 += kB) {
-      uint2 v[kB];
+    for (int s0 = 0; s0 < S; s0 += kB1) {
+      uint2 v[kB1];
 #pragma unroll
-      for (int i = 0; i < kB; ++i)
+      for (int i = 0; i < kB1; ++i)
         if (s0 + i < S) v[i] = ld_relaxed_v2(mlp(s0 + i));
 #pragma unroll
-      for (int i = 0; i < kB; ++i) {
-        if (s0 + i >= S || !w.ok) continue;
-        if (v[i].x == kF32Empty || v[i].y == kF32Empty) w.ok = poll_f32x2(cx, mlp(s0 + i), v[i], PH_ATTN_MERGE);
-        M = fmaxf(M, __uint_as_float(v[i].x));
-      }
+      for (int i = 0; i < kB1; ++i)
+        if (s0 + i < S) M = fmaxf(M, __uint_as_float(v[i].x));
     }
-    w.ok = __all_sync(0xffffffffu, w.ok);
-    if (!w.ok) break;
     const float Mu = (M == -INFINITY) ? 0.f : M;
     float acc[PER], L = 0.f;
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] = 0.f;
     // pass 2: weighted sum of the partials, in split order
-    for (int s0 = 0; s0 < S && w.ok; s0 += kB) {
+    constexpr int kB = 8;
+    for (int s0 = 0; s0 < S; s0 += kB) {
       uint2 mv[kB];
       float av[kB][PER];
 #pragma unroll
@@ -1176,38 +1218,13 @@ __device__ void attn_merge_phase(Worker& w) {
       }
 #pragma unroll
       for (int i = 0; i < kB; ++i) {
-        if (s0 + i >= S || !w.ok) continue;
-        bool ready = true;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) ready &= __float_as_uint(av[i][e]) != kF32Empty;
-        if (!ready) {
-          if constexpr (PER == 4) {
-            uint4 q4;
-            w.ok = poll_f32x4(cx, accp(s0 + i), q4, PH_ATTN_MERGE);
-            av[i][0] = __uint_as_float(q4.x); av[i][1 % PER] = __uint_as_float(q4.y);
-            av[i][2 % PER] = __uint_as_float(q4.z); av[i][3 % PER] = __uint_as_float(q4.w);
-          } else {
-            uint2 q2;
-            w.ok = poll_f32x2(cx, accp(s0 + i), q2, PH_ATTN_MERGE);
-            av[i][0] = __uint_as_float(q2.x); av[i][1 % PER] = __uint_as_float(q2.y);
-          }
-        }
+        if (s0 + i >= S) continue;
         const float ws = exp2f(__uint_as_float(mv[i].x) - Mu);
         L += ws * __uint_as_float(mv[i].y);
 #pragma unroll
         for (int e = 0; e < PER; ++e) acc[e] += ws * av[i][e];
-        if constexpr (PER == 4) st_relaxed_v4(accp(s0 + i), make_uint4(kF32Empty, kF32Empty, kF32Empty, kF32Empty));
-        else asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%2};" ::"l"(accp(s0 + i)), "r"(kF32Empty), "r"(kF32Empty) : "memory");
       }
     }
-    w.ok = __all_sync(0xffffffffu, w.ok);
-    if (!w.ok) break;
-    __syncwarp();
-    if (w.lane == 0)
-      for (int s = 0; s < S; ++s)
-        asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%2};" ::"l"(part_ml + (((size_t)(hk * S + s) * T + t) * group + j) * 2),
-                     "r"(kF32Empty), "r"(kF32Empty)
-                     : "memory");
     const float inv = 1.f / L;
     uint16_t* dst = o_out + (size_t)t * dm.hq * D + (size_t)h * D + w.lane * PER;
     if constexpr (PER == 4) {
@@ -1242,18 +1259,12 @@ __device__ void route_phase(Worker& w) {
       const int e = w.lane + 32 * i;
       bits[i] = (i < per && e < E) ? ld_relaxed_u32(logits + t * E + e) : 0u;
     }
+    // (every block published its router logits before this phase began)
 #pragma unroll
     for (int i = 0; i < kMaxExperts / 32; ++i) {
       const int e = w.lane + 32 * i;
       key[i] = 0u;  // below every real logit's key
-      if (i < per && e < E && w.ok) {
-        uint32_t n = 0;
-        while (bits[i] == kF32Empty) {
-          if ((++n & 31) == 0 && cx.expired(PH_ROUTE)) { w.ok = false; break; }
-          bits[i] = ld_relaxed_u32(logits + t * E + e);
-        }
-        key[i] = (bits[i] & 0x80000000u) ? ~bits[i] : (bits[i] | 0x80000000u);
-      }
+      if (i < per && e < E && w.ok) key[i] = (bits[i] & 0x80000000u) ? ~bits[i] : (bits[i] | 0x80000000u);
     }
     w.ok = __all_sync(0xffffffffu, w.ok);
     if (!w.ok) break;
@@ -1717,6 +1728,7 @@ __device__ void combine_phase(Worker& w) {
   uint16_t* z = reinterpret_cast<uint16_t*>(P.x_cur + P.xo.z);
   const int nch = dm.p / 8;
   const int gt = rot_block(cx.block, P.phase_rot * 10, G) * kComputeThreads + w.cw * 32 + w.lane;
+  if (!await_phase(w, CNT_GEMM2, PH_COMBINE)) return;
   for (int it = gt; it < T * nch && w.ok; it += G * kComputeThreads) {
     const int t = it / nch, pc = it % nch;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -1726,9 +1738,7 @@ __device__ void combine_phase(Worker& w) {
       if (c < dm.k) v[c] = ld_relaxed_v4(y + (size_t)(t * dm.k + c) * dm.p + pc * 8);
 #pragma unroll
     for (int c = 0; c < kMaxTopK; ++c) {
-      if (c >= dm.k || !w.ok) continue;
-      uint16_t* src = y + (size_t)(t * dm.k + c) * dm.p + pc * 8;
-      if (!bf16x8_ready(v[c]) && !poll_bf16x8(cx, src, v[c], PH_COMBINE)) { w.ok = false; continue; }
+      if (c >= dm.k) continue;
       const float wt = cx.S.topk_w[t * kMaxTopK + c];
       const uint32_t wd[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
 #pragma unroll
@@ -1736,9 +1746,7 @@ __device__ void combine_phase(Worker& w) {
         acc[2 * i] += wt * bf16_to_f32((uint16_t)(wd[i] & 0xFFFF));
         acc[2 * i + 1] += wt * bf16_to_f32((uint16_t)(wd[i] >> 16));
       }
-      st_relaxed_v4(src, make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu));
     }
-    if (!w.ok) break;
     st_relaxed_v4(z + (size_t)t * dm.p + pc * 8,
                   make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
                              pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
@@ -1772,10 +1780,10 @@ __device__ void rearm(const LaunchParams& P, int block, int tid, int nthreads) {
       {P.xo.u, P.xo.logits - P.xo.u, 0xFFFFFFFFu}, {P.xo.logits, P.xo.a - P.xo.logits, kF32Empty},
       {P.xo.a, P.xo.z - P.xo.a, kF32Empty},       {P.xo.z, P.xo.h2 - P.xo.z, 0xFFFFFFFFu},
       {P.xo.h2, P.xo.q0 - P.xo.h2, 0xFFFFFFFFu},   {P.xo.q0, P.xo.tkv0 - P.xo.q0, 0xFFFFFFFFu},
-      {P.xo.tkv0, P.xo.total - P.xo.tkv0, 0xFFFFFFFFu}};
+      {P.xo.tkv0, P.xo.cnt - P.xo.tkv0, 0xFFFFFFFFu}, {P.xo.cnt, P.xo.total - P.xo.cnt, 0u}};
   const int G = gridDim.x;
 #pragma unroll 1
-  for (int ri = 0; ri < 9; ++ri) {
+  for (int ri = 0; ri < 10; ++ri) {
     const R& r = regs[ri];
     const uint64_t n16 = r.bytes / 16;
     const uint64_t lo = n16 * block / G, hi = n16 * (block + 1) / G;
@@ -1799,7 +1807,7 @@ __device__ void compute_main(Worker& w) {
     // the rotary table of this step's tree positions, then the prologue:
     // RMSNorm(hidden_in) -> layer 0 QKV -> RoPE -> layer 0 KV rows and Q
     rope_table(w);
-    stage_act(w, P.hidden_in, dm.d, false, P.g_attn_pro, dm.rms_eps, PH_PROLOGUE);
+    stage_act(w, P.hidden_in, dm.d, -1, false, P.g_attn_pro, dm.rms_eps, PH_PROLOGUE);
     stamp<kTiming>(P, b, EV_PRO_IN);
     EpiArgs ea{};
     ea.kind = EPI_QKV;
@@ -1811,53 +1819,59 @@ __device__ void compute_main(Worker& w) {
   // a2: tree attention (split over blocks), a3: merge of the split partials
   if (dm.hd == 128) attention_phase<128>(w);
   else attention_phase<64>(w);
+  publish(w, CNT_ATTN);
   stamp<kTiming>(P, b, EV_ATTN_DONE);
   if (dm.hd == 128) attn_merge_phase<128>(w);
   else attn_merge_phase<64>(w);
+  publish(w, CNT_MERGE);
   stamp<kTiming>(P, b, EV_MERGE_DONE);
   // a4: h1 = bf16(h + bf16(O W_o^T))
   {
     const uint16_t* hprev = P.first ? P.hidden_in : P.in_h;
     uint16_t* h1 = reinterpret_cast<uint16_t*>(X + P.xo.h1);
-    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.o), dm.hq * dm.hd, true, nullptr, 0.f, PH_OPROJ);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.o), dm.hq * dm.hd, CNT_MERGE, false, nullptr, 0.f, PH_OPROJ);
     stamp<kTiming>(P, b, EV_OPROJ_IN);
     EpiArgs ea{};
     ea.kind = EPI_OPROJ;
     ea.res = hprev;
     ea.out = h1;
     dense_phase(w, dm.hq * dm.hd, dm.d, P.phase_rot * 3, ea, EV_OP_U0_FIRST);
+    publish(w, CNT_OPROJ);
     stamp<kTiming>(P, b, EV_OPROJ_DONE);
   }
   // a5: u = bf16(bf16(RMSNorm(h1)) W_pool^T)
   {
     uint16_t* uo = reinterpret_cast<uint16_t*>(X + P.xo.u);
-    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h1), dm.d, true, P.g_moe, dm.rms_eps, PH_POOL);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h1), dm.d, CNT_OPROJ, false, P.g_moe, dm.rms_eps, PH_POOL);
     stamp<kTiming>(P, b, EV_POOL_IN);
     EpiArgs ea{};
     ea.kind = EPI_POOL;
     ea.out = uo;
     dense_phase(w, dm.d, dm.p, P.phase_rot * 4, ea, -1);
+    publish(w, CNT_POOL);
     stamp<kTiming>(P, b, EV_POOL_DONE);
   }
   // a6: router logits = u W_r^T + b (fp32)
   {
     float* lg = reinterpret_cast<float*>(X + P.xo.logits);
-    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.u), dm.p, true, nullptr, 0.f, PH_ROUTER);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.u), dm.p, CNT_POOL, false, nullptr, 0.f, PH_ROUTER);
     stamp<kTiming>(P, b, EV_ROUTER_IN);
     EpiArgs ea{};
     ea.kind = EPI_ROUTER;
     ea.out32 = lg;
     dense_phase(w, dm.p, dm.e, P.phase_rot * 5, ea, -1);
+    publish(w, CNT_ROUTER);
     stamp<kTiming>(P, b, EV_ROUTER_DONE);
   }
   // a6/a7/a8: top-k, dispatch, NVFP4 activations
-  cbar();
+  await_phase(w, CNT_ROUTER, PH_ROUTE);
   route_phase(w);
   stamp<kTiming>(P, b, EV_ROUTE_DONE);
   // a9, a10: the expert GEMMs
   gemm1_phase(w);
   stamp<kTiming>(P, b, EV_GEMM1_DONE);
   gemm2_phase(w);
+  publish(w, CNT_GEMM2);
   stamp<kTiming>(P, b, EV_GEMM2_DONE);
   // move the next layer's KV history toward L2 while the combine waits
   if ((P.flags & 0x4u) && !P.last && w.cw == 0 && w.lane == 0 && P.kc_pf != nullptr) {
@@ -1871,12 +1885,13 @@ __device__ void compute_main(Worker& w) {
   }
   // a11: combine, then h2 = bf16(h1 + bf16(z W_unp^T))
   combine_phase(w);
+  publish(w, CNT_COMBINE);
   stamp<kTiming>(P, b, EV_COMBINE_DONE);
   {
     const uint16_t* h1 = reinterpret_cast<const uint16_t*>(X + P.xo.h1);
     uint16_t* h2 = reinterpret_cast<uint16_t*>(X + P.xo.h2);
     uint16_t* hnext = P.last ? P.hidden_out : P.out_h;
-    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.z), dm.p, true, nullptr, 0.f, PH_UNPOOL);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.z), dm.p, CNT_COMBINE, false, nullptr, 0.f, PH_UNPOOL);
     stamp<kTiming>(P, b, EV_UNPOOL_IN);
     EpiArgs ea{};
     ea.kind = EPI_UNPOOL;
@@ -1884,19 +1899,20 @@ __device__ void compute_main(Worker& w) {
     ea.out = h2;
     ea.out2 = hnext;
     dense_phase(w, dm.p, dm.d, P.phase_rot * 8, ea, -1);
+    publish(w, CNT_UNPOOL);
     stamp<kTiming>(P, b, EV_UNPOOL_DONE);
   }
   pdl_launch_dependents();
   // a12: next layer's RMSNorm + QKV + RoPE + KV write; a12': final norm + LM head
   if (!P.last) {
-    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h2), dm.d, true, P.g_tail, dm.rms_eps, PH_TAIL);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h2), dm.d, CNT_UNPOOL, false, P.g_tail, dm.rms_eps, PH_TAIL);
     stamp<kTiming>(P, b, EV_TAIL_IN);
     EpiArgs ea{};
     ea.kind = EPI_QKV;
     ea.dq = QkvDst{P.out_q, false, P.kc_next, P.vc_next, nullptr};
     dense_phase(w, dm.d, dm.nqkv, P.phase_rot * 9, ea, -1);
   } else if (dm.vocab > 0) {
-    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h2), dm.d, true, P.g_tail, dm.rms_eps, PH_TAIL);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h2), dm.d, CNT_UNPOOL, false, P.g_tail, dm.rms_eps, PH_TAIL);
     stamp<kTiming>(P, b, EV_TAIL_IN);
     EpiArgs ea{};
     ea.kind = EPI_LMHEAD;
