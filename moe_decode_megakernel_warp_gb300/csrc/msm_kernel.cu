@@ -968,18 +968,15 @@ __device__ __forceinline__ void attn_keys16(AttnState<D>& st, const uint32_t (&q
     st.o[n][2] *= alpha[1];
     st.o[n][3] *= alpha[1];
   }
-  // P as the sum of three bf16 parts: P.V carries ~24 significant bits of P, as
-  // much as the fp32 softmax itself
-  uint32_t ph[4], pm[4], pl[4];
+  // P as the sum of two bf16 parts: P.V carries ~16 significant bits of P (the
+  // residual error, 2^-17 of each weight, is far below the bf16 rounding of the output)
+  uint32_t ph[4], pm[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float x0 = s[i >> 1][(i & 1) * 2], x1 = s[i >> 1][(i & 1) * 2 + 1];
     const uint32_t h = pack_bf16x2(x0, x1);
-    const float r0 = x0 - bf16_to_f32((uint16_t)(h & 0xFFFFu)), r1 = x1 - bf16_to_f32((uint16_t)(h >> 16));
-    const uint32_t mm = pack_bf16x2(r0, r1);
     ph[i] = h;
-    pm[i] = mm;
-    pl[i] = pack_bf16x2(r0 - bf16_to_f32((uint16_t)(mm & 0xFFFFu)), r1 - bf16_to_f32((uint16_t)(mm >> 16)));
+    pm[i] = pack_bf16x2(x0 - bf16_to_f32((uint16_t)(h & 0xFFFFu)), x1 - bf16_to_f32((uint16_t)(h >> 16)));
   }
 #pragma unroll
   for (int n = 0; n < D / 8; n += 2) {
@@ -991,8 +988,6 @@ __device__ __forceinline__ void attn_keys16(AttnState<D>& st, const uint32_t (&q
     mma_bf16(st.o[n + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
     mma_bf16(st.o[n], pm[0], pm[1], pm[2], pm[3], b0, b1);
     mma_bf16(st.o[n + 1], pm[0], pm[1], pm[2], pm[3], b2, b3);
-    mma_bf16(st.o[n], pl[0], pl[1], pl[2], pl[3], b0, b1);
-    mma_bf16(st.o[n + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
   }
 }
 
@@ -1182,24 +1177,12 @@ __device__ void attn_merge_phase(Worker& w) {
     const int t = it / dm.hq, h = it % dm.hq, hk = h / group, j = h % group;
     auto mlp = [&](int s) { return part_ml + (((size_t)(hk * S + s) * T + t) * group + j) * 2; };
     auto accp = [&](int s) { return part_acc + (((size_t)(hk * S + s) * T + t) * group + j) * D + w.lane * PER; };
-    // pass 1: the running maximum over the splits (loads issued 16 at a time)
-    constexpr int kB1 = 16;
-    float M = -INFINITY;
-    for (int s0 = 0; s0 < S; s0 += kB1) {
-      uint2 v[kB1];
-#pragma unroll
-      for (int i = 0; i < kB1; ++i)
-        if (s0 + i < S) v[i] = ld_relaxed_v2(mlp(s0 + i));
-#pragma unroll
-      for (int i = 0; i < kB1; ++i)
-        if (s0 + i < S) M = fmaxf(M, __uint_as_float(v[i].x));
-    }
-    const float Mu = (M == -INFINITY) ? 0.f : M;
-    float acc[PER], L = 0.f;
+    // splits in batches of 10, every load of a batch in flight together; a batch's
+    // partials are rescaled to the running maximum (M, L, acc in log2 units)
+    constexpr int kB = 10;
+    float M = -INFINITY, L = 0.f, acc[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-    // pass 2: weighted sum of the partials, in split order
-    constexpr int kB = 8;
     for (int s0 = 0; s0 < S; s0 += kB) {
       uint2 mv[kB];
       float av[kB][PER];
@@ -1216,6 +1199,15 @@ __device__ void attn_merge_phase(Worker& w) {
           av[i][0] = __uint_as_float(q2.x); av[i][1 % PER] = __uint_as_float(q2.y);
         }
       }
+      float Mb = M;
+#pragma unroll
+      for (int i = 0; i < kB; ++i)
+        if (s0 + i < S) Mb = fmaxf(Mb, __uint_as_float(mv[i].x));
+      const float Mu = (Mb == -INFINITY) ? 0.f : Mb;
+      const float al = exp2f(M - Mu);  // 0 while M is still -inf
+      L *= al;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] *= al;
 #pragma unroll
       for (int i = 0; i < kB; ++i) {
         if (s0 + i >= S) continue;
@@ -1224,6 +1216,7 @@ __device__ void attn_merge_phase(Worker& w) {
 #pragma unroll
         for (int e = 0; e < PER; ++e) acc[e] += ws * av[i][e];
       }
+      M = Mb;
     }
     const float inv = 1.f / L;
     uint16_t* dst = o_out + (size_t)t * dm.hq * D + (size_t)h * D + w.lane * PER;
