@@ -1403,19 +1403,24 @@ __device__ void route_phase(Worker& w) {
 // weights dequantised e2m1 * e4m3 into f16 (exact)
 // f16x2 {s, s} * 2^-8 of a UE4M3 scale byte: E4M3 has exponent bias 7 and f16 bias 15,
 // so the byte's 7 magnitude bits shifted into f16 position give the value times 2^-8,
-// exactly (subnormal scales included); bit 7 (a sign UE4M3 does not have) is ignored
-__device__ __forceinline__ uint32_t ue4m3_pair_f16(uint32_t word, int byte) {
-  return (__byte_perm(word, 0u, 0x4040u | (uint32_t)byte | ((uint32_t)byte << 8)) & 0x007F007Fu) << 7;
+// exactly (subnormal scales included).  `wm` is the group's scale word with bit 7 of
+// every byte (a sign UE4M3 does not have) already cleared.
+__device__ __forceinline__ uint32_t ue4m3_pair_f16(uint32_t wm, int byte) {
+  return __byte_perm(wm, 0u, 0x4040u | (uint32_t)byte | ((uint32_t)byte << 8)) << 7;
 }
 
-// NVFP4 expert tile: A fragments of rows g and g+8 for one 16-column k-step, the
 // weights dequantised e2m1 * e4m3 into f16 times 2^-8 (exact: every product has at
-// most 6 significant bits and lies in [2^-18, 10.5]); the caller scales by 2^8
-__device__ __forceinline__ void exp_frags(uint64_t cg, uint64_t cg8, uint32_t sg, uint32_t sg8, int ks,
+// most 6 significant bits and lies in [2^-18, 10.5]); the caller scales by 2^8.
+// Code bytes of k-step ks: bytes 2 ks (columns 2q, 2q+1) and 2 ks + 1 (2q+8, 2q+9) of
+// the lane's 8-byte word of each row, moved to the low byte with one byte_perm each.
+__device__ __forceinline__ void exp_frags(uint64_t cg, uint64_t cg8, uint32_t sgm, uint32_t sg8m, int ks,
                                           uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
-  const uint32_t lo_g = (uint32_t)(cg >> (ks * 16)) & 0xFFu, hi_g = (uint32_t)(cg >> (ks * 16 + 8)) & 0xFFu;
-  const uint32_t lo_8 = (uint32_t)(cg8 >> (ks * 16)) & 0xFFu, hi_8 = (uint32_t)(cg8 >> (ks * 16 + 8)) & 0xFFu;
-  const uint32_t f_g = ue4m3_pair_f16(sg, ks), f_8 = ue4m3_pair_f16(sg8, ks);
+  const uint32_t wg = ks < 2 ? (uint32_t)cg : (uint32_t)(cg >> 32);
+  const uint32_t w8 = ks < 2 ? (uint32_t)cg8 : (uint32_t)(cg8 >> 32);
+  const uint32_t b = (uint32_t)(ks & 1) * 2;
+  const uint32_t lo_g = __byte_perm(wg, 0u, 0x4440u | b), hi_g = __byte_perm(wg, 0u, 0x4440u | (b + 1));
+  const uint32_t lo_8 = __byte_perm(w8, 0u, 0x4440u | b), hi_8 = __byte_perm(w8, 0u, 0x4440u | (b + 1));
+  const uint32_t f_g = ue4m3_pair_f16(sgm, ks), f_8 = ue4m3_pair_f16(sg8m, ks);
   a0 = hmul2(e2m1x2_to_f16x2(lo_g), f_g);
   a2 = hmul2(e2m1x2_to_f16x2(hi_g), f_g);
   a1 = hmul2(e2m1x2_to_f16x2(lo_8), f_8);
@@ -1425,54 +1430,72 @@ __device__ __forceinline__ void exp_frags(uint64_t cg, uint64_t cg8, uint32_t sg
 constexpr float kExpScaleUndo = 256.0f;
 
 // acc[nt] += 2^-8 W_unit (16 rows, 64-column groups [g0, g1) of the NVFP4 tile at tbase)
-// * act rows; rows[nt]: the token (activation row) this lane addresses in ldmatrix
-// for n-tile nt
-__device__ __forceinline__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* tbase, int g0, int g1, int ntiles,
+// * act rows, for NT n-tiles of 8 tokens; rows[nt]: the token (activation row) this
+// lane addresses in ldmatrix for n-tile nt.  Software-pipelined one group ahead: the
+// next group's code and scale words and its B fragments are loaded while this group's
+// four k-steps are dequantised (all before its MMAs, so the conversions overlap).
+template <int NT>
+__device__ __forceinline__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* tbase, int g0, int g1,
                                              uint32_t act_s, int lane, const int (&rows)[2]) {
   const int g = lane >> 2, q = lane & 3;
   const int mi = lane >> 3;
   float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  // B rows: token rows[nt] of matrix m; k-step & 3 is (kp + (mi >> 1)) & 3 with kp in {0, 2}
-  uint32_t bro[2][2];
+  // B rows: token rows[nt] of matrix m; k-step & 3 is (2 h + (mi >> 1)) & 3 for h in {0, 1}
+  uint32_t bro[NT][2];
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
+  for (int nt = 0; nt < NT; ++nt) {
     const int t = rows[nt];
     const int m = ((t >> 3) << 1) + (mi & 1);
 #pragma unroll
     for (int h = 0; h < 2; ++h)
       bro[nt][h] = act_s + (uint32_t)m * 128u + ((((uint32_t)t & 7u) ^ act_sw(2 * h + (mi >> 1), m)) << 4);
   }
-  // the next group's code and scale words are read while this group computes
   const uint8_t* gb0 = tbase + g0 * kExpGroupBytes;
   uint64_t ncg = *reinterpret_cast<const uint64_t*>(gb0 + g * 32 + q * 8);
   uint64_t ncg8 = *reinterpret_cast<const uint64_t*>(gb0 + (g + 8) * 32 + q * 8);
   uint32_t nsg = *reinterpret_cast<const uint32_t*>(gb0 + 512 + g * 4);
   uint32_t nsg8 = *reinterpret_cast<const uint32_t*>(gb0 + 512 + (g + 8) * 4);
+  uint32_t nb[NT][2][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      ldsm_x4(bro[nt][h] + (uint32_t)(g0 * 4 + 2 * h + (mi >> 1)) * kKStepBytes, nb[nt][h][0], nb[nt][h][1],
+              nb[nt][h][2], nb[nt][h][3]);
   for (int gi = g0; gi < g1; ++gi) {
     const uint64_t cg = ncg, cg8 = ncg8;
-    const uint32_t sg = nsg, sg8 = nsg8;
+    const uint32_t sg = nsg & 0x7F7F7F7Fu, sg8 = nsg8 & 0x7F7F7F7Fu;
+    uint32_t b[NT][2][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) b[nt][h][i] = nb[nt][h][i];
     if (gi + 1 < g1) {
       const uint8_t* gb = tbase + (gi + 1) * kExpGroupBytes;
       ncg = *reinterpret_cast<const uint64_t*>(gb + g * 32 + q * 8);
       ncg8 = *reinterpret_cast<const uint64_t*>(gb + (g + 8) * 32 + q * 8);
       nsg = *reinterpret_cast<const uint32_t*>(gb + 512 + g * 4);
       nsg8 = *reinterpret_cast<const uint32_t*>(gb + 512 + (g + 8) * 4);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          ldsm_x4(bro[nt][h] + (uint32_t)((gi + 1) * 4 + 2 * h + (mi >> 1)) * kKStepBytes, nb[nt][h][0],
+                  nb[nt][h][1], nb[nt][h][2], nb[nt][h][3]);
     }
+    uint32_t a[4][4];
 #pragma unroll
-    for (int kp = 0; kp < 4; kp += 2) {
-      uint32_t a[2][4];
-      exp_frags(cg, cg8, sg, sg8, kp, a[0][0], a[0][1], a[0][2], a[0][3]);
-      exp_frags(cg, cg8, sg, sg8, kp + 1, a[1][0], a[1][1], a[1][2], a[1][3]);
-      const uint32_t kstep = (uint32_t)(gi * 4 + kp + (mi >> 1)) * kKStepBytes;
+    for (int ks = 0; ks < 4; ++ks) exp_frags(cg, cg8, sg, sg8, ks, a[ks][0], a[ks][1], a[ks][2], a[ks][3]);
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        if (nt >= ntiles) break;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(bro[nt][kp >> 1] + kstep, b0, b1, b2, b3);
-        mma_f16(acc[nt], a[0][0], a[0][1], a[0][2], a[0][3], b0, b1);
-        mma_f16(acc2[nt], a[1][0], a[1][1], a[1][2], a[1][3], b2, b3);
+    for (int kp = 0; kp < 4; kp += 2)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma_f16(acc[nt], a[kp][0], a[kp][1], a[kp][2], a[kp][3], b[nt][kp >> 1][0], b[nt][kp >> 1][1]);
+        mma_f16(acc2[nt], a[kp + 1][0], a[kp + 1][1], a[kp + 1][2], a[kp + 1][3], b[nt][kp >> 1][2],
+                b[nt][kp >> 1][3]);
       }
-    }
   }
   // two independent chains (even / odd k-steps), summed in a fixed order
 #pragma unroll
@@ -1541,7 +1564,8 @@ __device__ void gemm1_phase(Worker& w) {
     if (got) {
       const int r8 = w.lane & 7;
       const int rows[2] = {(int)toks[r8 < n ? r8 : 0], (int)toks[8 + r8 < n ? 8 + r8 : 0]};
-      exp_unit_mma(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, n > 8 ? 2 : 1, act_s, w.lane, rows);
+      if (n > 8) exp_unit_mma<2>(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, act_s, w.lane, rows);
+      else exp_unit_mma<1>(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, act_s, w.lane, rows);
       __syncwarp();
       if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps / 2);
     }
@@ -1679,7 +1703,8 @@ __device__ void gemm2_phase(Worker& w) {
         if (got) {
           const int r8 = w.lane & 7;
           const int rows[2] = {r8 < n ? r8 : 0, 8 + r8 < n ? 8 + r8 : 0};
-          exp_unit_mma(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, n > 8 ? 2 : 1, act_s, w.lane, rows);
+          if (n > 8) exp_unit_mma<2>(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, act_s, w.lane, rows);
+          else exp_unit_mma<1>(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, act_s, w.lane, rows);
           __syncwarp();
           if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps / 2);
         }
