@@ -49,7 +49,7 @@ struct Smem {
   float* a_ts;        // [16]
   float* red;         // [8][16]
   volatile uint32_t* slot_tile;  // [kSlots] index of the tile the loader last put in each slot
-  struct Ring* ring_state;        // the loader's ring bookkeeping
+  struct RunAhead* ring_state;    // the loader's L2 run-ahead lists
   float* dred;        // [8][16][16] dense-phase cross-warp partial sums
 };
 
@@ -78,7 +78,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const LaunchParams& P) {
   s.a_ts = reinterpret_cast<float*>(sm + 6016);
   s.red = reinterpret_cast<float*>(sm + 6080);
   s.slot_tile = reinterpret_cast<volatile uint32_t*>(sm + 6592);
-  s.ring_state = reinterpret_cast<struct Ring*>(sm + kRingStateOff);
+  s.ring_state = reinterpret_cast<struct RunAhead*>(sm + kRingStateOff);
   s.dred = reinterpret_cast<float*>(sm + 8192);
   return s;
 }
@@ -284,32 +284,53 @@ struct RunAhead {
   }
 };
 
+// The loader's view of the ring: a FIFO of tiles laid out circularly.  Only scalars,
+// so that they stay in the loader lane's registers; a tile's offset is read back from
+// the slot table in shared memory once, when the tile before it is released.
 struct Ring {
-  uint32_t issued;  // tiles issued
-  uint32_t tail;    // oldest tile not known to be released
-  uint32_t head;    // next free byte
-  uint32_t off[kSlots], end[kSlots];
-  RunAhead ra;
+  uint32_t issued;    // tiles issued
+  uint32_t tail;      // oldest tile not known to be released
+  uint32_t head;      // end of the newest tile
+  uint32_t tail_off;  // start of the oldest outstanding tile (tail < issued)
+  bool wrapped;       // the outstanding tiles run to the top and continue at 0
+  bool ra_on;         // L2 run-ahead enabled
+  RunAhead* ra;       // L2 run-ahead state (shared memory)
 };
-static_assert(kRingStateOff + sizeof(Ring) <= 8192, "ring bookkeeping overlaps the reduction scratch");
+static_assert(kRingStateOff + sizeof(RunAhead) <= 8192, "run-ahead state overlaps the reduction scratch");
 
+// a free run of `bytes` (1 KB granules) after the newest tile, at the bottom once the
+// top is too short; waits for the oldest tiles' release until there is one
 __device__ bool ring_place(Ctx& cx, Ring& r, uint32_t bytes, uint32_t& off_out) {
   const uint32_t cap = (uint32_t)cx.P->ring_bytes;
-  uint32_t off = r.head;
-  if (off + bytes > cap) off = 0;
+  const uint32_t need = (bytes + 1023u) & ~1023u;
+  uint32_t off = 0;
   for (;;) {
-    bool conflict = (r.issued - r.tail) >= (uint32_t)kSlots;
-    for (uint32_t j = r.tail; j < r.issued && !conflict; ++j) {
-      uint32_t s = j % kSlots;
-      if (r.off[s] < off + bytes && off < r.end[s]) conflict = true;
+    if (r.issued - r.tail < (uint32_t)kSlots) {
+      if (r.tail == r.issued) {  // empty: start again at the bottom
+        r.wrapped = false;
+        off = 0;
+        r.tail_off = 0;
+        break;
+      }
+      if (!r.wrapped) {  // occupied: [tail_off, head)
+        if (r.head + need <= cap) { off = r.head; break; }
+        if (need <= r.tail_off) { off = 0; r.wrapped = true; break; }
+      } else if (r.head + need <= r.tail_off) {  // occupied: [tail_off, top) and [0, head)
+        off = r.head;
+        break;
+      }
     }
-    if (!conflict) break;
-    uint32_t s = r.tail % kSlots;
+    const uint32_t s = r.tail % kSlots;
     if (!wait_bar(cx, &cx.S.empty[s], (r.tail / kSlots) & 1, 99)) return false;
     ++r.tail;
+    if (r.tail != r.issued) {
+      const uint32_t next = cx.S.slot_off[r.tail % kSlots];
+      if (next < r.tail_off) r.wrapped = false;  // the span no longer crosses the top
+      r.tail_off = next;
+    }
   }
   off_out = off;
-  r.head = off + ((bytes + 1023u) & ~1023u);
+  r.head = off + need;
   return true;
 }
 
@@ -318,15 +339,15 @@ __device__ bool ring_issue(Ctx& cx, Ring& r, const uint8_t* src, uint32_t bytes,
   uint32_t off;
   if (!ring_place(cx, r, bytes, off)) return false;
   const uint32_t s = r.issued % kSlots;
-  r.off[s] = off;
-  r.end[s] = off + bytes;
   cx.S.slot_off[s] = off;
   cx.S.slot_tile[s] = r.issued;
   mbar_expect_tx(&cx.S.full[s], bytes);
   bulk_g2s(cx.S.ring + off, src, bytes, &cx.S.full[s], pol);
   ++r.issued;
-  r.ra.used += bytes;
-  r.ra.pump();
+  if (r.ra_on) {
+    r.ra->used += bytes;
+    r.ra->pump();
+  }
   return true;
 }
 
@@ -335,8 +356,6 @@ __device__ bool ring_issue_kv(Ctx& cx, Ring& r, int hk, int row, uint32_t tile_b
   uint32_t off;
   if (!ring_place(cx, r, tile_bytes, off)) return false;
   const uint32_t s = r.issued % kSlots;
-  r.off[s] = off;
-  r.end[s] = off + tile_bytes;
   cx.S.slot_off[s] = off;
   cx.S.slot_tile[s] = r.issued;
   mbar_expect_tx(&cx.S.full[s], tile_bytes);
@@ -348,8 +367,10 @@ __device__ bool ring_issue_kv(Ctx& cx, Ring& r, int hk, int row, uint32_t tile_b
     tma_load_3d(dst + (halves + h) * R * 128, &P.tmap_v, h * 64, row, hk, &cx.S.full[s]);
   }
   ++r.issued;
-  r.ra.used += tile_bytes;
-  r.ra.pump();
+  if (r.ra_on) {
+    r.ra->used += tile_bytes;
+    r.ra->pump();
+  }
   return true;
 }
 
@@ -392,30 +413,33 @@ __device__ void loader(Ctx& cx) {
   const uint64_t pol = policy_evict_first();
   prefetch_tensormap(&P.tmap_k);
   prefetch_tensormap(&P.tmap_v);
-  // the ring's bookkeeping lives in shared memory: as a local array it would sit in
-  // the small L1 left beside a 227 KB carve-out, and its lines, evicted by the compute
+  // the run-ahead lists live in shared memory: as local arrays they would sit in the
+  // small L1 left beside a 227 KB carve-out, and their lines, evicted by the compute
   // warps' traffic, would cost the loader an L2 round trip per access
-  Ring& r = *cx.S.ring_state;
-  r.issued = r.tail = r.head = 0;
-  r.ra.init(P.runahead_bytes);
+  Ring r;
+  r.issued = r.tail = r.head = r.tail_off = 0;
+  r.wrapped = false;
+  r.ra = cx.S.ring_state;
+  r.ra->init(P.runahead_bytes);
+  r.ra_on = P.runahead_bytes != 0;
   bool ok = true;
   const AttnUnit au = attn_unit(P, rot_block(cx.block, P.phase_rot * 2, G), P.is_global);
-  if (r.ra.ahead) {
+  if (r.ra->ahead) {
     // everything up to the routing decision, in the order the ring streams it
-    if (P.first) add_dense_range(r.ra, P.w_qkv_pro, dm.d, dm.nqkv, P.phase_rot * 1);
+    if (P.first) add_dense_range(*r.ra, P.w_qkv_pro, dm.d, dm.nqkv, P.phase_rot * 1);
     if (au.valid && au.r1 > au.r0) {
       const uint64_t off = ((uint64_t)au.hk * dm.max_ctx + au.r0) * dm.hd, bytes = (uint64_t)(au.r1 - au.r0) * dm.hd * 2;
-      r.ra.add(P.kc + off, bytes);
-      r.ra.add(P.vc + off, bytes);
+      r.ra->add(P.kc + off, bytes);
+      r.ra->add(P.vc + off, bytes);
     }
-    add_dense_range(r.ra, P.w_o, dm.hq * dm.hd, dm.d, P.phase_rot * 3);
-    add_dense_range(r.ra, P.w_pool, dm.d, dm.p, P.phase_rot * 4);
-    add_dense_range(r.ra, P.w_router, dm.p, dm.e, P.phase_rot * 5);
+    add_dense_range(*r.ra, P.w_o, dm.hq * dm.hd, dm.d, P.phase_rot * 3);
+    add_dense_range(*r.ra, P.w_pool, dm.d, dm.p, P.phase_rot * 4);
+    add_dense_range(*r.ra, P.w_router, dm.p, dm.e, P.phase_rot * 5);
     if (cx.block == 0) {
       prefetch_l2(P.g_moe, (uint32_t)dm.d * 2);
       if (P.g_tail) prefetch_l2(P.g_tail, (uint32_t)dm.d * 2);
     }
-    r.ra.pump();
+    r.ra->pump();
   }
   // weights do not depend on the previous launch: stream before the dependency wait
   if (P.first) ok = ok && load_dense(cx, r, P.w_qkv_pro, dm.d, dm.nqkv, P.phase_rot * 1, pol);
@@ -437,7 +461,7 @@ __device__ void loader(Ctx& cx) {
     const int u1pe = dm.f / 8, u2pe = dm.p / 16;
     const uint64_t ub1 = exp_unit_bytes(dm.p), ub2 = exp_unit_bytes(dm.f);
     int lo, hi;
-    if (r.ra.ahead) {
+    if (r.ra->ahead) {
       // the rest of the launch's stream: this block's expert units (runs of one expert
       // are contiguous), the unpooler, then the next layer's QKV or the LM head
       for (int pass = 0; pass < 2; ++pass) {
@@ -446,14 +470,14 @@ __device__ void loader(Ctx& cx) {
         unit_range(na * upe, rot_block(cx.block, P.phase_rot * (pass ? 7 : 6), G), G, lo, hi);
         for (int gu = lo; gu < hi;) {
           const int run = min(hi, (gu / upe + 1) * upe) - gu;
-          r.ra.add(nullptr, (uint64_t)run * ub);  // expert tiles: streamed, not prefetched
+          r.ra->add(nullptr, (uint64_t)run * ub);  // expert tiles: streamed, not prefetched
           gu += run;
         }
       }
-      add_dense_range(r.ra, P.w_unpool, dm.p, dm.d, P.phase_rot * 8);
-      if (!P.last) add_dense_range(r.ra, P.w_tail, dm.d, dm.nqkv, P.phase_rot * 9);
-      else if (dm.vocab > 0) add_dense_range(r.ra, P.w_tail, dm.d, dm.vocab, P.phase_rot * 9);
-      r.ra.pump();
+      add_dense_range(*r.ra, P.w_unpool, dm.p, dm.d, P.phase_rot * 8);
+      if (!P.last) add_dense_range(*r.ra, P.w_tail, dm.d, dm.nqkv, P.phase_rot * 9);
+      else if (dm.vocab > 0) add_dense_range(*r.ra, P.w_tail, dm.d, dm.vocab, P.phase_rot * 9);
+      r.ra->pump();
     }
     unit_range(na * u1pe, rot_block(cx.block, P.phase_rot * 6, G), G, lo, hi);
     for (int gu = lo; ok && gu < hi; ++gu) {
