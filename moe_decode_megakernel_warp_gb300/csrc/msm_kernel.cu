@@ -1263,50 +1263,65 @@ __device__ void route_phase(Worker& w) {
   const Dims& dm = P.dm;
   const int E = dm.e, K = dm.k;
   const float* logits = reinterpret_cast<const float*>(P.x_cur + P.xo.logits);
-  // top-k: warp cw takes tokens 2cw, 2cw+1.  Logits become order-preserving unsigned
-  // keys (router logits are canonical: never -0.0); each round takes the warp-wide
-  // largest key, ties to the lowest expert index, with two warp reductions.
+  // top-k: warp cw takes tokens 2cw and 2cw+1, both at once (independent chains).
+  // Logits become order-preserving unsigned keys (router logits are canonical: never
+  // -0.0); each round takes the warp-wide largest key, ties to the lowest expert
+  // index, with two warp reductions.  Lane c keeps round c's pick; the softmax of the
+  // K picks is then one expf per lane and a fixed-order butterfly sum.
   const int per = (E + 31) / 32;
-  for (int tt = 0; tt < 2; ++tt) {
-    const int t = w.cw * 2 + tt;
-    uint32_t key[kMaxExperts / 32];
-    uint32_t bits[kMaxExperts / 32];
-#pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
-      const int e = w.lane + 32 * i;
-      bits[i] = (i < per && e < E) ? ld_relaxed_u32(logits + t * E + e) : 0u;
-    }
+  {
+    const int t0 = w.cw * 2;
+    uint32_t key[2][kMaxExperts / 32];
     // (every block published its router logits before this phase began)
 #pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
-      const int e = w.lane + 32 * i;
-      key[i] = 0u;  // below every real logit's key
-      if (i < per && e < E && w.ok) key[i] = (bits[i] & 0x80000000u) ? ~bits[i] : (bits[i] | 0x80000000u);
-    }
-    w.ok = __all_sync(0xffffffffu, w.ok);
-    if (!w.ok) break;
-    float sel_v[kMaxTopK];
-    uint32_t taken = 0u;  // bit i: v[i] of this lane already selected
-    for (int c = 0; c < K; ++c) {
-      // this lane's best unselected key (lowest i among equal keys)
-      uint32_t bk = 0u;
-      int bi = 0;
+    for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
-      for (int i = kMaxExperts / 32 - 1; i >= 0; --i)
-        if (!((taken >> i) & 1u) && key[i] >= bk && i < per) { bk = key[i]; bi = i; }
-      const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
-      const uint32_t e_me = (bk == wk) ? (uint32_t)(w.lane + 32 * bi) : 0xFFFFFFFFu;
-      uint32_t e = __reduce_min_sync(0xffffffffu, e_me);
-      if (e >= (uint32_t)E) e = 0;  // only for NaN logits, which are outside the contract
-      if ((int)(e & 31) == w.lane) taken |= 1u << (e >> 5);
-      const uint32_t vb = (wk & 0x80000000u) ? (wk & 0x7FFFFFFFu) : ~wk;
-      sel_v[c] = __uint_as_float(vb);
-      if (w.lane == 0) cx.S.topk_idx[t * kMaxTopK + c] = (int)e;
+      for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = w.lane + 32 * i;
+        key[tt][i] = (i < per && e < E) ? ld_relaxed_u32(logits + (t0 + tt) * E + e) : 0u;
+      }
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+      for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = w.lane + 32 * i;
+        const uint32_t b = key[tt][i];
+        key[tt][i] = (i < per && e < E) ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;  // 0: below every key
+      }
+    uint32_t taken[2] = {0u, 0u};  // bit i: key[tt][i] of this lane already selected
+    float my_v[2] = {0.f, 0.f};    // lane c < K: round c's logit
+    int my_e[2] = {0, 0};          // and expert
+    for (int c = 0; c < K; ++c) {
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        // this lane's best unselected key (lowest i among equal keys)
+        uint32_t bk = 0u;
+        int bi = 0;
+#pragma unroll
+        for (int i = kMaxExperts / 32 - 1; i >= 0; --i)
+          if (!((taken[tt] >> i) & 1u) && key[tt][i] >= bk && i < per) { bk = key[tt][i]; bi = i; }
+        const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t e_me = (bk == wk) ? (uint32_t)(w.lane + 32 * bi) : 0xFFFFFFFFu;
+        uint32_t e = __reduce_min_sync(0xffffffffu, e_me);
+        if (e >= (uint32_t)E) e = 0;  // only for NaN logits, which are outside the contract
+        if ((int)(e & 31) == w.lane) taken[tt] |= 1u << (e >> 5);
+        if (w.lane == c) {
+          my_v[tt] = __uint_as_float((wk & 0x80000000u) ? (wk & 0x7FFFFFFFu) : ~wk);
+          my_e[tt] = (int)e;
+        }
+      }
     }
-    if (w.lane == 0) {
-      float sum = 0.f, ex[kMaxTopK];
-      for (int c = 0; c < K; ++c) { ex[c] = expf(sel_v[c] - sel_v[0]); sum += ex[c]; }
-      for (int c = 0; c < K; ++c) cx.S.topk_w[t * kMaxTopK + c] = ex[c] / sum;
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt) {
+      const float v0 = __shfl_sync(0xffffffffu, my_v[tt], 0);  // the largest
+      const float ex = w.lane < K ? expf(my_v[tt] - v0) : 0.f;
+      float sum = ex;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (w.lane < K && w.ok) {
+        cx.S.topk_idx[(t0 + tt) * kMaxTopK + w.lane] = my_e[tt];
+        cx.S.topk_w[(t0 + tt) * kMaxTopK + w.lane] = ex / sum;
+      }
     }
   }
   cbar();
@@ -1379,6 +1394,10 @@ __device__ void route_phase(Worker& w) {
     }
   }
   stamp_rt(P, EV_ROUTE_DISPATCH);
+  // the dispatch tables are complete: the loader may stream this block's expert tiles
+  // while the rows below are converted
+  cbar();
+  if (tid == 0) mbar_arrive(cx.S.route_bar, 1);
   // GEMM1 B operand: the bf16 pooled vectors, one row per token, as f16 scaled by a
   // power of two per row (largest magnitude lands in [2^14, 2^15)).  Every bf16
   // value within 2^29 of the row's largest is exact in f16, so GEMM1 sees u as it
@@ -1420,7 +1439,6 @@ __device__ void route_phase(Worker& w) {
   }
   cbar();
   if (*cx.S.abort) w.ok = false;
-  if (tid == 0) mbar_arrive(cx.S.route_bar, 1);
 }
 
 // NVFP4 expert tile: A fragments of rows g and g+8 for one 16-column k-step,
