@@ -217,6 +217,15 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   dm.attn_wph = dm.attn_rows / dm.attn_nk;
   dm.rms_eps = c.rms_eps;
   m->G = c.grid_blocks > 0 ? std::min(c.grid_blocks, sms) : sms;
+  {
+    // the kernel splits work units over the grid in 32-bit arithmetic
+    const uint64_t units = std::max({(uint64_t)dm.vocab / 16, (uint64_t)dm.nqkv / 16, (uint64_t)dm.d / 16,
+                                     (uint64_t)std::min(dm.e, T * dm.k) * std::max(dm.f / 8, dm.p / 16)});
+    if (units * (uint64_t)(m->G + 1) >= (1ull << 32)) {
+      delete m;
+      return fail(MSM_ERR_UNSUPPORTED, "too many work units per phase for the grid split");
+    }
+  }
   dm.splits = c.attn_splits > 0 ? c.attn_splits : std::max(1, m->G / dm.hkv);
   if (dm.hkv * dm.splits > m->G) {
     delete m;

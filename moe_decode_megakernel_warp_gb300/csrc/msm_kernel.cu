@@ -213,8 +213,10 @@ __device__ __forceinline__ void stamp_rt(const LaunchParams& P, int ev) {
 // work split (identical in the loader and the consumers)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void unit_range(int n_units, int bb, int G, int& lo, int& hi) {
-  lo = (int)(((long long)n_units * bb) / G);
-  hi = (int)(((long long)n_units * (bb + 1)) / G);
+  // 32-bit: n_units * G stays far below 2^32 for every shape the host accepts (a
+  // 64-bit division is a long subroutine, inlined at every call site)
+  lo = (int)(((uint32_t)n_units * (uint32_t)bb) / (uint32_t)G);
+  hi = (int)(((uint32_t)n_units * (uint32_t)(bb + 1)) / (uint32_t)G);
 }
 __device__ __forceinline__ int rot_block(int b, int rot, int G) { return (b + rot) % G; }
 
@@ -334,47 +336,7 @@ __device__ bool ring_place(Ctx& cx, Ring& r, uint32_t bytes, uint32_t& off_out) 
   return true;
 }
 
-// issue one tile (one contiguous run of bytes)
-__device__ bool ring_issue(Ctx& cx, Ring& r, const uint8_t* src, uint32_t bytes, uint64_t pol) {
-  uint32_t off;
-  if (!ring_place(cx, r, bytes, off)) return false;
-  const uint32_t s = r.issued % kSlots;
-  cx.S.slot_off[s] = off;
-  cx.S.slot_tile[s] = r.issued;
-  mbar_expect_tx(&cx.S.full[s], bytes);
-  bulk_g2s(cx.S.ring + off, src, bytes, &cx.S.full[s], pol);
-  ++r.issued;
-  if (r.ra_on) {
-    r.ra->used += bytes;
-    r.ra->pump();
-  }
-  return true;
-}
-
-__device__ bool ring_issue_kv(Ctx& cx, Ring& r, int hk, int row, uint32_t tile_bytes) {
-  const LaunchParams& P = *cx.P;
-  uint32_t off;
-  if (!ring_place(cx, r, tile_bytes, off)) return false;
-  const uint32_t s = r.issued % kSlots;
-  cx.S.slot_off[s] = off;
-  cx.S.slot_tile[s] = r.issued;
-  mbar_expect_tx(&cx.S.full[s], tile_bytes);
-  const int R = P.dm.attn_rows;
-  const int halves = P.dm.hd / 64;
-  uint8_t* dst = cx.S.ring + off;
-  for (int h = 0; h < halves; ++h) {
-    tma_load_3d(dst + h * R * 128, &P.tmap_k, h * 64, row, hk, &cx.S.full[s]);
-    tma_load_3d(dst + (halves + h) * R * 128, &P.tmap_v, h * 64, row, hk, &cx.S.full[s]);
-  }
-  ++r.issued;
-  if (r.ra_on) {
-    r.ra->used += tile_bytes;
-    r.ra->pump();
-  }
-  return true;
-}
-
-// the contiguous bytes of this block's units of a dense weight (see load_dense)
+// the contiguous bytes of this block's units of a dense weight (run-ahead lists)
 __device__ void add_dense_range(RunAhead& ra, const uint8_t* W, int K, int N, int rot) {
   int lo, hi;
   unit_range(N / 16, rot_block(blockIdx.x, rot, gridDim.x), gridDim.x, lo, hi);
@@ -382,34 +344,149 @@ __device__ void add_dense_range(RunAhead& ra, const uint8_t* W, int K, int N, in
   ra.add(W + (uint64_t)lo * ub, (uint64_t)(hi - lo) * ub);
 }
 
-__device__ bool load_dense(Ctx& cx, Ring& r, const uint8_t* W, int K, int N, int rot, uint64_t pol,
-                           int trace = -1) {
-  const LaunchParams& P = *cx.P;
+// L2 run-ahead lists (off by default): kept out of line, so that the loader's hot
+// path stays small in the instruction cache
+__device__ __noinline__ void ra_front(const LaunchParams& P, RunAhead* ra, int block, int r0, int r1, int hk) {
+  const Dims& dm = P.dm;
+  // everything up to the routing decision, in the order the ring streams it
+  if (P.first) add_dense_range(*ra, P.w_qkv_pro, dm.d, dm.nqkv, P.phase_rot * 1);
+  if (r1 > r0) {
+    const uint64_t off = ((uint64_t)hk * dm.max_ctx + r0) * dm.hd, bytes = (uint64_t)(r1 - r0) * dm.hd * 2;
+    ra->add(P.kc + off, bytes);
+    ra->add(P.vc + off, bytes);
+  }
+  add_dense_range(*ra, P.w_o, dm.hq * dm.hd, dm.d, P.phase_rot * 3);
+  add_dense_range(*ra, P.w_pool, dm.d, dm.p, P.phase_rot * 4);
+  add_dense_range(*ra, P.w_router, dm.p, dm.e, P.phase_rot * 5);
+  if (block == 0) {
+    prefetch_l2(P.g_moe, (uint32_t)dm.d * 2);
+    if (P.g_tail) prefetch_l2(P.g_tail, (uint32_t)dm.d * 2);
+  }
+  ra->pump();
+}
+__device__ __noinline__ void ra_back(const LaunchParams& P, RunAhead* ra, int block, int na) {
+  const Dims& dm = P.dm;
   const int G = gridDim.x;
-  int lo, hi;
-  unit_range(N / 16, rot_block(cx.block, rot, G), G, lo, hi);
-  const int steps = K / 16;
-  const uint64_t ub = dense_unit_bytes(K);
-  for (int u = lo; u < hi; ++u) {
-    for (int k0 = 0; k0 < steps; k0 += kDenseTileSteps) {
-      int ns = min(kDenseTileSteps, steps - k0);
-      const uint8_t* src = W + (uint64_t)u * ub + (uint64_t)k0 * kKStepBytes;
-      if (!ring_issue(cx, r, src, (uint32_t)ns * kKStepBytes, pol)) return false;
-      if (trace >= 0 && (P.flags & 0x1u) && ((u == lo && k0 == 0) || (u == hi - 1 && k0 + kDenseTileSteps >= steps)))
-        P.timing[(size_t)cx.block * kTimingEvents + trace + (u == lo && k0 == 0 ? 0 : 1)] = globaltimer();
-      if (trace >= 0 && (P.flags & 0x1u) && u == lo + 1 && k0 == 0)
-        P.timing[(size_t)cx.block * kTimingEvents + EV_LD_OP_U1] = globaltimer();
+  const int u1pe = dm.f / 8, u2pe = dm.p / 16;
+  const uint64_t ub1 = exp_unit_bytes(dm.p), ub2 = exp_unit_bytes(dm.f);
+  // the rest of the launch's stream: this block's expert units (runs of one expert
+  // are contiguous), the unpooler, then the next layer's QKV or the LM head
+  for (int pass = 0; pass < 2; ++pass) {
+    const int upe = pass ? u2pe : u1pe;
+    const uint64_t ub = pass ? ub2 : ub1;
+    int lo, hi;
+    unit_range(na * upe, rot_block(block, P.phase_rot * (pass ? 7 : 6), G), G, lo, hi);
+    for (int gu = lo; gu < hi;) {
+      const int run = min(hi, (gu / upe + 1) * upe) - gu;
+      ra->add(nullptr, (uint64_t)run * ub);  // expert tiles: streamed, not prefetched
+      gu += run;
     }
   }
-  (void)P;
-  return true;
+  add_dense_range(*ra, P.w_unpool, dm.p, dm.d, P.phase_rot * 8);
+  if (!P.last) add_dense_range(*ra, P.w_tail, dm.d, dm.nqkv, P.phase_rot * 9);
+  else if (dm.vocab > 0) add_dense_range(*ra, P.w_tail, dm.d, dm.vocab, P.phase_rot * 9);
+  ra->pump();
 }
+__device__ __noinline__ void ra_pump(RunAhead* ra, uint32_t bytes) {
+  ra->used += bytes;
+  ra->pump();
+}
+
+// The launch's tile stream in consumption order, produced one tile per call of next()
+// (one copy of the issue path, instead of one inlined per weight): segment 0 the
+// prologue QKV (launch 0), 1 this block's KV tiles, 2 the dependency wait, 3 o_proj,
+// 4 pooler, 5 router, 6 this block's routing decision, 7 GEMM1 units, 8 GEMM2 units,
+// 9 unpooler, 10 the next layer's QKV or the LM head.  Only scalars (registers).
+enum : int { TS_TILE = 0, TS_KV = 1, TS_DEP_WAIT = 2, TS_ROUTE_WAIT = 3, TS_END = 4 };
+struct TileStream {
+  int seg;
+  int lo, hi, u;     // units of the segment; u: unit of the next tile
+  int k0, steps;     // dense: next k-step within unit u; k-steps per unit
+  int upe;           // experts: units per expert
+  uint64_t ub;       // bytes per unit
+  const uint8_t* W;  // weights of the segment
+  int kv_r0, kv_hk;  // KV: first row, kv head
+  // the tile just produced: its unit and first k-step (for the loader's stamps)
+  int t_u, t_k0;
+
+  __device__ void dense(const uint8_t* w, int K, int N, int rot) {
+    unit_range(N / 16, rot_block(blockIdx.x, rot, gridDim.x), gridDim.x, lo, hi);
+    u = lo;
+    k0 = 0;
+    steps = K / 16;
+    ub = dense_unit_bytes(K);
+    W = w;
+  }
+  __device__ void experts(const uint8_t* w, int n_units, int per_expert, uint64_t unit_bytes, int rot) {
+    unit_range(n_units, rot_block(blockIdx.x, rot, gridDim.x), gridDim.x, lo, hi);
+    u = lo;
+    upe = per_expert;
+    ub = unit_bytes;
+    W = w;
+  }
+  // TS_TILE: src / bytes set; TS_KV: kv_row set; else a wait or the end
+  __device__ int next(const Ctx& cx, const uint8_t*& src, uint32_t& bytes, int& kv_row) {
+    const LaunchParams& P = *cx.P;
+    const Dims& dm = P.dm;
+    for (;;) {
+      if (u < hi) {
+        t_u = u;
+        t_k0 = k0;
+        if (seg == 1) {
+          kv_row = kv_r0 + (u - lo) * dm.attn_rows;
+          bytes = (uint32_t)dm.attn_rows * dm.hd * 2 * 2;
+          ++u;
+          return TS_KV;
+        }
+        if (seg == 7 || seg == 8) {
+          const int e = cx.S.act_e[u / upe];
+          src = W + ((uint64_t)e * upe + u % upe) * ub;
+          bytes = (uint32_t)ub;
+          ++u;
+          return TS_TILE;
+        }
+        const int ns = min(kDenseTileSteps, steps - k0);
+        src = W + (uint64_t)u * ub + (uint64_t)k0 * kKStepBytes;
+        bytes = (uint32_t)ns * kKStepBytes;
+        k0 += kDenseTileSteps;
+        if (k0 >= steps) {
+          k0 = 0;
+          ++u;
+        }
+        return TS_TILE;
+      }
+      ++seg;
+      lo = hi = u = k0 = 0;
+      switch (seg) {
+        case 1: {
+          const AttnUnit au = attn_unit(P, rot_block(cx.block, P.phase_rot * 2, gridDim.x), P.is_global);
+          hi = au.n_sub;
+          kv_r0 = au.r0;
+          kv_hk = au.hk;
+          break;
+        }
+        case 2: return TS_DEP_WAIT;
+        case 3: dense(P.w_o, dm.hq * dm.hd, dm.d, P.phase_rot * 3); break;
+        case 4: dense(P.w_pool, dm.d, dm.p, P.phase_rot * 4); break;
+        case 5: dense(P.w_router, dm.p, dm.e, P.phase_rot * 5); break;
+        case 6: return TS_ROUTE_WAIT;
+        case 7: experts(P.w1, *cx.S.n_active * (dm.f / 8), dm.f / 8, exp_unit_bytes(dm.p), P.phase_rot * 6); break;
+        case 8: experts(P.w2, *cx.S.n_active * (dm.p / 16), dm.p / 16, exp_unit_bytes(dm.f), P.phase_rot * 7); break;
+        case 9: dense(P.w_unpool, dm.p, dm.d, P.phase_rot * 8); break;
+        case 10:
+          if (!P.last) dense(P.w_tail, dm.d, dm.nqkv, P.phase_rot * 9);
+          else if (dm.vocab > 0) dense(P.w_tail, dm.d, dm.vocab, P.phase_rot * 9);
+          break;
+        default: return TS_END;
+      }
+    }
+  }
+};
 
 template <bool kTiming>
 __device__ void loader(Ctx& cx) {
   const LaunchParams& P = *cx.P;
   const Dims& dm = P.dm;
-  const int G = gridDim.x;
   const uint64_t pol = policy_evict_first();
   prefetch_tensormap(&P.tmap_k);
   prefetch_tensormap(&P.tmap_v);
@@ -422,79 +499,70 @@ __device__ void loader(Ctx& cx) {
   r.ra = cx.S.ring_state;
   r.ra->init(P.runahead_bytes);
   r.ra_on = P.runahead_bytes != 0;
+  TileStream ts;
+  ts.seg = 0;
+  ts.lo = ts.hi = ts.u = ts.k0 = 0;
+  // segment 0: the prologue QKV (launch 0); weights and KV rows do not depend on the
+  // previous launch, so they stream before the dependency wait
+  if (P.first) ts.dense(P.w_qkv_pro, dm.d, dm.nqkv, P.phase_rot * 1);
+  if (r.ra_on) {
+    const AttnUnit au = attn_unit(P, rot_block(cx.block, P.phase_rot * 2, gridDim.x), P.is_global);
+    ra_front(P, r.ra, cx.block, au.valid ? au.r0 : 0, au.valid ? au.r1 : 0, au.hk);
+  }
   bool ok = true;
-  const AttnUnit au = attn_unit(P, rot_block(cx.block, P.phase_rot * 2, G), P.is_global);
-  if (r.ra->ahead) {
-    // everything up to the routing decision, in the order the ring streams it
-    if (P.first) add_dense_range(*r.ra, P.w_qkv_pro, dm.d, dm.nqkv, P.phase_rot * 1);
-    if (au.valid && au.r1 > au.r0) {
-      const uint64_t off = ((uint64_t)au.hk * dm.max_ctx + au.r0) * dm.hd, bytes = (uint64_t)(au.r1 - au.r0) * dm.hd * 2;
-      r.ra->add(P.kc + off, bytes);
-      r.ra->add(P.vc + off, bytes);
+  int g1_last = -1;
+  while (ok) {
+    const uint8_t* src = nullptr;
+    uint32_t bytes = 0;
+    int kv_row = 0;
+    const int st = ts.next(cx, src, bytes, kv_row);
+    if (st == TS_END) break;
+    if (st == TS_DEP_WAIT) {
+      // the deadline of the bounded waits starts once the previous launch is done
+      pdl_wait();
+      cx.deadline = globaltimer() + (((uint64_t)P.timeout_ns_hi << 32) | P.timeout_ns_lo);
+      continue;
     }
-    add_dense_range(*r.ra, P.w_o, dm.hq * dm.hd, dm.d, P.phase_rot * 3);
-    add_dense_range(*r.ra, P.w_pool, dm.d, dm.p, P.phase_rot * 4);
-    add_dense_range(*r.ra, P.w_router, dm.p, dm.e, P.phase_rot * 5);
-    if (cx.block == 0) {
-      prefetch_l2(P.g_moe, (uint32_t)dm.d * 2);
-      if (P.g_tail) prefetch_l2(P.g_tail, (uint32_t)dm.d * 2);
+    if (st == TS_ROUTE_WAIT) {
+      // expert tiles wait for this block's routing decision
+      ok = wait_bar(cx, cx.S.route_bar, 0, PH_ROUTE);
+      stamp<kTiming>(P, cx.block, EV_LOADER_ROUTED);
+      if (ok && r.ra_on) ra_back(P, r.ra, cx.block, *cx.S.n_active);
+      continue;
     }
-    r.ra->pump();
-  }
-  // weights do not depend on the previous launch: stream before the dependency wait
-  if (P.first) ok = ok && load_dense(cx, r, P.w_qkv_pro, dm.d, dm.nqkv, P.phase_rot * 1, pol);
-  {
-    const uint32_t tb = (uint32_t)dm.attn_rows * dm.hd * 2 * 2;
-    for (int i = 0; ok && i < au.n_sub; ++i) ok = ring_issue_kv(cx, r, au.hk, au.r0 + i * dm.attn_rows, tb);
-  }
-  // the deadline of the bounded waits starts once the previous launch is done
-  pdl_wait();
-  cx.deadline = globaltimer() + (((uint64_t)P.timeout_ns_hi << 32) | P.timeout_ns_lo);
-  ok = ok && load_dense(cx, r, P.w_o, dm.hq * dm.hd, dm.d, P.phase_rot * 3, pol, EV_LD_OP_FIRST);
-  ok = ok && load_dense(cx, r, P.w_pool, dm.d, dm.p, P.phase_rot * 4, pol);
-  ok = ok && load_dense(cx, r, P.w_router, dm.p, dm.e, P.phase_rot * 5, pol);
-  // expert tiles wait for this block's routing decision
-  ok = ok && wait_bar(cx, cx.S.route_bar, 0, PH_ROUTE);
-  stamp<kTiming>(P, cx.block, EV_LOADER_ROUTED);
-  if (ok) {
-    const int na = *cx.S.n_active;
-    const int u1pe = dm.f / 8, u2pe = dm.p / 16;
-    const uint64_t ub1 = exp_unit_bytes(dm.p), ub2 = exp_unit_bytes(dm.f);
-    int lo, hi;
-    if (r.ra->ahead) {
-      // the rest of the launch's stream: this block's expert units (runs of one expert
-      // are contiguous), the unpooler, then the next layer's QKV or the LM head
-      for (int pass = 0; pass < 2; ++pass) {
-        const int upe = pass ? u2pe : u1pe;
-        const uint64_t ub = pass ? ub2 : ub1;
-        unit_range(na * upe, rot_block(cx.block, P.phase_rot * (pass ? 7 : 6), G), G, lo, hi);
-        for (int gu = lo; gu < hi;) {
-          const int run = min(hi, (gu / upe + 1) * upe) - gu;
-          r.ra->add(nullptr, (uint64_t)run * ub);  // expert tiles: streamed, not prefetched
-          gu += run;
-        }
+    uint32_t off;
+    if (!ring_place(cx, r, bytes, off)) {
+      ok = false;
+      break;
+    }
+    const uint32_t s = r.issued % kSlots;
+    cx.S.slot_off[s] = off;
+    cx.S.slot_tile[s] = r.issued;
+    mbar_expect_tx(&cx.S.full[s], bytes);
+    if (st == TS_KV) {
+      const int R = dm.attn_rows, halves = dm.hd / 64;
+      uint8_t* dst = cx.S.ring + off;
+      for (int h = 0; h < halves; ++h) {
+        tma_load_3d(dst + h * R * 128, &P.tmap_k, h * 64, kv_row, ts.kv_hk, &cx.S.full[s]);
+        tma_load_3d(dst + (halves + h) * R * 128, &P.tmap_v, h * 64, kv_row, ts.kv_hk, &cx.S.full[s]);
       }
-      add_dense_range(*r.ra, P.w_unpool, dm.p, dm.d, P.phase_rot * 8);
-      if (!P.last) add_dense_range(*r.ra, P.w_tail, dm.d, dm.nqkv, P.phase_rot * 9);
-      else if (dm.vocab > 0) add_dense_range(*r.ra, P.w_tail, dm.d, dm.vocab, P.phase_rot * 9);
-      r.ra->pump();
+    } else {
+      bulk_g2s(cx.S.ring + off, src, bytes, &cx.S.full[s], pol);
     }
-    unit_range(na * u1pe, rot_block(cx.block, P.phase_rot * 6, G), G, lo, hi);
-    for (int gu = lo; ok && gu < hi; ++gu) {
-      int e = cx.S.act_e[gu / u1pe];
-      ok = ring_issue(cx, r, P.w1 + ((uint64_t)e * u1pe + gu % u1pe) * ub1, (uint32_t)ub1, pol);
-      if (gu == lo) stamp<kTiming>(P, cx.block, EV_LD_G1_FIRST);
-      if (gu == hi - 1) stamp<kTiming>(P, cx.block, EV_LD_G1_LAST);
-    }
-    unit_range(na * u2pe, rot_block(cx.block, P.phase_rot * 7, G), G, lo, hi);
-    for (int gu = lo; ok && gu < hi; ++gu) {
-      int e = cx.S.act_e[gu / u2pe];
-      ok = ring_issue(cx, r, P.w2 + ((uint64_t)e * u2pe + gu % u2pe) * ub2, (uint32_t)ub2, pol);
+    ++r.issued;
+    if (r.ra_on) ra_pump(r.ra, bytes);
+    if (kTiming) {
+      if (ts.seg == 3) {
+        if (ts.t_u == ts.lo && ts.t_k0 == 0) stamp<kTiming>(P, cx.block, EV_LD_OP_FIRST);
+        if (ts.t_u == ts.lo + 1 && ts.t_k0 == 0) stamp<kTiming>(P, cx.block, EV_LD_OP_U1);
+        if (ts.u == ts.hi) stamp<kTiming>(P, cx.block, EV_LD_OP_LAST);
+      } else if (ts.seg == 7) {
+        if (ts.t_u == ts.lo) stamp<kTiming>(P, cx.block, EV_LD_G1_FIRST);
+        if (ts.u == ts.hi) g1_last = ts.t_u;
+        if (ts.t_u == g1_last) stamp<kTiming>(P, cx.block, EV_LD_G1_LAST);
+      }
     }
   }
-  ok = ok && load_dense(cx, r, P.w_unpool, dm.p, dm.d, P.phase_rot * 8, pol);
-  if (!P.last) ok = ok && load_dense(cx, r, P.w_tail, dm.d, dm.nqkv, P.phase_rot * 9, pol);
-  else if (dm.vocab > 0) ok = ok && load_dense(cx, r, P.w_tail, dm.d, dm.vocab, P.phase_rot * 9, pol);
   stamp<kTiming>(P, cx.block, EV_LOADER_END);
   if (!ok) {
     // give every copy still in flight a chance to land before the block exits
