@@ -269,8 +269,8 @@ msm_status msm_get_tree(msm_model* model, uint32_t* anc, int32_t* tpos);
  *   warp (first unit's tile ready / unit done, last unit's tile ready / done),
  *   44 / 45 loader issued the first / last o_proj tile, 46 / 47 the first / last
  *   GEMM1 tile; 48-51 GEMM2 of the first compute warp pair (first unit's tile ready
- *   / unit done, last unit's tile ready / done), 52 / 53 staging of the block's
- *   second expert for GEMM2 begun / done, 54 loader issued the first tile of the
+ *   / unit done, last unit's tile ready / done), 52 / 53 second GEMM2 staging
+ *   round (experts 3-4 of a block; two per round) begun / done, 54 loader issued the first tile of the
  *   block's second o_proj unit.
  * `n` is the capacity of `buf` in elements. */
 #define MSM_TIMING_EVENTS 64

@@ -236,9 +236,9 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   const uint64_t attn_need = (uint64_t)dm.group * (D / 16) * kKStepBytes + 2ull * 16 * D * 2 +
                              (uint64_t)dm.group * dm.attn_wph * 32 * (4 + D / 2) * 4;
   const uint64_t kmax = (uint64_t)std::max(std::max(dm.d, dm.hq * dm.hd), dm.p);
-  // GEMM1: x_q of 16 tokens + one bf16 row per warp; GEMM2: one expert's a_q + one fp32 row per warp
-  const uint64_t g1_need = (uint64_t)dm.p * 32 + (uint64_t)kComputeWarps * dm.p * 2;
-  const uint64_t g2_need = (uint64_t)dm.f * 32 + (uint64_t)kComputeWarps * dm.f * 4;
+  // GEMM1: the 16 tokens' pooled vectors; GEMM2: two experts' a_q + one fp32 row per warp
+  const uint64_t g1_need = (uint64_t)dm.p * 32;
+  const uint64_t g2_need = 2ull * dm.f * 32 + (uint64_t)kComputeWarps * dm.f * 4;
   uint64_t act = std::max(std::max(kmax * 32, g1_need), std::max(g2_need, attn_need));
   act = (act + 1023) & ~uint64_t(1023);
   const int smem_cap = std::min(kMaxSmem, smem_optin);

@@ -46,14 +46,15 @@ struct Smem {
   uint8_t* act_tok;   // [128][16]
   uint8_t* act_slot;  // [128][16]
   float* x_ts;        // [16]
-  float* a_ts;        // [16]
+  float* a_ts;        // [2][16]
   float* red;         // [8][16]
   volatile uint32_t* slot_tile;  // [kSlots] index of the tile the loader last put in each slot
   struct RunAhead* ring_state;    // the loader's L2 run-ahead lists
   float* dred;        // [8][16][16] dense-phase cross-warp partial sums
 };
 
-constexpr int kRingStateOff = 6656;  // in the small area, below the reduction scratch at 8192
+constexpr int kRingStateOff = 6656;  // in the small area, below the GEMM2 row scales
+constexpr int kATsOff = 7936;        // [2][16] floats, below the reduction scratch at 8192
 __device__ __forceinline__ Smem carve(uint8_t* base, const LaunchParams& P) {
   Smem s;
   s.ring = base;
@@ -75,7 +76,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const LaunchParams& P) {
   s.act_tok = sm + 1856;
   s.act_slot = sm + 3904;
   s.x_ts = reinterpret_cast<float*>(sm + 5952);
-  s.a_ts = reinterpret_cast<float*>(sm + 6016);
+  s.a_ts = reinterpret_cast<float*>(sm + kATsOff);
   s.red = reinterpret_cast<float*>(sm + 6080);
   s.slot_tile = reinterpret_cast<volatile uint32_t*>(sm + 6592);
   s.ring_state = reinterpret_cast<struct RunAhead*>(sm + kRingStateOff);
@@ -298,7 +299,7 @@ struct Ring {
   bool ra_on;         // L2 run-ahead enabled
   RunAhead* ra;       // L2 run-ahead state (shared memory)
 };
-static_assert(kRingStateOff + sizeof(RunAhead) <= 8192, "run-ahead state overlaps the reduction scratch");
+static_assert(kRingStateOff + sizeof(RunAhead) <= kATsOff, "run-ahead state overlaps the GEMM2 row scales");
 
 // a free run of `bytes` (1 KB granules) after the newest tile, at the bottom once the
 // top is too short; waits for the oldest tiles' release until there is one
@@ -1715,21 +1716,26 @@ __device__ void gemm2_phase(Worker& w) {
   unit_range(na * u2pe, rot_block(cx.block, P.phase_rot * 7, G), G, lo, hi);
   const float* ain = reinterpret_cast<const float*>(P.x_cur + P.xo.a);
   uint16_t* yout = reinterpret_cast<uint16_t*>(P.s_buf + P.so.y);
-  const uint32_t act_s = smem_u32(cx.S.act);
+  const uint32_t region = (uint32_t)dm.f * 32;  // one expert's 16 activation rows, f16, B layout
   const int pair = w.cw >> 1, half = w.cw & 1, ng = dm.f / 64;
   const int g0 = half ? ng / 2 : 0, g1 = half ? ng : ng / 2;
   int it = 0;
   if (hi > lo) {
     const int a_first = lo / u2pe, a_last = (hi - 1) / u2pe;
-    for (int a = a_first; a <= a_last; ++a) {
-      const int e = cx.S.act_e[a], n = cx.S.act_n[a];
-      cbar();  // previous expert's units are done with the act buffer
-      if (a == a_first + 1) stamp_rt(P, EV_G2_STAGE2_IN);
+    // the block's experts two at a time (one round unless its units span more than
+    // two), so that a block whose units cross an expert boundary does not stop half
+    // way to stage the second expert's input
+    for (int a0 = a_first; a0 <= a_last; a0 += 2) {
+      const int a1 = min(a0 + 1, a_last);
+      cbar();  // the previous round's units are done with the act buffer
+      if (a0 != a_first) stamp_rt(P, EV_G2_STAGE2_IN);
       if (*cx.S.abort) w.ok = false;
-      // stage this expert's NVFP4 activations: row p = p-th token of the expert
-      for (int p = w.cw; p < n && w.ok; p += kComputeWarps) {
-        const float* row = ain + (size_t)cx.S.act_slot[a * 16 + p] * dm.f;
-        float* rowbuf = reinterpret_cast<float*>(cx.S.act + (size_t)dm.f * 32) + (size_t)w.cw * dm.f;
+      // NVFP4 of every activation row of the round: row p of expert a = its p-th token
+      const int n0 = cx.S.act_n[a0], nrows = n0 + (a1 > a0 ? cx.S.act_n[a1] : 0);
+      float* rowbuf = reinterpret_cast<float*>(cx.S.act + 2 * region) + (size_t)w.cw * dm.f;
+      for (int r = w.cw; r < nrows && w.ok; r += kComputeWarps) {
+        const int ea = r < n0 ? 0 : 1, p = r - ea * n0;
+        const float* row = ain + (size_t)cx.S.act_slot[(a0 + ea) * 16 + p] * dm.f;
         // poll the row into shared memory (every pending chunk of a batch is re-read in
         // the same round), tracking the row's largest magnitude on the way
         const int nch4 = dm.f / 4;
@@ -1766,7 +1772,7 @@ __device__ void gemm2_phase(Worker& w) {
           const float m = frexpf(ts, &ex);
           if (m != 0.5f) ts = ldexpf(1.0f, ex);
         }
-        uint8_t* act = cx.S.act;
+        uint8_t* act = cx.S.act + ea * region;
         for (int base = 0; base < dm.f; base += 128) {
           const int k = base + w.lane * 4;
           const bool in = k < dm.f;
@@ -1788,57 +1794,61 @@ __device__ void gemm2_phase(Worker& w) {
             *reinterpret_cast<uint32_t*>(act + act_off(p, k + 2) + ((k + 2) & 7) * 2) = hmul2(e2m1x2_to_f16x2(c23), s2);
           }
         }
-        __syncwarp();
-        if (w.lane == 0) cx.S.a_ts[p] = ts;
+        __syncwarp();  // the warp's next row reuses rowbuf
+        if (w.lane == 0) cx.S.a_ts[ea * 16 + p] = ts;
       }
       w.ok = __all_sync(0xffffffffu, w.ok);
       cbar();
-      if (a == a_first) stamp_rt(P, EV_GEMM2_IN);
-      if (a == a_first + 1) stamp_rt(P, EV_G2_STAGE2_DONE);
+      if (a0 == a_first) stamp_rt(P, EV_GEMM2_IN);
+      else stamp_rt(P, EV_G2_STAGE2_DONE);
       if (*cx.S.abort) w.ok = false;
-      const int u_lo = max(lo, a * u2pe), u_hi = min(hi, (a + 1) * u2pe);
-      // units of this expert: pair j takes every 4th (counted from the block's first unit)
-      int gu = u_lo + ((pair - (u_lo - lo)) % (kComputeWarps / 2) + kComputeWarps / 2) % (kComputeWarps / 2);
-      for (; gu < u_hi; gu += kComputeWarps / 2, ++it) {
-        const int loc = gu - lo;
-        const int pr = gu % u2pe;
-        const uint32_t t = w.ti + (uint32_t)loc;
-        const uint32_t s = t % kSlots;
-        bool got = w.ok && wait_tile(cx, t, PH_GEMM2);
-        const bool first_u = gu - pair < lo + kComputeWarps / 2 && a == a_first;
-        const bool last_u = gu + kComputeWarps / 2 >= hi;
-        if (half == 0 && first_u) stamp_rt(P, EV_G2_FIRST_READY);
-        if (half == 0 && last_u) stamp_rt(P, EV_G2_LAST_READY);
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        if (got) {
-          const int r8 = w.lane & 7;
-          const int rows[2] = {r8 < n ? r8 : 0, 8 + r8 < n ? 8 + r8 : 0};
-          if (n > 8) exp_unit_mma<2>(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, act_s, w.lane, rows);
-          else exp_unit_mma<1>(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, act_s, w.lane, rows);
-          __syncwarp();
-          if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps / 2);
-        }
-        if (!pair_reduce(w, acc, got, it)) {
-          w.ok = false;
-          break;
-        }
-        if (half == 0) {
-          const float gs = P.w2_gs[e] * kExpScaleUndo;
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int ii = 0; ii < 2; ++ii) {
-              const int p = nt * 8 + 2 * w.q + ii;
-              if (p < n) {
-                const int slot = cx.S.act_slot[a * 16 + p];
-                const float sc = cx.S.a_ts[p] * gs;
-                st_relaxed_u16(yout + (size_t)slot * dm.p + pr * 16 + w.g, bf16_bits_rn(acc[nt][ii] * sc));
-                st_relaxed_u16(yout + (size_t)slot * dm.p + pr * 16 + w.g + 8, bf16_bits_rn(acc[nt][2 + ii] * sc));
+      for (int a = a0; a <= a1; ++a) {
+        const int e = cx.S.act_e[a], n = cx.S.act_n[a], ea = a - a0;
+        const uint32_t act_s = smem_u32(cx.S.act) + ea * region;
+        const int u_lo = max(lo, a * u2pe), u_hi = min(hi, (a + 1) * u2pe);
+        // units of this expert: pair j takes every 4th (counted from the block's first unit)
+        int gu = u_lo + ((pair - (u_lo - lo)) % (kComputeWarps / 2) + kComputeWarps / 2) % (kComputeWarps / 2);
+        for (; gu < u_hi; gu += kComputeWarps / 2, ++it) {
+          const int loc = gu - lo;
+          const int pr = gu % u2pe;
+          const uint32_t t = w.ti + (uint32_t)loc;
+          const uint32_t s = t % kSlots;
+          bool got = w.ok && wait_tile(cx, t, PH_GEMM2);
+          const bool first_u = gu - pair < lo + kComputeWarps / 2 && a == a_first;
+          const bool last_u = gu + kComputeWarps / 2 >= hi;
+          if (half == 0 && first_u) stamp_rt(P, EV_G2_FIRST_READY);
+          if (half == 0 && last_u) stamp_rt(P, EV_G2_LAST_READY);
+          float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+          if (got) {
+            const int r8 = w.lane & 7;
+            const int rows[2] = {r8 < n ? r8 : 0, 8 + r8 < n ? 8 + r8 : 0};
+            if (n > 8) exp_unit_mma<2>(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, act_s, w.lane, rows);
+            else exp_unit_mma<1>(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, act_s, w.lane, rows);
+            __syncwarp();
+            if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps / 2);
+          }
+          if (!pair_reduce(w, acc, got, it)) {
+            w.ok = false;
+            break;
+          }
+          if (half == 0) {
+            const float gs = P.w2_gs[e] * kExpScaleUndo;
+  #pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+  #pragma unroll
+              for (int ii = 0; ii < 2; ++ii) {
+                const int p = nt * 8 + 2 * w.q + ii;
+                if (p < n) {
+                  const int slot = cx.S.act_slot[a * 16 + p];
+                  const float sc = cx.S.a_ts[ea * 16 + p] * gs;
+                  st_relaxed_u16(yout + (size_t)slot * dm.p + pr * 16 + w.g, bf16_bits_rn(acc[nt][ii] * sc));
+                  st_relaxed_u16(yout + (size_t)slot * dm.p + pr * 16 + w.g + 8, bf16_bits_rn(acc[nt][2 + ii] * sc));
+                }
               }
-            }
+          }
+          if (half == 0 && first_u) stamp_rt(P, EV_G2_FIRST_DONE);
+          if (half == 0 && last_u) stamp_rt(P, EV_G2_LAST_DONE);
         }
-        if (half == 0 && first_u) stamp_rt(P, EV_G2_FIRST_DONE);
-        if (half == 0 && last_u) stamp_rt(P, EV_G2_LAST_DONE);
       }
     }
   }
