@@ -13,12 +13,17 @@
 //   warps 4-11  attention, dense GEMMs, expert GEMMs, combines
 // The launch covers layer l's attention through layer l+1's QKV projection and
 // KV-cache write (alphasignal.ai, § "Launch boundaries leave hardware idle").
-// Blocks hand data to each other through global-memory slots that carry their
-// own readiness: a slot is empty while it holds a sentinel (0xFFFF for bf16, an
-// all-ones NaN no rounding produces; -0.0 for fp32, since writers store x+0.0)
-// and consumers poll the payload itself, with no write-fence-flag sequence
-// (alphasignal.ai, § "Four mechanisms keep work moving"; orcarouter.ai, §
-// "three bills").  Every wait is bounded by %globaltimer.
+// Blocks hand each phase's output to each other through global memory. Every
+// block, once it has stored its share, adds 1 to that phase's counter after a
+// gpu-scope fence, and consumers wait for the counter to reach the grid size:
+// on one GPU every dense phase's output is read by all blocks, and polling each
+// element while producers write held consumers far longer than one counter.
+// The expert GEMM1 -> GEMM2 rows and the prologue's Q / tree K/V keep the
+// pages' data-as-flag slots: empty while they hold a sentinel (0xFFFF for bf16,
+// an all-ones NaN no rounding produces; -0.0 for fp32, since writers store
+// x+0.0), polled in the payload itself (alphasignal.ai, § "Four mechanisms keep
+// work moving"; orcarouter.ai, § "three bills").  Every wait is bounded by
+// %globaltimer.
 #include "msm_device.cuh"
 #include "msm_internal.h"
 
@@ -152,24 +157,6 @@ __device__ __forceinline__ bool poll_bf16x8(Ctx& cx, const void* p, uint4& v, in
   while (!bf16x8_ready(v)) {
     if ((++n & 31) == 0 && cx.expired(phase)) return false;
     v = ld_relaxed_v4(p);
-  }
-  return true;
-}
-__device__ __forceinline__ bool poll_f32x4(Ctx& cx, const void* p, uint4& v, int phase) {
-  uint32_t n = 0;
-  v = ld_relaxed_v4(p);
-  while (!f32x4_ready(v)) {
-    if ((++n & 31) == 0 && cx.expired(phase)) return false;
-    v = ld_relaxed_v4(p);
-  }
-  return true;
-}
-__device__ __forceinline__ bool poll_f32x2(Ctx& cx, const void* p, uint2& v, int phase) {
-  uint32_t n = 0;
-  v = ld_relaxed_v2(p);
-  while (v.x == kF32Empty || v.y == kF32Empty) {
-    if ((++n & 31) == 0 && cx.expired(phase)) return false;
-    v = ld_relaxed_v2(p);
   }
   return true;
 }
