@@ -155,6 +155,21 @@ def test_repeat_runs_and_self_timing_are_bitwise_identical():
             assert np.array_equal(a["caches"][l][1], x["caches"][l][1])
 
 
+def test_prefetch_flags_are_bitwise_identical():
+    """The expert and KV L2 prefetches (and the L2 run-ahead) only move bytes toward
+    L2 earlier: the outputs are the same bits with them on or off, over two steps (the
+    expert prefetch uses the previous step's routing)."""
+    import moe_decode_megakernel_warp_gb300 as msm
+    case = make_case("cfg1_stack")
+    base = run_gpu(case, steps=2)
+    pf = run_gpu(case, steps=2, flags=msm.MSM_FLAG_PDL | msm.MSM_FLAG_EXPERT_PREFETCH | msm.MSM_FLAG_KV_PREFETCH)
+    assert base["status"] == [0, 0] and pf["status"] == [0, 0]
+    assert np.array_equal(base["logits"], pf["logits"])
+    for l in range(case.cfg.n_layers):
+        assert np.array_equal(base["caches"][l][0], pf["caches"][l][0])
+        assert np.array_equal(base["caches"][l][1], pf["caches"][l][1])
+
+
 def test_grid_size_invariance():
     """With the attention split count pinned, the result does not depend on how
     many blocks share the work (each output's reduction order is fixed)."""
