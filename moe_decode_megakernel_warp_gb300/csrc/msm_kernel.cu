@@ -1048,16 +1048,10 @@ __device__ __forceinline__ void attn_keys16(AttnState<D>& st, const uint32_t (&q
     st.o[n][2] *= alpha[1];
     st.o[n][3] *= alpha[1];
   }
-  // P as the sum of two bf16 parts: P.V carries ~16 significant bits of P (the
-  // residual error, 2^-17 of each weight, is far below the bf16 rounding of the output)
-  uint32_t ph[4], pm[4];
+  // P in bf16 (8 significant bits, as the bf16 rounding the attention output gets)
+  uint32_t ph[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float x0 = s[i >> 1][(i & 1) * 2], x1 = s[i >> 1][(i & 1) * 2 + 1];
-    const uint32_t h = pack_bf16x2(x0, x1);
-    ph[i] = h;
-    pm[i] = pack_bf16x2(x0 - bf16_to_f32((uint16_t)(h & 0xFFFFu)), x1 - bf16_to_f32((uint16_t)(h >> 16)));
-  }
+  for (int i = 0; i < 4; ++i) ph[i] = pack_bf16x2(s[i >> 1][(i & 1) * 2], s[i >> 1][(i & 1) * 2 + 1]);
 #pragma unroll
   for (int n = 0; n < D / 8; n += 2) {
     const int key = kb + (mi & 1) * 8 + r8;
@@ -1066,8 +1060,6 @@ __device__ __forceinline__ void attn_keys16(AttnState<D>& st, const uint32_t (&q
     ldsm_x4_t(vbase + swz(key, d0, rows), b0, b1, b2, b3);
     mma_bf16(st.o[n], ph[0], ph[1], ph[2], ph[3], b0, b1);
     mma_bf16(st.o[n + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
-    mma_bf16(st.o[n], pm[0], pm[1], pm[2], pm[3], b0, b1);
-    mma_bf16(st.o[n + 1], pm[0], pm[1], pm[2], pm[3], b2, b3);
   }
 }
 
