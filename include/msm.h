@@ -271,7 +271,9 @@ msm_status msm_get_tree(msm_model* model, uint32_t* anc, int32_t* tpos);
  *   GEMM1 tile; 48-51 GEMM2 of the first compute warp pair (first unit's tile ready
  *   / unit done, last unit's tile ready / done), 52 / 53 second GEMM2 staging
  *   round (experts 3-4 of a block; two per round) begun / done, 54 loader issued the first tile of the
- *   block's second o_proj unit.
+ *   block's second o_proj unit; 55-62 the block's poller saw the phase-completion
+ *   counter that releases the split merge, o_proj, pooler, router, top-k, combine,
+ *   unpooler and tail reach the grid size.
  * `n` is the capacity of `buf` in elements. */
 #define MSM_TIMING_EVENTS 64
 msm_status msm_get_timing(msm_model* model, uint64_t* buf, size_t n);

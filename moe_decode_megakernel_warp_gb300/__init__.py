@@ -44,7 +44,8 @@ EV = dict(start=0, pro_in=1, pro_done=2, attn_in=3, attn_done=4, merge_done=5, o
           op_u1_red=38, op_u1_epi=39, g1_first_ready=40, g1_first_done=41, g1_last_ready=42, g1_last_done=43,
           ld_op_first=44, ld_op_last=45, ld_g1_first=46, ld_g1_last=47,
           g2_first_ready=48, g2_first_done=49, g2_last_ready=50, g2_last_done=51, g2_stage2_in=52,
-          g2_stage2_done=53, ld_op_u1=54)
+          g2_stage2_done=53, ld_op_u1=54, seen_merge=55, seen_oproj=56, seen_pool=57, seen_router=58,
+          seen_route=59, seen_combine=60, seen_unpool=61, seen_tail=62)
 T = 16
 
 EXPORTED = ["msm_model_create", "msm_model_destroy", "msm_verify_step", "msm_verify_step_host", "msm_sync",

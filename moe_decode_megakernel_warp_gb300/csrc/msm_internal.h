@@ -42,7 +42,10 @@ enum TimingEvent : int {
   // the staging of the block's second expert (start, done)
   EV_G2_FIRST_READY = 48, EV_G2_FIRST_DONE = 49, EV_G2_LAST_READY = 50, EV_G2_LAST_DONE = 51,
   EV_G2_STAGE2_IN = 52, EV_G2_STAGE2_DONE = 53,
-  EV_LD_OP_U1 = 54  // loader issued the first tile of the block's second o_proj unit
+  EV_LD_OP_U1 = 54,  // loader issued the first tile of the block's second o_proj unit
+  // the block's poller saw a phase-completion counter reach the grid size
+  EV_SEEN_MERGE = 55, EV_SEEN_OPROJ = 56, EV_SEEN_POOL = 57, EV_SEEN_ROUTER = 58, EV_SEEN_ROUTE = 59,
+  EV_SEEN_COMBINE = 60, EV_SEEN_UNPOOL = 61, EV_SEEN_TAIL = 62
 };
 
 // phases of one layer launch (recorded in the status word on a timeout)

@@ -611,6 +611,11 @@ __device__ bool await_phase(Worker& w, int i, int phase) {
       if (v >= target) break;
       if ((++n & 15) == 0 && cx.expired(phase)) break;
     }
+    const int ev = phase == PH_ATTN_MERGE ? EV_SEEN_MERGE : phase == PH_OPROJ ? EV_SEEN_OPROJ
+                 : phase == PH_POOL ? EV_SEEN_POOL : phase == PH_ROUTER ? EV_SEEN_ROUTER
+                 : phase == PH_ROUTE ? EV_SEEN_ROUTE : phase == PH_COMBINE ? EV_SEEN_COMBINE
+                 : phase == PH_UNPOOL ? EV_SEEN_UNPOOL : EV_SEEN_TAIL;
+    stamp_rt(*cx.P, ev);
   }
   cbar();
   if (*cx.S.abort) w.ok = false;
@@ -640,12 +645,11 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, int cnt, bool p
   const int nch = K / 8;
   float2 ss2 = make_float2(0.f, 0.f);  // sums of squares of even / odd elements
   bool ok = w.ok;
-  // the norm gain does not depend on the producers: fetch it now (one copy per block,
-  // kept in the reduction scratch, which no one uses between dense phases)
-  const bool gain_smem = gain != nullptr && nch <= 2 * kComputeThreads &&
-                         K * 2 <= (int)(sizeof(float) * kComputeWarps * 16 * 16);
+  // the norm gain does not depend on the producers: fetch the two chunks this thread
+  // normalises now
+  const bool gain_pre = gain != nullptr && nch <= 2 * kComputeThreads;
   uint4 gpre[2];
-  if (gain_smem) {
+  if (gain_pre) {
 #pragma unroll
     for (int j = 0; j < 2; ++j)
       if (tid + j * kComputeThreads < nch) gpre[j] = ld_nc_v4_early(reinterpret_cast<const uint4*>(gain) + tid + j * kComputeThreads);
@@ -689,54 +693,57 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, int cnt, bool p
     }
   }
   if (gain != nullptr && phase == PH_POOL) stamp_rt(*cx.P, EV_POOL_STAGED);
-  if (gain_smem) {
-    uint4* gs = reinterpret_cast<uint4*>(cx.S.dred);
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-      if (tid + j * kComputeThreads < nch) gs[tid + j * kComputeThreads] = gpre[j];
-    cbar();
-    if (phase == PH_POOL) stamp_rt(*cx.P, EV_POOL_GAIN);
-  }
   ok = __all_sync(0xffffffffu, ok);
-  if (ok && gain != nullptr) {
+  if (gain != nullptr) {
+    // 1 / rms of each row: the row's 16 threads reduce their partial sums of squares,
+    // one of them leaves the factor in the (then unused) scan scratch
     float ss = ss2.x + ss2.y;
 #pragma unroll
     for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
-    const float2 inv2 = make_float2(inv, inv);
-    const uint4* gs = reinterpret_cast<const uint4*>(cx.S.dred);
-    // compact loop (this code runs once per phase, cold in the instruction cache):
-    // four chunks per iteration, all loads before any store
-    constexpr int kN = 4;
+    float* inv_s = cx.S.red;
+    if (sub == 0) inv_s[t] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
+    cbar();
+    if (phase == PH_POOL) stamp_rt(*cx.P, EV_POOL_GAIN);
+    if (ok) {
+      // thread tid owns chunk columns tid, tid + 256, ...: one gain chunk, then the 16
+      // rows, four at a time (all loads before any store).  A compact loop: this code
+      // runs once per phase, cold in the instruction cache.
 #pragma unroll 1
-    for (int c0 = sub; c0 < nch; c0 += 16 * kN) {
-      uint4 v[kN], gv[kN];
-      uint32_t off[kN];
+      for (int j = 0, c = tid; c < nch; ++j, c += kComputeThreads) {
+        const uint4 gv = (gain_pre && j < 2) ? (j == 0 ? gpre[0] : gpre[1])
+                                             : __ldg(reinterpret_cast<const uint4*>(gain + c * 8));
+        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+        float2 g2[4];
 #pragma unroll
-      for (int j = 0; j < kN; ++j) {
-        const int c = min(c0 + 16 * j, nch - 1);
-        off[j] = act_off(t, c * 8);
-        v[j] = *reinterpret_cast<const uint4*>(cx.S.act + off[j]);
-        gv[j] = gain_smem ? gs[c] : __ldg(reinterpret_cast<const uint4*>(gain + c * 8));
-      }
+        for (int i = 0; i < 4; ++i) g2[i] = make_float2(__uint_as_float(gw[i] << 16), __uint_as_float(gw[i] & 0xFFFF0000u));
+#pragma unroll 1
+        for (int r0 = 0; r0 < 16; r0 += 4) {
+          uint4 v[4];
+          uint32_t off[4];
+          float iv[4];
 #pragma unroll
-      for (int j = 0; j < kN; ++j) {
-        uint32_t wd[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-        const uint32_t gw[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
+          for (int q = 0; q < 4; ++q) {
+            off[q] = act_off(r0 + q, c * 8);
+            v[q] = *reinterpret_cast<const uint4*>(cx.S.act + off[q]);
+            iv[q] = inv_s[r0 + q];
+          }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          // (x * inv) * g per element in fp32, two elements per instruction; the result
-          // stays in shared memory, so no sentinel mapping is needed
-          const float2 xs = __fmul2_rn(make_float2(__uint_as_float(wd[i] << 16), __uint_as_float(wd[i] & 0xFFFF0000u)), inv2);
-          const float2 y = __fmul2_rn(xs, make_float2(__uint_as_float(gw[i] << 16), __uint_as_float(gw[i] & 0xFFFF0000u)));
-          const __nv_bfloat162 h = __floats2bfloat162_rn(y.x, y.y);
-          wd[i] = *reinterpret_cast<const uint32_t*>(&h);
+          for (int q = 0; q < 4; ++q) {
+            uint32_t wd[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+            const float2 inv2 = make_float2(iv[q], iv[q]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              // (x * inv) * g per element in fp32, two elements per instruction; the
+              // result stays in shared memory, so no sentinel mapping is needed
+              const float2 xs = __fmul2_rn(make_float2(__uint_as_float(wd[i] << 16), __uint_as_float(wd[i] & 0xFFFF0000u)), inv2);
+              const float2 y = __fmul2_rn(xs, g2[i]);
+              const __nv_bfloat162 h = __floats2bfloat162_rn(y.x, y.y);
+              wd[i] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(cx.S.act + off[q]) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          }
         }
-        v[j] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
       }
-#pragma unroll
-      for (int j = 0; j < kN; ++j)
-        if (c0 + 16 * j < nch) *reinterpret_cast<uint4*>(cx.S.act + off[j]) = v[j];
     }
   }
   if (gain != nullptr && phase == PH_POOL) stamp_rt(*cx.P, EV_POOL_NORMED);
