@@ -291,6 +291,57 @@ msm_status msm_get_stats(const msm_model* model, msm_stats* out);
 msm_status msm_get_exchange(msm_model* model, const char* name, void* host, size_t bytes);
 
 /*
+ * Accept step after a verify step: the target's greedy choice at each tree node,
+ * the walk down the tree, and KV-cache compaction (alphasignal.ai, § "Draft and
+ * verify share one graph": candidates the target agrees with become output
+ * tokens, rejected branches are dropped; orcarouter.ai, closing figure: greedy
+ * decoding, accept inside the step's CUDA graph).
+ *   logits   device fp32 [16][vocab], the verify step's logits_out (read)
+ *   tokens   host int32 [16]: the draft token of each tree node; tokens[0] (the
+ *            root) is not checked; every id must lie in [0, vocab)
+ *   parent   host int32 [16], the verify step's tree
+ *   pos0, k_cache, v_cache   as passed to the verify step
+ *   result   device int32 [MSM_ACCEPT_RESULT_INTS] (written):
+ *            [0] a = number of accepted nodes, root included (1..16)
+ *            [1] the bonus token: the greedy choice at the last accepted node
+ *            [2 + j] path[j], the j-th accepted node (path[0] = 0), -1 for j >= a
+ *            [18 + i] the greedy choice (argmax of the logits) at node i
+ * Greedy choice: the largest logit, the smallest index among equal ones; a NaN
+ * ranks above every number.  Walk: from the root, move to the child (smallest
+ * tree index first) whose token is the current node's choice; stop when none is.
+ * Compaction: for j < a, cache row pos0 + j of every layer, K and V, every KV head
+ * receives row pos0 + path[j]; no other row is written.  Everything runs on the
+ * device (two launches on `stream`, no host round trip), so a stream capture
+ * records it.  Errors: MSM_ERR_UNSUPPORTED when vocab == 0, MSM_ERR_INVALID_ARG
+ * for NULL or misaligned buffers, an invalid parent array, token ids or pos0;
+ * nothing is enqueued then.
+ */
+#define MSM_ACCEPT_RESULT_INTS 34
+msm_status msm_accept(msm_model* model, const float* logits, const int32_t* tokens, const int32_t* parent,
+                      int32_t pos0, void* const* k_cache, void* const* v_cache, int32_t* result, void* stream);
+
+/*
+ * One CUDA graph per decode step (alphasignal.ai, § "Draft and verify share one
+ * graph"; orcarouter.ai, closing figure): msm_graph_create captures the arming of
+ * the model's exchange buffers, the verify step's n_layers launches and, if
+ * accept_result is not NULL, msm_accept's launches, and instantiates the graph.
+ * Arguments are those of msm_verify_step and msm_accept; the tree, the tokens and
+ * pos0 are recorded in the graph, as are all buffer addresses, so a replay reads
+ * the buffers' current contents at those addresses.  msm_graph_launch replays it
+ * on `stream`; every replay computes what the captured calls compute.  The draft
+ * step is not part of the graph (not built).  The model must outlive its graphs;
+ * replays of one model must not overlap on the GPU.  msm_graph_destroy frees the
+ * graph (NULL is ignored).  Errors: those of the captured calls (nothing is
+ * recorded then), MSM_ERR_CUDA for a failed capture or instantiation.
+ */
+typedef struct msm_graph msm_graph;
+msm_status msm_graph_create(msm_model* model, const void* hidden_in, const int32_t* parent, const int32_t* tokens,
+                            int32_t pos0, void* const* k_cache, void* const* v_cache, float* logits_out,
+                            void* hidden_out, int32_t* accept_result, msm_graph** out);
+msm_status msm_graph_launch(msm_graph* graph, void* stream);
+void msm_graph_destroy(msm_graph* graph);
+
+/*
  * Draft step (DFlash-style draft proposing the 15 tree candidates).  Not built
  * in this version: always returns MSM_ERR_UNSUPPORTED.
  */

@@ -21,7 +21,7 @@ _BUILD = os.path.join(_HERE, "_build")
 _ROOT = os.path.dirname(_HERE)
 _INCLUDE = os.path.join(_ROOT, "include")
 LIB_PATH = os.path.join(_BUILD, "libmsm.so")
-_SOURCES = ["msm_kernel.cu", "msm_pack.cu", "msm_api.cu"]
+_SOURCES = ["msm_kernel.cu", "msm_pack.cu", "msm_api.cu", "msm_accept.cu"]
 _HEADERS = ["msm_device.cuh", "msm_internal.h"]
 NVCC_ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -34,6 +34,8 @@ MSM_FLAG_KV_PREFETCH = 0x4
 MSM_FLAG_PDL = 0x8
 MSM_FLAG_TEST_DROP_HANDOFF = 0x10000
 MSM_TIMING_EVENTS = 64
+# entries of msm_accept's result buffer (MSM_ACCEPT_RESULT_INTS)
+MSM_ACCEPT_RESULT_INTS = 34
 # self-timing event ids (see msm.h)
 EV = dict(start=0, pro_in=1, pro_done=2, attn_in=3, attn_done=4, merge_done=5, oproj_in=6, oproj_done=7,
           pool_in=8, pool_done=9, router_in=10, router_done=11, route_topk=12, route_done=13, gemm1_done=14,
@@ -50,7 +52,8 @@ T = 16
 
 EXPORTED = ["msm_model_create", "msm_model_destroy", "msm_verify_step", "msm_verify_step_host", "msm_sync",
             "msm_get_routing", "msm_get_tree", "msm_get_timing", "msm_get_stats", "msm_get_exchange",
-            "msm_draft_step", "msm_last_error", "msm_verify_step_noalloc"]
+            "msm_draft_step", "msm_last_error", "msm_verify_step_noalloc", "msm_accept", "msm_graph_create",
+            "msm_graph_launch", "msm_graph_destroy"]
 # capacity of the static scratch array behind msm_verify_step_noalloc (MSM_NOALLOC_SCRATCH_BYTES)
 MSM_NOALLOC_SCRATCH_BYTES = 10 << 20
 
@@ -156,6 +159,15 @@ def lib():
             L.msm_get_stats.restype = st
             L.msm_get_exchange.argtypes = [vp, ctypes.c_char_p, vp, ctypes.c_size_t]
             L.msm_get_exchange.restype = st
+            L.msm_accept.argtypes = [vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32), i32, _PP, _PP, vp, vp]
+            L.msm_accept.restype = st
+            L.msm_graph_create.argtypes = [vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32), i32, _PP, _PP, vp, vp,
+                                           vp, ctypes.POINTER(vp)]
+            L.msm_graph_create.restype = st
+            L.msm_graph_launch.argtypes = [vp, vp]
+            L.msm_graph_launch.restype = st
+            L.msm_graph_destroy.argtypes = [vp]
+            L.msm_graph_destroy.restype = None
             L.msm_draft_step.argtypes = [vp, vp, vp, vp, vp]
             L.msm_draft_step.restype = st
             L.msm_last_error.argtypes = []
@@ -252,6 +264,33 @@ def msm_get_exchange(model, name: str, host_ptr, nbytes) -> int:
     return lib().msm_get_exchange(model, name.encode(), ctypes.c_void_p(host_ptr), nbytes)
 
 
+def msm_accept(model, logits, tokens, parent, pos0, k_ptrs, v_ptrs, result, stream=0) -> int:
+    kp, ka = _ptr_array(k_ptrs)
+    vpp, va = _ptr_array(v_ptrs)
+    return lib().msm_accept(model, ctypes.c_void_p(logits), _i32_array(tokens), _i32_array(parent), int(pos0),
+                            kp, vpp, ctypes.c_void_p(result), ctypes.c_void_p(stream))
+
+
+def msm_graph_create(model, hidden_in, parent, tokens, pos0, k_ptrs, v_ptrs, logits_out, hidden_out,
+                     accept_result):
+    """Returns the graph handle; raises MsmError on failure."""
+    kp, ka = _ptr_array(k_ptrs)
+    vpp, va = _ptr_array(v_ptrs)
+    g = ctypes.c_void_p()
+    _check(lib().msm_graph_create(model, ctypes.c_void_p(hidden_in), _i32_array(parent), _i32_array(tokens),
+                                  int(pos0), kp, vpp, ctypes.c_void_p(logits_out), ctypes.c_void_p(hidden_out),
+                                  ctypes.c_void_p(accept_result), ctypes.byref(g)))
+    return g
+
+
+def msm_graph_launch(graph, stream=0) -> int:
+    return lib().msm_graph_launch(graph, ctypes.c_void_p(stream))
+
+
+def msm_graph_destroy(graph) -> None:
+    lib().msm_graph_destroy(graph)
+
+
 def msm_draft_step(model, draft_hidden_in=0, tokens_out=0, parent_out=0, stream=0) -> int:
     return lib().msm_draft_step(model, ctypes.c_void_p(draft_hidden_in), ctypes.c_void_p(tokens_out),
                                 ctypes.c_void_p(parent_out), ctypes.c_void_p(stream))
@@ -330,6 +369,22 @@ class Model:
                                     logits_host.ctypes.data if logits_host is not None else 0,
                                     hidden_out_host.ctypes.data if hidden_out_host is not None else 0, stream)
 
+    def accept(self, logits, tokens, parent, pos0, k_caches, v_caches, result, stream=0):
+        """msm_accept: result is a device int32 tensor of MSM_ACCEPT_RESULT_INTS entries."""
+        return _check(msm_accept(self.handle, logits.data_ptr(), tokens, parent, pos0,
+                                 [k.data_ptr() for k in k_caches], [v.data_ptr() for v in v_caches],
+                                 result.data_ptr(), stream))
+
+    def graph(self, hidden_in, parent, pos0, k_caches, v_caches, logits_out=None, hidden_out=None,
+              tokens=None, accept_result=None):
+        """msm_graph_create: a StepGraph replaying verify (+ accept when accept_result is given)."""
+        g = msm_graph_create(self.handle, hidden_in.data_ptr(), parent, tokens if tokens is not None else [0] * T,
+                             pos0, [k.data_ptr() for k in k_caches], [v.data_ptr() for v in v_caches],
+                             logits_out.data_ptr() if logits_out is not None else 0,
+                             hidden_out.data_ptr() if hidden_out is not None else 0,
+                             accept_result.data_ptr() if accept_result is not None else 0)
+        return StepGraph(g, self)
+
     def sync(self, stream=0) -> int:
         return msm_sync(self.handle, stream)
 
@@ -370,3 +425,24 @@ class Model:
         buf = np.empty(shape, dt)
         _check(msm_get_exchange(self.handle, name, buf.ctypes.data, buf.nbytes))
         return buf
+
+
+class StepGraph:
+    """An instantiated step graph (msm_graph); keeps its model alive."""
+
+    def __init__(self, handle, model):
+        self.handle, self.model = handle, model
+
+    def launch(self, stream=0):
+        return _check(msm_graph_launch(self.handle, stream))
+
+    def close(self):
+        if getattr(self, "handle", None):
+            msm_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,146 @@
+// msm_accept.cu — the accept step after a verify step: the target's greedy
+// choice at every tree node, the walk down the tree, and the move of the accepted
+// nodes' K/V rows to the front of the tree's rows.
+//
+// alphasignal.ai, "LMSYS Doubles Muse Spark Open Speed to 1,109 Tokens per
+// Second", § "Draft and verify share one graph": candidates the target agrees with
+// become output tokens, rejected branches are dropped; orcarouter.ai, "Muse Spark
+// Open: 1,109 tokens/s is a kernel-level change", closing figure (the repository
+// screenshot): greedy decoding at batch 1, accept inside the step's CUDA graph.
+//
+// Two launches, both free of host round trips (so a stream capture records them):
+//   1. accept_argmax_kernel: block b scans a contiguous slice of all 16 logit rows
+//      and leaves one 64-bit key per row, value-ordered bits above the complement
+//      of the index, so that the largest key is the largest logit with the
+//      smallest index (a NaN ranks above +inf, -0 equals +0);
+//   2. accept_walk_kernel: every block reduces the 16 x G keys, walks the tree
+//      (the same walk in every block), and copies its share of the K/V columns:
+//      one thread owns a 16-byte column of one (layer, K|V, head) and moves the
+//      accepted rows in path order.  The j-th accepted node has index >= j, so a
+//      row is read before any write of this column reaches it.
+#include "msm_internal.h"
+
+namespace msm {
+namespace {
+
+constexpr int kAcceptThreads = 256;
+constexpr int kRowsPerThread = 16;
+
+__device__ __forceinline__ uint64_t argmax_key(float x, uint32_t idx) {
+  uint32_t b = __float_as_uint(x);
+  if (x != x) b = 0x7FFFFFFFu;      // every NaN ranks above +inf
+  else if (x == 0.0f) b = 0u;       // -0 == +0
+  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((uint64_t)ord << 32) | (uint64_t)(0xFFFFFFFFu - idx);
+}
+
+__device__ __forceinline__ uint64_t max_u64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+
+__global__ void __launch_bounds__(kAcceptThreads) accept_argmax_kernel(const float* __restrict__ logits,
+                                                                        int vocab, uint64_t* __restrict__ part) {
+  __shared__ uint64_t red[kRowsPerThread][kAcceptThreads / 32];
+  const int G = gridDim.x, b = blockIdx.x;
+  const int n4 = vocab / 4;
+  const int per = (n4 + G - 1) / G;
+  const int c0 = min(n4, b * per), c1 = min(n4, c0 + per);
+  uint64_t best[kRowsPerThread];
+#pragma unroll
+  for (int r = 0; r < kRowsPerThread; ++r) best[r] = 0ull;  // below every element's key
+  for (int c = c0 + (int)threadIdx.x; c < c1; c += kAcceptThreads) {
+    float4 v[kRowsPerThread];
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r) v[r] = __ldcs(reinterpret_cast<const float4*>(logits + (size_t)r * vocab) + c);
+    const uint32_t i0 = (uint32_t)c * 4u;
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r) {
+      best[r] = max_u64(best[r], max_u64(max_u64(argmax_key(v[r].x, i0), argmax_key(v[r].y, i0 + 1)),
+                                         max_u64(argmax_key(v[r].z, i0 + 2), argmax_key(v[r].w, i0 + 3))));
+    }
+  }
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int r = 0; r < kRowsPerThread; ++r) {
+    uint64_t x = best[r];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) x = max_u64(x, __shfl_xor_sync(0xffffffffu, x, o));
+    if (lane == 0) red[r][wid] = x;
+  }
+  __syncthreads();
+  if (threadIdx.x < kRowsPerThread) {
+    uint64_t x = 0ull;
+#pragma unroll
+    for (int w = 0; w < kAcceptThreads / 32; ++w) x = max_u64(x, red[threadIdx.x][w]);
+    part[(size_t)threadIdx.x * G + b] = x;
+  }
+}
+
+__global__ void __launch_bounds__(kAcceptThreads) accept_walk_kernel(const AcceptParams p) {
+  __shared__ int32_t s_arg[kRowsPerThread];
+  __shared__ int32_t s_path[kRowsPerThread];
+  __shared__ int32_t s_n;
+  if (threadIdx.x < kRowsPerThread) {
+    const uint64_t* row = p.part + (size_t)threadIdx.x * p.parts;
+    uint64_t x = 0ull;
+    for (int i = 0; i < p.parts; ++i) x = max_u64(x, row[i]);
+    s_arg[threadIdx.x] = (int32_t)(0xFFFFFFFFu - (uint32_t)x);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // from the root, the first child (in tree order) whose draft token is the
+    // parent's greedy choice; stop at the first node without one
+    int cur = 0, n = 1;
+    s_path[0] = 0;
+    for (;;) {
+      int nxt = -1;
+      for (int c = cur + 1; c < kRowsPerThread; ++c)
+        if (p.parent[c] == cur && p.tokens[c] == s_arg[cur]) {
+          nxt = c;
+          break;
+        }
+      if (nxt < 0) break;
+      s_path[n++] = nxt;
+      cur = nxt;
+    }
+    s_n = n;
+    if (p.result != nullptr && blockIdx.x == 0) {
+      p.result[0] = n;
+      p.result[1] = s_arg[cur];
+      for (int j = 0; j < kRowsPerThread; ++j) {
+        p.result[2 + j] = j < n ? s_path[j] : -1;
+        p.result[2 + kRowsPerThread + j] = s_arg[j];
+      }
+    }
+  }
+  __syncthreads();
+  const int n = s_n;
+  if (n <= 1) return;
+  const int chunks = p.head_dim / 8;  // 16-byte chunks per row
+  const int per_layer = 2 * p.n_kv_heads * chunks;
+  const int cols = p.n_layers * per_layer;
+  for (int col = blockIdx.x * kAcceptThreads + threadIdx.x; col < cols; col += gridDim.x * kAcceptThreads) {
+    const int l = col / per_layer, rem = col - l * per_layer;
+    const int kv = rem / (p.n_kv_heads * chunks), rem2 = rem - kv * (p.n_kv_heads * chunks);
+    const int h = rem2 / chunks, ch = rem2 - h * chunks;
+    uint16_t* base = (kv ? p.vc[l] : p.kc[l]) + ((size_t)h * p.max_ctx + p.pos0) * p.head_dim + ch * 8;
+    for (int j = 1; j < n; ++j) {
+      const int src = s_path[j];
+      if (src == j) continue;
+      *reinterpret_cast<uint4*>(base + (size_t)j * p.head_dim) =
+          *reinterpret_cast<const uint4*>(base + (size_t)src * p.head_dim);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_accept_argmax(const float* logits, int vocab, uint64_t* part, int parts, cudaStream_t s) {
+  accept_argmax_kernel<<<parts, kAcceptThreads, 0, s>>>(logits, vocab, part);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_accept_walk(const AcceptParams& p, int blocks, cudaStream_t s) {
+  accept_walk_kernel<<<blocks, kAcceptThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace msm

@@ -90,6 +90,7 @@ struct msm_model {
   uint16_t* io_in = nullptr;      // device staging of msm_verify_step_host
   uint16_t* io_hidden = nullptr;
   float* io_logits = nullptr;
+  uint64_t* accept_part = nullptr;  // msm_accept: argmax partial keys [16][G]
 
   template <class Tp>
   cudaError_t alloc(Tp** p, uint64_t bytes) {
@@ -368,6 +369,7 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   CKM(m->alloc(&m->io_in, (uint64_t)T * dm.d * 2));
   CKM(m->alloc(&m->io_hidden, (uint64_t)T * dm.d * 2));
   if (dm.vocab > 0) CKM(m->alloc(&m->io_logits, (uint64_t)T * dm.vocab * 4));
+  if (dm.vocab > 0) CKM(m->alloc(&m->accept_part, (uint64_t)T * m->G * 8));
   CKM(cudaMemsetAsync(m->hist, 0, 2ull * c.n_layers * dm.e * 4, s));
   CKM(cudaMemsetAsync(m->status, 0, sizeof(DevStatus), s));
   CKM(cudaMemsetAsync(m->timing, 0, (uint64_t)c.n_layers * m->G * kTimingEvents * 8, s));
@@ -620,6 +622,115 @@ msm_status msm_get_exchange(msm_model* m, const char* name, void* host, size_t b
     return MSM_OK;
   }
   return fail(MSM_ERR_INVALID_ARG, std::string("unknown exchange buffer ") + name);
+}
+
+msm_status msm_accept(msm_model* m, const float* logits, const int32_t* tokens, const int32_t* parent,
+                      int32_t pos0, void* const* k_cache, void* const* v_cache, int32_t* result, void* stream) {
+  if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
+  const Dims& dm = m->dm;
+  if (dm.vocab <= 0) return fail(MSM_ERR_UNSUPPORTED, "accept needs the LM head (vocab > 0)");
+  if (!logits || !tokens || !result || !k_cache || !v_cache)
+    return fail(MSM_ERR_INVALID_ARG, "NULL logits, tokens, result or cache array");
+  if (!parent_valid(parent)) return fail(MSM_ERR_INVALID_ARG, "parent must satisfy parent[0] == -1, 0 <= parent[i] < i");
+  for (int i = 0; i < T; ++i)
+    if (tokens[i] < 0 || tokens[i] >= dm.vocab) return fail(MSM_ERR_INVALID_ARG, "token id out of [0, vocab)");
+  if (pos0 < 0 || (int64_t)pos0 + T > dm.max_ctx) return fail(MSM_ERR_INVALID_ARG, "pos0 out of range");
+  if ((reinterpret_cast<uintptr_t>(logits) & 15) || (reinterpret_cast<uintptr_t>(result) & 3))
+    return fail(MSM_ERR_INVALID_ARG, "logits must be 16-byte and result 4-byte aligned");
+  for (int l = 0; l < dm.n_layers; ++l) {
+    if (!k_cache[l] || !v_cache[l]) return fail(MSM_ERR_INVALID_ARG, "NULL KV cache pointer");
+    if ((reinterpret_cast<uintptr_t>(k_cache[l]) & 15) || (reinterpret_cast<uintptr_t>(v_cache[l]) & 15))
+      return fail(MSM_ERR_INVALID_ARG, "KV caches must be 16-byte aligned");
+  }
+  CK(cudaSetDevice(m->device));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CK(launch_accept_argmax(logits, dm.vocab, m->accept_part, m->G, s));
+  AcceptParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.part = m->accept_part;
+  p.parts = m->G;
+  std::memcpy(p.parent, parent, sizeof(p.parent));
+  std::memcpy(p.tokens, tokens, sizeof(p.tokens));
+  p.pos0 = pos0;
+  p.n_kv_heads = dm.hkv;
+  p.head_dim = dm.hd;
+  p.max_ctx = dm.max_ctx;
+  for (int l0 = 0; l0 < dm.n_layers; l0 += kAcceptLayers) {
+    p.n_layers = std::min(kAcceptLayers, dm.n_layers - l0);
+    for (int l = 0; l < p.n_layers; ++l) {
+      p.kc[l] = static_cast<uint16_t*>(k_cache[l0 + l]);
+      p.vc[l] = static_cast<uint16_t*>(v_cache[l0 + l]);
+    }
+    p.result = l0 == 0 ? result : nullptr;
+    const int cols = p.n_layers * 2 * dm.hkv * (dm.hd / 8);
+    const int blocks = std::max(1, std::min(m->G, (cols + 255) / 256));
+    CK(launch_accept_walk(p, blocks, s));
+  }
+  return MSM_OK;
+}
+
+struct msm_graph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int device = 0;
+};
+
+void msm_graph_destroy(msm_graph* g) {
+  if (!g) return;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  delete g;
+}
+
+msm_status msm_graph_create(msm_model* m, const void* hidden_in, const int32_t* parent, const int32_t* tokens,
+                            int32_t pos0, void* const* k_cache, void* const* v_cache, float* logits_out,
+                            void* hidden_out, int32_t* accept_result, msm_graph** out) {
+  if (!out) return fail(MSM_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
+  CK(cudaSetDevice(m->device));
+  cudaStream_t cs = nullptr;
+  CK(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+  cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return cuda_fail(e, "cudaStreamBeginCapture");
+  }
+  // the graph arms the exchange buffers itself, so a replay never depends on the
+  // state an earlier step (eager or replayed) left behind
+  msm_status st = rearm_all(m, cs);
+  if (st == MSM_OK) st = msm_verify_step(m, hidden_in, parent, pos0, k_cache, v_cache, logits_out, hidden_out, cs);
+  if (st == MSM_OK && accept_result)
+    st = msm_accept(m, logits_out, tokens, parent, pos0, k_cache, v_cache, accept_result, cs);
+  std::string msg = st == MSM_OK ? std::string() : std::string(msm_last_error());
+  cudaGraph_t graph = nullptr;
+  e = cudaStreamEndCapture(cs, &graph);
+  cudaStreamDestroy(cs);
+  if (st != MSM_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return fail(st, msg);
+  }
+  if (e != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    return cuda_fail(e, "cudaStreamEndCapture");
+  }
+  msm_graph* g = new msm_graph;
+  g->graph = graph;
+  g->device = m->device;
+  e = cudaGraphInstantiate(&g->exec, graph, 0);
+  if (e != cudaSuccess) {
+    msm_graph_destroy(g);
+    return cuda_fail(e, "cudaGraphInstantiate");
+  }
+  *out = g;
+  return MSM_OK;
+}
+
+msm_status msm_graph_launch(msm_graph* g, void* stream) {
+  if (!g) return fail(MSM_ERR_INVALID_ARG, "graph is NULL");
+  CK(cudaSetDevice(g->device));
+  CK(cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream)));
+  return MSM_OK;
 }
 
 msm_status msm_draft_step(msm_model* m, const void* draft_hidden_in, int32_t* tokens_out, int32_t* parent_out,

@@ -37,6 +37,9 @@ def test_null_arguments_are_rejected_without_a_device():
     assert lib.msm_get_stats(None, None) == msm.MSM_ERR_INVALID_ARG
     assert msm.msm_draft_step(None) == msm.MSM_ERR_UNSUPPORTED
     assert msm.msm_verify_step_noalloc(None, 0, list(range(-1, 15)), 0, [0], [0], 0, 0) == msm.MSM_ERR_INVALID_ARG
+    assert msm.msm_accept(None, 0, [0] * 16, list(range(-1, 15)), 0, [0], [0], 0) == msm.MSM_ERR_INVALID_ARG
+    assert msm.msm_graph_launch(None) == msm.MSM_ERR_INVALID_ARG
+    msm.msm_graph_destroy(None)
 
 
 def test_noalloc_scratch_capacity_matches_the_header():

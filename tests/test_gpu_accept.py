@@ -1,0 +1,227 @@
+"""GPU parity of the accept step (greedy walk + KV compaction) and of the step
+graph, through the C ABI, against the accept oracle."""
+import numpy as np
+import pytest
+
+import gpu_cases
+import synth
+from oracle import accept as acc
+
+T = 16
+pytestmark = pytest.mark.gpu
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _model(cfg_name):
+    import moe_decode_megakernel_warp_gb300 as msm
+    case = gpu_cases.make_case(cfg_name)
+    torch = _torch()
+    dev = torch.device("cuda", 0)
+    layers_t = [synth.to_torch(w, dev) for w in case.layers]
+    final_t = synth.to_torch(case.final, dev)
+    return case, msm.Model(case.cfg, layers_t, final_t, device=0, flags=msm.MSM_FLAG_PDL)
+
+
+def planted(rng, vocab, parent):
+    """Logits, tokens: random rows with a planted maximum per row (sometimes two equal
+    maxima, once a NaN), tokens that match the parent's maximum about half the time
+    (duplicate siblings included)."""
+    lg = rng.standard_normal((T, vocab)).astype(np.float32)
+    g = rng.integers(0, vocab, T)
+    for i in range(T):
+        lg[i, g[i]] = 8.0
+        if rng.random() < 0.25:  # an equal maximum elsewhere: the smaller index wins
+            lg[i, rng.integers(0, vocab)] = 8.0
+    if rng.random() < 0.3:
+        lg[rng.integers(0, T), rng.integers(0, vocab)] = np.nan
+    want = acc.target_argmax(lg)
+    tokens = [int(rng.integers(0, vocab))]
+    for c in range(1, T):
+        tokens.append(int(want[parent[c]]) if rng.random() < 0.5 else int(rng.integers(0, vocab)))
+    return lg, tokens
+
+
+def check_result(res, path, bonus, g):
+    assert res[0] == len(path)
+    assert res[1] == bonus
+    assert list(res[2:2 + T]) == path + [-1] * (T - len(path))
+    assert list(res[2 + T:2 + 2 * T]) == [int(x) for x in g]
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_accept_matches_oracle_on_planted_logits(seed):
+    torch = _torch()
+    import moe_decode_megakernel_warp_gb300 as msm
+    case, m = _model("cfg1_stack")
+    try:
+        cfg = case.cfg
+        rng = np.random.default_rng(7000 + seed)
+        parent = [-1] + [int(rng.integers(0, i)) for i in range(1, T)]
+        if seed == 0:
+            parent = [-1] + list(range(T - 1))  # a chain
+        lg, tokens = planted(rng, cfg.vocab, parent)
+        if seed == 0:  # accept all 16
+            want0 = acc.target_argmax(lg)
+            tokens = [0] + [int(want0[i - 1]) for i in range(1, T)]
+        pos0 = [cfg.pos0, 0, cfg.max_ctx - T][seed % 3]
+        ks = [rng.integers(0, 2**16, (cfg.hkv, cfg.max_ctx, cfg.hd)).astype(np.uint16) for _ in range(cfg.n_layers)]
+        vs = [rng.integers(0, 2**16, (cfg.hkv, cfg.max_ctx, cfg.hd)).astype(np.uint16) for _ in range(cfg.n_layers)]
+        dev = torch.device("cuda", 0)
+        kc = [torch.from_numpy(k.view(np.int16)).to(dev) for k in ks]
+        vc = [torch.from_numpy(v.view(np.int16)).to(dev) for v in vs]
+        lg_d = torch.from_numpy(lg).to(dev)
+        res = torch.full((msm.MSM_ACCEPT_RESULT_INTS,), -7, dtype=torch.int32, device=dev)
+        m.accept(lg_d, tokens, parent, pos0, kc, vc, res)
+        assert m.sync() == 0
+        path, bonus, g = acc.greedy_accept(lg, tokens, parent)
+        check_result(res.cpu().numpy(), path, bonus, g)
+        wk, wv = acc.compact_kv(ks, vs, pos0, path)
+        for l in range(cfg.n_layers):
+            assert np.array_equal(kc[l].cpu().numpy().view(np.uint16), wk[l])
+            assert np.array_equal(vc[l].cpu().numpy().view(np.uint16), wv[l])
+    finally:
+        m.close()
+
+
+def test_accept_after_a_verify_step():
+    """Verify step on cfg1_stack, then accept with tokens built from the greedy choices
+    (a planted accepted path along the tree); caches compared with the oracle's
+    compaction of the caches the verify step left."""
+    torch = _torch()
+    import moe_decode_megakernel_warp_gb300 as msm
+    case, m = _model("cfg1_stack")
+    try:
+        cfg = case.cfg
+        dev = torch.device("cuda", 0)
+        kc = [torch.from_numpy(k.view(np.int16)).to(dev) for k, _ in case.kv]
+        vc = [torch.from_numpy(v.view(np.int16)).to(dev) for _, v in case.kv]
+        hid = torch.from_numpy(case.hidden.view(np.int16)).to(dev)
+        lg_d = torch.empty((T, cfg.vocab), dtype=torch.float32, device=dev)
+        m.verify_step(hid, case.parent, case.pos0, kc, vc, logits_out=lg_d)
+        assert m.sync() == 0
+        lg = lg_d.cpu().numpy()
+        before_k = [k.cpu().numpy().view(np.uint16).copy() for k in kc]
+        before_v = [v.cpu().numpy().view(np.uint16).copy() for v in vc]
+        g = acc.target_argmax(lg)
+        parent = [int(x) for x in case.parent]
+        # follow the first child at every level and give it its parent's choice
+        tokens = [0] + [(int(g[parent[c]]) + 1) % cfg.vocab for c in range(1, T)]
+        cur = 0
+        for c in range(1, T):
+            if parent[c] == cur:
+                tokens[c] = int(g[cur])
+                cur = c
+        res = torch.zeros((msm.MSM_ACCEPT_RESULT_INTS,), dtype=torch.int32, device=dev)
+        m.accept(lg_d, tokens, parent, case.pos0, kc, vc, res)
+        assert m.sync() == 0
+        path, bonus, g2 = acc.greedy_accept(lg, tokens, parent)
+        assert len(path) >= 2
+        check_result(res.cpu().numpy(), path, bonus, g2)
+        wk, wv = acc.compact_kv(before_k, before_v, case.pos0, path)
+        for l in range(cfg.n_layers):
+            assert np.array_equal(kc[l].cpu().numpy().view(np.uint16), wk[l])
+            assert np.array_equal(vc[l].cpu().numpy().view(np.uint16), wv[l])
+    finally:
+        m.close()
+
+
+def test_step_graph_replays_verify_and_accept():
+    """msm_graph_create / msm_graph_launch: every replay gives the eager results bit for
+    bit (logits, accept result, compacted caches), with the caches restored between runs."""
+    torch = _torch()
+    import moe_decode_megakernel_warp_gb300 as msm
+    case, m = _model("cfg1_stack")
+    try:
+        cfg = case.cfg
+        dev = torch.device("cuda", 0)
+        kc = [torch.from_numpy(k.view(np.int16)).to(dev) for k, _ in case.kv]
+        vc = [torch.from_numpy(v.view(np.int16)).to(dev) for _, v in case.kv]
+        k0 = [k.clone() for k in kc]
+        v0 = [v.clone() for v in vc]
+        hid = torch.from_numpy(case.hidden.view(np.int16)).to(dev)
+        lg_d = torch.empty((T, cfg.vocab), dtype=torch.float32, device=dev)
+        res = torch.zeros((msm.MSM_ACCEPT_RESULT_INTS,), dtype=torch.int32, device=dev)
+        # tokens: the eager step's greedy choices along the first-child chain
+        m.verify_step(hid, case.parent, case.pos0, kc, vc, logits_out=lg_d)
+        assert m.sync() == 0
+        g = acc.target_argmax(lg_d.cpu().numpy())
+        parent = [int(x) for x in case.parent]
+        tokens = [0] * T
+        cur = 0
+        for c in range(1, T):
+            tokens[c] = int(g[cur]) if parent[c] == cur else (int(g[parent[c]]) + 3) % cfg.vocab
+            if parent[c] == cur:
+                cur = c
+
+        def restore():
+            for a, b in zip(kc + vc, k0 + v0):
+                a.copy_(b)
+
+        restore()
+        m.verify_step(hid, parent, case.pos0, kc, vc, logits_out=lg_d)
+        m.accept(lg_d, tokens, parent, case.pos0, kc, vc, res)
+        assert m.sync() == 0
+        want = (lg_d.cpu().numpy().copy(), res.cpu().numpy().copy(),
+                [t.cpu().numpy().copy() for t in kc + vc])
+        assert want[1][0] >= 2
+        graph = m.graph(hid, parent, case.pos0, kc, vc, logits_out=lg_d, tokens=tokens, accept_result=res)
+        try:
+            for _ in range(2):
+                restore()
+                lg_d.fill_(0.0)
+                res.fill_(-1)
+                torch.cuda.synchronize()
+                graph.launch()
+                assert m.sync() == 0
+                assert np.array_equal(lg_d.cpu().numpy(), want[0])
+                assert np.array_equal(res.cpu().numpy(), want[1])
+                for t, w in zip(kc + vc, want[2]):
+                    assert np.array_equal(t.cpu().numpy(), w)
+        finally:
+            graph.close()
+    finally:
+        m.close()
+
+
+def test_accept_full_size_sampled():
+    """The 62-layer, 131,072-token vocabulary shapes: result against the oracle on the
+    whole logits, caches checked on the tree rows of every layer."""
+    torch = _torch()
+    import moe_decode_megakernel_warp_gb300 as msm
+    cfg = synth.CONFIGS["cfg4"]
+    dev = torch.device("cuda", 0)
+    # accept touches only the dims and the caches: a model of the full shape is needed
+    # for the C ABI; build it from the bench's device-side weights
+    import bench
+    s = synth.parity_seeds("cfg4")
+    m = bench.build_model(cfg, s["seed"], s["bias_seeds"], dev, 0, msm.MSM_FLAG_PDL)
+    try:
+        rng = np.random.default_rng(42)
+        parent = [-1] + [int(rng.integers(0, i)) for i in range(1, T)]
+        lg, tokens = planted(rng, cfg.vocab, parent)
+        pos0 = cfg.pos0
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(5)
+        kc = [torch.randint(-2**15, 2**15, (cfg.hkv, cfg.max_ctx, cfg.hd), dtype=torch.int16, device=dev, generator=gen)
+              for _ in range(cfg.n_layers)]
+        vc = [torch.randint(-2**15, 2**15, (cfg.hkv, cfg.max_ctx, cfg.hd), dtype=torch.int16, device=dev, generator=gen)
+              for _ in range(cfg.n_layers)]
+        rows = slice(pos0, pos0 + T)
+        bk = [k[:, rows].cpu().numpy().view(np.uint16).copy() for k in kc]
+        bv = [v[:, rows].cpu().numpy().view(np.uint16).copy() for v in vc]
+        lg_d = torch.from_numpy(lg).to(dev)
+        res = torch.zeros((msm.MSM_ACCEPT_RESULT_INTS,), dtype=torch.int32, device=dev)
+        m.accept(lg_d, tokens, parent, pos0, kc, vc, res)
+        assert m.sync() == 0
+        path, bonus, g = acc.greedy_accept(lg, tokens, parent)
+        check_result(res.cpu().numpy(), path, bonus, g)
+        wk, wv = acc.compact_kv(bk, bv, 0, path)  # the slices start at the tree's first row
+        for l in range(cfg.n_layers):
+            assert np.array_equal(kc[l][:, rows].cpu().numpy().view(np.uint16), wk[l])
+            assert np.array_equal(vc[l][:, rows].cpu().numpy().view(np.uint16), wv[l])
+    finally:
+        m.close()
