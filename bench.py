@@ -295,6 +295,84 @@ def build_model(cfg, seed, bias, dev, local, flags, l2_runahead_kb=0):
     return model
 
 
+ACCEPT_DEPTH = 6  # accepted tree nodes below the root in the accept timing (the pages report 6.6 of 16)
+
+
+def accept_tokens(g, parent, depth):
+    """Draft tokens that make the greedy walk follow the first-child chain for `depth`
+    nodes: the chain's nodes carry their parent's choice g, every other node a token
+    the walk rejects."""
+    tokens = [0] * T
+    cur, taken = 0, 0
+    for c in range(1, T):
+        if parent[c] == cur and taken < depth:
+            tokens[c] = int(g[cur])
+            cur, taken = c, taken + 1
+        else:
+            tokens[c] = (int(g[parent[c]]) + 1) % (1 << 30)
+    return tokens, taken
+
+
+def measure_accept(model, cfg, hidden, parent, kc, vc, logits, stream, steps):
+    """msm_accept alone (its two launches) and the step graph (verify + accept)
+    against the same calls issued one by one, device time from CUDA events."""
+    import torch
+    import moe_decode_megakernel_warp_gb300 as msm
+    dev = logits.device
+    sptr = stream.cuda_stream
+    g = torch.argmax(logits, dim=1).cpu().numpy()  # the target's choices of the last step
+    tokens, depth = accept_tokens(g, [int(x) for x in parent], ACCEPT_DEPTH)
+    tokens = [t % cfg.vocab for t in tokens]
+    res = torch.zeros((msm.MSM_ACCEPT_RESULT_INTS,), dtype=torch.int32, device=dev)
+
+    def timed(fn, n, busy=None):
+        # `busy` (a verify step) is queued first, so that the host has queued the timed
+        # calls before the device reaches them: the events then see device time only
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if busy is not None:
+            busy()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    acc_ms = timed(lambda: model.accept(logits, tokens, parent, cfg.pos0, kc, vc, res, stream=sptr), 50,
+                   busy=lambda: model.verify_step(hidden, parent, cfg.pos0, kc, vc, logits_out=logits, stream=sptr))
+    if model.sync(sptr) != 0:
+        raise SystemExit("accept failed: %s" % msm.msm_last_error())
+    a = int(res[0].item())
+
+    def eager():
+        model.verify_step(hidden, parent, cfg.pos0, kc, vc, logits_out=logits, stream=sptr)
+        model.accept(logits, tokens, parent, cfg.pos0, kc, vc, res, stream=sptr)
+
+    eager_ms = timed(eager, steps)
+    graph = model.graph(hidden, parent, cfg.pos0, kc, vc, logits_out=logits, tokens=tokens, accept_result=res)
+    try:
+        graph_ms = timed(lambda: graph.launch(sptr), steps)
+    finally:
+        graph.close()
+    if model.sync(sptr) != 0:
+        raise SystemExit("step graph failed: %s" % msm.msm_last_error())
+    # algorithmic bytes: the logits once, the moved K/V rows read and written
+    logit_bytes = T * cfg.vocab * 4
+    move_bytes = 2 * (a - 1) * cfg.n_layers * 2 * cfg.hkv * cfg.hd * 2
+    peak, peak_kind = measured_peaks()
+    gbs = (logit_bytes + move_bytes) / (acc_ms * 1e-3) / 1e9
+    return {"us": acc_ms * 1e3, "accepted": a, "planted_depth": depth, "launches": 1 + (cfg.n_layers + 63) // 64,
+            "algorithmic_bytes": logit_bytes + move_bytes, "achieved_gbs": gbs, "frac": gbs / peak,
+            "peak_kind": peak_kind,
+            "step_graph_ms": graph_ms, "eager_verify_accept_ms": eager_ms,
+            "note": "msm_accept on the last step's logits (argmax over the vocabulary, tree walk, K/V "
+                    "compaction of the accepted rows); step graph = exchange arming + verify + accept "
+                    "replayed as one CUDA graph"}
+
+
 def run_ours(args):
     import torch
     import moe_decode_megakernel_warp_gb300 as msm
@@ -378,6 +456,7 @@ def run_ours(args):
         if step_host() != 0:
             raise SystemExit("host-buffer step failed: %s" % msm.msm_last_error())
     e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.steps, world, dev)
+    accept = measure_accept(model, cfg, hidden, parent, kc, vc, logits, stream, args.steps) if cfg.vocab else None
     model.close()
 
     # ---- per-layer times from the kernel's own %globaltimer stamps (separate, untimed model)
@@ -427,6 +506,8 @@ def run_ours(args):
                     "d2h_bytes_per_step": T * cfg.vocab * 4 if cfg.vocab else T * cfg.d * 2},
             "clocks": clk, "setup_seconds": setup_s,
         }
+        if accept is not None:
+            line["accept"] = accept
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line))

@@ -12,12 +12,13 @@
 //   1. accept_argmax_kernel: block b scans a contiguous slice of all 16 logit rows
 //      and leaves one 64-bit key per row, value-ordered bits above the complement
 //      of the index, so that the largest key is the largest logit with the
-//      smallest index (a NaN ranks above +inf, -0 equals +0);
-//   2. accept_walk_kernel: every block reduces the 16 x G keys, walks the tree
-//      (the same walk in every block), and copies its share of the K/V columns:
-//      one thread owns a 16-byte column of one (layer, K|V, head) and moves the
-//      accepted rows in path order.  The j-th accepted node has index >= j, so a
-//      row is read before any write of this column reaches it.
+//      smallest index (a NaN ranks above +inf, -0 equals +0); the last block to
+//      finish (a ticket counter after a gpu-scope fence) reduces the 16 x G keys
+//      to the 16 choices and re-zeroes the counter;
+//   2. accept_walk_kernel: every block walks the tree (the same walk in every
+//      block) and copies its share of the K/V columns: one thread owns a 16-byte
+//      column of one (layer, K|V, head), loads every moved row of it, then stores
+//      them, so row pos0 + j receives the old row pos0 + path[j] whatever the path.
 #include "msm_internal.h"
 
 namespace msm {
@@ -37,8 +38,10 @@ __device__ __forceinline__ uint64_t argmax_key(float x, uint32_t idx) {
 __device__ __forceinline__ uint64_t max_u64(uint64_t a, uint64_t b) { return a > b ? a : b; }
 
 __global__ void __launch_bounds__(kAcceptThreads) accept_argmax_kernel(const float* __restrict__ logits,
-                                                                        int vocab, uint64_t* __restrict__ part) {
+                                                                        int vocab, uint64_t* part,
+                                                                        uint32_t* ticket, int32_t* choice) {
   __shared__ uint64_t red[kRowsPerThread][kAcceptThreads / 32];
+  __shared__ bool last;
   const int G = gridDim.x, b = blockIdx.x;
   const int n4 = vocab / 4;
   const int per = (n4 + G - 1) / G;
@@ -72,18 +75,36 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_argmax_kernel(const flo
     for (int w = 0; w < kAcceptThreads / 32; ++w) x = max_u64(x, red[threadIdx.x][w]);
     part[(size_t)threadIdx.x * G + b] = x;
   }
+  // the last block reduces every block's keys
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(ticket, 1u) == (uint32_t)G - 1u;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const int r = threadIdx.x >> 4, sub = threadIdx.x & 15;  // 16 threads per row
+  uint64_t x = 0ull;
+  for (int i0 = 0; i0 < G; i0 += 16 * 8) {  // eight loads in flight per thread
+    uint64_t y[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = i0 + q * 16 + sub;
+      y[q] = i < G ? __ldcg(part + (size_t)r * G + i) : 0ull;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) x = max_u64(x, y[q]);
+  }
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) x = max_u64(x, __shfl_xor_sync(0xffffffffu, x, o));
+  if (sub == 0) choice[r] = (int32_t)(0xFFFFFFFFu - (uint32_t)x);
+  if (threadIdx.x == 0) *ticket = 0u;
 }
 
 __global__ void __launch_bounds__(kAcceptThreads) accept_walk_kernel(const AcceptParams p) {
   __shared__ int32_t s_arg[kRowsPerThread];
   __shared__ int32_t s_path[kRowsPerThread];
   __shared__ int32_t s_n;
-  if (threadIdx.x < kRowsPerThread) {
-    const uint64_t* row = p.part + (size_t)threadIdx.x * p.parts;
-    uint64_t x = 0ull;
-    for (int i = 0; i < p.parts; ++i) x = max_u64(x, row[i]);
-    s_arg[threadIdx.x] = (int32_t)(0xFFFFFFFFu - (uint32_t)x);
-  }
+  if (threadIdx.x < kRowsPerThread) s_arg[threadIdx.x] = p.choice[threadIdx.x];
   __syncthreads();
   if (threadIdx.x == 0) {
     // from the root, the first child (in tree order) whose draft token is the
@@ -122,19 +143,21 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_walk_kernel(const Accep
     const int kv = rem / (p.n_kv_heads * chunks), rem2 = rem - kv * (p.n_kv_heads * chunks);
     const int h = rem2 / chunks, ch = rem2 - h * chunks;
     uint16_t* base = (kv ? p.vc[l] : p.kc[l]) + ((size_t)h * p.max_ctx + p.pos0) * p.head_dim + ch * 8;
-    for (int j = 1; j < n; ++j) {
-      const int src = s_path[j];
-      if (src == j) continue;
-      *reinterpret_cast<uint4*>(base + (size_t)j * p.head_dim) =
-          *reinterpret_cast<const uint4*>(base + (size_t)src * p.head_dim);
-    }
+    uint4 v[kRowsPerThread - 1];
+#pragma unroll
+    for (int j = 1; j < kRowsPerThread; ++j)
+      if (j < n && s_path[j] != j) v[j - 1] = *reinterpret_cast<const uint4*>(base + (size_t)s_path[j] * p.head_dim);
+#pragma unroll
+    for (int j = 1; j < kRowsPerThread; ++j)
+      if (j < n && s_path[j] != j) *reinterpret_cast<uint4*>(base + (size_t)j * p.head_dim) = v[j - 1];
   }
 }
 
 }  // namespace
 
-cudaError_t launch_accept_argmax(const float* logits, int vocab, uint64_t* part, int parts, cudaStream_t s) {
-  accept_argmax_kernel<<<parts, kAcceptThreads, 0, s>>>(logits, vocab, part);
+cudaError_t launch_accept_argmax(const float* logits, int vocab, uint64_t* part, int parts, uint32_t* ticket,
+                                 int32_t* choice, cudaStream_t s) {
+  accept_argmax_kernel<<<parts, kAcceptThreads, 0, s>>>(logits, vocab, part, ticket, choice);
   return cudaGetLastError();
 }
 

@@ -90,7 +90,9 @@ struct msm_model {
   uint16_t* io_in = nullptr;      // device staging of msm_verify_step_host
   uint16_t* io_hidden = nullptr;
   float* io_logits = nullptr;
-  uint64_t* accept_part = nullptr;  // msm_accept: argmax partial keys [16][G]
+  uint64_t* accept_part = nullptr;  // msm_accept: argmax partial keys [16][G], then
+  int32_t* accept_choice = nullptr; // the 16 greedy choices [16] and
+  uint32_t* accept_ticket = nullptr;  // the last-block ticket (zero between calls)
 
   template <class Tp>
   cudaError_t alloc(Tp** p, uint64_t bytes) {
@@ -369,7 +371,12 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   CKM(m->alloc(&m->io_in, (uint64_t)T * dm.d * 2));
   CKM(m->alloc(&m->io_hidden, (uint64_t)T * dm.d * 2));
   if (dm.vocab > 0) CKM(m->alloc(&m->io_logits, (uint64_t)T * dm.vocab * 4));
-  if (dm.vocab > 0) CKM(m->alloc(&m->accept_part, (uint64_t)T * m->G * 8));
+  if (dm.vocab > 0) {
+    CKM(m->alloc(&m->accept_part, (uint64_t)T * m->G * 8 + T * 4 + 16));
+    m->accept_choice = reinterpret_cast<int32_t*>(m->accept_part + (size_t)T * m->G);
+    m->accept_ticket = reinterpret_cast<uint32_t*>(m->accept_choice + T);
+    CKM(cudaMemsetAsync(m->accept_ticket, 0, 4, s));
+  }
   CKM(cudaMemsetAsync(m->hist, 0, 2ull * c.n_layers * dm.e * 4, s));
   CKM(cudaMemsetAsync(m->status, 0, sizeof(DevStatus), s));
   CKM(cudaMemsetAsync(m->timing, 0, (uint64_t)c.n_layers * m->G * kTimingEvents * 8, s));
@@ -644,11 +651,10 @@ msm_status msm_accept(msm_model* m, const float* logits, const int32_t* tokens, 
   }
   CK(cudaSetDevice(m->device));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  CK(launch_accept_argmax(logits, dm.vocab, m->accept_part, m->G, s));
+  CK(launch_accept_argmax(logits, dm.vocab, m->accept_part, m->G, m->accept_ticket, m->accept_choice, s));
   AcceptParams p;
   std::memset(&p, 0, sizeof(p));
-  p.part = m->accept_part;
-  p.parts = m->G;
+  p.choice = m->accept_choice;
   std::memcpy(p.parent, parent, sizeof(p.parent));
   std::memcpy(p.tokens, tokens, sizeof(p.tokens));
   p.pos0 = pos0;
@@ -663,7 +669,7 @@ msm_status msm_accept(msm_model* m, const float* logits, const int32_t* tokens, 
     }
     p.result = l0 == 0 ? result : nullptr;
     const int cols = p.n_layers * 2 * dm.hkv * (dm.hd / 8);
-    const int blocks = std::max(1, std::min(m->G, (cols + 255) / 256));
+    const int blocks = std::max(1, std::min(m->G, (cols + 255) / 256));  // 256 threads per block
     CK(launch_accept_walk(p, blocks, s));
   }
   return MSM_OK;

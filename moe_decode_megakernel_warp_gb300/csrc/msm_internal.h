@@ -170,14 +170,13 @@ __host__ __device__ inline uint64_t exp_unit_bytes(int K) { return (uint64_t)(K 
 // kernel entry points (defined in msm_kernel.cu / msm_pack.cu)
 const void* layer_kernel(bool timing);
 
-// accept step (msm_accept.cu): argmax partials [16][parts] of the 16 logit rows,
-// then the walk + K/V compaction, up to kAcceptLayers layers per launch (the
+// accept step (msm_accept.cu): argmax partials [16][parts] of the 16 logit rows
+// reduced by the last block to the 16 choices, then the walk + K/V compaction, up to kAcceptLayers layers per launch (the
 // per-layer cache pointers travel in the kernel parameters, so a stream capture
 // needs no host-to-device copy)
 constexpr int kAcceptLayers = 64;
 struct AcceptParams {
-  const uint64_t* part;
-  int32_t parts;
+  const int32_t* choice;  // [16] greedy choice per tree node (launch 1's output)
   int32_t parent[16];
   int32_t tokens[16];
   int32_t pos0, n_kv_heads, head_dim, max_ctx, n_layers;
@@ -185,7 +184,8 @@ struct AcceptParams {
   uint16_t* kc[kAcceptLayers];
   uint16_t* vc[kAcceptLayers];
 };
-cudaError_t launch_accept_argmax(const float* logits, int vocab, uint64_t* part, int parts, cudaStream_t s);
+cudaError_t launch_accept_argmax(const float* logits, int vocab, uint64_t* part, int parts, uint32_t* ticket,
+                                 int32_t* choice, cudaStream_t s);
 cudaError_t launch_accept_walk(const AcceptParams& p, int blocks, cudaStream_t s);
 
 }  // namespace msm
