@@ -352,7 +352,13 @@ def measure_accept(model, cfg, hidden, parent, kc, vc, logits, stream, steps):
         model.accept(logits, tokens, parent, cfg.pos0, kc, vc, res, stream=sptr)
 
     eager_ms = timed(eager, steps)
-    graph = model.graph(hidden, parent, cfg.pos0, kc, vc, logits_out=logits, tokens=tokens, accept_result=res)
+    # the graph that serves every step: tree, tokens and pos0 read from a device state
+    state_h = np.zeros(msm.MSM_STEP_STATE_INTS, np.int32)
+    state_h[0] = cfg.pos0
+    state_h[1:1 + T] = parent
+    state_h[1 + T:1 + 2 * T] = tokens
+    state = torch.from_numpy(state_h).to(dev)
+    graph = model.graph_dev(hidden, state, kc, vc, logits_out=logits, accept_result=res)
     try:
         graph_ms = timed(lambda: graph.launch(sptr), steps)
     finally:
@@ -370,7 +376,7 @@ def measure_accept(model, cfg, hidden, parent, kc, vc, logits, stream, steps):
             "step_graph_ms": graph_ms, "eager_verify_accept_ms": eager_ms,
             "note": "msm_accept on the last step's logits (argmax over the vocabulary, tree walk, K/V "
                     "compaction of the accepted rows); step graph = exchange arming + verify + accept "
-                    "replayed as one CUDA graph"}
+                    "replayed as one CUDA graph that reads the tree, tokens and pos0 from a device state"}
 
 
 def run_ours(args):

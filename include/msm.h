@@ -329,12 +329,43 @@ msm_status msm_accept(msm_model* model, const float* logits, const int32_t* toke
  * pos0 are recorded in the graph, as are all buffer addresses, so a replay reads
  * the buffers' current contents at those addresses.  msm_graph_launch replays it
  * on `stream`; every replay computes what the captured calls compute.  The draft
- * step is not part of the graph (not built).  The model must outlive its graphs;
+ * step is not part of the graph (not built).  (msm_graph_create_dev below records a
+ * device-resident state instead of the tree, tokens and pos0.)  The model must outlive its graphs;
  * replays of one model must not overlap on the GPU.  msm_graph_destroy frees the
  * graph (NULL is ignored).  Errors: those of the captured calls (nothing is
  * recorded then), MSM_ERR_CUDA for a failed capture or instantiation.
  */
 typedef struct msm_graph msm_graph;
+
+/*
+ * Device-resident step inputs, so that one graph can serve every decode step
+ * (the pages' plugin replays one graph per step; orcarouter.ai, closing figure):
+ * a device int32 [MSM_STEP_STATE_INTS] array
+ *   [0] pos0, [1 + i] parent[i], [17 + i] the draft token of tree node i, [33] unused
+ * read by the kernels when they run, not when the call is made.  The caller
+ * writes it (for instance with cudaMemcpyAsync on the same stream) before each
+ * step.  The kernels check it (parent[0] == -1, 0 <= parent[i] < i, token ids in
+ * [0, vocab), 0 <= pos0 <= max_ctx - 16); an invalid state makes every launch of
+ * the step give up at entry without touching the caches or outputs, and the next
+ * msm_sync() returns MSM_ERR_INVALID_ARG (msm_accept_dev then also writes a = 0
+ * and -1 elsewhere in `result`).
+ *   msm_verify_step_dev  = msm_verify_step with the tree and pos0 from `state`
+ *   msm_accept_dev       = msm_accept with tree, tokens and pos0 from `state`
+ *   msm_graph_create_dev = msm_graph_create capturing those two: a replay reads the
+ *                          state's current contents, so one graph serves any tree
+ *                          and position
+ * Host errors as for the host-parameter calls, plus MSM_ERR_INVALID_ARG for a NULL
+ * or misaligned state.
+ */
+#define MSM_STEP_STATE_INTS 34
+msm_status msm_verify_step_dev(msm_model* model, const void* hidden_in, const int32_t* state, void* const* k_cache,
+                               void* const* v_cache, float* logits_out, void* hidden_out, void* stream);
+msm_status msm_accept_dev(msm_model* model, const float* logits, const int32_t* state, void* const* k_cache,
+                          void* const* v_cache, int32_t* result, void* stream);
+msm_status msm_graph_create_dev(msm_model* model, const void* hidden_in, const int32_t* state, void* const* k_cache,
+                                void* const* v_cache, float* logits_out, void* hidden_out, int32_t* accept_result,
+                                msm_graph** out);
+
 msm_status msm_graph_create(msm_model* model, const void* hidden_in, const int32_t* parent, const int32_t* tokens,
                             int32_t pos0, void* const* k_cache, void* const* v_cache, float* logits_out,
                             void* hidden_out, int32_t* accept_result, msm_graph** out);

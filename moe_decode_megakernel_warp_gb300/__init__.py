@@ -36,6 +36,8 @@ MSM_FLAG_TEST_DROP_HANDOFF = 0x10000
 MSM_TIMING_EVENTS = 64
 # entries of msm_accept's result buffer (MSM_ACCEPT_RESULT_INTS)
 MSM_ACCEPT_RESULT_INTS = 34
+# entries of the device-resident step state (MSM_STEP_STATE_INTS): pos0, parent[16], tokens[16], spare
+MSM_STEP_STATE_INTS = 34
 # self-timing event ids (see msm.h)
 EV = dict(start=0, pro_in=1, pro_done=2, attn_in=3, attn_done=4, merge_done=5, oproj_in=6, oproj_done=7,
           pool_in=8, pool_done=9, router_in=10, router_done=11, route_topk=12, route_done=13, gemm1_done=14,
@@ -53,7 +55,8 @@ T = 16
 EXPORTED = ["msm_model_create", "msm_model_destroy", "msm_verify_step", "msm_verify_step_host", "msm_sync",
             "msm_get_routing", "msm_get_tree", "msm_get_timing", "msm_get_stats", "msm_get_exchange",
             "msm_draft_step", "msm_last_error", "msm_verify_step_noalloc", "msm_accept", "msm_graph_create",
-            "msm_graph_launch", "msm_graph_destroy"]
+            "msm_graph_launch", "msm_graph_destroy", "msm_verify_step_dev", "msm_accept_dev",
+            "msm_graph_create_dev"]
 # capacity of the static scratch array behind msm_verify_step_noalloc (MSM_NOALLOC_SCRATCH_BYTES)
 MSM_NOALLOC_SCRATCH_BYTES = 10 << 20
 
@@ -164,6 +167,12 @@ def lib():
             L.msm_graph_create.argtypes = [vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32), i32, _PP, _PP, vp, vp,
                                            vp, ctypes.POINTER(vp)]
             L.msm_graph_create.restype = st
+            L.msm_verify_step_dev.argtypes = [vp, vp, vp, _PP, _PP, vp, vp, vp]
+            L.msm_verify_step_dev.restype = st
+            L.msm_accept_dev.argtypes = [vp, vp, vp, _PP, _PP, vp, vp]
+            L.msm_accept_dev.restype = st
+            L.msm_graph_create_dev.argtypes = [vp, vp, vp, _PP, _PP, vp, vp, vp, ctypes.POINTER(vp)]
+            L.msm_graph_create_dev.restype = st
             L.msm_graph_launch.argtypes = [vp, vp]
             L.msm_graph_launch.restype = st
             L.msm_graph_destroy.argtypes = [vp]
@@ -283,6 +292,31 @@ def msm_graph_create(model, hidden_in, parent, tokens, pos0, k_ptrs, v_ptrs, log
     return g
 
 
+def msm_verify_step_dev(model, hidden_in, state, k_ptrs, v_ptrs, logits_out, hidden_out, stream=0) -> int:
+    kp, ka = _ptr_array(k_ptrs)
+    vpp, va = _ptr_array(v_ptrs)
+    return lib().msm_verify_step_dev(model, ctypes.c_void_p(hidden_in), ctypes.c_void_p(state), kp, vpp,
+                                     ctypes.c_void_p(logits_out), ctypes.c_void_p(hidden_out), ctypes.c_void_p(stream))
+
+
+def msm_accept_dev(model, logits, state, k_ptrs, v_ptrs, result, stream=0) -> int:
+    kp, ka = _ptr_array(k_ptrs)
+    vpp, va = _ptr_array(v_ptrs)
+    return lib().msm_accept_dev(model, ctypes.c_void_p(logits), ctypes.c_void_p(state), kp, vpp,
+                                ctypes.c_void_p(result), ctypes.c_void_p(stream))
+
+
+def msm_graph_create_dev(model, hidden_in, state, k_ptrs, v_ptrs, logits_out, hidden_out, accept_result):
+    """Returns the graph handle; raises MsmError on failure."""
+    kp, ka = _ptr_array(k_ptrs)
+    vpp, va = _ptr_array(v_ptrs)
+    g = ctypes.c_void_p()
+    _check(lib().msm_graph_create_dev(model, ctypes.c_void_p(hidden_in), ctypes.c_void_p(state), kp, vpp,
+                                      ctypes.c_void_p(logits_out), ctypes.c_void_p(hidden_out),
+                                      ctypes.c_void_p(accept_result), ctypes.byref(g)))
+    return g
+
+
 def msm_graph_launch(graph, stream=0) -> int:
     return lib().msm_graph_launch(graph, ctypes.c_void_p(stream))
 
@@ -383,6 +417,27 @@ class Model:
                              logits_out.data_ptr() if logits_out is not None else 0,
                              hidden_out.data_ptr() if hidden_out is not None else 0,
                              accept_result.data_ptr() if accept_result is not None else 0)
+        return StepGraph(g, self)
+
+    def verify_step_dev(self, hidden_in, state, k_caches, v_caches, logits_out=None, hidden_out=None, stream=0):
+        """msm_verify_step_dev: `state` is a device int32 tensor of MSM_STEP_STATE_INTS entries."""
+        return _check(msm_verify_step_dev(self.handle, hidden_in.data_ptr(), state.data_ptr(),
+                                          [k.data_ptr() for k in k_caches], [v.data_ptr() for v in v_caches],
+                                          logits_out.data_ptr() if logits_out is not None else 0,
+                                          hidden_out.data_ptr() if hidden_out is not None else 0, stream))
+
+    def accept_dev(self, logits, state, k_caches, v_caches, result, stream=0):
+        return _check(msm_accept_dev(self.handle, logits.data_ptr(), state.data_ptr(),
+                                     [k.data_ptr() for k in k_caches], [v.data_ptr() for v in v_caches],
+                                     result.data_ptr(), stream))
+
+    def graph_dev(self, hidden_in, state, k_caches, v_caches, logits_out=None, hidden_out=None, accept_result=None):
+        """msm_graph_create_dev: a StepGraph that reads the tree, tokens and pos0 from `state` at each replay."""
+        g = msm_graph_create_dev(self.handle, hidden_in.data_ptr(), state.data_ptr(),
+                                 [k.data_ptr() for k in k_caches], [v.data_ptr() for v in v_caches],
+                                 logits_out.data_ptr() if logits_out is not None else 0,
+                                 hidden_out.data_ptr() if hidden_out is not None else 0,
+                                 accept_result.data_ptr() if accept_result is not None else 0)
         return StepGraph(g, self)
 
     def sync(self, stream=0) -> int:

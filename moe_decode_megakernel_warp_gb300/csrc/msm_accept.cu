@@ -103,29 +103,57 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_argmax_kernel(const flo
 __global__ void __launch_bounds__(kAcceptThreads) accept_walk_kernel(const AcceptParams p) {
   __shared__ int32_t s_arg[kRowsPerThread];
   __shared__ int32_t s_path[kRowsPerThread];
-  __shared__ int32_t s_n;
-  if (threadIdx.x < kRowsPerThread) s_arg[threadIdx.x] = p.choice[threadIdx.x];
+  __shared__ int32_t s_n, s_pos0;
+  __shared__ int32_t s_par[kRowsPerThread], s_tok[kRowsPerThread];
+  __shared__ int s_ok;
+  if (threadIdx.x < 32) {
+    // the tree, the draft tokens and pos0: launch parameters, or the device-resident
+    // state checked here (parent[0] == -1, 0 <= parent[i] < i, tokens in [0, vocab),
+    // 0 <= pos0 <= max_ctx - 16)
+    const int i = threadIdx.x;
+    int pv = 0, tv = 0, pos0 = p.pos0;
+    if (i < kRowsPerThread) {
+      pv = p.state ? p.state[1 + i] : p.parent[i];
+      tv = p.state ? p.state[1 + kRowsPerThread + i] : p.tokens[i];
+      s_arg[i] = p.choice[i];
+      s_par[i] = pv;
+      s_tok[i] = tv;
+    }
+    if (p.state) pos0 = p.state[0];
+    const bool ok = __all_sync(0xffffffffu, i >= kRowsPerThread ||
+                                                ((i == 0 ? pv == -1 : (pv >= 0 && pv < i)) && tv >= 0 && tv < p.vocab)) &&
+                    pos0 >= 0 && pos0 <= p.max_ctx - kRowsPerThread;
+    if (i == 0) {
+      s_ok = ok;
+      s_pos0 = pos0;
+    }
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
-    // from the root, the first child (in tree order) whose draft token is the
-    // parent's greedy choice; stop at the first node without one
     int cur = 0, n = 1;
     s_path[0] = 0;
-    for (;;) {
-      int nxt = -1;
-      for (int c = cur + 1; c < kRowsPerThread; ++c)
-        if (p.parent[c] == cur && p.tokens[c] == s_arg[cur]) {
-          nxt = c;
-          break;
-        }
-      if (nxt < 0) break;
-      s_path[n++] = nxt;
-      cur = nxt;
+    if (s_ok) {
+      // from the root, the first child (in tree order) whose draft token is the
+      // parent's greedy choice; stop at the first node without one
+      for (;;) {
+        int nxt = -1;
+        for (int c = cur + 1; c < kRowsPerThread; ++c)
+          if (s_par[c] == cur && s_tok[c] == s_arg[cur]) {
+            nxt = c;
+            break;
+          }
+        if (nxt < 0) break;
+        s_path[n++] = nxt;
+        cur = nxt;
+      }
+    } else {
+      n = 0;  // nothing accepted, nothing moved
+      if (blockIdx.x == 0 && p.status) atomicCAS(&p.status->code, 0, 1 /* MSM_ERR_INVALID_ARG */);
     }
     s_n = n;
     if (p.result != nullptr && blockIdx.x == 0) {
       p.result[0] = n;
-      p.result[1] = s_arg[cur];
+      p.result[1] = n ? s_arg[cur] : -1;
       for (int j = 0; j < kRowsPerThread; ++j) {
         p.result[2 + j] = j < n ? s_path[j] : -1;
         p.result[2 + kRowsPerThread + j] = s_arg[j];
@@ -142,7 +170,7 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_walk_kernel(const Accep
     const int l = col / per_layer, rem = col - l * per_layer;
     const int kv = rem / (p.n_kv_heads * chunks), rem2 = rem - kv * (p.n_kv_heads * chunks);
     const int h = rem2 / chunks, ch = rem2 - h * chunks;
-    uint16_t* base = (kv ? p.vc[l] : p.kc[l]) + ((size_t)h * p.max_ctx + p.pos0) * p.head_dim + ch * 8;
+    uint16_t* base = (kv ? p.vc[l] : p.kc[l]) + ((size_t)h * p.max_ctx + s_pos0) * p.head_dim + ch * 8;
     uint4 v[kRowsPerThread - 1];
 #pragma unroll
     for (int j = 1; j < kRowsPerThread; ++j)

@@ -401,14 +401,24 @@ void msm_model_destroy(msm_model* m) {
   delete m;
 }
 
-msm_status msm_verify_step(msm_model* m, const void* hidden_in, const int32_t* parent, int32_t pos0,
-                           void* const* k_cache, void* const* v_cache, float* logits_out, void* hidden_out,
-                           void* stream) {
+}  // extern "C"
+
+namespace {
+// the verify step with the tree and pos0 from the host (state == nullptr) or from a
+// device-resident step state that the kernels validate
+msm_status enqueue_verify(msm_model* m, const void* hidden_in, const int32_t* parent, int32_t pos0,
+                          const int32_t* state, void* const* k_cache, void* const* v_cache, float* logits_out,
+                          void* hidden_out, void* stream) {
   if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
   const Dims& dm = m->dm;
   if (!hidden_in || !k_cache || !v_cache) return fail(MSM_ERR_INVALID_ARG, "NULL hidden_in or cache array");
-  if (!parent_valid(parent)) return fail(MSM_ERR_INVALID_ARG, "parent must satisfy parent[0] == -1, 0 <= parent[i] < i");
-  if (pos0 < 0 || (int64_t)pos0 + T > dm.max_ctx) return fail(MSM_ERR_INVALID_ARG, "pos0 out of range");
+  if (!state) {
+    if (!parent_valid(parent))
+      return fail(MSM_ERR_INVALID_ARG, "parent must satisfy parent[0] == -1, 0 <= parent[i] < i");
+    if (pos0 < 0 || (int64_t)pos0 + T > dm.max_ctx) return fail(MSM_ERR_INVALID_ARG, "pos0 out of range");
+  } else if (reinterpret_cast<uintptr_t>(state) & 3) {
+    return fail(MSM_ERR_INVALID_ARG, "state must be 4-byte aligned");
+  }
   if (dm.vocab > 0 && !logits_out) return fail(MSM_ERR_INVALID_ARG, "logits_out is NULL but vocab > 0");
   if (dm.vocab == 0 && !hidden_out) return fail(MSM_ERR_INVALID_ARG, "hidden_out is NULL but vocab == 0");
   if ((reinterpret_cast<uintptr_t>(hidden_in) & 15) || (reinterpret_cast<uintptr_t>(hidden_out) & 15) ||
@@ -454,7 +464,12 @@ msm_status msm_verify_step(msm_model* m, const void* hidden_in, const int32_t* p
   P.prefetch_experts = m->cfg.prefetch_experts > 0 ? m->cfg.prefetch_experts : 14;
   P.runahead_bytes = m->cfg.l2_runahead_kb > 0 ? (uint32_t)m->cfg.l2_runahead_kb * 1024u : 0u;
   P.phase_rot = 13;
-  std::memcpy(P.parent, parent, sizeof(int32_t) * T);
+  if (state) {
+    P.state = state;
+    P.pos0 = 0;
+  } else {
+    std::memcpy(P.parent, parent, sizeof(int32_t) * T);
+  }
   P.hidden_in = static_cast<const uint16_t*>(hidden_in);
   P.logits = logits_out;
   const bool timing = (m->cfg.flags & MSM_FLAG_SELF_TIMING) != 0;
@@ -526,6 +541,21 @@ msm_status msm_verify_step(msm_model* m, const void* hidden_in, const int32_t* p
   ++m->step_count;
   return MSM_OK;
 }
+}  // namespace
+
+extern "C" {
+
+msm_status msm_verify_step(msm_model* m, const void* hidden_in, const int32_t* parent, int32_t pos0,
+                           void* const* k_cache, void* const* v_cache, float* logits_out, void* hidden_out,
+                           void* stream) {
+  return enqueue_verify(m, hidden_in, parent, pos0, nullptr, k_cache, v_cache, logits_out, hidden_out, stream);
+}
+
+msm_status msm_verify_step_dev(msm_model* m, const void* hidden_in, const int32_t* state, void* const* k_cache,
+                               void* const* v_cache, float* logits_out, void* hidden_out, void* stream) {
+  if (!state) return fail(MSM_ERR_INVALID_ARG, "state is NULL");
+  return enqueue_verify(m, hidden_in, nullptr, 0, state, k_cache, v_cache, logits_out, hidden_out, stream);
+}
 
 msm_status msm_sync(msm_model* m, void* stream) {
   if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
@@ -536,8 +566,12 @@ msm_status msm_sync(msm_model* m, void* stream) {
   if (ds.code == 0) return MSM_OK;
   char buf[160];
   std::snprintf(buf, sizeof(buf), "device wait timed out (layer %d, phase %d, block %d)", ds.layer, ds.phase, ds.block);
-  msm_status st = (ds.code == MSM_ERR_DEVICE_TIMEOUT) ? MSM_ERR_DEVICE_TIMEOUT : MSM_ERR_CUDA;
-  if (ds.code != MSM_ERR_DEVICE_TIMEOUT) std::snprintf(buf, sizeof(buf), "device error %d (phase %d)", ds.code, ds.phase);
+  msm_status st = (ds.code == MSM_ERR_DEVICE_TIMEOUT) ? MSM_ERR_DEVICE_TIMEOUT
+                  : (ds.code == MSM_ERR_INVALID_ARG) ? MSM_ERR_INVALID_ARG : MSM_ERR_CUDA;
+  if (ds.code == MSM_ERR_INVALID_ARG)
+    std::snprintf(buf, sizeof(buf), "device-resident step state invalid (pos0, parent or token ids)");
+  else if (ds.code != MSM_ERR_DEVICE_TIMEOUT)
+    std::snprintf(buf, sizeof(buf), "device error %d (phase %d)", ds.code, ds.phase);
   // re-arm every exchange buffer and clear the status for the next step
   msm_status r = rearm_all(m, m->aux);
   if (r != MSM_OK) return r;
@@ -631,17 +665,27 @@ msm_status msm_get_exchange(msm_model* m, const char* name, void* host, size_t b
   return fail(MSM_ERR_INVALID_ARG, std::string("unknown exchange buffer ") + name);
 }
 
-msm_status msm_accept(msm_model* m, const float* logits, const int32_t* tokens, const int32_t* parent,
-                      int32_t pos0, void* const* k_cache, void* const* v_cache, int32_t* result, void* stream) {
+}  // extern "C"
+
+namespace {
+msm_status enqueue_accept(msm_model* m, const float* logits, const int32_t* tokens, const int32_t* parent,
+                          int32_t pos0, const int32_t* state, void* const* k_cache, void* const* v_cache,
+                          int32_t* result, void* stream) {
   if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
   const Dims& dm = m->dm;
   if (dm.vocab <= 0) return fail(MSM_ERR_UNSUPPORTED, "accept needs the LM head (vocab > 0)");
-  if (!logits || !tokens || !result || !k_cache || !v_cache)
-    return fail(MSM_ERR_INVALID_ARG, "NULL logits, tokens, result or cache array");
-  if (!parent_valid(parent)) return fail(MSM_ERR_INVALID_ARG, "parent must satisfy parent[0] == -1, 0 <= parent[i] < i");
-  for (int i = 0; i < T; ++i)
-    if (tokens[i] < 0 || tokens[i] >= dm.vocab) return fail(MSM_ERR_INVALID_ARG, "token id out of [0, vocab)");
-  if (pos0 < 0 || (int64_t)pos0 + T > dm.max_ctx) return fail(MSM_ERR_INVALID_ARG, "pos0 out of range");
+  if (!logits || !result || !k_cache || !v_cache)
+    return fail(MSM_ERR_INVALID_ARG, "NULL logits, result or cache array");
+  if (!state) {
+    if (!tokens) return fail(MSM_ERR_INVALID_ARG, "tokens is NULL");
+    if (!parent_valid(parent))
+      return fail(MSM_ERR_INVALID_ARG, "parent must satisfy parent[0] == -1, 0 <= parent[i] < i");
+    for (int i = 0; i < T; ++i)
+      if (tokens[i] < 0 || tokens[i] >= dm.vocab) return fail(MSM_ERR_INVALID_ARG, "token id out of [0, vocab)");
+    if (pos0 < 0 || (int64_t)pos0 + T > dm.max_ctx) return fail(MSM_ERR_INVALID_ARG, "pos0 out of range");
+  } else if (reinterpret_cast<uintptr_t>(state) & 3) {
+    return fail(MSM_ERR_INVALID_ARG, "state must be 4-byte aligned");
+  }
   if ((reinterpret_cast<uintptr_t>(logits) & 15) || (reinterpret_cast<uintptr_t>(result) & 3))
     return fail(MSM_ERR_INVALID_ARG, "logits must be 16-byte and result 4-byte aligned");
   for (int l = 0; l < dm.n_layers; ++l) {
@@ -655,9 +699,15 @@ msm_status msm_accept(msm_model* m, const float* logits, const int32_t* tokens, 
   AcceptParams p;
   std::memset(&p, 0, sizeof(p));
   p.choice = m->accept_choice;
-  std::memcpy(p.parent, parent, sizeof(p.parent));
-  std::memcpy(p.tokens, tokens, sizeof(p.tokens));
-  p.pos0 = pos0;
+  if (state) {
+    p.state = state;
+  } else {
+    std::memcpy(p.parent, parent, sizeof(p.parent));
+    std::memcpy(p.tokens, tokens, sizeof(p.tokens));
+    p.pos0 = pos0;
+  }
+  p.status = m->status;
+  p.vocab = dm.vocab;
   p.n_kv_heads = dm.hkv;
   p.head_dim = dm.hd;
   p.max_ctx = dm.max_ctx;
@@ -674,6 +724,20 @@ msm_status msm_accept(msm_model* m, const float* logits, const int32_t* tokens, 
   }
   return MSM_OK;
 }
+}  // namespace
+
+extern "C" {
+
+msm_status msm_accept(msm_model* m, const float* logits, const int32_t* tokens, const int32_t* parent,
+                      int32_t pos0, void* const* k_cache, void* const* v_cache, int32_t* result, void* stream) {
+  return enqueue_accept(m, logits, tokens, parent, pos0, nullptr, k_cache, v_cache, result, stream);
+}
+
+msm_status msm_accept_dev(msm_model* m, const float* logits, const int32_t* state, void* const* k_cache,
+                          void* const* v_cache, int32_t* result, void* stream) {
+  if (!state) return fail(MSM_ERR_INVALID_ARG, "state is NULL");
+  return enqueue_accept(m, logits, nullptr, nullptr, 0, state, k_cache, v_cache, result, stream);
+}
 
 struct msm_graph {
   cudaGraph_t graph = nullptr;
@@ -688,9 +752,12 @@ void msm_graph_destroy(msm_graph* g) {
   delete g;
 }
 
-msm_status msm_graph_create(msm_model* m, const void* hidden_in, const int32_t* parent, const int32_t* tokens,
-                            int32_t pos0, void* const* k_cache, void* const* v_cache, float* logits_out,
-                            void* hidden_out, int32_t* accept_result, msm_graph** out) {
+}  // extern "C"
+
+namespace {
+msm_status capture_step(msm_model* m, const void* hidden_in, const int32_t* parent, const int32_t* tokens,
+                        int32_t pos0, const int32_t* state, void* const* k_cache, void* const* v_cache,
+                        float* logits_out, void* hidden_out, int32_t* accept_result, msm_graph** out) {
   if (!out) return fail(MSM_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
@@ -705,9 +772,10 @@ msm_status msm_graph_create(msm_model* m, const void* hidden_in, const int32_t* 
   // the graph arms the exchange buffers itself, so a replay never depends on the
   // state an earlier step (eager or replayed) left behind
   msm_status st = rearm_all(m, cs);
-  if (st == MSM_OK) st = msm_verify_step(m, hidden_in, parent, pos0, k_cache, v_cache, logits_out, hidden_out, cs);
+  if (st == MSM_OK)
+    st = enqueue_verify(m, hidden_in, parent, pos0, state, k_cache, v_cache, logits_out, hidden_out, cs);
   if (st == MSM_OK && accept_result)
-    st = msm_accept(m, logits_out, tokens, parent, pos0, k_cache, v_cache, accept_result, cs);
+    st = enqueue_accept(m, logits_out, tokens, parent, pos0, state, k_cache, v_cache, accept_result, cs);
   std::string msg = st == MSM_OK ? std::string() : std::string(msm_last_error());
   cudaGraph_t graph = nullptr;
   e = cudaStreamEndCapture(cs, &graph);
@@ -730,6 +798,27 @@ msm_status msm_graph_create(msm_model* m, const void* hidden_in, const int32_t* 
   }
   *out = g;
   return MSM_OK;
+}
+}  // namespace
+
+extern "C" {
+
+msm_status msm_graph_create(msm_model* m, const void* hidden_in, const int32_t* parent, const int32_t* tokens,
+                            int32_t pos0, void* const* k_cache, void* const* v_cache, float* logits_out,
+                            void* hidden_out, int32_t* accept_result, msm_graph** out) {
+  return capture_step(m, hidden_in, parent, tokens, pos0, nullptr, k_cache, v_cache, logits_out, hidden_out,
+                      accept_result, out);
+}
+
+msm_status msm_graph_create_dev(msm_model* m, const void* hidden_in, const int32_t* state, void* const* k_cache,
+                                void* const* v_cache, float* logits_out, void* hidden_out, int32_t* accept_result,
+                                msm_graph** out) {
+  if (!state) {
+    if (out) *out = nullptr;
+    return fail(MSM_ERR_INVALID_ARG, "state is NULL");
+  }
+  return capture_step(m, hidden_in, nullptr, nullptr, 0, state, k_cache, v_cache, logits_out, hidden_out,
+                      accept_result, out);
 }
 
 msm_status msm_graph_launch(msm_graph* g, void* stream) {

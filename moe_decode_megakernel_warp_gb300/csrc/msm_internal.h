@@ -158,6 +158,10 @@ struct LaunchParams {
   uint32_t runahead_bytes;  // L2 run-ahead of the loader's stream; 0 = off
   int phase_rot;
   int32_t parent[16];
+  // device-resident step inputs, or null: int32 [34] = pos0, parent[16], draft
+  // tokens[16], spare; when set, pos0 and parent above are unused and each
+  // launch validates the state at entry (a bad one fails the launch with code 1)
+  const int32_t* state;
   // KV cache tensor maps of this layer: 3-D {hd, max_ctx, hkv}, 128-byte swizzle
   CUtensorMap tmap_k;
   CUtensorMap tmap_v;
@@ -179,8 +183,10 @@ struct AcceptParams {
   const int32_t* choice;  // [16] greedy choice per tree node (launch 1's output)
   int32_t parent[16];
   int32_t tokens[16];
-  int32_t pos0, n_kv_heads, head_dim, max_ctx, n_layers;
+  int32_t pos0, n_kv_heads, head_dim, max_ctx, n_layers, vocab;
   int32_t* result;  // written by block 0 of the launch that carries it, else nullptr
+  const int32_t* state;  // device-resident pos0 / parent / tokens (then the fields above are unused), or null
+  DevStatus* status;     // where a launch reports an invalid device-resident state
   uint16_t* kc[kAcceptLayers];
   uint16_t* vc[kAcceptLayers];
 };

@@ -41,6 +41,7 @@ struct Smem {
   uint32_t* slot_off;
   volatile int* abort;
   int* n_active;
+  int* pos0;          // first tree row of this step (the launch parameter or the device state)
   uint32_t* anc;
   int32_t* tpos;
   int32_t* depth;
@@ -84,6 +85,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const LaunchParams& P) {
   s.a_ts = reinterpret_cast<float*>(sm + kATsOff);
   s.red = reinterpret_cast<float*>(sm + 6080);
   s.slot_tile = reinterpret_cast<volatile uint32_t*>(sm + 6592);
+  s.pos0 = reinterpret_cast<int*>(sm + 6640);
   s.ring_state = reinterpret_cast<struct RunAhead*>(sm + kRingStateOff);
   s.dred = reinterpret_cast<float*>(sm + 8192);
   return s;
@@ -96,6 +98,7 @@ struct Ctx {
   const LaunchParams* P;
   Smem S;
   uint64_t deadline;
+  int pos0;  // copy of *S.pos0
   uint64_t next_abort_check = 0;
   int block;
 
@@ -212,19 +215,19 @@ __device__ __forceinline__ int rot_block(int b, int rot, int G) { return (b + ro
 struct AttnUnit {
   int valid, hk, s, r0, r1, n_sub, tree;
 };
-__device__ __forceinline__ AttnUnit attn_unit(const LaunchParams& P, int bb, int is_global) {
+__device__ __forceinline__ AttnUnit attn_unit(const LaunchParams& P, int pos0, int bb, int is_global) {
   const Dims& dm = P.dm;
   AttnUnit u;
   u.valid = bb < dm.hkv * dm.splits;
   u.hk = u.valid ? bb / dm.splits : 0;
   u.s = u.valid ? bb % dm.splits : 0;
-  int lo = is_global ? 0 : max(0, P.pos0 - dm.window + 1);
-  int n = P.pos0 - lo;
+  int lo = is_global ? 0 : max(0, pos0 - dm.window + 1);
+  int n = pos0 - lo;
   int chunk = (n + dm.splits - 1) / dm.splits;
   chunk = ((chunk + dm.attn_rows - 1) / dm.attn_rows) * dm.attn_rows;
   if (chunk < dm.attn_rows) chunk = dm.attn_rows;
-  u.r0 = min(P.pos0, lo + u.s * chunk);
-  u.r1 = min(P.pos0, u.r0 + chunk);
+  u.r0 = min(pos0, lo + u.s * chunk);
+  u.r1 = min(pos0, u.r0 + chunk);
   u.n_sub = u.valid ? (u.r1 - u.r0 + dm.attn_rows - 1) / dm.attn_rows : 0;
   u.tree = u.valid && (u.s == dm.splits - 1);
   return u;
@@ -447,7 +450,7 @@ struct TileStream {
       lo = hi = u = k0 = 0;
       switch (seg) {
         case 1: {
-          const AttnUnit au = attn_unit(P, rot_block(cx.block, P.phase_rot * 2, gridDim.x), P.is_global);
+          const AttnUnit au = attn_unit(P, cx.pos0, rot_block(cx.block, P.phase_rot * 2, gridDim.x), P.is_global);
           hi = au.n_sub;
           kv_r0 = au.r0;
           kv_hk = au.hk;
@@ -494,7 +497,7 @@ __device__ void loader(Ctx& cx) {
   // previous launch, so they stream before the dependency wait
   if (P.first) ts.dense(P.w_qkv_pro, dm.d, dm.nqkv, P.phase_rot * 1);
   if (r.ra_on) {
-    const AttnUnit au = attn_unit(P, rot_block(cx.block, P.phase_rot * 2, gridDim.x), P.is_global);
+    const AttnUnit au = attn_unit(P, cx.pos0, rot_block(cx.block, P.phase_rot * 2, gridDim.x), P.is_global);
     ra_front(P, r.ra, cx.block, au.valid ? au.r0 : 0, au.valid ? au.r1 : 0, au.hk);
   }
   bool ok = true;
@@ -784,7 +787,7 @@ __device__ __forceinline__ void qkv_epilogue(const LaunchParams& P, const Smem& 
       if (dst.q_relaxed) { st_relaxed_u16(q, xr); st_relaxed_u16(q + D / 2, yr); }
       else { q[0] = xr; q[D / 2] = yr; }
     } else {
-      uint16_t* k = dst.kc + ((size_t)h * dm.max_ctx + P.pos0 + t) * D + dim;
+      uint16_t* k = dst.kc + ((size_t)h * dm.max_ctx + *S.pos0 + t) * D + dim;
       k[0] = xr;
       k[D / 2] = yr;
       if (dst.tkv) {
@@ -796,7 +799,7 @@ __device__ __forceinline__ void qkv_epilogue(const LaunchParams& P, const Smem& 
   } else {
     const int hu = u - nQ - nK, h = hu / upd, j = hu % upd;
     const uint16_t a = bf16_bits_rn(vlo), b = bf16_bits_rn(vhi);
-    uint16_t* v = dst.vc + ((size_t)h * dm.max_ctx + P.pos0 + t) * D + j * 16 + p;
+    uint16_t* v = dst.vc + ((size_t)h * dm.max_ctx + *S.pos0 + t) * D + j * 16 + p;
     v[0] = a;
     v[8] = b;
     if (dst.tkv) {
@@ -1076,7 +1079,7 @@ __device__ void attention_phase(Worker& w) {
   const LaunchParams& P = *cx.P;
   const Dims& dm = P.dm;
   const int G = gridDim.x;
-  const AttnUnit au = attn_unit(P, rot_block(cx.block, P.phase_rot * 2, G), P.is_global);
+  const AttnUnit au = attn_unit(P, cx.pos0, rot_block(cx.block, P.phase_rot * 2, G), P.is_global);
   if (!au.valid) return;
   const int group = dm.group, R = dm.attn_rows, NK = dm.attn_nk, WPH = dm.attn_wph;
   // act buffer regions: Q fragments source, tree K/V, merge scratch
@@ -1121,7 +1124,7 @@ __device__ void attention_phase(Worker& w) {
           w.ok = poll_bf16x8(cx, p, v, PH_ATTN);
         } else {
           const uint16_t* cache = kv ? P.vc : P.kc;
-          v = *reinterpret_cast<const uint4*>(cache + ((size_t)au.hk * dm.max_ctx + P.pos0 + row) * D + d);
+          v = *reinterpret_cast<const uint4*>(cache + ((size_t)au.hk * dm.max_ctx + cx.pos0 + row) * D + d);
         }
         *reinterpret_cast<uint4*>((kv ? tv : tk) + swz(row, d, 16)) = v;
       }
@@ -1145,7 +1148,7 @@ __device__ void attention_phase(Worker& w) {
     for (int ks = 0; ks < D / 16; ++ks) ldsm_x4(qb + ks * kKStepBytes, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
   }
   const float scale_log2 = 1.4426950408889634f * rsqrtf((float)D);
-  const int pos0 = P.pos0, window = dm.window, glob = P.is_global;
+  const int pos0 = cx.pos0, window = dm.window, glob = P.is_global;
   const int32_t* tpos = cx.S.tpos;
   for (int i = 0; i < au.n_sub; ++i) {
     const uint32_t t = w.ti + (uint32_t)i;
@@ -1885,7 +1888,7 @@ __device__ void rope_table(Worker& w) {
   const int tid = w.cw * 32 + w.lane;
   for (int i = tid; i < 16 * half; i += kComputeThreads) {
     const int dep = i / half, k = i % half;
-    double ang = (double)(P.pos0 + dep) * P.inv_freq[k];
+    double ang = (double)(w.cx->pos0 + dep) * P.inv_freq[k];
     const double two_pi = 6.283185307179586476925286766559;
     ang = ang - two_pi * rint(ang / two_pi);
     float s, c;
@@ -1999,7 +2002,7 @@ __device__ void compute_main(Worker& w) {
   stamp<kTiming>(P, b, EV_GEMM2_DONE);
   // move the next layer's KV history toward L2 while the combine waits
   if ((P.flags & 0x4u) && !P.last && w.cw == 0 && w.lane == 0 && P.kc_pf != nullptr) {
-    const AttnUnit au = attn_unit(P, rot_block(b, P.phase_rot * 2, gridDim.x), P.next_global);
+    const AttnUnit au = attn_unit(P, cx.pos0, rot_block(b, P.phase_rot * 2, gridDim.x), P.next_global);
     if (au.valid && au.r1 > au.r0) {
       const size_t off = ((size_t)au.hk * dm.max_ctx + au.r0) * dm.hd;
       const uint32_t bytes = (uint32_t)((au.r1 - au.r0) * dm.hd * 2);
@@ -2068,20 +2071,40 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
     *cx.S.abort = (smem_u32(smem) & 1023u) != 0u;  // the swizzled tiles need 1 KB alignment
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // a1: the tree (ancestor-or-self masks, depths, positions) from the parent array
-  if (warp == 1 && lane < T) {
-    uint32_t m = 0;
-    int dep = 0;
-    for (int j = lane; j >= 0; j = P.parent[j]) {
-      m |= 1u << j;
-      if (j != lane) ++dep;
+  // a1: the tree (ancestor-or-self masks, depths, positions) from the parent array,
+  // taken from the launch parameters or from the device-resident step state; a state
+  // is checked first (parent[0] == -1, 0 <= parent[i] < i, 0 <= pos0 <= max_ctx - 16),
+  // so the walk below always ends and every cache row stays in range
+  if (warp == 1) {
+    // the parents travel through the GEMM1 row-scale scratch, unused until routing
+    int* par = reinterpret_cast<int*>(cx.S.x_ts);
+    int pos0 = P.pos0, pv = lane < T ? P.parent[lane] : 0;
+    if (P.state != nullptr) {
+      pos0 = P.state[0];
+      pv = lane < T ? P.state[1 + lane] : 0;
     }
-    cx.S.anc[lane] = m;
-    cx.S.depth[lane] = dep;
-    cx.S.tpos[lane] = P.pos0 + dep;
+    const bool ok = __all_sync(0xffffffffu, lane >= T || (lane == 0 ? pv == -1 : (pv >= 0 && pv < lane))) &&
+                    pos0 >= 0 && pos0 <= P.dm.max_ctx - T;
+    if (lane < T) par[lane] = pv;
+    if (lane == 0) *cx.S.pos0 = ok ? pos0 : -1;  // -1: the block gives up below
+    __syncwarp();
+    if (!ok) {
+      if (lane == 0) atomicCAS(&P.status->code, 0, 1 /* MSM_ERR_INVALID_ARG */);
+    } else if (lane < T) {
+      uint32_t m = 0;
+      int dep = 0;
+      for (int j = lane; j >= 0; j = par[j]) {
+        m |= 1u << j;
+        if (j != lane) ++dep;
+      }
+      cx.S.anc[lane] = m;
+      cx.S.depth[lane] = dep;
+      cx.S.tpos[lane] = pos0 + dep;
+    }
   }
   __syncthreads();
-  if (*cx.S.abort) {
+  cx.pos0 = *cx.S.pos0;
+  if (*cx.S.abort || cx.pos0 < 0) {
     if (threadIdx.x == 0 && atomicCAS(&P.status->code, 0, 2) == 0) P.status->phase = PH_START;
     pdl_launch_dependents();
     return;

@@ -39,6 +39,8 @@ def test_null_arguments_are_rejected_without_a_device():
     assert msm.msm_verify_step_noalloc(None, 0, list(range(-1, 15)), 0, [0], [0], 0, 0) == msm.MSM_ERR_INVALID_ARG
     assert msm.msm_accept(None, 0, [0] * 16, list(range(-1, 15)), 0, [0], [0], 0) == msm.MSM_ERR_INVALID_ARG
     assert msm.msm_graph_launch(None) == msm.MSM_ERR_INVALID_ARG
+    assert msm.msm_verify_step_dev(None, 0, 0, [0], [0], 0, 0) == msm.MSM_ERR_INVALID_ARG
+    assert msm.msm_accept_dev(None, 0, 0, [0], [0], 0) == msm.MSM_ERR_INVALID_ARG
     msm.msm_graph_destroy(None)
 
 

@@ -225,3 +225,155 @@ def test_accept_full_size_sampled():
             assert np.array_equal(vc[l][:, rows].cpu().numpy().view(np.uint16), wv[l])
     finally:
         m.close()
+
+
+def _state(torch, dev, pos0, parent, tokens):
+    import moe_decode_megakernel_warp_gb300 as msm
+    st = np.zeros(msm.MSM_STEP_STATE_INTS, np.int32)
+    st[0] = pos0
+    st[1:1 + T] = parent
+    st[1 + T:1 + 2 * T] = tokens
+    return torch.from_numpy(st).to(dev)
+
+
+def _steps(cfg, n, seed):
+    """n (pos0, parent, tokens) triples: random trees, positions across the cache."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        parent = [-1] + [int(rng.integers(0, j)) for j in range(1, T)]
+        pos0 = [cfg.pos0, 17, cfg.max_ctx - T][i % 3]
+        tokens = [int(x) for x in rng.integers(0, cfg.vocab, T)]
+        out.append((pos0, parent, tokens))
+    return out
+
+
+def _eager(m, torch, hid, kc, vc, k0, v0, lg_d, res, pos0, parent, tokens, cfg, rng_seed):
+    """Host-parameter verify + accept from the saved caches; tokens along the first-child
+    chain are replaced by the greedy choices so that the walk accepts a few nodes."""
+    for a, b in zip(kc + vc, k0 + v0):
+        a.copy_(b)
+    m.verify_step(hid, parent, pos0, kc, vc, logits_out=lg_d)
+    g = acc.target_argmax(lg_d.cpu().numpy())
+    tokens = list(tokens)
+    cur = 0
+    for c in range(1, T):
+        if parent[c] == cur and c % 4 != 3:
+            tokens[c] = int(g[cur])
+            cur = c
+    for a, b in zip(kc + vc, k0 + v0):
+        a.copy_(b)
+    m.verify_step(hid, parent, pos0, kc, vc, logits_out=lg_d)
+    m.accept(lg_d, tokens, parent, pos0, kc, vc, res)
+    assert m.sync() == 0
+    return tokens, (lg_d.cpu().numpy().copy(), res.cpu().numpy().copy(), [t.cpu().numpy().copy() for t in kc + vc])
+
+
+def test_device_state_calls_and_one_graph_for_every_step():
+    """msm_verify_step_dev / msm_accept_dev equal the host-parameter calls bit for bit,
+    and one msm_graph_create_dev graph replays three different steps (trees, tokens,
+    positions written into the state between replays) with the same results."""
+    torch = _torch()
+    import moe_decode_megakernel_warp_gb300 as msm
+    case, m = _model("cfg1_stack")
+    try:
+        cfg = case.cfg
+        dev = torch.device("cuda", 0)
+        kc = [torch.from_numpy(k.view(np.int16)).to(dev) for k, _ in case.kv]
+        vc = [torch.from_numpy(v.view(np.int16)).to(dev) for _, v in case.kv]
+        k0 = [k.clone() for k in kc]
+        v0 = [v.clone() for v in vc]
+        hid = torch.from_numpy(case.hidden.view(np.int16)).to(dev)
+        lg_d = torch.empty((T, cfg.vocab), dtype=torch.float32, device=dev)
+        res = torch.zeros((msm.MSM_ACCEPT_RESULT_INTS,), dtype=torch.int32, device=dev)
+        state = torch.zeros((msm.MSM_STEP_STATE_INTS,), dtype=torch.int32, device=dev)
+        steps = _steps(cfg, 3, 11)
+        wants = []
+        for pos0, parent, tokens in steps:
+            tokens, want = _eager(m, torch, hid, kc, vc, k0, v0, lg_d, res, pos0, parent, tokens, cfg, 0)
+            wants.append((pos0, parent, tokens, want))
+        # direct calls
+        for pos0, parent, tokens, want in wants:
+            for a, b in zip(kc + vc, k0 + v0):
+                a.copy_(b)
+            state.copy_(_state(torch, dev, pos0, parent, tokens))
+            m.verify_step_dev(hid, state, kc, vc, logits_out=lg_d)
+            m.accept_dev(lg_d, state, kc, vc, res)
+            assert m.sync() == 0
+            assert np.array_equal(lg_d.cpu().numpy(), want[0])
+            assert np.array_equal(res.cpu().numpy(), want[1])
+            for t, w in zip(kc + vc, want[2]):
+                assert np.array_equal(t.cpu().numpy(), w)
+        # one graph, three steps
+        graph = m.graph_dev(hid, state, kc, vc, logits_out=lg_d, accept_result=res)
+        try:
+            for pos0, parent, tokens, want in wants:
+                for a, b in zip(kc + vc, k0 + v0):
+                    a.copy_(b)
+                state.copy_(_state(torch, dev, pos0, parent, tokens))
+                lg_d.fill_(0.0)
+                res.fill_(-5)
+                torch.cuda.synchronize()
+                graph.launch()
+                assert m.sync() == 0
+                assert np.array_equal(lg_d.cpu().numpy(), want[0])
+                assert np.array_equal(res.cpu().numpy(), want[1])
+                for t, w in zip(kc + vc, want[2]):
+                    assert np.array_equal(t.cpu().numpy(), w)
+        finally:
+            graph.close()
+    finally:
+        m.close()
+
+
+def test_invalid_device_state_is_reported_and_touches_nothing():
+    """A state with a cycle in the parent array, a pos0 past the cache or an
+    out-of-range token id: the kernels' own checks reject it (MSM_ERR_INVALID_ARG at
+    the next sync), no cache row or output changes, and the next valid step is exact."""
+    torch = _torch()
+    import moe_decode_megakernel_warp_gb300 as msm
+    case, m = _model("cfg1_stack")
+    try:
+        cfg = case.cfg
+        dev = torch.device("cuda", 0)
+        kc = [torch.from_numpy(k.view(np.int16)).to(dev) for k, _ in case.kv]
+        vc = [torch.from_numpy(v.view(np.int16)).to(dev) for _, v in case.kv]
+        k0 = [t.cpu().numpy().copy() for t in kc + vc]
+        hid = torch.from_numpy(case.hidden.view(np.int16)).to(dev)
+        lg_d = torch.full((T, cfg.vocab), 3.0, dtype=torch.float32, device=dev)
+        res = torch.zeros((msm.MSM_ACCEPT_RESULT_INTS,), dtype=torch.int32, device=dev)
+        parent = [int(x) for x in case.parent]
+        good_tokens = [1] * T
+        cyc = list(parent)
+        cyc[3] = 5  # not a parent below 3: a cycle 3 -> 5 -> ... is possible
+        bad = [(cfg.pos0, cyc, good_tokens), (cfg.max_ctx - T + 1, parent, good_tokens), (-1, parent, good_tokens)]
+        for pos0, par, tok in bad:
+            state = _state(torch, dev, pos0, par, tok)
+            m.verify_step_dev(hid, state, kc, vc, logits_out=lg_d)
+            assert m.sync() == msm.MSM_ERR_INVALID_ARG
+            assert "state" in msm.msm_last_error()
+            assert np.all(lg_d.cpu().numpy() == 3.0)
+            for t, w in zip(kc + vc, k0):
+                assert np.array_equal(t.cpu().numpy(), w)
+        # accept with a token id outside the vocabulary
+        tok = list(good_tokens)
+        tok[5] = cfg.vocab
+        state = _state(torch, dev, cfg.pos0, parent, tok)
+        m.accept_dev(lg_d, state, kc, vc, res)
+        assert m.sync() == msm.MSM_ERR_INVALID_ARG
+        r = res.cpu().numpy()
+        assert r[0] == 0 and r[1] == -1 and np.all(r[2:2 + T] == -1)
+        for t, w in zip(kc + vc, k0):
+            assert np.array_equal(t.cpu().numpy(), w)
+        # the model still computes the exact step afterwards
+        state = _state(torch, dev, cfg.pos0, parent, good_tokens)
+        m.verify_step_dev(hid, state, kc, vc, logits_out=lg_d)
+        assert m.sync() == 0
+        got = lg_d.cpu().numpy().copy()
+        for t, w in zip(kc + vc, k0):
+            t.copy_(torch.from_numpy(w).to(dev))
+        m.verify_step(hid, parent, cfg.pos0, kc, vc, logits_out=lg_d)
+        assert m.sync() == 0
+        assert np.array_equal(got, lg_d.cpu().numpy())
+    finally:
+        m.close()
