@@ -377,3 +377,40 @@ def test_invalid_device_state_is_reported_and_touches_nothing():
         assert np.array_equal(got, lg_d.cpu().numpy())
     finally:
         m.close()
+
+
+def test_accept_with_more_layers_than_one_launch_carries():
+    """70 layers: the compaction runs as two walk launches (64 layers' cache pointers
+    per launch); every layer's caches must match the oracle."""
+    import dataclasses
+    torch = _torch()
+    import moe_decode_megakernel_warp_gb300 as msm
+    base = synth.CONFIGS["cfg1_stack"]
+    cfg = dataclasses.replace(base, name="70-layer stack at tiny widths", n_layers=70, layer_global=(0, 1) * 35)
+    case = gpu_cases.make_case(cfg, seed=3)
+    dev = torch.device("cuda", 0)
+    layers_t = [synth.to_torch(w, dev) for w in case.layers]
+    m = msm.Model(cfg, layers_t, synth.to_torch(case.final, dev), device=0, flags=msm.MSM_FLAG_PDL)
+    del layers_t
+    try:
+        rng = np.random.default_rng(77)
+        parent = [-1] + list(range(T - 1))
+        lg, _ = planted(rng, cfg.vocab, parent)
+        g = acc.target_argmax(lg)
+        tokens = [0] + [int(g[i - 1]) for i in range(1, 10)] + [(int(g[i - 1]) + 1) % cfg.vocab for i in range(10, T)]
+        ks = [rng.integers(0, 2**16, (cfg.hkv, cfg.max_ctx, cfg.hd)).astype(np.uint16) for _ in range(cfg.n_layers)]
+        vs = [rng.integers(0, 2**16, (cfg.hkv, cfg.max_ctx, cfg.hd)).astype(np.uint16) for _ in range(cfg.n_layers)]
+        kc = [torch.from_numpy(k.view(np.int16)).to(dev) for k in ks]
+        vc = [torch.from_numpy(v.view(np.int16)).to(dev) for v in vs]
+        res = torch.zeros((msm.MSM_ACCEPT_RESULT_INTS,), dtype=torch.int32, device=dev)
+        m.accept(torch.from_numpy(lg).to(dev), tokens, parent, cfg.pos0, kc, vc, res)
+        assert m.sync() == 0
+        path, bonus, g2 = acc.greedy_accept(lg, tokens, parent)
+        assert len(path) == 10
+        check_result(res.cpu().numpy(), path, bonus, g2)
+        wk, wv = acc.compact_kv(ks, vs, cfg.pos0, path)
+        for l in range(cfg.n_layers):
+            assert np.array_equal(kc[l].cpu().numpy().view(np.uint16), wk[l])
+            assert np.array_equal(vc[l].cpu().numpy().view(np.uint16), wv[l])
+    finally:
+        m.close()
