@@ -129,3 +129,25 @@ def test_compaction_moves_accepted_rows_only():
     # an identity path (a chain accepted node by node) changes nothing
     ik, iv = acc.compact_kv(ks, vs, pos0, list(range(7)))
     assert all(np.array_equal(a, b) for a, b in itertools.chain(zip(ik, ks), zip(iv, vs)))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_bench_accept_tokens_plant_the_requested_depth(seed):
+    """bench.accept_tokens: the walk follows the first-child chain for `depth` nodes
+    (or the whole chain when it is shorter) and stops there."""
+    import bench
+    rng = np.random.default_rng(500 + seed)
+    parent = [-1] + [int(rng.integers(0, i)) for i in range(1, T)]
+    choice = rng.integers(0, 50, T)
+    lg = planted_logits(rng, choice, vocab=64)
+    depth = int(rng.integers(0, 9))
+    tokens, taken = bench.accept_tokens(choice, parent, depth)
+    tokens = [t % 64 for t in tokens]
+    path, _, _ = acc.greedy_accept(lg, tokens, parent)
+    assert len(path) == taken + 1 and taken <= depth
+    chain, cur = [0], 0
+    for c in range(1, T):
+        if parent[c] == cur:
+            chain.append(c)
+            cur = c
+    assert path == chain[:taken + 1]
