@@ -148,6 +148,8 @@ typedef struct {
   int cooperative;               /* 1 if launches are cooperative (co-residency guaranteed) */
   uint64_t packed_weight_bytes;  /* model-owned packed weights */
   uint64_t exchange_bytes;       /* model-owned exchange buffers */
+  int tma_act_staging;           /* 1 if dense activations are staged by tensor copies
+                                    (msm_verify_step / _dev), 0 if by plain loads */
 } msm_stats;
 
 /*

@@ -124,7 +124,8 @@ class MsmWeights(ctypes.Structure):
 class MsmStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "grid_blocks", "threads_per_block", "smem_bytes", "attn_splits", "launches_per_step", "cooperative")] + [
-        ("packed_weight_bytes", ctypes.c_uint64), ("exchange_bytes", ctypes.c_uint64)]
+        ("packed_weight_bytes", ctypes.c_uint64), ("exchange_bytes", ctypes.c_uint64),
+        ("tma_act_staging", ctypes.c_int)]
 
 
 _LIB = None

@@ -90,6 +90,9 @@ struct msm_model {
   uint16_t* io_in = nullptr;      // device staging of msm_verify_step_host
   uint16_t* io_hidden = nullptr;
   float* io_logits = nullptr;
+  CUtensorMap tma_act[2][5];  // dense activations of each exchange parity (ActMap order)
+  int act_box[5] = {0, 0, 0, 0, 0};
+  bool act_tma = false;
   uint64_t* accept_part = nullptr;  // msm_accept: argmax partial keys [16][G], then
   int32_t* accept_choice = nullptr; // the 16 greedy choices [16] and
   uint32_t* accept_ticket = nullptr;  // the last-block ticket (zero between calls)
@@ -354,6 +357,28 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
     CKM(m->alloc(&m->in_q[i], (uint64_t)T * dm.hq * dm.hd * 2));
     CKM(m->alloc(&m->in_h[i], (uint64_t)T * dm.d * 2));
   }
+  {
+    // tensor maps of the dense activations for staging by tensor copies; if the
+    // driver rejects one, every phase stages with plain loads instead
+    const uint64_t offs[5] = {xo.o, xo.h1, xo.u, xo.z, xo.h2};
+    const int ks[5] = {dm.hq * dm.hd, dm.d, dm.p, dm.p, dm.d};
+    bool ok = m->encode != nullptr;
+    for (int c = 0; c < 2 && ok; ++c)
+      for (int i = 0; i < 5 && ok; ++i) {
+        const int nblk = ks[i] / 64;
+        int nb = 8;
+        while (nblk % nb) nb >>= 1;
+        m->act_box[i] = nb;
+        cuuint64_t dims[3] = {64, (cuuint64_t)T, (cuuint64_t)nblk};
+        cuuint64_t strides[2] = {(cuuint64_t)ks[i] * 2, 128};
+        cuuint32_t box[3] = {64, (cuuint32_t)T, (cuuint32_t)nb};
+        cuuint32_t es[3] = {1, 1, 1};
+        ok = m->encode(&m->tma_act[c][i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, m->x[c] + offs[i], dims, strides,
+                       box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+      }
+    m->act_tma = ok;
+  }
   CKM(m->alloc(&m->rope, (uint64_t)T * (dm.hd / 2) * 2 * 4));
   CKM(m->alloc(&m->inv_freq, (uint64_t)(dm.hd / 2) * 8));
   {
@@ -506,6 +531,11 @@ msm_status enqueue_verify(msm_model* m, const void* hidden_in, const int32_t* pa
     P.vc_pf = P.vc_next;
     P.x_cur = m->x[c];
     P.x_next = m->x[c ^ 1];
+    P.act_tma = m->act_tma ? 1 : 0;
+    for (int i = 0; i < 5; ++i) {
+      P.tmap_act[i] = m->tma_act[c][i];
+      P.act_box[i] = m->act_box[i];
+    }
     P.in_q = m->in_q[c];
     P.in_h = m->in_h[c];
     P.out_q = m->in_q[c ^ 1];
@@ -641,6 +671,7 @@ msm_status msm_get_stats(const msm_model* m, msm_stats* out) {
   out->cooperative = 0;
   out->packed_weight_bytes = m->packed_bytes;
   out->exchange_bytes = 2 * m->xo.total + m->so.total;
+  out->tma_act_staging = m->act_tma ? 1 : 0;
   return MSM_OK;
 }
 

@@ -165,7 +165,14 @@ struct LaunchParams {
   // KV cache tensor maps of this layer: 3-D {hd, max_ctx, hkv}, 128-byte swizzle
   CUtensorMap tmap_k;
   CUtensorMap tmap_v;
+  // the five dense activations of this launch's exchange buffer (ActMap order) as
+  // 3-D tensor maps {64 columns, 16 rows, K / 64 blocks} with the 128-byte swizzle,
+  // which is the shared-memory activation layout; act_tma == 0: plain loads
+  CUtensorMap tmap_act[5];
+  int act_tma;
+  int act_box[5];  // 64-column blocks per copy
 };
+enum ActMap : int { ACT_O = 0, ACT_H1 = 1, ACT_U = 2, ACT_Z = 3, ACT_H2 = 4 };
 
 // packed sizes
 __host__ __device__ inline uint64_t dense_unit_bytes(int K) { return (uint64_t)K * 32; }  // 16 rows x K bf16

@@ -42,6 +42,7 @@ struct Smem {
   volatile int* abort;
   int* n_active;
   int* pos0;          // first tree row of this step (the launch parameter or the device state)
+  uint64_t* stage_bar;  // completion of the activation tensor copies
   uint32_t* anc;
   int32_t* tpos;
   int32_t* depth;
@@ -86,6 +87,7 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const LaunchParams& P) {
   s.red = reinterpret_cast<float*>(sm + 6080);
   s.slot_tile = reinterpret_cast<volatile uint32_t*>(sm + 6592);
   s.pos0 = reinterpret_cast<int*>(sm + 6640);
+  s.stage_bar = reinterpret_cast<uint64_t*>(sm + 6648);
   s.ring_state = reinterpret_cast<struct RunAhead*>(sm + kRingStateOff);
   s.dred = reinterpret_cast<float*>(sm + 8192);
   return s;
@@ -99,6 +101,7 @@ struct Ctx {
   Smem S;
   uint64_t deadline;
   int pos0;  // copy of *S.pos0
+  uint32_t stage_n = 0;  // activation stagings by tensor copies so far (stage_bar's phase)
   uint64_t next_abort_check = 0;
   int block;
 
@@ -625,23 +628,22 @@ __device__ bool await_phase(Worker& w, int i, int phase) {
   return w.ok;
 }
 
-// B-operand layout of a [16 tokens][K] activation: per 16-column k-step four 8x8
-// matrices m (tokens 0-7 | k 0-7, tokens 0-7 | k 8-15, tokens 8-15 | k 0-7,
-// tokens 8-15 | k 8-15), 16 bytes per matrix row.  Row r of matrix m of k-step ks
-// sits at slot r ^ act_sw(ks, m) of its 128-byte block, so that one token's
-// consecutive 16-byte chunks fall in different banks (ldmatrix still reads each
-// matrix as one 128-byte block).
-__device__ __forceinline__ uint32_t act_sw(int ks, int m) { return (uint32_t)((ks * 2 + m) & 7); }
-__device__ __forceinline__ uint32_t act_off(int t, int k) {
-  const int ks = k >> 4, m = ((t >> 3) << 1) + ((k >> 3) & 1);
-  return (uint32_t)ks * kKStepBytes + (uint32_t)m * 128u + ((((uint32_t)t & 7u) ^ act_sw(ks, m)) << 4);
+// B-operand layout of a [16 tokens][K] activation: blocks of 64 columns, each 16
+// rows (tokens) of 128 bytes; the 16-byte chunk c of row t sits at slot c ^ (t & 7)
+// of its row.  This is the tensor-memory-access 128-byte swizzle of a {64, 16} box,
+// and ldmatrix reads any 8x8 matrix (8 tokens, 8 columns) from 8 different bank
+// groups.
+constexpr uint32_t kActBlockBytes = 2048;  // 16 rows x 64 bf16 columns
+__device__ __forceinline__ uint32_t act_chunk(int t, int c) {  // c: 16-byte chunk (8 columns) of row t
+  return (uint32_t)(c >> 3) * kActBlockBytes + (uint32_t)t * 128u + ((((uint32_t)c & 7u) ^ ((uint32_t)t & 7u)) << 4);
 }
+__device__ __forceinline__ uint32_t act_off(int t, int k) { return act_chunk(t, k >> 3); }
 
 // Stage a [16][K] bf16 activation from global memory into the B layout, optionally
 // applying RMSNorm with `gain`.  cnt >= 0: wait for every block to publish that
 // phase counter first; else, with `poll`, poll each chunk's sentinels; else plain loads.
 __device__ bool stage_act(Worker& w, const uint16_t* src, int K, int cnt, bool poll, const uint16_t* gain,
-                                       float eps, int phase) {
+                                       float eps, int phase, int map = -1) {
   Ctx& cx = *w.cx;
   const int tid = w.cw * 32 + w.lane;
   const int t = tid >> 4, sub = tid & 15;
@@ -657,6 +659,37 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, int cnt, bool p
     for (int j = 0; j < 2; ++j)
       if (tid + j * kComputeThreads < nch) gpre[j] = ld_nc_v4_early(reinterpret_cast<const uint4*>(gain) + tid + j * kComputeThreads);
   }
+  if (map >= 0 && cx.P->act_tma && cnt >= 0 && !poll) {
+    // tensor copies of the whole [16][K] activation in the act layout: one thread
+    // issues them once every block has published the phase and every compute warp is
+    // done with the buffer (its generic accesses ordered before the copies' writes)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    await_phase(w, cnt, phase);
+    ok = w.ok;
+    if (tid == 0 && ok) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // the producers' stores, acquired above
+      const int nblk = K / 64, nb = cx.P->act_box[map];
+      mbar_expect_tx(cx.S.stage_bar, (uint32_t)K * 32u);
+      for (int z = 0; z < nblk; z += nb)
+        tma_load_3d(cx.S.act + (size_t)z * kActBlockBytes, &cx.P->tmap_act[map], 0, 0, z, cx.S.stage_bar);
+    }
+    const uint32_t par = cx.stage_n & 1u;
+    ++cx.stage_n;
+    if (ok) ok = wait_bar(cx, cx.S.stage_bar, par, phase);
+    if (ok && gain != nullptr) {
+      // the row's sum of squares in the order of the load path below (bitwise the same)
+#pragma unroll 4
+      for (int c = sub; c < nch; c += 16) {
+        const uint4 v = *reinterpret_cast<const uint4*>(cx.S.act + act_off(t, c * 8));
+        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 x2 = make_float2(__uint_as_float(wd[i] << 16), __uint_as_float(wd[i] & 0xFFFF0000u));
+          ss2 = __ffma2_rn(x2, x2, ss2);
+        }
+      }
+    }
+  } else {
   // every compute warp is done with the act buffer (and, with a counter, the producers are done)
   if (cnt >= 0) await_phase(w, cnt, phase);
   else cbar();
@@ -694,6 +727,7 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, int cnt, bool p
       }
       *reinterpret_cast<uint4*>(cx.S.act + act_off(t, c * 8)) = v[j];
     }
+  }
   }
   if (gain != nullptr && phase == PH_POOL) stamp_rt(*cx.P, EV_POOL_STAGED);
   ok = __all_sync(0xffffffffu, ok);
@@ -884,11 +918,13 @@ __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, 
   // loop index & 3.
   const int group = w.cw >> 2, wi = w.cw & 3;
   constexpr int kStepsPerWarp = kDenseTileSteps / 4;
+  // lane l addresses row l & 7 of matrix m = l >> 3 (tokens 8 (m >> 1) .., columns
+  // 8 (m & 1) .. of the k-step); k-step ks sits in 64-column block ks >> 2
   uint32_t act_lane[4];
 #pragma unroll
   for (int ii = 0; ii < 4; ++ii) {
-    const int m = w.lane >> 3;
-    act_lane[ii] = smem_u32(cx.S.act) + (uint32_t)m * 128u + ((((uint32_t)w.lane & 7u) ^ act_sw(ii, m)) << 4);
+    const int m = w.lane >> 3, t = (m >> 1) * 8 + (w.lane & 7);
+    act_lane[ii] = smem_u32(cx.S.act) + act_chunk(t, ii * 2 + (m & 1));
   }
   float* red = cx.S.dred;  // [8 warps][16 rows][16 tokens]
   const int tid = w.cw * 32 + w.lane;
@@ -932,7 +968,7 @@ __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, 
           if (i >= ke) break;
           uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
           ldsm_x4(wbase + i * kKStepBytes, a0, a1, a2, a3);
-          ldsm_x4(act_lane[ii & 3] + (k0 + i) * kKStepBytes, b0, b1, b2, b3);
+          ldsm_x4(act_lane[ii & 3] + (uint32_t)((k0 + i) >> 2) * kActBlockBytes, b0, b1, b2, b3);
           float(&c)[2][4] = (ii & 1) ? acc2 : acc;
           mma_bf16(c[0], a0, a1, a2, a3, b0, b1);
           mma_bf16(c[1], a0, a1, a2, a3, b2, b3);
@@ -1540,15 +1576,14 @@ __device__ __forceinline__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* 
   const int g = lane >> 2, q = lane & 3;
   const int mi = lane >> 3;
   float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  // B rows: token rows[nt] of matrix m; k-step & 3 is (2 h + (mi >> 1)) & 3 for h in {0, 1}
+  // B rows: token rows[nt]; matrix mi covers k-step 2 h + (mi >> 1) of the group and its
+  // columns 8 (mi & 1) ..; a group is one 64-column block of the activation
   uint32_t bro[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int t = rows[nt];
-    const int m = ((t >> 3) << 1) + (mi & 1);
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-      bro[nt][h] = act_s + (uint32_t)m * 128u + ((((uint32_t)t & 7u) ^ act_sw(2 * h + (mi >> 1), m)) << 4);
+    for (int h = 0; h < 2; ++h) bro[nt][h] = act_s + act_chunk(t, (2 * h + (mi >> 1)) * 2 + (mi & 1));
   }
   const uint8_t* gb0 = tbase + g0 * kExpGroupBytes;
   uint64_t ncg = *reinterpret_cast<const uint64_t*>(gb0 + g * 32 + q * 8);
@@ -1560,7 +1595,7 @@ __device__ __forceinline__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* 
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int h = 0; h < 2; ++h)
-      ldsm_x4(bro[nt][h] + (uint32_t)(g0 * 4 + 2 * h + (mi >> 1)) * kKStepBytes, nb[nt][h][0], nb[nt][h][1],
+      ldsm_x4(bro[nt][h] + (uint32_t)g0 * kActBlockBytes, nb[nt][h][0], nb[nt][h][1],
               nb[nt][h][2], nb[nt][h][3]);
   for (int gi = g0; gi < g1; ++gi) {
     const uint64_t cg = ncg, cg8 = ncg8;
@@ -1582,7 +1617,7 @@ __device__ __forceinline__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* 
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-          ldsm_x4(bro[nt][h] + (uint32_t)((gi + 1) * 4 + 2 * h + (mi >> 1)) * kKStepBytes, nb[nt][h][0],
+          ldsm_x4(bro[nt][h] + (uint32_t)(gi + 1) * kActBlockBytes, nb[nt][h][0],
                   nb[nt][h][1], nb[nt][h][2], nb[nt][h][3]);
     }
     uint32_t a[4][4];
@@ -1956,7 +1991,8 @@ __device__ void compute_main(Worker& w) {
   {
     const uint16_t* hprev = P.first ? P.hidden_in : P.in_h;
     uint16_t* h1 = reinterpret_cast<uint16_t*>(X + P.xo.h1);
-    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.o), dm.hq * dm.hd, CNT_MERGE, false, nullptr, 0.f, PH_OPROJ);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.o), dm.hq * dm.hd, CNT_MERGE, false, nullptr, 0.f, PH_OPROJ,
+              ACT_O);
     stamp<kTiming>(P, b, EV_OPROJ_IN);
     EpiArgs ea{};
     ea.kind = EPI_OPROJ;
@@ -1969,7 +2005,8 @@ __device__ void compute_main(Worker& w) {
   // a5: u = bf16(bf16(RMSNorm(h1)) W_pool^T)
   {
     uint16_t* uo = reinterpret_cast<uint16_t*>(X + P.xo.u);
-    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h1), dm.d, CNT_OPROJ, false, P.g_moe, dm.rms_eps, PH_POOL);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h1), dm.d, CNT_OPROJ, false, P.g_moe, dm.rms_eps, PH_POOL,
+              ACT_H1);
     stamp<kTiming>(P, b, EV_POOL_IN);
     EpiArgs ea{};
     ea.kind = EPI_POOL;
@@ -1981,7 +2018,7 @@ __device__ void compute_main(Worker& w) {
   // a6: router logits = u W_r^T + b (fp32)
   {
     float* lg = reinterpret_cast<float*>(X + P.xo.logits);
-    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.u), dm.p, CNT_POOL, false, nullptr, 0.f, PH_ROUTER);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.u), dm.p, CNT_POOL, false, nullptr, 0.f, PH_ROUTER, ACT_U);
     stamp<kTiming>(P, b, EV_ROUTER_IN);
     EpiArgs ea{};
     ea.kind = EPI_ROUTER;
@@ -2018,7 +2055,7 @@ __device__ void compute_main(Worker& w) {
     const uint16_t* h1 = reinterpret_cast<const uint16_t*>(X + P.xo.h1);
     uint16_t* h2 = reinterpret_cast<uint16_t*>(X + P.xo.h2);
     uint16_t* hnext = P.last ? P.hidden_out : P.out_h;
-    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.z), dm.p, CNT_COMBINE, false, nullptr, 0.f, PH_UNPOOL);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.z), dm.p, CNT_COMBINE, false, nullptr, 0.f, PH_UNPOOL, ACT_Z);
     stamp<kTiming>(P, b, EV_UNPOOL_IN);
     EpiArgs ea{};
     ea.kind = EPI_UNPOOL;
@@ -2032,14 +2069,16 @@ __device__ void compute_main(Worker& w) {
   pdl_launch_dependents();
   // a12: next layer's RMSNorm + QKV + RoPE + KV write; a12': final norm + LM head
   if (!P.last) {
-    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h2), dm.d, CNT_UNPOOL, false, P.g_tail, dm.rms_eps, PH_TAIL);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h2), dm.d, CNT_UNPOOL, false, P.g_tail, dm.rms_eps, PH_TAIL,
+              ACT_H2);
     stamp<kTiming>(P, b, EV_TAIL_IN);
     EpiArgs ea{};
     ea.kind = EPI_QKV;
     ea.dq = QkvDst{P.out_q, false, P.kc_next, P.vc_next, nullptr};
     dense_phase(w, dm.d, dm.nqkv, P.phase_rot * 9, ea, -1);
   } else if (dm.vocab > 0) {
-    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h2), dm.d, CNT_UNPOOL, false, P.g_tail, dm.rms_eps, PH_TAIL);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.h2), dm.d, CNT_UNPOOL, false, P.g_tail, dm.rms_eps, PH_TAIL,
+              ACT_H2);
     stamp<kTiming>(P, b, EV_TAIL_IN);
     EpiArgs ea{};
     ea.kind = EPI_LMHEAD;
@@ -2067,6 +2106,7 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
       mbar_init(&cx.S.empty[i], kComputeWarps);
     }
     mbar_init(cx.S.route_bar, 1);
+    mbar_init(cx.S.stage_bar, 1);
     for (int i = 0; i < kSlots; ++i) cx.S.slot_tile[i] = 0xFFFFFFFFu;
     *cx.S.abort = (smem_u32(smem) & 1023u) != 0u;  // the swizzled tiles need 1 KB alignment
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
