@@ -314,7 +314,9 @@ msm_status msm_get_exchange(msm_model* model, const char* name, void* host, size
  * Compaction: for j < a, cache row pos0 + j of every layer, K and V, every KV head
  * receives row pos0 + path[j]; no other row is written.  Everything runs on the
  * device (two launches on `stream`, no host round trip), so a stream capture
- * records it.  Errors: MSM_ERR_UNSUPPORTED when vocab == 0, MSM_ERR_INVALID_ARG
+ * records it.  It uses model-owned scratch (argmax partials, a ticket counter), so
+ * accept calls of one model must not overlap on the GPU, like its steps.
+ * Errors: MSM_ERR_UNSUPPORTED when vocab == 0, MSM_ERR_INVALID_ARG
  * for NULL or misaligned buffers, an invalid parent array, token ids or pos0;
  * nothing is enqueued then.
  */

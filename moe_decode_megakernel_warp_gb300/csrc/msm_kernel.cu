@@ -666,7 +666,8 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, int cnt, bool p
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     await_phase(w, cnt, phase);
     ok = w.ok;
-    if (tid == 0 && ok) {
+    const bool issuer = tid == 0 && ok;
+    if (issuer) {
       asm volatile("fence.proxy.async.global;" ::: "memory");  // the producers' stores, acquired above
       const int nblk = K / 64, nb = cx.P->act_box[map];
       mbar_expect_tx(cx.S.stage_bar, (uint32_t)K * 32u);
@@ -676,6 +677,12 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, int cnt, bool p
     const uint32_t par = cx.stage_n & 1u;
     ++cx.stage_n;
     if (ok) ok = wait_bar(cx, cx.S.stage_bar, par, phase);
+    if (issuer && !ok) {
+      // the block gives up (another block failed): the copies read valid memory and
+      // land within microseconds, but must land before this block may exit
+      for (uint32_t n = 0; n < (1u << 24) && !mbar_try_wait(cx.S.stage_bar, par); ++n) {
+      }
+    }
     if (ok && gain != nullptr) {
       // the row's sum of squares in the order of the load path below (bitwise the same)
 #pragma unroll 4
