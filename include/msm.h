@@ -327,8 +327,9 @@ msm_status msm_accept(msm_model* model, const float* logits, const int32_t* toke
 /*
  * One CUDA graph per decode step (alphasignal.ai, § "Draft and verify share one
  * graph"; orcarouter.ai, closing figure): msm_graph_create captures the arming of
- * the model's exchange buffers, the verify step's n_layers launches and, if
- * accept_result is not NULL, msm_accept's launches, and instantiates the graph.
+ * the model's exchange buffers, the verify step's n_layers launches, if
+ * accept_result is not NULL msm_accept's launches, and a second arming (so eager
+ * steps and replays may be mixed freely), and instantiates the graph.
  * Arguments are those of msm_verify_step and msm_accept; the tree, the tokens and
  * pos0 are recorded in the graph, as are all buffer addresses, so a replay reads
  * the buffers' current contents at those addresses.  msm_graph_launch replays it

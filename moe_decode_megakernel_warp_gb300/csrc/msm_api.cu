@@ -800,13 +800,21 @@ msm_status capture_step(msm_model* m, const void* hidden_in, const int32_t* pare
     cudaStreamDestroy(cs);
     return cuda_fail(e, "cudaStreamBeginCapture");
   }
-  // the graph arms the exchange buffers itself, so a replay never depends on the
-  // state an earlier step (eager or replayed) left behind
+  // the graph arms both parities of the exchange buffers before its launches and
+  // again after them, so a replay neither depends on nor leaves behind state that
+  // an eager step of either launch parity (odd layer counts) could trip over
+  const uint64_t launches0 = m->launch_count, steps0 = m->step_count;
   msm_status st = rearm_all(m, cs);
   if (st == MSM_OK)
     st = enqueue_verify(m, hidden_in, parent, pos0, state, k_cache, v_cache, logits_out, hidden_out, cs);
   if (st == MSM_OK && accept_result)
     st = enqueue_accept(m, logits_out, tokens, parent, pos0, state, k_cache, v_cache, accept_result, cs);
+  if (st == MSM_OK) st = rearm_all(m, cs);
+  if (st != MSM_OK) {
+    // nothing recorded will run: the model's launch parity stays where it was
+    m->launch_count = launches0;
+    m->step_count = steps0;
+  }
   std::string msg = st == MSM_OK ? std::string() : std::string(msm_last_error());
   cudaGraph_t graph = nullptr;
   e = cudaStreamEndCapture(cs, &graph);

@@ -414,3 +414,39 @@ def test_accept_with_more_layers_than_one_launch_carries():
             assert np.array_equal(vc[l].cpu().numpy().view(np.uint16), wv[l])
     finally:
         m.close()
+
+
+def test_graph_replays_and_eager_steps_mix_with_an_odd_layer_count():
+    """Three layers: every launch flips the exchange-buffer parity, so after a replay
+    an eager step starts on the other parity; results must not change."""
+    import dataclasses
+    torch = _torch()
+    import moe_decode_megakernel_warp_gb300 as msm
+    base = synth.CONFIGS["cfg1_stack"]
+    cfg = dataclasses.replace(base, name="3-layer stack at tiny widths", n_layers=3, layer_global=(0, 1, 0))
+    case = gpu_cases.make_case(cfg, seed=4)
+    dev = torch.device("cuda", 0)
+    m = msm.Model(cfg, [synth.to_torch(w, dev) for w in case.layers], synth.to_torch(case.final, dev), device=0,
+                  flags=msm.MSM_FLAG_PDL)
+    try:
+        kc = [torch.from_numpy(k.view(np.int16)).to(dev) for k, _ in case.kv]
+        vc = [torch.from_numpy(v.view(np.int16)).to(dev) for _, v in case.kv]
+        hid = torch.from_numpy(case.hidden.view(np.int16)).to(dev)
+        lg = torch.empty((T, cfg.vocab), dtype=torch.float32, device=dev)
+        m.verify_step(hid, case.parent, case.pos0, kc, vc, logits_out=lg)
+        assert m.sync() == 0
+        want = lg.cpu().numpy().copy()
+        graph = m.graph(hid, case.parent, case.pos0, kc, vc, logits_out=lg)
+        try:
+            for run in ("eager", "graph", "eager", "graph", "eager", "eager"):
+                lg.fill_(0.0)
+                if run == "graph":
+                    graph.launch()
+                else:
+                    m.verify_step(hid, case.parent, case.pos0, kc, vc, logits_out=lg)
+                assert m.sync() == 0, run
+                assert np.array_equal(lg.cpu().numpy(), want), run
+        finally:
+            graph.close()
+    finally:
+        m.close()
