@@ -802,7 +802,8 @@ msm_status capture_step(msm_model* m, const void* hidden_in, const int32_t* pare
   }
   // the graph arms both parities of the exchange buffers before its launches and
   // again after them, so a replay neither depends on nor leaves behind state that
-  // an eager step of either launch parity (odd layer counts) could trip over
+  // an eager step of either launch parity (odd layer counts) could trip over; the
+  // capture leaves the model's launch counters as they were
   const uint64_t launches0 = m->launch_count, steps0 = m->step_count;
   msm_status st = rearm_all(m, cs);
   if (st == MSM_OK)
@@ -810,11 +811,10 @@ msm_status capture_step(msm_model* m, const void* hidden_in, const int32_t* pare
   if (st == MSM_OK && accept_result)
     st = enqueue_accept(m, logits_out, tokens, parent, pos0, state, k_cache, v_cache, accept_result, cs);
   if (st == MSM_OK) st = rearm_all(m, cs);
-  if (st != MSM_OK) {
-    // nothing recorded will run: the model's launch parity stays where it was
-    m->launch_count = launches0;
-    m->step_count = steps0;
-  }
+  // recording runs nothing: the model's launch parity must keep following the
+  // launches that did run (a replay arms both parities, so it needs no count)
+  m->launch_count = launches0;
+  m->step_count = steps0;
   std::string msg = st == MSM_OK ? std::string() : std::string(msm_last_error());
   cudaGraph_t graph = nullptr;
   e = cudaStreamEndCapture(cs, &graph);
