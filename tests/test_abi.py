@@ -41,6 +41,18 @@ def test_null_arguments_are_rejected_without_a_device():
     assert msm.msm_graph_launch(None) == msm.MSM_ERR_INVALID_ARG
     assert msm.msm_verify_step_dev(None, 0, 0, [0], [0], 0, 0) == msm.MSM_ERR_INVALID_ARG
     assert msm.msm_accept_dev(None, 0, 0, [0], [0], 0) == msm.MSM_ERR_INVALID_ARG
+    g = ctypes.c_void_p(123)
+    par = (ctypes.c_int32 * 16)(*range(-1, 15))
+    tok = (ctypes.c_int32 * 16)()
+    kp = (ctypes.c_void_p * 1)()
+    assert lib.msm_graph_create(None, None, par, tok, 0, kp, kp, None, None, None, ctypes.byref(g)) == \
+        msm.MSM_ERR_INVALID_ARG
+    assert g.value is None  # *out cleared on failure
+    g = ctypes.c_void_p(123)
+    assert lib.msm_graph_create_dev(None, None, None, kp, kp, None, None, None, ctypes.byref(g)) == \
+        msm.MSM_ERR_INVALID_ARG
+    assert g.value is None and "state" in msm.msm_last_error()
+    assert lib.msm_graph_create(None, None, par, tok, 0, kp, kp, None, None, None, None) == msm.MSM_ERR_INVALID_ARG
     msm.msm_graph_destroy(None)
 
 
