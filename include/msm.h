@@ -78,7 +78,7 @@ typedef enum {
   MSM_ERR_CUDA = 2,           /* a CUDA runtime call failed (see msm_last_error) */
   MSM_ERR_OOM = 3,            /* device allocation failed */
   MSM_ERR_DEVICE_TIMEOUT = 4, /* a bounded in-kernel wait expired */
-  MSM_ERR_UNSUPPORTED = 5     /* widths / features this build does not implement */
+  MSM_ERR_UNSUPPORTED = 5     /* widths / features this library does not implement */
 } msm_status;
 
 /* msm_config.flags */
