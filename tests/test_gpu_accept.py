@@ -450,3 +450,40 @@ def test_graph_replays_and_eager_steps_mix_with_an_odd_layer_count():
             graph.close()
     finally:
         m.close()
+
+
+def test_device_state_path_at_full_size():
+    """The 62-layer workload as the bench builds it: msm_verify_step_dev and a replay of
+    the device-state graph give the host-parameter step's logits bit for bit."""
+    torch = _torch()
+    import bench
+    import moe_decode_megakernel_warp_gb300 as msm
+    cfg = synth.CONFIGS["cfg4"]
+    s = synth.parity_seeds("cfg4")
+    dev = torch.device("cuda", 0)
+    m = bench.build_model(cfg, s["seed"], s["bias_seeds"], dev, 0, msm.MSM_FLAG_PDL)
+    try:
+        kv = [synth.gpu_kv_history(cfg, s["seed"], l, device=dev) for l in range(cfg.n_layers)]
+        kc, vc = [k for k, _ in kv], [v for _, v in kv]
+        hid = torch.from_numpy(synth.hidden_in(cfg, s["seed"]).view(np.int16)).to(dev)
+        parent = [int(x) for x in synth.parent_array(s["seed"])]
+        lg = torch.empty((T, cfg.vocab), dtype=torch.float32, device=dev)
+        m.verify_step(hid, parent, cfg.pos0, kc, vc, logits_out=lg)
+        assert m.sync() == 0
+        want = lg.cpu().numpy().copy()
+        state = _state(torch, dev, cfg.pos0, parent, [0] * T)
+        lg.fill_(0.0)
+        m.verify_step_dev(hid, state, kc, vc, logits_out=lg)
+        assert m.sync() == 0
+        assert np.array_equal(lg.cpu().numpy(), want)
+        graph = m.graph_dev(hid, state, kc, vc, logits_out=lg)
+        try:
+            lg.fill_(0.0)
+            torch.cuda.synchronize()
+            graph.launch()
+            assert m.sync() == 0
+            assert np.array_equal(lg.cpu().numpy(), want)
+        finally:
+            graph.close()
+    finally:
+        m.close()
