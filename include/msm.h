@@ -150,6 +150,9 @@ typedef struct {
   uint64_t exchange_bytes;       /* model-owned exchange buffers */
   int tma_act_staging;           /* 1 if dense activations are staged by tensor copies
                                     (msm_verify_step / _dev), 0 if by plain loads */
+  uint64_t launches_run;         /* layer-kernel launches enqueued so far by every verify
+                                    entry point (a graph capture records, not runs) */
+  uint64_t noalloc_scratch_bytes;  /* static scratch one msm_verify_step_noalloc call needs */
 } msm_stats;
 
 /*
@@ -213,18 +216,21 @@ msm_status msm_verify_step_host(msm_model* model, const void* hidden_in_host,
  *
  * Scratch: MSM_NOALLOC_SCRATCH_BYTES (10 MiB) of __device__ memory per device,
  * shared by every model on that device.  A step needs
- *   2 * exchange + attention/expert partials + 2 * (16 n_q_heads head_dim * 2)
- *   + 2 * (16 d_model * 2) bytes (each part rounded up to 256 bytes), about
- * 8.2 MiB at d_model 4096, 32/8 heads of 128, pool_dim 2048, ffn_dim 1024,
- * top-8 on 152 SMs.  A model whose step needs more is rejected with
- * MSM_ERR_UNSUPPORTED and a message giving both sizes; nothing is launched.
+ *   2 * (exchange buffers + 256 bytes of phase counters) + attention/expert
+ *   partials + 2 * (16 n_q_heads head_dim * 2) + 2 * (16 d_model * 2) bytes
+ * (each part rounded up to 256 bytes), about 8.2 MiB at d_model 4096, 32/8
+ * heads of 128, pool_dim 2048, ffn_dim 1024, top-8 on 152 SMs; the exact
+ * figure of a model is msm_stats.noalloc_scratch_bytes.  A model whose step
+ * needs more is rejected with MSM_ERR_UNSUPPORTED and a message giving both
+ * sizes; nothing is launched.
  * The exchange part must hold its empty sentinels when a step starts; every
  * call arms it on `stream` before its first layer launch, so no state carries
  * over from an earlier call, a failed step or another model.
  *
- * Set-up: the first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current).  Make that first call
- * before any stream capture is begun on the calling thread.
+ * Set-up: msm_model_create looks up the array's device address
+ * (cudaGetSymbolAddress, with the model's device current), which loads the code
+ * module that holds the array and so gives the array its device memory then, at
+ * creation, not at the first call; the calls themselves do no set-up.
  *
  * Concurrency: the scratch is one array per device.  Calls that overlap on the
  * device (from other threads, or on other streams of the same device before the
@@ -277,7 +283,7 @@ msm_status msm_get_tree(msm_model* model, uint32_t* anc, int32_t* tpos);
  *   counter that releases the split merge, o_proj, pooler, router, top-k, combine,
  *   unpooler and tail reach the grid size.
  * `n` is the capacity of `buf` in elements. */
-#define MSM_TIMING_EVENTS 64
+#define MSM_TIMING_EVENTS 192
 msm_status msm_get_timing(msm_model* model, uint64_t* buf, size_t n);
 
 msm_status msm_get_stats(const msm_model* model, msm_stats* out);

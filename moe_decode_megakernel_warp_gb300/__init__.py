@@ -33,7 +33,7 @@ MSM_FLAG_EXPERT_PREFETCH = 0x2
 MSM_FLAG_KV_PREFETCH = 0x4
 MSM_FLAG_PDL = 0x8
 MSM_FLAG_TEST_DROP_HANDOFF = 0x10000
-MSM_TIMING_EVENTS = 64
+MSM_TIMING_EVENTS = 192
 # entries of msm_accept's result buffer (MSM_ACCEPT_RESULT_INTS)
 MSM_ACCEPT_RESULT_INTS = 34
 # entries of the device-resident step state (MSM_STEP_STATE_INTS): pos0, parent[16], tokens[16], spare
@@ -49,7 +49,12 @@ EV = dict(start=0, pro_in=1, pro_done=2, attn_in=3, attn_done=4, merge_done=5, o
           ld_op_first=44, ld_op_last=45, ld_g1_first=46, ld_g1_last=47,
           g2_first_ready=48, g2_first_done=49, g2_last_ready=50, g2_last_done=51, g2_stage2_in=52,
           g2_stage2_done=53, ld_op_u1=54, seen_merge=55, seen_oproj=56, seen_pool=57, seen_router=58,
-          seen_route=59, seen_combine=60, seen_unpool=61, seen_tail=62)
+          seen_route=59, seen_combine=60, seen_unpool=61, seen_tail=62,
+          **{"tc_g1_ready%d" % i: 64 + i for i in range(16)}, **{"tc_g1_issued%d" % i: 80 + i for i in range(16)},
+          **{"wg_g1_landed%d" % i: 96 + i for i in range(16)}, **{"tc_g2_ready%d" % i: 112 + i for i in range(8)},
+          **{"tc_g2_issued%d" % i: 120 + i for i in range(8)},
+          **{"ld_g1_issued%d" % i: 128 + i for i in range(16)}, ld_ring_grown=144,
+          **{"ld_g1_next%d" % i: 160 + i for i in range(16)}, **{"ld_g1_placed%d" % i: 176 + i for i in range(16)})
 T = 16
 
 EXPORTED = ["msm_model_create", "msm_model_destroy", "msm_verify_step", "msm_verify_step_host", "msm_sync",
@@ -125,7 +130,8 @@ class MsmStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "grid_blocks", "threads_per_block", "smem_bytes", "attn_splits", "launches_per_step", "cooperative")] + [
         ("packed_weight_bytes", ctypes.c_uint64), ("exchange_bytes", ctypes.c_uint64),
-        ("tma_act_staging", ctypes.c_int)]
+        ("tma_act_staging", ctypes.c_int), ("launches_run", ctypes.c_uint64),
+        ("noalloc_scratch_bytes", ctypes.c_uint64)]
 
 
 _LIB = None

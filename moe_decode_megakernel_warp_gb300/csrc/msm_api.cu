@@ -63,6 +63,7 @@ struct msm_model {
   Dims dm{};
   std::vector<uint8_t> global;
   int G = 0, ring_bytes = 0, act_bytes = 0, smem_bytes = 0;
+  int g1_u_off = 0, g1_x_off = 0, g2_off = 0, ring_ext = 0;
   std::vector<LayerPack> L;
   uint8_t* lm = nullptr;
   uint16_t* g_final = nullptr;
@@ -93,6 +94,15 @@ struct msm_model {
   CUtensorMap tma_act[2][5];  // dense activations of each exchange parity (ActMap order)
   int act_box[5] = {0, 0, 0, 0, 0};
   bool act_tma = false;
+  // msm_verify_step_noalloc: device address of the static scratch array (looked up at
+  // creation, which also loads the module that holds it), the bytes one step needs
+  // there, and the activation tensor maps of its two exchange parities
+  unsigned char* noalloc = nullptr;
+  uint64_t noalloc_need = 0;
+  CUtensorMap tma_act_na[2][5];
+  bool act_tma_na = false;
+  uint64_t launches_run = 0;   // launches enqueued by every verify entry point
+  uint8_t* last_x = nullptr;   // exchange buffer of the last launch enqueued
   uint64_t* accept_part = nullptr;  // msm_accept: argmax partial keys [16][G], then
   int32_t* accept_choice = nullptr; // the 16 greedy choices [16] and
   uint32_t* accept_ticket = nullptr;  // the last-block ticket (zero between calls)
@@ -123,6 +133,9 @@ msm_status validate_config(const msm_config* c) {
     return fail(MSM_ERR_UNSUPPORTED, "n_q_heads / n_kv_heads must be 1, 2, 4 or 8");
   if (c->d_model % 64 || c->pool_dim % 64 || c->ffn_dim % 64 || (c->n_q_heads * c->head_dim) % 64)
     return fail(MSM_ERR_UNSUPPORTED, "d_model, pool_dim, ffn_dim, n_q_heads*head_dim must be multiples of 64");
+  if (c->pool_dim % kExpBlockK || c->ffn_dim % kExpBlockK)
+    return fail(MSM_ERR_UNSUPPORTED, "pool_dim and ffn_dim must be multiples of 256 (expert tensor-core tiles)");
+  if (c->ffn_dim > 1024) return fail(MSM_ERR_UNSUPPORTED, "ffn_dim > 1024 (activation scales in tensor memory)");
   if (c->top_k > kMaxTopK) return fail(MSM_ERR_UNSUPPORTED, "top_k > 8");
   if (c->n_experts > kMaxExperts || c->n_experts % 16) return fail(MSM_ERR_UNSUPPORTED, "n_experts must be <= 256 and a multiple of 16");
   if (c->vocab % 16) return fail(MSM_ERR_UNSUPPORTED, "vocab must be a multiple of 16");
@@ -162,6 +175,35 @@ msm_status arm_exchange(uint8_t* x, const XOffsets& o, cudaStream_t s) {
   return MSM_OK;
 }
 
+// tensor maps of the five dense activations of one exchange buffer (ActMap order);
+// false if the driver rejects one (the kernel then stages with plain loads)
+bool encode_act_maps(msm_model* m, uint8_t* x, CUtensorMap* maps) {
+  const Dims& dm = m->dm;
+  const XOffsets& xo = m->xo;
+  const uint64_t offs[5] = {xo.o, xo.h1, xo.u, xo.z, xo.h2};
+  const int ks[5] = {dm.hq * dm.hd, dm.d, dm.p, dm.p, dm.d};
+  if (!m->encode) return false;
+  for (int i = 0; i < 5; ++i) {
+    const int nblk = ks[i] / 64;
+    int nb = 8;
+    while (nblk % nb) nb >>= 1;
+    m->act_box[i] = nb;
+    cuuint64_t dims[3] = {64, (cuuint64_t)T, (cuuint64_t)nblk};
+    cuuint64_t strides[2] = {(cuuint64_t)ks[i] * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)T, (cuuint32_t)nb};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (m->encode(&maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x + offs[i], dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
+// device address of the static scratch array on the current device (defined with the
+// array, at the end of this file)
+msm_status noalloc_lookup(unsigned char** base);
+
 msm_status rearm_all(msm_model* m, cudaStream_t s) {
   for (int c = 0; c < 2; ++c) {
     msm_status st = arm_exchange(m->x[c], m->xo, s);
@@ -195,6 +237,10 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
         !w->w2_codes[l] || !w->w2_scales[l] || !w->w2_tensor_scale[l])
       return fail(MSM_ERR_INVALID_ARG, "weights: NULL pointer for layer " + std::to_string(l));
   if (c.vocab > 0 && (!w->norm_final || !w->w_lm)) return fail(MSM_ERR_INVALID_ARG, "vocab > 0 needs norm_final and w_lm");
+  for (int l = 0; l < c.n_layers; ++l)
+    if ((reinterpret_cast<uintptr_t>(w->w1_codes[l]) | reinterpret_cast<uintptr_t>(w->w1_scales[l]) |
+         reinterpret_cast<uintptr_t>(w->w2_codes[l]) | reinterpret_cast<uintptr_t>(w->w2_scales[l])) & 15)
+      return fail(MSM_ERR_INVALID_ARG, "weights: NVFP4 codes and scales must be 16-byte aligned (layer " + std::to_string(l) + ")");
 
   int ndev = 0;
   CK(cudaGetDeviceCount(&ndev));
@@ -226,7 +272,7 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   {
     // the kernel splits work units over the grid in 32-bit arithmetic
     const uint64_t units = std::max({(uint64_t)dm.vocab / 16, (uint64_t)dm.nqkv / 16, (uint64_t)dm.d / 16,
-                                     (uint64_t)std::min(dm.e, T * dm.k) * std::max(dm.f / 8, dm.p / 16)});
+                                     (uint64_t)std::min(dm.e, T * dm.k) * std::max(w1_units(dm.f), w2_units(dm.p))});
     if (units * (uint64_t)(m->G + 1) >= (1ull << 32)) {
       delete m;
       return fail(MSM_ERR_UNSUPPORTED, "too many work units per phase for the grid split");
@@ -242,23 +288,32 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   const uint64_t attn_need = (uint64_t)dm.group * (D / 16) * kKStepBytes + 2ull * 16 * D * 2 +
                              (uint64_t)dm.group * dm.attn_wph * 32 * (4 + D / 2) * 4;
   const uint64_t kmax = (uint64_t)std::max(std::max(dm.d, dm.hq * dm.hd), dm.p);
-  // GEMM1: the 16 tokens' pooled vectors; GEMM2: two experts' a_q + one fp32 row per warp
-  const uint64_t g1_need = (uint64_t)dm.p * 32;
-  const uint64_t g2_need = 2ull * dm.f * 32 + (uint64_t)kComputeWarps * dm.f * 4;
+  // GEMM1: the 16 tokens' pooled vectors (f16) + the epilogue exchange rows of both
+  // warp groups; GEMM2: two experts' NVFP4 rows (E2M1 + scales) + one fp32 row per warp
+  // (both at the top of the buffer; the router stages the bf16 pooled vectors at its
+  // bottom, and routing converts them into the top: the two must not overlap)
+  const uint64_t g1_need = (uint64_t)dm.p * 32 + 2ull * 128 * 17 * 4;
+  const uint64_t g2_need = ((18ull * dm.f + 1023) & ~1023ull) + (uint64_t)kComputeWarps * dm.f * 4;
   uint64_t act = std::max(std::max(kmax * 32, g1_need), std::max(g2_need, attn_need));
+  act = std::max(act, (uint64_t)dm.p * 64);
   act = (act + 1023) & ~uint64_t(1023);
+  const uint64_t expert_top = (std::max(g1_need, g2_need) + 1023) & ~uint64_t(1023);
   const int smem_cap = std::min(kMaxSmem, smem_optin);
   long long ring = (long long)smem_cap - (long long)act - kSmallBytes;
   ring &= ~1023ll;
   const uint64_t max_tile =
-      std::max(std::max((uint64_t)kDenseTileSteps * kKStepBytes, exp_unit_bytes(dm.p)),
-               std::max(exp_unit_bytes(dm.f), (uint64_t)dm.attn_rows * D * 4));
+      std::max(std::max((uint64_t)kDenseTileSteps * kKStepBytes, (uint64_t)std::max(exp_tile_bytes(dm.p), exp_tile_bytes(dm.f))),
+               (uint64_t)dm.attn_rows * D * 4);
   if (ring < (long long)(2 * max_tile)) {
     delete m;
     return fail(MSM_ERR_UNSUPPORTED, "widths too large for the shared-memory budget");
   }
   m->act_bytes = (int)act;
   m->ring_bytes = (int)ring;
+  m->g1_u_off = (int)(act - (uint64_t)dm.p * 32);
+  m->g1_x_off = (int)(act - g1_need);
+  m->g2_off = (int)(act - ((g2_need + 1023) & ~uint64_t(1023)));
+  m->ring_ext = (int)((act - expert_top) & ~uint64_t(1023));
   m->smem_bytes = (int)(ring + act + kSmallBytes);
 
   auto bail = [&](msm_status s2) {
@@ -287,7 +342,7 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   // ---- pack weights ----
   cudaStream_t s = m->aux;
   m->L.resize(c.n_layers);
-  const int u1pe = dm.f / 8, u2pe = dm.p / 16;
+  const int u1pe = w1_units(dm.f), u2pe = w2_units(dm.p);
   for (int l = 0; l < c.n_layers; ++l) {
     LayerPack& lp = m->L[l];
     const uint64_t b_qkv = (dm.nqkv / 16) * dense_unit_bytes(dm.d), b_o = (dm.d / 16) * dense_unit_bytes(dm.hq * dm.hd),
@@ -357,27 +412,20 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
     CKM(m->alloc(&m->in_q[i], (uint64_t)T * dm.hq * dm.hd * 2));
     CKM(m->alloc(&m->in_h[i], (uint64_t)T * dm.d * 2));
   }
+  // tensor maps of the dense activations for staging by tensor copies; if the driver
+  // rejects one, every phase stages with plain loads instead
+  m->act_tma = encode_act_maps(m, m->x[0], m->tma_act[0]) && encode_act_maps(m, m->x[1], m->tma_act[1]);
   {
-    // tensor maps of the dense activations for staging by tensor copies; if the
-    // driver rejects one, every phase stages with plain loads instead
-    const uint64_t offs[5] = {xo.o, xo.h1, xo.u, xo.z, xo.h2};
-    const int ks[5] = {dm.hq * dm.hd, dm.d, dm.p, dm.p, dm.d};
-    bool ok = m->encode != nullptr;
-    for (int c = 0; c < 2 && ok; ++c)
-      for (int i = 0; i < 5 && ok; ++i) {
-        const int nblk = ks[i] / 64;
-        int nb = 8;
-        while (nblk % nb) nb >>= 1;
-        m->act_box[i] = nb;
-        cuuint64_t dims[3] = {64, (cuuint64_t)T, (cuuint64_t)nblk};
-        cuuint64_t strides[2] = {(cuuint64_t)ks[i] * 2, 128};
-        cuuint32_t box[3] = {64, (cuuint32_t)T, (cuuint32_t)nb};
-        cuuint32_t es[3] = {1, 1, 1};
-        ok = m->encode(&m->tma_act[c][i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, m->x[c] + offs[i], dims, strides,
-                       box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-      }
-    m->act_tma = ok;
+    // the static scratch of msm_verify_step_noalloc: its address is looked up now, so
+    // that loading the module holding it (and with it the array's device memory)
+    // happens here and never inside a no-allocation call
+    const uint64_t q_bytes = align256((uint64_t)T * dm.hq * dm.hd * 2), h_bytes = align256((uint64_t)T * dm.d * 2);
+    m->noalloc_need = 2 * xo.total + so.total + 2 * q_bytes + 2 * h_bytes;
+    st = noalloc_lookup(&m->noalloc);
+    if (st != MSM_OK) return bail(st);
+    if (m->noalloc_need <= (uint64_t)MSM_NOALLOC_SCRATCH_BYTES)
+      m->act_tma_na = encode_act_maps(m, m->noalloc, m->tma_act_na[0]) &&
+                      encode_act_maps(m, m->noalloc + xo.total, m->tma_act_na[1]);
   }
   CKM(m->alloc(&m->rope, (uint64_t)T * (dm.hd / 2) * 2 * 4));
   CKM(m->alloc(&m->inv_freq, (uint64_t)(dm.hd / 2) * 8));
@@ -429,11 +477,36 @@ void msm_model_destroy(msm_model* m) {
 }  // extern "C"
 
 namespace {
-// the verify step with the tree and pos0 from the host (state == nullptr) or from a
-// device-resident step state that the kernels validate
-msm_status enqueue_verify(msm_model* m, const void* hidden_in, const int32_t* parent, int32_t pos0,
-                          const int32_t* state, void* const* k_cache, void* const* v_cache, float* logits_out,
-                          void* hidden_out, void* stream) {
+// The per-step buffers a verify step hands data through: the model's own (their two
+// exchange parities alternate launch by launch across steps, each launch re-arming the
+// other one) or the static scratch of msm_verify_step_noalloc (both parities armed by
+// the call, launch l uses parity l & 1).
+struct StepBuffers {
+  uint8_t* x[2];
+  uint8_t* sbuf;
+  uint16_t* in_q[2];
+  uint16_t* in_h[2];
+  const CUtensorMap (*tma_act)[5];  // [2][5], or null: plain-load staging
+  bool model_owned;
+};
+
+StepBuffers own_buffers(msm_model* m) {
+  StepBuffers b;
+  for (int c = 0; c < 2; ++c) {
+    b.x[c] = m->x[c];
+    b.in_q[c] = m->in_q[c];
+    b.in_h[c] = m->in_h[c];
+  }
+  b.sbuf = m->sbuf;
+  b.tma_act = m->act_tma ? m->tma_act : nullptr;
+  b.model_owned = true;
+  return b;
+}
+
+// host-detectable errors of a verify step, found before anything is enqueued
+msm_status validate_step(msm_model* m, const void* hidden_in, const int32_t* parent, int32_t pos0,
+                         const int32_t* state, void* const* k_cache, void* const* v_cache, float* logits_out,
+                         void* hidden_out) {
   if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
   const Dims& dm = m->dm;
   if (!hidden_in || !k_cache || !v_cache) return fail(MSM_ERR_INVALID_ARG, "NULL hidden_in or cache array");
@@ -454,6 +527,17 @@ msm_status enqueue_verify(msm_model* m, const void* hidden_in, const int32_t* pa
     if ((reinterpret_cast<uintptr_t>(k_cache[l]) & 15) || (reinterpret_cast<uintptr_t>(v_cache[l]) & 15))
       return fail(MSM_ERR_INVALID_ARG, "KV caches must be 16-byte aligned");
   }
+  return MSM_OK;
+}
+
+// the verify step with the tree and pos0 from the host (state == nullptr) or from a
+// device-resident step state that the kernels validate
+msm_status enqueue_verify(msm_model* m, const StepBuffers& B, const void* hidden_in, const int32_t* parent,
+                          int32_t pos0, const int32_t* state, void* const* k_cache, void* const* v_cache,
+                          float* logits_out, void* hidden_out, void* stream) {
+  msm_status vst = validate_step(m, hidden_in, parent, pos0, state, k_cache, v_cache, logits_out, hidden_out);
+  if (vst != MSM_OK) return vst;
+  const Dims& dm = m->dm;
   CK(cudaSetDevice(m->device));
   for (int l = 0; l < dm.n_layers; ++l) {
     if (m->tmk_ptr[l] != k_cache[l]) {
@@ -475,7 +559,7 @@ msm_status enqueue_verify(msm_model* m, const void* hidden_in, const int32_t* pa
   P.dm = dm;
   P.xo = m->xo;
   P.so = m->so;
-  P.s_buf = m->sbuf;
+  P.s_buf = B.sbuf;
   P.rope = m->rope;
   P.inv_freq = m->inv_freq;
   P.tree_dbg = m->tree_dbg;
@@ -483,6 +567,10 @@ msm_status enqueue_verify(msm_model* m, const void* hidden_in, const int32_t* pa
   P.pos0 = pos0;
   P.ring_bytes = m->ring_bytes;
   P.act_bytes = m->act_bytes;
+  P.g1_u_off = m->g1_u_off;
+  P.g1_x_off = m->g1_x_off;
+  P.g2_off = m->g2_off;
+  P.ring_ext = m->ring_ext;
   P.flags = m->cfg.flags;
   P.timeout_ns_lo = (uint32_t)tmo;
   P.timeout_ns_hi = (uint32_t)(tmo >> 32);
@@ -502,7 +590,7 @@ msm_status enqueue_verify(msm_model* m, const void* hidden_in, const int32_t* pa
   for (int l = 0; l < dm.n_layers; ++l) {
     const LayerPack& lp = m->L[l];
     const bool first = l == 0, last = l == dm.n_layers - 1;
-    const int c = (int)(m->launch_count & 1);
+    const int c = B.model_owned ? (int)(m->launch_count & 1) : (l & 1);
     P.layer = l;
     P.first = first;
     P.last = last;
@@ -529,17 +617,17 @@ msm_status enqueue_verify(msm_model* m, const void* hidden_in, const int32_t* pa
     P.vc_next = last ? nullptr : static_cast<uint16_t*>(v_cache[l + 1]);
     P.kc_pf = P.kc_next;
     P.vc_pf = P.vc_next;
-    P.x_cur = m->x[c];
-    P.x_next = m->x[c ^ 1];
-    P.act_tma = m->act_tma ? 1 : 0;
+    P.x_cur = B.x[c];
+    P.x_next = B.x[c ^ 1];
+    P.act_tma = B.tma_act ? 1 : 0;
     for (int i = 0; i < 5; ++i) {
-      P.tmap_act[i] = m->tma_act[c][i];
+      if (B.tma_act) P.tmap_act[i] = B.tma_act[c][i];
       P.act_box[i] = m->act_box[i];
     }
-    P.in_q = m->in_q[c];
-    P.in_h = m->in_h[c];
-    P.out_q = m->in_q[c ^ 1];
-    P.out_h = m->in_h[c ^ 1];
+    P.in_q = B.in_q[c];
+    P.in_h = B.in_h[c];
+    P.out_q = B.in_q[c ^ 1];
+    P.out_h = B.in_h[c ^ 1];
     P.routing_idx = m->routing_idx + (size_t)l * T * dm.k;
     P.routing_w = m->routing_w + (size_t)l * T * dm.k;
     P.hist_cur = m->hist + ((size_t)sp * dm.n_layers + l) * dm.e;
@@ -566,7 +654,9 @@ msm_status enqueue_verify(msm_model* m, const void* hidden_in, const int32_t* pa
     void* args[] = {&P};
     cudaError_t e = cudaLaunchKernelExC(&lc, layer_kernel(timing), args);
     if (e != cudaSuccess) return cuda_fail(e, "layer kernel launch");
-    ++m->launch_count;
+    if (B.model_owned) ++m->launch_count;
+    ++m->launches_run;
+    m->last_x = B.x[c];
   }
   ++m->step_count;
   return MSM_OK;
@@ -578,13 +668,17 @@ extern "C" {
 msm_status msm_verify_step(msm_model* m, const void* hidden_in, const int32_t* parent, int32_t pos0,
                            void* const* k_cache, void* const* v_cache, float* logits_out, void* hidden_out,
                            void* stream) {
-  return enqueue_verify(m, hidden_in, parent, pos0, nullptr, k_cache, v_cache, logits_out, hidden_out, stream);
+  if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
+  return enqueue_verify(m, own_buffers(m), hidden_in, parent, pos0, nullptr, k_cache, v_cache, logits_out, hidden_out,
+                        stream);
 }
 
 msm_status msm_verify_step_dev(msm_model* m, const void* hidden_in, const int32_t* state, void* const* k_cache,
                                void* const* v_cache, float* logits_out, void* hidden_out, void* stream) {
   if (!state) return fail(MSM_ERR_INVALID_ARG, "state is NULL");
-  return enqueue_verify(m, hidden_in, nullptr, 0, state, k_cache, v_cache, logits_out, hidden_out, stream);
+  if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
+  return enqueue_verify(m, own_buffers(m), hidden_in, nullptr, 0, state, k_cache, v_cache, logits_out, hidden_out,
+                        stream);
 }
 
 msm_status msm_sync(msm_model* m, void* stream) {
@@ -672,12 +766,14 @@ msm_status msm_get_stats(const msm_model* m, msm_stats* out) {
   out->packed_weight_bytes = m->packed_bytes;
   out->exchange_bytes = 2 * m->xo.total + m->so.total;
   out->tma_act_staging = m->act_tma ? 1 : 0;
+  out->launches_run = m->launches_run;
+  out->noalloc_scratch_bytes = m->noalloc_need;
   return MSM_OK;
 }
 
 msm_status msm_get_exchange(msm_model* m, const char* name, void* host, size_t bytes) {
   if (!m || !name || !host) return fail(MSM_ERR_INVALID_ARG, "model, name or buffer is NULL");
-  if (m->launch_count == 0) return fail(MSM_ERR_INVALID_ARG, "no step has run");
+  if (m->last_x == nullptr) return fail(MSM_ERR_INVALID_ARG, "no step has run");
   const XOffsets& o = m->xo;
   struct { const char* n; uint64_t off, len; } tab[] = {
       {"o", o.o, (uint64_t)T * m->dm.hq * m->dm.hd * 2}, {"h1", o.h1, (uint64_t)T * m->dm.d * 2},
@@ -689,8 +785,7 @@ msm_status msm_get_exchange(msm_model* m, const char* name, void* host, size_t b
     if (bytes < e.len) return fail(MSM_ERR_INVALID_ARG, "buffer too small");
     CK(cudaSetDevice(m->device));
     CK(cudaDeviceSynchronize());
-    const int c = (int)((m->launch_count - 1) & 1);
-    CK(cudaMemcpy(host, m->x[c] + e.off, e.len, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(host, m->last_x + e.off, e.len, cudaMemcpyDeviceToHost));
     return MSM_OK;
   }
   return fail(MSM_ERR_INVALID_ARG, std::string("unknown exchange buffer ") + name);
@@ -804,10 +899,12 @@ msm_status capture_step(msm_model* m, const void* hidden_in, const int32_t* pare
   // again after them, so a replay neither depends on nor leaves behind state that
   // an eager step of either launch parity (odd layer counts) could trip over; the
   // capture leaves the model's launch counters as they were
-  const uint64_t launches0 = m->launch_count, steps0 = m->step_count;
+  const uint64_t launches0 = m->launch_count, steps0 = m->step_count, run0 = m->launches_run;
+  uint8_t* const last_x0 = m->last_x;
   msm_status st = rearm_all(m, cs);
   if (st == MSM_OK)
-    st = enqueue_verify(m, hidden_in, parent, pos0, state, k_cache, v_cache, logits_out, hidden_out, cs);
+    st = enqueue_verify(m, own_buffers(m), hidden_in, parent, pos0, state, k_cache, v_cache, logits_out, hidden_out,
+                        cs);
   if (st == MSM_OK && accept_result)
     st = enqueue_accept(m, logits_out, tokens, parent, pos0, state, k_cache, v_cache, accept_result, cs);
   if (st == MSM_OK) st = rearm_all(m, cs);
@@ -815,6 +912,8 @@ msm_status capture_step(msm_model* m, const void* hidden_in, const int32_t* pare
   // launches that did run (a replay arms both parities, so it needs no count)
   m->launch_count = launches0;
   m->step_count = steps0;
+  m->launches_run = run0;
+  m->last_x = last_x0;
   std::string msg = st == MSM_OK ? std::string() : std::string(msm_last_error());
   cudaGraph_t graph = nullptr;
   e = cudaStreamEndCapture(cs, &graph);
@@ -885,22 +984,12 @@ msm_status msm_draft_step(msm_model* m, const void* draft_hidden_in, int32_t* to
 static __device__ __align__(256) unsigned char msm_noalloc_scratch[MSM_NOALLOC_SCRATCH_BYTES];
 
 namespace {
-constexpr int kNoAllocMaxDevices = 64;
-unsigned char* g_noalloc_base[kNoAllocMaxDevices] = {};
-std::mutex g_noalloc_mu;
-
-// device address of the array on `device` (current); looked up once per device
-msm_status noalloc_base(int device, unsigned char** base) {
-  if (device < 0 || device >= kNoAllocMaxDevices) return fail(MSM_ERR_UNSUPPORTED, "device index above 63");
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_base[device]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, msm_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-    if (!p) return fail(MSM_ERR_CUDA, "cudaGetSymbolAddress(static scratch) returned NULL");
-    g_noalloc_base[device] = static_cast<unsigned char*>(p);
-  }
-  *base = g_noalloc_base[device];
+msm_status noalloc_lookup(unsigned char** base) {
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, msm_noalloc_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+  if (!p) return fail(MSM_ERR_CUDA, "cudaGetSymbolAddress(static scratch) returned NULL");
+  *base = static_cast<unsigned char*>(p);
   return MSM_OK;
 }
 }  // namespace
@@ -910,150 +999,38 @@ extern "C" msm_status msm_verify_step_noalloc(msm_model* m, const void* hidden_i
                                               float* logits_out, void* hidden_out, void* stream) {
   if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
   const Dims& dm = m->dm;
-  if (!hidden_in || !k_cache || !v_cache) return fail(MSM_ERR_INVALID_ARG, "NULL hidden_in or cache array");
-  if (!parent_valid(parent)) return fail(MSM_ERR_INVALID_ARG, "parent must satisfy parent[0] == -1, 0 <= parent[i] < i");
-  if (pos0 < 0 || (int64_t)pos0 + T > dm.max_ctx) return fail(MSM_ERR_INVALID_ARG, "pos0 out of range");
-  if (dm.vocab > 0 && !logits_out) return fail(MSM_ERR_INVALID_ARG, "logits_out is NULL but vocab > 0");
-  if (dm.vocab == 0 && !hidden_out) return fail(MSM_ERR_INVALID_ARG, "hidden_out is NULL but vocab == 0");
-  if ((reinterpret_cast<uintptr_t>(hidden_in) & 15) || (reinterpret_cast<uintptr_t>(hidden_out) & 15) ||
-      (reinterpret_cast<uintptr_t>(logits_out) & 15))
-    return fail(MSM_ERR_INVALID_ARG, "hidden / logits buffers must be 16-byte aligned");
-  for (int l = 0; l < dm.n_layers; ++l) {
-    if (!k_cache[l] || !v_cache[l]) return fail(MSM_ERR_INVALID_ARG, "NULL KV cache pointer");
-    if ((reinterpret_cast<uintptr_t>(k_cache[l]) & 15) || (reinterpret_cast<uintptr_t>(v_cache[l]) & 15))
-      return fail(MSM_ERR_INVALID_ARG, "KV caches must be 16-byte aligned");
-  }
-  // carve: x[0] | x[1] | partials | in_q[0] | in_q[1] | in_h[0] | in_h[1]
-  const uint64_t q_bytes = align256((uint64_t)T * dm.hq * dm.hd * 2), h_bytes = align256((uint64_t)T * dm.d * 2);
-  const uint64_t need = 2 * m->xo.total + m->so.total + 2 * q_bytes + 2 * h_bytes;
-  if (need > (uint64_t)MSM_NOALLOC_SCRATCH_BYTES) {
+  msm_status vst = validate_step(m, hidden_in, parent, pos0, nullptr, k_cache, v_cache, logits_out, hidden_out);
+  if (vst != MSM_OK) return vst;
+  if (m->noalloc_need > (uint64_t)MSM_NOALLOC_SCRATCH_BYTES) {
     char buf[200];
     std::snprintf(buf, sizeof(buf),
                   "msm_verify_step_noalloc: this model's step needs %llu bytes of scratch; the static array holds "
                   "%llu (MSM_NOALLOC_SCRATCH_BYTES)",
-                  (unsigned long long)need, (unsigned long long)MSM_NOALLOC_SCRATCH_BYTES);
+                  (unsigned long long)m->noalloc_need, (unsigned long long)MSM_NOALLOC_SCRATCH_BYTES);
     return fail(MSM_ERR_UNSUPPORTED, buf);
   }
+  // carve: x[0] | x[1] | partials | in_q[0] | in_q[1] | in_h[0] | in_h[1]
+  const uint64_t q_bytes = align256((uint64_t)T * dm.hq * dm.hd * 2), h_bytes = align256((uint64_t)T * dm.d * 2);
+  unsigned char* base = m->noalloc;
+  StepBuffers B;
+  B.x[0] = base;
+  B.x[1] = base + m->xo.total;
+  B.sbuf = base + 2 * m->xo.total;
+  B.in_q[0] = reinterpret_cast<uint16_t*>(B.sbuf + m->so.total);
+  B.in_q[1] = reinterpret_cast<uint16_t*>(B.sbuf + m->so.total + q_bytes);
+  B.in_h[0] = reinterpret_cast<uint16_t*>(B.sbuf + m->so.total + 2 * q_bytes);
+  B.in_h[1] = reinterpret_cast<uint16_t*>(B.sbuf + m->so.total + 2 * q_bytes + h_bytes);
+  B.tma_act = m->act_tma_na ? m->tma_act_na : nullptr;
+  B.model_owned = false;
   CK(cudaSetDevice(m->device));
-  unsigned char* base = nullptr;
-  msm_status st = noalloc_base(m->device, &base);
-  if (st != MSM_OK) return st;
-  uint8_t* xs[2] = {base, base + m->xo.total};
-  uint8_t* sb = base + 2 * m->xo.total;
-  uint16_t* iq[2] = {reinterpret_cast<uint16_t*>(sb + m->so.total),
-                     reinterpret_cast<uint16_t*>(sb + m->so.total + q_bytes)};
-  uint16_t* ih[2] = {reinterpret_cast<uint16_t*>(sb + m->so.total + 2 * q_bytes),
-                     reinterpret_cast<uint16_t*>(sb + m->so.total + 2 * q_bytes + h_bytes)};
-  for (int l = 0; l < dm.n_layers; ++l) {
-    if (m->tmk_ptr[l] != k_cache[l]) {
-      st = encode_kv_map(m, &m->tmk[l], k_cache[l]);
-      if (st != MSM_OK) return st;
-      m->tmk_ptr[l] = k_cache[l];
-    }
-    if (m->tmv_ptr[l] != v_cache[l]) {
-      st = encode_kv_map(m, &m->tmv[l], v_cache[l]);
-      if (st != MSM_OK) return st;
-      m->tmv_ptr[l] = v_cache[l];
-    }
-  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // arm the exchange part (sentinels, zeroed counters) on the caller's stream
+  // the array keeps the last call's contents: arm the exchange part (sentinels, zeroed
+  // counters) and the partials on the caller's stream before the launches
   for (int c = 0; c < 2; ++c) {
-    st = arm_exchange(xs[c], m->xo, s);
+    msm_status st = arm_exchange(B.x[c], m->xo, s);
     if (st != MSM_OK) return st;
   }
-  CK(launch_fill_u32(sb, m->so.y / 4, 0x80000000u, s));
-  CK(launch_fill_u32(sb + m->so.y, (m->so.total - m->so.y) / 4, 0xFFFFFFFFu, s));
-
-  const uint64_t tmo = (uint64_t)(m->cfg.timeout_us ? m->cfg.timeout_us : 200000u) * 1000ull;
-  const int sp = (int)(m->step_count & 1);
-  LaunchParams P;
-  std::memset(&P, 0, sizeof(P));
-  P.dm = dm;
-  P.xo = m->xo;
-  P.so = m->so;
-  P.s_buf = sb;
-  P.rope = m->rope;
-  P.inv_freq = m->inv_freq;
-  P.tree_dbg = m->tree_dbg;
-  P.status = m->status;
-  P.pos0 = pos0;
-  P.ring_bytes = m->ring_bytes;
-  P.act_bytes = m->act_bytes;
-  P.flags = m->cfg.flags;
-  P.timeout_ns_lo = (uint32_t)tmo;
-  P.timeout_ns_hi = (uint32_t)(tmo >> 32);
-  P.prefetch_experts = m->cfg.prefetch_experts > 0 ? m->cfg.prefetch_experts : 14;
-  P.runahead_bytes = m->cfg.l2_runahead_kb > 0 ? (uint32_t)m->cfg.l2_runahead_kb * 1024u : 0u;
-  P.phase_rot = 13;
-  std::memcpy(P.parent, parent, sizeof(int32_t) * T);
-  P.hidden_in = static_cast<const uint16_t*>(hidden_in);
-  P.logits = logits_out;
-  const bool timing = (m->cfg.flags & MSM_FLAG_SELF_TIMING) != 0;
-  const bool pdl = (m->cfg.flags & MSM_FLAG_PDL) != 0;
-  for (int l = 0; l < dm.n_layers; ++l) {
-    const LayerPack& lp = m->L[l];
-    const bool first = l == 0, last = l == dm.n_layers - 1;
-    const int c = l & 1;  // both parities were armed above
-    P.layer = l;
-    P.first = first;
-    P.last = last;
-    P.is_global = m->global[l] != 0;
-    P.next_global = last ? 0 : (m->global[l + 1] != 0);
-    P.w_qkv_pro = first ? lp.qkv : nullptr;
-    P.g_attn_pro = first ? lp.g_attn : nullptr;
-    P.w_o = lp.o;
-    P.w_pool = lp.pool;
-    P.w_router = lp.router;
-    P.b_router = lp.b;
-    P.w_unpool = lp.unpool;
-    P.g_moe = lp.g_moe;
-    P.w1 = lp.w1;
-    P.w2 = lp.w2;
-    P.w1_gs = lp.w1gs;
-    P.w2_gs = lp.w2gs;
-    P.w_tail = last ? m->lm : m->L[l + 1].qkv;
-    P.g_tail = last ? m->g_final : m->L[l + 1].g_attn;
-    P.hidden_out = last ? static_cast<uint16_t*>(hidden_out) : nullptr;
-    P.kc = static_cast<uint16_t*>(k_cache[l]);
-    P.vc = static_cast<uint16_t*>(v_cache[l]);
-    P.kc_next = last ? nullptr : static_cast<uint16_t*>(k_cache[l + 1]);
-    P.vc_next = last ? nullptr : static_cast<uint16_t*>(v_cache[l + 1]);
-    P.kc_pf = P.kc_next;
-    P.vc_pf = P.vc_next;
-    P.x_cur = xs[c];
-    P.x_next = xs[c ^ 1];
-    P.in_q = iq[c];
-    P.in_h = ih[c];
-    P.out_q = iq[c ^ 1];
-    P.out_h = ih[c ^ 1];
-    P.routing_idx = m->routing_idx + (size_t)l * T * dm.k;
-    P.routing_w = m->routing_w + (size_t)l * T * dm.k;
-    P.hist_cur = m->hist + ((size_t)sp * dm.n_layers + l) * dm.e;
-    P.hist_prev = m->step_count > 0 ? m->hist + ((size_t)(sp ^ 1) * dm.n_layers + l) * dm.e : nullptr;
-    P.timing = m->timing + (size_t)l * m->G * kTimingEvents;
-    P.tmap_k = m->tmk[l];
-    P.tmap_v = m->tmv[l];
-
-    cudaLaunchConfig_t lc;
-    std::memset(&lc, 0, sizeof(lc));
-    lc.gridDim = dim3(m->G);
-    lc.blockDim = dim3(kThreads);
-    lc.dynamicSmemBytes = m->smem_bytes;
-    lc.stream = s;
-    cudaLaunchAttribute attr[1];
-    int na = 0;
-    if (pdl && !first) {
-      attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      attr[na].val.programmaticStreamSerializationAllowed = 1;
-      ++na;
-    }
-    lc.attrs = na ? attr : nullptr;
-    lc.numAttrs = na;
-    void* args[] = {&P};
-    cudaError_t e = cudaLaunchKernelExC(&lc, layer_kernel(timing), args);
-    if (e != cudaSuccess) return cuda_fail(e, "layer kernel launch");
-  }
-  ++m->step_count;
-  return MSM_OK;
+  CK(launch_fill_u32(B.sbuf, m->so.y / 4, 0x80000000u, s));
+  CK(launch_fill_u32(B.sbuf + m->so.y, (m->so.total - m->so.y) / 4, 0xFFFFFFFFu, s));
+  return enqueue_verify(m, B, hidden_in, parent, pos0, nullptr, k_cache, v_cache, logits_out, hidden_out, stream);
 }

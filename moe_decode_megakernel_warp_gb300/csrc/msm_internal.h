@@ -14,12 +14,20 @@ constexpr int kFirstCompute = 4;      // warps 4..11: attention / GEMM / expert 
 constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kSlots = 12;            // descriptors of the variable-size ring
-constexpr int kDenseTileSteps = 32;   // 16-row x 512-column bf16 tiles: 32 k-steps x 512 B
+constexpr int kDenseTileSteps = 64;   // 16-row x 1024-column bf16 tiles: 64 k-steps x 512 B
 constexpr int kKStepBytes = 512;      // one 16x16 bf16 (or f16) block in ldmatrix order
-constexpr int kExpGroupBytes = 576;   // 16 rows x 64 columns NVFP4: 512 B codes + 64 B scales
+// NVFP4 expert tiles: 128 rows x tk columns (tk = 512 where the width allows, else 256):
+// tk / 256 column blocks of 128 rows x 128 code bytes in the 128-byte swizzle layout
+// (16 KB each), then the rows' tk / 16 UE4M3 block scales (row after row)
+constexpr int kExpTileRows = 128;
+constexpr int kExpBlockK = 256;                                  // columns per 16 KB code block
+constexpr int kExpBlockBytes = kExpTileRows * kExpBlockK / 2;
+__host__ __device__ constexpr int exp_tile_k(int K) { return K % 512 == 0 ? 512 : 256; }
+__host__ __device__ constexpr int exp_tile_bytes(int K) { return exp_tile_k(K) / kExpBlockK * kExpBlockBytes + kExpTileRows * exp_tile_k(K) / 16; }
+__host__ __device__ constexpr int exp_scale_off(int K) { return exp_tile_k(K) / kExpBlockK * kExpBlockBytes; }
 constexpr int kSmallBytes = 16 * 1024; // barriers, routing tables, scratch, dense partials
 constexpr int kMaxSmem = 232448;      // 227 KB opt-in dynamic shared memory per block
-constexpr int kTimingEvents = 64;
+constexpr int kTimingEvents = 192;
 constexpr int kMaxTopK = 8;
 constexpr int kMaxExperts = 256;
 
@@ -45,7 +53,19 @@ enum TimingEvent : int {
   EV_LD_OP_U1 = 54,  // loader issued the first tile of the block's second o_proj unit
   // the block's poller saw a phase-completion counter reach the grid size
   EV_SEEN_MERGE = 55, EV_SEEN_OPROJ = 56, EV_SEEN_POOL = 57, EV_SEEN_ROUTER = 58, EV_SEEN_ROUTE = 59,
-  EV_SEEN_COMBINE = 60, EV_SEEN_UNPOOL = 61, EV_SEEN_TAIL = 62
+  EV_SEEN_COMBINE = 60, EV_SEEN_UNPOOL = 61, EV_SEEN_TAIL = 62,
+  // per-tile trace of the expert GEMMs (the block's first tiles): the tensor-core warp
+  // saw tile i's operands ready / had issued its MMAs, and the compute warp group saw
+  // tile i land in the ring
+  EV_TC_G1_READY = 64,   // + i, i < 16
+  EV_TC_G1_ISSUED = 80,  // + i, i < 16
+  EV_WG_G1_LANDED = 96,  // + i, i < 16
+  EV_TC_G2_READY = 112,  // + i, i < 8
+  EV_TC_G2_ISSUED = 120, // + i, i < 8
+  EV_LD_G1_ISSUED = 128, // + i, i < 16: the loader issued the copy of GEMM1 tile i
+  EV_LD_RING_GROWN = 144, // the loader's ring grew into the activation buffer
+  EV_LD_G1_NEXT = 160,    // + i, i < 16: the loader had GEMM1 tile i's source (after the stream step)
+  EV_LD_G1_PLACED = 176   // + i, i < 16: ... and its ring space
 };
 
 // phases of one layer launch (recorded in the status word on a timeout)
@@ -152,6 +172,11 @@ struct LaunchParams {
   // scalars
   int layer, first, last, is_global, next_global, pos0;
   int ring_bytes, act_bytes;
+  // expert phases: the pooled vectors in f16 (GEMM1 operand B), the GEMM1 epilogue
+  // exchange rows and the GEMM2 operands sit at these offsets at the top of the
+  // activation buffer; from the end of routing to the unpooler the weight ring may grow
+  // by ring_ext bytes into the bottom of it
+  int g1_u_off, g1_x_off, g2_off, ring_ext;
   uint32_t flags;
   uint32_t timeout_ns_lo, timeout_ns_hi;
   int prefetch_experts;
@@ -176,7 +201,10 @@ enum ActMap : int { ACT_O = 0, ACT_H1 = 1, ACT_U = 2, ACT_Z = 3, ACT_H2 = 4 };
 
 // packed sizes
 __host__ __device__ inline uint64_t dense_unit_bytes(int K) { return (uint64_t)K * 32; }  // 16 rows x K bf16
-__host__ __device__ inline uint64_t exp_unit_bytes(int K) { return (uint64_t)(K / 64) * kExpGroupBytes; }
+// an expert unit: 128 rows x K columns = K / 256 tiles (W1: 64 gate + 64 up rows; W2: 128 rows)
+__host__ __device__ inline uint64_t exp_unit_bytes(int K) { return (uint64_t)(K / exp_tile_k(K)) * exp_tile_bytes(K); }
+__host__ __device__ inline int w1_units(int f) { return f / 64; }
+__host__ __device__ inline int w2_units(int p) { return p / kExpTileRows; }
 
 // kernel entry points (defined in msm_kernel.cu / msm_pack.cu)
 const void* layer_kernel(bool timing);

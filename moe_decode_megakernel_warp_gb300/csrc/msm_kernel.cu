@@ -58,7 +58,38 @@ struct Smem {
   volatile uint32_t* slot_tile;  // [kSlots] index of the tile the loader last put in each slot
   struct RunAhead* ring_state;    // the loader's L2 run-ahead lists
   float* dred;        // [8][16][16] dense-phase cross-warp partial sums
+  uint64_t* tcbar;    // tensor-core pipeline barriers (TcBar)
+  uint32_t* tmem_base;  // tensor-memory columns of the block (written by the allocating warp)
+  uint32_t* tc_ti;      // [1]: first ring tile of GEMM2 (for the tensor-core warp)
 };
+
+// Tensor-core pipeline of the expert GEMMs: mbarriers between the compute warp groups
+// (dequantisation / scale staging / epilogues) and the tensor-core warp (MMA issue).
+enum TcBar : int {
+  TB_G1_FREE = 0,    // [2 groups][2 chunk buffers] GEMM1 A chunk consumed by its MMAs (4 issuer commits)
+  TB_D1_FULL = 4,    // [2 groups][4 issuers][2 parities] an issuer's GEMM1 accumulator of a unit done
+  TB_D1_FREE = 20,   // [2 parities] ... read by the unit's epilogue (4 warps)
+  TB_SFA_FULL = 22,  // [4] GEMM2 weight block scales of a tile in tensor memory (4 warps)
+  TB_SFA_FREE = 26,  // [4] ... the tile's MMAs are done (commit)
+  TB_D2_FULL = 30,   // [2]
+  TB_D2_FREE = 32,   // [2]
+  TB_G2_STAGE = 34,  // a GEMM2 round's activations and their block scales staged
+  TB_DONE = 35,      // the compute warps are done with tensor memory (8 warps)
+  TB_DRAIN = 36,     // every MMA of the tensor-core warp has completed
+  TB_WDRAIN = 37,    // [8] every MMA a compute warp issued has completed
+  TB_ROUTED = 45,    // the block's routing (expert list, GEMM2 tile base) is in shared memory
+  kTcBars = 46
+};
+// tensor-memory columns (512 allocated: one block per SM).  GEMM2 reuses GEMM1's chunk
+// columns: its first tensor-memory write follows every GEMM1 epilogue, and so every
+// GEMM1 MMA.
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t TM_ABUF = 0;    // [2 groups][2] x 64: GEMM1 dequantised weight chunks (128 rows x 128 K, f16)
+constexpr uint32_t TM_D1 = 256;    // [2 groups][4 issuers][2 parities] x 16: GEMM1 partial accumulators (fp32)
+constexpr uint32_t TM_SFB = 0;     // 2 x 64: GEMM2 activation scales of a round's two experts
+constexpr uint32_t TM_SFA = 128;   // 4 x 32: GEMM2 weight scales of a tile (up to 8 K=64 steps x 4 columns)
+constexpr uint32_t TM_D2 = 256;    // 2 x 16: GEMM2 accumulators
+__host__ __device__ constexpr uint32_t tm_d1(int wg, int q, int d) { return TM_D1 + (uint32_t)(((wg * 4 + q) * 2 + d) * 16); }
 
 constexpr int kRingStateOff = 6656;  // in the small area, below the GEMM2 row scales
 constexpr int kATsOff = 7936;        // [2][16] floats, below the reduction scratch at 8192
@@ -90,12 +121,27 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const LaunchParams& P) {
   s.stage_bar = reinterpret_cast<uint64_t*>(sm + 6648);
   s.ring_state = reinterpret_cast<struct RunAhead*>(sm + kRingStateOff);
   s.dred = reinterpret_cast<float*>(sm + 8192);
+  s.tc_ti = reinterpret_cast<uint32_t*>(sm + 7416);
+  s.tmem_base = reinterpret_cast<uint32_t*>(sm + 7420);
+  s.tcbar = reinterpret_cast<uint64_t*>(sm + 7424);
   return s;
 }
 
 // ---------------------------------------------------------------------------
 // bounded waits
 // ---------------------------------------------------------------------------
+// A bounded wait ran out: record it in the status word and make every wait give up.
+// Out of line, and with no pointer to the context: a call that took the context's
+// address would keep the whole context in local memory for the launch.
+__device__ __noinline__ void fail_timeout(const LaunchParams* P, volatile int* abort, int block, int phase) {
+  *abort = 1;
+  if (atomicCAS(&P->status->code, 0, 4 /* MSM_ERR_DEVICE_TIMEOUT */) == 0) {
+    P->status->phase = phase;
+    P->status->block = block;
+    P->status->layer = P->layer;
+  }
+  atomicExch(&P->status->abort, 1);
+}
 struct Ctx {
   const LaunchParams* P;
   Smem S;
@@ -105,19 +151,11 @@ struct Ctx {
   uint64_t next_abort_check = 0;
   int block;
 
-  __device__ __noinline__ void fail(int phase) {
-    *S.abort = 1;
-    if (atomicCAS(&P->status->code, 0, 4 /* MSM_ERR_DEVICE_TIMEOUT */) == 0) {
-      P->status->phase = phase;
-      P->status->block = block;
-      P->status->layer = P->layer;
-    }
-    atomicExch(&P->status->abort, 1);
-  }
+  __device__ __forceinline__ void fail(int phase) { fail_timeout(P, S.abort, block, phase); }
   // true when the caller must give up.  The grid-wide abort word lives in global
   // memory: it is read at most every 4 us per thread, since a global round trip in
   // a spin loop would delay the caller's notice of the very data it waits for.
-  __device__ bool expired(int phase) {
+  __device__ __forceinline__ bool expired(int phase) {
     if (*S.abort) return true;
     const uint64_t now = globaltimer();
     if (now > deadline) {
@@ -197,6 +235,10 @@ __device__ __forceinline__ void stamp(const LaunchParams& P, int block, int ev) 
     P.timing[(size_t)block * kTimingEvents + ev] = globaltimer();
 }
 
+// stamp of any one thread (runtime flag)
+__device__ __forceinline__ void stamp_any(const LaunchParams& P, int ev) {
+  if (P.flags & 0x1u) P.timing[(size_t)blockIdx.x * kTimingEvents + ev] = globaltimer();
+}
 // sub-phase stamps inside helpers shared by both kernel variants (runtime flag)
 __device__ __forceinline__ void stamp_rt(const LaunchParams& P, int ev) {
   if ((P.flags & 0x1u) && threadIdx.x == kFirstCompute * 32)
@@ -284,6 +326,7 @@ struct RunAhead {
 // so that they stay in the loader lane's registers; a tile's offset is read back from
 // the slot table in shared memory once, when the tile before it is released.
 struct Ring {
+  uint32_t cap;       // bytes the ring may use now (grows during the expert phases)
   uint32_t issued;    // tiles issued
   uint32_t tail;      // oldest tile not known to be released
   uint32_t head;      // end of the newest tile
@@ -292,12 +335,15 @@ struct Ring {
   bool ra_on;         // L2 run-ahead enabled
   RunAhead* ra;       // L2 run-ahead state (shared memory)
 };
-static_assert(kRingStateOff + sizeof(RunAhead) <= kATsOff, "run-ahead state overlaps the GEMM2 row scales");
+static_assert(kRingStateOff + sizeof(RunAhead) <= 7416, "run-ahead state overlaps the tensor-core barriers");
+static_assert(7424 + kTcBars * 8 <= kATsOff, "tensor-core barriers overlap the GEMM2 row scales");
+static_assert(TM_ABUF + 4 * 64 <= TM_D1 && tm_d1(1, 3, 1) + 16 <= kTmemCols && TM_SFA + 4 * 32 <= TM_D2 &&
+              TM_D2 + 32 <= kTmemCols, "tensor-memory map");
 
 // a free run of `bytes` (1 KB granules) after the newest tile, at the bottom once the
 // top is too short; waits for the oldest tiles' release until there is one
-__device__ bool ring_place(Ctx& cx, Ring& r, uint32_t bytes, uint32_t& off_out) {
-  const uint32_t cap = (uint32_t)cx.P->ring_bytes;
+__device__ __forceinline__ bool ring_place(Ctx& cx, Ring& r, uint32_t bytes, uint32_t& off_out) {
+  const uint32_t cap = r.cap;
   const uint32_t need = (bytes + 1023u) & ~1023u;
   uint32_t off = 0;
   for (;;) {
@@ -311,7 +357,7 @@ __device__ bool ring_place(Ctx& cx, Ring& r, uint32_t bytes, uint32_t& off_out) 
       if (!r.wrapped) {  // occupied: [tail_off, head)
         if (r.head + need <= cap) { off = r.head; break; }
         if (need <= r.tail_off) { off = 0; r.wrapped = true; break; }
-      } else if (r.head + need <= r.tail_off) {  // occupied: [tail_off, top) and [0, head)
+      } else if (r.head + need <= r.tail_off && r.head + need <= cap) {  // occupied: [tail_off, top) and [0, head)
         off = r.head;
         break;
       }
@@ -361,7 +407,7 @@ __device__ __noinline__ void ra_front(const LaunchParams& P, RunAhead* ra, int b
 __device__ __noinline__ void ra_back(const LaunchParams& P, RunAhead* ra, int block, int na) {
   const Dims& dm = P.dm;
   const int G = gridDim.x;
-  const int u1pe = dm.f / 8, u2pe = dm.p / 16;
+  const int u1pe = w1_units(dm.f), u2pe = w2_units(dm.p);
   const uint64_t ub1 = exp_unit_bytes(dm.p), ub2 = exp_unit_bytes(dm.f);
   // the rest of the launch's stream: this block's expert units (runs of one expert
   // are contiguous), the unpooler, then the next layer's QKV or the LM head
@@ -411,15 +457,18 @@ struct TileStream {
     ub = dense_unit_bytes(K);
     W = w;
   }
-  __device__ void experts(const uint8_t* w, int n_units, int per_expert, uint64_t unit_bytes, int rot) {
+  // expert units: 128 rows x K as K / exp_tile_k(K) tiles of exp_tile_bytes(K) each
+  __device__ void experts(const uint8_t* w, int n_units, int per_expert, int K, int rot) {
     unit_range(n_units, rot_block(blockIdx.x, rot, gridDim.x), gridDim.x, lo, hi);
     u = lo;
+    k0 = 0;
+    steps = K / exp_tile_k(K);
     upe = per_expert;
-    ub = unit_bytes;
+    ub = (uint64_t)exp_tile_bytes(K);
     W = w;
   }
   // TS_TILE: src / bytes set; TS_KV: kv_row set; else a wait or the end
-  __device__ int next(const Ctx& cx, const uint8_t*& src, uint32_t& bytes, int& kv_row) {
+  __device__ __forceinline__ int next(const Ctx& cx, const uint8_t*& src, uint32_t& bytes, int& kv_row) {
     const LaunchParams& P = *cx.P;
     const Dims& dm = P.dm;
     for (;;) {
@@ -434,9 +483,12 @@ struct TileStream {
         }
         if (seg == 7 || seg == 8) {
           const int e = cx.S.act_e[u / upe];
-          src = W + ((uint64_t)e * upe + u % upe) * ub;
+          src = W + (((uint64_t)e * upe + u % upe) * steps + k0) * ub;
           bytes = (uint32_t)ub;
-          ++u;
+          if (++k0 == steps) {
+            k0 = 0;
+            ++u;
+          }
           return TS_TILE;
         }
         const int ns = min(kDenseTileSteps, steps - k0);
@@ -464,8 +516,8 @@ struct TileStream {
         case 4: dense(P.w_pool, dm.d, dm.p, P.phase_rot * 4); break;
         case 5: dense(P.w_router, dm.p, dm.e, P.phase_rot * 5); break;
         case 6: return TS_ROUTE_WAIT;
-        case 7: experts(P.w1, *cx.S.n_active * (dm.f / 8), dm.f / 8, exp_unit_bytes(dm.p), P.phase_rot * 6); break;
-        case 8: experts(P.w2, *cx.S.n_active * (dm.p / 16), dm.p / 16, exp_unit_bytes(dm.f), P.phase_rot * 7); break;
+        case 7: experts(P.w1, *cx.S.n_active * w1_units(dm.f), w1_units(dm.f), dm.p, P.phase_rot * 6); break;
+        case 8: experts(P.w2, *cx.S.n_active * w2_units(dm.p), w2_units(dm.p), dm.f, P.phase_rot * 7); break;
         case 9: dense(P.w_unpool, dm.p, dm.d, P.phase_rot * 8); break;
         case 10:
           if (!P.last) dense(P.w_tail, dm.d, dm.nqkv, P.phase_rot * 9);
@@ -488,6 +540,7 @@ __device__ void loader(Ctx& cx) {
   // small L1 left beside a 227 KB carve-out, and their lines, evicted by the compute
   // warps' traffic, would cost the loader an L2 round trip per access
   Ring r;
+  r.cap = (uint32_t)P.ring_bytes;
   r.issued = r.tail = r.head = r.tail_off = 0;
   r.wrapped = false;
   r.ra = cx.S.ring_state;
@@ -524,11 +577,25 @@ __device__ void loader(Ctx& cx) {
       if (ok && r.ra_on) ra_back(P, r.ra, cx.block, *cx.S.n_active);
       continue;
     }
+    // the expert tiles may also use the bottom of the activation buffer once routing has
+    // moved the pooled vectors out of it; the unpooler's tiles may not (its activation
+    // is staged there)
+    if (ts.seg == 7 || ts.seg == 8) {
+      if (r.cap == (uint32_t)P.ring_bytes && P.ring_ext > 0 && mbar_try_wait(&cx.S.tcbar[TB_ROUTED], 0)) {
+        r.cap = (uint32_t)(P.ring_bytes + P.ring_ext);
+        stamp_any(P, EV_LD_RING_GROWN);
+      }
+    } else {
+      r.cap = (uint32_t)P.ring_bytes;
+    }
+    const int g1i = ts.seg == 7 ? (ts.t_u - ts.lo) * ts.steps + ts.t_k0 : 99;
+    if (g1i < 16) stamp_any(P, EV_LD_G1_NEXT + g1i);
     uint32_t off;
     if (!ring_place(cx, r, bytes, off)) {
       ok = false;
       break;
     }
+    if (g1i < 16) stamp_any(P, EV_LD_G1_PLACED + g1i);
     const uint32_t s = r.issued % kSlots;
     cx.S.slot_off[s] = off;
     cx.S.slot_tile[s] = r.issued;
@@ -544,6 +611,7 @@ __device__ void loader(Ctx& cx) {
       bulk_g2s(cx.S.ring + off, src, bytes, &cx.S.full[s], pol);
     }
     ++r.issued;
+    if (g1i < 16) stamp_any(P, EV_LD_G1_ISSUED + g1i);
     if (r.ra_on) ra_pump(r.ra, bytes);
     if (kTiming) {
       if (ts.seg == 3) {
@@ -551,9 +619,9 @@ __device__ void loader(Ctx& cx) {
         if (ts.t_u == ts.lo + 1 && ts.t_k0 == 0) stamp<kTiming>(P, cx.block, EV_LD_OP_U1);
         if (ts.u == ts.hi) stamp<kTiming>(P, cx.block, EV_LD_OP_LAST);
       } else if (ts.seg == 7) {
-        if (ts.t_u == ts.lo) stamp<kTiming>(P, cx.block, EV_LD_G1_FIRST);
+        if (ts.t_u == ts.lo && ts.t_k0 == 0) stamp<kTiming>(P, cx.block, EV_LD_G1_FIRST);
         if (ts.u == ts.hi) g1_last = ts.t_u;
-        if (ts.t_u == g1_last) stamp<kTiming>(P, cx.block, EV_LD_G1_LAST);
+        if (ts.t_u == g1_last && ts.u == ts.hi) stamp<kTiming>(P, cx.block, EV_LD_G1_LAST);
       }
     }
   }
@@ -1504,7 +1572,7 @@ __device__ void route_phase(Worker& w) {
   // value within 2^29 of the row's largest is exact in f16, so GEMM1 sees u as it
   // is; the scale goes back in through x_ts in the GEMM1 epilogue.  The router phase
   // left u staged in the activation buffer (bf16, same layout), so the rows are
-  // converted in place.
+  // converted into the top of the buffer (the bottom then takes ring tiles).
   uint8_t* actb = cx.S.act;
   const int nch = dm.p / 8;
   for (int tt = 0; tt < 2 && w.ok; ++tt) {
@@ -1524,217 +1592,268 @@ __device__ void route_phase(Worker& w) {
     if (amax > 0.f) frexpf(amax, &ex);  // amax = m 2^ex, m in [0.5, 1)
     const float2 up = make_float2(ldexpf(1.0f, 15 - ex), ldexpf(1.0f, 15 - ex));
     for (int c = w.lane; c < nch; c += 32) {
-      uint4* sp = reinterpret_cast<uint4*>(actb + act_off(t, c * 8));
-      const uint4 v = *sp;
+      const uint4 v = *reinterpret_cast<const uint4*>(actb + act_off(t, c * 8));
       uint32_t wd[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float2 f = __fmul2_rn(make_float2(__uint_as_float(wd[j] << 16), __uint_as_float(wd[j] & 0xFFFF0000u)), up);
         wd[j] = pack_f16x2(f.x, f.y);
       }
-      *sp = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      *reinterpret_cast<uint4*>(actb + P.g1_u_off + act_off(t, c * 8)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
     }
     if (w.lane == 0) cx.S.x_ts[t] = ldexpf(1.0f, ex - 15);
     __syncwarp();
     stamp_rt(P, tt == 0 ? EV_XQ_ROW0_DONE : EV_XQ_ROW1_DONE);
   }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // B operand rows -> the MMAs
   cbar();
+  if (tid == 0) {
+    // first ring tile of GEMM2 (after this block's GEMM1 tiles), for the tensor-core warp
+    int lo1, hi1;
+    unit_range(*cx.S.n_active * w1_units(dm.f), rot_block(cx.block, P.phase_rot * 6, gridDim.x), gridDim.x, lo1, hi1);
+    *cx.S.tc_ti = w.ti + (uint32_t)((hi1 - lo1) * (dm.p / exp_tile_k(dm.p)));
+    mbar_arrive(&cx.S.tcbar[TB_ROUTED], 1);
+  }
   if (*cx.S.abort) w.ok = false;
 }
 
-// NVFP4 expert tile: A fragments of rows g and g+8 for one 16-column k-step,
-// weights dequantised e2m1 * e4m3 into f16 (exact)
-// f16x2 {s, s} * 2^-8 of a UE4M3 scale byte: E4M3 has exponent bias 7 and f16 bias 15,
-// so the byte's 7 magnitude bits shifted into f16 position give the value times 2^-8,
-// exactly (subnormal scales included).  `wm` is the group's scale word with bit 7 of
-// every byte (a sign UE4M3 does not have) already cleared.
+// ---------------------------------------------------------------------------
+// expert GEMMs on the tensor cores (tcgen05, accumulators in tensor memory)
+// ---------------------------------------------------------------------------
+// Work split: the block's expert units (128 rows x K, streamed as 256-column tiles)
+// are processed by the two compute warp groups in turn, tile i of the block by group
+// i & 1, and the MMAs of every tile are issued in tile order by one thread of the
+// tensor-core warp (warp 2), so each accumulator sums its K steps in a fixed order.
+// The epilogue of unit u (tensor memory -> registers -> global) is run by group u & 1
+// once it reaches unit u + 2; the two accumulators of each GEMM alternate by unit.
+//
+// GEMM1 (W4A16): the group dequantises its tile's E2M1 codes times their UE4M3 scales
+// (exact in f16, times 2^-8) into tensor memory, 128 rows x 128 K per chunk, and the
+// MMAs read A there (kind::f16) and B, the 16 pooled vectors in f16, from the
+// activation buffer.  GEMM2 (W4A4): A is the tile itself in the ring (E2M1 in the
+// 128-byte swizzle layout), B the expert's NVFP4 activation rows, and the block
+// scales of both are in tensor memory (kind::mxf4nvf4, 16-element blocks).
+
+// UE4M3 scale byte -> f16x2 {s, s} * 2^-8: E4M3 has exponent bias 7 and f16 bias 15, so
+// the byte's 7 magnitude bits shifted into f16 position give the value times 2^-8,
+// exactly (subnormal scales included).  `wm` is the scale word with bit 7 of every byte
+// (a sign UE4M3 does not have) cleared.
 __device__ __forceinline__ uint32_t ue4m3_pair_f16(uint32_t wm, int byte) {
   return __byte_perm(wm, 0u, 0x4040u | (uint32_t)byte | ((uint32_t)byte << 8)) << 7;
 }
-
-// weights dequantised e2m1 * e4m3 into f16 times 2^-8 (exact: every product has at
-// most 6 significant bits and lies in [2^-18, 10.5]); the caller scales by 2^8.
-// Code bytes of k-step ks: bytes 2 ks (columns 2q, 2q+1) and 2 ks + 1 (2q+8, 2q+9) of
-// the lane's 8-byte word of each row, moved to the low byte with one byte_perm each.
-__device__ __forceinline__ void exp_frags(uint64_t cg, uint64_t cg8, uint32_t sgm, uint32_t sg8m, int ks,
-                                          uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
-  const uint32_t wg = ks < 2 ? (uint32_t)cg : (uint32_t)(cg >> 32);
-  const uint32_t w8 = ks < 2 ? (uint32_t)cg8 : (uint32_t)(cg8 >> 32);
-  const uint32_t b = (uint32_t)(ks & 1) * 2;
-  const uint32_t lo_g = __byte_perm(wg, 0u, 0x4440u | b), hi_g = __byte_perm(wg, 0u, 0x4440u | (b + 1));
-  const uint32_t lo_8 = __byte_perm(w8, 0u, 0x4440u | b), hi_8 = __byte_perm(w8, 0u, 0x4440u | (b + 1));
-  const uint32_t f_g = ue4m3_pair_f16(sgm, ks), f_8 = ue4m3_pair_f16(sg8m, ks);
-  a0 = hmul2(e2m1x2_to_f16x2(lo_g), f_g);
-  a2 = hmul2(e2m1x2_to_f16x2(hi_g), f_g);
-  a1 = hmul2(e2m1x2_to_f16x2(lo_8), f_8);
-  a3 = hmul2(e2m1x2_to_f16x2(hi_8), f_8);
-}
-// the factor exp_frags leaves out
+// the factor the dequantised GEMM1 weights leave out
 constexpr float kExpScaleUndo = 256.0f;
 
-// acc[nt] += 2^-8 W_unit (16 rows, 64-column groups [g0, g1) of the NVFP4 tile at tbase)
-// * act rows, for NT n-tiles of 8 tokens; rows[nt]: the token (activation row) this
-// lane addresses in ldmatrix for n-tile nt.  Software-pipelined one group ahead: the
-// next group's code and scale words and its B fragments are loaded while this group's
-// four k-steps are dequantised (all before its MMAs, so the conversions overlap).
-template <int NT>
-__device__ __forceinline__ void exp_unit_mma(float (&acc)[2][4], const uint8_t* tbase, int g0, int g1,
-                                             uint32_t act_s, int lane, const int (&rows)[2]) {
-  const int g = lane >> 2, q = lane & 3;
-  const int mi = lane >> 3;
-  float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  // B rows: token rows[nt]; matrix mi covers k-step 2 h + (mi >> 1) of the group and its
-  // columns 8 (mi & 1) ..; a group is one 64-column block of the activation
-  uint32_t bro[NT][2];
+__device__ __forceinline__ uint32_t tm_lane(int quadrant) { return (uint32_t)(quadrant * 32) << 16; }
+
+// GEMM1 epilogue of block-local unit `loc`: h = silu(gate) * up for the expert's tokens,
+// fp32 rows of `a` (the GEMM2 input; the consumer polls the -0.0 sentinel).  The unit's
+// sum is the issuers' partial accumulators added in a fixed order (group, issuer).
+// Every warp of the group passes both named barriers, whatever failed before.
+__device__ void g1_epilogue(Worker& w, int lo, int loc, int NT, uint32_t tm, float* xchg) {
+  Ctx& cx = *w.cx;
+  const LaunchParams& P = *cx.P;
+  const Dims& dm = P.dm;
+  const int upe = w1_units(dm.f);
+  const int gu = lo + loc, a = gu / upe, jg = gu % upe;
+  const int wg = w.cw >> 2, q = w.cw & 3, m = q * 32 + w.lane;
+  const int d = loc & 1;
+  float acc[16];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int t = rows[nt];
+  for (int t = 0; t < 16; ++t) acc[t] = 0.f;
+  bool ok = w.ok;
+  for (int g = 0; g < 2; ++g) {
+    if (NT == 1 && g != (loc & 1)) continue;  // one tile per unit: only its group's issuers added to it
+    for (int iq = 0; iq < 4; ++iq) {
+      ok = __all_sync(0xffffffffu, ok && wait_bar(cx, &cx.S.tcbar[TB_D1_FULL + (g * 4 + iq) * 2 + d], (loc >> 1) & 1, PH_GEMM1));
+      if (ok) {
+        tc_fence_after();
+        uint32_t r[16];
+        tmem_ld16(tm + tm_lane(q) + tm_d1(g, iq, d), r);
+        tmem_ld_wait();
 #pragma unroll
-    for (int h = 0; h < 2; ++h) bro[nt][h] = act_s + act_chunk(t, (2 * h + (mi >> 1)) * 2 + (mi & 1));
-  }
-  const uint8_t* gb0 = tbase + g0 * kExpGroupBytes;
-  uint64_t ncg = *reinterpret_cast<const uint64_t*>(gb0 + g * 32 + q * 8);
-  uint64_t ncg8 = *reinterpret_cast<const uint64_t*>(gb0 + (g + 8) * 32 + q * 8);
-  uint32_t nsg = *reinterpret_cast<const uint32_t*>(gb0 + 512 + g * 4);
-  uint32_t nsg8 = *reinterpret_cast<const uint32_t*>(gb0 + 512 + (g + 8) * 4);
-  uint32_t nb[NT][2][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-      ldsm_x4(bro[nt][h] + (uint32_t)g0 * kActBlockBytes, nb[nt][h][0], nb[nt][h][1],
-              nb[nt][h][2], nb[nt][h][3]);
-  for (int gi = g0; gi < g1; ++gi) {
-    const uint64_t cg = ncg, cg8 = ncg8;
-    const uint32_t sg = nsg & 0x7F7F7F7Fu, sg8 = nsg8 & 0x7F7F7F7Fu;
-    uint32_t b[NT][2][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) b[nt][h][i] = nb[nt][h][i];
-    if (gi + 1 < g1) {
-      const uint8_t* gb = tbase + (gi + 1) * kExpGroupBytes;
-      ncg = *reinterpret_cast<const uint64_t*>(gb + g * 32 + q * 8);
-      ncg8 = *reinterpret_cast<const uint64_t*>(gb + (g + 8) * 32 + q * 8);
-      nsg = *reinterpret_cast<const uint32_t*>(gb + 512 + g * 4);
-      nsg8 = *reinterpret_cast<const uint32_t*>(gb + 512 + (g + 8) * 4);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          ldsm_x4(bro[nt][h] + (uint32_t)(gi + 1) * kActBlockBytes, nb[nt][h][0],
-                  nb[nt][h][1], nb[nt][h][2], nb[nt][h][3]);
-    }
-    uint32_t a[4][4];
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) exp_frags(cg, cg8, sg, sg8, ks, a[ks][0], a[ks][1], a[ks][2], a[ks][3]);
-#pragma unroll
-    for (int kp = 0; kp < 4; kp += 2)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        mma_f16(acc[nt], a[kp][0], a[kp][1], a[kp][2], a[kp][3], b[nt][kp >> 1][0], b[nt][kp >> 1][1]);
-        mma_f16(acc2[nt], a[kp + 1][0], a[kp + 1][1], a[kp + 1][2], a[kp + 1][3], b[nt][kp >> 1][2],
-                b[nt][kp >> 1][3]);
+        for (int t = 0; t < 16; ++t) acc[t] += __uint_as_float(r[t]);
       }
+    }
   }
-  // two independent chains (even / odd k-steps), summed in a fixed order
+  tc_fence_before();
+  __syncwarp();
+  if (w.lane == 0) mbar_arrive(&cx.S.tcbar[TB_D1_FREE + d], 1);
+  // rows (lanes) -> shared memory, 17-float pitch (conflict-free both ways): gate rows
+  // 0..63, up rows 64..127 of the unit
+  if (ok) {
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[nt][i] += acc2[nt][i];
+    for (int t = 0; t < 16; ++t) xchg[m * 17 + t] = acc[t];
+  }
+  named_bar(2 + wg, 128);
+  if (ok && m < 64) {
+    const int e = cx.S.act_e[a], n = cx.S.act_n[a];
+    float* aout = reinterpret_cast<float*>(P.x_cur + P.xo.a);
+    const uint8_t* toks = cx.S.act_tok + a * 16;
+    const float gs = P.w1_gs[e] * kExpScaleUndo;
+    for (int p = 0; p < n; ++p) {
+      const int tok = toks[p], slot = cx.S.act_slot[a * 16 + p];
+      const float sc = cx.S.x_ts[tok] * gs;
+      const float gate = xchg[m * 17 + tok] * sc, up = xchg[(64 + m) * 17 + tok] * sc;
+      const float av = gate / (1.0f + expf(-gate)) * up;
+      st_relaxed_u32(aout + (size_t)slot * dm.f + jg * 64 + m, __float_as_uint(f32_canon(av)));
+    }
+  }
+  named_bar(2 + wg, 128);  // the exchange rows are free for the group's next epilogue
+  if (!ok) w.ok = false;
 }
 
-// Expert units are shared by a pair of compute warps (warps 2j and 2j+1), each taking
-// half of the unit's 64-column groups, so twice as many warps work on the tiles the
-// ring holds.  The odd warp hands its partial sums (and whether it got its tile) to
-// the even warp through a double-buffered slot of the reduction scratch; both warps
-// meet at the pair's named barrier once per unit and leave the loop together.
-__device__ __forceinline__ void pair_bar(int pair) { named_bar(2 + pair, 64); }
-
-// returns false (for both warps of the pair) if either warp failed; on success the
-// even warp's acc holds the unit's sum (even half first, then odd half)
-__device__ __forceinline__ bool pair_reduce(Worker& w, float (&acc)[2][4], bool ok, int it) {
-  const int pair = w.cw >> 1, half = w.cw & 1;
-  // partials: [pair][buffer][8][32 lanes] floats = the 8 KB reduction scratch; flags
-  // [pair][buffer][half] in the (then unused) scan scratch
-  float* x = w.cx->S.dred + (pair * 2 + (it & 1)) * 256;
-  int* fl = reinterpret_cast<int*>(w.cx->S.red) + (pair * 2 + (it & 1)) * 2;
-  if (half) {
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) x[(nt * 4 + i) * 32 + w.lane] = acc[nt][i];
-  }
-  if (w.lane == 0) fl[half] = ok ? 1 : 0;
-  pair_bar(pair);
-  const bool both = fl[0] != 0 && fl[1] != 0;
-  if (!half && both) {
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[nt][i] += x[(nt * 4 + i) * 32 + w.lane];
-  }
-  return both;
-}
-
+// GEMM1: the block's units are streamed as tiles, tile i to warp group i & 1.  The
+// group dequantises the tile's 128-column chunks into its two chunk buffers in tensor
+// memory (each thread one row, a warp the 32 lanes of its quadrant); once all four
+// warps have stored a chunk, lane 0 of each warp issues two of its eight K=16 MMAs into
+// that warp's own accumulator (four issuers per group run in parallel: one thread
+// issues an MMA only every ~100 cycles, four reach ~30).  The four warps of a group run
+// the same sequence of named barriers whatever fails; a failure only skips work.
 __device__ void gemm1_phase(Worker& w) {
   Ctx& cx = *w.cx;
   const LaunchParams& P = *cx.P;
   const Dims& dm = P.dm;
   const int G = gridDim.x;
-  const int na = *cx.S.n_active, u1pe = dm.f / 8;
+  const int tk = exp_tile_k(dm.p), nch = tk / 128;  // tile columns, 128-column chunks per tile
+  const int na = *cx.S.n_active, upe = w1_units(dm.f), NT = dm.p / tk;
   int lo, hi;
-  unit_range(na * u1pe, rot_block(cx.block, P.phase_rot * 6, G), G, lo, hi);
-  float* aout = reinterpret_cast<float*>(P.x_cur + P.xo.a);
-  const uint32_t act_s = smem_u32(cx.S.act);
-  const int pair = w.cw >> 1, half = w.cw & 1, ng = dm.p / 64;
-  const int g0 = half ? ng / 2 : 0, g1 = half ? ng : ng / 2;
-  int it = 0;
-  for (int loc = pair; loc < hi - lo; loc += kComputeWarps / 2, ++it) {
-    const int gu = lo + loc, a = gu / u1pe, jg = gu % u1pe;
-    const int e = cx.S.act_e[a], n = cx.S.act_n[a];
-    const uint8_t* toks = cx.S.act_tok + a * 16;
-    const uint32_t t = w.ti + (uint32_t)loc;
+  unit_range(na * upe, rot_block(cx.block, P.phase_rot * 6, G), G, lo, hi);
+  const int wg = w.cw >> 2, q = w.cw & 3, m = q * 32 + w.lane;
+  const uint32_t tm = *cx.S.tmem_base, tl = tm + tm_lane(q);
+  const uint32_t act_s = smem_u32(cx.S.act + P.g1_u_off);  // the 16 pooled vectors, f16
+  float* xchg = reinterpret_cast<float*>(cx.S.act + P.g1_x_off) + wg * 128 * 17;
+  const int ntiles = (hi - lo) * NT;
+  int epi = wg;        // next unit whose epilogue this group runs
+  int prev_loc = -1;   // unit of the group's previous tile
+  for (int i = wg; i < ntiles; i += 2) {
+    const int loc = i / NT, kt = i % NT, d = loc & 1;
+    for (; epi <= loc - 2; epi += 2) g1_epilogue(w, lo, epi, NT, tm, xchg);
+    const bool unit_start = loc != prev_loc;  // the group's first tile of this unit
+    prev_loc = loc;
+    bool ok = w.ok && !*cx.S.abort;
+    // this warp's accumulator of the unit's parity is free once the epilogue of unit
+    // loc - 2 has read it
+    if (unit_start && loc >= 2)
+      ok = __all_sync(0xffffffffu, ok && wait_bar(cx, &cx.S.tcbar[TB_D1_FREE + d], ((loc >> 1) - 1) & 1, PH_GEMM1));
+    const uint32_t t = w.ti + (uint32_t)i;
     const uint32_t s = t % kSlots;
-    bool got = w.ok && wait_tile(cx, t, PH_GEMM1);
-    const bool last_u = loc + kComputeWarps / 2 >= hi - lo;
-    if (loc == pair && half == 0) stamp_rt(P, EV_G1_FIRST_READY);
-    if (last_u && half == 0) stamp_rt(P, EV_G1_LAST_READY);
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    if (got) {
-      const int r8 = w.lane & 7;
-      const int rows[2] = {(int)toks[r8 < n ? r8 : 0], (int)toks[8 + r8 < n ? 8 + r8 : 0]};
-      if (n > 8) exp_unit_mma<2>(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, act_s, w.lane, rows);
-      else exp_unit_mma<1>(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, act_s, w.lane, rows);
-      __syncwarp();
-      if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps / 2);
-    }
-    if (!pair_reduce(w, acc, got, it)) {
-      w.ok = false;
-      break;
-    }
-    if (half == 0) {
-      const float gs = P.w1_gs[e] * kExpScaleUndo;
+    ok = __all_sync(0xffffffffu, ok && wait_tile(cx, t, PH_GEMM1));
+    if (loc == 0 && i < 2) stamp_rt(P, EV_G1_FIRST_READY);
+    if (i < 16 && w.lane == 0 && q == 0) stamp_any(P, EV_WG_G1_LANDED + i);
+    const uint8_t* tb = cx.S.ring + cx.S.slot_off[s];
+    uint32_t sw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // the row's block scales, bit 7 cleared
+    if (ok) {
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int i2 = 0; i2 < 2; ++i2) {
+        if (i2 * 256 >= tk) break;
+        const uint4 scw = *reinterpret_cast<const uint4*>(tb + exp_scale_off(dm.p) + m * (tk / 16) + i2 * 16);
+        sw[4 * i2 + 0] = scw.x & 0x7F7F7F7Fu; sw[4 * i2 + 1] = scw.y & 0x7F7F7F7Fu;
+        sw[4 * i2 + 2] = scw.z & 0x7F7F7F7Fu; sw[4 * i2 + 3] = scw.w & 0x7F7F7F7Fu;
+      }
+    }
+    const int n = i >> 1;  // the group's tile count so far
 #pragma unroll
-        for (int ii = 0; ii < 2; ++ii) {
-          const int p = nt * 8 + 2 * w.q + ii;
-          if (p < n) {
-            const int tok = toks[p], slot = cx.S.act_slot[a * 16 + p];
-            const float sc = cx.S.x_ts[tok] * gs;
-            const float gate = acc[nt][ii] * sc, up = acc[nt][2 + ii] * sc;
-            const float av = gate / (1.0f + expf(-gate)) * up;
-            st_relaxed_u32(aout + (size_t)slot * dm.f + jg * 8 + w.g, __float_as_uint(f32_canon(av)));
-          }
+    for (int h = 0; h < 4; ++h) {
+      if (h >= nch) break;
+      // the group's chunk n nch + h goes to its chunk buffer (n nch + h) & 1
+      const int cc = n * nch + h, b = wg * 2 + (cc & 1), use = cc >> 1;
+      if (use >= 1) {
+        ok = __all_sync(0xffffffffu, ok && wait_bar(cx, &cx.S.tcbar[TB_G1_FREE + b], (use - 1) & 1, PH_GEMM1));
+        if (ok) tc_fence_after();
+      }
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          // 16 code bytes = K 32 c .. 32 c + 31 of the chunk = two 16-element scale blocks
+          const uint4 cw = *reinterpret_cast<const uint4*>(tb + (h >> 1) * kExpBlockBytes + m * 128 +
+                                                           ((((4 * (h & 1) + c) ^ (m & 7))) << 4));
+          const int blk = 8 * h + 2 * c;
+          const uint32_t s0 = ue4m3_pair_f16(sw[blk >> 2], blk & 3), s1 = ue4m3_pair_f16(sw[(blk + 1) >> 2], (blk + 1) & 3);
+          uint32_t v[16];
+          e2m1x8_to_f16x8(cw.x, v[0], v[1], v[2], v[3]);
+          e2m1x8_to_f16x8(cw.y, v[4], v[5], v[6], v[7]);
+          e2m1x8_to_f16x8(cw.z, v[8], v[9], v[10], v[11]);
+          e2m1x8_to_f16x8(cw.w, v[12], v[13], v[14], v[15]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = hmul2(v[j], s0);
+#pragma unroll
+          for (int j = 8; j < 16; ++j) v[j] = hmul2(v[j], s1);
+          tmem_st16(tl + TM_ABUF + b * 64 + c * 16, v);
         }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      named_bar(2 + wg, 128);  // the chunk's 128 rows are in tensor memory
+      if (w.lane == 0 && ok) {
+        tc_fence_after();
+        if (h == 0 && i < 16 && q == 0) stamp_any(P, EV_TC_G1_READY + i);
+#pragma unroll
+        for (int jj = 2 * q; jj < 2 * q + 2; ++jj) {
+          const int ks = (kt * tk + h * 128) / 16 + jj;  // 16-column step of the pooled vectors
+          mma_f16_ts(tm + tm_d1(wg, q, d), tm + TM_ABUF + b * 64 + jj * 8,
+                     sdesc_k_sw128(act_s + (ks >> 2) * 2048 + (ks & 3) * 32), idesc_f16(16),
+                     !(unit_start && h == 0 && jj == 2 * q));
+        }
+        tc_commit(&cx.S.tcbar[TB_G1_FREE + b]);
+        // the group's last chunk of the unit: this issuer's accumulator is complete
+        if (h == nch - 1 && kt + 2 >= NT) tc_commit(&cx.S.tcbar[TB_D1_FULL + (wg * 4 + q) * 2 + d]);
+        if (h == nch - 1 && i < 16 && q == 0) stamp_any(P, EV_TC_G1_ISSUED + i);
+      }
+      __syncwarp();
     }
-    if (loc == pair && half == 0) stamp_rt(P, EV_G1_FIRST_DONE);
-    if (last_u && half == 0) stamp_rt(P, EV_G1_LAST_DONE);
+    // the tile's shared memory is read: release its ring slot
+    if (w.lane == 0 && ok) mbar_arrive(&cx.S.empty[s], kComputeWarps / 4);
+    if (!ok) w.ok = false;
   }
-  w.ti += (uint32_t)(hi - lo);
+  for (; epi < hi - lo; epi += 2) g1_epilogue(w, lo, epi, NT, tm, xchg);
+  if (hi > lo) stamp_rt(P, EV_G1_LAST_DONE);
+  w.ti += (uint32_t)ntiles;
+}
+
+// every MMA this thread issued has completed (bounded wait) before tensor memory is freed
+__device__ void tc_drain(uint64_t* bar) {
+  tc_commit(bar);
+  const uint64_t dl = globaltimer() + 50000000ull;
+  for (uint32_t it = 0; !mbar_try_wait(bar, 0); ++it)
+    if ((it & 15) == 0 && globaltimer() > dl) break;
+}
+
+// GEMM2 epilogue of block-local unit `loc` (expert a of the round starting at a0):
+// y rows of the expert's token slots, bf16
+__device__ void g2_epilogue(Worker& w, int lo, int loc, int a0, uint32_t tm) {
+  Ctx& cx = *w.cx;
+  const LaunchParams& P = *cx.P;
+  const Dims& dm = P.dm;
+  const int upe = w2_units(dm.p);
+  const int gu = lo + loc, a = gu / upe, pr = gu % upe, ea = a - a0;
+  const int e = cx.S.act_e[a], n = cx.S.act_n[a];
+  const int q = w.cw & 3, m = q * 32 + w.lane;
+  const int d = loc & 1;
+  uint32_t r[16];
+  const bool ok = __all_sync(0xffffffffu, w.ok && wait_bar(cx, &cx.S.tcbar[TB_D2_FULL + d], (loc >> 1) & 1, PH_GEMM2));
+  if (ok) {
+    tc_fence_after();
+    tmem_ld16(tm + tm_lane(q) + TM_D2 + d * 16, r);
+    tmem_ld_wait();
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (w.lane == 0) mbar_arrive(&cx.S.tcbar[TB_D2_FREE + d], 1);
+  if (ok) {
+    uint16_t* yout = reinterpret_cast<uint16_t*>(P.s_buf + P.so.y);
+    const float gs = P.w2_gs[e];
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+      if (p < n) {
+        const int slot = cx.S.act_slot[a * 16 + p];
+        const float sc = cx.S.a_ts[ea * 16 + p] * gs;
+        st_relaxed_u16(yout + (size_t)slot * dm.p + pr * kExpTileRows + m, bf16_bits_rn(__uint_as_float(r[p]) * sc));
+      }
+    }
+  } else {
+    w.ok = false;
+  }
 }
 
 __device__ void gemm2_phase(Worker& w) {
@@ -1742,28 +1861,29 @@ __device__ void gemm2_phase(Worker& w) {
   const LaunchParams& P = *cx.P;
   const Dims& dm = P.dm;
   const int G = gridDim.x;
-  const int na = *cx.S.n_active, u2pe = dm.p / 16;
+  const int tk = exp_tile_k(dm.f), nmma = tk / 64;  // tile columns, K=64 MMAs per tile
+  const int na = *cx.S.n_active, upe = w2_units(dm.p), NT = dm.f / tk;
   int lo, hi;
-  unit_range(na * u2pe, rot_block(cx.block, P.phase_rot * 7, G), G, lo, hi);
+  unit_range(na * upe, rot_block(cx.block, P.phase_rot * 7, G), G, lo, hi);
   const float* ain = reinterpret_cast<const float*>(P.x_cur + P.xo.a);
-  uint16_t* yout = reinterpret_cast<uint16_t*>(P.s_buf + P.so.y);
-  const uint32_t region = (uint32_t)dm.f * 32;  // one expert's 16 activation rows, f16, B layout
-  const int pair = w.cw >> 1, half = w.cw & 1, ng = dm.f / 64;
-  const int g0 = half ? ng / 2 : 0, g1 = half ? ng : ng / 2;
-  int it = 0;
+  const uint32_t region = (uint32_t)dm.f * 8;  // one expert's 16 activation rows, E2M1, B layout
+  uint8_t* g2b = cx.S.act + P.g2_off;          // the round's two experts' B operands
+  uint8_t* sfb_stage = g2b + 2 * region;       // [2][16][F/16] UE4M3 block scales
+  const int wg = w.cw >> 2, q = w.cw & 3, m = q * 32 + w.lane;
+  const uint32_t tm = *cx.S.tmem_base, tl = tm + tm_lane(q);
+  const int tid = w.cw * 32 + w.lane;
   if (hi > lo) {
-    const int a_first = lo / u2pe, a_last = (hi - 1) / u2pe;
-    // the block's experts two at a time (one round unless its units span more than
-    // two), so that a block whose units cross an expert boundary does not stop half
-    // way to stage the second expert's input
+    const int a_first = lo / upe, a_last = (hi - 1) / upe;
+    int epi = wg;  // next unit whose epilogue this group runs
+    // the block's experts two at a time (one round unless its units span more than two)
     for (int a0 = a_first; a0 <= a_last; a0 += 2) {
       const int a1 = min(a0 + 1, a_last);
-      cbar();  // the previous round's units are done with the act buffer
+      cbar();  // the previous round's MMAs and epilogues are done with the staged operands
       if (a0 != a_first) stamp_rt(P, EV_G2_STAGE2_IN);
       if (*cx.S.abort) w.ok = false;
       // NVFP4 of every activation row of the round: row p of expert a = its p-th token
       const int n0 = cx.S.act_n[a0], nrows = n0 + (a1 > a0 ? cx.S.act_n[a1] : 0);
-      float* rowbuf = reinterpret_cast<float*>(cx.S.act + 2 * region) + (size_t)w.cw * dm.f;
+      float* rowbuf = reinterpret_cast<float*>(g2b + ((2 * region + 2 * dm.f + 1023) & ~1023u)) + (size_t)w.cw * dm.f;
       for (int r = w.cw; r < nrows && w.ok; r += kComputeWarps) {
         const int ea = r < n0 ? 0 : 1, p = r - ea * n0;
         const float* row = ain + (size_t)cx.S.act_slot[(a0 + ea) * 16 + p] * dm.f;
@@ -1800,10 +1920,10 @@ __device__ void gemm2_phase(Worker& w) {
         float ts = __fdiv_rn(amax, 2688.0f);  // amax / (6 * 448), rounded up to a power of two
         if (ts > 0.f) {
           int ex;
-          const float m = frexpf(ts, &ex);
-          if (m != 0.5f) ts = ldexpf(1.0f, ex);
+          const float mn = frexpf(ts, &ex);
+          if (mn != 0.5f) ts = ldexpf(1.0f, ex);
         }
-        uint8_t* act = cx.S.act + ea * region;
+        uint8_t* bq = g2b + ea * region;
         for (int base = 0; base < dm.f; base += 128) {
           const int k = base + w.lane * 4;
           const bool in = k < dm.f;
@@ -1814,76 +1934,157 @@ __device__ void gemm2_phase(Worker& w) {
           uint32_t sc = 0;
           if (ts > 0.f) sc = f32_to_e4m3(__fdiv_rn(bmax, __fmul_rn(6.0f, ts)));
           const float denom = __fmul_rn(e4m3_to_f32(sc), ts);
-          const uint32_t s2 = e4m3x2_to_f16x2(sc | (sc << 8));
           uint32_t c01 = 0, c23 = 0;
           if (sc != 0) {
             c01 = f32x2_to_e2m1x2(__fdiv_rn(x.x, denom), __fdiv_rn(x.y, denom));
             c23 = f32x2_to_e2m1x2(__fdiv_rn(x.z, denom), __fdiv_rn(x.w, denom));
           }
           if (in) {
-            *reinterpret_cast<uint32_t*>(act + act_off(p, k) + (k & 7) * 2) = hmul2(e2m1x2_to_f16x2(c01), s2);
-            *reinterpret_cast<uint32_t*>(act + act_off(p, k + 2) + ((k + 2) & 7) * 2) = hmul2(e2m1x2_to_f16x2(c23), s2);
+            // row p, byte k / 2 of the B operand: 256-column blocks of 16 rows x 128 bytes
+            const int kb = k >> 8, bir = (k & 255) >> 1;
+            *reinterpret_cast<uint16_t*>(bq + kb * 2048 + p * 128 + ((((bir >> 4) ^ (p & 7))) << 4) + (bir & 15)) =
+                (uint16_t)(c01 | (c23 << 8));
+            if ((w.lane & 3) == 0) sfb_stage[(ea * 16 + p) * (dm.f / 16) + (k >> 4)] = (uint8_t)sc;
           }
         }
         __syncwarp();  // the warp's next row reuses rowbuf
         if (w.lane == 0) cx.S.a_ts[ea * 16 + p] = ts;
       }
       w.ok = __all_sync(0xffffffffu, w.ok);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // B rows -> the MMAs
       cbar();
+      // activation block scales -> tensor memory: lane p of every quadrant, per K=64 step
+      // one word (its four scales) in four columns; rows past the expert's tokens hold 0
+      if (wg == 0 && w.ok) {
+        const int nk = dm.f / 64;
+        for (int ea = 0; ea <= a1 - a0; ++ea) {
+          const int na_rows = cx.S.act_n[a0 + ea];
+          for (int g = 0; g < nk; g += 4) {
+            uint32_t v[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t wd = (w.lane < na_rows && g + j < nk)
+                                      ? *reinterpret_cast<const uint32_t*>(sfb_stage + (ea * 16 + w.lane) * (dm.f / 16) + 4 * (g + j))
+                                      : 0u;
+              v[4 * j] = v[4 * j + 1] = v[4 * j + 2] = v[4 * j + 3] = wd;
+            }
+            tmem_st16(tl + TM_SFB + ea * 64 + g * 4, v);
+          }
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      cbar();
+      if (tid == 0) mbar_arrive(&cx.S.tcbar[TB_G2_STAGE], 1);
       if (a0 == a_first) stamp_rt(P, EV_GEMM2_IN);
       else stamp_rt(P, EV_G2_STAGE2_DONE);
       if (*cx.S.abort) w.ok = false;
-      for (int a = a0; a <= a1; ++a) {
-        const int e = cx.S.act_e[a], n = cx.S.act_n[a], ea = a - a0;
-        const uint32_t act_s = smem_u32(cx.S.act) + ea * region;
-        const int u_lo = max(lo, a * u2pe), u_hi = min(hi, (a + 1) * u2pe);
-        // units of this expert: pair j takes every 4th (counted from the block's first unit)
-        int gu = u_lo + ((pair - (u_lo - lo)) % (kComputeWarps / 2) + kComputeWarps / 2) % (kComputeWarps / 2);
-        for (; gu < u_hi; gu += kComputeWarps / 2, ++it) {
-          const int loc = gu - lo;
-          const int pr = gu % u2pe;
-          const uint32_t t = w.ti + (uint32_t)loc;
-          const uint32_t s = t % kSlots;
-          bool got = w.ok && wait_tile(cx, t, PH_GEMM2);
-          const bool first_u = gu - pair < lo + kComputeWarps / 2 && a == a_first;
-          const bool last_u = gu + kComputeWarps / 2 >= hi;
-          if (half == 0 && first_u) stamp_rt(P, EV_G2_FIRST_READY);
-          if (half == 0 && last_u) stamp_rt(P, EV_G2_LAST_READY);
-          float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-          if (got) {
-            const int r8 = w.lane & 7;
-            const int rows[2] = {r8 < n ? r8 : 0, 8 + r8 < n ? 8 + r8 : 0};
-            if (n > 8) exp_unit_mma<2>(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, act_s, w.lane, rows);
-            else exp_unit_mma<1>(acc, cx.S.ring + cx.S.slot_off[s], g0, g1, act_s, w.lane, rows);
-            __syncwarp();
-            if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps / 2);
-          }
-          if (!pair_reduce(w, acc, got, it)) {
+      // this round's units: weight block scales of the group's tiles -> tensor memory
+      const int u_lo = max(lo, a0 * upe), u_hi = min(hi, (a1 + 1) * upe);
+      const int i_lo = (u_lo - lo) * NT, i_hi = (u_hi - lo) * NT;
+      for (int i = i_lo + ((i_lo & 1) != wg ? 1 : 0); i < i_hi && w.ok; i += 2) {
+        const int loc = i / NT;
+        for (; epi <= loc - 2 && w.ok; epi += 2) g2_epilogue(w, lo, epi, a0, tm);
+        if (!w.ok) break;
+        const int n = i >> 1, b = 2 * wg + (n & 1), use = n >> 1;
+        if (use >= 1) {
+          if (!__all_sync(0xffffffffu, wait_bar(cx, &cx.S.tcbar[TB_SFA_FREE + b], (use - 1) & 1, PH_GEMM2))) {
             w.ok = false;
             break;
           }
-          if (half == 0) {
-            const float gs = P.w2_gs[e] * kExpScaleUndo;
-  #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-  #pragma unroll
-              for (int ii = 0; ii < 2; ++ii) {
-                const int p = nt * 8 + 2 * w.q + ii;
-                if (p < n) {
-                  const int slot = cx.S.act_slot[a * 16 + p];
-                  const float sc = cx.S.a_ts[ea * 16 + p] * gs;
-                  st_relaxed_u16(yout + (size_t)slot * dm.p + pr * 16 + w.g, bf16_bits_rn(acc[nt][ii] * sc));
-                  st_relaxed_u16(yout + (size_t)slot * dm.p + pr * 16 + w.g + 8, bf16_bits_rn(acc[nt][2 + ii] * sc));
-                }
-              }
+          tc_fence_after();
+        }
+        const uint32_t t = w.ti + (uint32_t)i;
+        if (!__all_sync(0xffffffffu, wait_tile(cx, t, PH_GEMM2))) {
+          w.ok = false;
+          break;
+        }
+        if (i < 2 && a0 == a_first) stamp_rt(P, EV_G2_FIRST_READY);
+        // the row's scale word of each K=64 step in four columns (row m reads lane m,
+        // column + m / 32)
+#pragma unroll
+        for (int i2 = 0; i2 < 2; ++i2) {
+          if (i2 * 4 >= nmma) break;
+          const uint4 scw = *reinterpret_cast<const uint4*>(cx.S.ring + cx.S.slot_off[t % kSlots] + exp_scale_off(dm.f) +
+                                                            m * (tk / 16) + i2 * 16);
+          const uint32_t v[16] = {scw.x, scw.x, scw.x, scw.x, scw.y, scw.y, scw.y, scw.y,
+                                  scw.z, scw.z, scw.z, scw.z, scw.w, scw.w, scw.w, scw.w};
+          tmem_st16(tl + TM_SFA + b * 32 + i2 * 16, v);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (w.lane == 0) mbar_arrive(&cx.S.tcbar[TB_SFA_FULL + b], 1);
+      }
+      // every epilogue of the round before its operands are replaced
+      for (; epi < u_hi - lo && w.ok; epi += 2) g2_epilogue(w, lo, epi, a0, tm);
+    }
+    stamp_rt(P, EV_G2_LAST_DONE);
+  }
+  w.ti += (uint32_t)((hi - lo) * NT);
+}
+
+// The tensor-core warp: one thread issues every GEMM2 MMA of the block in tile order
+// (orcarouter.ai, § "where the kernel boundary sits": warps dedicated to driving the
+// tensor cores), and the ring tiles go back to the loader when their MMAs are done.
+__device__ void tc_issuer(Ctx& cx) {
+  const LaunchParams& P = *cx.P;
+  const Dims& dm = P.dm;
+  uint64_t* tb = cx.S.tcbar;
+  const uint32_t tm = *cx.S.tmem_base;
+  const int G = gridDim.x;
+  const uint32_t act_s = smem_u32(cx.S.act + P.g2_off);  // GEMM2 operand B of the round
+  bool ok = wait_bar(cx, &tb[TB_ROUTED], 0, PH_ROUTE);
+  if (ok) {
+    const int tk = exp_tile_k(dm.f), nmma = tk / 64;
+    const int na = *cx.S.n_active, upe = w2_units(dm.p), NT = dm.f / tk;
+    int lo, hi;
+    unit_range(na * upe, rot_block(cx.block, P.phase_rot * 7, G), G, lo, hi);
+    const uint32_t t0 = *cx.S.tc_ti, region = (uint32_t)dm.f * 8;
+    if (hi > lo) {
+      const int a_first = lo / upe, a_last = (hi - 1) / upe;
+      int round = 0;
+      for (int a0 = a_first; a0 <= a_last && ok; a0 += 2, ++round) {
+        const int a1 = min(a0 + 1, a_last);
+        ok = wait_bar(cx, &tb[TB_G2_STAGE], round & 1, PH_GEMM2);
+        if (!ok) break;
+        tc_fence_after();
+        const int u_lo = max(lo, a0 * upe), u_hi = min(hi, (a1 + 1) * upe);
+        for (int gu = u_lo; gu < u_hi && ok; ++gu) {
+          const int loc = gu - lo, ea = gu / upe - a0, d = loc & 1;
+          if (loc >= 2) {
+            ok = wait_bar(cx, &tb[TB_D2_FREE + d], ((loc >> 1) - 1) & 1, PH_GEMM2);
+            if (!ok) break;
+            tc_fence_after();
           }
-          if (half == 0 && first_u) stamp_rt(P, EV_G2_FIRST_DONE);
-          if (half == 0 && last_u) stamp_rt(P, EV_G2_LAST_DONE);
+          for (int kt = 0; kt < NT && ok; ++kt) {
+            const int i = loc * NT + kt, n = i >> 1, b = 2 * (i & 1) + (n & 1);
+            ok = wait_bar(cx, &tb[TB_SFA_FULL + b], (n >> 1) & 1, PH_GEMM2);
+            const uint32_t t = t0 + (uint32_t)i;
+            if (ok) ok = wait_tile(cx, t, PH_GEMM2);
+            if (!ok) break;
+            if (i < 8) stamp_any(P, EV_TC_G2_READY + i);
+            tc_fence_after();
+            const uint32_t a_s = smem_u32(cx.S.ring + cx.S.slot_off[t % kSlots]);
+            for (int j = 0; j < nmma; ++j) {
+              const int kb = j >> 2, jj = j & 3;  // 16 KB column block, K=64 step inside it
+              mma_nvf4_ss(tm + TM_D2 + d * 16, sdesc_k_sw128(a_s + kb * kExpBlockBytes + jj * 32),
+                          sdesc_k_sw128(act_s + ea * region + (kt * (tk / 256) + kb) * 2048 + jj * 32), idesc_nvf4(16),
+                          tm + TM_SFA + b * 32 + j * 4, tm + TM_SFB + ea * 64 + (kt * nmma + j) * 4, (kt | j) != 0);
+            }
+            tc_commit(&tb[TB_SFA_FREE + b]);
+            // the ring slot goes back to the loader when the tile's MMAs are done: one
+            // arrival per commit, as many as a slot's consumers give
+#pragma unroll
+            for (int c = 0; c < kComputeWarps; ++c) tc_commit(&cx.S.empty[t % kSlots]);
+            if (i < 8) stamp_any(P, EV_TC_G2_ISSUED + i);
+          }
+          if (ok) tc_commit(&tb[TB_D2_FULL + d]);
         }
       }
     }
   }
-  w.ti += (uint32_t)(hi - lo);
+  tc_drain(&tb[TB_DRAIN]);
 }
 
 // z[t] = bf16(sum_c w[t][c] * y[t*k + c]); each y element has this one consumer,
@@ -2114,6 +2315,11 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
     }
     mbar_init(cx.S.route_bar, 1);
     mbar_init(cx.S.stage_bar, 1);
+    for (int i = 0; i < kTcBars; ++i) {
+      const bool by4 = (i >= TB_G1_FREE && i < TB_G1_FREE + 4) || (i >= TB_D1_FREE && i < TB_D1_FREE + 2) ||
+                       (i >= TB_SFA_FULL && i < TB_SFA_FULL + 4) || (i >= TB_D2_FREE && i < TB_D2_FREE + 2);
+      mbar_init(&cx.S.tcbar[i], i == TB_DONE ? kComputeWarps : by4 ? 4 : 1);
+    }
     for (int i = 0; i < kSlots; ++i) cx.S.slot_tile[i] = 0xFFFFFFFFu;
     *cx.S.abort = (smem_u32(smem) & 1023u) != 0u;  // the swizzled tiles need 1 KB alignment
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -2149,10 +2355,19 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
       cx.S.tpos[lane] = pos0 + dep;
     }
   }
+  if (warp == 2) {
+    // the tensor-core warp holds the block's tensor memory for the whole launch (one
+    // block per SM, so the columns are free once the previous launch's block has left)
+    tmem_alloc(cx.S.tmem_base, kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
   __syncthreads();
+  tc_fence_after();
   cx.pos0 = *cx.S.pos0;
   if (*cx.S.abort || cx.pos0 < 0) {
     if (threadIdx.x == 0 && atomicCAS(&P.status->code, 0, 2) == 0) P.status->phase = PH_START;
+    if (warp == 2) tmem_dealloc(*cx.S.tmem_base, kTmemCols);
     pdl_launch_dependents();
     return;
   }
@@ -2161,9 +2376,26 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
     pdl_launch_dependents();
     return;
   }
-  if (warp == 1 || warp == 2) {
+  if (warp == 1) {
     pdl_wait();
-    rearm(P, blockIdx.x, threadIdx.x - 32, 64);
+    rearm(P, blockIdx.x, lane, 32);
+    pdl_launch_dependents();
+    return;
+  }
+  if (warp == 2) {
+    pdl_wait();
+    cx.deadline = globaltimer() + (((uint64_t)P.timeout_ns_hi << 32) | P.timeout_ns_lo);
+    if (lane == 0) tc_issuer(cx);
+    __syncwarp();
+    // free tensor memory once the compute warps are done with it
+    if (lane == 0) {
+      const uint64_t dl = globaltimer() + (((uint64_t)P.timeout_ns_hi << 32) | P.timeout_ns_lo) + 50000000ull;
+      for (uint32_t it = 0; !mbar_try_wait(&cx.S.tcbar[TB_DONE], 0); ++it)
+        if ((it & 15) == 0 && globaltimer() > dl) break;
+    }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(*cx.S.tmem_base, kTmemCols);
     pdl_launch_dependents();
     return;
   }
@@ -2172,7 +2404,7 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
     if ((P.flags & 0x2u) && P.hist_prev != nullptr && P.prefetch_experts > 0) {
       // the previous step's most-used experts of this layer -> L2 (block-strided slices)
       const Dims& dm = P.dm;
-      const uint64_t ub1 = exp_unit_bytes(dm.p) * (dm.f / 8), ub2 = exp_unit_bytes(dm.f) * (dm.p / 16);
+      const uint64_t ub1 = exp_unit_bytes(dm.p) * w1_units(dm.f), ub2 = exp_unit_bytes(dm.f) * w2_units(dm.p);
       uint32_t taken[kMaxExperts / 32] = {0};
       for (int c = 0; c < P.prefetch_experts && c < dm.e; ++c) {
         uint32_t best = 0;
@@ -2218,6 +2450,11 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
   stamp<kTiming>(P, blockIdx.x, EV_START);
   compute_main<kTiming>(w);
   stamp<kTiming>(P, blockIdx.x, EV_END);
+  // every MMA this warp issued has completed before the block frees tensor memory
+  if (lane == 0) tc_drain(&cx.S.tcbar[TB_WDRAIN + w.cw]);
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&cx.S.tcbar[TB_DONE], 1);
 }
 
 const void* layer_kernel(bool timing) {

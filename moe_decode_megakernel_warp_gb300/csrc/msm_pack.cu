@@ -8,10 +8,12 @@
 // epilogue thread holds both halves of a pair: the q/k rows of a head as
 // (d, d + hd/2) for rotate-half RoPE, and W1 as (gate j, up j) for SwiGLU.
 //
-// NVFP4 expert matrices become 16-row units of 64-column groups (576 bytes):
-// 512 bytes of E2M1 codes ordered [row][quad q][k-step][2 bytes: the bytes
-// holding columns 2q,2q+1 and 2q+8,2q+9], then 64 bytes of E4M3 scales
-// [row][k-step], so each thread loads its A-fragment codes with one 8-byte load.
+// NVFP4 expert matrices become 128-row units of 512-column tiles (256 where the width is
+// not a multiple of 512): column blocks of 128 rows x 128 code bytes in the 128-byte
+// swizzle layout the tensor cores read (and the dequantising threads read without bank
+// conflicts), then each row's block scales.  W1 units
+// hold 64 gate rows then the 64 matching up rows, so one unit feeds the SwiGLU
+// epilogue.
 #include "msm_device.cuh"
 #include "msm_internal.h"
 
@@ -48,36 +50,31 @@ __global__ void pack_dense_kernel(const uint16_t* __restrict__ W, uint8_t* __res
   }
 }
 
-// one thread per (expert, unit, group, row)
+// one thread per (expert, unit, k-tile, row): the row's code bytes of the tile go to row m
+// of each 16 KB column block with 16-byte chunk c at chunk c ^ (m & 7) (the 128-byte
+// swizzle of a K-major tensor-core operand), its block scales to the tile's scale rows
 __global__ void pack_nvfp4_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ sf,
                                   uint8_t* __restrict__ out, int E, int rows, int K, int swiglu, int F) {
-  const int units = swiglu ? F / 8 : rows / 16;
-  const int ng = K / 64;
-  const long long total = (long long)E * units * ng * 16;
+  const int units = swiglu ? w1_units(F) : w2_units(rows);
+  const int tk = exp_tile_k(K), nt = K / tk, nkb = tk / kExpBlockK;
+  const long long total = (long long)E * units * nt * kExpTileRows;
   for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < total;
        c += (long long)gridDim.x * blockDim.x) {
-    const int r = (int)(c & 15);
-    const long long rest = c >> 4;
-    const int gi = (int)(rest % ng);
-    const long long eu = rest / ng;
+    const int m = (int)(c % kExpTileRows);
+    const long long rest = c / kExpTileRows;
+    const int kt = (int)(rest % nt);
+    const long long eu = rest / nt;
     const int u = (int)(eu % units), e = (int)(eu / units);
-    const int R = swiglu ? ((r < 8) ? u * 8 + r : F + u * 8 + (r - 8)) : u * 16 + r;
-    const uint8_t* crow = codes + ((size_t)e * rows + R) * (K / 2) + gi * 32;
-    const uint8_t* srow = sf + ((size_t)e * rows + R) * (K / 16) + gi * 4;
-    uint8_t* gout = out + ((size_t)eu * ng + gi) * kExpGroupBytes;
-    uint8_t cb[32];
+    const int R = swiglu ? ((m < 64) ? u * 64 + m : F + u * 64 + (m - 64)) : u * kExpTileRows + m;
+    const uint4* crow = reinterpret_cast<const uint4*>(codes + ((size_t)e * rows + R) * (K / 2) + (size_t)kt * (tk / 2));
+    const uint4* srow = reinterpret_cast<const uint4*>(sf + ((size_t)e * rows + R) * (K / 16) + (size_t)kt * (tk / 16));
+    uint8_t* tile = out + ((size_t)eu * nt + kt) * exp_tile_bytes(K);
+    for (int kb = 0; kb < nkb; ++kb)
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        cb[q * 8 + ks * 2 + 0] = crow[ks * 8 + q];
-        cb[q * 8 + ks * 2 + 1] = crow[ks * 8 + q + 4];
-      }
-#pragma unroll
-    for (int i = 0; i < 32; i += 16)
-      *reinterpret_cast<uint4*>(gout + r * 32 + i) = *reinterpret_cast<const uint4*>(cb + i);
-    *reinterpret_cast<uint32_t*>(gout + 512 + r * 4) =
-        (uint32_t)srow[0] | ((uint32_t)srow[1] << 8) | ((uint32_t)srow[2] << 16) | ((uint32_t)srow[3] << 24);
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(tile + kb * kExpBlockBytes + m * 128 + ((ch ^ (m & 7)) << 4)) = crow[kb * 8 + ch];
+    for (int i = 0; i < tk / 256; ++i)
+      *reinterpret_cast<uint4*>(tile + exp_scale_off(K) + m * (tk / 16) + i * 16) = srow[i];
   }
 }
 

@@ -51,21 +51,6 @@ def _assert_same(got, want):
         assert np.array_equal(a, b)
 
 
-def _a256(x):
-    return (x + 255) // 256 * 256
-
-
-def _scratch_need(cfg, splits):
-    """Bytes of static scratch one step needs (the sum msm.h states)."""
-    g = cfg.hq // cfg.hkv
-    x = sum(_a256(b) for b in (T * cfg.hq * cfg.hd * 2, T * cfg.d * 2, T * cfg.p * 2, T * cfg.e * 4,
-                                 T * cfg.k * cfg.f * 4, T * cfg.p * 2, T * cfg.d * 2, T * cfg.hq * cfg.hd * 2,
-                                 2 * cfg.hkv * T * cfg.hd * 2))
-    s = sum(_a256(b) for b in (cfg.hkv * splits * T * g * cfg.hd * 4, cfg.hkv * splits * T * g * 2 * 4,
-                                 T * cfg.k * cfg.p * 2))
-    return 2 * x + s + 2 * _a256(T * cfg.hq * cfg.hd * 2) + 2 * _a256(T * cfg.d * 2)
-
-
 @pytest.mark.parametrize("name", ["cfg1_stack", "cfg2"])
 def test_noalloc_matches_verify_step_on_two_calls_in_a_row(name):
     torch = pytest.importorskip("torch")
@@ -83,6 +68,7 @@ def test_noalloc_matches_verify_step_on_two_calls_in_a_row(name):
         assert model.sync() == msm.MSM_OK
         want = _host(lg, ho, kc, vc)
         # two no-allocation calls back to back on one stream, one sync after both
+        launches0 = model.stats().launches_run
         runs = []
         for _ in range(2):
             kc2, vc2 = _caches(case, dev)
@@ -90,6 +76,7 @@ def test_noalloc_matches_verify_step_on_two_calls_in_a_row(name):
             model.verify_step_noalloc(hid, case.parent, case.pos0, kc2, vc2, logits_out=lg2, hidden_out=ho2)
             runs.append((lg2, ho2, kc2, vc2))
         assert model.sync() == msm.MSM_OK
+        assert model.stats().launches_run == launches0 + 2 * cfg.n_layers
         for r in runs:
             _assert_same(_host(*r), want)
         # and the model-owned path is unaffected afterwards
@@ -113,7 +100,8 @@ def test_noalloc_rejects_a_model_whose_scratch_does_not_fit():
     dev = torch.device("cuda", 0)
     model = _model(case, dev)
     try:
-        if _scratch_need(cfg, model.stats().attn_splits) <= msm.MSM_NOALLOC_SCRATCH_BYTES:
+        need = model.stats().noalloc_scratch_bytes
+        if need <= msm.MSM_NOALLOC_SCRATCH_BYTES:
             pytest.skip("on this GPU's SM count the case fits the static scratch")
         kc, vc = _caches(case, dev)
         lg, ho = _outputs(cfg, dev)
@@ -121,7 +109,7 @@ def test_noalloc_rejects_a_model_whose_scratch_does_not_fit():
         with pytest.raises(msm.MsmError) as ei:
             model.verify_step_noalloc(hid, case.parent, case.pos0, kc, vc, logits_out=lg, hidden_out=ho)
         assert ei.value.code == msm.MSM_ERR_UNSUPPORTED
-        assert "bytes of scratch" in str(ei.value) and str(msm.MSM_NOALLOC_SCRATCH_BYTES) in str(ei.value)
+        assert "%d bytes of scratch" % need in str(ei.value) and str(msm.MSM_NOALLOC_SCRATCH_BYTES) in str(ei.value)
         assert model.sync() == msm.MSM_OK  # nothing was launched
     finally:
         model.close()
