@@ -195,87 +195,97 @@ def sample_layers(cfg):
     return [l for l in (swa, glb) if l is not None]
 
 
-def oracle_step_ms(cfg, seed, bias, min_seconds=10.0, max_seconds=30.0):
-    """Time the oracle on a bounded sample of one step -- the sample layers, evaluated
-    repeatedly for about min_seconds, and one eighth of the LM head -- and extrapolate
-    to the whole step (46 sliding-window + 16 global layers + LM head)."""
+def oracle_sampler(cfg, seed, bias):
+    """A sampled step of the CPU oracle on the host cores: one evaluation of a
+    sliding-window or a global layer of this workload (alternating) plus the LM head,
+    extrapolated to the whole step (every sliding-window layer at the latest
+    sliding-window time, every global one at the latest global time, the LM head from
+    one timed eighth of its rows).  Both the reference arm and the CPU baseline of our
+    arm time steps with this.  Returns (next_step() -> ms, description, threads)."""
+    import dataclasses
     import oracle
     parent = synth.parent_array(seed)
     h = synth.hidden_in(cfg, seed)
     layers = sample_layers(cfg)
     wts = {l: host_layer_weights(cfg, seed, bias, l) for l in layers}
     kv = {l: synth.kv_history(cfg, seed, l) for l in layers}
-    times = {l: [] for l in layers}
-    t_start = time.perf_counter()
-    i = 0
-    while True:
-        l = layers[i % len(layers)]
-        k, v = kv[l][0].copy(), kv[l][1].copy()
-        t0 = time.perf_counter()
-        oracle.layer(cfg, wts[l], cfg.is_global(l), h, parent, cfg.pos0, k, v)
-        times[l].append(time.perf_counter() - t0)
-        i += 1
-        el = time.perf_counter() - t_start
-        if (el >= min_seconds and i >= len(layers)) or el >= max_seconds:
-            break
     lm_s = 0.0
     if cfg.vocab:
-        import dataclasses
         c8 = dataclasses.replace(cfg, vocab=cfg.vocab // 8)
         fw = synth.final_weights(c8, seed)
         t0 = time.perf_counter()
         oracle.lm_head(c8, fw["norm_final"], fw["w_lm"], h)
         lm_s = (time.perf_counter() - t0) * 8
     n_glob = sum(1 for l in range(cfg.n_layers) if cfg.is_global(l))
-    mean = {l: statistics.mean(v) for l, v in times.items()}
-    t_swa = next((mean[l] for l in layers if not cfg.is_global(l)), None)
-    t_glb = next((mean[l] for l in layers if cfg.is_global(l)), None)
-    t_swa = t_glb if t_swa is None else t_swa
-    t_glb = t_swa if t_glb is None else t_glb
-    step_ms = ((cfg.n_layers - n_glob) * t_swa + n_glob * t_glb + lm_s) * 1e3
-    sample = ("CPU oracle (fp64) on %d host threads: %d evaluations of layers %s of this workload (%.1f s) "
-              "plus 1/8 of the LM head, extrapolated to %d layers + LM head"
-              % (oracle.num_threads(), i, layers, sum(sum(v) for v in times.values()), cfg.n_layers))
-    return step_ms, sample, oracle.num_threads()
+    last = {}
+    state = {"i": 0}
 
-
-def run_reference(args):
-    """The reference arm: the CPU oracle, on the host cores, on a bounded sample of
-    the same workload per step (rank 0 only)."""
-    rank, world, _ = dist_env()
-    if rank != 0:
-        return 0
-    import oracle
-    cfg = synth.CONFIGS[args.workload]
-    seeds = synth.parity_seeds(args.workload)
-    seed, bias = seeds["seed"], seeds["bias_seeds"]
-    parent = synth.parent_array(seed)
-    h = synth.hidden_in(cfg, seed)
-    layers = sample_layers(cfg)
-    wts = {l: host_layer_weights(cfg, seed, bias, l) for l in layers}
-    kv = {l: synth.kv_history(cfg, seed, l) for l in layers}
-    per = {l: [] for l in layers}
-    for i in range(args.warmup + args.steps):
-        l = layers[i % len(layers)]
+    def timed_layer(l):
         k, v = kv[l][0].copy(), kv[l][1].copy()
         t0 = time.perf_counter()
         oracle.layer(cfg, wts[l], cfg.is_global(l), h, parent, cfg.pos0, k, v)
-        if i >= args.warmup:
-            per[l].append(time.perf_counter() - t0)
-    n_glob = sum(1 for l in range(cfg.n_layers) if cfg.is_global(l))
-    mean = {l: statistics.mean(v) for l, v in per.items() if v}
-    t_any = statistics.mean(mean.values())
-    t_swa = next((mean[l] for l in mean if not cfg.is_global(l)), t_any)
-    t_glb = next((mean[l] for l in mean if cfg.is_global(l)), t_any)
-    step_ms = ((cfg.n_layers - n_glob) * t_swa + n_glob * t_glb) * 1e3
-    sample = ("each step: one decoder layer of this workload on the CPU oracle (alternating sliding-window and "
-              "global layers), extrapolated to %d layers; LM head not included" % cfg.n_layers)
+        last[l] = time.perf_counter() - t0
+
+    for l in layers:  # one evaluation of each kind before the first step
+        timed_layer(l)
+
+    def next_step():
+        l = layers[state["i"] % len(layers)]
+        state["i"] += 1
+        timed_layer(l)
+        t_swa = next((last[x] for x in layers if not cfg.is_global(x)), None)
+        t_glb = next((last[x] for x in layers if cfg.is_global(x)), None)
+        t_swa = t_glb if t_swa is None else t_swa
+        t_glb = t_swa if t_glb is None else t_glb
+        return ((cfg.n_layers - n_glob) * t_swa + n_glob * t_glb + lm_s) * 1e3
+
+    desc = ("CPU oracle (fp64, OpenMP) on %d host threads; each step = one timed evaluation of layer %s of this "
+            "workload (alternating sliding-window / global), extrapolated to %d layers, plus the LM head "
+            "extrapolated from one timed eighth of its rows (%.2f s): an extrapolated step, not a timed one"
+            % (oracle.num_threads(), " / ".join(str(x) for x in layers), cfg.n_layers, lm_s))
+    return next_step, desc, oracle.num_threads()
+
+
+def oracle_step_ms(cfg, seed, bias, min_seconds=10.0, max_seconds=30.0):
+    """The CPU baseline of our arm: sampled oracle steps for about min_seconds
+    (at most max_seconds); the median extrapolated step."""
+    t_start = time.perf_counter()
+    next_step, desc, threads = oracle_sampler(cfg, seed, bias)
+    vals = []
+    while True:
+        vals.append(next_step())
+        el = time.perf_counter() - t_start
+        if (el >= min_seconds and len(vals) >= 2) or el >= max_seconds:
+            break
+    return statistics.median(vals), "%s; median of %d sampled steps" % (desc, len(vals)), threads
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, on the host cores, sampled steps of the same
+    workload (rank 0 only).  A bounded run: steps stop once about 150 s have passed,
+    and the line says how many were timed."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    cfg = synth.CONFIGS[args.workload]
+    seeds = synth.parity_seeds(args.workload)
+    seed, bias = seeds["seed"], seeds["bias_seeds"]
+    t_start = time.perf_counter()
+    next_step, desc, threads = oracle_sampler(cfg, seed, bias)
+    for _ in range(min(args.warmup, 1)):
+        next_step()
+    vals = []
+    while len(vals) < args.steps:
+        vals.append(next_step())
+        if time.perf_counter() - t_start > 150.0 and len(vals) >= 2:
+            break
+    step_ms = statistics.median(vals)
+    sample = "%s; median of %d sampled steps (the run is bounded to about 150 s)" % (desc, len(vals))
     line = {"impl": "reference", "metric": METRIC, "value": step_ms, "unit": "ms", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": False,
+            "steps": len(vals), "warmup": min(args.warmup, 1), "ms_per_step": step_ms, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": cfg.name, "parallelism": "replicas"},
-            "cpu_baseline": {"kind": "oracle", "cores": oracle.num_threads(), "sample": sample,
-                             "value": step_ms, "unit": "ms"},
+            "cpu_baseline": {"kind": "oracle", "cores": threads, "sample": sample, "value": step_ms, "unit": "ms"},
             "e2e": {"value": step_ms, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -434,7 +444,8 @@ def run_ours(args):
     if model.sync(sptr) != 0:
         raise SystemExit("timed steps failed: %s" % msm.msm_last_error())
     per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    ms_step = max_over_ranks(ev[0].elapsed_time(ev[args.steps]) / args.steps, world, dev)
+    ms_mean = max_over_ranks(ev[0].elapsed_time(ev[args.steps]) / args.steps, world, dev)
+    ms_step = max_over_ranks(statistics.median(per_step), world, dev)  # the headline: median step
 
     # ---- algorithmic bytes from the step's routing
     idx, _ = model.routing()
@@ -465,13 +476,27 @@ def run_ours(args):
     accept = measure_accept(model, cfg, hidden, parent, kc, vc, logits, stream, args.steps) if cfg.vocab else None
     model.close()
 
-    # ---- per-layer times from the kernel's own %globaltimer stamps (separate, untimed model)
+    # ---- per-layer times from the kernel's own %globaltimer stamps (separate model),
+    # and what the stamps cost: the same steps timed with the flag on
     us_layer = lm_us = None
+    self_timing = None
     if not args.no_self_timing:
         tm_model = build_model(cfg, seed, bias, dev, local, flags | msm.MSM_FLAG_SELF_TIMING, args.l2_runahead_kb)
         for _ in range(3):
             step(tm_model)
         tm_model.sync(sptr)
+        n_on = min(args.steps, 50)
+        e_on = [torch.cuda.Event(enable_timing=True) for _ in range(n_on + 1)]
+        e_on[0].record(stream)
+        for i in range(n_on):
+            step(tm_model)
+            e_on[i + 1].record(stream)
+        torch.cuda.synchronize()
+        on_ms = statistics.median([e_on[i].elapsed_time(e_on[i + 1]) for i in range(n_on)])
+        self_timing = {"ms_per_step_on": on_ms, "ms_per_step_off": statistics.median(per_step),
+                       "us_per_launch": (on_ms - statistics.median(per_step)) * 1e3 / n_launch,
+                       "steps": n_on, "note": "MSM_FLAG_SELF_TIMING: %globaltimer stamps of every block and "
+                                              "phase; median steps, flag on vs off"}
         tm = tm_model.timing().astype(np.int64)  # [L][G][events]
         tm_model.close()
         ev = msm.EV
@@ -489,7 +514,8 @@ def run_ours(args):
     if rank == 0:
         line = {
             "metric": METRIC, "value": ms_step, "unit": "ms", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "ms_per_step_median": statistics.median(per_step),
+            "warmup": args.warmup, "ms_per_step": ms_step, "ms_per_step_mean": ms_mean,
+            "timing": "value = median of the timed steps' CUDA-event times (max over ranks); mean alongside",
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4+bf16",
             "data": "synthetic (seeded; weights drawn on the device)",
             "config": {"workload": cfg.name, "layers": cfg.n_layers, "tree_tokens": T, "pos0": cfg.pos0,
@@ -514,6 +540,8 @@ def run_ours(args):
         }
         if accept is not None:
             line["accept"] = accept
+        if self_timing is not None:
+            line["self_timing"] = self_timing
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line))
@@ -526,7 +554,7 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="cfg4", choices=sorted(synth.CONFIGS))

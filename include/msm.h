@@ -36,6 +36,13 @@
  *     model.  Nothing traps.
  *   - A model is not thread-safe; one model may be used by one host thread at a
  *     time.  Two steps of one model must not overlap on the GPU.
+ *   - Co-residency: the blocks of a layer launch (one per SM, grid_blocks of them)
+ *     wait on each other, so all of them must be resident at once.  The model checks
+ *     at creation that the grid fits the device (one 384-thread block with ~227 KB
+ *     of shared memory per SM); while steps run, nothing else may occupy the SMs
+ *     (another kernel, another model's step, MPS or MIG clients).  If blocks cannot
+ *     be co-resident, the bounded waits run out and the step reports
+ *     MSM_ERR_DEVICE_TIMEOUT instead of hanging.
  *
  * Layouts (row-major; "bf16" is the 16-bit brain-float bit pattern)
  *   hidden state      bf16 [16][d_model]        (tree token i in row i)

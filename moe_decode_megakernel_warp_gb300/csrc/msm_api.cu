@@ -332,6 +332,10 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   int occ = 0;
   CKM(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, layer_kernel(false), kThreads, m->smem_bytes));
   if (occ < 1) return bail(fail(MSM_ERR_UNSUPPORTED, "the layer kernel does not fit on an SM"));
+  // the blocks of a launch wait on each other (phase counters, handoff slots), so all of
+  // them must be resident at once: one block per SM, at most one per SM of the device
+  if ((long long)m->G > (long long)sms * occ)
+    return bail(fail(MSM_ERR_UNSUPPORTED, "grid larger than the blocks the device holds at once"));
 
   cudaDriverEntryPointQueryResult qr;
   void* fn = nullptr;

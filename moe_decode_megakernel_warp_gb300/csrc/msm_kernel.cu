@@ -1169,10 +1169,17 @@ __device__ __forceinline__ void attn_keys16(AttnState<D>& st, const uint32_t (&q
     st.o[n][2] *= alpha[1];
     st.o[n][3] *= alpha[1];
   }
-  // P in bf16 (8 significant bits, as the bf16 rounding the attention output gets)
-  uint32_t ph[4];
+  // P as two bf16 terms, P = hi + lo (about 16 significant bits): with P in one bf16
+  // term the attention output carried ~2e-3 relative error, which its own bf16 rounding
+  // then spread to most elements, and through h1 and the pooled vector to the router
+  // logits (a few 1e-3, above the top-8 margin of the inputs)
+  uint32_t ph[4], pl[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) ph[i] = pack_bf16x2(s[i >> 1][(i & 1) * 2], s[i >> 1][(i & 1) * 2 + 1]);
+  for (int i = 0; i < 4; ++i) {
+    const float a = s[i >> 1][(i & 1) * 2], b = s[i >> 1][(i & 1) * 2 + 1];
+    ph[i] = pack_bf16x2(a, b);
+    pl[i] = pack_bf16x2(a - bf16_to_f32((uint16_t)(ph[i] & 0xFFFFu)), b - bf16_to_f32((uint16_t)(ph[i] >> 16)));
+  }
 #pragma unroll
   for (int n = 0; n < D / 8; n += 2) {
     const int key = kb + (mi & 1) * 8 + r8;
@@ -1181,6 +1188,8 @@ __device__ __forceinline__ void attn_keys16(AttnState<D>& st, const uint32_t (&q
     ldsm_x4_t(vbase + swz(key, d0, rows), b0, b1, b2, b3);
     mma_bf16(st.o[n], ph[0], ph[1], ph[2], ph[3], b0, b1);
     mma_bf16(st.o[n + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+    mma_bf16(st.o[n], pl[0], pl[1], pl[2], pl[3], b0, b1);
+    mma_bf16(st.o[n + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
   }
 }
 

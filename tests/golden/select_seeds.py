@@ -12,10 +12,11 @@ experts, the routing pattern of the pages' profiling runs (orcarouter.ai,
 is": 49 experts per layer).  Calls only oracle/ and synth/.
 
     python tests/golden/select_seeds.py cfg1 cfg1_stack [cfg2 cfg3 cfg4]
+    python tests/golden/select_seeds.py --extra cfg1 cfg2      # extra_seeds.json
 
 Deep stacks (the 62-layer workload) keep the weight seed and choose each layer's
-bias seed for the margin rule only (margin 1e-2), drawing just the routed experts
-of a layer.
+bias seed for the margin rule (margin 1e-2) and, with a 49-expert hot set, for
+exactly 49 distinct experts, drawing just the routed experts of a layer.
 """
 import json
 import os
@@ -68,8 +69,9 @@ def run_layers(cfg, seed, bias_for_layer):
 
 
 def run_stack_routed(cfg, seed, max_tries):
-    """Per-layer bias seeds for a deep full-width stack (margin rule only), drawing
-    only the routed experts of each layer (tests/full_stack.py)."""
+    """Per-layer bias seeds for a deep full-width stack (margin rule, and 49 distinct
+    experts with a 49-expert hot set), drawing only the routed experts of each layer
+    (tests/full_stack.py)."""
     sys.path.insert(0, os.path.dirname(HERE))
     import full_stack
     h = synth.hidden_in(cfg, seed)
@@ -81,10 +83,22 @@ def run_stack_routed(cfg, seed, max_tries):
         w.update(experts.as_dict())
         k, v = synth.kv_history(cfg, seed, l)
         experts.clear()
-        for bs in range(1, max_tries):
-            w["b_router"] = synth.router_bias(cfg, bs, l)
+        # the bias enters only after the router's product (logits = u W_r^T + b), so
+        # the unbiased logits of one routing pass screen the candidate biases; the
+        # oracle then confirms the pick with that bias
+        w["b_router"] = np.zeros(cfg.e, np.float32)
+        base, _ = full_stack.routing_pass(cfg, w, l, h, parent, cfg.pos0, k, v)
+        base = base.astype(np.float64)
+        want49 = cfg.n_hot == 49
+        for bs in range(1, max_tries * 50):
+            b = synth.router_bias(cfg, bs, l)
+            est = base + b.astype(np.float64)[None, :]
+            top = np.argsort(-est, axis=1, kind="stable")[:, :cfg.k]
+            if not margin_ok(est, cfg.k, 2 * DEEP_MARGIN) or (want49 and len(np.unique(top)) != 49):
+                continue
+            w["b_router"] = b
             logits, idx = full_stack.routing_pass(cfg, w, l, h, parent, cfg.pos0, k, v)
-            if margin_ok(logits, cfg.k, DEEP_MARGIN):
+            if margin_ok(logits, cfg.k, DEEP_MARGIN) and (not want49 or len(np.unique(idx)) == 49):
                 break
         else:
             raise SystemExit("no bias seed found for layer %d" % l)
@@ -113,7 +127,49 @@ def select(name, max_tries=400):
     raise SystemExit("no seed found for " + name)
 
 
+def select_extra(name, count=5, max_tries=400):
+    """Further draws of a single-layer workload that keep the margin rule (1e-3) --
+    extra cases for the set-exact routing check -- beyond the one in seeds.json."""
+    cfg = synth.CONFIGS[name]
+    assert cfg.n_layers == 1
+    base = json.load(open(os.path.join(HERE, "seeds.json")))[name]
+    out = []
+    if cfg.n_hot > 0:
+        seed = base["seed"]
+        w = synth.layer_weights(cfg, seed, 0, bias_seed=1)
+        k0, v0 = synth.kv_history(cfg, seed, 0)
+        h = synth.hidden_in(cfg, seed)
+        parent = synth.parent_array(seed)
+        for bs in range(base["bias_seeds"][0] + 1, max_tries):
+            w["b_router"] = synth.router_bias(cfg, bs, 0)
+            k, v = k0.copy(), v0.copy()
+            _, tr = oracle.layer(cfg, w, cfg.is_global(0), h, parent, cfg.pos0, k, v, trace=True)
+            if margin_ok(tr["router_logits"], cfg.k):
+                out.append({"seed": seed, "bias_seeds": [bs]})
+                print(name, "bias seed", bs, flush=True)
+                if len(out) == count:
+                    return out
+    else:
+        for seed in range(base["seed"] + 1, max_tries):
+            chosen = run_layers(cfg, seed, lambda l: [1])
+            if chosen is not None:
+                out.append({"seed": seed, "bias_seeds": chosen})
+                print(name, "seed", seed, flush=True)
+                if len(out) == count:
+                    return out
+    raise SystemExit("not enough extra seeds for " + name)
+
+
 if __name__ == "__main__":
+    if len(sys.argv) > 1 and sys.argv[1] == "--extra":
+        # extra cases of the single-layer workloads (writes extra_seeds.json)
+        path = os.path.join(HERE, "extra_seeds.json")
+        cur = json.load(open(path)) if os.path.exists(path) else {}
+        for name in sys.argv[2:]:
+            cur[name] = select_extra(name)
+            with open(path, "w") as fh:
+                json.dump(cur, fh, indent=1, sort_keys=True)
+        sys.exit(0)
     path = os.path.join(HERE, "seeds.json")
     cur = json.load(open(path)) if os.path.exists(path) else {}
     for name in sys.argv[1:]:

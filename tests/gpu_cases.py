@@ -71,7 +71,10 @@ def run_gpu(case, flags=None, grid_blocks=0, attn_splits=0, steps=1, timeout_us=
         model.verify_step(hid, case.parent, case.pos0, kc, vc, logits_out=logits, hidden_out=hout)
         status.append(model.sync())
     torch.cuda.synchronize()
+    # the staged activations of the last layer (exchange buffers of the last launch)
+    exchange = {n: model.exchange(n) for n in ("o", "h1", "u", "logits", "z")} if all(x == 0 for x in status) else None
     out = {
+        "exchange": exchange,
         "status": status,
         "hidden": hout.cpu().numpy().view(np.uint16),
         "logits": logits.cpu().numpy() if logits is not None else None,
@@ -85,6 +88,17 @@ def run_gpu(case, flags=None, grid_blocks=0, attn_splits=0, steps=1, timeout_us=
     else:
         model.close()
     return out
+
+
+def extra_cases(name):
+    """Further seeds of a single-layer workload that keep the router margin rule
+    (tests/golden/extra_seeds.json, written by tests/golden/select_seeds.py --extra)."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "extra_seeds.json")
+    if not os.path.exists(path):
+        return []
+    return json.load(open(path)).get(name, [])
 
 
 def bf(a):
