@@ -167,10 +167,12 @@ typedef struct {
  * into the model's layout (GPU kernels on an internal stream, completed before
  * return) and allocate the exchange buffers.
  * Errors: MSM_ERR_INVALID_ARG (null pointer, bad config), MSM_ERR_UNSUPPORTED
- * (widths outside what the kernels implement: d_model, pool_dim, ffn_dim and
- * n_q_heads*head_dim multiples of 64, head_dim 64 or 128, n_q_heads/n_kv_heads
- * in {1,2,4,8}, top_k <= 8, n_experts <= 256 and a multiple of 16, vocab a
- * multiple of 16), MSM_ERR_OOM, MSM_ERR_CUDA.  On error *out is NULL.
+ * (widths outside what the kernels implement: d_model and n_q_heads*head_dim
+ * multiples of 64, pool_dim and ffn_dim multiples of 256 with pool_dim <= 2048
+ * and ffn_dim <= 1024, head_dim 64 or 128, n_q_heads/n_kv_heads in {1,2,4,8},
+ * top_k <= 8, n_experts <= 256 and a multiple of 16, vocab a multiple of 16; a
+ * grid larger than the device keeps resident), MSM_ERR_OOM, MSM_ERR_CUDA.  On
+ * error *out is NULL.
  */
 msm_status msm_model_create(const msm_config* config, const msm_weights* weights, int device,
                             msm_model** out);

@@ -43,7 +43,7 @@ EV = dict(start=0, pro_in=1, pro_done=2, attn_in=3, attn_done=4, merge_done=5, o
           pool_in=8, pool_done=9, router_in=10, router_done=11, route_topk=12, route_done=13, gemm1_done=14,
           gemm2_in=15, gemm2_done=16, combine_done=17, unpool_in=18, unpool_done=19, tail_in=20, tail_done=21,
           end=22, loader_routed=23, loader_end=24, route_dispatch=25,
-          pool_staged=26, xq_row_in=27, xq_row0_done=28, xq_row1_done=29, pool_normed=30, pool_gain=31,
+          pool_staged=26, split_done=27, b1_issued=28, b1_landed=29, pool_normed=30, pool_gain=31,
           op_u0_first=32, op_u0_last=33, op_u0_red=34, op_u0_epi=35, op_u1_first=36, op_u1_last=37,
           op_u1_red=38, op_u1_epi=39, g1_first_ready=40, g1_first_done=41, g1_last_ready=42, g1_last_done=43,
           ld_op_first=44, ld_op_last=45, ld_g1_first=46, ld_g1_last=47,
@@ -51,7 +51,7 @@ EV = dict(start=0, pro_in=1, pro_done=2, attn_in=3, attn_done=4, merge_done=5, o
           g2_stage2_done=53, ld_op_u1=54, seen_merge=55, seen_oproj=56, seen_pool=57, seen_router=58,
           seen_route=59, seen_combine=60, seen_unpool=61, seen_tail=62,
           **{"tc_g1_ready%d" % i: 64 + i for i in range(16)}, **{"tc_g1_issued%d" % i: 80 + i for i in range(16)},
-          **{"wg_g1_landed%d" % i: 96 + i for i in range(16)}, **{"tc_g2_ready%d" % i: 112 + i for i in range(8)},
+          **{"g1_epi_done%d" % i: 96 + i for i in range(16)}, **{"tc_g2_ready%d" % i: 112 + i for i in range(8)},
           **{"tc_g2_issued%d" % i: 120 + i for i in range(8)},
           **{"ld_g1_issued%d" % i: 128 + i for i in range(16)}, ld_ring_grown=144,
           **{"ld_g1_next%d" % i: 160 + i for i in range(16)}, **{"ld_g1_placed%d" % i: 176 + i for i in range(16)})

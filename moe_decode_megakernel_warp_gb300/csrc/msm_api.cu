@@ -63,7 +63,7 @@ struct msm_model {
   Dims dm{};
   std::vector<uint8_t> global;
   int G = 0, ring_bytes = 0, act_bytes = 0, smem_bytes = 0;
-  int g1_u_off = 0, g1_x_off = 0, g2_off = 0, ring_ext = 0;
+  int g1_b_off = 0, g2_off = 0, ring_ext = 0;
   std::vector<LayerPack> L;
   uint8_t* lm = nullptr;
   uint16_t* g_final = nullptr;
@@ -136,6 +136,7 @@ msm_status validate_config(const msm_config* c) {
   if (c->pool_dim % kExpBlockK || c->ffn_dim % kExpBlockK)
     return fail(MSM_ERR_UNSUPPORTED, "pool_dim and ffn_dim must be multiples of 256 (expert tensor-core tiles)");
   if (c->ffn_dim > 1024) return fail(MSM_ERR_UNSUPPORTED, "ffn_dim > 1024 (activation scales in tensor memory)");
+  if (c->pool_dim > 2048) return fail(MSM_ERR_UNSUPPORTED, "pool_dim > 2048 (activation scales in tensor memory)");
   if (c->top_k > kMaxTopK) return fail(MSM_ERR_UNSUPPORTED, "top_k > 8");
   if (c->n_experts > kMaxExperts || c->n_experts % 16) return fail(MSM_ERR_UNSUPPORTED, "n_experts must be <= 256 and a multiple of 16");
   if (c->vocab % 16) return fail(MSM_ERR_UNSUPPORTED, "vocab must be a multiple of 16");
@@ -171,7 +172,7 @@ msm_status arm_exchange(uint8_t* x, const XOffsets& o, cudaStream_t s) {
   CK(launch_fill_u32(x, o.logits / 4, 0xFFFFFFFFu, s));                       // o, h1, u
   CK(launch_fill_u32(x + o.logits, (o.z - o.logits) / 4, 0x80000000u, s));    // logits, a
   CK(launch_fill_u32(x + o.z, (o.cnt - o.z) / 4, 0xFFFFFFFFu, s));            // z, h2, q0, tkv0
-  CK(launch_fill_u32(x + o.cnt, (o.total - o.cnt) / 4, 0u, s));               // counters
+  CK(launch_fill_u32(x + o.cnt, (o.b1 - o.cnt) / 4, 0u, s));                  // counters
   return MSM_OK;
 }
 
@@ -288,14 +289,13 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   const uint64_t attn_need = (uint64_t)dm.group * (D / 16) * kKStepBytes + 2ull * 16 * D * 2 +
                              (uint64_t)dm.group * dm.attn_wph * 32 * (4 + D / 2) * 4;
   const uint64_t kmax = (uint64_t)std::max(std::max(dm.d, dm.hq * dm.hd), dm.p);
-  // GEMM1: the 16 tokens' pooled vectors (f16) + the epilogue exchange rows of both
-  // warp groups; GEMM2: two experts' NVFP4 rows (E2M1 + scales) + one fp32 row per warp
-  // (both at the top of the buffer; the router stages the bf16 pooled vectors at its
-  // bottom, and routing converts them into the top: the two must not overlap)
-  const uint64_t g1_need = (uint64_t)dm.p * 32 + 2ull * 128 * 17 * 4;
+  // GEMM1: operand B, the split pooled vectors with their scale groups; GEMM2: two
+  // experts' NVFP4 rows (E2M1 + scales) + one fp32 row per warp (both at the top of the
+  // buffer; the router stages the bf16 pooled vectors at its bottom, dead once the
+  // router phase has split them, before operand B is copied in)
+  const uint64_t g1_need = b1_bytes(dm.p);
   const uint64_t g2_need = ((18ull * dm.f + 1023) & ~1023ull) + (uint64_t)kComputeWarps * dm.f * 4;
   uint64_t act = std::max(std::max(kmax * 32, g1_need), std::max(g2_need, attn_need));
-  act = std::max(act, (uint64_t)dm.p * 64);
   act = (act + 1023) & ~uint64_t(1023);
   const uint64_t expert_top = (std::max(g1_need, g2_need) + 1023) & ~uint64_t(1023);
   const int smem_cap = std::min(kMaxSmem, smem_optin);
@@ -310,8 +310,7 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   }
   m->act_bytes = (int)act;
   m->ring_bytes = (int)ring;
-  m->g1_u_off = (int)(act - (uint64_t)dm.p * 32);
-  m->g1_x_off = (int)(act - g1_need);
+  m->g1_b_off = (int)(act - ((g1_need + 1023) & ~uint64_t(1023)));
   m->g2_off = (int)(act - ((g2_need + 1023) & ~uint64_t(1023)));
   m->ring_ext = (int)((act - expert_top) & ~uint64_t(1023));
   m->smem_bytes = (int)(ring + act + kSmallBytes);
@@ -402,6 +401,7 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   xo.q0 = o; o += align256((uint64_t)T * dm.hq * dm.hd * 2);
   xo.tkv0 = o; o += align256(2ull * dm.hkv * T * dm.hd * 2);
   xo.cnt = o; o += kCounterBytes;
+  xo.b1 = o; o += align256(b1_bytes(dm.p));
   xo.total = o;
   SOffsets& so = m->so;
   o = 0;
@@ -571,8 +571,7 @@ msm_status enqueue_verify(msm_model* m, const StepBuffers& B, const void* hidden
   P.pos0 = pos0;
   P.ring_bytes = m->ring_bytes;
   P.act_bytes = m->act_bytes;
-  P.g1_u_off = m->g1_u_off;
-  P.g1_x_off = m->g1_x_off;
+  P.g1_b_off = m->g1_b_off;
   P.g2_off = m->g2_off;
   P.ring_ext = m->ring_ext;
   P.flags = m->cfg.flags;

@@ -56,6 +56,13 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// ... with the default L2 policy (data many blocks read)
+__device__ __forceinline__ void bulk_g2s_plain(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 // 3-D tiled tensor load (coordinates innermost first)
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
                                             uint64_t* bar) {
@@ -209,15 +216,6 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
   uint32_t h2 = e4m3x2_to_f16x2(code & 0xFFu);
   return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
 }
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)bf16_bits_rn(lo) | ((uint32_t)bf16_bits_rn(hi) << 16);
 }
@@ -249,26 +247,20 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// Instruction descriptors: fp32 accumulator, K-major A and B, M = 128.
-//   f16 x f16 (kind::f16)
-__host__ __device__ constexpr uint32_t idesc_f16(int n) {
-  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((128u >> 4) << 24);
+// Shared-memory descriptor of a plain (unswizzled) column of 8-row core matrices, each
+// 8 rows x 16 bytes = 128 contiguous bytes, `sbo` bytes from one 8-row group to the next.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(sbo >> 4) << 32) | ((uint64_t)1 << 46);
 }
-//   E2M1 x E2M1 with UE4M3 scales per 16 elements (kind::mxf4nvf4, scale_vec::4X)
+// Instruction descriptor: E2M1 x E2M1 with UE4M3 scales per 16 elements (kind::mxf4nvf4,
+// scale_vec::4X), fp32 accumulator, K-major A and B, M = 128, N = n.
 __host__ __device__ constexpr uint32_t idesc_nvf4(int n) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((128u >> 4) << 24);
 }
-// D[tmem] (+)= A[tmem] . B[smem]^T, f16 inputs (one thread issues)
-__device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 // D[tmem] (+)= (A[smem] * SFA) . (B[smem] * SFB)^T, E2M1 operands, UE4M3 block scales in
-// tensor memory (row m of A reads its four scales of the K=64 step at lane m, column
-// sfa + m / 32; column n of B at lane n, column sfb)
+// tensor memory, one 32-bit word (the four scales of a K=64 step) per row: row m of A at
+// lane m, column sfa + m / 32; row n of B at lane n % 32, column sfb + n / 32 (the
+// writers fill every quadrant and column the layout could name)
 __device__ __forceinline__ void mma_nvf4_ss(uint32_t d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                             uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
   asm volatile(
@@ -276,6 +268,12 @@ __device__ __forceinline__ void mma_nvf4_ss(uint32_t d, uint64_t a_desc, uint64_
       "[%0], %1, %2, %3, [%4], [%5], p; }" ::"r"(d),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
       : "memory");
+}
+// shared memory -> tensor memory, asynchronous, ordered with the issuing thread's MMAs:
+// 32 rows of 16 bytes (sdesc_plain, 128-byte groups) to lanes 0-31 of every quadrant,
+// row l's four words in columns taddr .. taddr + 3 of lane l
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 // the mbarrier completes one arrival once every tcgen05 operation this thread issued so far is done
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
@@ -300,12 +298,4 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-// four E2M1 code bytes (eight codes) -> four f16x2 (low half from the low nibble)
-__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t& o0, uint32_t& o1, uint32_t& o2, uint32_t& o3) {
-  asm("{ .reg .b8 b0, b1, b2, b3; mov.b32 {b0, b1, b2, b3}, %4; cvt.rn.f16x2.e2m1x2 %0, b0; "
-      "cvt.rn.f16x2.e2m1x2 %1, b1; cvt.rn.f16x2.e2m1x2 %2, b2; cvt.rn.f16x2.e2m1x2 %3, b3; }"
-      : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
-      : "r"(w));
-}
-
 }  // namespace msm

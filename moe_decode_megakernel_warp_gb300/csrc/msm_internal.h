@@ -18,7 +18,8 @@ constexpr int kDenseTileSteps = 64;   // 16-row x 1024-column bf16 tiles: 64 k-s
 constexpr int kKStepBytes = 512;      // one 16x16 bf16 (or f16) block in ldmatrix order
 // NVFP4 expert tiles: 128 rows x tk columns (tk = 512 where the width allows, else 256):
 // tk / 256 column blocks of 128 rows x 128 code bytes in the 128-byte swizzle layout
-// (16 KB each), then the rows' tk / 16 UE4M3 block scales (row after row)
+// (16 KB each), then the UE4M3 block scales as tk / 64 groups of 512 bytes, one per K=64
+// step: the word of row m's four scales at byte (m % 32) * 16 + (m / 32) * 4 of its group
 constexpr int kExpTileRows = 128;
 constexpr int kExpBlockK = 256;                                  // columns per 16 KB code block
 constexpr int kExpBlockBytes = kExpTileRows * kExpBlockK / 2;
@@ -38,7 +39,7 @@ enum TimingEvent : int {
   EV_ROUTE_TOPK = 12, EV_ROUTE_DONE = 13, EV_GEMM1_DONE = 14, EV_GEMM2_IN = 15, EV_GEMM2_DONE = 16,
   EV_COMBINE_DONE = 17, EV_UNPOOL_IN = 18, EV_UNPOOL_DONE = 19, EV_TAIL_IN = 20, EV_TAIL_DONE = 21, EV_END = 22,
   EV_LOADER_ROUTED = 23, EV_LOADER_END = 24, EV_ROUTE_DISPATCH = 25,
-  EV_POOL_STAGED = 26, EV_XQ_ROW_IN = 27, EV_XQ_ROW0_DONE = 28, EV_XQ_ROW1_DONE = 29,
+  EV_POOL_STAGED = 26, EV_SPLIT_DONE = 27, EV_B1_ISSUED = 28, EV_B1_LANDED = 29,
   EV_POOL_NORMED = 30, EV_POOL_GAIN = 31,
   // finer stamps: o_proj units 0 / 1 of the block (first tile ready, last tile ready,
   // partial sums stored, epilogue done), GEMM1 of the first compute warp, and the loader
@@ -55,11 +56,10 @@ enum TimingEvent : int {
   EV_SEEN_MERGE = 55, EV_SEEN_OPROJ = 56, EV_SEEN_POOL = 57, EV_SEEN_ROUTER = 58, EV_SEEN_ROUTE = 59,
   EV_SEEN_COMBINE = 60, EV_SEEN_UNPOOL = 61, EV_SEEN_TAIL = 62,
   // per-tile trace of the expert GEMMs (the block's first tiles): the tensor-core warp
-  // saw tile i's operands ready / had issued its MMAs, and the compute warp group saw
-  // tile i land in the ring
+  // saw tile i's operands ready / had issued its MMAs; GEMM1 epilogue of unit i done
   EV_TC_G1_READY = 64,   // + i, i < 16
   EV_TC_G1_ISSUED = 80,  // + i, i < 16
-  EV_WG_G1_LANDED = 96,  // + i, i < 16
+  EV_G1_EPI_DONE = 96,   // + i, i < 16
   EV_TC_G2_READY = 112,  // + i, i < 8
   EV_TC_G2_ISSUED = 120, // + i, i < 8
   EV_LD_G1_ISSUED = 128, // + i, i < 16: the loader issued the copy of GEMM1 tile i
@@ -89,6 +89,7 @@ struct DevStatus {
 struct XOffsets {
   uint64_t o, h1, u, logits, a, z, h2, q0, tkv0;  // re-armed by the next launch
   uint64_t cnt;                                   // phase-completion counters, zeroed likewise
+  uint64_t b1;    // GEMM1 operand B of the launch (written whole by the router phase)
   uint64_t total;
 };
 // Phase-completion counters of one launch: every block adds 1 to counter i once it
@@ -172,11 +173,11 @@ struct LaunchParams {
   // scalars
   int layer, first, last, is_global, next_global, pos0;
   int ring_bytes, act_bytes;
-  // expert phases: the pooled vectors in f16 (GEMM1 operand B), the GEMM1 epilogue
-  // exchange rows and the GEMM2 operands sit at these offsets at the top of the
-  // activation buffer; from the end of routing to the unpooler the weight ring may grow
-  // by ring_ext bytes into the bottom of it
-  int g1_u_off, g1_x_off, g2_off, ring_ext;
+  // expert phases: GEMM1's operand B (the split pooled vectors and their scales) and
+  // the GEMM2 operands sit at these offsets at the top of the activation buffer; from
+  // the end of routing to the unpooler the weight ring may grow by ring_ext bytes into
+  // the bottom of it
+  int g1_b_off, g2_off, ring_ext;
   uint32_t flags;
   uint32_t timeout_ns_lo, timeout_ns_hi;
   int prefetch_experts;
@@ -201,10 +202,20 @@ enum ActMap : int { ACT_O = 0, ACT_H1 = 1, ACT_U = 2, ACT_Z = 3, ACT_H2 = 4 };
 
 // packed sizes
 __host__ __device__ inline uint64_t dense_unit_bytes(int K) { return (uint64_t)K * 32; }  // 16 rows x K bf16
-// an expert unit: 128 rows x K columns = K / 256 tiles (W1: 64 gate + 64 up rows; W2: 128 rows)
+// an expert unit: 128 rows x K columns = K / exp_tile_k(K) tiles (W1: 64 gate rows and the
+// 64 matching up rows, interleaved gate, up, gate, ...; W2: 128 rows)
 __host__ __device__ inline uint64_t exp_unit_bytes(int K) { return (uint64_t)(K / exp_tile_k(K)) * exp_tile_bytes(K); }
 __host__ __device__ inline int w1_units(int f) { return f / 64; }
 __host__ __device__ inline int w2_units(int p) { return p / kExpTileRows; }
+// GEMM1 operand B: the 16 pooled vectors, each as the sum of kSplitTerms NVFP4 terms,
+// one B row per (term, token) pair, row n = term * 16 + token: p / 256 column blocks of
+// 64 rows x 128 code bytes (128-byte swizzle, 8 KB each), then p / 64 scale groups of
+// 512 bytes, one per K=64 step, for the tensor-memory copy (32 lines of 16 bytes; line l:
+// the scale words of rows l and l + 32, two zero words)
+constexpr int kSplitTerms = 4;
+constexpr int kSplitRows = kSplitTerms * T;
+__host__ __device__ inline uint64_t b1_code_bytes(int p) { return (uint64_t)p / 256 * kSplitRows * 128; }
+__host__ __device__ inline uint64_t b1_bytes(int p) { return b1_code_bytes(p) + (uint64_t)p / 64 * 512; }
 
 // kernel entry points (defined in msm_kernel.cu / msm_pack.cu)
 const void* layer_kernel(bool timing);

@@ -63,33 +63,34 @@ struct Smem {
   uint32_t* tc_ti;      // [1]: first ring tile of GEMM2 (for the tensor-core warp)
 };
 
-// Tensor-core pipeline of the expert GEMMs: mbarriers between the compute warp groups
-// (dequantisation / scale staging / epilogues) and the tensor-core warp (MMA issue).
+// Tensor-core pipeline of the expert GEMMs: mbarriers between the tensor-core warp (MMA
+// and scale-copy issue) and the compute warp groups (operand staging, epilogues).
 enum TcBar : int {
-  TB_G1_FREE = 0,    // [2 groups][2 chunk buffers] GEMM1 A chunk consumed by its MMAs (4 issuer commits)
-  TB_D1_FULL = 4,    // [2 groups][4 issuers][2 parities] an issuer's GEMM1 accumulator of a unit done
-  TB_D1_FREE = 20,   // [2 parities] ... read by the unit's epilogue (4 warps)
-  TB_SFA_FULL = 22,  // [4] GEMM2 weight block scales of a tile in tensor memory (4 warps)
-  TB_SFA_FREE = 26,  // [4] ... the tile's MMAs are done (commit)
-  TB_D2_FULL = 30,   // [2]
-  TB_D2_FREE = 32,   // [2]
-  TB_G2_STAGE = 34,  // a GEMM2 round's activations and their block scales staged
-  TB_DONE = 35,      // the compute warps are done with tensor memory (8 warps)
-  TB_DRAIN = 36,     // every MMA of the tensor-core warp has completed
-  TB_WDRAIN = 37,    // [8] every MMA a compute warp issued has completed
-  TB_ROUTED = 45,    // the block's routing (expert list, GEMM2 tile base) is in shared memory
-  kTcBars = 46
+  TB_D1_FULL = 0,    // [2 parities] a unit's GEMM1 accumulator complete (commit)
+  TB_D1_FREE = 2,    // [2] ... read by the unit's epilogue (4 warps)
+  TB_SFA_DONE = 4,   // [4] the MMAs that read a weight-scale buffer are done (commit)
+  TB_D2_FULL = 8,    // [2]
+  TB_D2_FREE = 10,   // [2] (4 warps)
+  TB_G2_STAGE = 12,  // a GEMM2 round's activations and their block scales staged
+  TB_DONE = 13,      // the compute warps are done with tensor memory (8 warps)
+  TB_DRAIN = 14,     // every MMA of the tensor-core warp has completed
+  TB_ROUTED = 15,    // the block's routing (expert list, first expert tile) is in shared memory
+  TB_B1 = 16,        // GEMM1's operand B has landed in the activation buffer (transaction count)
+  TB_SFA_FULL = 17,  // [4] a tile's weight scales are in a scale buffer (4 warps)
+  TB_SLOT = 21,      // [kSlots] the MMAs of the expert tile in a ring slot are done (commit):
+                     // the loader's release of expert tiles (one commit, where the other
+                     // tiles' consumers arrive on the slot's `empty` barrier eight times)
+  kTcBars = TB_SLOT + kSlots
 };
-// tensor-memory columns (512 allocated: one block per SM).  GEMM2 reuses GEMM1's chunk
-// columns: its first tensor-memory write follows every GEMM1 epilogue, and so every
-// GEMM1 MMA.
+// tensor-memory columns (512 allocated: one block per SM).  GEMM2 reuses GEMM1's
+// operand-scale and accumulator columns: its first tensor-memory write follows every
+// GEMM1 epilogue, and so every GEMM1 MMA.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TM_ABUF = 0;    // [2 groups][2] x 64: GEMM1 dequantised weight chunks (128 rows x 128 K, f16)
-constexpr uint32_t TM_D1 = 256;    // [2 groups][4 issuers][2 parities] x 16: GEMM1 partial accumulators (fp32)
-constexpr uint32_t TM_SFB = 0;     // 2 x 64: GEMM2 activation scales of a round's two experts
-constexpr uint32_t TM_SFA = 128;   // 4 x 32: GEMM2 weight scales of a tile (up to 8 K=64 steps x 4 columns)
+constexpr uint32_t TM_SFB1 = 0;    // GEMM1 operand-B scales: 4 columns per K=64 step (p / 64 steps)
+constexpr uint32_t TM_SFA = 128;   // 4 x 32: weight scales of a tile (up to 8 K=64 steps x 4 columns)
+constexpr uint32_t TM_D1 = 256;    // 2 x 64: GEMM1 accumulators, column term * 16 + token
+constexpr uint32_t TM_SFB2 = 0;    // 2 x 64: GEMM2 activation scales of a round's two experts
 constexpr uint32_t TM_D2 = 256;    // 2 x 16: GEMM2 accumulators
-__host__ __device__ constexpr uint32_t tm_d1(int wg, int q, int d) { return TM_D1 + (uint32_t)(((wg * 4 + q) * 2 + d) * 16); }
 
 constexpr int kRingStateOff = 6656;  // in the small area, below the GEMM2 row scales
 constexpr int kATsOff = 7936;        // [2][16] floats, below the reduction scratch at 8192
@@ -327,6 +328,9 @@ struct RunAhead {
 // the slot table in shared memory once, when the tile before it is released.
 struct Ring {
   uint32_t cap;       // bytes the ring may use now (grows during the expert phases)
+  uint32_t xmask;     // bit s: slot s holds an expert tile (released through TB_SLOT + s)
+  uint32_t par_e;     // bit s: parity of slot s's next `empty` phase
+  uint32_t par_x;     // bit s: ... of its next TB_SLOT phase
   uint32_t issued;    // tiles issued
   uint32_t tail;      // oldest tile not known to be released
   uint32_t head;      // end of the newest tile
@@ -337,8 +341,8 @@ struct Ring {
 };
 static_assert(kRingStateOff + sizeof(RunAhead) <= 7416, "run-ahead state overlaps the tensor-core barriers");
 static_assert(7424 + kTcBars * 8 <= kATsOff, "tensor-core barriers overlap the GEMM2 row scales");
-static_assert(TM_ABUF + 4 * 64 <= TM_D1 && tm_d1(1, 3, 1) + 16 <= kTmemCols && TM_SFA + 4 * 32 <= TM_D2 &&
-              TM_D2 + 32 <= kTmemCols, "tensor-memory map");
+static_assert(TM_SFB1 + 2048 / 64 * 4 <= TM_SFA && TM_SFB2 + 2 * 64 <= TM_SFA && TM_SFA + 4 * 32 <= TM_D1 &&
+              TM_D1 + 2 * kSplitRows <= kTmemCols && TM_D2 + 32 <= kTmemCols, "tensor-memory map");
 
 // a free run of `bytes` (1 KB granules) after the newest tile, at the bottom once the
 // top is too short; waits for the oldest tiles' release until there is one
@@ -362,8 +366,14 @@ __device__ __forceinline__ bool ring_place(Ctx& cx, Ring& r, uint32_t bytes, uin
         break;
       }
     }
-    const uint32_t s = r.tail % kSlots;
-    if (!wait_bar(cx, &cx.S.empty[s], (r.tail / kSlots) & 1, 99)) return false;
+    const uint32_t s = r.tail % kSlots, bit = 1u << s;
+    if (r.xmask & bit) {
+      if (!wait_bar(cx, &cx.S.tcbar[TB_SLOT + s], (r.par_x & bit) ? 1u : 0u, 99)) return false;
+      r.par_x ^= bit;
+    } else {
+      if (!wait_bar(cx, &cx.S.empty[s], (r.par_e & bit) ? 1u : 0u, 99)) return false;
+      r.par_e ^= bit;
+    }
     ++r.tail;
     if (r.tail != r.issued) {
       const uint32_t next = cx.S.slot_off[r.tail % kSlots];
@@ -541,6 +551,7 @@ __device__ void loader(Ctx& cx) {
   // warps' traffic, would cost the loader an L2 round trip per access
   Ring r;
   r.cap = (uint32_t)P.ring_bytes;
+  r.xmask = r.par_e = r.par_x = 0u;
   r.issued = r.tail = r.head = r.tail_off = 0;
   r.wrapped = false;
   r.ra = cx.S.ring_state;
@@ -597,6 +608,8 @@ __device__ void loader(Ctx& cx) {
     }
     if (g1i < 16) stamp_any(P, EV_LD_G1_PLACED + g1i);
     const uint32_t s = r.issued % kSlots;
+    if (ts.seg == 7 || ts.seg == 8) r.xmask |= 1u << s;
+    else r.xmask &= ~(1u << s);
     cx.S.slot_off[s] = off;
     cx.S.slot_tile[s] = r.issued;
     mbar_expect_tx(&cx.S.full[s], bytes);
@@ -648,6 +661,8 @@ struct Worker {
   int cw, lane, g, q;
   uint32_t ti;  // next tile index of the block's sequence
   bool ok;
+  bool b1;      // this thread issued the copy of GEMM1's operand B
+  uint32_t xseq;  // expert tiles of the block before GEMM2's first (weight-scale buffer rotation)
 };
 
 __device__ __forceinline__ void cbar() { named_bar(1, kComputeThreads); }
@@ -1435,6 +1450,85 @@ __device__ void attn_merge_phase(Worker& w) {
 // routing: top-k per token, expert dispatch, GEMM1 input (orcarouter.ai, § "where
 // the kernel boundary sits": top-8 of 256, experts in NVFP4)
 // ---------------------------------------------------------------------------
+// GEMM1's operand B: each pooled vector u_t as a sum of kSplitTerms NVFP4 terms,
+// u_t[k] ~ ts_t sum_j 4^-j S_tj[k / 16] c_tj[k], with ts_t = amax_t / 2688 rounded up to a
+// power of two; term j quantises what the terms before it left (block scale S_tj =
+// E4M3(bmax / (6 ts_t 4^-j)), E2M1 codes c_tj).  A term leaves at most ~0.18 of its
+// block's largest residual, so four leave ~1e-3 of the block's largest magnitude, below
+// bf16's own rounding of the larger elements.  With u in this form the GEMM1 products
+// run on the block-scaled tensor cores straight from the weights' E2M1 codes in the ring
+// (one B row per (term, token)); the 4^-j ts_t factors go in per accumulator column in
+// the epilogue.  The blocks split the 16 x p/16 (token, 16-column block) pairs, 16
+// threads per pair, and store their share in the launch's exchange buffer; the router
+// counter publishes it and every block then copies the whole operand in.
+__device__ void split_pooled(Worker& w) {
+  Ctx& cx = *w.cx;
+  const LaunchParams& P = *cx.P;
+  const int p = P.dm.p;
+  const int tid = w.cw * 32 + w.lane;
+  if (w.ok) {
+    // the row scales: 16 threads per pooled vector (staged in the activation buffer)
+    const int t = tid >> 4, sub = tid & 15;
+    uint32_t am = 0u;  // |x| of non-negative floats orders like its bits
+    for (int c = sub; c < p / 8; c += 16) {
+      const uint4 v = *reinterpret_cast<const uint4*>(cx.S.act + act_off(t, c * 8));
+      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) am = max(am, max((wd[j] & 0x7FFFu) << 16, wd[j] & 0x7FFF0000u));
+    }
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, o));
+    if (sub == 0) {
+      float ts = __fdiv_rn(__uint_as_float(am), 2688.0f);  // amax / (6 * 448), up to a power of two
+      if (ts > 0.f) {
+        int ex;
+        if (frexpf(ts, &ex) != 0.5f) ts = ldexpf(1.0f, ex);
+      }
+      cx.S.x_ts[t] = ts;
+    }
+  }
+  cbar();
+  if (!w.ok) return;
+  const int nb = p / 16;
+  int lo, hi;
+  unit_range(T * nb, cx.block, gridDim.x, lo, hi);
+  const int h = tid >> 4, i = tid & 15;
+  const uint32_t hmask = 0xFFFFu << (w.lane & 16);  // this half-warp's lanes
+  uint8_t* img = P.x_cur + P.xo.b1;
+  uint8_t* sfimg = img + b1_code_bytes(p);
+  for (int pr = lo + h; pr < hi; pr += 16) {
+    const int t = pr / nb, c = pr % nb, k = c * 16 + i;
+    float x = bf16_to_f32(*reinterpret_cast<const uint16_t*>(cx.S.act + act_off(t, k) + (k & 7) * 2));
+    float ts = cx.S.x_ts[t];
+#pragma unroll
+    for (int j = 0; j < kSplitTerms; ++j, ts *= 0.25f) {
+      float bmax = fabsf(x);
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(hmask, bmax, o));
+      const uint32_t sc = ts > 0.f ? f32_to_e4m3(__fdiv_rn(bmax, 6.0f * ts)) : 0u;
+      const float den = e4m3_to_f32(sc) * ts;
+      const float qx = sc != 0u ? __fdiv_rn(x, den) : 0.f;
+      const float qn = __shfl_xor_sync(hmask, qx, 1);
+      const uint32_t byte = (i & 1) ? f32x2_to_e2m1x2(qn, qx) : f32x2_to_e2m1x2(qx, qn);  // even element low
+      const uint32_t h2 = e2m1x2_to_f16x2(byte);
+      const float mine = __half2float(__ushort_as_half((unsigned short)((i & 1) ? (h2 >> 16) : (h2 & 0xFFFFu))));
+      x -= mine * den;  // the residual for the next term
+      const int n = j * T + t;  // operand row
+      if (!(i & 1)) {
+        const int bi = (k & 255) >> 1;  // byte of the 128-byte row
+        img[(k >> 8) * 8192 + n * 128 + (((bi >> 4) ^ (n & 7)) << 4) + (bi & 15)] = (uint8_t)byte;
+      }
+      if (i == 0) sfimg[(c >> 2) * 512 + (n & 31) * 16 + (n >> 5) * 4 + (c & 3)] = (uint8_t)sc;
+    }
+    if (t == 0 && (c & 3) == 0) {
+      // the scale group's words of rows 64..127 (no such rows): zero
+      uint32_t* g = reinterpret_cast<uint32_t*>(sfimg + (c >> 2) * 512);
+      g[(2 * i) * 4 + 2] = 0u; g[(2 * i) * 4 + 3] = 0u;
+      g[(2 * i + 1) * 4 + 2] = 0u; g[(2 * i + 1) * 4 + 3] = 0u;
+    }
+  }
+}
+
 __device__ void route_phase(Worker& w) {
   Ctx& cx = *w.cx;
   const LaunchParams& P = *cx.P;
@@ -1447,6 +1541,19 @@ __device__ void route_phase(Worker& w) {
   // index, with two warp reductions.  Lane c keeps round c's pick; the softmax of the
   // K picks is then one expf per lane and a fixed-order butterfly sum.
   const int per = (E + 31) / 32;
+  if (w.cw == 0 && w.lane == 0 && w.ok) {
+    // GEMM1's operand B (every block's share is published with the router counter seen
+    // above) -> the top of the activation buffer, whose generic reads every thread
+    // fenced before that wait; it lands while routing runs
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    const uint32_t bytes = (uint32_t)b1_bytes(dm.p);
+    const uint8_t* src = P.x_cur + P.xo.b1;
+    mbar_expect_tx(&cx.S.tcbar[TB_B1], bytes);
+    for (uint32_t o = 0; o < bytes; o += 16384)
+      bulk_g2s_plain(cx.S.act + P.g1_b_off + o, src + o, min(16384u, bytes - o), &cx.S.tcbar[TB_B1]);
+    w.b1 = true;
+    stamp_rt(P, EV_B1_ISSUED);
+  }
   {
     const int t0 = w.cw * 2;
     uint32_t key[2][kMaxExperts / 32];
@@ -1576,51 +1683,10 @@ __device__ void route_phase(Worker& w) {
   // while the rows below are converted
   cbar();
   if (tid == 0) mbar_arrive(cx.S.route_bar, 1);
-  // GEMM1 B operand: the bf16 pooled vectors, one row per token, as f16 scaled by a
-  // power of two per row (largest magnitude lands in [2^14, 2^15)).  Every bf16
-  // value within 2^29 of the row's largest is exact in f16, so GEMM1 sees u as it
-  // is; the scale goes back in through x_ts in the GEMM1 epilogue.  The router phase
-  // left u staged in the activation buffer (bf16, same layout), so the rows are
-  // converted into the top of the buffer (the bottom then takes ring tiles).
-  uint8_t* actb = cx.S.act;
-  const int nch = dm.p / 8;
-  for (int tt = 0; tt < 2 && w.ok; ++tt) {
-    const int t = w.cw * 2 + tt;
-    uint32_t amax_bits = 0u;  // |x| of non-negative floats orders like its bits
-    for (int c = w.lane; c < nch; c += 32) {
-      const uint4 v = *reinterpret_cast<const uint4*>(actb + act_off(t, c * 8));
-      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        amax_bits = max(amax_bits, max((wd[j] & 0x7FFFu) << 16, wd[j] & 0x7FFF0000u));
-    }
-    amax_bits = __reduce_max_sync(0xffffffffu, amax_bits);
-    if (tt == 0) stamp_rt(P, EV_XQ_ROW_IN);
-    const float amax = __uint_as_float(amax_bits);
-    int ex = 0;
-    if (amax > 0.f) frexpf(amax, &ex);  // amax = m 2^ex, m in [0.5, 1)
-    const float2 up = make_float2(ldexpf(1.0f, 15 - ex), ldexpf(1.0f, 15 - ex));
-    for (int c = w.lane; c < nch; c += 32) {
-      const uint4 v = *reinterpret_cast<const uint4*>(actb + act_off(t, c * 8));
-      uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f = __fmul2_rn(make_float2(__uint_as_float(wd[j] << 16), __uint_as_float(wd[j] & 0xFFFF0000u)), up);
-        wd[j] = pack_f16x2(f.x, f.y);
-      }
-      *reinterpret_cast<uint4*>(actb + P.g1_u_off + act_off(t, c * 8)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-    }
-    if (w.lane == 0) cx.S.x_ts[t] = ldexpf(1.0f, ex - 15);
-    __syncwarp();
-    stamp_rt(P, tt == 0 ? EV_XQ_ROW0_DONE : EV_XQ_ROW1_DONE);
-  }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // B operand rows -> the MMAs
   cbar();
   if (tid == 0) {
-    // first ring tile of GEMM2 (after this block's GEMM1 tiles), for the tensor-core warp
-    int lo1, hi1;
-    unit_range(*cx.S.n_active * w1_units(dm.f), rot_block(cx.block, P.phase_rot * 6, gridDim.x), gridDim.x, lo1, hi1);
-    *cx.S.tc_ti = w.ti + (uint32_t)((hi1 - lo1) * (dm.p / exp_tile_k(dm.p)));
+    // the tensor-core warp's first GEMM1 tile of the ring, then its go
+    *cx.S.tc_ti = w.ti;
     mbar_arrive(&cx.S.tcbar[TB_ROUTED], 1);
   }
   if (*cx.S.abort) w.ok = false;
@@ -1629,195 +1695,140 @@ __device__ void route_phase(Worker& w) {
 // ---------------------------------------------------------------------------
 // expert GEMMs on the tensor cores (tcgen05, accumulators in tensor memory)
 // ---------------------------------------------------------------------------
-// Work split: the block's expert units (128 rows x K, streamed as 256-column tiles)
-// are processed by the two compute warp groups in turn, tile i of the block by group
-// i & 1, and the MMAs of every tile are issued in tile order by one thread of the
-// tensor-core warp (warp 2), so each accumulator sums its K steps in a fixed order.
-// The epilogue of unit u (tensor memory -> registers -> global) is run by group u & 1
-// once it reaches unit u + 2; the two accumulators of each GEMM alternate by unit.
-//
-// GEMM1 (W4A16): the group dequantises its tile's E2M1 codes times their UE4M3 scales
-// (exact in f16, times 2^-8) into tensor memory, 128 rows x 128 K per chunk, and the
-// MMAs read A there (kind::f16) and B, the 16 pooled vectors in f16, from the
-// activation buffer.  GEMM2 (W4A4): A is the tile itself in the ring (E2M1 in the
-// 128-byte swizzle layout), B the expert's NVFP4 activation rows, and the block
-// scales of both are in tensor memory (kind::mxf4nvf4, 16-element blocks).
-
-// UE4M3 scale byte -> f16x2 {s, s} * 2^-8: E4M3 has exponent bias 7 and f16 bias 15, so
-// the byte's 7 magnitude bits shifted into f16 position give the value times 2^-8,
-// exactly (subnormal scales included).  `wm` is the scale word with bit 7 of every byte
-// (a sign UE4M3 does not have) cleared.
-__device__ __forceinline__ uint32_t ue4m3_pair_f16(uint32_t wm, int byte) {
-  return __byte_perm(wm, 0u, 0x4040u | (uint32_t)byte | ((uint32_t)byte << 8)) << 7;
-}
-// the factor the dequantised GEMM1 weights leave out
-constexpr float kExpScaleUndo = 256.0f;
+// Work split: the block's expert units (128 rows x K, streamed as tiles of 512 or 256
+// columns) are multiplied by one thread of the tensor-core warp (warp 2), which issues
+// every MMA of the block in tile order, so each accumulator sums its K steps in a fixed
+// order, and hands each ring slot back (one commit) once the tile's MMAs are done.  Both
+// GEMMs run kind::mxf4nvf4 (E2M1 x E2M1, UE4M3 scales per 16 elements) with A the weight
+// tile in the ring.  GEMM1's B is the split pooled vectors (64 rows: 4 terms x 16
+// tokens, copied in once per launch); GEMM2's B is the expert's NVFP4 activation rows.
+// The compute warp groups put each tile's weight scales into one of four scale buffers
+// in tensor memory (the block's expert tile n by group n & 1, into buffer n & 3) and run
+// the epilogues (tensor memory -> registers -> global), unit u by group u & 1; the
+// accumulators alternate by unit.  (The tensor-core warp could copy the scales itself,
+// but eight copies cost it as much issue time as the tile's eight MMAs.)
 
 __device__ __forceinline__ uint32_t tm_lane(int quadrant) { return (uint32_t)(quadrant * 32) << 16; }
 
-// GEMM1 epilogue of block-local unit `loc`: h = silu(gate) * up for the expert's tokens,
-// fp32 rows of `a` (the GEMM2 input; the consumer polls the -0.0 sentinel).  The unit's
-// sum is the issuers' partial accumulators added in a fixed order (group, issuer).
-// Every warp of the group passes both named barriers, whatever failed before.
-__device__ void g1_epilogue(Worker& w, int lo, int loc, int NT, uint32_t tm, float* xchg) {
+// GEMM1 epilogue of block-local unit `loc`: the unit's 128 accumulator rows are 64
+// (gate, up) row pairs, interleaved, so lane pairs hold the two halves of one output
+// column; h = silu(gate) * up for the expert's tokens goes to fp32 rows of `a` (the
+// GEMM2 input; the consumer polls the -0.0 sentinel).  The accumulator is released
+// whatever failed, so the tensor-core warp never waits on a skipped epilogue.
+__device__ void g1_epilogue(Worker& w, int lo, int loc, uint32_t tm) {
   Ctx& cx = *w.cx;
   const LaunchParams& P = *cx.P;
   const Dims& dm = P.dm;
   const int upe = w1_units(dm.f);
   const int gu = lo + loc, a = gu / upe, jg = gu % upe;
-  const int wg = w.cw >> 2, q = w.cw & 3, m = q * 32 + w.lane;
+  const int q = w.cw & 3, m = q * 32 + w.lane;
   const int d = loc & 1;
-  float acc[16];
+  float v[T];
+  const bool ok = __all_sync(0xffffffffu, w.ok && wait_bar(cx, &cx.S.tcbar[TB_D1_FULL + d], (loc >> 1) & 1, PH_GEMM1));
+  if (ok) {
+    tc_fence_after();
+    uint32_t r[kSplitTerms][16];
 #pragma unroll
-  for (int t = 0; t < 16; ++t) acc[t] = 0.f;
-  bool ok = w.ok;
-  for (int g = 0; g < 2; ++g) {
-    if (NT == 1 && g != (loc & 1)) continue;  // one tile per unit: only its group's issuers added to it
-    for (int iq = 0; iq < 4; ++iq) {
-      ok = __all_sync(0xffffffffu, ok && wait_bar(cx, &cx.S.tcbar[TB_D1_FULL + (g * 4 + iq) * 2 + d], (loc >> 1) & 1, PH_GEMM1));
-      if (ok) {
-        tc_fence_after();
-        uint32_t r[16];
-        tmem_ld16(tm + tm_lane(q) + tm_d1(g, iq, d), r);
-        tmem_ld_wait();
+    for (int j = 0; j < kSplitTerms; ++j) tmem_ld16(tm + tm_lane(q) + TM_D1 + d * kSplitRows + j * 16, r[j]);
+    tmem_ld_wait();
+    // sum_j 4^-j D[term j][t], smallest term first (the factors are exact)
 #pragma unroll
-        for (int t = 0; t < 16; ++t) acc[t] += __uint_as_float(r[t]);
-      }
+    for (int t = 0; t < T; ++t) {
+      float acc = __uint_as_float(r[kSplitTerms - 1][t]);
+#pragma unroll
+      for (int j = kSplitTerms - 2; j >= 0; --j) acc = fmaf(acc, 0.25f, __uint_as_float(r[j][t]));
+      v[t] = acc;
     }
   }
   tc_fence_before();
   __syncwarp();
   if (w.lane == 0) mbar_arrive(&cx.S.tcbar[TB_D1_FREE + d], 1);
-  // rows (lanes) -> shared memory, 17-float pitch (conflict-free both ways): gate rows
-  // 0..63, up rows 64..127 of the unit
-  if (ok) {
-#pragma unroll
-    for (int t = 0; t < 16; ++t) xchg[m * 17 + t] = acc[t];
+  if (!ok) {
+    w.ok = false;
+    return;
   }
-  named_bar(2 + wg, 128);
-  if (ok && m < 64) {
-    const int e = cx.S.act_e[a], n = cx.S.act_n[a];
-    float* aout = reinterpret_cast<float*>(P.x_cur + P.xo.a);
-    const uint8_t* toks = cx.S.act_tok + a * 16;
-    const float gs = P.w1_gs[e] * kExpScaleUndo;
-    for (int p = 0; p < n; ++p) {
-      const int tok = toks[p], slot = cx.S.act_slot[a * 16 + p];
-      const float sc = cx.S.x_ts[tok] * gs;
-      const float gate = xchg[m * 17 + tok] * sc, up = xchg[(64 + m) * 17 + tok] * sc;
+  const int e = cx.S.act_e[a], n = cx.S.act_n[a];
+  float* aout = reinterpret_cast<float*>(P.x_cur + P.xo.a);
+  const float gs = P.w1_gs[e];
+  for (int pi = 0; pi < n; ++pi) {
+    const int tok = cx.S.act_tok[a * 16 + pi], slot = cx.S.act_slot[a * 16 + pi];
+    float mine = 0.f;
+#pragma unroll
+    for (int t = 0; t < T; ++t) mine = t == tok ? v[t] : mine;
+    const float sc = cx.S.x_ts[tok] * gs;
+    const float up = __shfl_xor_sync(0xffffffffu, mine, 1) * sc;  // (odd lanes: the gate, unused)
+    if (!(w.lane & 1)) {
+      const float gate = mine * sc;
       const float av = gate / (1.0f + expf(-gate)) * up;
-      st_relaxed_u32(aout + (size_t)slot * dm.f + jg * 64 + m, __float_as_uint(f32_canon(av)));
+      st_relaxed_u32(aout + (size_t)slot * dm.f + jg * 64 + (m >> 1), __float_as_uint(f32_canon(av)));
     }
   }
-  named_bar(2 + wg, 128);  // the exchange rows are free for the group's next epilogue
+  if (loc < 16 && q == 0 && w.lane == 0) stamp_any(P, EV_G1_EPI_DONE + loc);
+}
+
+// Expert tile n of the block (ring tile t): its weight scales -> scale buffer n & 3 of
+// tensor memory once the MMAs of tile n - 4 are done with it, one word (a K=64 step's
+// four scales) per row in four columns, lane m = row m.  The buffer's barrier is
+// arrived at whatever failed (the tensor-core warp then gives up on its own waits).
+__device__ void stage_sfa(Worker& w, uint32_t n, uint32_t t, int K, int phase) {
+  Ctx& cx = *w.cx;
+  const int q = w.cw & 3, m = q * 32 + w.lane;
+  const uint32_t b = n & 3;
+  bool ok = w.ok && !*cx.S.abort;
+  if (n >= 4) ok = __all_sync(0xffffffffu, ok && wait_bar(cx, &cx.S.tcbar[TB_SFA_DONE + b], ((n >> 2) - 1) & 1, phase));
+  ok = __all_sync(0xffffffffu, ok && wait_tile(cx, t, phase));
+  if (ok) {
+    tc_fence_after();
+    const uint8_t* sc = cx.S.ring + cx.S.slot_off[t % kSlots] + exp_scale_off(K) + (m & 31) * 16 + (m >> 5) * 4;
+    const uint32_t dst = *cx.S.tmem_base + tm_lane(q) + TM_SFA + 32 * b;
+    for (int h = 0; h < exp_tile_k(K) / 256; ++h) {
+      uint32_t v[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t wd = *reinterpret_cast<const uint32_t*>(sc + (4 * h + j) * 512);
+        v[4 * j] = v[4 * j + 1] = v[4 * j + 2] = v[4 * j + 3] = wd;
+      }
+      tmem_st16(dst + 16 * h, v);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (w.lane == 0) mbar_arrive(&cx.S.tcbar[TB_SFA_FULL + b], 1);
   if (!ok) w.ok = false;
 }
 
-// GEMM1: the block's units are streamed as tiles, tile i to warp group i & 1.  The
-// group dequantises the tile's 128-column chunks into its two chunk buffers in tensor
-// memory (each thread one row, a warp the 32 lanes of its quadrant); once all four
-// warps have stored a chunk, lane 0 of each warp issues two of its eight K=16 MMAs into
-// that warp's own accumulator (four issuers per group run in parallel: one thread
-// issues an MMA only every ~100 cycles, four reach ~30).  The four warps of a group run
-// the same sequence of named barriers whatever fails; a failure only skips work.
+// GEMM1 on the compute side: the weight scales of tiles i = group, group + 2, ... and the
+// epilogues of units u = group, group + 2, ..., each epilogue once the group has reached
+// unit u + 2 (the tensor-core warp does the rest).
 __device__ void gemm1_phase(Worker& w) {
   Ctx& cx = *w.cx;
   const LaunchParams& P = *cx.P;
   const Dims& dm = P.dm;
   const int G = gridDim.x;
-  const int tk = exp_tile_k(dm.p), nch = tk / 128;  // tile columns, 128-column chunks per tile
-  const int na = *cx.S.n_active, upe = w1_units(dm.f), NT = dm.p / tk;
+  const int NT = dm.p / exp_tile_k(dm.p);
+  const int na = *cx.S.n_active, upe = w1_units(dm.f);
   int lo, hi;
   unit_range(na * upe, rot_block(cx.block, P.phase_rot * 6, G), G, lo, hi);
-  const int wg = w.cw >> 2, q = w.cw & 3, m = q * 32 + w.lane;
-  const uint32_t tm = *cx.S.tmem_base, tl = tm + tm_lane(q);
-  const uint32_t act_s = smem_u32(cx.S.act + P.g1_u_off);  // the 16 pooled vectors, f16
-  float* xchg = reinterpret_cast<float*>(cx.S.act + P.g1_x_off) + wg * 128 * 17;
-  const int ntiles = (hi - lo) * NT;
-  int epi = wg;        // next unit whose epilogue this group runs
-  int prev_loc = -1;   // unit of the group's previous tile
-  for (int i = wg; i < ntiles; i += 2) {
-    const int loc = i / NT, kt = i % NT, d = loc & 1;
-    for (; epi <= loc - 2; epi += 2) g1_epilogue(w, lo, epi, NT, tm, xchg);
-    const bool unit_start = loc != prev_loc;  // the group's first tile of this unit
-    prev_loc = loc;
-    bool ok = w.ok && !*cx.S.abort;
-    // this warp's accumulator of the unit's parity is free once the epilogue of unit
-    // loc - 2 has read it
-    if (unit_start && loc >= 2)
-      ok = __all_sync(0xffffffffu, ok && wait_bar(cx, &cx.S.tcbar[TB_D1_FREE + d], ((loc >> 1) - 1) & 1, PH_GEMM1));
-    const uint32_t t = w.ti + (uint32_t)i;
-    const uint32_t s = t % kSlots;
-    ok = __all_sync(0xffffffffu, ok && wait_tile(cx, t, PH_GEMM1));
-    if (loc == 0 && i < 2) stamp_rt(P, EV_G1_FIRST_READY);
-    if (i < 16 && w.lane == 0 && q == 0) stamp_any(P, EV_WG_G1_LANDED + i);
-    const uint8_t* tb = cx.S.ring + cx.S.slot_off[s];
-    uint32_t sw[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // the row's block scales, bit 7 cleared
-    if (ok) {
-#pragma unroll
-      for (int i2 = 0; i2 < 2; ++i2) {
-        if (i2 * 256 >= tk) break;
-        const uint4 scw = *reinterpret_cast<const uint4*>(tb + exp_scale_off(dm.p) + m * (tk / 16) + i2 * 16);
-        sw[4 * i2 + 0] = scw.x & 0x7F7F7F7Fu; sw[4 * i2 + 1] = scw.y & 0x7F7F7F7Fu;
-        sw[4 * i2 + 2] = scw.z & 0x7F7F7F7Fu; sw[4 * i2 + 3] = scw.w & 0x7F7F7F7Fu;
-      }
+  if (w.b1) {
+    // the operand copy has landed before the top of the buffer is used again (GEMM2),
+    // or the block exits, whatever failed
+    for (uint32_t it = 0; it < (1u << 24) && !mbar_try_wait(&cx.S.tcbar[TB_B1], 0); ++it) {
     }
-    const int n = i >> 1;  // the group's tile count so far
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      if (h >= nch) break;
-      // the group's chunk n nch + h goes to its chunk buffer (n nch + h) & 1
-      const int cc = n * nch + h, b = wg * 2 + (cc & 1), use = cc >> 1;
-      if (use >= 1) {
-        ok = __all_sync(0xffffffffu, ok && wait_bar(cx, &cx.S.tcbar[TB_G1_FREE + b], (use - 1) & 1, PH_GEMM1));
-        if (ok) tc_fence_after();
-      }
-      if (ok) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          // 16 code bytes = K 32 c .. 32 c + 31 of the chunk = two 16-element scale blocks
-          const uint4 cw = *reinterpret_cast<const uint4*>(tb + (h >> 1) * kExpBlockBytes + m * 128 +
-                                                           ((((4 * (h & 1) + c) ^ (m & 7))) << 4));
-          const int blk = 8 * h + 2 * c;
-          const uint32_t s0 = ue4m3_pair_f16(sw[blk >> 2], blk & 3), s1 = ue4m3_pair_f16(sw[(blk + 1) >> 2], (blk + 1) & 3);
-          uint32_t v[16];
-          e2m1x8_to_f16x8(cw.x, v[0], v[1], v[2], v[3]);
-          e2m1x8_to_f16x8(cw.y, v[4], v[5], v[6], v[7]);
-          e2m1x8_to_f16x8(cw.z, v[8], v[9], v[10], v[11]);
-          e2m1x8_to_f16x8(cw.w, v[12], v[13], v[14], v[15]);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = hmul2(v[j], s0);
-#pragma unroll
-          for (int j = 8; j < 16; ++j) v[j] = hmul2(v[j], s1);
-          tmem_st16(tl + TM_ABUF + b * 64 + c * 16, v);
-        }
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      named_bar(2 + wg, 128);  // the chunk's 128 rows are in tensor memory
-      if (w.lane == 0 && ok) {
-        tc_fence_after();
-        if (h == 0 && i < 16 && q == 0) stamp_any(P, EV_TC_G1_READY + i);
-#pragma unroll
-        for (int jj = 2 * q; jj < 2 * q + 2; ++jj) {
-          const int ks = (kt * tk + h * 128) / 16 + jj;  // 16-column step of the pooled vectors
-          mma_f16_ts(tm + tm_d1(wg, q, d), tm + TM_ABUF + b * 64 + jj * 8,
-                     sdesc_k_sw128(act_s + (ks >> 2) * 2048 + (ks & 3) * 32), idesc_f16(16),
-                     !(unit_start && h == 0 && jj == 2 * q));
-        }
-        tc_commit(&cx.S.tcbar[TB_G1_FREE + b]);
-        // the group's last chunk of the unit: this issuer's accumulator is complete
-        if (h == nch - 1 && kt + 2 >= NT) tc_commit(&cx.S.tcbar[TB_D1_FULL + (wg * 4 + q) * 2 + d]);
-        if (h == nch - 1 && i < 16 && q == 0) stamp_any(P, EV_TC_G1_ISSUED + i);
-      }
-      __syncwarp();
-    }
-    // the tile's shared memory is read: release its ring slot
-    if (w.lane == 0 && ok) mbar_arrive(&cx.S.empty[s], kComputeWarps / 4);
-    if (!ok) w.ok = false;
   }
-  for (; epi < hi - lo; epi += 2) g1_epilogue(w, lo, epi, NT, tm, xchg);
+  const uint32_t tm = *cx.S.tmem_base;
+  const int wg = w.cw >> 2;
+  const int ntiles = (hi - lo) * NT;
+  if (hi > lo) stamp_rt(P, EV_G1_FIRST_READY);
+  int epi = wg;  // next unit whose epilogue this group runs
+  for (int i = wg; i < ntiles; i += 2) {
+    for (; epi <= i / NT - 2; epi += 2) g1_epilogue(w, lo, epi, tm);
+    stage_sfa(w, (uint32_t)i, w.ti + (uint32_t)i, dm.p, PH_GEMM1);
+  }
+  for (; epi < hi - lo; epi += 2) g1_epilogue(w, lo, epi, tm);
   if (hi > lo) stamp_rt(P, EV_G1_LAST_DONE);
   w.ti += (uint32_t)ntiles;
+  w.xseq = (uint32_t)ntiles;
 }
 
 // every MMA this thread issued has completed (bounded wait) before tensor memory is freed
@@ -1870,15 +1881,14 @@ __device__ void gemm2_phase(Worker& w) {
   const LaunchParams& P = *cx.P;
   const Dims& dm = P.dm;
   const int G = gridDim.x;
-  const int tk = exp_tile_k(dm.f), nmma = tk / 64;  // tile columns, K=64 MMAs per tile
-  const int na = *cx.S.n_active, upe = w2_units(dm.p), NT = dm.f / tk;
+  const int na = *cx.S.n_active, upe = w2_units(dm.p), NT = dm.f / exp_tile_k(dm.f);
   int lo, hi;
   unit_range(na * upe, rot_block(cx.block, P.phase_rot * 7, G), G, lo, hi);
   const float* ain = reinterpret_cast<const float*>(P.x_cur + P.xo.a);
   const uint32_t region = (uint32_t)dm.f * 8;  // one expert's 16 activation rows, E2M1, B layout
   uint8_t* g2b = cx.S.act + P.g2_off;          // the round's two experts' B operands
   uint8_t* sfb_stage = g2b + 2 * region;       // [2][16][F/16] UE4M3 block scales
-  const int wg = w.cw >> 2, q = w.cw & 3, m = q * 32 + w.lane;
+  const int wg = w.cw >> 2, q = w.cw & 3;
   const uint32_t tm = *cx.S.tmem_base, tl = tm + tm_lane(q);
   const int tid = w.cw * 32 + w.lane;
   if (hi > lo) {
@@ -1977,7 +1987,7 @@ __device__ void gemm2_phase(Worker& w) {
                                       : 0u;
               v[4 * j] = v[4 * j + 1] = v[4 * j + 2] = v[4 * j + 3] = wd;
             }
-            tmem_st16(tl + TM_SFB + ea * 64 + g * 4, v);
+            tmem_st16(tl + TM_SFB2 + ea * 64 + g * 4, v);
           }
         }
         tmem_st_wait();
@@ -1988,42 +1998,14 @@ __device__ void gemm2_phase(Worker& w) {
       if (a0 == a_first) stamp_rt(P, EV_GEMM2_IN);
       else stamp_rt(P, EV_G2_STAGE2_DONE);
       if (*cx.S.abort) w.ok = false;
-      // this round's units: weight block scales of the group's tiles -> tensor memory
+      // this round's tiles: weight scales of the group's tiles (expert tile n = xseq + i
+      // by group n & 1), epilogues interleaved
       const int u_lo = max(lo, a0 * upe), u_hi = min(hi, (a1 + 1) * upe);
       const int i_lo = (u_lo - lo) * NT, i_hi = (u_hi - lo) * NT;
-      for (int i = i_lo + ((i_lo & 1) != wg ? 1 : 0); i < i_hi && w.ok; i += 2) {
-        const int loc = i / NT;
-        for (; epi <= loc - 2 && w.ok; epi += 2) g2_epilogue(w, lo, epi, a0, tm);
-        if (!w.ok) break;
-        const int n = i >> 1, b = 2 * wg + (n & 1), use = n >> 1;
-        if (use >= 1) {
-          if (!__all_sync(0xffffffffu, wait_bar(cx, &cx.S.tcbar[TB_SFA_FREE + b], (use - 1) & 1, PH_GEMM2))) {
-            w.ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
-        const uint32_t t = w.ti + (uint32_t)i;
-        if (!__all_sync(0xffffffffu, wait_tile(cx, t, PH_GEMM2))) {
-          w.ok = false;
-          break;
-        }
+      for (int i = i_lo + ((int)((w.xseq + (uint32_t)i_lo) & 1u) != wg ? 1 : 0); i < i_hi; i += 2) {
+        for (; epi <= i / NT - 2 && w.ok; epi += 2) g2_epilogue(w, lo, epi, a0, tm);
+        stage_sfa(w, w.xseq + (uint32_t)i, w.ti + (uint32_t)i, dm.f, PH_GEMM2);
         if (i < 2 && a0 == a_first) stamp_rt(P, EV_G2_FIRST_READY);
-        // the row's scale word of each K=64 step in four columns (row m reads lane m,
-        // column + m / 32)
-#pragma unroll
-        for (int i2 = 0; i2 < 2; ++i2) {
-          if (i2 * 4 >= nmma) break;
-          const uint4 scw = *reinterpret_cast<const uint4*>(cx.S.ring + cx.S.slot_off[t % kSlots] + exp_scale_off(dm.f) +
-                                                            m * (tk / 16) + i2 * 16);
-          const uint32_t v[16] = {scw.x, scw.x, scw.x, scw.x, scw.y, scw.y, scw.y, scw.y,
-                                  scw.z, scw.z, scw.z, scw.z, scw.w, scw.w, scw.w, scw.w};
-          tmem_st16(tl + TM_SFA + b * 32 + i2 * 16, v);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (w.lane == 0) mbar_arrive(&cx.S.tcbar[TB_SFA_FULL + b], 1);
       }
       // every epilogue of the round before its operands are replaced
       for (; epi < u_hi - lo && w.ok; epi += 2) g2_epilogue(w, lo, epi, a0, tm);
@@ -2033,62 +2015,120 @@ __device__ void gemm2_phase(Worker& w) {
   w.ti += (uint32_t)((hi - lo) * NT);
 }
 
-// The tensor-core warp: one thread issues every GEMM2 MMA of the block in tile order
+// The tensor-core warp: one thread issues every expert MMA of the block in tile order
 // (orcarouter.ai, § "where the kernel boundary sits": warps dedicated to driving the
-// tensor cores), and the ring tiles go back to the loader when their MMAs are done.
+// tensor cores) and hands each ring slot back to the loader when the tile's MMAs are done.
+
+// expert tile seq's weight scales are in scale buffer seq & 3 and the tile has landed
+__device__ __forceinline__ bool tile_ready(Ctx& cx, uint32_t seq, uint32_t t, int phase) {
+  return wait_bar(cx, &cx.S.tcbar[TB_SFA_FULL + (seq & 3)], (seq >> 2) & 1, phase) && wait_tile(cx, t, phase);
+}
+// a tile's MMAs are issued: its scale buffer and its ring slot are released when they are done
+__device__ __forceinline__ void tile_done(Ctx& cx, uint32_t seq, uint32_t t) {
+  tc_commit(&cx.S.tcbar[TB_SFA_DONE + (seq & 3)]);
+  tc_commit(&cx.S.tcbar[TB_SLOT + t % kSlots]);
+}
+
 __device__ void tc_issuer(Ctx& cx) {
   const LaunchParams& P = *cx.P;
   const Dims& dm = P.dm;
   uint64_t* tb = cx.S.tcbar;
   const uint32_t tm = *cx.S.tmem_base;
   const int G = gridDim.x;
-  const uint32_t act_s = smem_u32(cx.S.act + P.g2_off);  // GEMM2 operand B of the round
   bool ok = wait_bar(cx, &tb[TB_ROUTED], 0, PH_ROUTE);
   if (ok) {
-    const int tk = exp_tile_k(dm.f), nmma = tk / 64;
-    const int na = *cx.S.n_active, upe = w2_units(dm.p), NT = dm.f / tk;
-    int lo, hi;
-    unit_range(na * upe, rot_block(cx.block, P.phase_rot * 7, G), G, lo, hi);
-    const uint32_t t0 = *cx.S.tc_ti, region = (uint32_t)dm.f * 8;
-    if (hi > lo) {
-      const int a_first = lo / upe, a_last = (hi - 1) / upe;
-      int round = 0;
-      for (int a0 = a_first; a0 <= a_last && ok; a0 += 2, ++round) {
-        const int a1 = min(a0 + 1, a_last);
-        ok = wait_bar(cx, &tb[TB_G2_STAGE], round & 1, PH_GEMM2);
-        if (!ok) break;
-        tc_fence_after();
-        const int u_lo = max(lo, a0 * upe), u_hi = min(hi, (a1 + 1) * upe);
-        for (int gu = u_lo; gu < u_hi && ok; ++gu) {
-          const int loc = gu - lo, ea = gu / upe - a0, d = loc & 1;
-          if (loc >= 2) {
-            ok = wait_bar(cx, &tb[TB_D2_FREE + d], ((loc >> 1) - 1) & 1, PH_GEMM2);
-            if (!ok) break;
-            tc_fence_after();
+    const int na = *cx.S.n_active;
+    uint32_t seq = 0;                 // expert tiles issued so far
+    const uint32_t t1 = *cx.S.tc_ti;  // ring index of the block's first expert tile
+    uint32_t t2 = t1;                 // ... of its first GEMM2 tile
+    // ---- GEMM1: D[128 rows][term 16 + token] += W1 tile . B^T ----
+    {
+      const int tk = exp_tile_k(dm.p), nst = tk / 64, NT = dm.p / tk;
+      int lo, hi;
+      unit_range(na * w1_units(dm.f), rot_block(cx.block, P.phase_rot * 6, G), G, lo, hi);
+      t2 = t1 + (uint32_t)((hi - lo) * NT);
+      const uint32_t b_s = smem_u32(cx.S.act + P.g1_b_off);
+      if (hi > lo) {
+        ok = wait_bar(cx, &tb[TB_B1], 0, PH_GEMM1);
+        if (ok) {
+          stamp_any(P, EV_B1_LANDED);
+          // the operand's scale groups -> tensor memory, one per K=64 step
+          for (int s = 0; s < dm.p / 64; ++s)
+            tc_cp_32x128b_x4(tm + TM_SFB1 + 4 * s, sdesc_plain(b_s + (uint32_t)b1_code_bytes(dm.p) + 512 * s, 128));
+        }
+      }
+      for (int loc = 0; loc < hi - lo && ok; ++loc) {
+        const int d = loc & 1;
+        if (loc >= 2) {
+          ok = wait_bar(cx, &tb[TB_D1_FREE + d], ((loc >> 1) - 1) & 1, PH_GEMM1);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        for (int kt = 0; kt < NT; ++kt) {
+          const int i = loc * NT + kt;
+          const uint32_t t = t1 + (uint32_t)i;
+          ok = tile_ready(cx, seq, t, PH_GEMM1);
+          if (!ok) break;
+          if (i < 16) stamp_any(P, EV_TC_G1_READY + i);
+          tc_fence_after();
+          const uint32_t a_s = smem_u32(cx.S.ring + cx.S.slot_off[t % kSlots]);
+          const uint32_t sfa = tm + TM_SFA + 32 * (seq & 3);
+          for (int j = 0; j < nst; ++j) {
+            const int kg = kt * tk + 64 * j;  // first column of the step
+            mma_nvf4_ss(tm + TM_D1 + d * kSplitRows, sdesc_k_sw128(a_s + (j >> 2) * kExpBlockBytes + (j & 3) * 32),
+                        sdesc_k_sw128(b_s + (kg >> 8) * (kSplitRows * 128) + ((kg >> 6) & 3) * 32), idesc_nvf4(kSplitRows),
+                        sfa + 4 * j, tm + TM_SFB1 + 4 * (kg >> 6), (kt | j) != 0);
           }
-          for (int kt = 0; kt < NT && ok; ++kt) {
-            const int i = loc * NT + kt, n = i >> 1, b = 2 * (i & 1) + (n & 1);
-            ok = wait_bar(cx, &tb[TB_SFA_FULL + b], (n >> 1) & 1, PH_GEMM2);
-            const uint32_t t = t0 + (uint32_t)i;
-            if (ok) ok = wait_tile(cx, t, PH_GEMM2);
-            if (!ok) break;
-            if (i < 8) stamp_any(P, EV_TC_G2_READY + i);
-            tc_fence_after();
-            const uint32_t a_s = smem_u32(cx.S.ring + cx.S.slot_off[t % kSlots]);
-            for (int j = 0; j < nmma; ++j) {
-              const int kb = j >> 2, jj = j & 3;  // 16 KB column block, K=64 step inside it
-              mma_nvf4_ss(tm + TM_D2 + d * 16, sdesc_k_sw128(a_s + kb * kExpBlockBytes + jj * 32),
-                          sdesc_k_sw128(act_s + ea * region + (kt * (tk / 256) + kb) * 2048 + jj * 32), idesc_nvf4(16),
-                          tm + TM_SFA + b * 32 + j * 4, tm + TM_SFB + ea * 64 + (kt * nmma + j) * 4, (kt | j) != 0);
+          tile_done(cx, seq, t);
+          ++seq;
+          if (i < 16) stamp_any(P, EV_TC_G1_ISSUED + i);
+        }
+        if (ok) tc_commit(&tb[TB_D1_FULL + d]);
+      }
+    }
+    // ---- GEMM2: D[128 rows][token slot] += W2 tile . B^T, two experts per round ----
+    if (ok) {
+      const int tk = exp_tile_k(dm.f), nst = tk / 64, NT = dm.f / tk, upe = w2_units(dm.p);
+      int lo, hi;
+      unit_range(na * upe, rot_block(cx.block, P.phase_rot * 7, G), G, lo, hi);
+      const uint32_t act_s = smem_u32(cx.S.act + P.g2_off), region = (uint32_t)dm.f * 8;
+      if (hi > lo) {
+        const int a_first = lo / upe, a_last = (hi - 1) / upe;
+        int round = 0;
+        for (int a0 = a_first; a0 <= a_last && ok; a0 += 2, ++round) {
+          const int a1 = min(a0 + 1, a_last);
+          ok = wait_bar(cx, &tb[TB_G2_STAGE], round & 1, PH_GEMM2);
+          if (!ok) break;
+          tc_fence_after();
+          const int u_lo = max(lo, a0 * upe), u_hi = min(hi, (a1 + 1) * upe);
+          for (int gu = u_lo; gu < u_hi && ok; ++gu) {
+            const int loc = gu - lo, ea = gu / upe - a0, d = loc & 1;
+            if (loc >= 2) {
+              ok = wait_bar(cx, &tb[TB_D2_FREE + d], ((loc >> 1) - 1) & 1, PH_GEMM2);
+              if (!ok) break;
+              tc_fence_after();
             }
-            tc_commit(&tb[TB_SFA_FREE + b]);
-            // the ring slot goes back to the loader when the tile's MMAs are done: one
-            // arrival per commit, as many as a slot's consumers give
-#pragma unroll
-            for (int c = 0; c < kComputeWarps; ++c) tc_commit(&cx.S.empty[t % kSlots]);
-            if (i < 8) stamp_any(P, EV_TC_G2_ISSUED + i);
+            for (int kt = 0; kt < NT; ++kt) {
+              const int i = loc * NT + kt;
+              const uint32_t t = t2 + (uint32_t)i;
+              ok = tile_ready(cx, seq, t, PH_GEMM2);
+              if (!ok) break;
+              if (i < 8) stamp_any(P, EV_TC_G2_READY + i);
+              tc_fence_after();
+              const uint32_t a_s = smem_u32(cx.S.ring + cx.S.slot_off[t % kSlots]);
+              const uint32_t sfa = tm + TM_SFA + 32 * (seq & 3);
+              for (int j = 0; j < nst; ++j) {
+                const int kb = j >> 2, jj = j & 3;  // 16 KB column block, K=64 step inside it
+                mma_nvf4_ss(tm + TM_D2 + d * 16, sdesc_k_sw128(a_s + kb * kExpBlockBytes + jj * 32),
+                            sdesc_k_sw128(act_s + ea * region + (kt * (tk / 256) + kb) * 2048 + jj * 32), idesc_nvf4(16),
+                            sfa + 4 * j, tm + TM_SFB2 + ea * 64 + (kt * nst + j) * 4, (kt | j) != 0);
+              }
+              tile_done(cx, seq, t);
+              ++seq;
+              if (i < 8) stamp_any(P, EV_TC_G2_ISSUED + i);
+            }
+            if (ok) tc_commit(&tb[TB_D2_FULL + d]);
           }
-          if (ok) tc_commit(&tb[TB_D2_FULL + d]);
         }
       }
     }
@@ -2159,7 +2199,7 @@ __device__ void rearm(const LaunchParams& P, int block, int tid, int nthreads) {
       {P.xo.u, P.xo.logits - P.xo.u, 0xFFFFFFFFu}, {P.xo.logits, P.xo.a - P.xo.logits, kF32Empty},
       {P.xo.a, P.xo.z - P.xo.a, kF32Empty},       {P.xo.z, P.xo.h2 - P.xo.z, 0xFFFFFFFFu},
       {P.xo.h2, P.xo.q0 - P.xo.h2, 0xFFFFFFFFu},   {P.xo.q0, P.xo.tkv0 - P.xo.q0, 0xFFFFFFFFu},
-      {P.xo.tkv0, P.xo.cnt - P.xo.tkv0, 0xFFFFFFFFu}, {P.xo.cnt, P.xo.total - P.xo.cnt, 0u}};
+      {P.xo.tkv0, P.xo.cnt - P.xo.tkv0, 0xFFFFFFFFu}, {P.xo.cnt, P.xo.b1 - P.xo.cnt, 0u}};
   const int G = gridDim.x;
 #pragma unroll 1
   for (int ri = 0; ri < 10; ++ri) {
@@ -2241,10 +2281,15 @@ __device__ void compute_main(Worker& w) {
     ea.kind = EPI_ROUTER;
     ea.out32 = lg;
     dense_phase(w, dm.p, dm.e, P.phase_rot * 5, ea, -1);
+    // a8 (GEMM1 side): this block's share of the split pooled vectors
+    split_pooled(w);
+    stamp_rt(P, EV_SPLIT_DONE);
     publish(w, CNT_ROUTER);
     stamp<kTiming>(P, b, EV_ROUTER_DONE);
   }
-  // a6/a7/a8: top-k, dispatch, NVFP4 activations
+  // a6/a7: top-k and dispatch (and the copy of GEMM1's operand B, which overwrites the
+  // staged pooled vectors: every thread's generic accesses of them go first)
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   await_phase(w, CNT_ROUTER, PH_ROUTE);
   route_phase(w);
   stamp<kTiming>(P, b, EV_ROUTE_DONE);
@@ -2325,8 +2370,8 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
     mbar_init(cx.S.route_bar, 1);
     mbar_init(cx.S.stage_bar, 1);
     for (int i = 0; i < kTcBars; ++i) {
-      const bool by4 = (i >= TB_G1_FREE && i < TB_G1_FREE + 4) || (i >= TB_D1_FREE && i < TB_D1_FREE + 2) ||
-                       (i >= TB_SFA_FULL && i < TB_SFA_FULL + 4) || (i >= TB_D2_FREE && i < TB_D2_FREE + 2);
+      const bool by4 = (i >= TB_D1_FREE && i < TB_D1_FREE + 2) || (i >= TB_D2_FREE && i < TB_D2_FREE + 2) ||
+                       (i >= TB_SFA_FULL && i < TB_SFA_FULL + 4);
       mbar_init(&cx.S.tcbar[i], i == TB_DONE ? kComputeWarps : by4 ? 4 : 1);
     }
     for (int i = 0; i < kSlots; ++i) cx.S.slot_tile[i] = 0xFFFFFFFFu;
@@ -2454,13 +2499,14 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
   w.q = lane & 3;
   w.ti = 0;
   w.ok = true;
+  w.b1 = false;
+  w.xseq = 0;
   pdl_wait();
   cx.deadline = globaltimer() + (((uint64_t)P.timeout_ns_hi << 32) | P.timeout_ns_lo);
   stamp<kTiming>(P, blockIdx.x, EV_START);
   compute_main<kTiming>(w);
   stamp<kTiming>(P, blockIdx.x, EV_END);
-  // every MMA this warp issued has completed before the block frees tensor memory
-  if (lane == 0) tc_drain(&cx.S.tcbar[TB_WDRAIN + w.cw]);
+  // the warp's tensor-memory accesses are done before the block frees it
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(&cx.S.tcbar[TB_DONE], 1);

@@ -10,10 +10,12 @@
 //
 // NVFP4 expert matrices become 128-row units of 512-column tiles (256 where the width is
 // not a multiple of 512): column blocks of 128 rows x 128 code bytes in the 128-byte
-// swizzle layout the tensor cores read (and the dequantising threads read without bank
-// conflicts), then each row's block scales.  W1 units
-// hold 64 gate rows then the 64 matching up rows, so one unit feeds the SwiGLU
-// epilogue.
+// swizzle layout the tensor cores read, then the block scales grouped per K=64 step (the
+// scale word of row m at (m % 32) * 16 + (m / 32) * 4 of its 512-byte group: 128 threads
+// read a step's words with 4-way bank conflicts at most).  W1 units hold 64 gate rows and
+// the 64 matching up
+// rows, interleaved (gate j, up j, gate j + 1, ...), so neighbouring lanes of the SwiGLU
+// epilogue hold the two halves of an output.
 #include "msm_device.cuh"
 #include "msm_internal.h"
 
@@ -52,7 +54,8 @@ __global__ void pack_dense_kernel(const uint16_t* __restrict__ W, uint8_t* __res
 
 // one thread per (expert, unit, k-tile, row): the row's code bytes of the tile go to row m
 // of each 16 KB column block with 16-byte chunk c at chunk c ^ (m & 7) (the 128-byte
-// swizzle of a K-major tensor-core operand), its block scales to the tile's scale rows
+// swizzle of a K-major tensor-core operand), its block scales to byte (m % 32) * 16 +
+// (m / 32) * 4 + b % 4 of the tile's scale group b / 4
 __global__ void pack_nvfp4_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ sf,
                                   uint8_t* __restrict__ out, int E, int rows, int K, int swiglu, int F) {
   const int units = swiglu ? w1_units(F) : w2_units(rows);
@@ -65,16 +68,16 @@ __global__ void pack_nvfp4_kernel(const uint8_t* __restrict__ codes, const uint8
     const int kt = (int)(rest % nt);
     const long long eu = rest / nt;
     const int u = (int)(eu % units), e = (int)(eu / units);
-    const int R = swiglu ? ((m < 64) ? u * 64 + m : F + u * 64 + (m - 64)) : u * kExpTileRows + m;
+    const int R = swiglu ? ((m & 1) ? F : 0) + u * 64 + (m >> 1) : u * kExpTileRows + m;
     const uint4* crow = reinterpret_cast<const uint4*>(codes + ((size_t)e * rows + R) * (K / 2) + (size_t)kt * (tk / 2));
-    const uint4* srow = reinterpret_cast<const uint4*>(sf + ((size_t)e * rows + R) * (K / 16) + (size_t)kt * (tk / 16));
+    const uint8_t* srow = sf + ((size_t)e * rows + R) * (K / 16) + (size_t)kt * (tk / 16);
     uint8_t* tile = out + ((size_t)eu * nt + kt) * exp_tile_bytes(K);
     for (int kb = 0; kb < nkb; ++kb)
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
         *reinterpret_cast<uint4*>(tile + kb * kExpBlockBytes + m * 128 + ((ch ^ (m & 7)) << 4)) = crow[kb * 8 + ch];
-    for (int i = 0; i < tk / 256; ++i)
-      *reinterpret_cast<uint4*>(tile + exp_scale_off(K) + m * (tk / 16) + i * 16) = srow[i];
+    for (int b = 0; b < tk / 16; ++b)
+      tile[exp_scale_off(K) + (b >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (b & 3)] = srow[b];
   }
 }
 
