@@ -211,11 +211,13 @@ __host__ __device__ inline int w2_units(int p) { return p / kExpTileRows; }
 // one B row per (term, token) pair, row n = term * 16 + token: p / 256 column blocks of
 // 64 rows x 128 code bytes (128-byte swizzle, 8 KB each), then p / 64 scale groups of
 // 512 bytes, one per K=64 step, for the tensor-memory copy (32 lines of 16 bytes; line l:
-// the scale words of rows l and l + 32, two zero words)
+// the scale words of rows l and l + 32, two zero words), then the 16 tokens' fp32 row
+// scales (256 bytes)
 constexpr int kSplitTerms = 4;
 constexpr int kSplitRows = kSplitTerms * T;
 __host__ __device__ inline uint64_t b1_code_bytes(int p) { return (uint64_t)p / 256 * kSplitRows * 128; }
-__host__ __device__ inline uint64_t b1_bytes(int p) { return b1_code_bytes(p) + (uint64_t)p / 64 * 512; }
+__host__ __device__ inline uint64_t b1_ts_off(int p) { return b1_code_bytes(p) + (uint64_t)p / 64 * 512; }
+__host__ __device__ inline uint64_t b1_bytes(int p) { return b1_ts_off(p) + 256; }
 
 // kernel entry points (defined in msm_kernel.cu / msm_pack.cu)
 const void* layer_kernel(bool timing);

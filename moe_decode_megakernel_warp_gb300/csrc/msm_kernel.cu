@@ -1458,40 +1458,56 @@ __device__ void attn_merge_phase(Worker& w) {
 // bf16's own rounding of the larger elements.  With u in this form the GEMM1 products
 // run on the block-scaled tensor cores straight from the weights' E2M1 codes in the ring
 // (one B row per (term, token)); the 4^-j ts_t factors go in per accumulator column in
-// the epilogue.  The blocks split the 16 x p/16 (token, 16-column block) pairs, 16
-// threads per pair, and store their share in the launch's exchange buffer; the router
-// counter publishes it and every block then copies the whole operand in.
+// the epilogue.  The blocks without router work split the 16 x p/16 (token, 16-column
+// block) pairs among themselves, 16 threads per pair, and store their share (and the
+// row scales of the tokens whose first pair they own) in the launch's exchange buffer;
+// the router counter publishes it and every block then copies the whole operand in.
 __device__ void split_pooled(Worker& w) {
   Ctx& cx = *w.cx;
   const LaunchParams& P = *cx.P;
-  const int p = P.dm.p;
+  const int p = P.dm.p, G = gridDim.x;
   const int tid = w.cw * 32 + w.lane;
-  if (w.ok) {
-    // the row scales: 16 threads per pooled vector (staged in the activation buffer)
-    const int t = tid >> 4, sub = tid & 15;
+  // the router phase's units go one per block (fewer units than blocks): the others split
+  const int n_router = P.dm.e / 16, bb = rot_block(cx.block, P.phase_rot * 5, G);
+  int rlo, rhi, idx = cx.block, nfree = G;
+  unit_range(n_router, bb, G, rlo, rhi);
+  if (n_router < G) {
+    if (rhi > rlo) return;
+    idx = bb - rlo;  // blocks before this one took one unit each
+    nfree = G - n_router;
+  }
+  const int nb = p / 16;
+  int lo, hi;
+  unit_range(T * nb, idx, nfree, lo, hi);
+  if (lo >= hi) return;
+  // the row scales of this block's tokens (at most two: a block has fewer than nb pairs;
+  // a warp that failed still passes the barriers)
+  const int t0 = lo / nb, t1 = (hi - 1) / nb;
+  float* red = cx.S.red;
+  for (int t = t0; t <= t1 && w.ok; ++t) {
     uint32_t am = 0u;  // |x| of non-negative floats orders like its bits
-    for (int c = sub; c < p / 8; c += 16) {
+    for (int c = tid; c < p / 8; c += kComputeThreads) {
       const uint4 v = *reinterpret_cast<const uint4*>(cx.S.act + act_off(t, c * 8));
       const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) am = max(am, max((wd[j] & 0x7FFFu) << 16, wd[j] & 0x7FFF0000u));
     }
-#pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, o));
-    if (sub == 0) {
-      float ts = __fdiv_rn(__uint_as_float(am), 2688.0f);  // amax / (6 * 448), up to a power of two
-      if (ts > 0.f) {
-        int ex;
-        if (frexpf(ts, &ex) != 0.5f) ts = ldexpf(1.0f, ex);
-      }
-      cx.S.x_ts[t] = ts;
-    }
+    am = __reduce_max_sync(0xffffffffu, am);
+    if (w.lane == 0) reinterpret_cast<uint32_t*>(red)[(t - t0) * kComputeWarps + w.cw] = am;
   }
   cbar();
-  if (!w.ok) return;
-  const int nb = p / 16;
-  int lo, hi;
-  unit_range(T * nb, cx.block, gridDim.x, lo, hi);
+  if (tid <= t1 - t0 && !*cx.S.abort) {
+    uint32_t am = 0u;
+    for (int i = 0; i < kComputeWarps; ++i) am = max(am, reinterpret_cast<uint32_t*>(red)[tid * kComputeWarps + i]);
+    float ts = __fdiv_rn(__uint_as_float(am), 2688.0f);  // amax / (6 * 448), up to a power of two
+    if (ts > 0.f) {
+      int ex;
+      if (frexpf(ts, &ex) != 0.5f) ts = ldexpf(1.0f, ex);
+    }
+    cx.S.x_ts[t0 + tid] = ts;
+  }
+  cbar();
+  if (!w.ok || *cx.S.abort) return;
   const int h = tid >> 4, i = tid & 15;
   const uint32_t hmask = 0xFFFFu << (w.lane & 16);  // this half-warp's lanes
   uint8_t* img = P.x_cur + P.xo.b1;
@@ -1500,6 +1516,7 @@ __device__ void split_pooled(Worker& w) {
     const int t = pr / nb, c = pr % nb, k = c * 16 + i;
     float x = bf16_to_f32(*reinterpret_cast<const uint16_t*>(cx.S.act + act_off(t, k) + (k & 7) * 2));
     float ts = cx.S.x_ts[t];
+    if (c == 0 && i == 0) reinterpret_cast<float*>(img + b1_ts_off(p))[t] = ts;
 #pragma unroll
     for (int j = 0; j < kSplitTerms; ++j, ts *= 0.25f) {
       float bmax = fabsf(x);
@@ -1750,12 +1767,13 @@ __device__ void g1_epilogue(Worker& w, int lo, int loc, uint32_t tm) {
   const int e = cx.S.act_e[a], n = cx.S.act_n[a];
   float* aout = reinterpret_cast<float*>(P.x_cur + P.xo.a);
   const float gs = P.w1_gs[e];
+  const float* ts1 = reinterpret_cast<const float*>(cx.S.act + P.g1_b_off + b1_ts_off(dm.p));  // row scales
   for (int pi = 0; pi < n; ++pi) {
     const int tok = cx.S.act_tok[a * 16 + pi], slot = cx.S.act_slot[a * 16 + pi];
     float mine = 0.f;
 #pragma unroll
     for (int t = 0; t < T; ++t) mine = t == tok ? v[t] : mine;
-    const float sc = cx.S.x_ts[tok] * gs;
+    const float sc = ts1[tok] * gs;
     const float up = __shfl_xor_sync(0xffffffffu, mine, 1) * sc;  // (odd lanes: the gate, unused)
     if (!(w.lane & 1)) {
       const float gate = mine * sc;
@@ -1810,9 +1828,11 @@ __device__ void gemm1_phase(Worker& w) {
   const int na = *cx.S.n_active, upe = w1_units(dm.f);
   int lo, hi;
   unit_range(na * upe, rot_block(cx.block, P.phase_rot * 6, G), G, lo, hi);
+  // the operand (its row scales are read by the epilogues) has landed; the thread that
+  // issued the copy waits for it whatever failed, before the top of the buffer is used
+  // again (GEMM2) or the block exits
+  if (!wait_bar(cx, &cx.S.tcbar[TB_B1], 0, PH_GEMM1)) w.ok = false;
   if (w.b1) {
-    // the operand copy has landed before the top of the buffer is used again (GEMM2),
-    // or the block exits, whatever failed
     for (uint32_t it = 0; it < (1u << 24) && !mbar_try_wait(&cx.S.tcbar[TB_B1], 0); ++it) {
     }
   }
