@@ -227,7 +227,7 @@ msm_status msm_verify_step_host(msm_model* model, const void* hidden_in_host,
  * shared by every model on that device.  A step needs
  *   2 * (exchange buffers + 256 bytes of phase counters) + attention/expert
  *   partials + 2 * (16 n_q_heads head_dim * 2) + 2 * (16 d_model * 2) bytes
- * (each part rounded up to 256 bytes), about 8.2 MiB at d_model 4096, 32/8
+ * (each part rounded up to 256 bytes), about 8.4 MiB at d_model 4096, 32/8
  * heads of 128, pool_dim 2048, ffn_dim 1024, top-8 on 152 SMs; the exact
  * figure of a model is msm_stats.noalloc_scratch_bytes.  A model whose step
  * needs more is rejected with MSM_ERR_UNSUPPORTED and a message giving both
