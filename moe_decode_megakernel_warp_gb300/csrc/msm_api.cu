@@ -63,7 +63,7 @@ struct msm_model {
   Dims dm{};
   std::vector<uint8_t> global;
   int G = 0, ring_bytes = 0, act_bytes = 0, smem_bytes = 0;
-  int g1_b_off = 0, g2_off = 0, ring_ext = 0;
+  int g1_b_off = 0, g2_off = 0, ring_ext = 0, unpool_act_off = 0, unpool_ext = 0;
   std::vector<LayerPack> L;
   uint8_t* lm = nullptr;
   uint16_t* g_final = nullptr;
@@ -313,6 +313,11 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   m->g1_b_off = (int)(act - ((g1_need + 1023) & ~uint64_t(1023)));
   m->g2_off = (int)(act - ((g2_need + 1023) & ~uint64_t(1023)));
   m->ring_ext = (int)((act - expert_top) & ~uint64_t(1023));
+  // the unpooler stages its [16][pool_dim] input at the top; its tiles may use the rest
+  // of the bottom, up to the expert phases' extension (so that no tile ever lands on
+  // GEMM1's operand, which a block may still read while its loader is past GEMM2)
+  m->unpool_act_off = (int)(act - (((uint64_t)dm.p * 32 + 1023) & ~uint64_t(1023)));
+  m->unpool_ext = std::min(m->ring_ext, m->unpool_act_off);
   m->smem_bytes = (int)(ring + act + kSmallBytes);
 
   auto bail = [&](msm_status s2) {
@@ -574,6 +579,8 @@ msm_status enqueue_verify(msm_model* m, const StepBuffers& B, const void* hidden
   P.g1_b_off = m->g1_b_off;
   P.g2_off = m->g2_off;
   P.ring_ext = m->ring_ext;
+  P.unpool_act_off = m->unpool_act_off;
+  P.unpool_ext = m->unpool_ext;
   P.flags = m->cfg.flags;
   P.timeout_ns_lo = (uint32_t)tmo;
   P.timeout_ns_hi = (uint32_t)(tmo >> 32);

@@ -178,6 +178,9 @@ struct LaunchParams {
   // the end of routing to the unpooler the weight ring may grow by ring_ext bytes into
   // the bottom of it
   int g1_b_off, g2_off, ring_ext;
+  // the unpooler's activation sits at this offset (the top of the buffer), and its
+  // weight tiles may take unpool_ext bytes of the bottom
+  int unpool_act_off, unpool_ext;
   uint32_t flags;
   uint32_t timeout_ns_lo, timeout_ns_hi;
   int prefetch_experts;

@@ -450,7 +450,8 @@ __device__ __noinline__ void ra_pump(RunAhead* ra, uint32_t bytes) {
 enum : int { TS_TILE = 0, TS_KV = 1, TS_DEP_WAIT = 2, TS_ROUTE_WAIT = 3, TS_END = 4 };
 struct TileStream {
   int seg;
-  int lo, hi, u;     // units of the segment; u: unit of the next tile
+  int lo, hi, u;     // units of the segment; u: unit of the next tile (dense: of its pair)
+  int half;          // dense: the next tile is of unit u + half (units go in pairs, tiles alternating)
   int k0, steps;     // dense: next k-step within unit u; k-steps per unit
   int upe;           // experts: units per expert
   uint64_t ub;       // bytes per unit
@@ -462,6 +463,7 @@ struct TileStream {
   __device__ void dense(const uint8_t* w, int K, int N, int rot) {
     unit_range(N / 16, rot_block(blockIdx.x, rot, gridDim.x), gridDim.x, lo, hi);
     u = lo;
+    half = 0;
     k0 = 0;
     steps = K / 16;
     ub = dense_unit_bytes(K);
@@ -501,18 +503,26 @@ struct TileStream {
           }
           return TS_TILE;
         }
-        const int ns = min(kDenseTileSteps, steps - k0);
-        src = W + (uint64_t)u * ub + (uint64_t)k0 * kKStepBytes;
+        // dense: the block's units in pairs (u, u + 1), their tiles alternating, so the two
+        // compute warp groups (one unit each) stream side by side
+        const int uu = u + half, ns = min(kDenseTileSteps, steps - k0);
+        t_u = uu;
+        src = W + (uint64_t)uu * ub + (uint64_t)k0 * kKStepBytes;
         bytes = (uint32_t)ns * kKStepBytes;
-        k0 += kDenseTileSteps;
-        if (k0 >= steps) {
-          k0 = 0;
-          ++u;
+        if (half == 0 && u + 1 < hi) {
+          half = 1;
+        } else {
+          half = 0;
+          k0 += kDenseTileSteps;
+          if (k0 >= steps) {
+            k0 = 0;
+            u += 2;
+          }
         }
         return TS_TILE;
       }
       ++seg;
-      lo = hi = u = k0 = 0;
+      lo = hi = u = k0 = half = 0;
       switch (seg) {
         case 1: {
           const AttnUnit au = attn_unit(P, cx.pos0, rot_block(cx.block, P.phase_rot * 2, gridDim.x), P.is_global);
@@ -559,7 +569,7 @@ __device__ void loader(Ctx& cx) {
   r.ra_on = P.runahead_bytes != 0;
   TileStream ts;
   ts.seg = 0;
-  ts.lo = ts.hi = ts.u = ts.k0 = 0;
+  ts.lo = ts.hi = ts.u = ts.k0 = ts.half = 0;
   // segment 0: the prologue QKV (launch 0); weights and KV rows do not depend on the
   // previous launch, so they stream before the dependency wait
   if (P.first) ts.dense(P.w_qkv_pro, dm.d, dm.nqkv, P.phase_rot * 1);
@@ -588,14 +598,16 @@ __device__ void loader(Ctx& cx) {
       if (ok && r.ra_on) ra_back(P, r.ra, cx.block, *cx.S.n_active);
       continue;
     }
-    // the expert tiles may also use the bottom of the activation buffer once routing has
-    // moved the pooled vectors out of it; the unpooler's tiles may not (its activation
-    // is staged there)
+    // the expert tiles may also use the bottom of the activation buffer once routing is
+    // done with the pooled vectors staged there, and so may the unpooler's tiles (its
+    // activation is staged at the top); the next layer's QKV tiles may not
     if (ts.seg == 7 || ts.seg == 8) {
       if (r.cap == (uint32_t)P.ring_bytes && P.ring_ext > 0 && mbar_try_wait(&cx.S.tcbar[TB_ROUTED], 0)) {
         r.cap = (uint32_t)(P.ring_bytes + P.ring_ext);
         stamp_any(P, EV_LD_RING_GROWN);
       }
+    } else if (ts.seg == 9) {
+      r.cap = (uint32_t)(P.ring_bytes + P.unpool_ext);
     } else {
       r.cap = (uint32_t)P.ring_bytes;
     }
@@ -630,7 +642,7 @@ __device__ void loader(Ctx& cx) {
       if (ts.seg == 3) {
         if (ts.t_u == ts.lo && ts.t_k0 == 0) stamp<kTiming>(P, cx.block, EV_LD_OP_FIRST);
         if (ts.t_u == ts.lo + 1 && ts.t_k0 == 0) stamp<kTiming>(P, cx.block, EV_LD_OP_U1);
-        if (ts.u == ts.hi) stamp<kTiming>(P, cx.block, EV_LD_OP_LAST);
+        if (ts.u >= ts.hi) stamp<kTiming>(P, cx.block, EV_LD_OP_LAST);
       } else if (ts.seg == 7) {
         if (ts.t_u == ts.lo && ts.t_k0 == 0) stamp<kTiming>(P, cx.block, EV_LD_G1_FIRST);
         if (ts.u == ts.hi) g1_last = ts.t_u;
@@ -726,8 +738,9 @@ __device__ __forceinline__ uint32_t act_off(int t, int k) { return act_chunk(t, 
 // applying RMSNorm with `gain`.  cnt >= 0: wait for every block to publish that
 // phase counter first; else, with `poll`, poll each chunk's sentinels; else plain loads.
 __device__ bool stage_act(Worker& w, const uint16_t* src, int K, int cnt, bool poll, const uint16_t* gain,
-                                       float eps, int phase, int map = -1) {
+                                       float eps, int phase, int map = -1, uint32_t aoff = 0) {
   Ctx& cx = *w.cx;
+  uint8_t* const act = cx.S.act + aoff;  // where the activation goes in the buffer (1 KB aligned)
   const int tid = w.cw * 32 + w.lane;
   const int t = tid >> 4, sub = tid & 15;
   const int nch = K / 8;
@@ -755,7 +768,7 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, int cnt, bool p
       const int nblk = K / 64, nb = cx.P->act_box[map];
       mbar_expect_tx(cx.S.stage_bar, (uint32_t)K * 32u);
       for (int z = 0; z < nblk; z += nb)
-        tma_load_3d(cx.S.act + (size_t)z * kActBlockBytes, &cx.P->tmap_act[map], 0, 0, z, cx.S.stage_bar);
+        tma_load_3d(act + (size_t)z * kActBlockBytes, &cx.P->tmap_act[map], 0, 0, z, cx.S.stage_bar);
     }
     const uint32_t par = cx.stage_n & 1u;
     ++cx.stage_n;
@@ -770,7 +783,7 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, int cnt, bool p
       // the row's sum of squares in the order of the load path below (bitwise the same)
 #pragma unroll 4
       for (int c = sub; c < nch; c += 16) {
-        const uint4 v = *reinterpret_cast<const uint4*>(cx.S.act + act_off(t, c * 8));
+        const uint4 v = *reinterpret_cast<const uint4*>(act + act_off(t, c * 8));
         const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -815,7 +828,7 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, int cnt, bool p
         const float2 x2 = make_float2(__uint_as_float(wd[i] << 16), __uint_as_float(wd[i] & 0xFFFF0000u));
         ss2 = __ffma2_rn(x2, x2, ss2);
       }
-      *reinterpret_cast<uint4*>(cx.S.act + act_off(t, c * 8)) = v[j];
+      *reinterpret_cast<uint4*>(act + act_off(t, c * 8)) = v[j];
     }
   }
   }
@@ -851,7 +864,7 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, int cnt, bool p
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             off[q] = act_off(r0 + q, c * 8);
-            v[q] = *reinterpret_cast<const uint4*>(cx.S.act + off[q]);
+            v[q] = *reinterpret_cast<const uint4*>(act + off[q]);
             iv[q] = inv_s[r0 + q];
           }
 #pragma unroll
@@ -867,7 +880,7 @@ __device__ bool stage_act(Worker& w, const uint16_t* src, int K, int cnt, bool p
               const __nv_bfloat162 h = __floats2bfloat162_rn(y.x, y.y);
               wd[i] = *reinterpret_cast<const uint32_t*>(&h);
             }
-            *reinterpret_cast<uint4*>(cx.S.act + off[q]) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+            *reinterpret_cast<uint4*>(act + off[q]) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
           }
         }
       }
@@ -988,24 +1001,25 @@ __device__ void dense_epi(const LaunchParams& P, const Smem& S, const EpiArgs& e
 }
 
 // Dense phase: out[16 tokens][N] = act[16][K] . W[N][K]^T over this block's
-// 16-row units.  Every tile (32 k-steps of one unit) is shared by the 8 compute
-// warps, warp w taking k-steps 4w..4w+3, so no warp carries a long dependent
-// MMA chain; each unit ends with a cross-warp sum in fixed warp order (the result
-// does not depend on the grid size) and an epilogue over (row pair, token):
-// dense_epi(unit, p, t, row p value, row p+8 value), run by 128 threads.
+// 16-row units.  The two warp groups take alternate units (unit lo + i by group i & 1),
+// so one group's cross-warp sum and epilogue overlap the other group's MMAs on the
+// next unit.  Inside a group, warp wi takes k-steps 16 wi .. 16 wi + 15 of every tile
+// of the unit, so no warp carries a long dependent MMA chain; each unit ends with the
+// sum of the group's four partials in fixed warp order (the result does not depend on
+// the grid size or the group) and an epilogue over (row pair, token):
+// dense_epi(unit, p, t, row p value, row p+8 value), run by the group's 128 threads.
 __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, const EpiArgs& ea,
-                                         int trace) {
+                                         int trace, uint32_t aoff = 0) {
   Ctx& cx = *w.cx;
   const int G = gridDim.x;
   int lo, hi;
   unit_range(N / 16, rot_block(cx.block, rot, G), G, lo, hi);
   const int steps = K / 16;
   const int ktiles = (steps + kDenseTileSteps - 1) / kDenseTileSteps;
-  // The compute warps form two groups of four; group g consumes the unit's tiles
-  // kt = g, g + 2, ... and warp wi of a group takes k-steps 8 wi .. 8 wi + 7 of a tile,
-  // so two tiles are consumed at a time (a tile held by all eight warps at once would
-  // be released only after one warp's whole dependent MMA chain).  k-step & 3 is the
-  // loop index & 3.
+  // The compute warps form two groups of four; group g takes the units lo + g, lo + g + 2,
+  // ... and warp wi of the group k-steps 16 wi .. 16 wi + 15 of each of their tiles (a
+  // tile held by all eight warps at once would be released only after one warp's whole
+  // dependent MMA chain).  k-step & 3 is the loop index & 3.
   const int group = w.cw >> 2, wi = w.cw & 3;
   constexpr int kStepsPerWarp = kDenseTileSteps / 4;
   // lane l addresses row l & 7 of matrix m = l >> 3 (tokens 8 (m >> 1) .., columns
@@ -1014,39 +1028,42 @@ __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, 
 #pragma unroll
   for (int ii = 0; ii < 4; ++ii) {
     const int m = w.lane >> 3, t = (m >> 1) * 8 + (w.lane & 7);
-    act_lane[ii] = smem_u32(cx.S.act) + act_chunk(t, ii * 2 + (m & 1));
+    act_lane[ii] = smem_u32(cx.S.act + aoff) + act_chunk(t, ii * 2 + (m & 1));
   }
   float* red = cx.S.dred;  // [8 warps][16 rows][16 tokens]
-  const int tid = w.cw * 32 + w.lane;
+  const int tig = wi * 32 + w.lane;  // thread in group
   const int ks_lo = wi * kStepsPerWarp;
   // the residual inputs of the o_proj / unpooler epilogues do not depend on this phase:
-  // read them for the block's first units now, while the tiles stream in
-  constexpr int kPreUnits = 4;
+  // read them for the group's first units now, while the tiles stream in
+  constexpr int kPreUnits = 2;
   uint32_t pre[kPreUnits];
-  const bool pre_res = (ea.kind == EPI_OPROJ || ea.kind == EPI_UNPOOL) && tid < 128;
+  const bool pre_res = ea.kind == EPI_OPROJ || ea.kind == EPI_UNPOOL;
   if (pre_res) {
-    const int d = cx.P->dm.d, p = tid >> 4, tok = tid & 15;
+    const int d = cx.P->dm.d, p = tig >> 4, tok = tig & 15;
 #pragma unroll
     for (int i = 0; i < kPreUnits; ++i) {
       pre[i] = 0u;
-      if (lo + i < hi) {
-        const uint16_t* r = ea.res + (size_t)tok * d + (lo + i) * 16 + p;
+      const int u = lo + group + 2 * i;
+      if (u < hi) {
+        const uint16_t* r = ea.res + (size_t)tok * d + u * 16 + p;
         const uint32_t a = ea.kind == EPI_OPROJ ? r[0] : ld_relaxed_u16(r);
         const uint32_t b = ea.kind == EPI_OPROJ ? r[8] : ld_relaxed_u16(r + 8);
         pre[i] = a | (b << 16);
       }
     }
   }
-  for (int u = lo; u < hi; ++u) {
+  for (int u = lo + group; u < hi; u += 2) {
     const int loc = u - lo;
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // odd k-steps
-    for (int kt = group; kt < ktiles; kt += 2) {
-      const uint32_t t = w.ti + (uint32_t)(loc * ktiles + kt);
+    // the loader streams the units in pairs, their tiles alternating
+    const bool paired = (loc | 1) < hi - lo;
+    const uint32_t t0 = w.ti + (uint32_t)((loc >> 1) * 2 * ktiles + (paired ? (loc & 1) : 0));
+    for (int kt = 0; kt < ktiles; ++kt) {
+      const uint32_t t = t0 + (uint32_t)(paired ? 2 * kt : kt);
       const uint32_t s = t % kSlots;
       if (w.ok) w.ok = wait_tile(cx, t, 50);
-      if (trace >= 0 && loc < 2 && (kt == group || kt + 2 >= ktiles))
-        stamp_rt(*cx.P, trace + loc * 4 + (kt == group ? 0 : 1));
+      if (trace >= 0 && loc < 2 && tig == 0 && (kt == 0 || kt + 1 == ktiles)) stamp_any(*cx.P, trace + loc * 4 + (kt == 0 ? 0 : 1));
       if (w.ok) {
         const uint32_t wbase = smem_u32(cx.S.ring + cx.S.slot_off[s]) + lane_mat_off(w.lane);
         const int k0 = kt * kDenseTileSteps;
@@ -1079,26 +1096,28 @@ __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, 
         const int row = w.g + ((i >> 1) << 3), tok = nt * 8 + 2 * w.q + (i & 1);
         red[(w.cw * 16 + row) * 16 + tok] = acc[nt][i];
       }
-    if (trace >= 0 && loc < 2) stamp_rt(*cx.P, trace + loc * 4 + 2);
-    cbar();
-    if (tid < 128 && w.ok) {
-      const int p = tid >> 4, tok = tid & 15;
+    if (trace >= 0 && loc < 2 && tig == 0) stamp_any(*cx.P, trace + loc * 4 + 2);
+    named_bar(2 + group, 128);
+    if (w.ok) {
+      const int p = tig >> 4, tok = tig & 15;
       float vlo = 0.f, vhi = 0.f;
 #pragma unroll
-      for (int ww = 0; ww < kComputeWarps; ++ww) {
+      for (int ww = 4 * group; ww < 4 * group + 4; ++ww) {
         vlo += red[(ww * 16 + p) * 16 + tok];
         vhi += red[(ww * 16 + p + 8) * 16 + tok];
       }
       uint32_t r2 = 0u;
 #pragma unroll
       for (int i = 0; i < kPreUnits; ++i)
-        if (loc == i) r2 = pre[i];
-      dense_epi(*cx.P, cx.S, ea, u, p, tok, vlo, vhi, pre_res && loc < kPreUnits, r2);
+        if (loc == group + 2 * i) r2 = pre[i];
+      dense_epi(*cx.P, cx.S, ea, u, p, tok, vlo, vhi, pre_res && loc < group + 2 * kPreUnits, r2);
     }
-    cbar();
-    if (trace >= 0 && loc < 2) stamp_rt(*cx.P, trace + loc * 4 + 3);
+    named_bar(2 + group, 128);  // the group's partial sums may be overwritten
+    if (trace >= 0 && loc < 2 && tig == 0) stamp_any(*cx.P, trace + loc * 4 + 3);
     if (*cx.S.abort) w.ok = false;
   }
+  // both groups' epilogues are stored before the phase is published
+  cbar();
   w.ti += (uint32_t)((hi - lo) * ktiles);
 }
 
@@ -2337,14 +2356,15 @@ __device__ void compute_main(Worker& w) {
     const uint16_t* h1 = reinterpret_cast<const uint16_t*>(X + P.xo.h1);
     uint16_t* h2 = reinterpret_cast<uint16_t*>(X + P.xo.h2);
     uint16_t* hnext = P.last ? P.hidden_out : P.out_h;
-    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.z), dm.p, CNT_COMBINE, false, nullptr, 0.f, PH_UNPOOL, ACT_Z);
+    stage_act(w, reinterpret_cast<const uint16_t*>(X + P.xo.z), dm.p, CNT_COMBINE, false, nullptr, 0.f, PH_UNPOOL, ACT_Z,
+              (uint32_t)P.unpool_act_off);
     stamp<kTiming>(P, b, EV_UNPOOL_IN);
     EpiArgs ea{};
     ea.kind = EPI_UNPOOL;
     ea.res = h1;
     ea.out = h2;
     ea.out2 = hnext;
-    dense_phase(w, dm.p, dm.d, P.phase_rot * 8, ea, -1);
+    dense_phase(w, dm.p, dm.d, P.phase_rot * 8, ea, -1, (uint32_t)P.unpool_act_off);
     publish(w, CNT_UNPOOL);
     stamp<kTiming>(P, b, EV_UNPOOL_DONE);
   }
