@@ -57,10 +57,10 @@ def step_bytes(cfg, distinct_per_layer, pos0):
 # ----------------------------------------------------------------- DRAM traffic
 # dram__bytes_read.sum + dram__bytes_write.sum of one layer launch, as a multiple of
 # that launch's algorithmic bytes, from an ncu capture of the kernel source whose
-# hash is given (one full-width SWA-2048 layer: 305.8 MB of traffic for 300.4 MB).
+# hash is given (one full-width SWA-2048 layer: 305.6 MB of traffic for 300.4 MB).
 # Reported only while the kernel source is unchanged; any edit makes it null.
-TRAFFIC_RATIO = {"kernel_sha256": "ea83b1531ec4fc69d66106545a5c5a1d3f68a3b801b91ca3ed1a9c643f5c7fbb", "ratio": 1.018,
-                 "capture": "profiles/layer_kernel_cfg2_one_layer_sections.md"}
+TRAFFIC_RATIO = {"kernel_sha256": "52f98908da9243efb0470cfd0df55eae54c282c49ef34c262df74e2bd4be9d8f", "ratio": 1.017,
+                 "capture": "profiles/layer_kernel_cfg2_expert_prefetch_l2.md (prefetch off)"}
 
 
 def kernel_sha256():
