@@ -389,6 +389,116 @@ def measure_accept(model, cfg, hidden, parent, kc, vc, logits, stream, steps):
                     "replayed as one CUDA graph that reads the tree, tokens and pos0 from a device state"}
 
 
+# ----------------------------------------------------------------- 20-step loop
+# The decode loop of the pages' measurement, verify half (the draft model's CUDA path
+# is not built): 20 consecutive steps of the 62-layer workload whose hidden-state
+# inputs are correlated step to step, h_s = rho h_(s-1) + sqrt(1 - rho^2) n_s, so that
+# routing carries over from step to step (the pages: each token keeps about 80 % of
+# its experts); the previous-step expert prefetch is timed off and on.  rho was chosen
+# on the GPU for about 80 % per-token persistence of the top-8 sets (all layers).
+LOOP_STEPS = 20
+LOOP_RHO = 0.95
+
+
+def bf16_bits(x):
+    """fp64 -> bf16 bit patterns, round to nearest even (inputs only)."""
+    b = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def loop_inputs(cfg, seed, rho, n=LOOP_STEPS):
+    h = synth.bf16_to_f32(synth.hidden_in(cfg, seed, 0)).astype(np.float64)
+    out = [bf16_bits(h)]
+    for s in range(1, n):
+        nz = synth.bf16_to_f32(synth.hidden_in(cfg, seed, s)).astype(np.float64)
+        h = rho * h + np.sqrt(1.0 - rho * rho) * nz
+        out.append(bf16_bits(h))
+    return out
+
+
+def routing_persistence(routes, k):
+    """Mean share of a token's top-k experts that it kept from the previous step."""
+    kept = []
+    for a, b in zip(routes, routes[1:]):
+        for l in range(a.shape[0]):
+            for t in range(a.shape[1]):
+                kept.append(len(set(a[l, t].tolist()) & set(b[l, t].tolist())) / k)
+    return float(np.mean(kept)) if kept else 0.0
+
+
+def prefetch_misses(routes, e, n_top=14):
+    """Per step and layer: experts among the previous step's n_top most-used that the
+    step does not use (the prefetch's wasted experts), mean over steps >= 1 and layers."""
+    miss = []
+    for a, b in zip(routes, routes[1:]):
+        for l in range(a.shape[0]):
+            cnt = np.bincount(a[l].reshape(-1), minlength=e)
+            order = sorted(range(e), key=lambda x: (-cnt[x], x))
+            top = [x for x in order[:n_top] if cnt[x] > 0]
+            used = set(b[l].reshape(-1).tolist())
+            miss.append(sum(1 for x in top if x not in used))
+    return float(np.mean(miss)) if miss else 0.0
+
+
+def run_loop(args):
+    import torch
+    import moe_decode_megakernel_warp_gb300 as msm
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    cfg = synth.CONFIGS["cfg4"]
+    seeds = synth.parity_seeds("cfg4")
+    seed, bias = seeds["seed"], seeds["bias_seeds"]
+    rho = args.loop_rho
+    hid = [torch.from_numpy(h.view(np.int16)).to(dev) for h in loop_inputs(cfg, seed, rho)]
+    parent = synth.parent_array(seed)
+    logits = torch.empty((T, cfg.vocab), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    res, routes = {}, None
+    for pf in (False, True):
+        flags = msm.MSM_FLAG_PDL | (msm.MSM_FLAG_EXPERT_PREFETCH if pf else 0)
+        model = build_model(cfg, seed, bias, dev, 0, flags)
+        kv = [synth.gpu_kv_history(cfg, seed, l, device=dev) for l in range(cfg.n_layers)]
+        kc, vc = [k for k, _ in kv], [v for _, v in kv]
+        rec = []
+        for s in range(LOOP_STEPS):  # untimed pass: warm-up, and each step's routing
+            model.verify_step(hid[s], parent, cfg.pos0, kc, vc, logits_out=logits, stream=sptr)
+            if model.sync(sptr) != 0:
+                raise SystemExit("loop step failed: %s" % msm.msm_last_error())
+            rec.append(model.routing()[0].copy())
+        routes = routes or rec
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(LOOP_STEPS + 1)]
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for s in range(LOOP_STEPS):
+            model.verify_step(hid[s], parent, cfg.pos0, kc, vc, logits_out=logits, stream=sptr)
+            ev[s + 1].record(stream)
+        torch.cuda.synchronize()
+        if model.sync(sptr) != 0:
+            raise SystemExit("loop steps failed: %s" % msm.msm_last_error())
+        res[pf] = [ev[i].elapsed_time(ev[i + 1]) for i in range(LOOP_STEPS)]
+        model.close()
+        del kv, kc, vc
+        torch.cuda.empty_cache()
+    expert_mb = (layer_bytes(cfg, 0, 1, cfg.pos0) - layer_bytes(cfg, 0, 0, cfg.pos0)) / 1e6
+    miss = prefetch_misses(routes, cfg.e)
+    line = {
+        "metric": "verify-step ms, 20-step loop with correlated routing", "unit": "ms", "higher_is_better": False,
+        "value": statistics.median(res[False]), "n_gpus": 1, "steps": LOOP_STEPS, "dtype": "nvfp4+bf16",
+        "data": "synthetic (seeded; consecutive hidden inputs correlated, rho %.3f)" % rho,
+        "config": {"workload": "20 consecutive verify steps of the 62-layer workload (draft model not built)"},
+        "routing_persistence": routing_persistence(routes, cfg.k),
+        "distinct_experts_per_layer": float(np.mean([len(np.unique(r[l])) for r in routes for l in range(cfg.n_layers)])),
+        "expert_prefetch": {
+            "off_ms_median": statistics.median(res[False]), "on_ms_median": statistics.median(res[True]),
+            "off_ms_mean": statistics.mean(res[False]), "on_ms_mean": statistics.mean(res[True]),
+            "top": 14, "mispredicted_experts_per_layer": miss,
+            "mispredicted_mb_per_step": miss * expert_mb * cfg.n_layers,
+        },
+    }
+    print(json.dumps(line))
+
+
 def run_ours(args):
     import torch
     import moe_decode_megakernel_warp_gb300 as msm
@@ -560,6 +670,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="cfg4", choices=sorted(synth.CONFIGS))
     ap.add_argument("--expert-prefetch", action="store_true")
     ap.add_argument("--kv-prefetch", action="store_true")
+    ap.add_argument("--loop", action="store_true",
+                    help="the 20-step loop with correlated routing, expert prefetch off and on (one JSON line)")
+    ap.add_argument("--loop-rho", type=float, default=LOOP_RHO)
     ap.add_argument("--l2-runahead-kb", type=int, default=0,
                     help="L2 prefetch distance of each block's stream in KiB (0 = off)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -569,6 +682,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.loop:
+        return run_loop(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
