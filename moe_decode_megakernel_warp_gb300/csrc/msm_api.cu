@@ -63,7 +63,7 @@ struct msm_model {
   Dims dm{};
   std::vector<uint8_t> global;
   int G = 0, ring_bytes = 0, act_bytes = 0, smem_bytes = 0;
-  int g1_b_off = 0, g2_off = 0, ring_ext = 0, unpool_act_off = 0, unpool_ext = 0;
+  int g1_b_off = 0, g2_off = 0, ring_ext = 0, unpool_act_off = 0, unpool_ext = 0, sfb_ext = 0;
   std::vector<LayerPack> L;
   uint8_t* lm = nullptr;
   uint16_t* g_final = nullptr;
@@ -318,6 +318,9 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   // GEMM1's operand, which a block may still read while its loader is past GEMM2)
   m->unpool_act_off = (int)(act - (((uint64_t)dm.p * 32 + 1023) & ~uint64_t(1023)));
   m->unpool_ext = std::min(m->ring_ext, m->unpool_act_off);
+  // GEMM1's operand-B scales are the bottom of its operand: when the operand is what sets
+  // the top of the expert phases, the ring may grow over them once they are copied
+  m->sfb_ext = (m->g1_b_off == m->ring_ext) ? (int)b1_sfb_bytes(dm.p) : 0;
   m->smem_bytes = (int)(ring + act + kSmallBytes);
 
   auto bail = [&](msm_status s2) {
@@ -579,6 +582,7 @@ msm_status enqueue_verify(msm_model* m, const StepBuffers& B, const void* hidden
   P.g1_b_off = m->g1_b_off;
   P.g2_off = m->g2_off;
   P.ring_ext = m->ring_ext;
+  P.sfb_ext = m->sfb_ext;
   P.unpool_act_off = m->unpool_act_off;
   P.unpool_ext = m->unpool_ext;
   P.flags = m->cfg.flags;

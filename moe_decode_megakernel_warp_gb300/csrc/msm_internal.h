@@ -178,6 +178,7 @@ struct LaunchParams {
   // the end of routing to the unpooler the weight ring may grow by ring_ext bytes into
   // the bottom of it
   int g1_b_off, g2_off, ring_ext;
+  int sfb_ext;  // bytes the expert ring may grow by once GEMM1's operand-B scales are in tensor memory
   // the unpooler's activation sits at this offset (the top of the buffer), and its
   // weight tiles may take unpool_ext bytes of the bottom
   int unpool_act_off, unpool_ext;
@@ -211,15 +212,17 @@ __host__ __device__ inline uint64_t exp_unit_bytes(int K) { return (uint64_t)(K 
 __host__ __device__ inline int w1_units(int f) { return f / 64; }
 __host__ __device__ inline int w2_units(int p) { return p / kExpTileRows; }
 // GEMM1 operand B: the 16 pooled vectors, each as the sum of kSplitTerms NVFP4 terms,
-// one B row per (term, token) pair, row n = term * 16 + token: p / 256 column blocks of
-// 64 rows x 128 code bytes (128-byte swizzle, 8 KB each), then p / 64 scale groups of
-// 512 bytes, one per K=64 step, for the tensor-memory copy (32 lines of 16 bytes; line l:
-// the scale words of rows l and l + 32, two zero words), then the 16 tokens' fp32 row
-// scales (256 bytes)
+// one B row per (term, token) pair, row n = term * 16 + token: first p / 64 scale groups
+// of 512 bytes, one per K=64 step, for the tensor-memory copy (32 lines of 16 bytes; line
+// l: the scale words of rows l and l + 32, two zero words) -- the part a block no longer
+// needs once they are copied; then p / 256 column blocks of 64 rows x 128 code bytes
+// (128-byte swizzle, 8 KB each, 1 KB aligned); then the 16 tokens' fp32 row scales
 constexpr int kSplitTerms = 4;
 constexpr int kSplitRows = kSplitTerms * T;
+__host__ __device__ inline uint64_t b1_sfb_bytes(int p) { return (uint64_t)p / 64 * 512; }
+__host__ __device__ inline uint64_t b1_code_off(int p) { return b1_sfb_bytes(p); }
 __host__ __device__ inline uint64_t b1_code_bytes(int p) { return (uint64_t)p / 256 * kSplitRows * 128; }
-__host__ __device__ inline uint64_t b1_ts_off(int p) { return b1_code_bytes(p) + (uint64_t)p / 64 * 512; }
+__host__ __device__ inline uint64_t b1_ts_off(int p) { return b1_code_off(p) + b1_code_bytes(p); }
 __host__ __device__ inline uint64_t b1_bytes(int p) { return b1_ts_off(p) + 256; }
 
 // kernel entry points (defined in msm_kernel.cu / msm_pack.cu)

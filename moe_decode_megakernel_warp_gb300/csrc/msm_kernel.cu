@@ -77,7 +77,8 @@ enum TcBar : int {
   TB_ROUTED = 15,    // the block's routing (expert list, first expert tile) is in shared memory
   TB_B1 = 16,        // GEMM1's operand B has landed in the activation buffer (transaction count)
   TB_SFA_FULL = 17,  // [4] a tile's weight scales are in a scale buffer (4 warps)
-  TB_SLOT = 21,      // [kSlots] the MMAs of the expert tile in a ring slot are done (commit):
+  TB_SFB1 = 21,      // GEMM1's operand-B scales are in tensor memory (commit)
+  TB_SLOT = 22,      // [kSlots] the MMAs of the expert tile in a ring slot are done (commit):
                      // the loader's release of expert tiles (one commit, where the other
                      // tiles' consumers arrive on the slot's `empty` barrier eight times)
   kTcBars = TB_SLOT + kSlots
@@ -337,6 +338,8 @@ struct Ring {
   uint32_t tail_off;  // start of the oldest outstanding tile (tail < issued)
   bool wrapped;       // the outstanding tiles run to the top and continue at 0
   bool ra_on;         // L2 run-ahead enabled
+  bool routed;        // the block's routing is done: expert tiles may use the bottom of the activation buffer
+  bool sfb_free;      // ... and GEMM1's operand-B scale groups above it
   RunAhead* ra;       // L2 run-ahead state (shared memory)
 };
 static_assert(kRingStateOff + sizeof(RunAhead) <= 7416, "run-ahead state overlaps the tensor-core barriers");
@@ -562,6 +565,7 @@ __device__ void loader(Ctx& cx) {
   Ring r;
   r.cap = (uint32_t)P.ring_bytes;
   r.xmask = r.par_e = r.par_x = 0u;
+  r.routed = r.sfb_free = false;
   r.issued = r.tail = r.head = r.tail_off = 0;
   r.wrapped = false;
   r.ra = cx.S.ring_state;
@@ -601,15 +605,22 @@ __device__ void loader(Ctx& cx) {
     // the expert tiles may also use the bottom of the activation buffer once routing is
     // done with the pooled vectors staged there, and so may the unpooler's tiles (its
     // activation is staged at the top); the next layer's QKV tiles may not
+    // (set for every tile from the tile's own segment: a block may have no tiles at all in
+    // the segments between two that grow the ring)
+    r.cap = (uint32_t)P.ring_bytes;
     if (ts.seg == 7 || ts.seg == 8) {
-      if (r.cap == (uint32_t)P.ring_bytes && P.ring_ext > 0 && mbar_try_wait(&cx.S.tcbar[TB_ROUTED], 0)) {
-        r.cap = (uint32_t)(P.ring_bytes + P.ring_ext);
+      if (!r.routed && P.ring_ext > 0 && mbar_try_wait(&cx.S.tcbar[TB_ROUTED], 0)) {
+        r.routed = true;
         stamp_any(P, EV_LD_RING_GROWN);
       }
+      if (r.routed) {
+        r.cap += (uint32_t)P.ring_ext;
+        // GEMM1's operand-B scales sit right above the extension: free once copied
+        if (!r.sfb_free && P.sfb_ext > 0 && mbar_try_wait(&cx.S.tcbar[TB_SFB1], 0)) r.sfb_free = true;
+        if (r.sfb_free) r.cap += (uint32_t)P.sfb_ext;
+      }
     } else if (ts.seg == 9) {
-      r.cap = (uint32_t)(P.ring_bytes + P.unpool_ext);
-    } else {
-      r.cap = (uint32_t)P.ring_bytes;
+      r.cap += (uint32_t)P.unpool_ext;
     }
     const int g1i = ts.seg == 7 ? (ts.t_u - ts.lo) * ts.steps + ts.t_k0 : 99;
     if (g1i < 16) stamp_any(P, EV_LD_G1_NEXT + g1i);
@@ -1529,13 +1540,14 @@ __device__ void split_pooled(Worker& w) {
   if (!w.ok || *cx.S.abort) return;
   const int h = tid >> 4, i = tid & 15;
   const uint32_t hmask = 0xFFFFu << (w.lane & 16);  // this half-warp's lanes
-  uint8_t* img = P.x_cur + P.xo.b1;
-  uint8_t* sfimg = img + b1_code_bytes(p);
+  uint8_t* sfimg = P.x_cur + P.xo.b1;
+  uint8_t* img = sfimg + b1_code_off(p);
+  float* tsimg = reinterpret_cast<float*>(sfimg + b1_ts_off(p));
   for (int pr = lo + h; pr < hi; pr += 16) {
     const int t = pr / nb, c = pr % nb, k = c * 16 + i;
     float x = bf16_to_f32(*reinterpret_cast<const uint16_t*>(cx.S.act + act_off(t, k) + (k & 7) * 2));
     float ts = cx.S.x_ts[t];
-    if (c == 0 && i == 0) reinterpret_cast<float*>(img + b1_ts_off(p))[t] = ts;
+    if (c == 0 && i == 0) tsimg[t] = ts;
 #pragma unroll
     for (int j = 0; j < kSplitTerms; ++j, ts *= 0.25f) {
       float bmax = fabsf(x);
@@ -1835,9 +1847,8 @@ __device__ void stage_sfa(Worker& w, uint32_t n, uint32_t t, int K, int phase) {
   if (!ok) w.ok = false;
 }
 
-// GEMM1 on the compute side: the weight scales of tiles i = group, group + 2, ... and the
-// epilogues of units u = group, group + 2, ..., each epilogue once the group has reached
-// unit u + 2 (the tensor-core warp does the rest).
+// GEMM1 on the compute side: group 1 stages the weight scales of every tile, group 0 runs
+// the epilogue of every unit (the tensor-core warp does the rest).
 __device__ void gemm1_phase(Worker& w) {
   Ctx& cx = *w.cx;
   const LaunchParams& P = *cx.P;
@@ -1859,12 +1870,13 @@ __device__ void gemm1_phase(Worker& w) {
   const int wg = w.cw >> 2;
   const int ntiles = (hi - lo) * NT;
   if (hi > lo) stamp_rt(P, EV_G1_FIRST_READY);
-  int epi = wg;  // next unit whose epilogue this group runs
-  for (int i = wg; i < ntiles; i += 2) {
-    for (; epi <= i / NT - 2; epi += 2) g1_epilogue(w, lo, epi, tm);
-    stage_sfa(w, (uint32_t)i, w.ti + (uint32_t)i, dm.p, PH_GEMM1);
+  if (wg == 1) {
+    // group 1 puts every tile's weight scales in place as the tile lands (never held up
+    // by an epilogue), group 0 runs every unit's epilogue
+    for (int i = 0; i < ntiles; ++i) stage_sfa(w, (uint32_t)i, w.ti + (uint32_t)i, dm.p, PH_GEMM1);
+  } else {
+    for (int loc = 0; loc < hi - lo; ++loc) g1_epilogue(w, lo, loc, tm);
   }
-  for (; epi < hi - lo; epi += 2) g1_epilogue(w, lo, epi, tm);
   if (hi > lo) stamp_rt(P, EV_G1_LAST_DONE);
   w.ti += (uint32_t)ntiles;
   w.xseq = (uint32_t)ntiles;
@@ -2086,14 +2098,15 @@ __device__ void tc_issuer(Ctx& cx) {
       int lo, hi;
       unit_range(na * w1_units(dm.f), rot_block(cx.block, P.phase_rot * 6, G), G, lo, hi);
       t2 = t1 + (uint32_t)((hi - lo) * NT);
-      const uint32_t b_s = smem_u32(cx.S.act + P.g1_b_off);
+      const uint32_t sfb_s = smem_u32(cx.S.act + P.g1_b_off), b_s = sfb_s + (uint32_t)b1_code_off(dm.p);
       if (hi > lo) {
         ok = wait_bar(cx, &tb[TB_B1], 0, PH_GEMM1);
         if (ok) {
           stamp_any(P, EV_B1_LANDED);
           // the operand's scale groups -> tensor memory, one per K=64 step
           for (int s = 0; s < dm.p / 64; ++s)
-            tc_cp_32x128b_x4(tm + TM_SFB1 + 4 * s, sdesc_plain(b_s + (uint32_t)b1_code_bytes(dm.p) + 512 * s, 128));
+            tc_cp_32x128b_x4(tm + TM_SFB1 + 4 * s, sdesc_plain(sfb_s + 512 * s, 128));
+          tc_commit(&tb[TB_SFB1]);  // once copied, the scale groups' shared memory may take ring tiles
         }
       }
       for (int loc = 0; loc < hi - lo && ok; ++loc) {
