@@ -1548,14 +1548,17 @@ __device__ void split_pooled(Worker& w) {
     float x = bf16_to_f32(*reinterpret_cast<const uint16_t*>(cx.S.act + act_off(t, k) + (k & 7) * 2));
     float ts = cx.S.x_ts[t];
     if (c == 0 && i == 0) tsimg[t] = ts;
-#pragma unroll
-    for (int j = 0; j < kSplitTerms; ++j, ts *= 0.25f) {
+    // (a compact loop: this code runs once per launch, cold in the instruction cache;
+    // the quotients are the kernel's own choice of split, so reciprocals serve)
+    float inv6 = ts > 0.f ? __frcp_rn(6.0f * ts) : 0.f;
+#pragma unroll 1
+    for (int j = 0; j < kSplitTerms; ++j, ts *= 0.25f, inv6 *= 4.0f) {
       float bmax = fabsf(x);
 #pragma unroll
       for (int o = 8; o >= 1; o >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(hmask, bmax, o));
-      const uint32_t sc = ts > 0.f ? f32_to_e4m3(__fdiv_rn(bmax, 6.0f * ts)) : 0u;
+      const uint32_t sc = ts > 0.f ? f32_to_e4m3(bmax * inv6) : 0u;
       const float den = e4m3_to_f32(sc) * ts;
-      const float qx = sc != 0u ? __fdiv_rn(x, den) : 0.f;
+      const float qx = sc != 0u ? x * __frcp_rn(den) : 0.f;
       const float qn = __shfl_xor_sync(hmask, qx, 1);
       const uint32_t byte = (i & 1) ? f32x2_to_e2m1x2(qn, qx) : f32x2_to_e2m1x2(qx, qn);  // even element low
       const uint32_t h2 = e2m1x2_to_f16x2(byte);
