@@ -47,6 +47,16 @@ def layer_bytes(cfg, layer, n_distinct, pos0):
     return dense + experts + kv_read + kv_write
 
 
+def draft_step_bytes(dc, pos0):
+    """Algorithmic bytes of one draft step: every layer's dense weights (QKV, o_proj,
+    gate + up, down, two gains), its KV history read and the block's K/V rows written;
+    the LM head and the fp32 logits."""
+    hd = dc.heads * dc.hd
+    per_layer = 2 * (3 * hd * dc.d + dc.d * hd + 3 * dc.f * dc.d + 2 * dc.d) + \
+        (pos0 + T) * dc.heads * dc.hd * 2 * 2 + T * dc.heads * dc.hd * 2 * 2
+    return dc.n_layers * per_layer + dc.vocab * dc.d * 2 + 2 * dc.d + T * dc.vocab * 4
+
+
 def step_bytes(cfg, distinct_per_layer, pos0):
     tot = sum(layer_bytes(cfg, l, distinct_per_layer[l], pos0) for l in range(cfg.n_layers))
     if cfg.vocab:
@@ -499,6 +509,74 @@ def run_loop(args):
     print(json.dumps(line))
 
 
+def measure_draft(dev, steps, warmup):
+    """The draft step of the pages' 5-layer draft at full width (msm_draft_step: one
+    launch per layer, LM head in the last, then the argmax proposal), timed with CUDA
+    events on the launching stream; median of the steps."""
+    import torch
+    import moe_decode_megakernel_warp_gb300 as msm
+    dc = synth.DRAFT_FULL
+    seed = 11
+    layers = [synth.gpu_draft_layer_weights(dc, seed, l, device=dev) for l in range(dc.n_layers)]
+    final = synth.gpu_draft_final_weights(dc, seed, device=dev)
+    kv = [synth.gpu_draft_kv_history(dc, seed, l, device=dev) for l in range(dc.n_layers)]
+    torch.cuda.synchronize()
+    model = msm.Model(dc, layers, final, device=dev.index or 0, flags=msm.MSM_FLAG_PDL | msm.MSM_FLAG_DRAFT)
+    del layers, final
+    torch.cuda.empty_cache()
+    kc, vc = [k for k, _ in kv], [v for _, v in kv]
+    hid = torch.from_numpy(synth.draft_hidden_in(dc, seed).view(np.int16)).to(dev)
+    logits = torch.empty((T, dc.vocab), dtype=torch.float32, device=dev)
+    tokens = torch.empty((T,), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    for _ in range(warmup):
+        model.draft_step(hid, dc.pos0, kc, vc, logits, tokens, stream=sptr)
+    if model.sync(sptr) != 0:
+        raise SystemExit("draft warm-up failed: %s" % msm.msm_last_error())
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(steps):
+        model.draft_step(hid, dc.pos0, kc, vc, logits, tokens, stream=sptr)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    if model.sync(sptr) != 0:
+        raise SystemExit("draft steps failed: %s" % msm.msm_last_error())
+    ms = statistics.median([ev[i].elapsed_time(ev[i + 1]) for i in range(steps)])
+    model.close()
+    del kv, kc, vc
+    torch.cuda.empty_cache()
+    b = draft_step_bytes(dc, dc.pos0)
+    peak, peak_kind = measured_peaks()
+    gbs = b / (ms * 1e-3) / 1e9
+    return {"workload": dc.name, "ms_per_step": ms, "steps": steps, "algorithmic_bytes_per_step": b,
+            "hbm_gbs": gbs, "frac": gbs / peak, "peak": peak, "peak_kind": peak_kind,
+            "launches_per_step": dc.n_layers + 2, "tokens_proposed": T - 1,
+            "note": "median of CUDA-event step times; layer launches + the two argmax launches; "
+                    "inputs larger than L2 (%.2f GB per step)" % (b / 1e9)}
+
+
+def run_draft(args):
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.4)
+    d = measure_draft(dev, args.steps, args.warmup)
+    clk = clocks.stop()
+    line = {"metric": "draft-step ms (15 tokens proposed in one pass)", "value": d["ms_per_step"], "unit": "ms",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": d["ms_per_step"],
+            "higher_is_better": False, "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded)",
+            "config": {"workload": d["workload"]},
+            "roofline": {"bound": "hbm", "achieved": d["hbm_gbs"], "peak": d["peak"], "unit": "GB/s",
+                         "frac": d["frac"], "traffic": None, "peak_kind": d["peak_kind"]},
+            "gpu_launches": d["launches_per_step"] * args.steps, "clocks": clk, "draft_step": d}
+    print(json.dumps(line))
+    return 0
+
+
 def run_ours(args):
     import torch
     import moe_decode_megakernel_warp_gb300 as msm
@@ -585,6 +663,7 @@ def run_ours(args):
     e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.steps, world, dev)
     accept = measure_accept(model, cfg, hidden, parent, kc, vc, logits, stream, args.steps) if cfg.vocab else None
     model.close()
+    draft = measure_draft(dev, min(args.steps, 50), 3) if (cfg.vocab and not args.no_draft) else None
 
     # ---- per-layer times from the kernel's own %globaltimer stamps (separate model),
     # and what the stamps cost: the same steps timed with the flag on
@@ -650,6 +729,8 @@ def run_ours(args):
         }
         if accept is not None:
             line["accept"] = accept
+        if draft is not None:
+            line["draft_step"] = draft
         if self_timing is not None:
             line["self_timing"] = self_timing
         if cpu is not None:
@@ -675,6 +756,9 @@ def main(argv=None):
     ap.add_argument("--loop-rho", type=float, default=LOOP_RHO)
     ap.add_argument("--l2-runahead-kb", type=int, default=0,
                     help="L2 prefetch distance of each block's stream in KiB (0 = off)")
+    ap.add_argument("--draft", action="store_true",
+                    help="time the draft step of the full-width 5-layer draft alone (one JSON line)")
+    ap.add_argument("--no-draft", action="store_true", help="leave the draft-step timing out of the main line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-self-timing", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
@@ -684,6 +768,8 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if args.loop:
         return run_loop(args)
+    if args.draft:
+        return run_draft(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -100,6 +100,16 @@ typedef enum {
                                           5.9 ms still goes") */
 #define MSM_FLAG_PDL 0x8u              /* chain layer launches with programmatic
                                           dependent launch */
+#define MSM_FLAG_DRAFT 0x20u           /* the model is the draft model of the decode
+                                          step (alphasignal.ai, § "Draft and verify share
+                                          one graph"): each layer's MoE half is a dense
+                                          SwiGLU FFN (w_gate, w_up, w_down; norm_moe is
+                                          its RMSNorm gain), every layer attends to its
+                                          whole KV history and to all 16 slots of the
+                                          block (no tree mask, no window); pool_dim,
+                                          n_experts and top_k are 0 and the expert,
+                                          pooler, router and unpooler weights NULL;
+                                          vocab > 0.  Run with msm_draft_step. */
 #define MSM_FLAG_TEST_DROP_HANDOFF 0x10000u /* test hook: one block never signals that
                                           its share of h1 is stored, so the pooler's
                                           consumers time out */
@@ -144,6 +154,11 @@ typedef struct {
   const float* const* w2_tensor_scale;
   const void* norm_final; /* required when vocab > 0 */
   const void* w_lm;       /* required when vocab > 0 */
+  /* MSM_FLAG_DRAFT models only (NULL otherwise): bf16 [ffn_dim][d_model] gate and up
+     projections and bf16 [d_model][ffn_dim] down projection of each layer's FFN */
+  const void* const* w_gate;
+  const void* const* w_up;
+  const void* const* w_down;
 } msm_weights;
 
 typedef struct msm_model msm_model;
@@ -393,11 +408,31 @@ msm_status msm_graph_launch(msm_graph* graph, void* stream);
 void msm_graph_destroy(msm_graph* graph);
 
 /*
- * Draft step (DFlash-style draft proposing the 15 tree candidates).  Not built
- * in this version: always returns MSM_ERR_UNSUPPORTED.
+ * msm_draft_step: one pass of the draft model (a model created with
+ * MSM_FLAG_DRAFT) over a block of 16 slots, proposing 15 tokens at once
+ * (alphasignal.ai, § "Draft and verify share one graph": a 5-layer draft, one
+ * launch per layer, its 15 candidates from one pass).  The pages give only the
+ * widths; the layer follows the target layer's conventions:
+ *   slot i sits at position pos0 + i (RoPE) and writes its K/V rows to cache row
+ *   pos0 + i; it attends to every history row [0, pos0) and to all 16 slots;
+ *   h1 = bf16(h + bf16(attn W_o^T)); z = bf16(silu(x W_gate^T) * (x W_up^T)) with
+ *   x = RMSNorm(h1); h2 = bf16(h1 + bf16(z W_down^T)); after the last layer the
+ *   final RMSNorm and the LM head give fp32 logits.
+ *   hidden_in  device bf16 [16][d_model]: the block's input rows
+ *   pos0       first cache row of the block: 0 <= pos0 <= max_ctx - 16
+ *   k_cache / v_cache  host arrays of n_layers device pointers, bf16
+ *              [n_kv_heads][max_ctx][head_dim] each (the draft's own caches)
+ *   logits_out device fp32 [16][vocab] (required)
+ *   tokens_out device int32 [16]: tokens_out[0] = -1 (slot 0 holds the caller's
+ *              known token), tokens_out[i] = the argmax of slot i's logits (the
+ *              smallest index among equal maxima): the proposal for position
+ *              pos0 + i.  The proposal is a chain, parent[i] = i - 1.
+ * Launches n_layers layer-kernel launches and two reduction launches on `stream`;
+ * returns after enqueueing.  Errors: MSM_ERR_INVALID_ARG (NULL pointer, pos0 out
+ * of range, model not a draft model); a failing launch reports at msm_sync.
  */
-msm_status msm_draft_step(msm_model* model, const void* draft_hidden_in, int32_t* tokens_out,
-                          int32_t* parent_out, void* stream);
+msm_status msm_draft_step(msm_model* draft, const void* hidden_in, int32_t pos0, void* const* k_cache,
+                          void* const* v_cache, float* logits_out, int32_t* tokens_out, void* stream);
 
 /* Message of the last error on the calling thread ("" if none). */
 const char* msm_last_error(void);

@@ -32,6 +32,7 @@ MSM_FLAG_SELF_TIMING = 0x1
 MSM_FLAG_EXPERT_PREFETCH = 0x2
 MSM_FLAG_KV_PREFETCH = 0x4
 MSM_FLAG_PDL = 0x8
+MSM_FLAG_DRAFT = 0x20
 MSM_FLAG_TEST_DROP_HANDOFF = 0x10000
 MSM_TIMING_EVENTS = 192
 # entries of msm_accept's result buffer (MSM_ACCEPT_RESULT_INTS)
@@ -123,7 +124,8 @@ class MsmWeights(ctypes.Structure):
     _fields_ = [(n, _PP) for n in (
         "w_qkv", "w_o", "w_pool", "w_router", "b_router", "w_unpool", "norm_attn", "norm_moe",
         "w1_codes", "w1_scales", "w1_tensor_scale", "w2_codes", "w2_scales", "w2_tensor_scale")] + [
-        ("norm_final", ctypes.c_void_p), ("w_lm", ctypes.c_void_p)]
+        ("norm_final", ctypes.c_void_p), ("w_lm", ctypes.c_void_p)] + [
+        (n, _PP) for n in ("w_gate", "w_up", "w_down")]
 
 
 class MsmStats(ctypes.Structure):
@@ -184,7 +186,7 @@ def lib():
             L.msm_graph_launch.restype = st
             L.msm_graph_destroy.argtypes = [vp]
             L.msm_graph_destroy.restype = None
-            L.msm_draft_step.argtypes = [vp, vp, vp, vp, vp]
+            L.msm_draft_step.argtypes = [vp, vp, i32, _PP, _PP, vp, vp, vp]
             L.msm_draft_step.restype = st
             L.msm_last_error.argtypes = []
             L.msm_last_error.restype = ctypes.c_char_p
@@ -332,9 +334,11 @@ def msm_graph_destroy(graph) -> None:
     lib().msm_graph_destroy(graph)
 
 
-def msm_draft_step(model, draft_hidden_in=0, tokens_out=0, parent_out=0, stream=0) -> int:
-    return lib().msm_draft_step(model, ctypes.c_void_p(draft_hidden_in), ctypes.c_void_p(tokens_out),
-                                ctypes.c_void_p(parent_out), ctypes.c_void_p(stream))
+def msm_draft_step(model, hidden_in, pos0, k_ptrs, v_ptrs, logits_out, tokens_out, stream=0) -> int:
+    kp, _ka = _ptr_array(k_ptrs)
+    vpp, _va = _ptr_array(v_ptrs)
+    return lib().msm_draft_step(model, ctypes.c_void_p(hidden_in), int(pos0), kp, vpp, ctypes.c_void_p(logits_out),
+                                ctypes.c_void_p(tokens_out), ctypes.c_void_p(stream))
 
 
 # ---------------------------------------------------------------- torch-facing wrapper
@@ -343,14 +347,27 @@ class Model:
 
     ``layers``: list of dicts with keys w_qkv, w_o, w_pool, w_router, b_router, w_unpool,
     norm_attn, norm_moe, w1_codes, w1_sf, w1_gs, w2_codes, w2_sf, w2_gs (torch tensors on the
-    device; bf16 data may be held as int16/uint16).  ``final``: dict with norm_final, w_lm
-    (or empty when vocab == 0).  The caller may drop its tensors after construction: the
-    model keeps packed copies."""
+    device; bf16 data may be held as int16/uint16); with MSM_FLAG_DRAFT in ``flags`` (a draft
+    model: dims with p = e = k = 0) the keys are w_qkv, w_o, norm_attn, norm_moe (the FFN's
+    norm gain), w_gate, w_up, w_down.  ``final``: dict with norm_final, w_lm (or empty when
+    vocab == 0).  The caller may drop its tensors after construction: the model keeps packed
+    copies."""
 
     def __init__(self, dims, layers, final=None, device=0, flags=MSM_FLAG_PDL, grid_blocks=0,
                  attn_splits=0, prefetch_experts=0, timeout_us=0, l2_runahead_kb=0):
         self.dims = dims
         L = dims.n_layers
+        if flags & MSM_FLAG_DRAFT:
+            # dims of a draft model: d, heads, hd, f, n_layers, vocab, max_ctx, rms_eps, rope_theta
+            self._glob = None
+            cfg = MsmConfig(d_model=dims.d, n_q_heads=dims.heads, n_kv_heads=dims.heads, head_dim=dims.hd,
+                            pool_dim=0, ffn_dim=dims.f, n_experts=0, top_k=0, n_layers=L, vocab=dims.vocab,
+                            window=0, max_ctx=dims.max_ctx, layer_is_global=None, rms_eps=dims.rms_eps,
+                            rope_theta=dims.rope_theta, flags=flags, grid_blocks=grid_blocks,
+                            attn_splits=attn_splits, prefetch_experts=0, timeout_us=timeout_us,
+                            l2_runahead_kb=l2_runahead_kb)
+            self._make(cfg, layers, final or {}, device, True)
+            return
         self._glob = (ctypes.c_uint8 * L)(*[1 if dims.is_global(l) else 0 for l in range(L)])
         cfg = MsmConfig(d_model=dims.d, n_q_heads=dims.hq, n_kv_heads=dims.hkv, head_dim=dims.hd,
                         pool_dim=dims.p, ffn_dim=dims.f, n_experts=dims.e, top_k=dims.k, n_layers=L,
@@ -359,14 +376,25 @@ class Model:
                         rms_eps=dims.rms_eps, rope_theta=dims.rope_theta, flags=flags,
                         grid_blocks=grid_blocks, attn_splits=attn_splits, prefetch_experts=prefetch_experts,
                         timeout_us=timeout_us, l2_runahead_kb=l2_runahead_kb)
+        self._make(cfg, layers, final or {}, device, False)
+
+    def _make(self, cfg, layers, final, device, draft):
+        L = cfg.n_layers
         keep = []
+        self.draft = draft
 
         def arr(key):
             p, a = _ptr_array([layers[l][key].data_ptr() for l in range(L)])
             keep.append(a)
             return p
 
-        final = final or {}
+        if draft:
+            w = MsmWeights(w_qkv=arr("w_qkv"), w_o=arr("w_o"), norm_attn=arr("norm_attn"), norm_moe=arr("norm_moe"),
+                           w_gate=arr("w_gate"), w_up=arr("w_up"), w_down=arr("w_down"),
+                           norm_final=final["norm_final"].data_ptr(), w_lm=final["w_lm"].data_ptr())
+            self.handle = msm_model_create(cfg, w, device)
+            self.config = cfg
+            return
         w = MsmWeights(w_qkv=arr("w_qkv"), w_o=arr("w_o"), w_pool=arr("w_pool"), w_router=arr("w_router"),
                        b_router=arr("b_router"), w_unpool=arr("w_unpool"), norm_attn=arr("norm_attn"),
                        norm_moe=arr("norm_moe"), w1_codes=arr("w1_codes"), w1_scales=arr("w1_sf"),
@@ -446,6 +474,13 @@ class Model:
                                  hidden_out.data_ptr() if hidden_out is not None else 0,
                                  accept_result.data_ptr() if accept_result is not None else 0)
         return StepGraph(g, self)
+
+    def draft_step(self, hidden_in, pos0, k_caches, v_caches, logits_out, tokens_out, stream=0):
+        """msm_draft_step (a draft model): logits_out device fp32 [16][vocab], tokens_out device
+        int32 [16] (tokens_out[0] = -1, tokens_out[i] = slot i's argmax)."""
+        return _check(msm_draft_step(self.handle, hidden_in.data_ptr(), pos0,
+                                     [k.data_ptr() for k in k_caches], [v.data_ptr() for v in v_caches],
+                                     logits_out.data_ptr(), tokens_out.data_ptr(), stream))
 
     def sync(self, stream=0) -> int:
         return msm_sync(self.handle, stream)

@@ -52,6 +52,7 @@ uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 struct LayerPack {
   uint8_t *qkv = nullptr, *o = nullptr, *pool = nullptr, *router = nullptr, *unpool = nullptr, *w1 = nullptr,
           *w2 = nullptr;
+  uint8_t *up = nullptr, *down = nullptr;  // draft models: FFN gate+up (paired rows) and down
   float *b = nullptr, *w1gs = nullptr, *w2gs = nullptr;
   uint16_t *g_attn = nullptr, *g_moe = nullptr;
 };
@@ -119,8 +120,31 @@ struct msm_model {
 
 namespace {
 
+// a draft model (MSM_FLAG_DRAFT): dense SwiGLU FFN layers, full attention
+msm_status validate_draft_config(const msm_config* c) {
+  if (c->d_model <= 0 || c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 || c->ffn_dim <= 0 ||
+      c->n_layers <= 0 || c->max_ctx < T || c->vocab <= 0)
+    return fail(MSM_ERR_INVALID_ARG, "draft config: non-positive size (vocab is required)");
+  if (c->pool_dim != 0 || c->n_experts != 0 || c->top_k != 0)
+    return fail(MSM_ERR_INVALID_ARG, "draft config: pool_dim, n_experts and top_k must be 0");
+  if (c->n_q_heads % c->n_kv_heads) return fail(MSM_ERR_INVALID_ARG, "config: n_q_heads % n_kv_heads != 0");
+  const int group = c->n_q_heads / c->n_kv_heads;
+  if (c->head_dim != 64 && c->head_dim != 128) return fail(MSM_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (group != 1 && group != 2 && group != 4 && group != 8)
+    return fail(MSM_ERR_UNSUPPORTED, "n_q_heads / n_kv_heads must be 1, 2, 4 or 8");
+  if (c->d_model % 64 || (c->n_q_heads * c->head_dim) % 64)
+    return fail(MSM_ERR_UNSUPPORTED, "d_model and n_q_heads*head_dim must be multiples of 64");
+  if (c->ffn_dim % 128) return fail(MSM_ERR_UNSUPPORTED, "draft ffn_dim must be a multiple of 128 (two staged K halves)");
+  if (c->vocab % 16) return fail(MSM_ERR_UNSUPPORTED, "vocab must be a multiple of 16");
+  if (c->grid_blocks < 0 || c->attn_splits < 0) return fail(MSM_ERR_INVALID_ARG, "config: negative grid_blocks / attn_splits");
+  if (c->flags & (MSM_FLAG_EXPERT_PREFETCH | MSM_FLAG_KV_PREFETCH))
+    return fail(MSM_ERR_INVALID_ARG, "draft config: the expert and KV prefetch flags do not apply");
+  return MSM_OK;
+}
+
 msm_status validate_config(const msm_config* c) {
   if (!c) return fail(MSM_ERR_INVALID_ARG, "config is NULL");
+  if (c->flags & MSM_FLAG_DRAFT) return validate_draft_config(c);
   if (c->d_model <= 0 || c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 || c->pool_dim <= 0 ||
       c->ffn_dim <= 0 || c->n_experts <= 0 || c->top_k <= 0 || c->n_layers <= 0 || c->max_ctx < T ||
       c->vocab < 0 || c->window <= 0 || !c->layer_is_global)
@@ -181,8 +205,11 @@ msm_status arm_exchange(uint8_t* x, const XOffsets& o, cudaStream_t s) {
 bool encode_act_maps(msm_model* m, uint8_t* x, CUtensorMap* maps) {
   const Dims& dm = m->dm;
   const XOffsets& xo = m->xo;
-  const uint64_t offs[5] = {xo.o, xo.h1, xo.u, xo.z, xo.h2};
-  const int ks[5] = {dm.hq * dm.hd, dm.d, dm.p, dm.p, dm.d};
+  // (a draft model: the two K halves of its FFN activation, [2][16][f/2], in place of u, z)
+  const uint64_t zh = (uint64_t)T * (dm.f / 2) * 2;
+  const uint64_t offs[5] = {xo.o, xo.h1, dm.draft ? xo.z : xo.u, dm.draft ? xo.z + zh : xo.z, xo.h2};
+  const int kz = dm.draft ? dm.f / 2 : dm.p;
+  const int ks[5] = {dm.hq * dm.hd, dm.d, kz, kz, dm.d};
   if (!m->encode) return false;
   for (int i = 0; i < 5; ++i) {
     const int nblk = ks[i] / 64;
@@ -228,20 +255,29 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   if (st != MSM_OK) return st;
   if (!w) return fail(MSM_ERR_INVALID_ARG, "weights is NULL");
   const msm_config& c = *config;
-  if (!w->w_qkv || !w->w_o || !w->w_pool || !w->w_router || !w->b_router || !w->w_unpool || !w->norm_attn ||
-      !w->norm_moe || !w->w1_codes || !w->w1_scales || !w->w1_tensor_scale || !w->w2_codes || !w->w2_scales ||
-      !w->w2_tensor_scale)
-    return fail(MSM_ERR_INVALID_ARG, "weights: a per-layer pointer array is NULL");
-  for (int l = 0; l < c.n_layers; ++l)
-    if (!w->w_qkv[l] || !w->w_o[l] || !w->w_pool[l] || !w->w_router[l] || !w->b_router[l] || !w->w_unpool[l] ||
-        !w->norm_attn[l] || !w->norm_moe[l] || !w->w1_codes[l] || !w->w1_scales[l] || !w->w1_tensor_scale[l] ||
-        !w->w2_codes[l] || !w->w2_scales[l] || !w->w2_tensor_scale[l])
-      return fail(MSM_ERR_INVALID_ARG, "weights: NULL pointer for layer " + std::to_string(l));
+  const bool draft = (c.flags & MSM_FLAG_DRAFT) != 0;
+  if (draft) {
+    if (!w->w_qkv || !w->w_o || !w->norm_attn || !w->norm_moe || !w->w_gate || !w->w_up || !w->w_down)
+      return fail(MSM_ERR_INVALID_ARG, "draft weights: a per-layer pointer array is NULL");
+    for (int l = 0; l < c.n_layers; ++l)
+      if (!w->w_qkv[l] || !w->w_o[l] || !w->norm_attn[l] || !w->norm_moe[l] || !w->w_gate[l] || !w->w_up[l] || !w->w_down[l])
+        return fail(MSM_ERR_INVALID_ARG, "draft weights: NULL pointer for layer " + std::to_string(l));
+  } else {
+    if (!w->w_qkv || !w->w_o || !w->w_pool || !w->w_router || !w->b_router || !w->w_unpool || !w->norm_attn ||
+        !w->norm_moe || !w->w1_codes || !w->w1_scales || !w->w1_tensor_scale || !w->w2_codes || !w->w2_scales ||
+        !w->w2_tensor_scale)
+      return fail(MSM_ERR_INVALID_ARG, "weights: a per-layer pointer array is NULL");
+    for (int l = 0; l < c.n_layers; ++l)
+      if (!w->w_qkv[l] || !w->w_o[l] || !w->w_pool[l] || !w->w_router[l] || !w->b_router[l] || !w->w_unpool[l] ||
+          !w->norm_attn[l] || !w->norm_moe[l] || !w->w1_codes[l] || !w->w1_scales[l] || !w->w1_tensor_scale[l] ||
+          !w->w2_codes[l] || !w->w2_scales[l] || !w->w2_tensor_scale[l])
+        return fail(MSM_ERR_INVALID_ARG, "weights: NULL pointer for layer " + std::to_string(l));
+    for (int l = 0; l < c.n_layers; ++l)
+      if ((reinterpret_cast<uintptr_t>(w->w1_codes[l]) | reinterpret_cast<uintptr_t>(w->w1_scales[l]) |
+           reinterpret_cast<uintptr_t>(w->w2_codes[l]) | reinterpret_cast<uintptr_t>(w->w2_scales[l])) & 15)
+        return fail(MSM_ERR_INVALID_ARG, "weights: NVFP4 codes and scales must be 16-byte aligned (layer " + std::to_string(l) + ")");
+  }
   if (c.vocab > 0 && (!w->norm_final || !w->w_lm)) return fail(MSM_ERR_INVALID_ARG, "vocab > 0 needs norm_final and w_lm");
-  for (int l = 0; l < c.n_layers; ++l)
-    if ((reinterpret_cast<uintptr_t>(w->w1_codes[l]) | reinterpret_cast<uintptr_t>(w->w1_scales[l]) |
-         reinterpret_cast<uintptr_t>(w->w2_codes[l]) | reinterpret_cast<uintptr_t>(w->w2_scales[l])) & 15)
-      return fail(MSM_ERR_INVALID_ARG, "weights: NVFP4 codes and scales must be 16-byte aligned (layer " + std::to_string(l) + ")");
 
   int ndev = 0;
   CK(cudaGetDeviceCount(&ndev));
@@ -257,12 +293,14 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   msm_model* m = new msm_model();
   m->device = device;
   m->cfg = c;
-  m->global.assign(c.layer_is_global, c.layer_is_global + c.n_layers);
+  if (draft) m->global.assign(c.n_layers, 1);  // the draft attends to its whole history
+  else m->global.assign(c.layer_is_global, c.layer_is_global + c.n_layers);
   m->cfg.layer_is_global = nullptr;
   Dims& dm = m->dm;
   dm.d = c.d_model; dm.hq = c.n_q_heads; dm.hkv = c.n_kv_heads; dm.hd = c.head_dim; dm.p = c.pool_dim;
   dm.f = c.ffn_dim; dm.e = c.n_experts; dm.k = c.top_k; dm.vocab = c.vocab; dm.max_ctx = c.max_ctx;
-  dm.window = c.window; dm.n_layers = c.n_layers;
+  dm.window = draft ? c.max_ctx : c.window; dm.n_layers = c.n_layers;
+  dm.draft = draft ? 1 : 0;
   dm.nqkv = (dm.hq + 2 * dm.hkv) * dm.hd;
   dm.group = dm.hq / dm.hkv;
   dm.attn_rows = dm.hd == 128 ? 32 : 64;
@@ -288,22 +326,22 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   const int D = dm.hd;
   const uint64_t attn_need = (uint64_t)dm.group * (D / 16) * kKStepBytes + 2ull * 16 * D * 2 +
                              (uint64_t)dm.group * dm.attn_wph * 32 * (4 + D / 2) * 4;
-  const uint64_t kmax = (uint64_t)std::max(std::max(dm.d, dm.hq * dm.hd), dm.p);
+  // (a draft model stages its FFN activation in two K halves)
+  const uint64_t kmax = (uint64_t)std::max(std::max(dm.d, dm.hq * dm.hd), draft ? dm.f / 2 : dm.p);
   // GEMM1: operand B, the split pooled vectors with their scale groups; GEMM2: two
   // experts' NVFP4 rows (E2M1 + scales) + one fp32 row per warp (both at the top of the
   // buffer; the router stages the bf16 pooled vectors at its bottom, dead once the
   // router phase has split them, before operand B is copied in)
-  const uint64_t g1_need = b1_bytes(dm.p);
-  const uint64_t g2_need = ((18ull * dm.f + 1023) & ~1023ull) + (uint64_t)kComputeWarps * dm.f * 4;
+  const uint64_t g1_need = draft ? 0 : b1_bytes(dm.p);
+  const uint64_t g2_need = draft ? 0 : ((18ull * dm.f + 1023) & ~1023ull) + (uint64_t)kComputeWarps * dm.f * 4;
   uint64_t act = std::max(std::max(kmax * 32, g1_need), std::max(g2_need, attn_need));
   act = (act + 1023) & ~uint64_t(1023);
   const uint64_t expert_top = (std::max(g1_need, g2_need) + 1023) & ~uint64_t(1023);
   const int smem_cap = std::min(kMaxSmem, smem_optin);
   long long ring = (long long)smem_cap - (long long)act - kSmallBytes;
   ring &= ~1023ll;
-  const uint64_t max_tile =
-      std::max(std::max((uint64_t)kDenseTileSteps * kKStepBytes, (uint64_t)std::max(exp_tile_bytes(dm.p), exp_tile_bytes(dm.f))),
-               (uint64_t)dm.attn_rows * D * 4);
+  const uint64_t exp_tile = draft ? 0 : (uint64_t)std::max(exp_tile_bytes(dm.p), exp_tile_bytes(dm.f));
+  const uint64_t max_tile = std::max(std::max((uint64_t)kDenseTileSteps * kKStepBytes, exp_tile), (uint64_t)dm.attn_rows * D * 4);
   if (ring < (long long)(2 * max_tile)) {
     delete m;
     return fail(MSM_ERR_UNSUPPORTED, "widths too large for the shared-memory budget");
@@ -321,6 +359,7 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   // GEMM1's operand-B scales are the bottom of its operand: when the operand is what sets
   // the top of the expert phases, the ring may grow over them once they are copied
   m->sfb_ext = (m->g1_b_off == m->ring_ext) ? (int)b1_sfb_bytes(dm.p) : 0;
+  if (draft) m->ring_ext = m->unpool_ext = m->sfb_ext = 0;  // (no expert or unpooler tiles)
   m->smem_bytes = (int)(ring + act + kSmallBytes);
 
   auto bail = [&](msm_status s2) {
@@ -354,7 +393,36 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   cudaStream_t s = m->aux;
   m->L.resize(c.n_layers);
   const int u1pe = w1_units(dm.f), u2pe = w2_units(dm.p);
-  for (int l = 0; l < c.n_layers; ++l) {
+  if (draft) {
+    // the FFN's gate and up projections go through one [2F][d] staging copy, packed with
+    // gate row j and up row j in the same 16-row unit (rows 0-7 / 8-15) for the SwiGLU epilogue
+    uint8_t* gu = nullptr;
+    const uint64_t b_gu = 2ull * dm.f * dm.d * 2;
+    CKM(cudaMalloc(&gu, b_gu));
+    for (int l = 0; l < c.n_layers; ++l) {
+      LayerPack& lp = m->L[l];
+      const uint64_t b_qkv = (dm.nqkv / 16) * dense_unit_bytes(dm.d), b_o = (dm.d / 16) * dense_unit_bytes(dm.hq * dm.hd),
+                     b_up = (2ull * dm.f / 16) * dense_unit_bytes(dm.d), b_down = (dm.d / 16) * dense_unit_bytes(dm.f);
+      CKM(m->alloc(&lp.qkv, b_qkv));
+      CKM(m->alloc(&lp.o, b_o));
+      CKM(m->alloc(&lp.up, b_up));
+      CKM(m->alloc(&lp.down, b_down));
+      CKM(m->alloc(&lp.g_attn, dm.d * 2));
+      CKM(m->alloc(&lp.g_moe, dm.d * 2));
+      m->packed_bytes += b_qkv + b_o + b_up + b_down;
+      CKM(launch_pack_dense(w->w_qkv[l], lp.qkv, dm.nqkv, dm.d, 1, dm.hd, dm.hq, dm.hkv, s));
+      CKM(launch_pack_dense(w->w_o[l], lp.o, dm.d, dm.hq * dm.hd, 0, dm.hd, dm.hq, dm.hkv, s));
+      CKM(cudaMemcpyAsync(gu, w->w_gate[l], b_gu / 2, cudaMemcpyDeviceToDevice, s));
+      CKM(cudaMemcpyAsync(gu + b_gu / 2, w->w_up[l], b_gu / 2, cudaMemcpyDeviceToDevice, s));
+      CKM(launch_pack_dense(gu, lp.up, 2 * dm.f, dm.d, 2, dm.hd, dm.hq, dm.hkv, s));
+      CKM(launch_pack_dense(w->w_down[l], lp.down, dm.d, dm.f, 0, dm.hd, dm.hq, dm.hkv, s));
+      CKM(cudaMemcpyAsync(lp.g_attn, w->norm_attn[l], dm.d * 2, cudaMemcpyDeviceToDevice, s));
+      CKM(cudaMemcpyAsync(lp.g_moe, w->norm_moe[l], dm.d * 2, cudaMemcpyDeviceToDevice, s));
+    }
+    CKM(cudaStreamSynchronize(s));
+    CKM(cudaFree(gu));
+  }
+  for (int l = 0; l < c.n_layers && !draft; ++l) {
     LayerPack& lp = m->L[l];
     const uint64_t b_qkv = (dm.nqkv / 16) * dense_unit_bytes(dm.d), b_o = (dm.d / 16) * dense_unit_bytes(dm.hq * dm.hd),
                    b_pool = (dm.p / 16) * dense_unit_bytes(dm.d), b_r = (dm.e / 16) * dense_unit_bytes(dm.p),
@@ -404,7 +472,7 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   xo.u = o; o += align256((uint64_t)T * dm.p * 2);
   xo.logits = o; o += align256((uint64_t)T * dm.e * 4);
   xo.a = o; o += align256((uint64_t)T * dm.k * dm.f * 4);
-  xo.z = o; o += align256((uint64_t)T * dm.p * 2);
+  xo.z = o; o += align256((uint64_t)T * (draft ? dm.f : dm.p) * 2);  // (a draft's FFN activation)
   xo.h2 = o; o += align256((uint64_t)T * dm.d * 2);
   xo.q0 = o; o += align256((uint64_t)T * dm.hq * dm.hd * 2);
   xo.tkv0 = o; o += align256(2ull * dm.hkv * T * dm.hd * 2);
@@ -413,7 +481,8 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   xo.total = o;
   SOffsets& so = m->so;
   o = 0;
-  so.part = o; o += align256((uint64_t)dm.hkv * dm.splits * T * dm.group * dm.hd * 4);
+  // (attention partials; a draft's first-half FFN-down partial sums reuse the space)
+  so.part = o; o += align256(std::max((uint64_t)dm.hkv * dm.splits * T * dm.group * dm.hd * 4, (uint64_t)T * dm.d * 4));
   so.ml = o; o += align256((uint64_t)dm.hkv * dm.splits * T * dm.group * 2 * 4);
   so.y = o; o += align256((uint64_t)T * dm.k * dm.p * 2);
   so.total = o;
@@ -546,9 +615,12 @@ msm_status validate_step(msm_model* m, const void* hidden_in, const int32_t* par
 // device-resident step state that the kernels validate
 msm_status enqueue_verify(msm_model* m, const StepBuffers& B, const void* hidden_in, const int32_t* parent,
                           int32_t pos0, const int32_t* state, void* const* k_cache, void* const* v_cache,
-                          float* logits_out, void* hidden_out, void* stream) {
+                          float* logits_out, void* hidden_out, void* stream, bool draft_call = false) {
   msm_status vst = validate_step(m, hidden_in, parent, pos0, state, k_cache, v_cache, logits_out, hidden_out);
   if (vst != MSM_OK) return vst;
+  if ((m->dm.draft != 0) != draft_call)
+    return fail(MSM_ERR_INVALID_ARG, draft_call ? "msm_draft_step needs a model created with MSM_FLAG_DRAFT"
+                                                : "a draft model (MSM_FLAG_DRAFT) runs with msm_draft_step only");
   const Dims& dm = m->dm;
   CK(cudaSetDevice(m->device));
   for (int l = 0; l < dm.n_layers; ++l) {
@@ -622,6 +694,8 @@ msm_status enqueue_verify(msm_model* m, const StepBuffers& B, const void* hidden
     P.w2 = lp.w2;
     P.w1_gs = lp.w1gs;
     P.w2_gs = lp.w2gs;
+    P.w_up = lp.up;
+    P.w_down = lp.down;
     P.w_tail = last ? m->lm : m->L[l + 1].qkv;
     P.g_tail = last ? m->g_final : m->L[l + 1].g_attn;
     P.hidden_out = last ? static_cast<uint16_t*>(hidden_out) : nullptr;
@@ -814,6 +888,7 @@ msm_status enqueue_accept(msm_model* m, const float* logits, const int32_t* toke
   if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
   const Dims& dm = m->dm;
   if (dm.vocab <= 0) return fail(MSM_ERR_UNSUPPORTED, "accept needs the LM head (vocab > 0)");
+  if (dm.draft) return fail(MSM_ERR_INVALID_ARG, "a draft model (MSM_FLAG_DRAFT) runs with msm_draft_step only");
   if (!logits || !result || !k_cache || !v_cache)
     return fail(MSM_ERR_INVALID_ARG, "NULL logits, result or cache array");
   if (!state) {
@@ -980,10 +1055,23 @@ msm_status msm_graph_launch(msm_graph* g, void* stream) {
   return MSM_OK;
 }
 
-msm_status msm_draft_step(msm_model* m, const void* draft_hidden_in, int32_t* tokens_out, int32_t* parent_out,
-                          void* stream) {
-  (void)m; (void)draft_hidden_in; (void)tokens_out; (void)parent_out; (void)stream;
-  return fail(MSM_ERR_UNSUPPORTED, "msm_draft_step is not built in this version");
+msm_status msm_draft_step(msm_model* m, const void* hidden_in, int32_t pos0, void* const* k_cache,
+                          void* const* v_cache, float* logits_out, int32_t* tokens_out, void* stream) {
+  if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
+  if (!logits_out || !tokens_out) return fail(MSM_ERR_INVALID_ARG, "logits_out and tokens_out are required");
+  if (reinterpret_cast<uintptr_t>(tokens_out) & 3) return fail(MSM_ERR_INVALID_ARG, "tokens_out must be 4-byte aligned");
+  // the block's slots form a chain (slot i at pos0 + i); the kernels give every slot
+  // the whole block, so the chain only fixes the positions
+  int32_t chain[T];
+  for (int i = 0; i < T; ++i) chain[i] = i - 1;
+  msm_status st = enqueue_verify(m, own_buffers(m), hidden_in, chain, pos0, nullptr, k_cache, v_cache, logits_out,
+                                 nullptr, stream, true);
+  if (st != MSM_OK) return st;
+  // the proposals: each slot's argmax (smallest index among equal maxima), slot 0 = -1
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CK(launch_accept_argmax(logits_out, m->dm.vocab, m->accept_part, m->G, m->accept_ticket, tokens_out, s));
+  CK(cudaMemsetAsync(tokens_out, 0xFF, sizeof(int32_t), s));
+  return MSM_OK;
 }
 
 }  // extern "C"

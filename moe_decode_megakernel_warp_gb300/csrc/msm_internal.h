@@ -122,6 +122,7 @@ struct Dims {
   int attn_wph;    // warps per q head
   int splits;      // attention splits per kv head
   float rms_eps;
+  int draft;       // a draft model: dense SwiGLU FFN layers (f = ffn_dim), attention to the whole block
 };
 
 struct LaunchParams {
@@ -139,6 +140,8 @@ struct LaunchParams {
   const uint8_t* w2;
   const float* w1_gs;
   const float* w2_gs;
+  const uint8_t* w_up;        // draft models: FFN gate + up (paired rows), FFN down
+  const uint8_t* w_down;
   const uint8_t* w_tail;      // next layer's QKV, or the LM head on the last layer
   const uint16_t* g_tail;     // next layer's attention gain, or the final gain
   // caller buffers

@@ -409,8 +409,16 @@ __device__ __noinline__ void ra_front(const LaunchParams& P, RunAhead* ra, int b
     ra->add(P.vc + off, bytes);
   }
   add_dense_range(*ra, P.w_o, dm.hq * dm.hd, dm.d, P.phase_rot * 3);
-  add_dense_range(*ra, P.w_pool, dm.d, dm.p, P.phase_rot * 4);
-  add_dense_range(*ra, P.w_router, dm.p, dm.e, P.phase_rot * 5);
+  if (dm.draft) {
+    // a draft model's whole stream: the FFN, then the next layer's QKV or the LM head
+    add_dense_range(*ra, P.w_up, dm.d, 2 * dm.f, P.phase_rot * 4);
+    add_dense_range(*ra, P.w_down, dm.f, dm.d, P.phase_rot * 5);
+    if (!P.last) add_dense_range(*ra, P.w_tail, dm.d, dm.nqkv, P.phase_rot * 9);
+    else add_dense_range(*ra, P.w_tail, dm.d, dm.vocab, P.phase_rot * 9);
+  } else {
+    add_dense_range(*ra, P.w_pool, dm.d, dm.p, P.phase_rot * 4);
+    add_dense_range(*ra, P.w_router, dm.p, dm.e, P.phase_rot * 5);
+  }
   if (block == 0) {
     prefetch_l2(P.g_moe, (uint32_t)dm.d * 2);
     if (P.g_tail) prefetch_l2(P.g_tail, (uint32_t)dm.d * 2);
@@ -456,6 +464,7 @@ struct TileStream {
   int lo, hi, u;     // units of the segment; u: unit of the next tile (dense: of its pair)
   int half;          // dense: the next tile is of unit u + half (units go in pairs, tiles alternating)
   int k0, steps;     // dense: next k-step within unit u; k-steps per unit
+  int kb;            // dense: first k-step of the streamed range (a K half of the unit)
   int upe;           // experts: units per expert
   uint64_t ub;       // bytes per unit
   const uint8_t* W;  // weights of the segment
@@ -468,9 +477,16 @@ struct TileStream {
     u = lo;
     half = 0;
     k0 = 0;
+    kb = 0;
     steps = K / 16;
     ub = dense_unit_bytes(K);
     W = w;
+  }
+  // K half h of every unit (a draft model's FFN down projection, its input staged in halves)
+  __device__ void dense_half(const uint8_t* w, int K, int N, int rot, int h) {
+    dense(w, K, N, rot);
+    steps = K / 32;
+    kb = h * steps;
   }
   // expert units: 128 rows x K as K / exp_tile_k(K) tiles of exp_tile_bytes(K) each
   __device__ void experts(const uint8_t* w, int n_units, int per_expert, int K, int rot) {
@@ -510,7 +526,7 @@ struct TileStream {
         // compute warp groups (one unit each) stream side by side
         const int uu = u + half, ns = min(kDenseTileSteps, steps - k0);
         t_u = uu;
-        src = W + (uint64_t)uu * ub + (uint64_t)k0 * kKStepBytes;
+        src = W + (uint64_t)uu * ub + (uint64_t)(kb + k0) * kKStepBytes;
         bytes = (uint32_t)ns * kKStepBytes;
         if (half == 0 && u + 1 < hi) {
           half = 1;
@@ -525,7 +541,7 @@ struct TileStream {
         return TS_TILE;
       }
       ++seg;
-      lo = hi = u = k0 = half = 0;
+      lo = hi = u = k0 = half = kb = 0;
       switch (seg) {
         case 1: {
           const AttnUnit au = attn_unit(P, cx.pos0, rot_block(cx.block, P.phase_rot * 2, gridDim.x), P.is_global);
@@ -536,12 +552,29 @@ struct TileStream {
         }
         case 2: return TS_DEP_WAIT;
         case 3: dense(P.w_o, dm.hq * dm.hd, dm.d, P.phase_rot * 3); break;
-        case 4: dense(P.w_pool, dm.d, dm.p, P.phase_rot * 4); break;
-        case 5: dense(P.w_router, dm.p, dm.e, P.phase_rot * 5); break;
-        case 6: return TS_ROUTE_WAIT;
-        case 7: experts(P.w1, *cx.S.n_active * w1_units(dm.f), w1_units(dm.f), dm.p, P.phase_rot * 6); break;
-        case 8: experts(P.w2, *cx.S.n_active * w2_units(dm.p), w2_units(dm.p), dm.f, P.phase_rot * 7); break;
-        case 9: dense(P.w_unpool, dm.p, dm.d, P.phase_rot * 8); break;
+        // a draft model: 4 = the FFN's paired gate/up rows, 5 and 6 = the two K halves of
+        // its down projection; no expert segments and no unpooler
+        case 4:
+          if (dm.draft) dense(P.w_up, dm.d, 2 * dm.f, P.phase_rot * 4);
+          else dense(P.w_pool, dm.d, dm.p, P.phase_rot * 4);
+          break;
+        case 5:
+          if (dm.draft) dense_half(P.w_down, dm.f, dm.d, P.phase_rot * 5, 0);
+          else dense(P.w_router, dm.p, dm.e, P.phase_rot * 5);
+          break;
+        case 6:
+          if (!dm.draft) return TS_ROUTE_WAIT;
+          dense_half(P.w_down, dm.f, dm.d, P.phase_rot * 5, 1);
+          break;
+        case 7:
+          if (!dm.draft) experts(P.w1, *cx.S.n_active * w1_units(dm.f), w1_units(dm.f), dm.p, P.phase_rot * 6);
+          break;
+        case 8:
+          if (!dm.draft) experts(P.w2, *cx.S.n_active * w2_units(dm.p), w2_units(dm.p), dm.f, P.phase_rot * 7);
+          break;
+        case 9:
+          if (!dm.draft) dense(P.w_unpool, dm.p, dm.d, P.phase_rot * 8);
+          break;
         case 10:
           if (!P.last) dense(P.w_tail, dm.d, dm.nqkv, P.phase_rot * 9);
           else if (dm.vocab > 0) dense(P.w_tail, dm.d, dm.vocab, P.phase_rot * 9);
@@ -573,7 +606,7 @@ __device__ void loader(Ctx& cx) {
   r.ra_on = P.runahead_bytes != 0;
   TileStream ts;
   ts.seg = 0;
-  ts.lo = ts.hi = ts.u = ts.k0 = ts.half = 0;
+  ts.lo = ts.hi = ts.u = ts.k0 = ts.half = ts.kb = 0;
   // segment 0: the prologue QKV (launch 0); weights and KV rows do not depend on the
   // previous launch, so they stream before the dependency wait
   if (P.first) ts.dense(P.w_qkv_pro, dm.d, dm.nqkv, P.phase_rot * 1);
@@ -959,14 +992,19 @@ __device__ __forceinline__ void qkv_epilogue(const LaunchParams& P, const Smem& 
 }
 
 // what a dense phase does with its outputs (one copy of the phase loop serves all)
-enum EpiKind { EPI_QKV = 0, EPI_OPROJ = 1, EPI_POOL = 2, EPI_ROUTER = 3, EPI_UNPOOL = 4, EPI_LMHEAD = 5 };
+enum EpiKind {
+  EPI_QKV = 0, EPI_OPROJ = 1, EPI_POOL = 2, EPI_ROUTER = 3, EPI_UNPOOL = 4, EPI_LMHEAD = 5,
+  EPI_SWIGLU = 6,   // dense FFN: z = bf16(silu(gate) * up) from a unit's paired rows
+  EPI_PARTIAL = 7   // fp32 partial sums of a K half (the other half adds them)
+};
 struct EpiArgs {
   int kind;
   QkvDst dq;               // EPI_QKV
   const uint16_t* res;     // residual input (EPI_OPROJ: h, EPI_UNPOOL: h1)
-  uint16_t* out;           // bf16 output (h1, u, h2)
+  uint16_t* out;           // bf16 output (h1, u, z, h2)
   uint16_t* out2;          // optional second copy of h2 (next launch / caller)
-  float* out32;            // fp32 output (router logits, LM-head logits)
+  float* out32;            // fp32 output (router logits, LM-head logits, EPI_PARTIAL's sums)
+  const float* part;       // EPI_UNPOOL: optional fp32 partial sums added before rounding
 };
 
 // epilogue of output rows u*16 + p and u*16 + p + 8 for token t (values lo, hi)
@@ -984,7 +1022,7 @@ __device__ void dense_epi(const LaunchParams& P, const Smem& S, const EpiArgs& e
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int n = u * 16 + p + hf * 8;
-        const float o = bf16_to_f32(bf16_bits_rn(v2[hf]));
+        const float o = bf16_to_f32(bf16_bits_rn(ea.part ? v2[hf] + ea.part[(size_t)t * dm.d + n] : v2[hf]));
         const uint16_t r = has_res ? (uint16_t)(hf ? res2 >> 16 : res2 & 0xFFFFu)
                            : ea.kind == EPI_OPROJ ? ea.res[(size_t)t * dm.d + n]
                                                   : ld_relaxed_u16(ea.res + (size_t)t * dm.d + n);
@@ -994,6 +1032,19 @@ __device__ void dense_epi(const LaunchParams& P, const Smem& S, const EpiArgs& e
       }
       break;
     }
+    case EPI_SWIGLU: {
+      // rows p / p+8 of unit u are gate and up row 8u + p; z is kept as its two K halves,
+      // [2][16][f/2], so each half stages like a [16][f/2] activation
+      const int n = u * 8 + p, fh = dm.f >> 1, hf = n >= fh ? 1 : 0;
+      const float zv = lo / (1.0f + expf(-lo)) * hi;
+      st_relaxed_u16(ea.out + ((size_t)hf * 16 + t) * fh + (n - hf * fh), bf16_bits_rn(zv));
+      break;
+    }
+    case EPI_PARTIAL:
+      // read back by this same thread in the second half's epilogue (same units, group, lane)
+      ea.out32[(size_t)t * dm.d + u * 16 + p] = lo;
+      ea.out32[(size_t)t * dm.d + u * 16 + p + 8] = hi;
+      break;
     case EPI_POOL:
       st_relaxed_u16(ea.out + (size_t)t * dm.p + u * 16 + p, bf16_bits_rn(lo));
       st_relaxed_u16(ea.out + (size_t)t * dm.p + u * 16 + p + 8, bf16_bits_rn(hi));
@@ -2267,6 +2318,52 @@ __device__ void rearm(const LaunchParams& P, int block, int tid, int nthreads) {
   }
 }
 
+// A draft model's FFN half of the layer, in place of the MoE half:
+//   z  = bf16(silu(x W_gate^T) * (x W_up^T)), x = bf16(RMSNorm(h1))
+//   h2 = bf16(h1 + bf16(z W_down^T))
+// The gate and up rows are paired in one unit (rows p / p + 8), so one dense phase
+// over N = 2f gives z.  z ([16][f] bf16) is larger than the activation buffer, so the
+// down projection runs as two dense phases over the two K halves of z: the first
+// leaves fp32 partial sums, the second (the same units, so the same threads) adds
+// them before the rounding.  The phase counters of the pooler and the unpooler mark
+// z and h2.
+__device__ void draft_ffn(Worker& w) {
+  Ctx& cx = *w.cx;
+  const LaunchParams& P = *cx.P;
+  const Dims& dm = P.dm;
+  uint8_t* X = P.x_cur;
+  const uint16_t* h1 = reinterpret_cast<const uint16_t*>(X + P.xo.h1);
+  uint16_t* z = reinterpret_cast<uint16_t*>(X + P.xo.z);
+  float* part = reinterpret_cast<float*>(P.s_buf + P.so.part);
+  const int fh = dm.f / 2;
+  stage_act(w, h1, dm.d, CNT_OPROJ, false, P.g_moe, dm.rms_eps, PH_POOL, ACT_H1);
+  {
+    EpiArgs ea{};
+    ea.kind = EPI_SWIGLU;
+    ea.out = z;
+    dense_phase(w, dm.d, 2 * dm.f, P.phase_rot * 4, ea, -1);
+    publish(w, CNT_POOL);
+  }
+  stage_act(w, z, fh, CNT_POOL, false, nullptr, 0.f, PH_ROUTER, ACT_U);
+  {
+    EpiArgs ea{};
+    ea.kind = EPI_PARTIAL;
+    ea.out32 = part;
+    dense_phase(w, fh, dm.d, P.phase_rot * 5, ea, -1);
+  }
+  stage_act(w, z + (size_t)16 * fh, fh, CNT_POOL, false, nullptr, 0.f, PH_UNPOOL, ACT_Z);
+  {
+    EpiArgs ea{};
+    ea.kind = EPI_UNPOOL;
+    ea.res = h1;
+    ea.out = reinterpret_cast<uint16_t*>(X + P.xo.h2);
+    ea.out2 = P.last ? P.hidden_out : P.out_h;
+    ea.part = part;
+    dense_phase(w, fh, dm.d, P.phase_rot * 5, ea, -1);
+    publish(w, CNT_UNPOOL);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // the compute warps' sequence of one launch
 // ---------------------------------------------------------------------------
@@ -2314,6 +2411,9 @@ __device__ void compute_main(Worker& w) {
     publish(w, CNT_OPROJ);
     stamp<kTiming>(P, b, EV_OPROJ_DONE);
   }
+  if (dm.draft) {
+    draft_ffn(w);
+  } else {
   // a5: u = bf16(bf16(RMSNorm(h1)) W_pool^T)
   {
     uint16_t* uo = reinterpret_cast<uint16_t*>(X + P.xo.u);
@@ -2383,6 +2483,7 @@ __device__ void compute_main(Worker& w) {
     dense_phase(w, dm.p, dm.d, P.phase_rot * 8, ea, -1, (uint32_t)P.unpool_act_off);
     publish(w, CNT_UNPOOL);
     stamp<kTiming>(P, b, EV_UNPOOL_DONE);
+  }
   }
   pdl_launch_dependents();
   // a12: next layer's RMSNorm + QKV + RoPE + KV write; a12': final norm + LM head
@@ -2460,7 +2561,8 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
         m |= 1u << j;
         if (j != lane) ++dep;
       }
-      cx.S.anc[lane] = m;
+      // (a draft model's block is a chain whose slots all see one another)
+      cx.S.anc[lane] = P.dm.draft ? 0xFFFFu : m;
       cx.S.depth[lane] = dep;
       cx.S.tpos[lane] = pos0 + dep;
     }
@@ -2495,7 +2597,7 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
   if (warp == 2) {
     pdl_wait();
     cx.deadline = globaltimer() + (((uint64_t)P.timeout_ns_hi << 32) | P.timeout_ns_lo);
-    if (lane == 0) tc_issuer(cx);
+    if (lane == 0 && !P.dm.draft) tc_issuer(cx);  // (a draft model has no expert GEMMs)
     __syncwarp();
     // free tensor memory once the compute warps are done with it
     if (lane == 0) {

@@ -6,7 +6,8 @@
 // so one contiguous bulk copy brings a tile and one ldmatrix.x4 yields the
 // m16n8k16 A fragment.  Two matrices get their rows paired inside a unit so an
 // epilogue thread holds both halves of a pair: the q/k rows of a head as
-// (d, d + hd/2) for rotate-half RoPE, and W1 as (gate j, up j) for SwiGLU.
+// (d, d + hd/2) for rotate-half RoPE, and a dense FFN's stacked [gate; up] as
+// (gate j, up j) for SwiGLU.
 //
 // NVFP4 expert matrices become 128-row units of 512-column tiles (256 where the width is
 // not a multiple of 512): column blocks of 128 rows x 128 code bytes in the 128-byte
@@ -21,8 +22,10 @@
 
 namespace msm {
 
-// row of the source matrix held by row `r` (0..15) of unit `u`
-__device__ __forceinline__ int dense_src_row(int kind, int u, int r, int hd, int hq, int hkv) {
+// row of the source matrix held by row `r` (0..15) of unit `u` (N: the packed rows)
+__device__ __forceinline__ int dense_src_row(int kind, int u, int r, int N, int hd, int hq, int hkv) {
+  if (kind == 2)  // [gate; up] stacked: rows 0-7 gate rows 8u.., rows 8-15 the matching up rows
+    return (r < 8) ? u * 8 + r : N / 2 + u * 8 + (r - 8);
   if (kind == 1) {  // QKV with RoPE pairing
     const int upd = hd / 16, nQ = hq * upd, nK = hkv * upd;
     if (u < nQ + nK) {
@@ -46,7 +49,7 @@ __global__ void pack_dense_kernel(const uint16_t* __restrict__ W, uint8_t* __res
     const long long ks = (c >> 5) % steps, u = (c >> 5) / steps;
     const int ur = (m & 1) * 8 + r;
     const int kcol = (int)ks * 16 + (m >> 1) * 8;
-    const int src = dense_src_row(kind, (int)u, ur, hd, hq, hkv);
+    const int src = dense_src_row(kind, (int)u, ur, N, hd, hq, hkv);
     const uint4 v = *reinterpret_cast<const uint4*>(W + (size_t)src * K + kcol);
     *reinterpret_cast<uint4*>(out + ((size_t)u * steps + ks) * kKStepBytes + m * 128 + r * 16) = v;
   }

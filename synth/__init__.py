@@ -37,6 +37,9 @@ T = 16  # tokens in the verification tree
 K_QKV, K_O, K_POOL, K_ROUTER, K_BIAS, K_UNPOOL, K_NORM_ATTN, K_NORM_MOE = 1, 2, 3, 4, 5, 6, 7, 8
 K_W1, K_W2, K_NORM_FINAL, K_LM, K_HIDDEN, K_PARENT, K_KCACHE, K_VCACHE = 9, 10, 11, 12, 13, 14, 15, 16
 K_ROUTE_KEEP, K_ROUTE_PICK = 17, 18
+# the draft model's tensors
+K_D_QKV, K_D_O, K_D_NORM_ATTN, K_D_NORM_FFN, K_D_GATE, K_D_UP, K_D_DOWN = 19, 20, 21, 22, 23, 24, 25
+K_D_NORM_FINAL, K_D_LM, K_D_HIDDEN, K_D_KCACHE, K_D_VCACHE = 26, 27, 28, 29, 30
 
 
 def build(force: bool = False) -> str:
@@ -151,6 +154,43 @@ CFG1_STACK = replace(CFG1, name="4-layer stack at tiny widths", n_layers=4, voca
                      layer_global=(0, 1, 0, 1))
 
 CONFIGS = {"cfg1": CFG1, "cfg2": CFG2, "cfg3": CFG3, "cfg4": CFG4, "cfg1_stack": CFG1_STACK}
+
+
+@dataclass(frozen=True)
+class DraftConfig:
+    """The draft model: dense layers (attention + SwiGLU FFN) proposing 15 tokens per pass
+    (alphasignal.ai, § "Draft and verify share one graph": 5 layers; d 2048, 16 heads of
+    128, FFN 8192).  All heads are KV heads and every layer attends to its whole history."""
+    name: str
+    d: int
+    heads: int
+    hd: int
+    f: int
+    n_layers: int
+    vocab: int
+    history: int
+    rms_eps: float = 1e-6
+    rope_theta: float = 10000.0
+
+    @property
+    def max_ctx(self) -> int:
+        return self.history + 64
+
+    @property
+    def pos0(self) -> int:
+        return self.history
+
+    @property
+    def resid_std(self) -> float:
+        # residual-branch output projections (o_proj, FFN down) scaled by 1 / sqrt(2 L)
+        return 0.02 / np.sqrt(2 * self.n_layers)
+
+
+DRAFT_SMALL = DraftConfig("2-layer draft at tiny widths (d256, 4 heads of 64, FFN 512)", d=256, heads=4, hd=64,
+                          f=512, n_layers=2, vocab=512, history=200)
+DRAFT_FULL = DraftConfig("5-layer draft (d2048, 16 heads of 128, FFN 8192, ctx 8192, vocab 131072)", d=2048,
+                         heads=16, hd=128, f=8192, n_layers=5, vocab=131072, history=8192)
+DRAFT_CONFIGS = {"draft_small": DRAFT_SMALL, "draft_full": DRAFT_FULL}
 
 
 # --------------------------------------------------------------------------
@@ -271,6 +311,43 @@ def parity_seeds(name: str) -> dict:
     return {"seed": 1, "bias_seeds": None}
 
 
+def draft_layer_weights(dc: DraftConfig, seed: int, layer: int) -> dict:
+    """One draft layer, host numpy (bf16 as uint16): w_qkv [3 H D][d] (q, k, v heads),
+    w_o [d][H D], norm_attn, norm_moe (the FFN's gain) [d], w_gate / w_up [f][d], w_down [d][f]."""
+    d, hd, f = dc.d, dc.heads * dc.hd, dc.f
+    return {
+        "w_qkv": normal_bf16(seed, stream(K_D_QKV, layer), 3 * hd * d, 0, 0.02).reshape(3 * hd, d),
+        "w_o": normal_bf16(seed, stream(K_D_O, layer), d * hd, 0, dc.resid_std).reshape(d, hd),
+        "norm_attn": normal_bf16(seed, stream(K_D_NORM_ATTN, layer), d, 1.0, 0.02),
+        "norm_moe": normal_bf16(seed, stream(K_D_NORM_FFN, layer), d, 1.0, 0.02),
+        "w_gate": normal_bf16(seed, stream(K_D_GATE, layer), f * d, 0, 0.02).reshape(f, d),
+        "w_up": normal_bf16(seed, stream(K_D_UP, layer), f * d, 0, 0.02).reshape(f, d),
+        "w_down": normal_bf16(seed, stream(K_D_DOWN, layer), d * f, 0, dc.resid_std).reshape(d, f),
+    }
+
+
+def draft_final_weights(dc: DraftConfig, seed: int) -> dict:
+    return {"norm_final": normal_bf16(seed, stream(K_D_NORM_FINAL), dc.d, 1.0, 0.02),
+            "w_lm": normal_bf16(seed, stream(K_D_LM), dc.vocab * dc.d, 0, 0.02).reshape(dc.vocab, dc.d)}
+
+
+def draft_hidden_in(dc: DraftConfig, seed: int, step: int = 0) -> np.ndarray:
+    return normal_bf16(seed, stream(K_D_HIDDEN, 0, 0, step), T * dc.d, 0, 1.0).reshape(T, dc.d)
+
+
+def draft_kv_history(dc: DraftConfig, seed: int, layer: int):
+    """K and V caches of one draft layer, [H][max_ctx][D] bf16: rows [0, history) drawn
+    N(0,1) (K taken as already rotated), the rest zero."""
+    out = []
+    for kind in (K_D_KCACHE, K_D_VCACHE):
+        c = np.zeros((dc.heads, dc.max_ctx, dc.hd), np.uint16)
+        for h in range(dc.heads):
+            c[h, :dc.history] = normal_bf16(seed, stream(kind, layer, h), dc.history * dc.hd,
+                                            0, 1.0).reshape(dc.history, dc.hd)
+        out.append(c)
+    return out[0], out[1]
+
+
 # --------------------------------------------------------------------------
 # device upload (torch is used for device memory only)
 # --------------------------------------------------------------------------
@@ -383,6 +460,39 @@ def gpu_kv_history(cfg: Config, seed: int, layer: int, device="cuda"):
         for h in range(cfg.hkv):
             if cfg.history:
                 view = c[h, :cfg.history]
+                _gchk(glib().synth_gpu_normal_bf16(seed, stream(kind, layer, h), view.numel(), 0.0, 1.0,
+                                                   view.data_ptr(), _cur_stream(c)))
+        out.append(c)
+    return out[0], out[1]
+
+
+def gpu_draft_layer_weights(dc: DraftConfig, seed: int, layer: int, device="cuda") -> dict:
+    """draft_layer_weights() drawn directly into device memory (torch tensors)."""
+    d, hd, f = dc.d, dc.heads * dc.hd, dc.f
+    return {
+        "w_qkv": gpu_normal_bf16(seed, stream(K_D_QKV, layer), (3 * hd, d), 0, 0.02, device),
+        "w_o": gpu_normal_bf16(seed, stream(K_D_O, layer), (d, hd), 0, dc.resid_std, device),
+        "norm_attn": gpu_normal_bf16(seed, stream(K_D_NORM_ATTN, layer), (d,), 1.0, 0.02, device),
+        "norm_moe": gpu_normal_bf16(seed, stream(K_D_NORM_FFN, layer), (d,), 1.0, 0.02, device),
+        "w_gate": gpu_normal_bf16(seed, stream(K_D_GATE, layer), (f, d), 0, 0.02, device),
+        "w_up": gpu_normal_bf16(seed, stream(K_D_UP, layer), (f, d), 0, 0.02, device),
+        "w_down": gpu_normal_bf16(seed, stream(K_D_DOWN, layer), (d, f), 0, dc.resid_std, device),
+    }
+
+
+def gpu_draft_final_weights(dc: DraftConfig, seed: int, device="cuda") -> dict:
+    return {"norm_final": gpu_normal_bf16(seed, stream(K_D_NORM_FINAL), (dc.d,), 1.0, 0.02, device),
+            "w_lm": gpu_normal_bf16(seed, stream(K_D_LM), (dc.vocab, dc.d), 0, 0.02, device)}
+
+
+def gpu_draft_kv_history(dc: DraftConfig, seed: int, layer: int, device="cuda"):
+    import torch
+    out = []
+    for kind in (K_D_KCACHE, K_D_VCACHE):
+        c = torch.zeros((dc.heads, dc.max_ctx, dc.hd), dtype=torch.int16, device=device)
+        for h in range(dc.heads):
+            if dc.history:
+                view = c[h, :dc.history]
                 _gchk(glib().synth_gpu_normal_bf16(seed, stream(kind, layer, h), view.numel(), 0.0, 1.0,
                                                    view.data_ptr(), _cur_stream(c)))
         out.append(c)

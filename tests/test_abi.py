@@ -35,7 +35,7 @@ def test_null_arguments_are_rejected_without_a_device():
     assert msm.msm_verify_step(None, 0, list(range(-1, 15)), 0, [0], [0], 0, 0) == msm.MSM_ERR_INVALID_ARG
     assert msm.msm_sync(None) == msm.MSM_ERR_INVALID_ARG
     assert lib.msm_get_stats(None, None) == msm.MSM_ERR_INVALID_ARG
-    assert msm.msm_draft_step(None) == msm.MSM_ERR_UNSUPPORTED
+    assert msm.msm_draft_step(None, 0, 0, [0], [0], 0, 0) == msm.MSM_ERR_INVALID_ARG
     assert msm.msm_verify_step_noalloc(None, 0, list(range(-1, 15)), 0, [0], [0], 0, 0) == msm.MSM_ERR_INVALID_ARG
     assert msm.msm_accept(None, 0, [0] * 16, list(range(-1, 15)), 0, [0], [0], 0) == msm.MSM_ERR_INVALID_ARG
     assert msm.msm_graph_launch(None) == msm.MSM_ERR_INVALID_ARG
@@ -99,3 +99,38 @@ def test_missing_weights_are_rejected():
     w = msm.MsmWeights()
     assert lib.msm_model_create(ctypes.byref(_config()), ctypes.byref(w), 0, ctypes.byref(out)) == \
         msm.MSM_ERR_INVALID_ARG
+
+
+def _draft_config(**kw):
+    c = msm.MsmConfig(d_model=256, n_q_heads=4, n_kv_heads=4, head_dim=64, pool_dim=0, ffn_dim=512, n_experts=0,
+                      top_k=0, n_layers=2, vocab=512, window=0, max_ctx=264, layer_is_global=None, rms_eps=1e-6,
+                      rope_theta=1e4, flags=msm.MSM_FLAG_DRAFT | msm.MSM_FLAG_PDL)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("pool_dim", 256, msm.MSM_ERR_INVALID_ARG),     # a draft model has no MoE half
+    ("n_experts", 32, msm.MSM_ERR_INVALID_ARG),
+    ("vocab", 0, msm.MSM_ERR_INVALID_ARG),          # the proposal needs the LM head
+    ("ffn_dim", 448, msm.MSM_ERR_UNSUPPORTED),      # two staged K halves of 64-column blocks
+    ("head_dim", 96, msm.MSM_ERR_UNSUPPORTED),
+    ("flags", msm.MSM_FLAG_DRAFT | msm.MSM_FLAG_EXPERT_PREFETCH, msm.MSM_ERR_INVALID_ARG),
+])
+def test_draft_config_validation(field, value, code):
+    lib = msm.lib()
+    out = ctypes.c_void_p()
+    w = msm.MsmWeights()
+    assert lib.msm_model_create(ctypes.byref(_draft_config(**{field: value})), ctypes.byref(w), 0,
+                                ctypes.byref(out)) == code
+    assert out.value is None
+
+
+def test_draft_weights_are_required():
+    lib = msm.lib()
+    out = ctypes.c_void_p()
+    w = msm.MsmWeights()
+    assert lib.msm_model_create(ctypes.byref(_draft_config()), ctypes.byref(w), 0, ctypes.byref(out)) == \
+        msm.MSM_ERR_INVALID_ARG
+    assert "draft weights" in msm.msm_last_error()

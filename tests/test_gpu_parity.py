@@ -268,7 +268,12 @@ def test_host_validation_errors():
     rc = msm.msm_verify_step(m.handle, h.data_ptr(), case.parent, case.pos0, [k[0].data_ptr()], [k[0].data_ptr()],
                              0, 0)
     assert rc == msm.MSM_ERR_INVALID_ARG
-    assert msm.msm_draft_step(m.handle) == msm.MSM_ERR_UNSUPPORTED
+    # a target model does not run the draft step
+    lg = torch.empty((T, 16), dtype=torch.float32, device=dev)
+    tok = torch.empty((T,), dtype=torch.int32, device=dev)
+    rc = msm.msm_draft_step(m.handle, h.data_ptr(), case.pos0, [k[0].data_ptr()], [k[0].data_ptr()], lg.data_ptr(),
+                            tok.data_ptr())
+    assert rc == msm.MSM_ERR_INVALID_ARG
     m.close()
 
 
