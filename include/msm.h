@@ -363,9 +363,10 @@ msm_status msm_accept(msm_model* model, const float* logits, const int32_t* toke
  * Arguments are those of msm_verify_step and msm_accept; the tree, the tokens and
  * pos0 are recorded in the graph, as are all buffer addresses, so a replay reads
  * the buffers' current contents at those addresses.  msm_graph_launch replays it
- * on `stream`; every replay computes what the captured calls compute.  The draft
- * step is not part of the graph (not built).  (msm_graph_create_dev below records a
- * device-resident state instead of the tree, tokens and pos0.)  The model must outlive its graphs;
+ * on `stream`; every replay computes what the captured calls compute.
+ * (msm_graph_create_dev below records a device-resident state instead of the tree,
+ * tokens and pos0; msm_graph_create_spec adds the draft step and the embedding of
+ * its proposal, so one graph holds the whole speculative step.)  The model must outlive its graphs;
  * replays of one model must not overlap on the GPU.  msm_graph_destroy frees the
  * graph (NULL is ignored).  Errors: those of the captured calls (nothing is
  * recorded then), MSM_ERR_CUDA for a failed capture or instantiation.
@@ -433,6 +434,54 @@ void msm_graph_destroy(msm_graph* graph);
  */
 msm_status msm_draft_step(msm_model* draft, const void* hidden_in, int32_t pos0, void* const* k_cache,
                           void* const* v_cache, float* logits_out, int32_t* tokens_out, void* stream);
+
+/*
+ * msm_draft_step_dev: msm_draft_step with pos0 read from a device-resident step
+ * state (MSM_STEP_STATE_INTS ints, as for msm_verify_step_dev) when the kernels run;
+ * the proposal goes into the state: parent[i] = i - 1 (the chain) for every i, and
+ * the token of node i = the argmax of slot i for i = 1..15.  The root's token
+ * (state[17]) is the caller's and is not written.  An invalid pos0 makes the layer
+ * launches give up at entry (msm_sync then returns MSM_ERR_INVALID_ARG); the state
+ * is still written, from whatever logits_out held.
+ */
+msm_status msm_draft_step_dev(msm_model* draft, const void* hidden_in, int32_t* state, void* const* k_cache,
+                              void* const* v_cache, float* logits_out, void* stream);
+
+/*
+ * msm_embed_dev: the verify step's input rows from an embedding table, read from a
+ * step state when the kernel runs: hidden_out[i] = table[state[17 + i]] (the token
+ * of tree node i).  The verify step takes its 16 input rows as given (the embedding
+ * precedes it in the pages' decoder); this call lets one graph go from the draft's
+ * proposal to the verify step's input without a host round trip.
+ *   model      the target model (vocab > 0; its d_model and vocab size the table)
+ *   table      device bf16 [vocab][d_model], caller-owned, 16-byte aligned
+ *   hidden_out device bf16 [16][d_model], 16-byte aligned
+ * One launch of 16 blocks on `stream`.  A token id outside [0, vocab) gives a zero
+ * row and MSM_ERR_INVALID_ARG at the next msm_sync (the verify step's own state
+ * check rejects the step then).  Host errors: MSM_ERR_INVALID_ARG (NULL or
+ * misaligned pointers), MSM_ERR_UNSUPPORTED (vocab == 0).
+ */
+msm_status msm_embed_dev(msm_model* model, const void* table, const int32_t* state, void* hidden_out, void* stream);
+
+/*
+ * msm_graph_create_spec: one CUDA graph holding a whole speculative decode step on
+ * a device-resident state (alphasignal.ai, § "Draft and verify share one graph"):
+ *   msm_draft_step_dev(draft, draft_hidden_in, state, draft caches, draft_logits)
+ *   msm_embed_dev(target, embed_table, state, hidden_buf)
+ *   msm_verify_step_dev(target, hidden_buf, state, k_cache, v_cache, logits_out)
+ *   msm_accept_dev(target, logits_out, state, k_cache, v_cache, accept_result)
+ * with both models' exchange buffers armed before and after.  Before each replay
+ * the caller sets state[0] (pos0) and state[17] (the root token, e.g. the previous
+ * step's bonus token) and fills draft_hidden_in; the graph writes the rest of the
+ * state, hidden_buf, both logits and accept_result.  Both models must be on one
+ * device and outlive the graph; replays must not overlap.  Errors: those of the
+ * captured calls, MSM_ERR_INVALID_ARG for a NULL draft, table, hidden_buf, state or
+ * accept_result or models on different devices.
+ */
+msm_status msm_graph_create_spec(msm_model* target, msm_model* draft, const void* draft_hidden_in,
+                                 void* const* draft_k_cache, void* const* draft_v_cache, float* draft_logits,
+                                 const void* embed_table, void* hidden_buf, int32_t* state, void* const* k_cache,
+                                 void* const* v_cache, float* logits_out, int32_t* accept_result, msm_graph** out);
 
 /* Message of the last error on the calling thread ("" if none). */
 const char* msm_last_error(void);

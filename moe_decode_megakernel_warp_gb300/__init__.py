@@ -62,7 +62,7 @@ EXPORTED = ["msm_model_create", "msm_model_destroy", "msm_verify_step", "msm_ver
             "msm_get_routing", "msm_get_tree", "msm_get_timing", "msm_get_stats", "msm_get_exchange",
             "msm_draft_step", "msm_last_error", "msm_verify_step_noalloc", "msm_accept", "msm_graph_create",
             "msm_graph_launch", "msm_graph_destroy", "msm_verify_step_dev", "msm_accept_dev",
-            "msm_graph_create_dev"]
+            "msm_graph_create_dev", "msm_draft_step_dev", "msm_embed_dev", "msm_graph_create_spec"]
 # capacity of the static scratch array behind msm_verify_step_noalloc (MSM_NOALLOC_SCRATCH_BYTES)
 MSM_NOALLOC_SCRATCH_BYTES = 10 << 20
 
@@ -188,6 +188,13 @@ def lib():
             L.msm_graph_destroy.restype = None
             L.msm_draft_step.argtypes = [vp, vp, i32, _PP, _PP, vp, vp, vp]
             L.msm_draft_step.restype = st
+            L.msm_draft_step_dev.argtypes = [vp, vp, vp, _PP, _PP, vp, vp]
+            L.msm_draft_step_dev.restype = st
+            L.msm_embed_dev.argtypes = [vp, vp, vp, vp, vp]
+            L.msm_embed_dev.restype = st
+            L.msm_graph_create_spec.argtypes = [vp, vp, vp, _PP, _PP, vp, vp, vp, vp, _PP, _PP, vp, vp,
+                                                ctypes.POINTER(vp)]
+            L.msm_graph_create_spec.restype = st
             L.msm_last_error.argtypes = []
             L.msm_last_error.restype = ctypes.c_char_p
             _LIB = L
@@ -341,6 +348,33 @@ def msm_draft_step(model, hidden_in, pos0, k_ptrs, v_ptrs, logits_out, tokens_ou
                                 ctypes.c_void_p(tokens_out), ctypes.c_void_p(stream))
 
 
+def msm_draft_step_dev(model, hidden_in, state, k_ptrs, v_ptrs, logits_out, stream=0) -> int:
+    kp, _ka = _ptr_array(k_ptrs)
+    vpp, _va = _ptr_array(v_ptrs)
+    return lib().msm_draft_step_dev(model, ctypes.c_void_p(hidden_in), ctypes.c_void_p(state), kp, vpp,
+                                    ctypes.c_void_p(logits_out), ctypes.c_void_p(stream))
+
+
+def msm_embed_dev(model, table, state, hidden_out, stream=0) -> int:
+    return lib().msm_embed_dev(model, ctypes.c_void_p(table), ctypes.c_void_p(state), ctypes.c_void_p(hidden_out),
+                               ctypes.c_void_p(stream))
+
+
+def msm_graph_create_spec(target, draft, draft_hidden_in, dk_ptrs, dv_ptrs, draft_logits, embed_table, hidden_buf,
+                          state, k_ptrs, v_ptrs, logits_out, accept_result):
+    """Returns the graph handle; raises MsmError on failure."""
+    dkp, _a1 = _ptr_array(dk_ptrs)
+    dvp, _a2 = _ptr_array(dv_ptrs)
+    kp, _a3 = _ptr_array(k_ptrs)
+    vpp, _a4 = _ptr_array(v_ptrs)
+    g = ctypes.c_void_p()
+    _check(lib().msm_graph_create_spec(target, draft, ctypes.c_void_p(draft_hidden_in), dkp, dvp,
+                                       ctypes.c_void_p(draft_logits), ctypes.c_void_p(embed_table),
+                                       ctypes.c_void_p(hidden_buf), ctypes.c_void_p(state), kp, vpp,
+                                       ctypes.c_void_p(logits_out), ctypes.c_void_p(accept_result), ctypes.byref(g)))
+    return g
+
+
 # ---------------------------------------------------------------- torch-facing wrapper
 class Model:
     """A model built from per-layer torch device tensors (caller layouts of msm.h).
@@ -482,6 +516,25 @@ class Model:
                                      [k.data_ptr() for k in k_caches], [v.data_ptr() for v in v_caches],
                                      logits_out.data_ptr(), tokens_out.data_ptr(), stream))
 
+    def draft_step_dev(self, hidden_in, state, k_caches, v_caches, logits_out, stream=0):
+        """msm_draft_step_dev: pos0 from `state`, the proposal (chain + tokens 1..15) written into it."""
+        return _check(msm_draft_step_dev(self.handle, hidden_in.data_ptr(), state.data_ptr(),
+                                         [k.data_ptr() for k in k_caches], [v.data_ptr() for v in v_caches],
+                                         logits_out.data_ptr(), stream))
+
+    def embed_dev(self, table, state, hidden_out, stream=0):
+        return _check(msm_embed_dev(self.handle, table.data_ptr(), state.data_ptr(), hidden_out.data_ptr(), stream))
+
+    def graph_spec(self, draft, draft_hidden_in, draft_k, draft_v, draft_logits, embed_table, hidden_buf, state,
+                   k_caches, v_caches, logits_out, accept_result):
+        """msm_graph_create_spec: draft -> embedding -> verify -> accept in one StepGraph."""
+        g = msm_graph_create_spec(self.handle, draft.handle, draft_hidden_in.data_ptr(),
+                                  [k.data_ptr() for k in draft_k], [v.data_ptr() for v in draft_v],
+                                  draft_logits.data_ptr(), embed_table.data_ptr(), hidden_buf.data_ptr(),
+                                  state.data_ptr(), [k.data_ptr() for k in k_caches], [v.data_ptr() for v in v_caches],
+                                  logits_out.data_ptr(), accept_result.data_ptr())
+        return StepGraph(g, self, keep=draft)
+
     def sync(self, stream=0) -> int:
         return msm_sync(self.handle, stream)
 
@@ -525,10 +578,10 @@ class Model:
 
 
 class StepGraph:
-    """An instantiated step graph (msm_graph); keeps its model alive."""
+    """An instantiated step graph (msm_graph); keeps its model (and a draft model) alive."""
 
-    def __init__(self, handle, model):
-        self.handle, self.model = handle, model
+    def __init__(self, handle, model, keep=None):
+        self.handle, self.model, self.keep = handle, model, keep
 
     def launch(self, stream=0):
         return _check(msm_graph_launch(self.handle, stream))

@@ -181,7 +181,45 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_walk_kernel(const Accep
   }
 }
 
+// The draft's proposal into a device-resident step state: the tree becomes the chain
+// (parent[i] = i - 1) and node i >= 1 takes slot i's greedy choice; the root's token
+// (state[17]) is the caller's and stays.
+__global__ void draft_propose_kernel(const int32_t* __restrict__ choice, int32_t* state) {
+  const int i = threadIdx.x;
+  if (i < kRowsPerThread) {
+    state[1 + i] = i - 1;
+    if (i > 0) state[1 + kRowsPerThread + i] = choice[i];
+  }
+}
+
+// Rows of an embedding table for the 16 tree tokens of a step state: out[i] =
+// table[state[17 + i]]; an id outside [0, vocab) gives a zero row and reports
+// MSM_ERR_INVALID_ARG through the status (the verify step's own state check then
+// gives the step up).  One block per token, 16-byte chunks.
+__global__ void embed_kernel(const uint16_t* __restrict__ table, int vocab, int d, const int32_t* __restrict__ state,
+                             uint16_t* __restrict__ out, DevStatus* status) {
+  const int i = blockIdx.x;
+  const int id = state[1 + kRowsPerThread + i];
+  const bool ok = id >= 0 && id < vocab;
+  if (!ok && threadIdx.x == 0 && status) atomicCAS(&status->code, 0, 1 /* MSM_ERR_INVALID_ARG */);
+  const uint4* src = reinterpret_cast<const uint4*>(table + (size_t)(ok ? id : 0) * d);
+  uint4* dst = reinterpret_cast<uint4*>(out + (size_t)i * d);
+  for (int c = threadIdx.x; c < d / 8; c += blockDim.x) dst[c] = ok ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+}
+
 }  // namespace
+
+cudaError_t launch_draft_propose(const int32_t* choice, int32_t* state, cudaStream_t s) {
+  draft_propose_kernel<<<1, 32, 0, s>>>(choice, state);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_embed(const void* table, int vocab, int d, const int32_t* state, void* out, DevStatus* status,
+                         cudaStream_t s) {
+  embed_kernel<<<kRowsPerThread, 256, 0, s>>>(static_cast<const uint16_t*>(table), vocab, d, state,
+                                              static_cast<uint16_t*>(out), status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_accept_argmax(const float* logits, int vocab, uint64_t* part, int parts, uint32_t* ticket,
                                  int32_t* choice, cudaStream_t s) {

@@ -882,6 +882,47 @@ msm_status msm_get_exchange(msm_model* m, const char* name, void* host, size_t b
 }  // extern "C"
 
 namespace {
+// the draft step: the n_layers layer launches (the block a chain at pos0, or at the
+// state's pos0), the argmax of each slot, and either tokens_out (slot 0 = -1) or the
+// proposal written into the state (the chain and tokens 1..15)
+msm_status enqueue_draft(msm_model* m, const void* hidden_in, int32_t pos0, int32_t* state, void* const* k_cache,
+                         void* const* v_cache, float* logits_out, int32_t* tokens_out, void* stream) {
+  if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
+  if (!logits_out || (!state && !tokens_out))
+    return fail(MSM_ERR_INVALID_ARG, "logits_out and tokens_out (or a state) are required");
+  if ((reinterpret_cast<uintptr_t>(tokens_out) & 3) || (reinterpret_cast<uintptr_t>(state) & 3))
+    return fail(MSM_ERR_INVALID_ARG, "tokens_out and state must be 4-byte aligned");
+  // the slots form a chain (slot i at pos0 + i); the kernels give every slot the whole
+  // block, so the chain only fixes the positions
+  int32_t chain[T];
+  for (int i = 0; i < T; ++i) chain[i] = i - 1;
+  msm_status st = enqueue_verify(m, own_buffers(m), hidden_in, chain, pos0, state, k_cache, v_cache, logits_out,
+                                 nullptr, stream, true);
+  if (st != MSM_OK) return st;
+  // each slot's argmax (the smallest index among equal maxima)
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (state) {
+    CK(launch_accept_argmax(logits_out, m->dm.vocab, m->accept_part, m->G, m->accept_ticket, m->accept_choice, s));
+    CK(launch_draft_propose(m->accept_choice, state, s));
+  } else {
+    CK(launch_accept_argmax(logits_out, m->dm.vocab, m->accept_part, m->G, m->accept_ticket, tokens_out, s));
+    CK(cudaMemsetAsync(tokens_out, 0xFF, sizeof(int32_t), s));
+  }
+  return MSM_OK;
+}
+
+msm_status enqueue_embed(msm_model* m, const void* table, const int32_t* state, void* hidden_out, void* stream) {
+  if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
+  if (!table || !state || !hidden_out) return fail(MSM_ERR_INVALID_ARG, "NULL table, state or hidden_out");
+  if (m->dm.vocab <= 0) return fail(MSM_ERR_UNSUPPORTED, "the embedding needs vocab > 0");
+  if ((reinterpret_cast<uintptr_t>(table) & 15) || (reinterpret_cast<uintptr_t>(hidden_out) & 15) ||
+      (reinterpret_cast<uintptr_t>(state) & 3))
+    return fail(MSM_ERR_INVALID_ARG, "table and hidden_out must be 16-byte and state 4-byte aligned");
+  CK(cudaSetDevice(m->device));
+  CK(launch_embed(table, m->dm.vocab, m->dm.d, state, hidden_out, m->status, static_cast<cudaStream_t>(stream)));
+  return MSM_OK;
+}
+
 msm_status enqueue_accept(msm_model* m, const float* logits, const int32_t* tokens, const int32_t* parent,
                           int32_t pos0, const int32_t* state, void* const* k_cache, void* const* v_cache,
                           int32_t* result, void* stream) {
@@ -970,12 +1011,26 @@ void msm_graph_destroy(msm_graph* g) {
 }  // extern "C"
 
 namespace {
+// the draft model's part of a speculative-step graph
+struct SpecArgs {
+  msm_model* draft;
+  const void* draft_hidden_in;
+  void* const* dk;
+  void* const* dv;
+  float* draft_logits;
+  const void* embed_table;
+  int32_t* state;
+};
+
 msm_status capture_step(msm_model* m, const void* hidden_in, const int32_t* parent, const int32_t* tokens,
                         int32_t pos0, const int32_t* state, void* const* k_cache, void* const* v_cache,
-                        float* logits_out, void* hidden_out, int32_t* accept_result, msm_graph** out) {
+                        float* logits_out, void* hidden_out, int32_t* accept_result, msm_graph** out,
+                        const SpecArgs* spec = nullptr) {
   if (!out) return fail(MSM_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
+  if (spec && spec->draft->device != m->device)
+    return fail(MSM_ERR_INVALID_ARG, "the draft and target models must be on one device");
   CK(cudaSetDevice(m->device));
   cudaStream_t cs = nullptr;
   CK(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
@@ -988,21 +1043,40 @@ msm_status capture_step(msm_model* m, const void* hidden_in, const int32_t* pare
   // again after them, so a replay neither depends on nor leaves behind state that
   // an eager step of either launch parity (odd layer counts) could trip over; the
   // capture leaves the model's launch counters as they were
+  msm_model* const dr = spec ? spec->draft : nullptr;
   const uint64_t launches0 = m->launch_count, steps0 = m->step_count, run0 = m->launches_run;
   uint8_t* const last_x0 = m->last_x;
+  const uint64_t d_launches0 = dr ? dr->launch_count : 0, d_steps0 = dr ? dr->step_count : 0,
+                 d_run0 = dr ? dr->launches_run : 0;
+  uint8_t* const d_last_x0 = dr ? dr->last_x : nullptr;
   msm_status st = rearm_all(m, cs);
+  if (st == MSM_OK && dr) {
+    // draft -> its proposal in the state -> the tokens' embedding rows -> verify -> accept
+    st = rearm_all(dr, cs);
+    if (st == MSM_OK)
+      st = enqueue_draft(dr, spec->draft_hidden_in, 0, spec->state, spec->dk, spec->dv, spec->draft_logits, nullptr,
+                         cs);
+    if (st == MSM_OK) st = enqueue_embed(m, spec->embed_table, spec->state, const_cast<void*>(hidden_in), cs);
+  }
   if (st == MSM_OK)
     st = enqueue_verify(m, own_buffers(m), hidden_in, parent, pos0, state, k_cache, v_cache, logits_out, hidden_out,
                         cs);
   if (st == MSM_OK && accept_result)
     st = enqueue_accept(m, logits_out, tokens, parent, pos0, state, k_cache, v_cache, accept_result, cs);
   if (st == MSM_OK) st = rearm_all(m, cs);
+  if (st == MSM_OK && dr) st = rearm_all(dr, cs);
   // recording runs nothing: the model's launch parity must keep following the
   // launches that did run (a replay arms both parities, so it needs no count)
   m->launch_count = launches0;
   m->step_count = steps0;
   m->launches_run = run0;
   m->last_x = last_x0;
+  if (dr) {
+    dr->launch_count = d_launches0;
+    dr->step_count = d_steps0;
+    dr->launches_run = d_run0;
+    dr->last_x = d_last_x0;
+  }
   std::string msg = st == MSM_OK ? std::string() : std::string(msm_last_error());
   cudaGraph_t graph = nullptr;
   e = cudaStreamEndCapture(cs, &graph);
@@ -1057,21 +1131,29 @@ msm_status msm_graph_launch(msm_graph* g, void* stream) {
 
 msm_status msm_draft_step(msm_model* m, const void* hidden_in, int32_t pos0, void* const* k_cache,
                           void* const* v_cache, float* logits_out, int32_t* tokens_out, void* stream) {
-  if (!m) return fail(MSM_ERR_INVALID_ARG, "model is NULL");
-  if (!logits_out || !tokens_out) return fail(MSM_ERR_INVALID_ARG, "logits_out and tokens_out are required");
-  if (reinterpret_cast<uintptr_t>(tokens_out) & 3) return fail(MSM_ERR_INVALID_ARG, "tokens_out must be 4-byte aligned");
-  // the block's slots form a chain (slot i at pos0 + i); the kernels give every slot
-  // the whole block, so the chain only fixes the positions
-  int32_t chain[T];
-  for (int i = 0; i < T; ++i) chain[i] = i - 1;
-  msm_status st = enqueue_verify(m, own_buffers(m), hidden_in, chain, pos0, nullptr, k_cache, v_cache, logits_out,
-                                 nullptr, stream, true);
-  if (st != MSM_OK) return st;
-  // the proposals: each slot's argmax (smallest index among equal maxima), slot 0 = -1
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  CK(launch_accept_argmax(logits_out, m->dm.vocab, m->accept_part, m->G, m->accept_ticket, tokens_out, s));
-  CK(cudaMemsetAsync(tokens_out, 0xFF, sizeof(int32_t), s));
-  return MSM_OK;
+  return enqueue_draft(m, hidden_in, pos0, nullptr, k_cache, v_cache, logits_out, tokens_out, stream);
+}
+
+msm_status msm_draft_step_dev(msm_model* m, const void* hidden_in, int32_t* state, void* const* k_cache,
+                              void* const* v_cache, float* logits_out, void* stream) {
+  if (!state) return fail(MSM_ERR_INVALID_ARG, "state is NULL");
+  return enqueue_draft(m, hidden_in, 0, state, k_cache, v_cache, logits_out, nullptr, stream);
+}
+
+msm_status msm_embed_dev(msm_model* m, const void* table, const int32_t* state, void* hidden_out, void* stream) {
+  return enqueue_embed(m, table, state, hidden_out, stream);
+}
+
+msm_status msm_graph_create_spec(msm_model* target, msm_model* draft, const void* draft_hidden_in,
+                                 void* const* draft_k_cache, void* const* draft_v_cache, float* draft_logits,
+                                 const void* embed_table, void* hidden_buf, int32_t* state, void* const* k_cache,
+                                 void* const* v_cache, float* logits_out, int32_t* accept_result, msm_graph** out) {
+  if (out) *out = nullptr;
+  if (!draft || !embed_table || !hidden_buf || !state || !accept_result)
+    return fail(MSM_ERR_INVALID_ARG, "draft, embed_table, hidden_buf, state and accept_result are required");
+  SpecArgs sa{draft, draft_hidden_in, draft_k_cache, draft_v_cache, draft_logits, embed_table, state};
+  return capture_step(target, hidden_buf, nullptr, nullptr, 0, state, k_cache, v_cache, logits_out, nullptr,
+                      accept_result, out, &sa);
 }
 
 }  // extern "C"

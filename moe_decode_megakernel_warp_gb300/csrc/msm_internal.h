@@ -250,5 +250,8 @@ struct AcceptParams {
 cudaError_t launch_accept_argmax(const float* logits, int vocab, uint64_t* part, int parts, uint32_t* ticket,
                                  int32_t* choice, cudaStream_t s);
 cudaError_t launch_accept_walk(const AcceptParams& p, int blocks, cudaStream_t s);
+cudaError_t launch_draft_propose(const int32_t* choice, int32_t* state, cudaStream_t s);
+cudaError_t launch_embed(const void* table, int vocab, int d, const int32_t* state, void* out, DevStatus* status,
+                         cudaStream_t s);
 
 }  // namespace msm

@@ -2544,8 +2544,9 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
     int* par = reinterpret_cast<int*>(cx.S.x_ts);
     int pos0 = P.pos0, pv = lane < T ? P.parent[lane] : 0;
     if (P.state != nullptr) {
+      // (a draft model reads only pos0: its block is always the chain)
       pos0 = P.state[0];
-      pv = lane < T ? P.state[1 + lane] : 0;
+      pv = lane < T ? (P.dm.draft ? lane - 1 : P.state[1 + lane]) : 0;
     }
     const bool ok = __all_sync(0xffffffffu, lane >= T || (lane == 0 ? pv == -1 : (pv >= 0 && pv < lane))) &&
                     pos0 >= 0 && pos0 <= P.dm.max_ctx - T;

@@ -40,6 +40,7 @@ K_ROUTE_KEEP, K_ROUTE_PICK = 17, 18
 # the draft model's tensors
 K_D_QKV, K_D_O, K_D_NORM_ATTN, K_D_NORM_FFN, K_D_GATE, K_D_UP, K_D_DOWN = 19, 20, 21, 22, 23, 24, 25
 K_D_NORM_FINAL, K_D_LM, K_D_HIDDEN, K_D_KCACHE, K_D_VCACHE = 26, 27, 28, 29, 30
+K_EMBED = 31  # a token-embedding table for the verify step's input rows
 
 
 def build(force: bool = False) -> str:
@@ -187,7 +188,7 @@ class DraftConfig:
 
 
 DRAFT_SMALL = DraftConfig("2-layer draft at tiny widths (d256, 4 heads of 64, FFN 512)", d=256, heads=4, hd=64,
-                          f=512, n_layers=2, vocab=512, history=200)
+                          f=512, n_layers=2, vocab=1024, history=200)
 DRAFT_FULL = DraftConfig("5-layer draft (d2048, 16 heads of 128, FFN 8192, ctx 8192, vocab 131072)", d=2048,
                          heads=16, hd=128, f=8192, n_layers=5, vocab=131072, history=8192)
 DRAFT_CONFIGS = {"draft_small": DRAFT_SMALL, "draft_full": DRAFT_FULL}
@@ -329,6 +330,11 @@ def draft_layer_weights(dc: DraftConfig, seed: int, layer: int) -> dict:
 def draft_final_weights(dc: DraftConfig, seed: int) -> dict:
     return {"norm_final": normal_bf16(seed, stream(K_D_NORM_FINAL), dc.d, 1.0, 0.02),
             "w_lm": normal_bf16(seed, stream(K_D_LM), dc.vocab * dc.d, 0, 0.02).reshape(dc.vocab, dc.d)}
+
+
+def embed_table(vocab: int, d: int, seed: int) -> np.ndarray:
+    """A token-embedding table [vocab][d] bf16, N(0, 1) (host numpy, uint16)."""
+    return normal_bf16(seed, stream(K_EMBED), vocab * d, 0, 1.0).reshape(vocab, d)
 
 
 def draft_hidden_in(dc: DraftConfig, seed: int, step: int = 0) -> np.ndarray:

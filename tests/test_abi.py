@@ -36,6 +36,10 @@ def test_null_arguments_are_rejected_without_a_device():
     assert msm.msm_sync(None) == msm.MSM_ERR_INVALID_ARG
     assert lib.msm_get_stats(None, None) == msm.MSM_ERR_INVALID_ARG
     assert msm.msm_draft_step(None, 0, 0, [0], [0], 0, 0) == msm.MSM_ERR_INVALID_ARG
+    assert msm.msm_draft_step_dev(None, 0, 0, [0], [0], 0) == msm.MSM_ERR_INVALID_ARG
+    assert msm.msm_embed_dev(None, 0, 0, 0) == msm.MSM_ERR_INVALID_ARG
+    with pytest.raises(msm.MsmError):
+        msm.msm_graph_create_spec(None, None, 0, [0], [0], 0, 0, 0, 0, [0], [0], 0, 0)
     assert msm.msm_verify_step_noalloc(None, 0, list(range(-1, 15)), 0, [0], [0], 0, 0) == msm.MSM_ERR_INVALID_ARG
     assert msm.msm_accept(None, 0, [0] * 16, list(range(-1, 15)), 0, [0], [0], 0) == msm.MSM_ERR_INVALID_ARG
     assert msm.msm_graph_launch(None) == msm.MSM_ERR_INVALID_ARG

@@ -169,3 +169,87 @@ def test_draft_step_full_width_matches_the_oracle():
     ref_logits, ref_tokens, ref_caches = oracle_draft(dc, layers, final, hidden, kv, dc.pos0)
     err, n_clear = check(dc, got_logits, got_tokens, caches, ref_logits, ref_tokens, ref_caches, kv, dc.pos0)
     assert n_clear >= 8, n_clear
+
+
+def test_speculative_step_graph_matches_the_eager_calls():
+    """msm_graph_create_spec: draft -> its proposal in the state -> the tokens' embedding
+    rows -> verify -> accept in one graph, bitwise equal to the same calls issued one by
+    one; the state holds the chain and each slot's argmax, the verify input holds the
+    table rows of the state's tokens, and the accept result follows the oracle's walk
+    on the step's logits."""
+    import torch
+    import moe_decode_megakernel_warp_gb300 as msm
+    from gpu_cases import make_case
+    from oracle import accept as acc
+    dev = torch.device("cuda", 0)
+    case = make_case("cfg1_stack")
+    cfg = case.cfg
+    import dataclasses
+    dc = dataclasses.replace(synth.DRAFT_SMALL, history=cfg.history)  # the draft's cache rows follow the target's
+    assert dc.vocab == cfg.vocab and dc.max_ctx == cfg.max_ctx
+    target = msm.Model(cfg, [synth.to_torch(w, dev) for w in case.layers], synth.to_torch(case.final, dev), device=0)
+    dl = [synth.draft_layer_weights(dc, 3, l) for l in range(dc.n_layers)]
+    draft = msm.Model(dc, [synth.to_torch(w, dev) for w in dl], synth.to_torch(synth.draft_final_weights(dc, 3), dev),
+                      device=0, flags=msm.MSM_FLAG_PDL | msm.MSM_FLAG_DRAFT)
+    table_np = synth.embed_table(cfg.vocab, cfg.d, 7)
+    table = torch.from_numpy(table_np.view(np.int16)).to(dev)
+    dh = torch.from_numpy(synth.draft_hidden_in(dc, 3).view(np.int16)).to(dev)
+    pos0 = cfg.pos0
+    kv0 = [(torch.from_numpy(k.view(np.int16)).to(dev), torch.from_numpy(v.view(np.int16)).to(dev)) for k, v in case.kv]
+    dkv0 = [tuple(torch.from_numpy(x.view(np.int16)).to(dev) for x in synth.draft_kv_history(dc, 3, l))
+            for l in range(dc.n_layers)]
+    state0 = torch.zeros((msm.MSM_STEP_STATE_INTS,), dtype=torch.int32, device=dev)
+    state0[0] = pos0
+    state0[17] = 5  # the root token
+
+    def buffers():
+        return {"kc": [k.clone() for k, _ in kv0], "vc": [v.clone() for _, v in kv0],
+                "dk": [k.clone() for k, _ in dkv0], "dv": [v.clone() for _, v in dkv0], "state": state0.clone(),
+                "hid": torch.empty((T, cfg.d), dtype=torch.int16, device=dev),
+                "dlog": torch.empty((T, dc.vocab), dtype=torch.float32, device=dev),
+                "lg": torch.empty((T, cfg.vocab), dtype=torch.float32, device=dev),
+                "res": torch.empty((msm.MSM_ACCEPT_RESULT_INTS,), dtype=torch.int32, device=dev)}
+
+    def host(b):
+        return {k: ([x.cpu().numpy() for x in v] if isinstance(v, list) else v.cpu().numpy()) for k, v in b.items()}
+
+    e = buffers()
+    draft.draft_step_dev(dh, e["state"], e["dk"], e["dv"], e["dlog"])
+    target.embed_dev(table, e["state"], e["hid"])
+    target.verify_step_dev(e["hid"], e["state"], e["kc"], e["vc"], logits_out=e["lg"])
+    target.accept_dev(e["lg"], e["state"], e["kc"], e["vc"], e["res"])
+    assert draft.sync() == 0 and target.sync() == 0
+    he = host(e)
+    g = buffers()
+    graph = target.graph_spec(draft, dh, g["dk"], g["dv"], g["dlog"], table, g["hid"], g["state"], g["kc"], g["vc"],
+                              g["lg"], g["res"])
+    graph.launch()
+    assert draft.sync() == 0 and target.sync() == 0
+    hg = host(g)
+    for k in he:
+        for x, y in zip(he[k] if isinstance(he[k], list) else [he[k]], hg[k] if isinstance(hg[k], list) else [hg[k]]):
+            assert np.array_equal(x.view(np.uint8), y.view(np.uint8)), k
+    st = he["state"]
+    assert st[0] == pos0 and st[17] == 5
+    assert list(st[1:17]) == [-1] + list(range(15))
+    dlog = he["dlog"]
+    for i in range(1, T):
+        assert st[17 + i] == int(np.argmax(dlog[i]))
+    assert np.array_equal(he["hid"].view(np.uint16), table_np[st[17:33]])
+    path, bonus, choice = acc.greedy_accept(he["lg"], list(st[17:33]), list(st[1:17]))
+    r = he["res"]
+    assert r[0] == len(path) and r[1] == bonus and list(r[2:2 + len(path)]) == list(path)
+    # a second replay with another root token: the graph reads the state's current contents
+    g2 = buffers()
+    graph.close()
+    graph = target.graph_spec(draft, dh, g2["dk"], g2["dv"], g2["dlog"], table, g2["hid"], g2["state"], g2["kc"],
+                              g2["vc"], g2["lg"], g2["res"])
+    g2["state"][17] = 9
+    graph.launch()
+    assert draft.sync() == 0 and target.sync() == 0
+    h2 = host(g2)
+    assert np.array_equal(h2["hid"][0].view(np.uint16), table_np[9])
+    assert np.array_equal(h2["dlog"].view(np.uint32), he["dlog"].view(np.uint32))  # the draft does not read the root
+    graph.close()
+    target.close()
+    draft.close()
