@@ -135,6 +135,9 @@ msm_status validate_draft_config(const msm_config* c) {
   if (c->d_model % 64 || (c->n_q_heads * c->head_dim) % 64)
     return fail(MSM_ERR_UNSUPPORTED, "d_model and n_q_heads*head_dim must be multiples of 64");
   if (c->ffn_dim % 128) return fail(MSM_ERR_UNSUPPORTED, "draft ffn_dim must be a multiple of 128 (two staged K halves)");
+  // each K half's weight tiles must start on a packed 1024-column tile (or lie in one)
+  if (c->ffn_dim > 1024 && c->ffn_dim % 2048)
+    return fail(MSM_ERR_UNSUPPORTED, "draft ffn_dim above 1024 must be a multiple of 2048");
   if (c->vocab % 16) return fail(MSM_ERR_UNSUPPORTED, "vocab must be a multiple of 16");
   if (c->grid_blocks < 0 || c->attn_splits < 0) return fail(MSM_ERR_INVALID_ARG, "config: negative grid_blocks / attn_splits");
   if (c->flags & (MSM_FLAG_EXPERT_PREFETCH | MSM_FLAG_KV_PREFETCH))
@@ -374,9 +377,9 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
 
   CKM(cudaStreamCreateWithFlags(&m->aux, cudaStreamNonBlocking));
   for (int t = 0; t < 2; ++t)
-    CKM(cudaFuncSetAttribute(layer_kernel(t != 0), cudaFuncAttributeMaxDynamicSharedMemorySize, m->smem_bytes));
+    CKM(cudaFuncSetAttribute(layer_kernel(t != 0, draft), cudaFuncAttributeMaxDynamicSharedMemorySize, m->smem_bytes));
   int occ = 0;
-  CKM(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, layer_kernel(false), kThreads, m->smem_bytes));
+  CKM(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, layer_kernel(false, draft), kThreads, m->smem_bytes));
   if (occ < 1) return bail(fail(MSM_ERR_UNSUPPORTED, "the layer kernel does not fit on an SM"));
   // the blocks of a launch wait on each other (phase counters, handoff slots), so all of
   // them must be resident at once: one block per SM, at most one per SM of the device
@@ -740,7 +743,7 @@ msm_status enqueue_verify(msm_model* m, const StepBuffers& B, const void* hidden
     lc.attrs = na ? attr : nullptr;
     lc.numAttrs = na;
     void* args[] = {&P};
-    cudaError_t e = cudaLaunchKernelExC(&lc, layer_kernel(timing), args);
+    cudaError_t e = cudaLaunchKernelExC(&lc, layer_kernel(timing, dm.draft != 0), args);
     if (e != cudaSuccess) return cuda_fail(e, "layer kernel launch");
     if (B.model_owned) ++m->launch_count;
     ++m->launches_run;

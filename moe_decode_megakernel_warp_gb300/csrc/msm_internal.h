@@ -15,7 +15,8 @@ constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kSlots = 12;            // descriptors of the variable-size ring
 constexpr int kDenseTileSteps = 64;   // 16-row x 1024-column bf16 tiles: 64 k-steps x 512 B
-constexpr int kKStepBytes = 512;      // one 16x16 bf16 (or f16) block in ldmatrix order
+constexpr int kKStepBytes = 512;      // one 16x16 bf16 block: its 32 threads' m16n8k16 A fragments
+constexpr int kDenseTmemSlots = 8;    // dense weight tiles held in tensor memory at once
 // NVFP4 expert tiles: 128 rows x tk columns (tk = 512 where the width allows, else 256):
 // tk / 256 column blocks of 128 rows x 128 code bytes in the 128-byte swizzle layout
 // (16 KB each), then the UE4M3 block scales as tk / 64 groups of 512 bytes, one per K=64
@@ -72,7 +73,8 @@ enum TimingEvent : int {
 enum Phase : int {
   PH_START = 0, PH_PROLOGUE = 1, PH_ATTN = 2, PH_ATTN_MERGE = 3, PH_OPROJ = 4, PH_POOL = 5,
   PH_ROUTER = 6, PH_ROUTE = 7, PH_GEMM1 = 8, PH_GEMM2 = 9, PH_COMBINE = 10, PH_UNPOOL = 11,
-  PH_TAIL = 12, PH_END = 13
+  PH_TAIL = 12, PH_END = 13,
+  PH_TC_DENSE = 14  // the tensor-core warp moving dense weight tiles into tensor memory
 };
 
 // device status word
@@ -229,7 +231,7 @@ __host__ __device__ inline uint64_t b1_ts_off(int p) { return b1_code_off(p) + b
 __host__ __device__ inline uint64_t b1_bytes(int p) { return b1_ts_off(p) + 256; }
 
 // kernel entry points (defined in msm_kernel.cu / msm_pack.cu)
-const void* layer_kernel(bool timing);
+const void* layer_kernel(bool timing, bool draft);  // the layer kernel's four instantiations
 
 // accept step (msm_accept.cu): argmax partials [16][parts] of the 16 logit rows
 // reduced by the last block to the 16 choices, then the walk + K/V compaction, up to kAcceptLayers layers per launch (the

@@ -61,7 +61,12 @@ struct Smem {
   uint64_t* tcbar;    // tensor-core pipeline barriers (TcBar)
   uint32_t* tmem_base;  // tensor-memory columns of the block (written by the allocating warp)
   uint32_t* tc_ti;      // [1]: first ring tile of GEMM2 (for the tensor-core warp)
+  uint32_t* dq_e;       // [kDenseQ] the loader's hand-over queue to the tensor-core warp:
+  volatile uint32_t* dq_seq;  // dense tiles (ring index | 2 KB chunks << 24) and markers
 };
+constexpr int kDenseQ = 32;
+constexpr uint32_t kDqRoute = 0xFFFFFFFEu;  // marker: the loader waits for the routing now
+constexpr uint32_t kDqEnd = 0xFFFFFFFFu;    // marker: the launch's stream is done
 
 // Tensor-core pipeline of the expert GEMMs: mbarriers between the tensor-core warp (MMA
 // and scale-copy issue) and the compute warp groups (operand staging, epilogues).
@@ -78,10 +83,13 @@ enum TcBar : int {
   TB_B1 = 16,        // GEMM1's operand B has landed in the activation buffer (transaction count)
   TB_SFA_FULL = 17,  // [4] a tile's weight scales are in a scale buffer (4 warps)
   TB_SFB1 = 21,      // GEMM1's operand-B scales are in tensor memory (commit)
-  TB_SLOT = 22,      // [kSlots] the MMAs of the expert tile in a ring slot are done (commit):
-                     // the loader's release of expert tiles (one commit, where the other
-                     // tiles' consumers arrive on the slot's `empty` barrier eight times)
-  kTcBars = TB_SLOT + kSlots
+  TB_SLOT = 22,      // [kSlots] the tensor-core reads of the weight tile in a ring slot are
+                     // done (commit): the loader's release of expert and dense tiles (one
+                     // commit; the KV tiles' consumers arrive on the slot's `empty` barrier)
+  TB_TFULL = TB_SLOT + kSlots,           // [kDenseTmemSlots] a dense tile is in tensor memory (commit)
+  TB_TFREE = TB_TFULL + kDenseTmemSlots,  // [kDenseTmemSlots] ... read by the 4 warps of its group
+  TB_XDONE = TB_TFREE + kDenseTmemSlots,  // the expert phases' tensor-memory reads are done (8 warps)
+  kTcBars
 };
 // tensor-memory columns (512 allocated: one block per SM).  GEMM2 reuses GEMM1's
 // operand-scale and accumulator columns: its first tensor-memory write follows every
@@ -92,6 +100,11 @@ constexpr uint32_t TM_SFA = 128;   // 4 x 32: weight scales of a tile (up to 8 K
 constexpr uint32_t TM_D1 = 256;    // 2 x 64: GEMM1 accumulators, column term * 16 + token
 constexpr uint32_t TM_SFB2 = 0;    // 2 x 64: GEMM2 activation scales of a round's two experts
 constexpr uint32_t TM_D2 = 256;    // 2 x 16: GEMM2 accumulators
+// Outside the expert phases all 512 columns hold dense weight tiles: slot j (64 columns)
+// takes the block's dense tiles di = j, j + 8, ...; lane 32 q + t, columns 4c .. 4c + 3
+// hold the A fragment of k-step 4c + q as thread t of warp q reads it (the packed layout)
+constexpr uint32_t kDenseTmemCols = 64;
+static_assert(kDenseTmemSlots * kDenseTmemCols == kTmemCols, "dense tiles fill the tensor memory");
 
 constexpr int kRingStateOff = 6656;  // in the small area, below the GEMM2 row scales
 constexpr int kATsOff = 7936;        // [2][16] floats, below the reduction scratch at 8192
@@ -126,6 +139,8 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const LaunchParams& P) {
   s.tc_ti = reinterpret_cast<uint32_t*>(sm + 7416);
   s.tmem_base = reinterpret_cast<uint32_t*>(sm + 7420);
   s.tcbar = reinterpret_cast<uint64_t*>(sm + 7424);
+  s.dq_e = reinterpret_cast<uint32_t*>(sm + 7040);
+  s.dq_seq = reinterpret_cast<volatile uint32_t*>(sm + 7168);
   return s;
 }
 
@@ -342,7 +357,8 @@ struct Ring {
   bool sfb_free;      // ... and GEMM1's operand-B scale groups above it
   RunAhead* ra;       // L2 run-ahead state (shared memory)
 };
-static_assert(kRingStateOff + sizeof(RunAhead) <= 7416, "run-ahead state overlaps the tensor-core barriers");
+static_assert(kRingStateOff + sizeof(RunAhead) <= 7040, "run-ahead state overlaps the dense hand-over queue");
+static_assert(7168 + kDenseQ * 4 <= 7416, "dense hand-over queue overlaps the tensor-core barriers");
 static_assert(7424 + kTcBars * 8 <= kATsOff, "tensor-core barriers overlap the GEMM2 row scales");
 static_assert(TM_SFB1 + 2048 / 64 * 4 <= TM_SFA && TM_SFB2 + 2 * 64 <= TM_SFA && TM_SFA + 4 * 32 <= TM_D1 &&
               TM_D1 + 2 * kSplitRows <= kTmemCols && TM_D2 + 32 <= kTmemCols, "tensor-memory map");
@@ -498,7 +514,16 @@ struct TileStream {
     ub = (uint64_t)exp_tile_bytes(K);
     W = w;
   }
-  // TS_TILE: src / bytes set; TS_KV: kv_row set; else a wait or the end
+  // the launch's stream starts with segment 0: the prologue QKV (launch 0 only)
+  __device__ void begin(const LaunchParams& P) {
+    seg = 0;
+    lo = hi = u = k0 = half = kb = 0;
+    if (P.first) dense(P.w_qkv_pro, P.dm.d, P.dm.nqkv, P.phase_rot * 1);
+  }
+  // TS_TILE: src / bytes set; TS_KV: kv_row set; else a wait or the end.  kDraft: the
+  // stream of a draft model's launch (a separate kernel, so that the target's carries
+  // none of the draft's code)
+  template <bool kDraft>
   __device__ __forceinline__ int next(const Ctx& cx, const uint8_t*& src, uint32_t& bytes, int& kv_row) {
     const LaunchParams& P = *cx.P;
     const Dims& dm = P.dm;
@@ -555,25 +580,25 @@ struct TileStream {
         // a draft model: 4 = the FFN's paired gate/up rows, 5 and 6 = the two K halves of
         // its down projection; no expert segments and no unpooler
         case 4:
-          if (dm.draft) dense(P.w_up, dm.d, 2 * dm.f, P.phase_rot * 4);
+          if (kDraft) dense(P.w_up, dm.d, 2 * dm.f, P.phase_rot * 4);
           else dense(P.w_pool, dm.d, dm.p, P.phase_rot * 4);
           break;
         case 5:
-          if (dm.draft) dense_half(P.w_down, dm.f, dm.d, P.phase_rot * 5, 0);
+          if (kDraft) dense_half(P.w_down, dm.f, dm.d, P.phase_rot * 5, 0);
           else dense(P.w_router, dm.p, dm.e, P.phase_rot * 5);
           break;
         case 6:
-          if (!dm.draft) return TS_ROUTE_WAIT;
+          if (!kDraft) return TS_ROUTE_WAIT;
           dense_half(P.w_down, dm.f, dm.d, P.phase_rot * 5, 1);
           break;
         case 7:
-          if (!dm.draft) experts(P.w1, *cx.S.n_active * w1_units(dm.f), w1_units(dm.f), dm.p, P.phase_rot * 6);
+          if (!kDraft) experts(P.w1, *cx.S.n_active * w1_units(dm.f), w1_units(dm.f), dm.p, P.phase_rot * 6);
           break;
         case 8:
-          if (!dm.draft) experts(P.w2, *cx.S.n_active * w2_units(dm.p), w2_units(dm.p), dm.f, P.phase_rot * 7);
+          if (!kDraft) experts(P.w2, *cx.S.n_active * w2_units(dm.p), w2_units(dm.p), dm.f, P.phase_rot * 7);
           break;
         case 9:
-          if (!dm.draft) dense(P.w_unpool, dm.p, dm.d, P.phase_rot * 8);
+          if (!kDraft) dense(P.w_unpool, dm.p, dm.d, P.phase_rot * 8);
           break;
         case 10:
           if (!P.last) dense(P.w_tail, dm.d, dm.nqkv, P.phase_rot * 9);
@@ -585,7 +610,15 @@ struct TileStream {
   }
 };
 
-template <bool kTiming>
+// an entry of the dense hand-over queue (the loader's q-th): written, then published
+__device__ __forceinline__ void dq_push(Ctx& cx, uint32_t& q, uint32_t e) {
+  const uint32_t k = q % kDenseQ;
+  cx.S.dq_e[k] = e;
+  __threadfence_block();
+  cx.S.dq_seq[k] = ++q;
+}
+
+template <bool kTiming, bool kDraft>
 __device__ void loader(Ctx& cx) {
   const LaunchParams& P = *cx.P;
   const Dims& dm = P.dm;
@@ -604,23 +637,22 @@ __device__ void loader(Ctx& cx) {
   r.ra = cx.S.ring_state;
   r.ra->init(P.runahead_bytes);
   r.ra_on = P.runahead_bytes != 0;
-  TileStream ts;
-  ts.seg = 0;
-  ts.lo = ts.hi = ts.u = ts.k0 = ts.half = ts.kb = 0;
   // segment 0: the prologue QKV (launch 0); weights and KV rows do not depend on the
   // previous launch, so they stream before the dependency wait
-  if (P.first) ts.dense(P.w_qkv_pro, dm.d, dm.nqkv, P.phase_rot * 1);
+  TileStream ts;
+  ts.begin(P);
   if (r.ra_on) {
     const AttnUnit au = attn_unit(P, cx.pos0, rot_block(cx.block, P.phase_rot * 2, gridDim.x), P.is_global);
     ra_front(P, r.ra, cx.block, au.valid ? au.r0 : 0, au.valid ? au.r1 : 0, au.hk);
   }
   bool ok = true;
   int g1_last = -1;
+  uint32_t dq = 0;  // entries of the dense hand-over queue
   while (ok) {
     const uint8_t* src = nullptr;
     uint32_t bytes = 0;
     int kv_row = 0;
-    const int st = ts.next(cx, src, bytes, kv_row);
+    const int st = ts.template next<kDraft>(cx, src, bytes, kv_row);
     if (st == TS_END) break;
     if (st == TS_DEP_WAIT) {
       // the deadline of the bounded waits starts once the previous launch is done
@@ -630,6 +662,7 @@ __device__ void loader(Ctx& cx) {
     }
     if (st == TS_ROUTE_WAIT) {
       // expert tiles wait for this block's routing decision
+      dq_push(cx, dq, kDqRoute);
       ok = wait_bar(cx, cx.S.route_bar, 0, PH_ROUTE);
       stamp<kTiming>(P, cx.block, EV_LOADER_ROUTED);
       if (ok && r.ra_on) ra_back(P, r.ra, cx.block, *cx.S.n_active);
@@ -664,7 +697,7 @@ __device__ void loader(Ctx& cx) {
     }
     if (g1i < 16) stamp_any(P, EV_LD_G1_PLACED + g1i);
     const uint32_t s = r.issued % kSlots;
-    if (ts.seg == 7 || ts.seg == 8) r.xmask |= 1u << s;
+    if (st == TS_TILE) r.xmask |= 1u << s;  // weight tiles: released by the tensor-core warp
     else r.xmask &= ~(1u << s);
     cx.S.slot_off[s] = off;
     cx.S.slot_tile[s] = r.issued;
@@ -678,6 +711,8 @@ __device__ void loader(Ctx& cx) {
       }
     } else {
       bulk_g2s(cx.S.ring + off, src, bytes, &cx.S.full[s], pol);
+      // a dense tile goes on to tensor memory through the tensor-core warp
+      if (ts.seg != 7 && ts.seg != 8) dq_push(cx, dq, r.issued | ((bytes / 2048u) << 24));
     }
     ++r.issued;
     if (g1i < 16) stamp_any(P, EV_LD_G1_ISSUED + g1i);
@@ -695,6 +730,7 @@ __device__ void loader(Ctx& cx) {
     }
   }
   stamp<kTiming>(P, cx.block, EV_LOADER_END);
+  dq_push(cx, dq, kDqEnd);
   if (!ok) {
     // give every copy still in flight a chance to land before the block exits
     cx.deadline = globaltimer() + 20000000ull;
@@ -716,6 +752,7 @@ struct Worker {
   Ctx* cx;
   int cw, lane, g, q;
   uint32_t ti;  // next tile index of the block's sequence
+  uint32_t di;  // next dense tile (tensor-memory hand-over) of the block's sequence
   bool ok;
   bool b1;      // this thread issued the copy of GEMM1's operand B
   uint32_t xseq;  // expert tiles of the block before GEMM2's first (weight-scale buffer rotation)
@@ -1065,11 +1102,14 @@ __device__ void dense_epi(const LaunchParams& P, const Smem& S, const EpiArgs& e
 // Dense phase: out[16 tokens][N] = act[16][K] . W[N][K]^T over this block's
 // 16-row units.  The two warp groups take alternate units (unit lo + i by group i & 1),
 // so one group's cross-warp sum and epilogue overlap the other group's MMAs on the
-// next unit.  Inside a group, warp wi takes k-steps 16 wi .. 16 wi + 15 of every tile
-// of the unit, so no warp carries a long dependent MMA chain; each unit ends with the
-// sum of the group's four partials in fixed warp order (the result does not depend on
-// the grid size or the group) and an epilogue over (row pair, token):
-// dense_epi(unit, p, t, row p value, row p+8 value), run by the group's 128 threads.
+// next unit.  The weight tiles come from tensor memory, where the tensor-core warp
+// copies each one as it lands (so the ring's space goes back to the loader at once and
+// the block holds up to 8 tiles beyond it): warp wi of the group reads its lane quadrant
+// of the tile's slot, the A fragments of k-steps wi, wi + 4, ... (tcgen05.ld), and runs
+// their MMAs against the staged activation; each unit ends with the sum of the group's
+// four partials in fixed warp order (the result does not depend on the grid size or the
+// group) and an epilogue over (row pair, token): dense_epi(unit, p, t, row p value,
+// row p+8 value), run by the group's 128 threads.
 __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, const EpiArgs& ea,
                                          int trace, uint32_t aoff = 0) {
   Ctx& cx = *w.cx;
@@ -1083,18 +1123,18 @@ __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, 
   // tile held by all eight warps at once would be released only after one warp's whole
   // dependent MMA chain).  k-step & 3 is the loop index & 3.
   const int group = w.cw >> 2, wi = w.cw & 3;
-  constexpr int kStepsPerWarp = kDenseTileSteps / 4;
   // lane l addresses row l & 7 of matrix m = l >> 3 (tokens 8 (m >> 1) .., columns
-  // 8 (m & 1) .. of the k-step); k-step ks sits in 64-column block ks >> 2
-  uint32_t act_lane[4];
-#pragma unroll
-  for (int ii = 0; ii < 4; ++ii) {
+  // 8 (m & 1) .. of the k-step); k-step ks sits at 16-column position ks & 3 (= wi for
+  // this warp's k-steps) of 64-column block ks >> 2
+  uint32_t act_lane;
+  {
     const int m = w.lane >> 3, t = (m >> 1) * 8 + (w.lane & 7);
-    act_lane[ii] = smem_u32(cx.S.act + aoff) + act_chunk(t, ii * 2 + (m & 1));
+    act_lane = smem_u32(cx.S.act + aoff) + act_chunk(t, wi * 2 + (m & 1));
   }
+  // this warp's lane quadrant of the dense slots
+  const uint32_t tq = *cx.S.tmem_base + ((uint32_t)(wi * 32) << 16);
   float* red = cx.S.dred;  // [8 warps][16 rows][16 tokens]
   const int tig = wi * 32 + w.lane;  // thread in group
-  const int ks_lo = wi * kStepsPerWarp;
   // the residual inputs of the o_proj / unpooler epilogues do not depend on this phase:
   // read them for the group's first units now, while the tiles stream in
   constexpr int kPreUnits = 2;
@@ -1120,30 +1160,41 @@ __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, 
     float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // odd k-steps
     // the loader streams the units in pairs, their tiles alternating
     const bool paired = (loc | 1) < hi - lo;
-    const uint32_t t0 = w.ti + (uint32_t)((loc >> 1) * 2 * ktiles + (paired ? (loc & 1) : 0));
+    const uint32_t d0 = w.di + (uint32_t)((loc >> 1) * 2 * ktiles + (paired ? (loc & 1) : 0));
     for (int kt = 0; kt < ktiles; ++kt) {
-      const uint32_t t = t0 + (uint32_t)(paired ? 2 * kt : kt);
-      const uint32_t s = t % kSlots;
-      if (w.ok) w.ok = wait_tile(cx, t, 50);
+      const uint32_t dd = d0 + (uint32_t)(paired ? 2 * kt : kt);
+      const uint32_t j = dd % kDenseTmemSlots;
+      if (w.ok) w.ok = wait_bar(cx, &cx.S.tcbar[TB_TFULL + j], (dd / kDenseTmemSlots) & 1, 50);
       if (trace >= 0 && loc < 2 && tig == 0 && (kt == 0 || kt + 1 == ktiles)) stamp_any(*cx.P, trace + loc * 4 + (kt == 0 ? 0 : 1));
       if (w.ok) {
-        const uint32_t wbase = smem_u32(cx.S.ring + cx.S.slot_off[s]) + lane_mat_off(w.lane);
+        tc_fence_after();
         const int k0 = kt * kDenseTileSteps;
-        const int ns = min(kDenseTileSteps, steps - k0);
-        const int ke = min(ns, ks_lo + kStepsPerWarp);
+        const int nc = min(kDenseTileSteps, steps - k0) >> 2;  // k-steps of this warp in the tile
+        const uint32_t bb = act_lane + (uint32_t)(k0 >> 2) * kActBlockBytes;
+        // two halves of 8 k-steps: the slot goes back once both are in registers
 #pragma unroll
-        for (int ii = 0; ii < kStepsPerWarp; ++ii) {
-          const int i = ks_lo + ii;
-          if (i >= ke) break;
-          uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-          ldsm_x4(wbase + i * kKStepBytes, a0, a1, a2, a3);
-          ldsm_x4(act_lane[ii & 3] + (uint32_t)((k0 + i) >> 2) * kActBlockBytes, b0, b1, b2, b3);
-          float(&c)[2][4] = (ii & 1) ? acc2 : acc;
-          mma_bf16(c[0], a0, a1, a2, a3, b0, b1);
-          mma_bf16(c[1], a0, a1, a2, a3, b2, b3);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t a[32];
+          if (h == 0 || nc > 8) {
+            tmem_ld32(tq + j * kDenseTmemCols + 32 * h, a);
+            tmem_ld_wait();
+          }
+          if (h == (nc > 8 ? 1 : 0)) {  // the tile's last tensor-memory read by this warp
+            tc_fence_before();
+            __syncwarp();
+            if (w.lane == 0) mbar_arrive(&cx.S.tcbar[TB_TFREE + j], 1);
+          }
+#pragma unroll
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const int c = h * 8 + c8;
+            if (c >= nc) break;
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(bb + (uint32_t)c * kActBlockBytes, b0, b1, b2, b3);
+            float(&cc)[2][4] = (c8 & 1) ? acc2 : acc;
+            mma_bf16(cc[0], a[4 * c8], a[4 * c8 + 1], a[4 * c8 + 2], a[4 * c8 + 3], b0, b1);
+            mma_bf16(cc[1], a[4 * c8], a[4 * c8 + 1], a[4 * c8 + 2], a[4 * c8 + 3], b2, b3);
+          }
         }
-        __syncwarp();
-        if (w.lane == 0) mbar_arrive(&cx.S.empty[s], kComputeWarps / 4);
       }
     }
 #pragma unroll
@@ -1181,6 +1232,7 @@ __device__ void dense_phase(Worker& w, const int K, const int N, const int rot, 
   // both groups' epilogues are stored before the phase is published
   cbar();
   w.ti += (uint32_t)((hi - lo) * ktiles);
+  w.di += (uint32_t)((hi - lo) * ktiles);
 }
 
 // ---------------------------------------------------------------------------
@@ -2134,14 +2186,65 @@ __device__ __forceinline__ void tile_done(Ctx& cx, uint32_t seq, uint32_t t) {
   tc_commit(&cx.S.tcbar[TB_SLOT + t % kSlots]);
 }
 
+// The block's dense weight tiles, in the loader's order (its hand-over queue): each goes
+// from its ring slot to tensor-memory slot di % 8 with 128x256b copies as soon as it
+// lands, which releases the ring slot (one commit) and hands the tile to its consumers
+// (another); the slot is reused once the tile eight before has been read.  Returns at
+// the loader's routing-wait or end marker.
+__device__ uint32_t dense_queue(Ctx& cx, uint32_t& q, uint32_t& di, bool& ok) {
+  uint64_t* tb = cx.S.tcbar;
+  const uint32_t tm = *cx.S.tmem_base;
+  for (;;) {
+    const uint32_t k = q % kDenseQ;
+    uint32_t n = 0;
+    while (cx.S.dq_seq[k] != q + 1) {
+      __nanosleep(32);
+      if ((++n & 15) == 0 && cx.expired(PH_TC_DENSE)) {
+        ok = false;
+        return kDqEnd;
+      }
+    }
+    __threadfence_block();
+    const uint32_t e = cx.S.dq_e[k];
+    ++q;
+    if (e == kDqRoute || e == kDqEnd) return e;
+    const uint32_t ti = e & 0xFFFFFFu, chunks = e >> 24;
+    const uint32_t j = di % kDenseTmemSlots;
+    if (di >= kDenseTmemSlots) ok = wait_bar(cx, &tb[TB_TFREE + j], ((di / kDenseTmemSlots) - 1) & 1, PH_TC_DENSE);
+    const uint32_t s = ti % kSlots;
+    if (ok) ok = wait_bar(cx, &cx.S.full[s], (ti / kSlots) & 1, PH_TC_DENSE);
+    if (!ok) return kDqEnd;
+    tc_fence_after();
+    const uint32_t a_s = smem_u32(cx.S.ring + cx.S.slot_off[s]);
+    for (uint32_t c = 0; c < chunks; c += 2)  // two 2 KB chunks per copy
+      tc_cp_128x256b(tm + j * kDenseTmemCols + 4 * c, sdesc_kmajor(a_s + c * 2048u, 2048, 128));
+    tc_commit(&tb[TB_SLOT + s]);
+    tc_commit(&tb[TB_TFULL + j]);
+    ++di;
+  }
+}
+// every dense tile handed over so far has been read (before other tensor-memory use)
+__device__ bool dense_drain(Ctx& cx, uint32_t di) {
+  for (uint32_t d = di > (uint32_t)kDenseTmemSlots ? di - kDenseTmemSlots : 0u; d < di; ++d)
+    if (!wait_bar(cx, &cx.S.tcbar[TB_TFREE + d % kDenseTmemSlots], (d / kDenseTmemSlots) & 1, PH_TC_DENSE))
+      return false;
+  tc_fence_after();
+  return true;
+}
+
 __device__ void tc_issuer(Ctx& cx) {
   const LaunchParams& P = *cx.P;
   const Dims& dm = P.dm;
   uint64_t* tb = cx.S.tcbar;
   const uint32_t tm = *cx.S.tmem_base;
   const int G = gridDim.x;
-  bool ok = wait_bar(cx, &tb[TB_ROUTED], 0, PH_ROUTE);
-  if (ok) {
+  // dense tiles up to the routing decision (a draft model: the whole launch)
+  uint32_t q = 0, di = 0;
+  bool ok = true;
+  const uint32_t m0 = dense_queue(cx, q, di, ok);
+  // the expert phases: their tensor-memory columns once every dense tile is read
+  if (ok && m0 == kDqRoute) ok = dense_drain(cx, di) && wait_bar(cx, &tb[TB_ROUTED], 0, PH_ROUTE);
+  if (ok && m0 == kDqRoute) {
     const int na = *cx.S.n_active;
     uint32_t seq = 0;                 // expert tiles issued so far
     const uint32_t t1 = *cx.S.tc_ti;  // ring index of the block's first expert tile
@@ -2237,6 +2340,13 @@ __device__ void tc_issuer(Ctx& cx) {
           }
         }
       }
+    }
+    // the unpooler and the next layer's QKV (or the LM head): dense tiles again, once the
+    // compute warps are done with the expert phases' tensor memory
+    if (ok) ok = wait_bar(cx, &tb[TB_XDONE], 0, PH_TC_DENSE);
+    if (ok) {
+      tc_fence_after();
+      dense_queue(cx, q, di, ok);
     }
   }
   tc_drain(&tb[TB_DRAIN]);
@@ -2367,7 +2477,7 @@ __device__ void draft_ffn(Worker& w) {
 // ---------------------------------------------------------------------------
 // the compute warps' sequence of one launch
 // ---------------------------------------------------------------------------
-template <bool kTiming>
+template <bool kTiming, bool kDraft>
 __device__ void compute_main(Worker& w) {
   Ctx& cx = *w.cx;
   const LaunchParams& P = *cx.P;
@@ -2411,7 +2521,7 @@ __device__ void compute_main(Worker& w) {
     publish(w, CNT_OPROJ);
     stamp<kTiming>(P, b, EV_OPROJ_DONE);
   }
-  if (dm.draft) {
+  if constexpr (kDraft) {
     draft_ffn(w);
   } else {
   // a5: u = bf16(bf16(RMSNorm(h1)) W_pool^T)
@@ -2452,6 +2562,10 @@ __device__ void compute_main(Worker& w) {
   gemm1_phase(w);
   stamp<kTiming>(P, b, EV_GEMM1_DONE);
   gemm2_phase(w);
+  // the expert phases' tensor-memory reads are done: the dense tiles may come back
+  tc_fence_before();
+  __syncwarp();
+  if (w.lane == 0) mbar_arrive(&cx.S.tcbar[TB_XDONE], 1);
   publish(w, CNT_GEMM2);
   stamp<kTiming>(P, b, EV_GEMM2_DONE);
   // move the next layer's KV history toward L2 while the combine waits
@@ -2510,7 +2624,7 @@ __device__ void compute_main(Worker& w) {
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <bool kTiming>
+template <bool kTiming, bool kDraft>
 __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_constant__ LaunchParams P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -2528,10 +2642,11 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
     mbar_init(cx.S.stage_bar, 1);
     for (int i = 0; i < kTcBars; ++i) {
       const bool by4 = (i >= TB_D1_FREE && i < TB_D1_FREE + 2) || (i >= TB_D2_FREE && i < TB_D2_FREE + 2) ||
-                       (i >= TB_SFA_FULL && i < TB_SFA_FULL + 4);
-      mbar_init(&cx.S.tcbar[i], i == TB_DONE ? kComputeWarps : by4 ? 4 : 1);
+                       (i >= TB_SFA_FULL && i < TB_SFA_FULL + 4) || (i >= TB_TFREE && i < TB_TFREE + kDenseTmemSlots);
+      mbar_init(&cx.S.tcbar[i], (i == TB_DONE || i == TB_XDONE) ? kComputeWarps : by4 ? 4 : 1);
     }
     for (int i = 0; i < kSlots; ++i) cx.S.slot_tile[i] = 0xFFFFFFFFu;
+    for (int i = 0; i < kDenseQ; ++i) cx.S.dq_seq[i] = 0u;
     *cx.S.abort = (smem_u32(smem) & 1023u) != 0u;  // the swizzled tiles need 1 KB alignment
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -2546,7 +2661,7 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
     if (P.state != nullptr) {
       // (a draft model reads only pos0: its block is always the chain)
       pos0 = P.state[0];
-      pv = lane < T ? (P.dm.draft ? lane - 1 : P.state[1 + lane]) : 0;
+      pv = lane < T ? (kDraft ? lane - 1 : P.state[1 + lane]) : 0;
     }
     const bool ok = __all_sync(0xffffffffu, lane >= T || (lane == 0 ? pv == -1 : (pv >= 0 && pv < lane))) &&
                     pos0 >= 0 && pos0 <= P.dm.max_ctx - T;
@@ -2563,7 +2678,7 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
         if (j != lane) ++dep;
       }
       // (a draft model's block is a chain whose slots all see one another)
-      cx.S.anc[lane] = P.dm.draft ? 0xFFFFu : m;
+      cx.S.anc[lane] = kDraft ? 0xFFFFu : m;
       cx.S.depth[lane] = dep;
       cx.S.tpos[lane] = pos0 + dep;
     }
@@ -2585,7 +2700,7 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
     return;
   }
   if (warp == kLoaderWarp) {
-    if (lane == 0) loader<kTiming>(cx);
+    if (lane == 0) loader<kTiming, kDraft>(cx);
     pdl_launch_dependents();
     return;
   }
@@ -2598,7 +2713,7 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
   if (warp == 2) {
     pdl_wait();
     cx.deadline = globaltimer() + (((uint64_t)P.timeout_ns_hi << 32) | P.timeout_ns_lo);
-    if (lane == 0 && !P.dm.draft) tc_issuer(cx);  // (a draft model has no expert GEMMs)
+    if (lane == 0) tc_issuer(cx);
     __syncwarp();
     // free tensor memory once the compute warps are done with it
     if (lane == 0) {
@@ -2657,13 +2772,14 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
   w.g = lane >> 2;
   w.q = lane & 3;
   w.ti = 0;
+  w.di = 0;
   w.ok = true;
   w.b1 = false;
   w.xseq = 0;
   pdl_wait();
   cx.deadline = globaltimer() + (((uint64_t)P.timeout_ns_hi << 32) | P.timeout_ns_lo);
   stamp<kTiming>(P, blockIdx.x, EV_START);
-  compute_main<kTiming>(w);
+  compute_main<kTiming, kDraft>(w);
   stamp<kTiming>(P, blockIdx.x, EV_END);
   // the warp's tensor-memory accesses are done before the block frees it
   tc_fence_before();
@@ -2671,9 +2787,12 @@ __global__ void __launch_bounds__(kThreads, 1) msm_layer_kernel(const __grid_con
   if (lane == 0) mbar_arrive(&cx.S.tcbar[TB_DONE], 1);
 }
 
-const void* layer_kernel(bool timing) {
-  return timing ? reinterpret_cast<const void*>(&msm_layer_kernel<true>)
-                : reinterpret_cast<const void*>(&msm_layer_kernel<false>);
+const void* layer_kernel(bool timing, bool draft) {
+  if (draft)
+    return timing ? reinterpret_cast<const void*>(&msm_layer_kernel<true, true>)
+                  : reinterpret_cast<const void*>(&msm_layer_kernel<false, true>);
+  return timing ? reinterpret_cast<const void*>(&msm_layer_kernel<true, false>)
+                : reinterpret_cast<const void*>(&msm_layer_kernel<false, false>);
 }
 
 }  // namespace msm

@@ -1,10 +1,15 @@
 // Weight packing kernels, run once at model creation, and the sentinel fill.
 //
-// Dense bf16 matrices W[N][K] become 16-row units; each unit holds its K columns
-// as k-steps of 16 columns, each k-step four 8x8 matrices in ldmatrix order
-// (rows 0-7 | k 0-7, rows 8-15 | k 0-7, rows 0-7 | k 8-15, rows 8-15 | k 8-15),
-// so one contiguous bulk copy brings a tile and one ldmatrix.x4 yields the
-// m16n8k16 A fragment.  Two matrices get their rows paired inside a unit so an
+// Dense bf16 matrices W[N][K] become 16-row units; each unit holds its K columns as
+// tiles of 64 k-steps of 16 columns (the last tile of a unit may be shorter), laid out
+// for the tensor-memory copy the dense phases read them through: the m16n8k16 A
+// fragment of k-step 4c + q of a tile, as thread t of a warp holds it (four words:
+// rows t/4 and t/4 + 8, columns 2(t%4) and 2(t%4) + 8 of the k-step), sits at byte
+// c * 2048 + (32 q + t) * 16 of the tile.  A 128x256b tensor-memory copy of chunks c,
+// c + 1 (core matrices 8 rows x 16 bytes, 2048 bytes apart along K, 128 along the rows)
+// puts it in lane 32 q + t, columns 4c .. 4c + 3, so warp q of a group reads its k-steps
+// q, q + 4, ... with one tcgen05.ld, and a shorter tile is a prefix of the layout.
+// Two matrices get their rows paired inside a unit so an
 // epilogue thread holds both halves of a pair: the q/k rows of a head as
 // (d, d + hd/2) for rotate-half RoPE, and a dense FFN's stacked [gate; up] as
 // (gate j, up j) for SwiGLU.
@@ -39,19 +44,24 @@ __device__ __forceinline__ int dense_src_row(int kind, int u, int r, int N, int 
   return u * 16 + r;
 }
 
+// one thread per fragment word (unit, k-step, thread t, word j): word j of the fragment
+// is rows (j & 1) * 8 + t / 4, columns (j >> 1) * 8 + 2 (t % 4) (+1) of the k-step
 __global__ void pack_dense_kernel(const uint16_t* __restrict__ W, uint8_t* __restrict__ out, int N, int K,
                                   int kind, int hd, int hq, int hkv) {
   const long long steps = K / 16;
-  const long long total = (long long)(N / 16) * steps * 32;
+  const long long total = (long long)(N / 16) * steps * 128;
   for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < total;
        c += (long long)gridDim.x * blockDim.x) {
-    const int r = (int)(c & 7), m = (int)((c >> 3) & 3);
-    const long long ks = (c >> 5) % steps, u = (c >> 5) / steps;
-    const int ur = (m & 1) * 8 + r;
-    const int kcol = (int)ks * 16 + (m >> 1) * 8;
+    const int j = (int)(c & 3), t = (int)((c >> 2) & 31);
+    const long long ks = (c >> 7) % steps, u = (c >> 7) / steps;
+    const int ur = (j & 1) * 8 + t / 4;
+    const int kcol = (int)ks * 16 + (j >> 1) * 8 + 2 * (t % 4);
     const int src = dense_src_row(kind, (int)u, ur, N, hd, hq, hkv);
-    const uint4 v = *reinterpret_cast<const uint4*>(W + (size_t)src * K + kcol);
-    *reinterpret_cast<uint4*>(out + ((size_t)u * steps + ks) * kKStepBytes + m * 128 + r * 16) = v;
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(W + (size_t)src * K + kcol);
+    const long long kt = ks / kDenseTileSteps, kin = ks % kDenseTileSteps;
+    const long long off = ((long long)u * steps + kt * kDenseTileSteps) * kKStepBytes + (kin >> 2) * 2048 +
+                          ((kin & 3) * 32 + t) * 16 + j * 4;
+    *reinterpret_cast<uint32_t*>(out + off) = v;
   }
 }
 
