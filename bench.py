@@ -66,11 +66,11 @@ def step_bytes(cfg, distinct_per_layer, pos0):
 
 # ----------------------------------------------------------------- DRAM traffic
 # dram__bytes_read.sum + dram__bytes_write.sum of one layer launch, as a multiple of
-# that launch's algorithmic bytes, from an ncu capture of the kernel source whose
-# hash is given (one full-width SWA-2048 layer: 305.6 MB of traffic for 300.4 MB).
-# Reported only while the kernel source is unchanged; any edit makes it null.
-TRAFFIC_RATIO = {"kernel_sha256": "52f98908da9243efb0470cfd0df55eae54c282c49ef34c262df74e2bd4be9d8f", "ratio": 1.017,
-                 "capture": "profiles/layer_kernel_cfg2_expert_prefetch_l2.md (prefetch off)"}
+# that launch's algorithmic bytes, from an ncu capture of the kernel sources whose
+# hash is given (one full-width SWA-2048 layer: 304.1 MB of traffic for 300.4 MB).
+# Reported only while the kernel sources are unchanged; any edit makes it null.
+TRAFFIC_RATIO = {"kernel_sha256": "a38ed598b4e38ff8a2f9dd17159219a9825d7396569178585cab1076e1fd6b80", "ratio": 1.012,
+                 "capture": "profiles/layer_kernel_cfg2_traffic.md"}
 
 
 def kernel_sha256():
