@@ -272,6 +272,20 @@ __device__ __forceinline__ void unit_range(int n_units, int bb, int G, int& lo, 
   hi = (int)(((uint32_t)n_units * (uint32_t)(bb + 1)) / (uint32_t)G);
 }
 __device__ __forceinline__ int rot_block(int b, int rot, int G) { return (b + rot) % G; }
+// The expert units: n / G units per block, the n % G extra ones on the first blocks for
+// GEMM1 (so its later-finishing sixth units all belong to the first experts) and on the
+// last blocks for GEMM2 (whose first experts' inputs are then the late ones, on blocks
+// with one unit less)
+__device__ __forceinline__ void expert_units(int n_units, int bb, int G, bool gemm2, int& lo, int& hi) {
+  const int q = n_units / G, x = n_units - q * G;
+  if (!gemm2) {
+    lo = bb * q + min(bb, x);
+    hi = lo + q + (bb < x ? 1 : 0);
+  } else {
+    lo = bb * q + max(0, bb - (G - x));
+    hi = lo + q + (bb >= G - x ? 1 : 0);
+  }
+}
 
 // attention unit of block bb: kv head, split, row range
 struct AttnUnit {
@@ -452,7 +466,7 @@ __device__ __noinline__ void ra_back(const LaunchParams& P, RunAhead* ra, int bl
     const int upe = pass ? u2pe : u1pe;
     const uint64_t ub = pass ? ub2 : ub1;
     int lo, hi;
-    unit_range(na * upe, rot_block(block, P.phase_rot * (pass ? 7 : 6), G), G, lo, hi);
+    expert_units(na * upe, rot_block(block, P.phase_rot * (pass ? 7 : 6), G), G, pass != 0, lo, hi);
     for (int gu = lo; gu < hi;) {
       const int run = min(hi, (gu / upe + 1) * upe) - gu;
       ra->add(nullptr, (uint64_t)run * ub);  // expert tiles: streamed, not prefetched
@@ -505,8 +519,8 @@ struct TileStream {
     kb = h * steps;
   }
   // expert units: 128 rows x K as K / exp_tile_k(K) tiles of exp_tile_bytes(K) each
-  __device__ void experts(const uint8_t* w, int n_units, int per_expert, int K, int rot) {
-    unit_range(n_units, rot_block(blockIdx.x, rot, gridDim.x), gridDim.x, lo, hi);
+  __device__ void experts(const uint8_t* w, int n_units, int per_expert, int K, int rot, bool gemm2) {
+    expert_units(n_units, rot_block(blockIdx.x, rot, gridDim.x), gridDim.x, gemm2, lo, hi);
     u = lo;
     k0 = 0;
     steps = K / exp_tile_k(K);
@@ -592,10 +606,10 @@ struct TileStream {
           dense_half(P.w_down, dm.f, dm.d, P.phase_rot * 5, 1);
           break;
         case 7:
-          if (!kDraft) experts(P.w1, *cx.S.n_active * w1_units(dm.f), w1_units(dm.f), dm.p, P.phase_rot * 6);
+          if (!kDraft) experts(P.w1, *cx.S.n_active * w1_units(dm.f), w1_units(dm.f), dm.p, P.phase_rot * 6, false);
           break;
         case 8:
-          if (!kDraft) experts(P.w2, *cx.S.n_active * w2_units(dm.p), w2_units(dm.p), dm.f, P.phase_rot * 7);
+          if (!kDraft) experts(P.w2, *cx.S.n_active * w2_units(dm.p), w2_units(dm.p), dm.f, P.phase_rot * 7, true);
           break;
         case 9:
           if (!kDraft) dense(P.w_unpool, dm.p, dm.d, P.phase_rot * 8);
@@ -1963,7 +1977,7 @@ __device__ void gemm1_phase(Worker& w) {
   const int NT = dm.p / exp_tile_k(dm.p);
   const int na = *cx.S.n_active, upe = w1_units(dm.f);
   int lo, hi;
-  unit_range(na * upe, rot_block(cx.block, P.phase_rot * 6, G), G, lo, hi);
+  expert_units(na * upe, rot_block(cx.block, P.phase_rot * 6, G), G, false, lo, hi);
   // the operand (its row scales are read by the epilogues) has landed; the thread that
   // issued the copy waits for it whatever failed, before the top of the buffer is used
   // again (GEMM2) or the block exits
@@ -2040,7 +2054,7 @@ __device__ void gemm2_phase(Worker& w) {
   const int G = gridDim.x;
   const int na = *cx.S.n_active, upe = w2_units(dm.p), NT = dm.f / exp_tile_k(dm.f);
   int lo, hi;
-  unit_range(na * upe, rot_block(cx.block, P.phase_rot * 7, G), G, lo, hi);
+  expert_units(na * upe, rot_block(cx.block, P.phase_rot * 7, G), G, true, lo, hi);
   const float* ain = reinterpret_cast<const float*>(P.x_cur + P.xo.a);
   const uint32_t region = (uint32_t)dm.f * 8;  // one expert's 16 activation rows, E2M1, B layout
   uint8_t* g2b = cx.S.act + P.g2_off;          // the round's two experts' B operands
@@ -2253,7 +2267,7 @@ __device__ void tc_issuer(Ctx& cx) {
     {
       const int tk = exp_tile_k(dm.p), nst = tk / 64, NT = dm.p / tk;
       int lo, hi;
-      unit_range(na * w1_units(dm.f), rot_block(cx.block, P.phase_rot * 6, G), G, lo, hi);
+      expert_units(na * w1_units(dm.f), rot_block(cx.block, P.phase_rot * 6, G), G, false, lo, hi);
       t2 = t1 + (uint32_t)((hi - lo) * NT);
       const uint32_t sfb_s = smem_u32(cx.S.act + P.g1_b_off), b_s = sfb_s + (uint32_t)b1_code_off(dm.p);
       if (hi > lo) {
@@ -2299,7 +2313,7 @@ __device__ void tc_issuer(Ctx& cx) {
     if (ok) {
       const int tk = exp_tile_k(dm.f), nst = tk / 64, NT = dm.f / tk, upe = w2_units(dm.p);
       int lo, hi;
-      unit_range(na * upe, rot_block(cx.block, P.phase_rot * 7, G), G, lo, hi);
+      expert_units(na * upe, rot_block(cx.block, P.phase_rot * 7, G), G, true, lo, hi);
       const uint32_t act_s = smem_u32(cx.S.act + P.g2_off), region = (uint32_t)dm.f * 8;
       if (hi > lo) {
         const int a_first = lo / upe, a_last = (hi - 1) / upe;
