@@ -1536,23 +1536,31 @@ __device__ void attn_merge_phase(Worker& w) {
   const float* part_acc = reinterpret_cast<const float*>(P.s_buf + P.so.part);
   const float* part_ml = reinterpret_cast<const float*>(P.s_buf + P.so.ml);
   uint16_t* o_out = reinterpret_cast<uint16_t*>(P.x_cur + P.xo.o);
+  // two warps per merged row (warps 2i and 2i + 1 of a block, i = pair): each takes half
+  // the splits, all of its loads in flight at once, and the odd warp hands its (M, L,
+  // acc) to the even one through the activation buffer (free between the attention and
+  // the o_proj staging)
+  const int half = w.cw & 1, pair = w.cw >> 1;
+  float* xs = reinterpret_cast<float*>(cx.S.act) + pair * 32 * (PER + 2);
+  const int s_mid = (S + 1) / 2, s_lo = half ? s_mid : 0, s_hi = half ? S : s_mid;
   if (!await_phase(w, CNT_ATTN, PH_ATTN_MERGE)) return;
-  for (int it = gw; it < T * dm.hq; it += G * kComputeWarps) {
+  for (int it = gw >> 1; it < T * dm.hq; it += G * kComputeWarps / 2) {
     const int t = it / dm.hq, h = it % dm.hq, hk = h / group, j = h % group;
     auto mlp = [&](int s) { return part_ml + (((size_t)(hk * S + s) * T + t) * group + j) * 2; };
     auto accp = [&](int s) { return part_acc + (((size_t)(hk * S + s) * T + t) * group + j) * D + w.lane * PER; };
-    // splits in batches of 10, every load of a batch in flight together; a batch's
-    // partials are rescaled to the running maximum (M, L, acc in log2 units)
+    // splits in batches of 10 (one batch for up to 20 splits), every load of a batch in
+    // flight together; a batch's partials are rescaled to the running maximum (M, L, acc
+    // in log2 units)
     constexpr int kB = 10;
     float M = -INFINITY, L = 0.f, acc[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-    for (int s0 = 0; s0 < S; s0 += kB) {
+    for (int s0 = s_lo; s0 < s_hi; s0 += kB) {
       uint2 mv[kB];
       float av[kB][PER];
 #pragma unroll
       for (int i = 0; i < kB; ++i) {
-        if (s0 + i >= S) continue;
+        if (s0 + i >= s_hi) continue;
         mv[i] = ld_relaxed_v2(mlp(s0 + i));
         if constexpr (PER == 4) {
           const uint4 q4 = ld_relaxed_v4(accp(s0 + i));
@@ -1566,7 +1574,7 @@ __device__ void attn_merge_phase(Worker& w) {
       float Mb = M;
 #pragma unroll
       for (int i = 0; i < kB; ++i)
-        if (s0 + i < S) Mb = fmaxf(Mb, __uint_as_float(mv[i].x));
+        if (s0 + i < s_hi) Mb = fmaxf(Mb, __uint_as_float(mv[i].x));
       const float Mu = (Mb == -INFINITY) ? 0.f : Mb;
       const float al = exp2f(M - Mu);  // 0 while M is still -inf
       L *= al;
@@ -1574,7 +1582,7 @@ __device__ void attn_merge_phase(Worker& w) {
       for (int e = 0; e < PER; ++e) acc[e] *= al;
 #pragma unroll
       for (int i = 0; i < kB; ++i) {
-        if (s0 + i >= S) continue;
+        if (s0 + i >= s_hi) continue;
         const float ws = exp2f(__uint_as_float(mv[i].x) - Mu);
         L += ws * __uint_as_float(mv[i].y);
 #pragma unroll
@@ -1582,14 +1590,33 @@ __device__ void attn_merge_phase(Worker& w) {
       }
       M = Mb;
     }
-    const float inv = 1.f / L;
-    uint16_t* dst = o_out + (size_t)t * dm.hq * D + (size_t)h * D + w.lane * PER;
-    if constexpr (PER == 4) {
-      uint2 v = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2 % PER] * inv, acc[3 % PER] * inv));
-      asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%2};" ::"l"(dst), "r"(v.x), "r"(v.y) : "memory");
-    } else {
-      st_relaxed_u32(dst, pack_bf16x2(acc[0] * inv, acc[1 % PER] * inv));
+    if (half) {
+      float* x = xs + w.lane * (PER + 2);
+      x[0] = M;
+      x[1] = L;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) x[2 + e] = acc[e];
     }
+    named_bar(4 + pair, 64);
+    if (!half) {
+      // the two halves: the even warp's, then the odd warp's, at their common maximum
+      const float* x = xs + w.lane * (PER + 2);
+      const float M1 = x[0], L1 = x[1];
+      const float Mm = fmaxf(M, M1), Mu = (Mm == -INFINITY) ? 0.f : Mm;
+      const float a0 = exp2f(M - Mu), a1 = exp2f(M1 - Mu);
+      L = L * a0 + L1 * a1;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] = acc[e] * a0 + x[2 + e] * a1;
+      const float inv = 1.f / L;
+      uint16_t* dst = o_out + (size_t)t * dm.hq * D + (size_t)h * D + w.lane * PER;
+      if constexpr (PER == 4) {
+        uint2 v = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2 % PER] * inv, acc[3 % PER] * inv));
+        asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%2};" ::"l"(dst), "r"(v.x), "r"(v.y) : "memory");
+      } else {
+        st_relaxed_u32(dst, pack_bf16x2(acc[0] * inv, acc[1 % PER] * inv));
+      }
+    }
+    named_bar(4 + pair, 64);  // the exchange slot may be reused
   }
 }
 
