@@ -499,6 +499,36 @@ void probe_handoff(Dev& d, bool quick) {
   }
 }
 
+// Clusters: how many clusters of 1, 2, 4 and 8 blocks of the layer kernel's shape (384
+// threads, 227 KB of dynamic shared memory, one block per SM) can be resident at once.
+// A query only: nothing is launched.
+__global__ void __launch_bounds__(384, 1) cluster_shape_kernel(int* p) {
+  if (p != nullptr && threadIdx.x == 0) p[blockIdx.x] = 1;
+}
+
+void probe_clusters() {
+  const int smem = 232448;
+  CK(cudaFuncSetAttribute(cluster_shape_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  CK(cudaFuncSetAttribute(cluster_shape_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+  for (int cs : {1, 2, 4, 8}) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs * 16);
+    cfg.blockDim = dim3(384);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = cs;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    int n = 0;
+    CK(cudaOccupancyMaxActiveClusters(&n, cluster_shape_kernel, &cfg));
+    std::printf("{\"probe\": \"clusters\", \"cluster_size\": %d, \"max_active_clusters\": %d, \"blocks\": %d, "
+                "\"error\": 0}\n", cs, n, n * cs);
+  }
+}
+
 }  // namespace
 
 int main(int argc, char** argv) {
@@ -514,5 +544,6 @@ int main(int argc, char** argv) {
   if (all || !std::strcmp(which, "fence")) probe_fence(d, quick);
   if (all || !std::strcmp(which, "icache")) probe_icache(d, quick);
   if ((all || !std::strcmp(which, "handoff")) && sms >= 152) probe_handoff(d, quick);
+  if (all || !std::strcmp(which, "clusters")) probe_clusters();
   return d.error() ? 1 : 0;
 }

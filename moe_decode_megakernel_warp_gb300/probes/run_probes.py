@@ -1,12 +1,13 @@
 """Build and run the intra-GPU probes of probes.cu (one JSON object per result).
 
-    python -m moe_decode_megakernel_warp_gb300.probes.run_probes [poll|fence|icache|handoff|all] [--quick]
+    python -m moe_decode_megakernel_warp_gb300.probes.run_probes [poll|fence|icache|handoff|clusters|all] [--quick]
 
 The probes measure, on the current GPU, the costs the layer kernel's handoff and
 prefetch design rests on: GPU-scope acquire-poll latency (idle and with bulk copies
 in flight), the cost of a gpu-scope fence (idle, after stores, with bulk copies in
-flight), instruction-cache capacity (straight-line code blocks run in a loop) and a
-grid-wide handoff polled element by element against one behind a counter.
+flight), instruction-cache capacity (straight-line code blocks run in a loop), a
+grid-wide handoff polled element by element against one behind a counter, and how many
+clusters of the layer kernel's block shape fit on the GPU at once.
 """
 import json
 import os

@@ -28,7 +28,9 @@ def test_probes_quick():
     from moe_decode_megakernel_warp_gb300.probes import run_probes
     res = run_probes.run("all", quick=True)
     kinds = {r["probe"] for r in res}
-    assert {"acquire_load", "poll", "fence", "icache", "handoff"} <= kinds, kinds
+    assert {"acquire_load", "poll", "fence", "icache", "handoff", "clusters"} <= kinds, kinds
+    cl = {r["cluster_size"]: r for r in res if r["probe"] == "clusters"}
+    assert cl[1]["max_active_clusters"] >= cl[2]["max_active_clusters"] >= cl[4]["max_active_clusters"] >= 1
     for r in res:
         assert r["error"] == 0, r
         for k, v in r.items():
