@@ -64,7 +64,7 @@ struct msm_model {
   Dims dm{};
   std::vector<uint8_t> global;
   int G = 0, ring_bytes = 0, act_bytes = 0, smem_bytes = 0;
-  int g1_b_off = 0, g2_off = 0, ring_ext = 0, unpool_act_off = 0, unpool_ext = 0, sfb_ext = 0;
+  int g1_b_off = 0, g2_off = 0, ring_ext = 0, unpool_act_off = 0, unpool_ext = 0, sfb_ext = 0, attn_act_off = 0, kv_ext = 0;
   std::vector<LayerPack> L;
   uint8_t* lm = nullptr;
   uint16_t* g_final = nullptr;
@@ -307,8 +307,14 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   dm.nqkv = (dm.hq + 2 * dm.hkv) * dm.hd;
   dm.group = dm.hq / dm.hkv;
   dm.attn_rows = dm.hd == 128 ? 32 : 64;
-  dm.attn_nk = std::max(16, dm.attn_rows * dm.group / 8);
-  dm.attn_wph = dm.attn_rows / dm.attn_nk;
+  if (draft) {
+    // the draft kernel's attention: the 8 / group warps of a head take alternate KV tiles
+    dm.attn_nk = dm.attn_rows;
+    dm.attn_wph = std::max(1, 8 / dm.group);
+  } else {
+    dm.attn_nk = std::max(16, dm.attn_rows * dm.group / 8);
+    dm.attn_wph = dm.attn_rows / dm.attn_nk;
+  }
   dm.rms_eps = c.rms_eps;
   m->G = c.grid_blocks > 0 ? std::min(c.grid_blocks, sms) : sms;
   {
@@ -351,6 +357,10 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   }
   m->act_bytes = (int)act;
   m->ring_bytes = (int)ring;
+  // attention stages Q, the tree rows and its merge scratch at the top of the activation
+  // buffer; the KV tiles of a launch after the first may use the rest as ring space
+  m->attn_act_off = (int)(act - ((attn_need + 1023) & ~uint64_t(1023)));
+  m->kv_ext = m->attn_act_off & ~1023;
   m->g1_b_off = (int)(act - ((g1_need + 1023) & ~uint64_t(1023)));
   m->g2_off = (int)(act - ((g2_need + 1023) & ~uint64_t(1023)));
   m->ring_ext = (int)((act - expert_top) & ~uint64_t(1023));
@@ -659,6 +669,8 @@ msm_status enqueue_verify(msm_model* m, const StepBuffers& B, const void* hidden
   P.ring_ext = m->ring_ext;
   P.sfb_ext = m->sfb_ext;
   P.unpool_act_off = m->unpool_act_off;
+  P.attn_act_off = m->attn_act_off;
+  P.kv_ext = m->kv_ext;
   P.unpool_ext = m->unpool_ext;
   P.flags = m->cfg.flags;
   P.timeout_ns_lo = (uint32_t)tmo;

@@ -187,6 +187,8 @@ struct LaunchParams {
   // the unpooler's activation sits at this offset (the top of the buffer), and its
   // weight tiles may take unpool_ext bytes of the bottom
   int unpool_act_off, unpool_ext;
+  int attn_act_off;  // attention's Q, tree rows and merge scratch: the top of the activation buffer
+  int kv_ext;        // ... below it, ring space for the KV tiles (launches after the first)
   uint32_t flags;
   uint32_t timeout_ns_lo, timeout_ns_hi;
   int prefetch_experts;

@@ -701,6 +701,10 @@ __device__ void loader(Ctx& cx) {
       }
     } else if (ts.seg == 9) {
       r.cap += (uint32_t)P.unpool_ext;
+    } else if (ts.seg == 1 && !P.first) {
+      // KV tiles: the activation buffer below attention's region is free until o_proj
+      // staging (launch 0 stages its prologue input there first)
+      r.cap += (uint32_t)P.kv_ext;
     }
     const int g1i = ts.seg == 7 ? (ts.t_u - ts.lo) * ts.steps + ts.t_k0 : 99;
     if (g1i < 16) stamp_any(P, EV_LD_G1_NEXT + g1i);
@@ -1355,7 +1359,104 @@ __device__ __forceinline__ void attn_keys16(AttnState<D>& st, const uint32_t (&q
   }
 }
 
-template <int D>
+// NKEYS keys (a multiple of 16, from key kb of a tile of `rows` rows) in one online-softmax
+// update: the whole-tile form the draft model's attention uses (one query head per KV
+// head, so the block's warps split the tiles of that head among themselves)
+template <int D, int NKEYS, class Vis>
+__device__ __forceinline__ void attn_keys_n(AttnState<D>& st, const uint32_t (&qa)[D / 16][4],
+                                            uint32_t kbase, uint32_t vbase, int rows, int kb, int lane,
+                                            float scale_log2, Vis vis) {
+  constexpr int NT = NKEYS / 8;
+  float s[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[nt][i] = 0.f;
+  }
+  const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ks += 2) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int key = kb + nt * 8 + r8;
+      const int d0 = (ks + (mi >> 1)) * 16 + (mi & 1) * 8;
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kbase + swz(key, d0, rows), b0, b1, b2, b3);
+      mma_bf16(s[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+      mma_bf16(s[nt], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
+    }
+  }
+  const int g = lane >> 2, q = lane & 3;
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int row = g + ((i >> 1) << 3);     // token
+      const int key = kb + nt * 8 + 2 * q + (i & 1);
+      float v = vis(row, key) ? s[nt][i] * scale_log2 : -INFINITY;
+      s[nt][i] = v;
+      mx[i >> 1] = fmaxf(mx[i >> 1], v);
+    }
+  }
+  float alpha[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+    const float mnew = fmaxf(st.m[r], mx[r]);
+    const float muse = (mnew == -INFINITY) ? 0.f : mnew;
+    alpha[r] = exp2f(st.m[r] - muse);
+    st.m[r] = mnew;
+    mx[r] = muse;
+  }
+  float rs[2] = {0.f, 0.f};
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float p = exp2f(s[nt][i] - mx[i >> 1]);
+      s[nt][i] = p;
+      rs[i >> 1] += p;
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) st.l[r] = st.l[r] * alpha[r] + rs[r];
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) {
+    st.o[n][0] *= alpha[0];
+    st.o[n][1] *= alpha[0];
+    st.o[n][2] *= alpha[1];
+    st.o[n][3] *= alpha[1];
+  }
+  // P as two bf16 terms (as in attn_keys16); k-step kk of P.V covers keys 16 kk ..
+  // 16 kk + 15, the score columns of nt = 2 kk and 2 kk + 1
+#pragma unroll
+  for (int kk = 0; kk < NKEYS / 16; ++kk) {
+    uint32_t ph[4], pl[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float a = s[2 * kk + (i >> 1)][(i & 1) * 2], b = s[2 * kk + (i >> 1)][(i & 1) * 2 + 1];
+      ph[i] = pack_bf16x2(a, b);
+      pl[i] = pack_bf16x2(a - bf16_to_f32((uint16_t)(ph[i] & 0xFFFFu)), b - bf16_to_f32((uint16_t)(ph[i] >> 16)));
+    }
+#pragma unroll
+    for (int n = 0; n < D / 8; n += 2) {
+      const int key = kb + kk * 16 + (mi & 1) * 8 + r8;
+      const int d0 = (n + (mi >> 1)) * 8;
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(vbase + swz(key, d0, rows), b0, b1, b2, b3);
+      mma_bf16(st.o[n], ph[0], ph[1], ph[2], ph[3], b0, b1);
+      mma_bf16(st.o[n + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+      mma_bf16(st.o[n], pl[0], pl[1], pl[2], pl[3], b0, b1);
+      mma_bf16(st.o[n + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
+    }
+  }
+}
+
+// kTiles: the WPH warps of a head take alternate KV tiles, all rows of each in one update
+// (the draft model); else each takes its NK keys of every tile (the target model)
+template <int D, bool kTiles>
 __device__ void attention_phase(Worker& w) {
   Ctx& cx = *w.cx;
   const LaunchParams& P = *cx.P;
@@ -1364,8 +1465,9 @@ __device__ void attention_phase(Worker& w) {
   const AttnUnit au = attn_unit(P, cx.pos0, rot_block(cx.block, P.phase_rot * 2, G), P.is_global);
   if (!au.valid) return;
   const int group = dm.group, R = dm.attn_rows, NK = dm.attn_nk, WPH = dm.attn_wph;
-  // act buffer regions: Q fragments source, tree K/V, merge scratch
-  uint8_t* qsm = cx.S.act;
+  // act buffer regions at its top: Q fragments source, tree K/V, merge scratch (the KV
+  // tiles may use the buffer below them)
+  uint8_t* qsm = cx.S.act + P.attn_act_off;
   uint8_t* tk = qsm + group * (D / 16) * kKStepBytes;
   uint8_t* tv = tk + 16 * D * 2;
   float* scratch = reinterpret_cast<float*>(tv + 16 * D * 2);
@@ -1445,14 +1547,23 @@ __device__ void attention_phase(Worker& w) {
         const int r = row0 + key;
         return r < r1 && (glob || tpos[tok] - r < window);
       };
-      for (int kb = part * NK; kb < (part + 1) * NK; kb += 16)
-        attn_keys16<D>(st, qa, kb_, vb_, R, kb, w.lane, scale_log2, vis);
+      if constexpr (kTiles) {
+        if (i % WPH == part) {
+          if (R == 32) attn_keys_n<D, 32>(st, qa, kb_, vb_, R, 0, w.lane, scale_log2, vis);
+          else attn_keys_n<D, 64>(st, qa, kb_, vb_, R, 0, w.lane, scale_log2, vis);
+        }
+      } else {
+        for (int kb = part * NK; kb < (part + 1) * NK; kb += 16)
+          attn_keys16<D>(st, qa, kb_, vb_, R, kb, w.lane, scale_log2, vis);
+      }
     }
     __syncwarp();
     if (w.lane == 0) mbar_arrive(&cx.S.empty[s], 1);
   }
   w.ti += (uint32_t)au.n_sub;
-  if (w.ok && active && au.tree && part == 0) {
+  // the tree rows: part 0, or with whole tiles the part after the last history tile's
+  const int tree_part = kTiles ? au.n_sub % WPH : 0;
+  if (w.ok && active && au.tree && part == tree_part) {
     const uint32_t* anc = cx.S.anc;
     auto vis = [&](int tok, int key) { return ((anc[tok] >> key) & 1u) != 0u; };
     attn_keys16<D>(st, qa, smem_u32(tk), smem_u32(tv), 16, 0, w.lane, scale_log2, vis);
@@ -2539,8 +2650,8 @@ __device__ void compute_main(Worker& w) {
     cbar();
   }
   // a2: tree attention (split over blocks), a3: merge of the split partials
-  if (dm.hd == 128) attention_phase<128>(w);
-  else attention_phase<64>(w);
+  if (dm.hd == 128) attention_phase<128, kDraft>(w);
+  else attention_phase<64, kDraft>(w);
   publish(w, CNT_ATTN);
   stamp<kTiming>(P, b, EV_ATTN_DONE);
   if (dm.hd == 128) attn_merge_phase<128>(w);
