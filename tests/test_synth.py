@@ -62,3 +62,29 @@ def test_nvfp4_weight_encoding_decodes_close():
     r, c = np.unravel_index(np.argmax(np.abs(x)), x.shape)
     back = oracle.nvfp4_dequant(codes[r], sf[r], gs, 256)
     assert abs(back[c]) == np.float64(np.float32(6 * 448) * gs) or abs(abs(back[c]) - abs(x[r, c])) < 1e-7
+
+
+def test_draft_draws_are_seeded_shaped_and_distinct_from_the_target():
+    """The draft model's inputs: shapes of the widths the pages give, reproducible per
+    seed, residual projections scaled by 1 / sqrt(2 L), streams apart from the target's."""
+    dc = synth.DRAFT_SMALL
+    w = synth.draft_layer_weights(dc, 3, 1)
+    hd = dc.heads * dc.hd
+    assert w["w_qkv"].shape == (3 * hd, dc.d) and w["w_o"].shape == (dc.d, hd)
+    assert w["w_gate"].shape == (dc.f, dc.d) and w["w_up"].shape == (dc.f, dc.d) and w["w_down"].shape == (dc.d, dc.f)
+    assert all(a.dtype == np.uint16 for a in w.values())
+    again = synth.draft_layer_weights(dc, 3, 1)
+    assert all(np.array_equal(w[k], again[k]) for k in w)
+    other = synth.draft_layer_weights(dc, 4, 1)
+    assert not np.array_equal(w["w_up"], other["w_up"])
+    down = synth.bf16_to_f32(w["w_down"]).astype(np.float64)
+    gate = synth.bf16_to_f32(w["w_gate"]).astype(np.float64)
+    assert abs(down.std() / dc.resid_std - 1) < 0.05 and abs(gate.std() / 0.02 - 1) < 0.05
+    k, v = synth.draft_kv_history(dc, 3, 0)
+    assert k.shape == (dc.heads, dc.max_ctx, dc.hd) and not k[:, dc.history:].any() and k[:, :dc.history].any()
+    assert synth.embed_table(64, 32, 7).shape == (64, 32)
+    assert synth.draft_hidden_in(dc, 3).shape == (16, dc.d)
+    # the draft's streams are not the target's (different kinds)
+    assert synth.stream(synth.K_D_QKV, 0) != synth.stream(synth.K_QKV, 0)
+    assert synth.DRAFT_FULL.d == 2048 and synth.DRAFT_FULL.heads * synth.DRAFT_FULL.hd == 2048
+    assert synth.DRAFT_FULL.f == 8192 and synth.DRAFT_FULL.n_layers == 5
