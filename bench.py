@@ -554,9 +554,10 @@ def measure_draft(dev, steps, warmup):
     gbs = b / (ms * 1e-3) / 1e9
     return {"workload": dc.name, "ms_per_step": ms, "steps": steps, "algorithmic_bytes_per_step": b,
             "hbm_gbs": gbs, "frac": gbs / peak, "peak": peak, "peak_kind": peak_kind,
-            "launches_per_step": dc.n_layers + 2, "tokens_proposed": T - 1,
-            "note": "median of CUDA-event step times; layer launches + the two argmax launches; "
-                    "inputs larger than L2 (%.2f GB per step)" % (b / 1e9)}
+            "launches_per_step": dc.n_layers + 1, "tokens_proposed": T - 1,
+            "note": "median of CUDA-event step times; kernel launches per step: the layer launches and the "
+                    "argmax (plus a 4-byte memset of tokens_out[0]); inputs larger than L2 (%.2f GB per step)"
+                    % (b / 1e9)}
 
 
 def run_draft(args):
