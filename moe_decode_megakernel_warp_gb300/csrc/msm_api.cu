@@ -185,7 +185,7 @@ msm_status encode_kv_map(msm_model* m, CUtensorMap* map, const void* ptr) {
   const Dims& dm = m->dm;
   cuuint64_t dims[3] = {(cuuint64_t)dm.hd, (cuuint64_t)dm.max_ctx, (cuuint64_t)dm.hkv};
   cuuint64_t strides[2] = {(cuuint64_t)dm.hd * 2, (cuuint64_t)dm.max_ctx * dm.hd * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)dm.attn_rows, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)dm.kv_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = m->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -307,6 +307,9 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   dm.nqkv = (dm.hq + 2 * dm.hkv) * dm.hd;
   dm.group = dm.hq / dm.hkv;
   dm.attn_rows = dm.hd == 128 ? 32 : 64;
+  // a draft model's blocks stream many KV tiles of one head, one per warp at a time:
+  // two attention tiles per ring tile halve the loader's work per byte
+  dm.kv_rows = draft && dm.max_ctx >= 2 * dm.attn_rows ? 2 * dm.attn_rows : dm.attn_rows;
   if (draft) {
     // the draft kernel's attention: the 8 / group warps of a head take alternate KV tiles
     dm.attn_nk = dm.attn_rows;
@@ -350,7 +353,7 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   long long ring = (long long)smem_cap - (long long)act - kSmallBytes;
   ring &= ~1023ll;
   const uint64_t exp_tile = draft ? 0 : (uint64_t)std::max(exp_tile_bytes(dm.p), exp_tile_bytes(dm.f));
-  const uint64_t max_tile = std::max(std::max((uint64_t)kDenseTileSteps * kKStepBytes, exp_tile), (uint64_t)dm.attn_rows * D * 4);
+  const uint64_t max_tile = std::max(std::max((uint64_t)kDenseTileSteps * kKStepBytes, exp_tile), (uint64_t)dm.kv_rows * D * 4);
   if (ring < (long long)(2 * max_tile)) {
     delete m;
     return fail(MSM_ERR_UNSUPPORTED, "widths too large for the shared-memory budget");

@@ -120,6 +120,7 @@ struct Dims {
   int nqkv;        // (hq + 2 hkv) hd
   int group;       // hq / hkv
   int attn_rows;   // R: KV rows per attention tile
+  int kv_rows;     // KV rows per ring tile: R, or 2R for a draft model (two attention tiles)
   int attn_nk;     // keys per warp per tile
   int attn_wph;    // warps per q head
   int splits;      // attention splits per kv head

@@ -300,11 +300,11 @@ __device__ __forceinline__ AttnUnit attn_unit(const LaunchParams& P, int pos0, i
   int lo = is_global ? 0 : max(0, pos0 - dm.window + 1);
   int n = pos0 - lo;
   int chunk = (n + dm.splits - 1) / dm.splits;
-  chunk = ((chunk + dm.attn_rows - 1) / dm.attn_rows) * dm.attn_rows;
-  if (chunk < dm.attn_rows) chunk = dm.attn_rows;
+  chunk = ((chunk + dm.kv_rows - 1) / dm.kv_rows) * dm.kv_rows;
+  if (chunk < dm.kv_rows) chunk = dm.kv_rows;
   u.r0 = min(pos0, lo + u.s * chunk);
   u.r1 = min(pos0, u.r0 + chunk);
-  u.n_sub = u.valid ? (u.r1 - u.r0 + dm.attn_rows - 1) / dm.attn_rows : 0;
+  u.n_sub = u.valid ? (u.r1 - u.r0 + dm.kv_rows - 1) / dm.kv_rows : 0;
   u.tree = u.valid && (u.s == dm.splits - 1);
   return u;
 }
@@ -546,8 +546,8 @@ struct TileStream {
         t_u = u;
         t_k0 = k0;
         if (seg == 1) {
-          kv_row = kv_r0 + (u - lo) * dm.attn_rows;
-          bytes = (uint32_t)dm.attn_rows * dm.hd * 2 * 2;
+          kv_row = kv_r0 + (u - lo) * dm.kv_rows;
+          bytes = (uint32_t)dm.kv_rows * dm.hd * 2 * 2;
           ++u;
           return TS_KV;
         }
@@ -721,7 +721,7 @@ __device__ void loader(Ctx& cx) {
     cx.S.slot_tile[s] = r.issued;
     mbar_expect_tx(&cx.S.full[s], bytes);
     if (st == TS_KV) {
-      const int R = dm.attn_rows, halves = dm.hd / 64;
+      const int R = dm.kv_rows, halves = dm.hd / 64;
       uint8_t* dst = cx.S.ring + off;
       for (int h = 0; h < halves; ++h) {
         tma_load_3d(dst + h * R * 128, &P.tmap_k, h * 64, kv_row, ts.kv_hk, &cx.S.full[s]);
@@ -1465,6 +1465,7 @@ __device__ void attention_phase(Worker& w) {
   const AttnUnit au = attn_unit(P, cx.pos0, rot_block(cx.block, P.phase_rot * 2, G), P.is_global);
   if (!au.valid) return;
   const int group = dm.group, R = dm.attn_rows, NK = dm.attn_nk, WPH = dm.attn_wph;
+  const int KR = dm.kv_rows, nsub = KR / R;  // rows of a ring tile, attention tiles in it
   // act buffer regions at its top: Q fragments source, tree K/V, merge scratch (the KV
   // tiles may use the buffer below them)
   uint8_t* qsm = cx.S.act + P.attn_act_off;
@@ -1541,20 +1542,22 @@ __device__ void attention_phase(Worker& w) {
     if (!w.ok) break;
     if (active) {
       const uint32_t kb_ = smem_u32(cx.S.ring + cx.S.slot_off[s]);
-      const uint32_t vb_ = kb_ + (uint32_t)R * D * 2;
-      const int row0 = au.r0 + i * R, r1 = au.r1;
+      const uint32_t vb_ = kb_ + (uint32_t)KR * D * 2;
+      const int row0 = au.r0 + i * KR, r1 = au.r1;
       auto vis = [&](int tok, int key) {
         const int r = row0 + key;
         return r < r1 && (glob || tpos[tok] - r < window);
       };
       if constexpr (kTiles) {
-        if (i % WPH == part) {
-          if (R == 32) attn_keys_n<D, 32>(st, qa, kb_, vb_, R, 0, w.lane, scale_log2, vis);
-          else attn_keys_n<D, 64>(st, qa, kb_, vb_, R, 0, w.lane, scale_log2, vis);
+        // attention tile i nsub + sb (keys sb R .. of the ring tile), while it holds rows
+        for (int sb = 0; sb < nsub && row0 + sb * R < r1; ++sb) {
+          if ((i * nsub + sb) % WPH != part) continue;
+          if (R == 32) attn_keys_n<D, 32>(st, qa, kb_, vb_, KR, sb * R, w.lane, scale_log2, vis);
+          else attn_keys_n<D, 64>(st, qa, kb_, vb_, KR, sb * R, w.lane, scale_log2, vis);
         }
       } else {
         for (int kb = part * NK; kb < (part + 1) * NK; kb += 16)
-          attn_keys16<D>(st, qa, kb_, vb_, R, kb, w.lane, scale_log2, vis);
+          attn_keys16<D>(st, qa, kb_, vb_, KR, kb, w.lane, scale_log2, vis);
       }
     }
     __syncwarp();
@@ -1562,7 +1565,7 @@ __device__ void attention_phase(Worker& w) {
   }
   w.ti += (uint32_t)au.n_sub;
   // the tree rows: part 0, or with whole tiles the part after the last history tile's
-  const int tree_part = kTiles ? au.n_sub % WPH : 0;
+  const int tree_part = kTiles ? ((au.r1 - au.r0 + R - 1) / R) % WPH : 0;
   if (w.ok && active && au.tree && part == tree_part) {
     const uint32_t* anc = cx.S.anc;
     auto vis = [&](int tok, int key) { return ((anc[tok] >> key) & 1u) != 0u; };
