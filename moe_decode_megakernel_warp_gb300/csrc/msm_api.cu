@@ -307,9 +307,8 @@ msm_status msm_model_create(const msm_config* config, const msm_weights* w, int 
   dm.nqkv = (dm.hq + 2 * dm.hkv) * dm.hd;
   dm.group = dm.hq / dm.hkv;
   dm.attn_rows = dm.hd == 128 ? 32 : 64;
-  // a draft model's blocks stream many KV tiles of one head, one per warp at a time:
-  // two attention tiles per ring tile halve the loader's work per byte
-  dm.kv_rows = draft && dm.max_ctx >= 2 * dm.attn_rows ? 2 * dm.attn_rows : dm.attn_rows;
+  // two attention tiles per KV ring tile: half the loader's and the barriers' work per byte
+  dm.kv_rows = dm.max_ctx >= 2 * dm.attn_rows ? 2 * dm.attn_rows : dm.attn_rows;
   if (draft) {
     // the draft kernel's attention: the 8 / group warps of a head take alternate KV tiles
     dm.attn_nk = dm.attn_rows;

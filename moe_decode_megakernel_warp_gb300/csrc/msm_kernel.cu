@@ -1556,8 +1556,9 @@ __device__ void attention_phase(Worker& w) {
           else attn_keys_n<D, 64>(st, qa, kb_, vb_, KR, sb * R, w.lane, scale_log2, vis);
         }
       } else {
-        for (int kb = part * NK; kb < (part + 1) * NK; kb += 16)
-          attn_keys16<D>(st, qa, kb_, vb_, KR, kb, w.lane, scale_log2, vis);
+        for (int sb = 0; sb < nsub && row0 + sb * R < r1; ++sb)
+          for (int kb = part * NK; kb < (part + 1) * NK; kb += 16)
+            attn_keys16<D>(st, qa, kb_, vb_, KR, sb * R + kb, w.lane, scale_log2, vis);
       }
     }
     __syncwarp();
